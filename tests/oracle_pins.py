@@ -1,0 +1,407 @@
+"""Pins of the oracle against facts that do not come from the oracle itself.
+
+Each ``pin_*`` raises AssertionError when the oracle disagrees with a closed form,
+an invariant, a brute-force evaluation written independently below (pure Python
+loops with a hand-written binary16 decoder), or a value the source pages print
+(``tests/golden/pages_constants.json``).  ``test_oracle_pins.py`` runs them as they
+are; ``test_oracle_mutations.py`` plants plausible mistakes in the oracle and checks
+that at least one pin fails for each.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+import struct
+
+import numpy as np
+
+import oracle.ref as R
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "pages_constants.json")
+
+
+# ------------------------------------------------------------ independent helpers
+def half_bits_to_float(bits: int) -> float:
+    """IEEE-754 binary16 decoding from the definition (1 sign, 5 exponent, 10
+    fraction bits, bias 15), independent of numpy's conversion."""
+    sign = -1.0 if bits & 0x8000 else 1.0
+    exp = (bits >> 10) & 0x1F
+    frac = bits & 0x3FF
+    if exp == 0:
+        return sign * frac * 2.0 ** -24
+    if exp == 31:
+        return sign * math.inf if frac == 0 else math.nan
+    return sign * (1.0 + frac / 1024.0) * 2.0 ** (exp - 15)
+
+
+def f16_list(a):
+    bits = np.asarray(a, np.float16).view(np.uint16).reshape(-1)
+    return [half_bits_to_float(int(b)) for b in bits]
+
+
+def brute_q8(codes, params, x):
+    """y[r] = Σ_c (scale·q + offset)·x[c], pure Python, f16 decoded by hand."""
+    rows, cols = codes.shape
+    nb = cols // 32
+    p = f16_list(params)
+    xs = [float(v) for v in np.asarray(x, np.float32)]
+    out = []
+    for r in range(rows):
+        acc = 0.0
+        for c in range(cols):
+            s = p[(r * nb + c // 32) * 2]
+            o = p[(r * nb + c // 32) * 2 + 1]
+            acc += (s * int(codes[r, c]) + o) * xs[c]
+        out.append(acc)
+    return out
+
+
+def brute_f16(W, x):
+    rows, cols = W.shape
+    w = f16_list(W)
+    xs = [float(v) for v in np.asarray(x, np.float32)]
+    return [sum(w[r * cols + c] * xs[c] for c in range(cols)) for r in range(rows)]
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _q8(rows, cols, seed):
+    r = _rng(seed)
+    codes = np.clip(np.rint(r.standard_normal((rows, cols)) * 40), -127, 127).astype(np.int8)
+    params = np.empty((rows, cols // 32, 2), np.float16)
+    params[..., 0] = r.uniform(1e-3, 4e-3, (rows, cols // 32))
+    params[..., 1] = r.standard_normal((rows, cols // 32)) * 1e-3
+    return codes, params
+
+
+def close(a, b, rel=1e-12, abs_=0.0):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    assert a.shape == b.shape, (a.shape, b.shape)
+    err = np.abs(a - b)
+    lim = rel * np.maximum(np.abs(a), np.abs(b)) + abs_
+    assert np.all(err <= lim), f"max err {err.max()} (limit {lim.max()})"
+
+
+# ------------------------------------------------------------ projections
+def pin_q8_identity():
+    n = 96
+    codes = np.eye(n, dtype=np.int8)
+    params = np.zeros((n, n // 32, 2), np.float16)
+    params[..., 0] = 1.0
+    x = _rng(1).standard_normal((3, n)).astype(np.float32)
+    y, _ = R.gemv_q8(codes, params, x)
+    assert np.array_equal(y, x.astype(np.float64)), "identity q8 must return x exactly"
+
+
+def pin_f16_identity():
+    n = 64
+    x = _rng(2).standard_normal((2, n)).astype(np.float32)
+    y, _ = R.gemv_f16(np.eye(n, dtype=np.float16), x)
+    assert np.array_equal(y, x.astype(np.float64))
+
+
+def pin_q8_onehot_rectangular():
+    """Row r holds one code at column π(r): y[r] = s·q·x[π(r)] (offset 0).  The
+    matrix is 64×96, so a transposed operand or a swapped axis cannot pass."""
+    rows, cols = 64, 96
+    r = _rng(3)
+    perm = r.permutation(cols)[:rows]
+    codes = np.zeros((rows, cols), np.int8)
+    qv = r.integers(-127, 128, rows)
+    codes[np.arange(rows), perm] = qv
+    params = np.zeros((rows, cols // 32, 2), np.float16)
+    params[..., 0] = r.uniform(1e-3, 4e-3, (rows, cols // 32))
+    x = r.standard_normal((2, cols)).astype(np.float32)
+    y, e = R.gemv_q8(codes, params, x)
+    s = params[np.arange(rows), perm // 32, 0].astype(np.float64)
+    want = s[None, :] * qv[None, :] * x[:, perm].astype(np.float64)
+    close(y, want, rel=0)
+    close(e, np.abs(want), rel=0)
+
+
+def pin_q8_zero_x():
+    codes, params = _q8(32, 64, 4)
+    y, e = R.gemv_q8(codes, params, np.zeros((1, 64), np.float32))
+    assert np.all(y == 0) and np.all(e == 0)
+
+
+def pin_q8_ones_closed_form():
+    """x = 1: y[r] = Σ_blk (scale·Σ_{c∈blk} q + 32·offset)."""
+    codes, params = _q8(40, 128, 5)
+    y, _ = R.gemv_q8(codes, params, np.ones((1, 128), np.float32))
+    p = params.astype(np.float64)
+    want = [sum(p[r, b, 0] * int(codes[r, 32 * b:32 * b + 32].astype(np.int64).sum()) + 32 * p[r, b, 1]
+                for b in range(4)) for r in range(40)]
+    close(y[0], want, rel=1e-12)
+
+
+def pin_q8_offset_only():
+    """Codes 0: y[r] = Σ_blk offset·Σ_{c∈blk} x[c] (the offset is additive)."""
+    rows, cols = 8, 96
+    codes = np.zeros((rows, cols), np.int8)
+    params = np.zeros((rows, cols // 32, 2), np.float16)
+    params[..., 0] = 3e-3
+    params[..., 1] = np.arange(rows * 3).reshape(rows, 3) * 0.125 - 1.0
+    x = _rng(6).standard_normal(cols).astype(np.float32)
+    y, _ = R.gemv_q8(codes, params, x)
+    xs = x.astype(np.float64).reshape(3, 32).sum(axis=1)
+    want = params[..., 1].astype(np.float64) @ xs
+    close(y[0], want, rel=1e-12)
+
+
+def pin_q8_bruteforce_tiny():
+    for rows, cols, seed in ((32, 32, 7), (33, 64, 8), (5, 96, 9)):
+        codes, params = _q8(rows, cols, seed)
+        x = _rng(seed + 100).standard_normal(cols).astype(np.float32)
+        y, e = R.gemv_q8(codes, params, x)
+        close(y[0], brute_q8(codes, params, x), rel=1e-11, abs_=1e-12)
+        w_abs = [[abs(v) for v in row] for row in R.dequant_q8(codes, params)]
+        e_bf = [sum(w_abs[r][c] * abs(float(x[c])) for c in range(cols)) for r in range(rows)]
+        close(e[0], e_bf, rel=1e-11)
+
+
+def pin_f16_bruteforce_tiny():
+    for rows, cols, seed in ((7, 32, 10), (64, 96, 11)):
+        W = (_rng(seed).standard_normal((rows, cols)) / np.sqrt(cols)).astype(np.float16)
+        x = _rng(seed + 1).standard_normal(cols).astype(np.float32)
+        y, _ = R.gemv_f16(W, x)
+        close(y[0], brute_f16(W, x), rel=1e-11, abs_=1e-12)
+
+
+def pin_projection_linearity():
+    codes, params = _q8(48, 160, 12)
+    r = _rng(13)
+    x1, x2 = r.standard_normal(160), r.standard_normal(160)
+    a = 2.5
+    y1, _ = R.gemv_q8(codes, params, x1)
+    y2, _ = R.gemv_q8(codes, params, x2)
+    y3, _ = R.gemv_q8(codes, params, a * x1 + x2)
+    close(y3, a * y1 + y2, rel=1e-9, abs_=1e-12)
+
+
+def pin_batch_rows_independent():
+    """Row b of a batch depends only on x[b]; permuting positions permutes outputs."""
+    codes, params = _q8(24, 64, 14)
+    X = _rng(15).standard_normal((5, 64))
+    Y, _ = R.gemv_q8(codes, params, X)
+    P = [3, 0, 4, 1, 2]
+    Yp, _ = R.gemv_q8(codes, params, X[P])
+    assert np.array_equal(Yp, Y[P])
+    for b in range(5):
+        yb, _ = R.gemv_q8(codes, params, X[b])
+        close(yb[0], Y[b], rel=1e-13, abs_=1e-15)
+
+
+def pin_quantize_roundtrip_bound():
+    """quantize → dequantize error ≤ scale/2 per element, plus any clamp excess."""
+    W = _rng(16).standard_normal((16, 256)) * 0.1
+    codes, params = R.quantize_q8(W)
+    Wd = R.dequant_q8(codes, params)
+    s = np.repeat(params[..., 0].astype(np.float64), 32, axis=1)
+    o = np.repeat(params[..., 1].astype(np.float64), 32, axis=1)
+    excess = np.maximum(0.0, np.abs(W - o) - 127.5 * s)
+    assert np.all(np.abs(W - Wd) <= s / 2 + excess + 1e-15)
+    assert np.all(np.abs(codes.astype(int)) <= 127)
+
+
+# ------------------------------------------------------------ norm, activation
+def pin_rmsnorm_invariant():
+    """mean_i (y_i/γ_i)² = ms/(ms + eps) with ms = mean(h²)."""
+    r = _rng(17)
+    h = r.standard_normal((4, 300)) * np.array([[1e-3], [1.0], [30.0], [1e3]])
+    g = r.uniform(0.5, 1.5, 300)
+    eps = 1e-6
+    y, inv = R.rmsnorm(h, g, eps)
+    ms = np.mean(h * h, axis=1)
+    close(np.mean((y / g) ** 2, axis=1), ms / (ms + eps), rel=1e-12)
+    close(inv, 1 / np.sqrt(ms + eps), rel=1e-14)
+
+
+def pin_rmsnorm_constant():
+    """h = c, γ = 1: y = c/√(c² + eps) (eps inside the root, as the pages write)."""
+    for c in (1e-3, 0.5, -2.0, 7.0):
+        y, _ = R.rmsnorm(np.full((1, 64), c), np.ones(64), 1e-6)
+        close(y, np.full((1, 64), c / math.sqrt(c * c + 1e-6)), rel=1e-14)
+
+
+def pin_add_rmsnorm_residual():
+    r = _rng(18)
+    h, a = r.standard_normal((3, 50)), r.standard_normal((3, 50))
+    g = r.uniform(0.5, 1.5, 50)
+    hn, y, inv = R.add_rmsnorm(h, a, g, 1e-6)
+    assert np.array_equal(hn, h + a)
+    y2, _ = R.rmsnorm(h + a, g, 1e-6)
+    assert np.array_equal(y, y2)
+    hn0, _, _ = R.add_rmsnorm(h, None, g, 1e-6)
+    assert np.array_equal(hn0, h)
+
+
+def pin_relu2_closed_form():
+    v = np.array([-3.0, -0.0, 0.0, 0.5, 2.0, -1e-30, 1e10])
+    assert np.array_equal(R.relu2(v), np.array([0, 0, 0, 0.25, 4.0, 0, 1e20]))
+
+
+# ------------------------------------------------------------ MoE
+def pin_softmax():
+    r = _rng(19)
+    l = r.standard_normal((6, 128)) * 3
+    p = R.softmax(l)
+    close(p.sum(axis=1), np.ones(6), rel=1e-12)
+    e = np.exp(l - l.max(axis=1, keepdims=True))
+    close(p[:, :5], (e / e.sum(axis=1, keepdims=True))[:, :5], rel=1e-12)
+    # shift invariance and a huge logit must not overflow
+    close(R.softmax(l + 1000.0), p, rel=1e-9)
+    big = R.softmax(np.array([[1000.0, 0.0]]))
+    assert np.isfinite(big).all() and big[0, 0] > 0.999
+    # two logits: p0 = 1/(1+e^(l1-l0))
+    close(R.softmax(np.array([[0.3, -0.2]]))[0, 0], 1 / (1 + math.exp(-0.5)), rel=1e-14)
+
+
+def pin_topk_bruteforce():
+    r = _rng(20)
+    s = np.round(r.standard_normal((10, 20)), 1)          # many exact ties
+    sel = R.topk(s, 6)
+    for b in range(10):
+        want = sorted(range(20), key=lambda i: (-s[b, i], i))[:6]
+        assert list(sel[b]) == want
+
+
+def pin_route_weights():
+    r = _rng(21)
+    l = r.standard_normal((4, 16))
+    sel, w = R.route(l, 3)
+    p = R.softmax(l)
+    for b in range(4):
+        assert list(sel[b]) == sorted(range(16), key=lambda i: (-p[b, i], i))[:3]
+        close(w[b], p[b, sel[b]], rel=0)
+    _, wn = R.route(l, 3, renorm=True)
+    close(wn.sum(axis=1), np.ones(4), rel=1e-14)
+
+
+def pin_group_bruteforce():
+    r = _rng(22)
+    B, k, E = 13, 4, 9
+    sel = np.array([r.choice(E, k, replace=False) for _ in range(B)], np.int32)
+    counts, offsets, entries = R.group(sel, E)
+    assert counts.sum() == B * k and offsets[0] == 0 and offsets[-1] == B * k
+    assert np.array_equal(np.diff(offsets), counts)
+    assert sorted(entries.tolist()) == list(range(B * k))
+    for e in range(E):
+        want = [j for j in range(B * k) if sel.reshape(-1)[j] == e]
+        assert entries[offsets[e]:offsets[e + 1]].tolist() == want
+
+
+def pin_combine_closed_form():
+    B, k, n = 3, 2, 5
+    eo = np.arange(B * k * n, dtype=np.float64).reshape(B * k, n)
+    w = np.array([[1.0, 10.0], [100.0, 0.0], [0.5, -1.0]])
+    m = R.combine(eo, w, k)
+    want = np.stack([1 * eo[0] + 10 * eo[1], 100 * eo[2] + 0 * eo[3], 0.5 * eo[4] - 1 * eo[5]])
+    assert np.array_equal(m, want)
+    o = np.ones((B, n))
+    assert np.array_equal(R.combine(eo, w, k, o), want + 1)
+
+
+def pin_argmax_rules():
+    l = np.array([[1.0, 5.0, 5.0, -2.0],
+                  [np.nan, 0.5, np.nan, 0.5],
+                  [np.nan, np.nan, np.nan, np.nan],
+                  [-np.inf, -3.0e38, -3.1e38, -np.inf],
+                  [-0.0, 0.0, -1.0, -0.0],
+                  [-4.0, -1.0, -1.0, -9.0]])
+    assert R.argmax(l).tolist() == [1, 1, 0, 0, 0, 1]
+
+
+# ------------------------------------------------------------ the pages' constants
+def pin_pages_constants():
+    g = json.load(open(GOLDEN))
+    assert R.PASS_MAX == g["pass_max"]["value"]
+    assert R.ARGMAX_FLOOR == g["argmax_floor"]["value"]
+    a = g["argmax_tie"]
+    assert int(R.argmax(np.array([a["example_logits"]]))[0]) == a["expected_index"]
+    t = g["route_tie"]
+    assert R.topk(np.array([t["example_scores"]]), t["k"])[0].tolist() == t["expected_sel"]
+    gr = g["group_order"]
+    counts, offsets, entries = R.group(np.array(gr["example_sel"]), gr["experts"])
+    assert counts.tolist() == gr["expected_counts"]
+    assert entries.tolist() == gr["expected_entries"]
+
+
+# ------------------------------------------------------------ workloads
+def pin_tiny_mlp_composition():
+    """Identity up (as f16 I), down = I: y = h + relu²(rms(h)·γ)."""
+    n = 32
+    h = _rng(23).standard_normal(n).astype(np.float32)
+    g = np.linspace(0.5, 1.5, n)
+    out = R.tiny_mlp(h, np.eye(n, dtype=np.float16), np.eye(n, dtype=np.float16), g, 1e-6)
+    nrm, _ = R.rmsnorm(h, g, 1e-6)
+    close(out["y"], h[None].astype(np.float64) + R.relu2(nrm), rel=1e-14)
+
+
+def pin_prefill_layer_composition():
+    """With q, o, up, down the identity (scale 1, code 1 on the diagonal) the layer
+    reduces to h1 = h + rms(h)·γ1, h2 = h1 + relu²(rms(h1)·γ2)."""
+    n = 64
+    eye = np.eye(n, dtype=np.int8)
+    par = np.zeros((n, n // 32, 2), np.float16)
+    par[..., 0] = 1.0
+    mats = {s: (eye, par) for s in ("q", "k", "v", "o", "up", "down")}
+    r = _rng(24)
+    h = r.standard_normal((3, n))
+    g1, g2 = r.uniform(0.5, 1.5, n), r.uniform(0.5, 1.5, n)
+    out = R.prefill_layer(h, mats, g1, g2, 1e-6)
+    n1, _ = R.rmsnorm(h, g1, 1e-6)
+    h1 = h + n1
+    n2, _ = R.rmsnorm(h1, g2, 1e-6)
+    close(out["h1"], h1, rel=1e-14)
+    close(out["h2"], h1 + R.relu2(n2), rel=1e-14)
+
+
+def pin_moe_layer_composition():
+    """Experts whose up and down are the identity scaled by (e+1): the MoE output for
+    a position is Σ_s w_s·(e_s+1)²·relu²(n) (with up scale e+1 and down scale 1:
+    eo = relu²((e+1)·n))."""
+    n, E, k, B = 32, 5, 2, 4
+    eye = np.eye(n, dtype=np.int8)
+    experts = []
+    for e in range(E):
+        pu = np.zeros((n, 1, 2), np.float16)
+        pu[..., 0] = e + 1
+        pd = np.zeros((n, 1, 2), np.float16)
+        pd[..., 0] = 1.0
+        experts.append((eye, pu, eye, pd))
+    r = _rng(25)
+    h = r.standard_normal((B, n))
+    g1, g2 = np.ones(n), np.ones(n)
+    router = r.standard_normal((E, n))
+    out = R.moe_layer(h, g1, g2, 1e-6, router, experts, k)
+    nrm, _ = R.rmsnorm(h, g1, 1e-6)
+    logits = nrm @ router.T
+    sel, w = R.route(logits, k)
+    m = np.zeros_like(h)
+    for b in range(B):
+        for s in range(k):
+            m[b] += w[b, s] * R.relu2((sel[b, s] + 1) * nrm[b])
+    close(out["m"], m, rel=1e-12, abs_=1e-15)
+    close(out["h"], h + m, rel=1e-13)
+
+
+def pin_vocab_head_ties():
+    """Duplicated rows give exact ties, which go to the lowest row."""
+    r = _rng(26)
+    W = (r.standard_normal((10, 64)) / 8).astype(np.float16)
+    x = r.standard_normal((2, 64)).astype(np.float32)
+    g = np.ones(64)
+    out = R.vocab_head(x, g, 1e-6, W)
+    best = out["ids"]
+    W2 = np.concatenate([W[best[0]:best[0] + 1], W])   # the winner of position 0 at row 0 and row best+1
+    out2 = R.vocab_head(x, g, 1e-6, W2)
+    assert out2["logits"][0, 0] == out2["logits"][0, best[0] + 1]
+    assert out2["ids"][0] == 0
+
+
+PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

@@ -1,0 +1,158 @@
+"""Plant plausible mistakes in the oracle (on the CPU, by monkeypatching) and check
+that at least one pin catches each: the pins are strong enough to trust."""
+import numpy as np
+import pytest
+
+import oracle.ref as R
+from oracle_pins import PINS
+
+_orig = {k: getattr(R, k) for k in ("dequant_q8", "project", "rmsnorm", "relu2", "softmax",
+                                    "topk", "route", "group", "combine", "argmax")}
+
+
+def _dequant_no_offset(codes, params):
+    rows, cols = np.asarray(codes).shape
+    p = R.as_f64(params).reshape(rows, cols // 32, 2)
+    q = R.as_f64(codes).reshape(rows, cols // 32, 32)
+    return (q * p[:, :, 0:1]).reshape(rows, cols)
+
+
+def _dequant_zero_point(codes, params):
+    rows, cols = np.asarray(codes).shape
+    p = R.as_f64(params).reshape(rows, cols // 32, 2)
+    q = R.as_f64(codes).reshape(rows, cols // 32, 32)
+    return ((q - p[:, :, 1:2]) * p[:, :, 0:1]).reshape(rows, cols)
+
+
+def _dequant_block_index_mod(codes, params):
+    # uses block c % nb instead of c // 32
+    rows, cols = np.asarray(codes).shape
+    nb = cols // 32
+    p = R.as_f64(params).reshape(rows, nb, 2)
+    idx = np.arange(cols) % nb
+    return R.as_f64(codes) * p[:, idx, 0] + p[:, idx, 1]
+
+
+def _dequant_block_16(codes, params):
+    # blocks of 16 columns
+    rows, cols = np.asarray(codes).shape
+    nb = cols // 32
+    p = R.as_f64(params).reshape(rows, nb, 2)
+    idx = np.minimum(np.arange(cols) // 16, nb - 1)
+    return R.as_f64(codes) * p[:, idx, 0] + p[:, idx, 1]
+
+
+def _project_transposed(W, X):
+    W = R.as_f64(W)
+    X = np.atleast_2d(R.as_f64(X))
+    if W.shape[0] == W.shape[1]:
+        return X @ W, np.abs(X) @ np.abs(W)
+    return _orig["project"](W, X)
+
+
+def _project_abs_wrong(W, X):
+    y, e = _orig["project"](W, X)
+    return y, np.abs(y)
+
+
+def _rms_eps_outside(h, gamma, eps):
+    h = np.atleast_2d(R.as_f64(h))
+    inv = 1.0 / (np.sqrt(np.mean(h * h, axis=1)) + eps)
+    return h * inv[:, None] * R.as_f64(gamma)[None, :], inv
+
+
+def _rms_sum_not_mean(h, gamma, eps):
+    h = np.atleast_2d(R.as_f64(h))
+    inv = 1.0 / np.sqrt(np.sum(h * h, axis=1) + eps)
+    return h * inv[:, None] * R.as_f64(gamma)[None, :], inv
+
+
+def _rms_no_gamma(h, gamma, eps):
+    y, inv = _orig["rmsnorm"](h, np.ones_like(R.as_f64(gamma)), eps)
+    return y, inv
+
+
+def _relu_not_squared(v):
+    return np.maximum(R.as_f64(v), 0.0)
+
+
+def _square_no_relu(v):
+    return R.as_f64(v) ** 2
+
+
+def _softmax_unshifted(l):
+    l = np.atleast_2d(R.as_f64(l))
+    with np.errstate(over="ignore", invalid="ignore"):
+        z = np.exp(l)
+        return z / z.sum(axis=1, keepdims=True)
+
+
+def _topk_ties_high(scores, k):
+    s = np.atleast_2d(R.as_f64(scores))
+    ids = np.arange(s.shape[1])
+    return np.array([np.lexsort((-ids, -row))[:k] for row in s], np.int32)
+
+
+def _route_always_renorm(logits, k, renorm=False):
+    return _orig["route"](logits, k, True)
+
+
+def _group_descending(sel, E):
+    c, o, e = _orig["group"](sel, E)
+    e = e.copy()
+    for i in range(E):
+        e[o[i]:o[i + 1]] = e[o[i]:o[i + 1]][::-1]
+    return c, o, e
+
+
+def _combine_slot_reversed(eo, w, k, o=None):
+    return _orig["combine"](eo, np.atleast_2d(R.as_f64(w))[:, ::-1], k, o)
+
+
+def _argmax_last(l):
+    l = np.atleast_2d(R.as_f64(l))
+    out = []
+    for row in l:
+        ok = row > R.ARGMAX_FLOOR
+        out.append(int(np.flatnonzero(ok & (row == row[ok].max()))[-1]) if ok.any() else 0)
+    return np.array(out, np.int32)
+
+
+def _argmax_numpy(l):
+    return np.argmax(np.atleast_2d(R.as_f64(l)), axis=1).astype(np.int32)
+
+
+MUTATIONS = {
+    "dequant drops the offset": ("dequant_q8", _dequant_no_offset),
+    "offset read as a zero-point": ("dequant_q8", _dequant_zero_point),
+    "block index c % nb": ("dequant_q8", _dequant_block_index_mod),
+    "16-column blocks": ("dequant_q8", _dequant_block_16),
+    "transposed weight operand": ("project", _project_transposed),
+    "error scale |W x| instead of |W||x|": ("project", _project_abs_wrong),
+    "eps outside the root": ("rmsnorm", _rms_eps_outside),
+    "sum instead of mean": ("rmsnorm", _rms_sum_not_mean),
+    "gamma dropped": ("rmsnorm", _rms_no_gamma),
+    "relu not squared": ("relu2", _relu_not_squared),
+    "square without relu": ("relu2", _square_no_relu),
+    "softmax without max shift": ("softmax", _softmax_unshifted),
+    "top-k tie to the higher id": ("topk", _topk_ties_high),
+    "router always renormalises": ("route", _route_always_renorm),
+    "groups in descending order": ("group", _group_descending),
+    "combine with slots reversed": ("combine", _combine_slot_reversed),
+    "argmax tie to the last index": ("argmax", _argmax_last),
+    "argmax picks NaN / ignores the floor": ("argmax", _argmax_numpy),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_mutation_is_caught(name, monkeypatch):
+    attr, fn = MUTATIONS[name]
+    monkeypatch.setattr(R, attr, fn)
+    failed = []
+    for pin in PINS:
+        try:
+            with np.errstate(all="ignore"):
+                pin()
+        except (AssertionError, ValueError, IndexError, FloatingPointError):
+            failed.append(pin.__name__)
+    assert failed, f"no pin catches the mutation: {name}"
