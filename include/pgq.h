@@ -1,0 +1,189 @@
+/*
+ * pgq — weight-streaming projection kernels for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI.  Every pointer named "device" is a CUDA device address that the caller
+ * allocated and owns; the library never allocates or frees device memory and keeps
+ * no device state between calls (except the per-device launch configuration it
+ * caches).  Calls are asynchronous and ordered on the given stream (`stream` is a
+ * cudaStream_t; NULL is the legacy default stream).  Argument errors are detected on
+ * the host before anything is launched: the call then returns a non-zero status,
+ * `pgq_last_error()` describes it, and no device memory is touched.  There is no CPU
+ * fallback: without a usable compute-capability-10.3 device every compute call
+ * returns PGQ_ENODEV.
+ *
+ * Layouts (all row-major, C order):
+ *   activations       f32 [B][n]               (B positions, n features)
+ *   f16 matrix W      binary16 [rows][cols]     y[b][r] = sum_c W[r][c] * x[b][c]
+ *   q8 matrix         codes int8 [rows][cols] and params binary16 pairs
+ *                     [rows][cols/32][2] = (scale, offset) per 32-column block:
+ *                     w[r][c] = scale[r][c/32] * codes[r][c] + offset[r][c/32]
+ *
+ * The projection is the one the cortiq-engine pages compute in gemma_batch.rs
+ * (`encode_q82_mm` / `q8_2f_mm_r2`: "y[nb][rows] = x[nb][cols]·Wᵀ") and in the row
+ * kernels the header of embryo_wide.wgsl describes (matrices kept in their packed
+ * form on the device and read in 16-byte loads).  The q8 block format (int8 codes
+ * with a binary16 scale and offset per 32-element block along the row) is this
+ * library's weight format.
+ */
+#ifndef PGQ_H
+#define PGQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- status codes */
+enum {
+  PGQ_OK = 0,
+  PGQ_EINVAL = 1,       /* null pointer, bad shape, B out of range, bad enum */
+  PGQ_EALIGN = 2,       /* a pointer is not aligned as the call requires */
+  PGQ_EUNSUPPORTED = 3, /* shape outside the kernels' limits: nothing launched */
+  PGQ_ECUDA = 4,        /* a CUDA runtime call or launch failed */
+  PGQ_ETIMEOUT = 5,     /* a bounded device-side wait expired */
+  PGQ_ENODEV = 6,       /* no current CUDA device of compute capability 10.3 */
+  PGQ_EWORKSPACE = 7    /* workspace pointer null or smaller than required */
+};
+
+/* Epilogue applied to each projection output element v = (W·x)[b][r]. */
+enum {
+  PGQ_EPI_NONE = 0,  /* y = v */
+  PGQ_EPI_RELU2 = 1, /* y = max(v, 0)^2        (nemotron_prefill.rs `pb_relu2`) */
+  PGQ_EPI_ADD = 2    /* y = residual + v; residual may be the same array as y
+                        (the residual update h += o of `pb_add_rms`, add == 1) */
+};
+
+/* Limits. */
+#define PGQ_QBLOCK 32     /* columns per (scale, offset) block of the q8 format */
+#define PGQ_DECODE_BMAX 8 /* positions per decode call (gemv_*) */
+#define PGQ_PASS_BMAX 64  /* positions per prefill pass (nemotron_prefill.rs `PB_MAX`) */
+#define PGQ_MULTI_MAX 8   /* matrices in one pgq_gemv_q8_multi launch */
+#define PGQ_STAGE_MAX 49152 /* f32 input values a decode launch stages on chip */
+
+/* Short text for a status code (static storage). */
+const char* pgq_status_string(int status);
+
+/* One-line description of the last argument error on the calling thread. */
+const char* pgq_last_error(void);
+
+/* ABI version of this header (incremented on any incompatible change). */
+int pgq_abi_version(void);
+
+/* PGQ_OK if the current CUDA device is a compute-capability-10.3 GPU the kernels
+ * were built for; PGQ_ENODEV otherwise.  Synchronous, launches nothing. */
+int pgq_device_check(void);
+
+/* ---------------------------------------------------------------- a1: add + RMSNorm
+ * For each position b (nemotron_prefill.rs `pb_add_rms` with add = 0/1;
+ * gemma_batch.rs `g4_add_norm_b`):
+ *   h[b] <- h[b] + add[b]                (skipped when add == NULL)
+ *   inv[b] = 1 / sqrt(mean_i h[b][i]^2 + eps)
+ *   y[b][i] = gamma[i] * (h[b][i] * inv[b])
+ * h: device f32 [B][n], updated in place; add: device f32 [B][n] or NULL;
+ * gamma: device f32 [n]; y: device f32 [B][n] (must not overlap h or add);
+ * inv_rms: device f32 [B] or NULL.  1 <= B <= 65535, 4 <= n <= 1<<20, n % 4 == 0,
+ * h, add, gamma, y 16-byte aligned. */
+int pgq_add_rmsnorm(float* h, const float* add, const float* gamma, float eps, int B, int n,
+                    float* y, float* inv_rms, void* stream);
+
+/* ---------------------------------------------------------------- a5: relu²
+ * v[i] <- max(v[i], 0)^2 in place (nemotron_prefill.rs `pb_relu2`).  v: device f32 [n],
+ * 16-byte aligned.  n == 0 is a no-op. */
+int pgq_relu2(float* v, size_t n, void* stream);
+
+/* ---------------------------------------------------------------- a2: f16 GEMV
+ * Decode projection through a binary16 matrix, 1 <= B <= 8 positions:
+ *   xin[b] = x[b]                                    (gamma == NULL)
+ *   xin[b] = gamma * x[b] / sqrt(mean(x[b]^2) + eps) (gamma != NULL: fused RMSNorm)
+ *   y[b][r] = epilogue( sum_c W[r][c] * xin[b][c] )
+ * W: device binary16 [rows][cols]; x: device f32 [B][cols]; gamma: device f32 [cols]
+ * or NULL; y: device f32 [B][rows]; residual: device f32 [B][rows] for PGQ_EPI_ADD
+ * (may equal y), else ignored.  cols % 32 == 0, B*cols <= PGQ_STAGE_MAX (the input
+ * is staged on chip), rows >= 1; W, x, gamma 16-byte aligned; y, residual 4-byte. */
+int pgq_gemv_f16(const uint16_t* W, int rows, int cols, const float* x, int B,
+                 const float* gamma, float eps, float* y, int epilogue, const float* residual,
+                 void* stream);
+
+/* ---------------------------------------------------------------- a7: vocab head
+ * pgq_gemv_f16 (no epilogue) and a per-position argmax of the logits with the rules
+ * of nemotron_prefill.rs `pb_argmax`: the best value starts at -3e38 with index 0 and
+ * only a strictly greater value replaces it, so an exact tie keeps the lowest index,
+ * NaN is never chosen and a row with nothing above -3e38 gives 0.
+ * logits: device f32 [B][rows] or NULL (then not written); ids: device int32 [B].
+ * workspace: device memory of at least pgq_argmax_workspace_bytes(B) bytes, 16-byte
+ * aligned; the call initialises what it uses (no caller set-up).  Calls that share
+ * a workspace must be ordered on one stream. */
+size_t pgq_argmax_workspace_bytes(int B);
+int pgq_gemv_f16_argmax(const uint16_t* W, int rows, int cols, const float* x, int B,
+                        const float* gamma, float eps, float* logits, int32_t* ids,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* Standalone argmax of logits f32 [B][V] (same rules) into ids int32 [B].
+ * 1 <= B <= 65535, V >= 1. */
+int pgq_argmax(const float* logits, int B, int V, int32_t* ids, void* stream);
+
+/* ---------------------------------------------------------------- a3: q8 GEMV
+ * Decode projection through a q8 block-format matrix, 1 <= B <= 8 positions:
+ *   y[b][r] = epilogue( sum_c (scale[r][c/32]*codes[r][c] + offset[r][c/32]) * xin[b][c] )
+ * with xin as in pgq_gemv_f16 (optional fused RMSNorm).  codes: device int8
+ * [rows][cols]; params: device binary16 [rows][cols/32][2]; other arguments as in
+ * pgq_gemv_f16.  cols % 32 == 0, B*cols <= PGQ_STAGE_MAX; codes 8-byte aligned,
+ * params 4-byte aligned, x and gamma 16-byte aligned. */
+int pgq_gemv_q8(const int8_t* codes, const uint16_t* params, int rows, int cols,
+                const float* x, int B, const float* gamma, float eps,
+                float* y, int epilogue, const float* residual, void* stream);
+
+/* Several q8 projections over the same column count in one launch (the layer's
+ * matrices that read the same normed input share its staging).  Each job reads one
+ * of up to 4 inputs; an input with gamma != NULL is RMS-normalised on the fly.
+ * All jobs use the same cols and B; up to PGQ_MULTI_MAX jobs;
+ * ninputs * B * cols <= PGQ_STAGE_MAX. */
+typedef struct {
+  const int8_t* codes;      /* device int8 [rows][cols] */
+  const uint16_t* params;   /* device binary16 [rows][cols/32][2] */
+  int rows;
+  int input;                /* index into the inputs array */
+  float* y;                 /* device f32 [B][rows] */
+  int epilogue;             /* PGQ_EPI_* */
+  const float* residual;    /* device f32 [B][rows] for PGQ_EPI_ADD */
+} pgq_q8_job;
+typedef struct {
+  const float* x;           /* device f32 [B][cols] */
+  const float* gamma;       /* device f32 [cols] or NULL */
+} pgq_input;
+int pgq_gemv_q8_multi(const pgq_q8_job* jobs, int njobs, const pgq_input* inputs, int ninputs,
+                      int cols, int B, float eps, void* stream);
+
+/* ---------------------------------------------------------------- decode workloads
+ * Tiny f16 MLP block for one position (the embryo_wide.wgsl `w_norm` → `w_ffn_up`
+ * → `w_ffn_down` dataflow with relu² as the activation):
+ *   y = h + W_down · relu²( W_up · (gamma * h / sqrt(mean(h^2) + eps)) )
+ * h: device f32 [hidden]; W_up: binary16 [inter][hidden]; W_down: binary16
+ * [hidden][inter]; u: device f32 [inter] (receives relu²(up)); y: device f32
+ * [hidden] (may equal h).  Two launches. */
+int pgq_mlp_f16_decode(const float* h, const uint16_t* W_up, const uint16_t* W_down, int hidden,
+                       int inter, const float* gamma, float eps, float* u, float* y, void* stream);
+
+/* q8 decode layer for one position: n = rms(x)·gamma feeds q, k, v and up (relu²);
+ * o reads x_o (the attention output, computed elsewhere); down reads u = relu²(up).
+ * Outputs q [hidden], k [kv], v [kv], o [hidden], u [inter], down [hidden], all
+ * device f32.  Two launches: {q, k, v, o, up} then {down}. */
+typedef struct {
+  const int8_t* codes;
+  const uint16_t* params;
+} pgq_q8_matrix;
+typedef struct {
+  pgq_q8_matrix q, k, v, o, up, down;  /* q,o [hidden][hidden]; k,v [kv][hidden];
+                                          up [inter][hidden]; down [hidden][inter] */
+  int hidden, kv, inter;
+} pgq_q8_layer;
+int pgq_q8_decode_layer(const pgq_q8_layer* layer, const float* x, const float* x_o,
+                        const float* gamma, float eps, float* q, float* k, float* v, float* o,
+                        float* u, float* down, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PGQ_H */

@@ -1,0 +1,287 @@
+"""Weight-streaming projection kernels for GB300 (sm_103a): the Python binding.
+
+This module only marshals arguments: it checks dtypes, shapes and devices of torch
+tensors, passes their device pointers and the current CUDA stream to the C ABI of
+``libpgq.so`` (declared in ``include/pgq.h``) and raises on a non-zero status.  Every
+step of the computation runs in the library's CUDA kernels; there is no fallback.
+If the library has not been built, every call raises ``RuntimeError``.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpgq.so")
+
+# status codes and epilogues (mirrors include/pgq.h)
+OK, EINVAL, EALIGN, EUNSUPPORTED, ECUDA, ETIMEOUT, ENODEV, EWORKSPACE = range(8)
+EPI_NONE, EPI_RELU2, EPI_ADD = 0, 1, 2
+EPILOGUES = {"none": EPI_NONE, "relu2": EPI_RELU2, "add": EPI_ADD}
+QBLOCK = 32
+DECODE_BMAX = 8
+PASS_BMAX = 64
+
+_vp = C.c_void_p
+
+
+class Q8Job(C.Structure):
+    _fields_ = [("codes", _vp), ("params", _vp), ("rows", C.c_int), ("input", C.c_int),
+                ("y", _vp), ("epilogue", C.c_int), ("residual", _vp)]
+
+
+class Input(C.Structure):
+    _fields_ = [("x", _vp), ("gamma", _vp)]
+
+
+class Q8Matrix(C.Structure):
+    _fields_ = [("codes", _vp), ("params", _vp)]
+
+
+class Q8Layer(C.Structure):
+    _fields_ = [("q", Q8Matrix), ("k", Q8Matrix), ("v", Q8Matrix), ("o", Q8Matrix),
+                ("up", Q8Matrix), ("down", Q8Matrix),
+                ("hidden", C.c_int), ("kv", C.c_int), ("inter", C.c_int)]
+
+
+_SIGS = {
+    "pgq_status_string": (C.c_char_p, [C.c_int]),
+    "pgq_last_error": (C.c_char_p, []),
+    "pgq_abi_version": (C.c_int, []),
+    "pgq_device_check": (C.c_int, []),
+    "pgq_add_rmsnorm": (C.c_int, [_vp, _vp, _vp, C.c_float, C.c_int, C.c_int, _vp, _vp, _vp]),
+    "pgq_relu2": (C.c_int, [_vp, C.c_size_t, _vp]),
+    "pgq_gemv_f16": (C.c_int, [_vp, C.c_int, C.c_int, _vp, C.c_int, _vp, C.c_float, _vp, C.c_int, _vp, _vp]),
+    "pgq_argmax_workspace_bytes": (C.c_size_t, [C.c_int]),
+    "pgq_gemv_f16_argmax": (C.c_int, [_vp, C.c_int, C.c_int, _vp, C.c_int, _vp, C.c_float, _vp, _vp, _vp,
+                                      C.c_size_t, _vp]),
+    "pgq_argmax": (C.c_int, [_vp, C.c_int, C.c_int, _vp, _vp]),
+    "pgq_gemv_q8": (C.c_int, [_vp, _vp, C.c_int, C.c_int, _vp, C.c_int, _vp, C.c_float, _vp, C.c_int, _vp, _vp]),
+    "pgq_gemv_q8_multi": (C.c_int, [C.POINTER(Q8Job), C.c_int, C.POINTER(Input), C.c_int, C.c_int, C.c_int,
+                                    C.c_float, _vp]),
+    "pgq_mlp_f16_decode": (C.c_int, [_vp, _vp, _vp, C.c_int, C.c_int, _vp, C.c_float, _vp, _vp, _vp]),
+    "pgq_q8_decode_layer": (C.c_int, [C.POINTER(Q8Layer), _vp, _vp, _vp, C.c_float, _vp, _vp, _vp, _vp, _vp,
+                                      _vp, _vp]),
+}
+
+_lib = None
+
+
+def lib():
+    """The loaded ``libpgq.so`` (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m prefill_gemv_q8_gb300.build` (nvcc, sm_103a)")
+        L = C.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype, fn.argtypes = res, args
+        _lib = L
+    return _lib
+
+
+class PgqError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(f"pgq status {status} ({status_string(status)}): {msg}")
+        self.status = status
+
+
+def status_string(status: int) -> str:
+    return lib().pgq_status_string(status).decode()
+
+
+def _check(status: int):
+    if status != OK:
+        raise PgqError(status, lib().pgq_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return C.c_void_p(s.cuda_stream)
+
+
+def _need(t, dtype, name, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t
+
+
+def _epi(e):
+    return EPILOGUES[e] if isinstance(e, str) else int(e)
+
+
+# ------------------------------------------------------------------ primitives
+def add_rmsnorm(h, gamma, eps, add=None, y=None, inv=None, stream=None):
+    """h += add (if given); y = gamma * h / sqrt(mean(h²) + eps).  h [B][n] in place."""
+    _need(h, torch.float32, "h")
+    B, n = h.shape
+    _need(gamma, torch.float32, "gamma", (n,))
+    if add is not None:
+        _need(add, torch.float32, "add", (B, n))
+    y = torch.empty_like(h) if y is None else _need(y, torch.float32, "y", (B, n))
+    if inv is not None:
+        _need(inv, torch.float32, "inv", (B,))
+    _check(lib().pgq_add_rmsnorm(_ptr(h), _ptr(add), _ptr(gamma), eps, B, n, _ptr(y), _ptr(inv), _stream(stream)))
+    return y
+
+
+def relu2(v, stream=None):
+    _need(v, torch.float32, "v")
+    _check(lib().pgq_relu2(_ptr(v), v.numel(), _stream(stream)))
+    return v
+
+
+def argmax(logits, ids=None, stream=None):
+    _need(logits, torch.float32, "logits")
+    B, V = logits.shape
+    ids = torch.empty(B, dtype=torch.int32, device=logits.device) if ids is None else ids
+    _need(ids, torch.int32, "ids", (B,))
+    _check(lib().pgq_argmax(_ptr(logits), B, V, _ptr(ids), _stream(stream)))
+    return ids
+
+
+def gemv_f16(W, x, gamma=None, eps=1e-6, epilogue="none", residual=None, y=None, stream=None):
+    """y[b] = epilogue(W · xin[b]) for a binary16 W [rows][cols] and x [B][cols]."""
+    _need(W, torch.float16, "W")
+    rows, cols = W.shape
+    _need(x, torch.float32, "x")
+    B = x.shape[0]
+    if gamma is not None:
+        _need(gamma, torch.float32, "gamma", (cols,))
+    y = torch.empty(B, rows, dtype=torch.float32, device=W.device) if y is None else y
+    _need(y, torch.float32, "y", (B, rows))
+    if residual is not None:
+        _need(residual, torch.float32, "residual", (B, rows))
+    _check(lib().pgq_gemv_f16(_ptr(W), rows, cols, _ptr(x), B, _ptr(gamma), eps, _ptr(y), _epi(epilogue),
+                              _ptr(residual), _stream(stream)))
+    return y
+
+
+def argmax_workspace_bytes(B):
+    return int(lib().pgq_argmax_workspace_bytes(B))
+
+
+def gemv_f16_argmax(W, x, gamma=None, eps=1e-6, logits=True, workspace=None, ids=None, stream=None):
+    """Vocab head: logits = W · xin, ids = per-position argmax.  Returns (ids, logits or None)."""
+    _need(W, torch.float16, "W")
+    rows, cols = W.shape
+    _need(x, torch.float32, "x")
+    B = x.shape[0]
+    dev = W.device
+    if logits is True:
+        logits = torch.empty(B, rows, dtype=torch.float32, device=dev)
+    elif logits is False:
+        logits = None
+    if logits is not None:
+        _need(logits, torch.float32, "logits", (B, rows))
+    ids = torch.empty(B, dtype=torch.int32, device=dev) if ids is None else ids
+    _need(ids, torch.int32, "ids", (B,))
+    need = argmax_workspace_bytes(B)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    _check(lib().pgq_gemv_f16_argmax(_ptr(W), rows, cols, _ptr(x), B, _ptr(gamma), eps, _ptr(logits), _ptr(ids),
+                                     _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                     _stream(stream)))
+    return ids, logits
+
+
+def _q8_check(codes, params, name="W"):
+    _need(codes, torch.int8, name + ".codes")
+    rows, cols = codes.shape
+    _need(params, torch.float16, name + ".params", (rows, cols // QBLOCK, 2))
+    return rows, cols
+
+
+def gemv_q8(codes, params, x, gamma=None, eps=1e-6, epilogue="none", residual=None, y=None, stream=None):
+    """y[b] = epilogue(W · xin[b]) for a q8 block-format W (codes int8 [rows][cols],
+    params binary16 [rows][cols/32][2])."""
+    rows, cols = _q8_check(codes, params)
+    _need(x, torch.float32, "x")
+    B = x.shape[0]
+    y = torch.empty(B, rows, dtype=torch.float32, device=codes.device) if y is None else y
+    _need(y, torch.float32, "y", (B, rows))
+    if residual is not None:
+        _need(residual, torch.float32, "residual", (B, rows))
+    _check(lib().pgq_gemv_q8(_ptr(codes), _ptr(params), rows, cols, _ptr(x), B, _ptr(gamma), eps, _ptr(y),
+                             _epi(epilogue), _ptr(residual), _stream(stream)))
+    return y
+
+
+def gemv_q8_multi(jobs, inputs, eps=1e-6, stream=None):
+    """jobs: list of dicts {codes, params, input, y, epilogue, residual}; inputs: list of
+    (x, gamma or None).  One launch."""
+    cols = jobs[0]["codes"].shape[1]
+    B = inputs[0][0].shape[0]
+    J = (Q8Job * len(jobs))()
+    keep = []
+    for i, j in enumerate(jobs):
+        rows, c = _q8_check(j["codes"], j["params"])
+        if c != cols:
+            raise ValueError("all jobs of one launch must share cols")
+        _need(j["y"], torch.float32, "y", (B, rows))
+        J[i] = Q8Job(j["codes"].data_ptr(), j["params"].data_ptr(), rows, j.get("input", 0), j["y"].data_ptr(),
+                     _epi(j.get("epilogue", "none")),
+                     j["residual"].data_ptr() if j.get("residual") is not None else None)
+    I = (Input * len(inputs))()
+    for i, (x, g) in enumerate(inputs):
+        _need(x, torch.float32, "x", (B, cols))
+        I[i] = Input(x.data_ptr(), g.data_ptr() if g is not None else None)
+    keep.append((J, I))
+    _check(lib().pgq_gemv_q8_multi(J, len(jobs), I, len(inputs), cols, B, eps, _stream(stream)))
+
+
+# ------------------------------------------------------------------ workloads
+def mlp_f16_decode(h, W_up, W_down, gamma, eps=1e-6, u=None, y=None, stream=None):
+    """y = h + W_down · relu²(W_up · rms(h)·gamma) for one position; returns (y, u)."""
+    _need(h, torch.float32, "h")
+    hidden = h.numel()
+    inter = W_up.shape[0]
+    _need(W_up, torch.float16, "W_up", (inter, hidden))
+    _need(W_down, torch.float16, "W_down", (hidden, inter))
+    _need(gamma, torch.float32, "gamma", (hidden,))
+    u = torch.empty(inter, dtype=torch.float32, device=h.device) if u is None else u
+    y = torch.empty_like(h) if y is None else y
+    _check(lib().pgq_mlp_f16_decode(_ptr(h), _ptr(W_up), _ptr(W_down), hidden, inter, _ptr(gamma), eps, _ptr(u),
+                                    _ptr(y), _stream(stream)))
+    return y, u
+
+
+def q8_layer_struct(mats):
+    """ctypes view of a decode layer {slot: (codes, params)}."""
+    hidden = mats["q"][0].shape[1]
+    L = Q8Layer()
+    for s in ("q", "k", "v", "o", "up", "down"):
+        c, p = mats[s]
+        _q8_check(c, p, s)
+        setattr(L, s, Q8Matrix(c.data_ptr(), p.data_ptr()))
+    L.hidden, L.kv, L.inter = hidden, mats["k"][0].shape[0], mats["up"][0].shape[0]
+    return L
+
+
+def q8_decode_layer(mats, x, x_o, gamma, eps=1e-6, out=None, stream=None):
+    """The q8 decode layer for one position; returns dict q, k, v, o, u, down."""
+    L = q8_layer_struct(mats)
+    dev = x.device
+    if out is None:
+        out = {s: torch.empty(n, dtype=torch.float32, device=dev) for s, n in
+               (("q", L.hidden), ("k", L.kv), ("v", L.kv), ("o", L.hidden), ("u", L.inter), ("down", L.hidden))}
+    _check(lib().pgq_q8_decode_layer(C.byref(L), _ptr(x), _ptr(x_o), _ptr(gamma), eps, _ptr(out["q"]),
+                                     _ptr(out["k"]), _ptr(out["v"]), _ptr(out["o"]), _ptr(out["u"]),
+                                     _ptr(out["down"]), _stream(stream)))
+    return out

@@ -1,0 +1,280 @@
+// The C ABI: argument checks on the host, then the launches.  Nothing here computes
+// any part of the path; every result comes from the kernels.
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace pgq {
+
+namespace {
+thread_local char g_err[512] = "";
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+bool g_dev_ok[64];
+bool g_dev_done[64];
+}  // namespace
+
+int set_error(int status, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return status;
+}
+
+bool device_info(DeviceInfo* out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return false;
+  }
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (!g_dev_done[dev]) {
+    DeviceInfo d;
+    d.device = dev;
+    int v = 0;
+    bool ok = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess;
+    ok = ok && cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess;
+    ok = ok && cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess;
+    ok = ok && cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess;
+    d.smem_optin = (size_t)v;
+    g_dev[dev] = d;
+    g_dev_ok[dev] = ok && d.cc_major == 10 && d.cc_minor == 3;
+    g_dev_done[dev] = true;
+  }
+  *out = g_dev[dev];
+  return g_dev_ok[dev];
+}
+
+}  // namespace pgq
+
+using namespace pgq;
+
+#define REQUIRE(cond, status, ...)                \
+  do {                                            \
+    if (!(cond)) return set_error(status, __VA_ARGS__); \
+  } while (0)
+
+#define GET_DEVICE(dev)                                                                  \
+  DeviceInfo dev;                                                                        \
+  if (!device_info(&dev)) return set_error(PGQ_ENODEV, "no current compute-capability-10.3 device")
+
+static inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+static bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const char* pa = static_cast<const char*>(a);
+  const char* pb = static_cast<const char*>(b);
+  return pa < pb + nb && pb < pa + na;
+}
+
+extern "C" {
+
+const char* pgq_status_string(int status) {
+  switch (status) {
+    case PGQ_OK: return "ok";
+    case PGQ_EINVAL: return "invalid argument";
+    case PGQ_EALIGN: return "misaligned pointer";
+    case PGQ_EUNSUPPORTED: return "shape outside the kernels' limits";
+    case PGQ_ECUDA: return "CUDA error";
+    case PGQ_ETIMEOUT: return "device-side wait expired";
+    case PGQ_ENODEV: return "no compute-capability-10.3 device";
+    case PGQ_EWORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+const char* pgq_last_error(void) { return g_err; }
+
+int pgq_abi_version(void) { return 1; }
+
+int pgq_device_check(void) {
+  GET_DEVICE(dev);
+  return PGQ_OK;
+}
+
+int pgq_add_rmsnorm(float* h, const float* add, const float* gamma, float eps, int B, int n, float* y,
+                    float* inv_rms, void* stream) {
+  REQUIRE(h && gamma && y, PGQ_EINVAL, "add_rmsnorm: h, gamma and y must be non-null");
+  REQUIRE(B >= 1 && B <= 65535, PGQ_EINVAL, "add_rmsnorm: B=%d outside 1..65535", B);
+  REQUIRE(n >= 4 && n <= (1 << 20) && n % 4 == 0, PGQ_EINVAL, "add_rmsnorm: n=%d must be a multiple of 4 in 4..2^20", n);
+  REQUIRE(eps >= 0.f, PGQ_EINVAL, "add_rmsnorm: eps must be >= 0");
+  REQUIRE(aligned16(h) && aligned16(gamma) && aligned16(y) && (!add || aligned16(add)), PGQ_EALIGN,
+          "add_rmsnorm: h, add, gamma, y must be 16-byte aligned");
+  REQUIRE(!inv_rms || aligned4(inv_rms), PGQ_EALIGN, "add_rmsnorm: inv_rms must be 4-byte aligned");
+  const size_t bytes = (size_t)B * n * sizeof(float);
+  REQUIRE(!overlaps(y, bytes, h, bytes) && (!add || !overlaps(y, bytes, add, bytes)), PGQ_EINVAL,
+          "add_rmsnorm: y must not overlap h or add");
+  GET_DEVICE(dev);
+  return launch_add_rmsnorm(h, add, gamma, eps, B, n, y, inv_rms, as_stream(stream));
+}
+
+int pgq_relu2(float* v, size_t n, void* stream) {
+  if (n == 0) return PGQ_OK;
+  REQUIRE(v, PGQ_EINVAL, "relu2: v must be non-null");
+  REQUIRE(aligned16(v), PGQ_EALIGN, "relu2: v must be 16-byte aligned");
+  GET_DEVICE(dev);
+  return launch_relu2(v, n, as_stream(stream), dev.sms);
+}
+
+int pgq_argmax(const float* logits, int B, int V, int32_t* ids, void* stream) {
+  REQUIRE(logits && ids, PGQ_EINVAL, "argmax: logits and ids must be non-null");
+  REQUIRE(B >= 1 && B <= 65535 && V >= 1, PGQ_EINVAL, "argmax: B=%d V=%d out of range", B, V);
+  REQUIRE(aligned4(logits) && aligned4(ids), PGQ_EALIGN, "argmax: pointers must be 4-byte aligned");
+  GET_DEVICE(dev);
+  return launch_argmax(logits, B, V, ids, as_stream(stream));
+}
+
+// ------------------------------------------------------------------ decode GEMVs
+static int check_decode_common(const char* name, int rows, int cols, const float* x, int B, const float* gamma,
+                               float eps, const float* y_or_null, int epilogue, const float* residual) {
+  REQUIRE(x, PGQ_EINVAL, "%s: x must be non-null", name);
+  REQUIRE(rows >= 1, PGQ_EINVAL, "%s: rows=%d must be >= 1", name, rows);
+  REQUIRE(cols >= 32 && cols % 32 == 0, PGQ_EINVAL, "%s: cols=%d must be a positive multiple of 32", name, cols);
+  REQUIRE(B >= 1 && B <= PGQ_DECODE_BMAX, PGQ_EINVAL, "%s: B=%d outside 1..%d", name, B, PGQ_DECODE_BMAX);
+  REQUIRE((size_t)B * cols <= PGQ_STAGE_MAX, PGQ_EUNSUPPORTED, "%s: B*cols=%d exceeds %d staged values", name,
+          B * cols, PGQ_STAGE_MAX);
+  REQUIRE(epilogue >= PGQ_EPI_NONE && epilogue <= PGQ_EPI_ADD, PGQ_EINVAL, "%s: bad epilogue %d", name, epilogue);
+  REQUIRE(epilogue != PGQ_EPI_ADD || residual, PGQ_EINVAL, "%s: PGQ_EPI_ADD needs a residual", name);
+  REQUIRE(!gamma || eps >= 0.f, PGQ_EINVAL, "%s: eps must be >= 0", name);
+  REQUIRE(aligned16(x) && (!gamma || aligned16(gamma)), PGQ_EALIGN, "%s: x and gamma must be 16-byte aligned", name);
+  REQUIRE((!y_or_null || aligned4(y_or_null)) && (!residual || aligned4(residual)), PGQ_EALIGN,
+          "%s: y and residual must be 4-byte aligned", name);
+  if (y_or_null) {
+    const size_t yb = (size_t)B * rows * sizeof(float);
+    REQUIRE(!overlaps(y_or_null, yb, x, (size_t)B * cols * sizeof(float)), PGQ_EINVAL, "%s: y overlaps x", name);
+    REQUIRE(!residual || residual == y_or_null || !overlaps(y_or_null, yb, residual, yb), PGQ_EINVAL,
+            "%s: residual must be y itself or not overlap it", name);
+  }
+  return PGQ_OK;
+}
+
+int pgq_gemv_f16(const uint16_t* W, int rows, int cols, const float* x, int B, const float* gamma, float eps, float* y,
+                 int epilogue, const float* residual, void* stream) {
+  REQUIRE(W && y, PGQ_EINVAL, "gemv_f16: W and y must be non-null");
+  REQUIRE(aligned16(W), PGQ_EALIGN, "gemv_f16: W must be 16-byte aligned");
+  int st = check_decode_common("gemv_f16", rows, cols, x, B, gamma, eps, y, epilogue, residual);
+  if (st) return st;
+  GET_DEVICE(dev);
+  GvParams P{};
+  P.job[0] = GvJob{reinterpret_cast<const uint8_t*>(W), nullptr, y, residual, rows, 0, epilogue, 0};
+  P.in[0] = GvInput{x, gamma};
+  P.njobs = 1;
+  P.ninputs = 1;
+  P.B = B;
+  P.cols = cols;
+  P.eps = eps;
+  return launch_gemv(P, false, false, dev, as_stream(stream));
+}
+
+size_t pgq_argmax_workspace_bytes(int B) {
+  DeviceInfo dev;
+  if (!device_info(&dev)) dev.sms = 160;  // an upper bound when no device is current
+  if (B < 1) B = 1;
+  return gemv_argmax_workspace_bytes(B, dev);
+}
+
+int pgq_gemv_f16_argmax(const uint16_t* W, int rows, int cols, const float* x, int B, const float* gamma, float eps,
+                        float* logits, int32_t* ids, void* workspace, size_t workspace_bytes, void* stream) {
+  REQUIRE(W && ids, PGQ_EINVAL, "gemv_f16_argmax: W and ids must be non-null");
+  REQUIRE(aligned16(W) && aligned4(ids), PGQ_EALIGN, "gemv_f16_argmax: W 16-byte, ids 4-byte aligned");
+  int st = check_decode_common("gemv_f16_argmax", rows, cols, x, B, gamma, eps, logits, PGQ_EPI_NONE, nullptr);
+  if (st) return st;
+  GET_DEVICE(dev);
+  const size_t need = gemv_argmax_workspace_bytes(B, dev);
+  REQUIRE(workspace && aligned16(workspace) && workspace_bytes >= need, PGQ_EWORKSPACE,
+          "gemv_f16_argmax: workspace needs %zu bytes, 16-byte aligned", need);
+  GvParams P{};
+  P.job[0] = GvJob{reinterpret_cast<const uint8_t*>(W), nullptr, logits, nullptr, rows, 0, PGQ_EPI_NONE, 0};
+  P.in[0] = GvInput{x, gamma};
+  P.njobs = 1;
+  P.ninputs = 1;
+  P.B = B;
+  P.cols = cols;
+  P.eps = eps;
+  const size_t parts = (size_t)dev.sms * B;
+  char* ws = static_cast<char*>(workspace);
+  P.part_val = reinterpret_cast<float*>(ws);
+  P.part_idx = reinterpret_cast<int*>(ws + ((parts * sizeof(float) + 15) & ~size_t(15)));
+  P.ticket = reinterpret_cast<unsigned*>(ws + ((parts * sizeof(float) + 15) & ~size_t(15)) +
+                                         ((parts * sizeof(int) + 15) & ~size_t(15)));
+  P.ids = ids;
+  return launch_gemv(P, false, true, dev, as_stream(stream));
+}
+
+int pgq_gemv_q8(const int8_t* codes, const uint16_t* params, int rows, int cols, const float* x, int B,
+                const float* gamma, float eps, float* y, int epilogue, const float* residual, void* stream) {
+  pgq_q8_job job{codes, params, rows, 0, y, epilogue, residual};
+  pgq_input in{x, gamma};
+  return pgq_gemv_q8_multi(&job, 1, &in, 1, cols, B, eps, stream);
+}
+
+int pgq_gemv_q8_multi(const pgq_q8_job* jobs, int njobs, const pgq_input* inputs, int ninputs, int cols, int B,
+                      float eps, void* stream) {
+  REQUIRE(jobs && inputs, PGQ_EINVAL, "gemv_q8: jobs and inputs must be non-null");
+  REQUIRE(njobs >= 1 && njobs <= PGQ_MULTI_MAX, PGQ_EINVAL, "gemv_q8: njobs=%d outside 1..%d", njobs, PGQ_MULTI_MAX);
+  REQUIRE(ninputs >= 1 && ninputs <= MAX_INPUTS, PGQ_EINVAL, "gemv_q8: ninputs=%d outside 1..%d", ninputs,
+          MAX_INPUTS);
+  REQUIRE((size_t)ninputs * B * cols <= PGQ_STAGE_MAX, PGQ_EUNSUPPORTED,
+          "gemv_q8: ninputs*B*cols=%d exceeds %d staged values", ninputs * B * cols, PGQ_STAGE_MAX);
+  for (int i = 0; i < ninputs; ++i) {
+    int st = check_decode_common("gemv_q8", 1, cols, inputs[i].x, B, inputs[i].gamma, eps, nullptr, PGQ_EPI_NONE,
+                                 nullptr);
+    if (st) return st;
+  }
+  GvParams P{};
+  for (int j = 0; j < njobs; ++j) {
+    const pgq_q8_job& J = jobs[j];
+    REQUIRE(J.codes && J.params && J.y, PGQ_EINVAL, "gemv_q8: job %d has a null codes/params/y", j);
+    REQUIRE(aligned8(J.codes) && aligned4(J.params), PGQ_EALIGN, "gemv_q8: job %d codes 8-byte, params 4-byte", j);
+    REQUIRE(J.input >= 0 && J.input < ninputs, PGQ_EINVAL, "gemv_q8: job %d input %d out of range", j, J.input);
+    int st = check_decode_common("gemv_q8", J.rows, cols, inputs[J.input].x, B, inputs[J.input].gamma, eps, J.y,
+                                 J.epilogue, J.residual);
+    if (st) return st;
+    for (int i = 0; i < ninputs; ++i)
+      REQUIRE(!overlaps(J.y, (size_t)B * J.rows * 4, inputs[i].x, (size_t)B * cols * 4), PGQ_EINVAL,
+              "gemv_q8: job %d output overlaps input %d", j, i);
+    P.job[j] = GvJob{reinterpret_cast<const uint8_t*>(J.codes), reinterpret_cast<const uint32_t*>(J.params), J.y,
+                     J.residual, J.rows, J.input, J.epilogue, 0};
+  }
+  GET_DEVICE(dev);
+  for (int i = 0; i < ninputs; ++i) P.in[i] = GvInput{inputs[i].x, inputs[i].gamma};
+  P.njobs = njobs;
+  P.ninputs = ninputs;
+  P.B = B;
+  P.cols = cols;
+  P.eps = eps;
+  return launch_gemv(P, true, false, dev, as_stream(stream));
+}
+
+// ------------------------------------------------------------------ decode workloads
+int pgq_mlp_f16_decode(const float* h, const uint16_t* W_up, const uint16_t* W_down, int hidden, int inter,
+                       const float* gamma, float eps, float* u, float* y, void* stream) {
+  REQUIRE(h && W_up && W_down && gamma && u && y, PGQ_EINVAL, "mlp_f16_decode: null pointer");
+  REQUIRE(!overlaps(u, (size_t)inter * 4, h, (size_t)hidden * 4) && !overlaps(u, (size_t)inter * 4, y, (size_t)hidden * 4),
+          PGQ_EINVAL, "mlp_f16_decode: u must not overlap h or y");
+  int st = pgq_gemv_f16(W_up, inter, hidden, h, 1, gamma, eps, u, PGQ_EPI_RELU2, nullptr, stream);
+  if (st) return st;
+  return pgq_gemv_f16(W_down, hidden, inter, u, 1, nullptr, 0.f, y, PGQ_EPI_ADD, h, stream);
+}
+
+int pgq_q8_decode_layer(const pgq_q8_layer* L, const float* x, const float* x_o, const float* gamma, float eps,
+                        float* q, float* k, float* v, float* o, float* u, float* down, void* stream) {
+  REQUIRE(L && x && x_o && gamma && q && k && v && o && u && down, PGQ_EINVAL, "q8_decode_layer: null pointer");
+  const int H = L->hidden, KV = L->kv, I = L->inter;
+  pgq_q8_job jobs[5] = {
+      {L->q.codes, L->q.params, H, 0, q, PGQ_EPI_NONE, nullptr},
+      {L->k.codes, L->k.params, KV, 0, k, PGQ_EPI_NONE, nullptr},
+      {L->v.codes, L->v.params, KV, 0, v, PGQ_EPI_NONE, nullptr},
+      {L->o.codes, L->o.params, H, 1, o, PGQ_EPI_NONE, nullptr},
+      {L->up.codes, L->up.params, I, 0, u, PGQ_EPI_RELU2, nullptr},
+  };
+  pgq_input ins[2] = {{x, gamma}, {x_o, nullptr}};
+  int st = pgq_gemv_q8_multi(jobs, 5, ins, 2, H, 1, eps, stream);
+  if (st) return st;
+  return pgq_gemv_q8(L->down.codes, L->down.params, H, I, u, 1, nullptr, 0.f, down, PGQ_EPI_NONE, nullptr, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,451 @@
+// Decode projections y[b] = W·x[b] for 1..8 positions, weights streamed from HBM
+// once, f32 arithmetic on the CUDA cores.
+//
+// Prior art: the row kernels of embryo_wide.wgsl (matrices in packed form, 16-byte
+// loads, a thread walks a bounded stretch of a row and partial sums are reduced by
+// the consumer) and nemotron_prefill.rs `pb_q8_bank` (a subgroup owns four rows at
+// a time and keeps the staged input in workgroup memory).  Here:
+//
+// * A task is R = 4 consecutive rows of one matrix over its whole row.  The row is
+//   cut into 256-column chunks; `wpt` warps of a block share a task, each taking
+//   every wpt-th chunk, so a task's weights stream through several warps at once
+//   and the per-task reduction is amortised over several chunks per warp.
+// * In a chunk each lane owns 8 consecutive columns: one 8-byte load of codes (q8)
+//   or one 16-byte load (f16) per row, fully coalesced.  For q8 the lane's 8 columns
+//   lie in one 32-column block, so one (scale, offset) pair serves them.
+// * The input x (optionally RMS-normalised on the fly) is staged once per block in
+//   shared memory in a permuted order that makes each lane's two float4 reads of a
+//   chunk bank-conflict free; it is reused for all rows of all tasks of the block.
+// * Loads run D steps ahead of the arithmetic (a register ring), so every warp keeps
+//   several kilobytes of weights in flight.
+// * q8 codes become exact floats with a byte-permute into the mantissa of 2^23 and a
+//   packed subtraction; w = scale·q + offset and the dot products use packed f32x2
+//   FMAs.  Each row's reduction order is independent of the row's index, so equal
+//   rows give equal bits (the argmax tie rule relies on it).
+#include <algorithm>
+#include <mutex>
+#include <map>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace pgq {
+
+constexpr int GV_WARPS = 8;
+constexpr int GV_THREADS = GV_WARPS * 32;
+constexpr int GV_CHUNK = 256;
+constexpr int GV_R = 4;
+
+template <bool Q8>
+struct Raw;
+template <>
+struct Raw<true> {
+  uint2 c[GV_R];
+  uint32_t p[GV_R];
+  int job, row0, chunk;
+  bool ok;
+};
+template <>
+struct Raw<false> {
+  uint4 w[GV_R];
+  int job, row0, chunk;
+  bool ok;
+};
+
+__device__ __forceinline__ void group_sync(int group, int wpt) {
+  if (wpt == 1) {
+    __syncwarp();
+  } else {
+    asm volatile("bar.sync %0, %1;" ::"r"(group + 1), "r"(wpt * 32) : "memory");
+  }
+}
+
+// Butterfly reduce-scatter of N (power of two, <= 32) per-lane values: afterwards
+// lane l with l % (32/N) == 0 holds the warp total of value l / (32/N).
+template <int N>
+__device__ __forceinline__ float reduce_scatter(float (&v)[N], int lane) {
+#pragma unroll
+  for (int n = N, o = 16; n > 1; n >>= 1, o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int j = 0; j < n / 2; ++j) {
+      const float mine = up ? v[j + n / 2] : v[j];
+      const float other = up ? v[j] : v[j + n / 2];
+      v[j] = mine + __shfl_xor_sync(0xffffffffu, other, o);
+    }
+  }
+  float t = v[0];
+#pragma unroll
+  for (int o = 16 / N; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+  return t;
+}
+
+// Position of column c in the staged (permuted) input row.
+__device__ __forceinline__ int perm_col(int c) {
+  const int chunk = c >> 8, within = c & 255;
+  return (chunk << 8) + (((within >> 2) & 1) << 7) + ((within >> 3) << 2) + (within & 3);
+}
+
+template <bool Q8, int NB, int D, bool ARGMAX>
+__global__ void __launch_bounds__(GV_THREADS, 1)
+gemv_kernel(const __grid_constant__ GvParams P) {
+  extern __shared__ __align__(16) float smem[];
+  float* xs = smem;                                           // [ninputs][NB][cols_pad]
+  float* red = xs + (size_t)P.ninputs * NB * P.cols_pad;      // [groups][2][wpt][GV_R*NB]
+  __shared__ float s_inv[MAX_INPUTS * NB];
+  __shared__ float s_red[GV_WARPS];
+  __shared__ float s_gbv[GV_WARPS * NB];
+  __shared__ int s_gbi[GV_WARPS * NB];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int cols = P.cols, cols_pad = P.cols_pad, cols4 = cols >> 2;
+
+  // ---- stage the inputs (RMS-normalised where gamma is given)
+  for (int i = 0; i < P.ninputs; ++i) {
+    const float4* x4 = reinterpret_cast<const float4*>(P.in[i].x);
+    const float4* g4 = reinterpret_cast<const float4*>(P.in[i].gamma);
+    if (g4) {
+      for (int b = 0; b < P.B; ++b) {
+        float ss = 0.f;
+        for (int c = tid; c < cols4; c += GV_THREADS) {
+          const float4 v = x4[(size_t)b * cols4 + c];
+          ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        }
+        ss = warp_sum(ss);
+        __syncthreads();
+        if (lane == 0) s_red[warp] = ss;
+        __syncthreads();
+        if (tid == 0) {
+          float t = 0.f;
+          for (int w = 0; w < GV_WARPS; ++w) t += s_red[w];
+          s_inv[i * NB + b] = rsqrtf(t / (float)cols + P.eps);
+        }
+      }
+      __syncthreads();
+    }
+    for (int e = tid; e < NB * cols4; e += GV_THREADS) {
+      const int b = e / cols4, c4 = e - b * cols4;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (b < P.B) {
+        v = x4[(size_t)b * cols4 + c4];
+        if (g4) {
+          const float inv = s_inv[i * NB + b];
+          const float4 g = g4[c4];
+          v = make_float4(g.x * (v.x * inv), g.y * (v.y * inv), g.z * (v.z * inv), g.w * (v.w * inv));
+        }
+      }
+      *reinterpret_cast<float4*>(xs + (size_t)(i * NB + b) * cols_pad + perm_col(c4 * 4)) = v;
+    }
+  }
+  __syncthreads();
+
+  // ---- task loop of this warp's group
+  const int wpt = P.wpt, groups = P.groups, cpw = P.cpw;
+  const int group = warp / wpt, wg = warp - group * wpt;
+  const int gg = blockIdx.x * groups + group;
+  const int TG = gridDim.x * groups;
+  const int my_tasks = gg < P.ntasks ? (P.ntasks - 1 - gg) / TG + 1 : 0;
+  const int nsteps = my_tasks * cpw;
+  float* gred = red + (size_t)group * 2 * wpt * (GV_R * NB);
+
+  auto fetch = [&](Raw<Q8>& raw, int s) {
+    raw.ok = false;
+    if (s >= nsteps) return;
+    const int i = s / cpw, cc = s - i * cpw;
+    const int task = gg + i * TG;
+    int j = 0;
+#pragma unroll 1
+    while (j + 1 < P.njobs && task >= P.job[j + 1].task_begin) ++j;
+    raw.job = j;
+    raw.row0 = (task - P.job[j].task_begin) * GV_R;
+    raw.chunk = wg + cc * wpt;
+    const int col = raw.chunk * GV_CHUNK + lane * 8;
+    if (raw.chunk >= P.nchunks || col >= cols) return;
+    raw.ok = true;
+    const int rows = P.job[j].rows;
+#pragma unroll
+    for (int r = 0; r < GV_R; ++r) {
+      const size_t row = (size_t)min(raw.row0 + r, rows - 1);
+      if constexpr (Q8) {
+        raw.c[r] = ld_stream_u2(P.job[j].w + row * cols + col);
+        raw.p[r] = ld_nc_u32(P.job[j].params + row * (cols >> 5) + (col >> 5));
+      } else {
+        raw.w[r] = ld_stream_u4(P.job[j].w + (row * cols + col) * 2);
+      }
+    }
+  };
+
+  float2 acc[GV_R][NB];
+#pragma unroll
+  for (int r = 0; r < GV_R; ++r)
+#pragma unroll
+    for (int b = 0; b < NB; ++b) acc[r][b] = make_float2(0.f, 0.f);
+
+  float best_v[NB];
+  int best_i[NB];
+#pragma unroll
+  for (int b = 0; b < NB; ++b) { best_v[b] = ARGMAX_FLOOR; best_i[b] = 0; }
+
+  auto compute = [&](const Raw<Q8>& raw) {
+    if (!raw.ok) return;
+    const float* xb = xs + (size_t)P.job[raw.job].input * NB * cols_pad + raw.chunk * GV_CHUNK + lane * 4;
+    float2 xv[NB][4];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      const float4 a = *reinterpret_cast<const float4*>(xb + (size_t)b * cols_pad);
+      const float4 c = *reinterpret_cast<const float4*>(xb + (size_t)b * cols_pad + 128);
+      xv[b][0] = make_float2(a.x, a.y); xv[b][1] = make_float2(a.z, a.w);
+      xv[b][2] = make_float2(c.x, c.y); xv[b][3] = make_float2(c.z, c.w);
+    }
+#pragma unroll
+    for (int r = 0; r < GV_R; ++r) {
+      float2 w[4];
+      if constexpr (Q8) {
+        float2 q[4];
+        s8x4_to_f32(raw.c[r].x, q[0], q[1]);
+        s8x4_to_f32(raw.c[r].y, q[2], q[3]);
+        const float2 so = h2_to_f2(raw.p[r]);
+        const float2 s2 = make_float2(so.x, so.x), o2 = make_float2(so.y, so.y);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) w[t] = ffma2(q[t], s2, o2);
+      } else {
+        w[0] = h2_to_f2(raw.w[r].x); w[1] = h2_to_f2(raw.w[r].y);
+        w[2] = h2_to_f2(raw.w[r].z); w[3] = h2_to_f2(raw.w[r].w);
+      }
+#pragma unroll
+      for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int t = 0; t < 4; ++t) acc[r][b] = ffma2(w[t], xv[b][t], acc[r][b]);
+    }
+  };
+
+  int rbuf = 0;
+  auto finish_task = [&](int s) {
+    const int i = s / cpw;
+    const int task = gg + i * TG;
+    int j = 0;
+#pragma unroll 1
+    while (j + 1 < P.njobs && task >= P.job[j + 1].task_begin) ++j;
+    const int row0 = (task - P.job[j].task_begin) * GV_R;
+    float v[GV_R * NB];
+#pragma unroll
+    for (int r = 0; r < GV_R; ++r)
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        v[r * NB + b] = acc[r][b].x + acc[r][b].y;
+        acc[r][b] = make_float2(0.f, 0.f);
+      }
+    constexpr int N = GV_R * NB;
+    const float t = reduce_scatter<N>(v, lane);
+    float* buf = gred + (size_t)rbuf * wpt * N;
+    if ((lane & (32 / N - 1)) == 0) buf[wg * N + lane / (32 / N)] = t;
+    group_sync(group, wpt);
+    if (wg == 0) {
+      float out = 0.f;
+      const int r = lane / NB, b = lane - (lane / NB) * NB;
+      if (lane < N) {
+        for (int w = 0; w < wpt; ++w) out += buf[w * N + lane];
+      }
+      const int rows = P.job[j].rows;
+      const int row = row0 + r;
+      const bool live = lane < N && row < rows && b < P.B;
+      if (live) {
+        const int epi = P.job[j].epilogue;
+        if (epi == PGQ_EPI_RELU2) {
+          out = fmaxf(out, 0.f);
+          out = out * out;
+        } else if (epi == PGQ_EPI_ADD) {
+          out += P.job[j].residual[(size_t)b * rows + row];
+        }
+        if (P.job[j].y) P.job[j].y[(size_t)b * rows + row] = out;
+      }
+      if constexpr (ARGMAX) {
+        float cv = live ? out : __int_as_float(0xff800000u);
+        int ci = live ? row : 0x7fffffff;
+#pragma unroll
+        for (int o = NB; o < N; o <<= 1) {
+          const float ov = __shfl_down_sync(0xffffffffu, cv, o);
+          const int oi = __shfl_down_sync(0xffffffffu, ci, o);
+          if (lane + o < 32) argmax_merge(cv, ci, ov, oi);
+        }
+        // lanes 0..NB-1 now hold this task's best for position `lane`
+#pragma unroll
+        for (int bb = 0; bb < NB; ++bb)
+          if (lane == bb) argmax_merge(best_v[bb], best_i[bb], cv, ci);
+      }
+    }
+    rbuf ^= 1;
+  };
+
+  Raw<Q8> ring[D];
+#pragma unroll
+  for (int d = 0; d < D; ++d) fetch(ring[d], d);
+  for (int s0 = 0; s0 < nsteps; s0 += D) {
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      const int s = s0 + d;
+      if (s < nsteps) {
+        compute(ring[d]);
+        fetch(ring[d], s + D);
+        if ((s % cpw) == cpw - 1) finish_task(s);
+      }
+    }
+  }
+
+  if constexpr (ARGMAX) {
+    __syncthreads();
+    if (wg == 0) {
+#pragma unroll
+      for (int bb = 0; bb < NB; ++bb)
+        if (lane == bb) {
+          s_gbv[group * NB + bb] = best_v[bb];
+          s_gbi[group * NB + bb] = best_i[bb];
+        }
+    }
+    __syncthreads();
+    if (tid < P.B) {
+      float bv = ARGMAX_FLOOR;
+      int bi = 0;
+      for (int g = 0; g < groups; ++g) argmax_merge(bv, bi, s_gbv[g * NB + tid], s_gbi[g * NB + tid]);
+      P.part_val[(size_t)blockIdx.x * P.B + tid] = bv;
+      P.part_idx[(size_t)blockIdx.x * P.B + tid] = bi;
+    }
+    __threadfence();
+    __syncthreads();
+    __shared__ unsigned s_ticket;
+    if (tid == 0) s_ticket = atomicAdd(P.ticket, 1u);
+    __syncthreads();
+    if (s_ticket == gridDim.x - 1) {
+      __threadfence();
+      if (tid < P.B) {
+        float bv = ARGMAX_FLOOR;
+        int bi = 0;
+        for (int c = 0; c < (int)gridDim.x; ++c)
+          argmax_merge(bv, bi, __ldcg(P.part_val + (size_t)c * P.B + tid),
+                       __ldcg(P.part_idx + (size_t)c * P.B + tid));
+        P.ids[tid] = bi;
+      }
+      if (tid == 0) *P.ticket = 0u;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ host side
+namespace {
+
+using KernelFn = void (*)(GvParams);
+
+template <bool Q8, int NB, bool ARGMAX>
+constexpr KernelFn pick_kernel() {
+  constexpr int D = NB <= 2 ? 4 : (NB <= 4 ? 3 : 2);
+  return reinterpret_cast<KernelFn>(&gemv_kernel<Q8, NB, D, ARGMAX>);
+}
+
+KernelFn kernel_for(bool q8, int nb, bool argmax) {
+  if (q8) {
+    switch (nb) {
+      case 1: return pick_kernel<true, 1, false>();
+      case 2: return pick_kernel<true, 2, false>();
+      case 4: return pick_kernel<true, 4, false>();
+      default: return pick_kernel<true, 8, false>();
+    }
+  }
+  if (argmax) {
+    switch (nb) {
+      case 1: return pick_kernel<false, 1, true>();
+      case 2: return pick_kernel<false, 2, true>();
+      case 4: return pick_kernel<false, 4, true>();
+      default: return pick_kernel<false, 8, true>();
+    }
+  }
+  switch (nb) {
+    case 1: return pick_kernel<false, 1, false>();
+    case 2: return pick_kernel<false, 2, false>();
+    case 4: return pick_kernel<false, 4, false>();
+    default: return pick_kernel<false, 8, false>();
+  }
+}
+
+int round_nb(int B) { return B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : 8; }
+
+struct OccKey {
+  KernelFn fn;
+  int dev;
+  size_t smem;
+  bool operator<(const OccKey& o) const {
+    if (fn != o.fn) return fn < o.fn;
+    if (dev != o.dev) return dev < o.dev;
+    return smem < o.smem;
+  }
+};
+std::mutex g_mu;
+std::map<OccKey, int> g_occ;
+
+int blocks_per_sm(KernelFn fn, const DeviceInfo& dev, size_t smem) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  OccKey key{fn, dev.device, smem};
+  auto it = g_occ.find(key);
+  if (it != g_occ.end()) return it->second;
+  cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)dev.smem_optin);
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, reinterpret_cast<const void*>(fn), GV_THREADS, smem) !=
+      cudaSuccess)
+    n = 1;
+  n = std::max(1, std::min(n, 2));
+  g_occ[key] = n;
+  return n;
+}
+
+}  // namespace
+
+int gemv_grid(int B, bool q8, bool argmax, const DeviceInfo& dev) {
+  (void)B; (void)q8; (void)argmax;
+  // the argmax variant always runs one block per SM so its partials are bounded
+  return dev.sms;
+}
+
+size_t gemv_argmax_workspace_bytes(int B, const DeviceInfo& dev) {
+  const size_t parts = (size_t)dev.sms * (size_t)B;
+  const size_t a = (parts * sizeof(float) + 15) & ~size_t(15);
+  const size_t b = (parts * sizeof(int) + 15) & ~size_t(15);
+  return a + b + 16;
+}
+
+int launch_gemv(GvParams& P, bool q8, bool argmax, const DeviceInfo& dev, cudaStream_t st) {
+  const int nb = round_nb(P.B);
+  P.nchunks = (P.cols + GV_CHUNK - 1) / GV_CHUNK;
+  P.cols_pad = P.nchunks * GV_CHUNK;
+  int wpt = 1;
+  while (wpt < GV_WARPS && P.nchunks >= 4 * (wpt * 2)) wpt *= 2;
+  P.wpt = wpt;
+  P.groups = GV_WARPS / wpt;
+  P.cpw = (P.nchunks + wpt - 1) / wpt;
+  int t = 0;
+  for (int j = 0; j < P.njobs; ++j) {
+    P.job[j].task_begin = t;
+    t += (P.job[j].rows + GV_R - 1) / GV_R;
+  }
+  P.ntasks = t;
+  const size_t smem = ((size_t)P.ninputs * nb * P.cols_pad + (size_t)P.groups * 2 * wpt * GV_R * nb) * sizeof(float);
+  if (smem > dev.smem_optin) return set_error(PGQ_EUNSUPPORTED, "staged input needs %zu bytes of shared memory", smem);
+  KernelFn fn = kernel_for(q8, nb, argmax);
+  int grid;
+  if (argmax) {
+    grid = dev.sms;
+    if (cudaMemsetAsync(P.ticket, 0, sizeof(unsigned), st) != cudaSuccess) return PGQ_ECUDA;
+  } else {
+    const int occ = blocks_per_sm(fn, dev, smem);
+    const int max_grid = dev.sms * occ;
+    // as many blocks as keep every group busy for the same number of tasks
+    const int per_group = (P.ntasks + max_grid * P.groups - 1) / (max_grid * P.groups);
+    grid = (P.ntasks + per_group * P.groups - 1) / (per_group * P.groups);
+    grid = std::max(1, std::min(grid, max_grid));
+  }
+  blocks_per_sm(fn, dev, smem);  // sets the dynamic shared-memory limit once
+  void* args[] = {&P};
+  return cuda_status(cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(grid), dim3(GV_THREADS), args,
+                                      smem, st));
+}
+
+}  // namespace pgq

@@ -1,0 +1,54 @@
+// Internal launch interface between the C-ABI layer and the kernel files.
+#pragma once
+#include "common.cuh"
+
+namespace pgq {
+
+constexpr int MAX_INPUTS = 4;
+
+// One projection of a multi-job decode launch.
+struct GvJob {
+  const uint8_t* w;          // int8 codes or binary16 matrix
+  const uint32_t* params;    // q8: (scale, offset) binary16 pairs [rows][cols/32]
+  float* y;                  // [B][rows] (may be null for the argmax variant)
+  const float* residual;     // [B][rows] for PGQ_EPI_ADD
+  int rows;
+  int input;
+  int epilogue;
+  int task_begin;            // first task index of this job (filled by the launcher)
+};
+struct GvInput {
+  const float* x;            // [B][cols]
+  const float* gamma;        // [cols] or null
+};
+struct GvParams {
+  GvJob job[PGQ_MULTI_MAX];
+  GvInput in[MAX_INPUTS];
+  int njobs, ninputs;
+  int B, cols, cols_pad, nchunks;
+  int wpt;                   // warps per task (K split inside the block)
+  int groups;                // tasks in flight per block = warps / wpt
+  int cpw;                   // chunks per warp per task
+  int ntasks;
+  float eps;
+  // argmax variant
+  float* part_val;           // [grid][B]
+  int* part_idx;             // [grid][B]
+  unsigned* ticket;
+  int32_t* ids;              // [B]
+};
+
+int launch_add_rmsnorm(float* h, const float* add, const float* gamma, float eps, int B, int n,
+                       float* y, float* inv, cudaStream_t st);
+int launch_relu2(float* v, size_t n, cudaStream_t st, int sms);
+int launch_argmax(const float* logits, int B, int V, int32_t* ids, cudaStream_t st);
+
+// Decode GEMV (q8 or f16), multi-job; `argmax` only with f16 and one job.
+// Fills the derived fields of P and the jobs' task_begin.
+int launch_gemv(GvParams& P, bool q8, bool argmax, const DeviceInfo& dev, cudaStream_t st);
+// Workspace of the argmax variant: partials [grid][B] (value, index) + ticket.
+size_t gemv_argmax_workspace_bytes(int B, const DeviceInfo& dev);
+// Exact grid of a decode GEMV launch (used to size the argmax partials).
+int gemv_grid(int B, bool q8, bool argmax, const DeviceInfo& dev);
+
+}  // namespace pgq

@@ -1,0 +1,123 @@
+// Residual add + RMSNorm, relu², and the standalone per-position argmax.
+//
+// add + RMSNorm follows nemotron_prefill.rs `pb_add_rms` (add = 0/1) and
+// gemma_batch.rs `g4_add_norm_b`: one block per position, the block's partial sums
+// of h² reduced in a fixed order, inv = 1/sqrt(mean + eps), y = γ·(h·inv).
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace pgq {
+
+constexpr int NORM_THREADS = 256;
+
+// Fixed-order block reduction of one float (result valid in every thread).
+__device__ __forceinline__ float block_sum_256(float v, float* red) {
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int i = 0; i < NORM_THREADS / 32; ++i) t += red[i];
+  return t;
+}
+
+__global__ void __launch_bounds__(NORM_THREADS)
+add_rmsnorm_kernel(float* __restrict__ h, const float* __restrict__ add,
+                   const float* __restrict__ gamma, float eps, int n,
+                   float* __restrict__ y, float* __restrict__ inv_out) {
+  __shared__ float red[NORM_THREADS / 32];
+  const size_t base = (size_t)blockIdx.x * n;
+  float4* h4 = reinterpret_cast<float4*>(h + base);
+  const float4* a4 = add ? reinterpret_cast<const float4*>(add + base) : nullptr;
+  const int n4 = n >> 2;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < n4; i += NORM_THREADS) {
+    float4 v = h4[i];
+    if (a4) {
+      const float4 a = a4[i];
+      v.x += a.x; v.y += a.y; v.z += a.z; v.w += a.w;
+      h4[i] = v;
+    }
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
+  ss = block_sum_256(ss, red);
+  const float inv = rsqrtf(ss / (float)n + eps);
+  if (inv_out && threadIdx.x == 0) inv_out[blockIdx.x] = inv;
+  const float4* g4 = reinterpret_cast<const float4*>(gamma);
+  float4* y4 = reinterpret_cast<float4*>(y + base);
+  for (int i = threadIdx.x; i < n4; i += NORM_THREADS) {
+    const float4 v = h4[i];
+    const float4 g = g4[i];
+    y4[i] = make_float4(g.x * (v.x * inv), g.y * (v.y * inv), g.z * (v.z * inv), g.w * (v.w * inv));
+  }
+}
+
+__global__ void relu2_kernel(float4* __restrict__ v, size_t n4) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4;
+       i += (size_t)gridDim.x * blockDim.x) {
+    float4 a = v[i];
+    a.x = fmaxf(a.x, 0.f); a.y = fmaxf(a.y, 0.f); a.z = fmaxf(a.z, 0.f); a.w = fmaxf(a.w, 0.f);
+    v[i] = make_float4(a.x * a.x, a.y * a.y, a.z * a.z, a.w * a.w);
+  }
+}
+__global__ void relu2_tail_kernel(float* __restrict__ v, size_t from, size_t n) {
+  const size_t i = from + threadIdx.x;
+  if (i < n) { const float a = fmaxf(v[i], 0.f); v[i] = a * a; }
+}
+
+// One block per position: a strided scan with a strict `>` (each thread keeps the
+// lowest index among its equal values), then a tree that keeps the larger value
+// or, on a tie, the lower index (nemotron_prefill.rs `pb_argmax`).
+__global__ void __launch_bounds__(NORM_THREADS)
+argmax_kernel(const float* __restrict__ logits, int V, int32_t* __restrict__ ids) {
+  __shared__ float sv[NORM_THREADS];
+  __shared__ int si[NORM_THREADS];
+  const float* row = logits + (size_t)blockIdx.x * V;
+  float bv = ARGMAX_FLOOR;
+  int bi = 0;
+  for (int i = threadIdx.x; i < V; i += NORM_THREADS) {
+    const float v = row[i];
+    if (v > bv) { bv = v; bi = i; }
+  }
+  sv[threadIdx.x] = bv;
+  si[threadIdx.x] = bi;
+  __syncthreads();
+  for (int s = NORM_THREADS / 2; s > 0; s >>= 1) {
+    if (threadIdx.x < s) {
+      float a = sv[threadIdx.x];
+      int ai = si[threadIdx.x];
+      argmax_merge(a, ai, sv[threadIdx.x + s], si[threadIdx.x + s]);
+      sv[threadIdx.x] = a;
+      si[threadIdx.x] = ai;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) ids[blockIdx.x] = si[0];
+}
+
+// ------------------------------------------------------------------ launchers
+int launch_add_rmsnorm(float* h, const float* add, const float* gamma, float eps, int B, int n,
+                       float* y, float* inv, cudaStream_t st) {
+  add_rmsnorm_kernel<<<B, NORM_THREADS, 0, st>>>(h, add, gamma, eps, n, y, inv);
+  return cuda_status(cudaGetLastError());
+}
+
+int launch_relu2(float* v, size_t n, cudaStream_t st, int sms) {
+  const size_t n4 = n / 4;
+  if (n4) {
+    const size_t want = (n4 + 255) / 256;
+    const int grid = (int)(want < (size_t)sms * 8 ? want : (size_t)sms * 8);
+    relu2_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<float4*>(v), n4);
+  }
+  if (n % 4) relu2_tail_kernel<<<1, 4, 0, st>>>(v, n4 * 4, n);
+  return cuda_status(cudaGetLastError());
+}
+
+int launch_argmax(const float* logits, int B, int V, int32_t* ids, cudaStream_t st) {
+  argmax_kernel<<<B, NORM_THREADS, 0, st>>>(logits, V, ids);
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace pgq
