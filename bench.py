@@ -1,0 +1,386 @@
+#!/usr/bin/env python3
+"""Benchmark of the weight-streaming projection path on GB300.
+
+Prints ONE JSON line.  The headline workload is the q8 decode layer (B = 1, hidden
+4096, kv 1024, inter 14336: q, k, v, o, up, down in the q8 block format, 179,306,496
+weight bytes): value = weight GB/s over the whole step (add+RMSNorm fused into the
+first launch, relu² fused into up, two launches).  The other workloads (the tiny f16
+MLP block, the 32-layer B = 64 prefill pass, the MoE prefill layer and the vocab head)
+are reported under "workloads" with their own metric, roofline and launch counts.
+
+Rules kept: W >= 3 warm-up steps; weights rotate over copies whose total exceeds the
+L2 (or exceed it on their own); CUDA events on the launching stream; clocks sampled
+with nvidia-smi during the timed region; the oracle (``--impl reference`` or the
+``cpu_baseline`` leg) runs on the host cores on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "weight GB/s & % of HBM roofline (B=1 decode); positions/s (B=64 prefill)"
+FALLBACK_HBM = 6800.0
+
+
+# ------------------------------------------------------------------ helpers
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), src="measured")
+    return dict(hbm=FALLBACK_HBM, bf16=1900.0, bf16_sustained=1700.0, src="fallback")
+
+
+def source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, "prefill_gemv_q8_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key, files):
+    """DRAM bytes per launch from a committed ncu capture, or None when the kernel's
+    source changed since the capture (or there is none)."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel_key)
+    if not d or d.get("source_sha") != source_sha(files):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) >= 9 and f[1].isdigit():
+                    rows.append(f)
+        except OSError:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except OSError:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [int(r[1]) for r in rows]
+        mx = max(int(r[2]) for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ workloads
+Q8_FILES = ["gemv.cu", "common.cuh", "kernels.cuh"]
+
+
+class Q8DecodeLayer:
+    """q8 decode layer, B = 1.  Step = {norm+q,k,v,o,up} launch + {down} launch."""
+    name = "q8 decode layer B=1 (hidden 4096, kv 1024, inter 14336)"
+
+    def __init__(self, torch, pgq, synth, copies=3):
+        c = synth.Q8_LAYER
+        self.t, self.pgq = torch, pgq
+        self.H, self.KV, self.I = c["hidden"], c["kv"], c["inter"]
+        wl = c["workload"]
+        base = synth.q8_layer(wl, 0, self.H, self.KV, self.I, "torch", "cuda")
+        # copies of the weights at distinct addresses: 3 x 179 MB > 129 MB L2
+        self.layers = [base] + [{s: (cc.clone(), pp.clone()) for s, (cc, pp) in base.items()}
+                                for _ in range(copies - 1)]
+        self.x = synth.normal((1, self.H), 1.0, wl, synth.T_X, "torch", "cuda")
+        self.xo = synth.normal((1, self.H), 1.0, wl, synth.T_XO, "torch", "cuda")
+        self.g = synth.gamma(self.H, wl, backend="torch", device="cuda")
+        f = lambda n: torch.empty(1, n, dtype=torch.float32, device="cuda")  # noqa: E731
+        self.out = dict(q=f(self.H), k=f(self.KV), v=f(self.KV), o=f(self.H), u=f(self.I), down=f(self.H))
+        sizes = {"q": (self.H, self.H), "k": (self.KV, self.H), "v": (self.KV, self.H), "o": (self.H, self.H),
+                 "up": (self.I, self.H), "down": (self.H, self.I)}
+        self.bytes = {s: r * c_ + r * (c_ // 32) * 4 for s, (r, c_) in sizes.items()}
+        self.step_bytes = sum(self.bytes.values())
+        self.k1_bytes = self.step_bytes - self.bytes["down"]
+        self.launches_per_step = 2
+        self.i = 0
+
+    def launch1(self, L):
+        o = self.out
+        self.pgq.gemv_q8_multi(
+            [dict(codes=L["q"][0], params=L["q"][1], y=o["q"], input=0),
+             dict(codes=L["k"][0], params=L["k"][1], y=o["k"], input=0),
+             dict(codes=L["v"][0], params=L["v"][1], y=o["v"], input=0),
+             dict(codes=L["o"][0], params=L["o"][1], y=o["o"], input=1),
+             dict(codes=L["up"][0], params=L["up"][1], y=o["u"], input=0, epilogue="relu2")],
+            [(self.x, self.g), (self.xo, None)], eps=1e-6)
+
+    def launch2(self, L):
+        self.pgq.gemv_q8(L["down"][0], L["down"][1], self.out["u"], y=self.out["down"])
+
+    def next_layer(self):
+        L = self.layers[self.i % len(self.layers)]
+        self.i += 1
+        return L
+
+    def e2e_setup(self):
+        t = self.t
+        self.hx = t.empty((1, self.H), dtype=t.float32).pin_memory()
+        self.hxo = t.empty((1, self.H), dtype=t.float32).pin_memory()
+        self.hx.copy_(self.x.cpu())
+        self.hxo.copy_(self.xo.cpu())
+        self.hout = {k: t.empty(v.shape, dtype=t.float32).pin_memory() for k, v in self.out.items()}
+        self.h2d = (self.hx.numel() + self.hxo.numel()) * 4
+        self.d2h = sum(v.numel() for v in self.out.values()) * 4
+
+    def e2e_step(self):
+        """Public API end to end: pinned host inputs in, the layer, outputs back out."""
+        self.x.copy_(self.hx, non_blocking=True)
+        self.xo.copy_(self.hxo, non_blocking=True)
+        L = self.next_layer()
+        self.pgq.q8_decode_layer(L, self.x[0], self.xo[0], self.g, 1e-6,
+                                 out={k: v[0] for k, v in self.out.items()})
+        for k, v in self.out.items():
+            self.hout[k].copy_(v, non_blocking=True)
+
+    def oracle_sample(self, frac):
+        """Oracle inputs for a row sample of every matrix (host copies of the inputs)."""
+        L = self.layers[0]
+        mats = {}
+        for s, (c, p) in L.items():
+            r = max(1, int(c.shape[0] * frac))
+            mats[s] = (c[:r].cpu().numpy(), p[:r].cpu().numpy())
+        x = self.x.cpu().numpy()[0]
+        xo = self.xo.cpu().numpy()[0]
+        g = self.g.cpu().numpy()
+        u = np.abs(np.random.default_rng(0).standard_normal(self.I)).astype(np.float32)
+        nbytes = sum(c.size + p.size * 2 for c, p in mats.values())
+        return mats, x, xo, g, u, nbytes
+
+
+def time_q8_layer(torch, W, steps, warmup):
+    st = torch.cuda.current_stream()
+    for _ in range(warmup):
+        L = W.next_layer()
+        W.launch1(L)
+        W.launch2(L)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        L = W.next_layer()
+        ev[i][0].record(st)
+        W.launch1(L)
+        ev[i][1].record(st)
+        W.launch2(L)
+        ev[i][2].record(st)
+    torch.cuda.synchronize()
+    total = ev[0][0].elapsed_time(ev[-1][2])
+    k1 = [e[0].elapsed_time(e[1]) for e in ev]
+    k2 = [e[1].elapsed_time(e[2]) for e in ev]
+    return total, statistics.mean(k1), statistics.mean(k2)
+
+
+def time_e2e(torch, W, steps, warmup):
+    W.e2e_setup()
+    st = torch.cuda.current_stream()
+    for _ in range(warmup):
+        W.e2e_step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for _ in range(steps):
+        W.e2e_step()
+    b.record(st)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def cpu_baseline_q8(W, target_s=15.0):
+    """The oracle as it stands, timed on the host on a row sample of the layer."""
+    import oracle
+    frac = 0.02
+    mats, x, xo, g, u, nbytes = W.oracle_sample(frac)
+    t0 = time.perf_counter()
+    oracle.q8_decode_layer(x, xo, g, 1e-6, mats, u_in=u[: mats["down"][0].shape[1]])
+    dt = time.perf_counter() - t0
+    # grow the sample to about target_s of work
+    frac = min(1.0, frac * max(1.0, target_s / max(dt, 1e-3)))
+    mats, x, xo, g, u, nbytes = W.oracle_sample(frac)
+    t0 = time.perf_counter()
+    oracle.q8_decode_layer(x, xo, g, 1e-6, mats, u_in=u)
+    dt = time.perf_counter() - t0
+    return dict(value=nbytes / dt / 1e9, unit="GB/s", cores=os.cpu_count(), kind="oracle",
+                sample=f"{frac:.3f} of the rows of each of the six matrices ({nbytes} weight bytes), one pass, "
+                       f"{dt:.1f} s; numpy f64 (elementwise single-threaded, matmul multi-threaded)")
+
+
+# ------------------------------------------------------------------ main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="pgq", choices=["pgq", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    import synth
+    import prefill_gemv_q8_gb300 as pgq
+    from prefill_gemv_q8_gb300 import build
+    build.build()
+    if pgq.lib().pgq_device_check() != pgq.OK:
+        raise SystemExit("libpgq: " + pgq.lib().pgq_last_error().decode())
+
+    pk = peaks()
+    W = Q8DecodeLayer(torch, pgq, synth)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    with Clocks(local) as clk:
+        total_ms, k1_ms, k2_ms = time_q8_layer(torch, W, args.steps, args.warmup)
+    clocks = clk.summary()
+    e2e_ms = time_e2e(torch, W, args.steps, args.warmup)
+    t = torch.tensor([total_ms, e2e_ms], device="cuda")
+    if dist:
+        dist.barrier()
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms, e2e_ms = float(t[0]), float(t[1])
+    ms_step = total_ms / args.steps
+    value = world * W.step_bytes / (ms_step * 1e-3) / 1e9
+    achieved = W.k1_bytes / (k1_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "q8 weights (int8 + f16 scale/offset), f32 arithmetic", "data": "synthetic",
+        "config": {"workload": W.name, "weight_bytes_per_step": W.step_bytes, "B": 1,
+                   "l2": "weights rotate over 3 copies (538 MB > 129 MB L2)", "launches_per_step": 2,
+                   "parallelism": f"replicas x{world}"},
+        "frac_of_hbm": round(value / world / pk["hbm"], 4),
+        "roofline": {"bound": "hbm", "kernel": "gemv_kernel<q8,B=1> (norm + q,k,v,o,up)",
+                     "achieved": round(achieved, 1), "peak": pk["hbm"], "unit": "GB/s",
+                     "frac": round(achieved / pk["hbm"], 4), "peak_src": pk["src"],
+                     "traffic": ncu_traffic("gemv_q8_layer_multi", Q8_FILES),
+                     "algorithmic_bytes_per_launch": W.k1_bytes, "avg_launch_ms": round(k1_ms, 5),
+                     "down_launch_ms": round(k2_ms, 5)},
+        "e2e": {"value": round(world * W.step_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": W.h2d, "d2h_bytes_per_step": W.d2h, "ms_per_step": round(e2e_ms, 5)},
+        "gpu_launches": W.launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_q8(W)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def run_reference(args, rank, world):
+    """The oracle timed on the host cores, on the headline workload's metric."""
+    if rank != 0:
+        return
+    import torch
+    import synth
+
+    class HostLayer(Q8DecodeLayer):
+        def __init__(self):
+            c = synth.Q8_LAYER
+            self.H, self.KV, self.I = c["hidden"], c["kv"], c["inter"]
+            self.frac = 1.0 / 8
+            wl = c["workload"]
+            self.mats = {}
+            nb = 0
+            for s, (r, cc) in synth.q8_layer_shapes(self.H, self.KV, self.I).items():
+                rr = max(4, int(r * self.frac))
+                codes, params = synth.q8_matrix(rr, cc, wl, synth.q8_tensor_id(0, s))
+                self.mats[s] = (codes, params)
+                nb += codes.size + params.size * 2
+            self.nbytes = nb
+            self.x = synth.normal((self.H,), 1.0, wl, synth.T_X)
+            self.xo = synth.normal((self.H,), 1.0, wl, synth.T_XO)
+            self.g = synth.gamma(self.H, wl)
+            self.u = np.abs(synth.normal((self.I,), 1.0, wl, 99))
+
+    import oracle
+    Wh = HostLayer()
+    for _ in range(args.warmup):
+        oracle.q8_decode_layer(Wh.x, Wh.xo, Wh.g, 1e-6, Wh.mats, u_in=Wh.u)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.q8_decode_layer(Wh.x, Wh.xo, Wh.g, 1e-6, Wh.mats, u_in=Wh.u)
+    dt = (time.perf_counter() - t0) / args.steps
+    v = Wh.nbytes / dt / 1e9
+    sample = (f"1/8 of the rows of each q8 matrix of the decode layer ({Wh.nbytes} weight bytes) per step; "
+              "numpy f64 oracle")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": Q8DecodeLayer.name, "B": 1},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+    del torch
+
+
+if __name__ == "__main__":
+    main()
