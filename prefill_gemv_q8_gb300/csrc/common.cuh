@@ -19,14 +19,17 @@ struct DeviceInfo {
 // Cached per device; returns false if no usable device is current.
 bool device_info(DeviceInfo* out);
 
-inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? PGQ_OK : PGQ_ECUDA; }
-
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned8(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
 inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-// Records a one-line description of the last argument error (per thread).
+// Records a one-line description of the last error (per thread); returns status.
 int set_error(int status, const char* fmt, ...);
+
+inline int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return PGQ_OK;
+  return set_error(PGQ_ECUDA, "CUDA: %s", cudaGetErrorString(e));
+}
 
 // ------------------------------------------------------------------ device side
 // Streaming 8/16-byte loads of read-once weights: not kept in L1.

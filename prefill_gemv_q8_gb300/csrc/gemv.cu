@@ -386,15 +386,29 @@ int blocks_per_sm(KernelFn fn, const DeviceInfo& dev, size_t smem) {
   OccKey key{fn, dev.device, smem};
   auto it = g_occ.find(key);
   if (it != g_occ.end()) return it->second;
-  cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       (int)dev.smem_optin);
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, reinterpret_cast<const void*>(fn), GV_THREADS, smem) !=
-      cudaSuccess)
+      cudaSuccess) {
+    cudaGetLastError();
     n = 1;
+  }
   n = std::max(1, std::min(n, 2));
   g_occ[key] = n;
   return n;
+}
+
+// Raises the kernel's dynamic shared-memory limit to `smem` (once per size).
+cudaError_t allow_smem(KernelFn fn, size_t smem) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  static std::map<std::pair<KernelFn, int>, size_t> done;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  auto& cur = done[{fn, dev}];
+  if (smem <= cur) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess) cur = smem;
+  return e;
 }
 
 }  // namespace
@@ -428,12 +442,15 @@ int launch_gemv(GvParams& P, bool q8, bool argmax, const DeviceInfo& dev, cudaSt
   }
   P.ntasks = t;
   const size_t smem = ((size_t)P.ninputs * nb * P.cols_pad + (size_t)P.groups * 2 * wpt * GV_R * nb) * sizeof(float);
-  if (smem > dev.smem_optin) return set_error(PGQ_EUNSUPPORTED, "staged input needs %zu bytes of shared memory", smem);
+  if (smem + 2048 > dev.smem_optin) return set_error(PGQ_EUNSUPPORTED, "staged input needs %zu bytes of shared memory", smem);
   KernelFn fn = kernel_for(q8, nb, argmax);
+  if (cudaError_t e = allow_smem(fn, smem); e != cudaSuccess)
+    return set_error(PGQ_ECUDA, "gemv: shared-memory limit %zu: %s", smem, cudaGetErrorString(e));
   int grid;
   if (argmax) {
     grid = dev.sms;
-    if (cudaMemsetAsync(P.ticket, 0, sizeof(unsigned), st) != cudaSuccess) return PGQ_ECUDA;
+    if (cudaError_t e = cudaMemsetAsync(P.ticket, 0, sizeof(unsigned), st); e != cudaSuccess)
+      return cuda_status(e);
   } else {
     const int occ = blocks_per_sm(fn, dev, smem);
     const int max_grid = dev.sms * occ;
@@ -442,7 +459,6 @@ int launch_gemv(GvParams& P, bool q8, bool argmax, const DeviceInfo& dev, cudaSt
     grid = (P.ntasks + per_group * P.groups - 1) / (per_group * P.groups);
     grid = std::max(1, std::min(grid, max_grid));
   }
-  blocks_per_sm(fn, dev, smem);  // sets the dynamic shared-memory limit once
   void* args[] = {&P};
   return cuda_status(cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(grid), dim3(GV_THREADS), args,
                                       smem, st));
