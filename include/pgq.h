@@ -183,6 +183,29 @@ int pgq_q8_decode_layer(const pgq_q8_layer* layer, const float* x, const float* 
                         const float* gamma, float eps, float* q, float* k, float* v, float* o,
                         float* u, float* down, void* stream);
 
+/* ---------------------------------------------------------------- a4: prefill q8
+ * Batched prefill projection of a pass of 1 <= B <= 64 positions through q8
+ * matrices, every weight read from memory once per pass (nemotron_prefill.rs
+ * module header: "every weight read once per pass"; gemma_batch.rs `q8_2f_mm_r2`):
+ *   Y[b][r] = epilogue( sum_c (scale[r][c/32]*codes[r][c] + offset[r][c/32]) * X[b][c] )
+ * computed on the tensor cores with binary16 operands and f32 accumulation: w is
+ * rounded once to binary16, X[b] is scaled by a power of two per position and
+ * rounded to binary16 (the scale is undone exactly in the epilogue), so
+ * |error| <= (2^-11 + 2^-11 + accumulation) * sum_c |w||x| per element.
+ * X: device f32 [B][cols]; Y, residual: device f32 [B][rows]; residual may equal Y
+ * for PGQ_EPI_ADD.  cols % 128 == 0; codes, params, X 16-byte aligned.
+ * workspace: device memory of pgq_prefill_q8_workspace_bytes(...) bytes (256-byte
+ * aligned) holding the binary16 copy of X, split-K partials, tile tickets and the
+ * status word; the call initialises what it uses.  Calls sharing a workspace must
+ * be ordered on one stream.  Up to 4 jobs (matrices reading the same X) per call. */
+size_t pgq_prefill_q8_workspace_bytes(const int* rows, int njobs, int cols, int B);
+int pgq_prefill_q8(const pgq_q8_job* jobs, int njobs, const float* X, int cols, int B,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* Status word of the last prefill call that used `workspace` (PGQ_OK or
+ * PGQ_ETIMEOUT when a bounded device-side wait expired).  Synchronises the stream. */
+int pgq_prefill_status(const void* workspace, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

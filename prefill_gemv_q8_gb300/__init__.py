@@ -64,6 +64,9 @@ _SIGS = {
     "pgq_mlp_f16_decode": (C.c_int, [_vp, _vp, _vp, C.c_int, C.c_int, _vp, C.c_float, _vp, _vp, _vp]),
     "pgq_q8_decode_layer": (C.c_int, [C.POINTER(Q8Layer), _vp, _vp, _vp, C.c_float, _vp, _vp, _vp, _vp, _vp,
                                       _vp, _vp]),
+    "pgq_prefill_q8_workspace_bytes": (C.c_size_t, [C.POINTER(C.c_int), C.c_int, C.c_int, C.c_int]),
+    "pgq_prefill_q8": (C.c_int, [C.POINTER(Q8Job), C.c_int, _vp, C.c_int, C.c_int, _vp, C.c_size_t, _vp]),
+    "pgq_prefill_status": (C.c_int, [_vp, _vp]),
 }
 
 _lib = None
@@ -244,6 +247,49 @@ def gemv_q8_multi(jobs, inputs, eps=1e-6, stream=None):
         I[i] = Input(x.data_ptr(), g.data_ptr() if g is not None else None)
     keep.append((J, I))
     _check(lib().pgq_gemv_q8_multi(J, len(jobs), I, len(inputs), cols, B, eps, _stream(stream)))
+
+
+def _jobs_struct(jobs, B, cols):
+    J = (Q8Job * len(jobs))()
+    for i, j in enumerate(jobs):
+        rows, c = _q8_check(j["codes"], j["params"])
+        if c != cols:
+            raise ValueError("all jobs of one launch must share cols")
+        _need(j["y"], torch.float32, "y", (B, rows))
+        res = j.get("residual")
+        if res is not None:
+            _need(res, torch.float32, "residual", (B, rows))
+        J[i] = Q8Job(j["codes"].data_ptr(), j["params"].data_ptr(), rows, j.get("input", 0), j["y"].data_ptr(),
+                     _epi(j.get("epilogue", "none")), res.data_ptr() if res is not None else None)
+    return J
+
+
+def prefill_workspace_bytes(rows, cols, B):
+    rows = list(rows)
+    arr = (C.c_int * len(rows))(*rows)
+    return int(lib().pgq_prefill_q8_workspace_bytes(arr, len(rows), cols, B))
+
+
+def prefill_workspace(rows, cols, B, device="cuda"):
+    return torch.empty(prefill_workspace_bytes(rows, cols, B), dtype=torch.uint8, device=device)
+
+
+def prefill_q8(jobs, X, workspace=None, stream=None):
+    """Batched prefill projection: for each job {codes, params, y, epilogue, residual},
+    y = epilogue(W · X[b]) for the B <= 64 positions of X [B][cols] (one launch of the
+    binary16 conversion of X and one tensor-core GEMM launch)."""
+    _need(X, torch.float32, "X")
+    B, cols = X.shape
+    J = _jobs_struct(jobs, B, cols)
+    if workspace is None:
+        workspace = prefill_workspace([j["codes"].shape[0] for j in jobs], cols, B, X.device)
+    _check(lib().pgq_prefill_q8(J, len(jobs), _ptr(X), cols, B, _ptr(workspace), workspace.numel(),
+                                _stream(stream)))
+    return workspace
+
+
+def prefill_status(workspace, stream=None):
+    return int(lib().pgq_prefill_status(_ptr(workspace), _stream(stream)))
 
 
 # ------------------------------------------------------------------ workloads

@@ -1,6 +1,7 @@
 // The C ABI: argument checks on the host, then the launches.  Nothing here computes
 // any part of the path; every result comes from the kernels.
 #include <cstdarg>
+#include <cstdlib>
 #include <cstdio>
 #include <mutex>
 
@@ -275,6 +276,68 @@ int pgq_q8_decode_layer(const pgq_q8_layer* L, const float* x, const float* x_o,
   int st = pgq_gemv_q8_multi(jobs, 5, ins, 2, H, 1, eps, stream);
   if (st) return st;
   return pgq_gemv_q8(L->down.codes, L->down.params, H, I, u, 1, nullptr, 0.f, down, PGQ_EPI_NONE, nullptr, stream);
+}
+
+// ------------------------------------------------------------------ prefill
+static int prefill_a_tmem = -1;  // A operand in tensor memory (1) or shared memory (0)
+
+static bool use_a_tmem() {
+  if (prefill_a_tmem < 0) {
+    const char* e = getenv("PGQ_PREFILL_A_SMEM");
+    prefill_a_tmem = (e && e[0] == '1') ? 0 : 1;
+  }
+  return prefill_a_tmem == 1;
+}
+
+size_t pgq_prefill_q8_workspace_bytes(const int* rows, int njobs, int cols, int B) {
+  if (!rows || njobs < 1 || njobs > TC_MAXJOBS || cols < 128 || B < 1 || B > PGQ_PASS_BMAX) return 0;
+  DeviceInfo dev;
+  if (!device_info(&dev)) dev.sms = 160;
+  return prefill_workspace_bytes(rows, njobs, cols, B, dev);
+}
+
+int pgq_prefill_q8(const pgq_q8_job* jobs, int njobs, const float* X, int cols, int B, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  REQUIRE(jobs && X, PGQ_EINVAL, "prefill_q8: jobs and X must be non-null");
+  REQUIRE(njobs >= 1 && njobs <= TC_MAXJOBS, PGQ_EINVAL, "prefill_q8: njobs=%d outside 1..%d", njobs, TC_MAXJOBS);
+  REQUIRE(B >= 1 && B <= PGQ_PASS_BMAX, PGQ_EINVAL, "prefill_q8: B=%d outside 1..%d", B, PGQ_PASS_BMAX);
+  REQUIRE(cols >= 128 && cols % 128 == 0, PGQ_EUNSUPPORTED, "prefill_q8: cols=%d must be a multiple of 128", cols);
+  REQUIRE(aligned16(X), PGQ_EALIGN, "prefill_q8: X must be 16-byte aligned");
+  REQUIRE(workspace && ((uintptr_t)workspace & 255) == 0, PGQ_EWORKSPACE,
+          "prefill_q8: workspace must be non-null and 256-byte aligned");
+  PrefillJob pj[TC_MAXJOBS];
+  int rows[TC_MAXJOBS];
+  for (int j = 0; j < njobs; ++j) {
+    const pgq_q8_job& J = jobs[j];
+    REQUIRE(J.codes && J.params && J.y, PGQ_EINVAL, "prefill_q8: job %d has a null codes/params/y", j);
+    REQUIRE(J.rows >= 1, PGQ_EINVAL, "prefill_q8: job %d rows=%d", j, J.rows);
+    REQUIRE(aligned16(J.codes) && aligned16(J.params), PGQ_EALIGN, "prefill_q8: job %d codes/params 16-byte", j);
+    REQUIRE(aligned4(J.y) && (!J.residual || aligned4(J.residual)), PGQ_EALIGN, "prefill_q8: job %d y/residual", j);
+    REQUIRE(J.epilogue >= PGQ_EPI_NONE && J.epilogue <= PGQ_EPI_ADD, PGQ_EINVAL, "prefill_q8: bad epilogue");
+    REQUIRE(J.epilogue != PGQ_EPI_ADD || J.residual, PGQ_EINVAL, "prefill_q8: PGQ_EPI_ADD needs a residual");
+    const size_t yb = (size_t)B * J.rows * 4;
+    REQUIRE(!overlaps(J.y, yb, X, (size_t)B * cols * 4), PGQ_EINVAL, "prefill_q8: job %d output overlaps X", j);
+    REQUIRE(!J.residual || J.residual == J.y || !overlaps(J.y, yb, J.residual, yb), PGQ_EINVAL,
+            "prefill_q8: residual must be y itself or not overlap it");
+    REQUIRE(!overlaps(J.y, yb, workspace, workspace_bytes), PGQ_EINVAL, "prefill_q8: output overlaps workspace");
+    pj[j] = PrefillJob{J.codes, J.params, J.rows, J.y, J.residual, J.epilogue};
+    rows[j] = J.rows;
+  }
+  GET_DEVICE(dev);
+  const size_t need = prefill_workspace_bytes(rows, njobs, cols, B, dev);
+  REQUIRE(workspace_bytes >= need, PGQ_EWORKSPACE, "prefill_q8: workspace needs %zu bytes", need);
+  return launch_prefill(pj, njobs, X, cols, B, workspace, workspace_bytes, use_a_tmem(), 0, dev, as_stream(stream));
+}
+
+int pgq_prefill_status(const void* workspace, void* stream) {
+  REQUIRE(workspace, PGQ_EINVAL, "prefill_status: null workspace");
+  GET_DEVICE(dev);
+  int v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, static_cast<const char*>(workspace) + prefill_status_offset(), sizeof(int),
+                                  cudaMemcpyDeviceToHost, as_stream(stream));
+  if (e == cudaSuccess) e = cudaStreamSynchronize(as_stream(stream));
+  if (e != cudaSuccess) return cuda_status(e);
+  return v;
 }
 
 }  // extern "C"

@@ -51,4 +51,21 @@ size_t gemv_argmax_workspace_bytes(int B, const DeviceInfo& dev);
 // Exact grid of a decode GEMV launch (used to size the argmax partials).
 int gemv_grid(int B, bool q8, bool argmax, const DeviceInfo& dev);
 
+// ------------------------------------------------------------------ prefill (tensor cores)
+constexpr int TC_MAXJOBS = 4;
+struct PrefillJob {
+  const int8_t* codes;
+  const uint16_t* params;
+  int rows;
+  float* y;
+  const float* residual;
+  int epilogue;
+};
+size_t prefill_workspace_bytes(const int* rows, int njobs, int cols, int B, const DeviceInfo& dev);
+int prefill_status_offset();
+// One launch of the binary16 conversion of X and one of the tensor-core GEMM.
+// `a_tmem` selects the A operand in tensor memory (else in shared memory).
+int launch_prefill(const PrefillJob* jobs, int njobs, const float* X, int cols, int B, void* ws, size_t ws_bytes,
+                   bool a_tmem, unsigned long long wait_limit_ns, const DeviceInfo& dev, cudaStream_t st);
+
 }  // namespace pgq

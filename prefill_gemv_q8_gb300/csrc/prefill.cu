@@ -1,0 +1,604 @@
+// Batched prefill projection Y[b][r] = Σ_c W[r][c]·X[b][c] for up to 64 positions,
+// q8 block-format weights read from HBM once per pass, on the 5th-generation tensor
+// cores (tcgen05.mma, binary16 operands, f32 accumulation in tensor memory).
+//
+// Prior art: nemotron_prefill.rs (a pass of at most PB_MAX = 64 positions, every
+// weight read once per pass) and gemma_batch.rs `q8_2f_mm_r2` (64×64 register tiles
+// on the shader cores, the scale factors folded in around the int8 products).
+// Here the contraction runs on the tensor cores:
+//
+// * X (f32) is first converted to binary16 with one power-of-two scale per position
+//   (exact; keeps any activation range inside binary16), and the scale is undone in
+//   the epilogue.
+// * A tile is 128 weight rows × all positions (N = B rounded up to 16).  The K
+//   dimension is walked in 128-column steps.  One warp issues TMA loads of the step's
+//   int8 codes (128×128 bytes, 128-byte swizzle), (scale, offset) pairs and the X
+//   slice (binary16, 128-byte swizzle, the MMA's B operand) into a ring of stages.
+// * Four dequantisation warps (one thread per weight row) turn codes into binary16
+//   w = scale·q + offset (exact byte→half conversion, one fused multiply-add,
+//   rounded once) and store the row into tensor memory, where it is the MMA's A
+//   operand: the dequantised weights never touch shared memory.
+// * One thread issues 8 tcgen05.mma (M=128, N, K=16) per step into one of two TMEM
+//   accumulators; tcgen05.commit releases the stage, the A buffer and, at the end of
+//   a tile, the accumulator.
+// * Four epilogue warps read the accumulator (one row per thread), undo the position
+//   scale, apply relu² / the residual add and store f32 rows, coalesced along rows.
+// * Work is split stream-K style: the (tile, k-step) items of the launch are cut into
+//   equal contiguous ranges, one per block (≤ one block per SM), so every SM streams
+//   the same number of weight bytes.  A tile cut between blocks leaves f32 partials
+//   in the workspace; the block that finishes a tile last (atomic ticket) sums the
+//   partials in block order (deterministic) and applies the epilogue.
+// * Every wait is bounded (%globaltimer); on expiry the block records PGQ_ETIMEOUT in
+//   the workspace status word, the other roles leave their loops, outstanding copies
+//   and MMAs are drained with bounded waits, and tensor memory is released.
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.cuh"
+#include "tc.cuh"
+
+namespace pgq {
+
+constexpr int TC_BM = 128;
+constexpr int TC_BK = 128;
+constexpr int TC_THREADS = 320;  // warp 0 TMA, warp 1 MMA+TMEM, warps 2-5 dequant, 6-9 epilogue
+constexpr int TC_STAGES = 5;
+constexpr int TC_CODES_BYTES = TC_BM * TC_BK;       // 16 KB
+constexpr int TC_PARAMS_BYTES = TC_BM * 16;         // 4 (scale, offset) pairs per row
+constexpr int TC_ACC_COLS = 64;                     // TMEM columns per accumulator (N <= 64)
+constexpr int TC_A_COLS = TC_BK / 2;                // TMEM columns per A buffer (2 halves per column)
+constexpr uint32_t TC_TMEM_COLS = 256;              // 2 accumulators + 2 A buffers
+
+struct TcParams {
+  CUtensorMap xmap;                       // X binary16 [Bp][cols], box {64, Bp}, 128B swizzle
+  CUtensorMap cmap[TC_MAXJOBS];           // codes int8 [rows][cols], box {128, 128}, 128B swizzle
+  CUtensorMap pmap[TC_MAXJOBS];           // params u32 [rows][cols/32], box {4, 128}
+  float* y[TC_MAXJOBS];
+  const float* residual[TC_MAXJOBS];
+  int rows[TC_MAXJOBS];
+  int tile_begin[TC_MAXJOBS + 1];
+  int epi[TC_MAXJOBS];
+  int njobs, ks, B, Bp, ntiles, maxseg;
+  long long total_items;
+  const float* xinv;                      // [Bp]
+  float* partials;                        // [grid][maxseg][Bp][128]
+  unsigned* tile_cnt;                     // [ntiles]
+  int* status;
+  unsigned long long wait_limit_ns;
+};
+
+// ------------------------------------------------------------------ schedule
+__device__ __forceinline__ long long item_begin(int c, int G, long long T) { return (long long)c * T / G; }
+
+__device__ __forceinline__ int cta_of_item(long long i, int G, long long T) {
+  int c = (int)((i * G) / T);
+  if (c >= G) c = G - 1;
+  while (c + 1 < G && item_begin(c + 1, G, T) <= i) ++c;
+  while (c > 0 && item_begin(c, G, T) > i) --c;
+  return c;
+}
+
+__device__ __forceinline__ int job_of_tile(const TcParams& P, int tile) {
+  int j = 0;
+#pragma unroll 1
+  while (j + 1 < P.njobs && tile >= P.tile_begin[j + 1]) ++j;
+  return j;
+}
+
+struct Waiter {
+  const TcParams& P;
+  volatile int* abort_flag;
+  __device__ bool wait(uint32_t bar, uint32_t parity) const {
+    if (tc::mbar_try(bar, parity)) return true;
+    const uint64_t t0 = tc::globaltimer();
+    while (true) {
+      if (tc::mbar_try(bar, parity)) return true;
+      if (*abort_flag) return false;
+      if (tc::globaltimer() - t0 > P.wait_limit_ns) {
+        *abort_flag = 1;
+        atomicCAS(P.status, 0, PGQ_ETIMEOUT);
+        return false;
+      }
+    }
+  }
+  // bounded wait that ignores the abort flag (drain of in-flight copies / MMAs)
+  __device__ bool drain(uint32_t bar, uint32_t parity) const {
+    const uint64_t t0 = tc::globaltimer();
+    while (!tc::mbar_try(bar, parity)) {
+      if (tc::globaltimer() - t0 > P.wait_limit_ns) {
+        atomicCAS(P.status, 0, PGQ_ETIMEOUT);
+        return false;
+      }
+    }
+    return true;
+  }
+};
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// AND of `ok` over the 128 epilogue threads (named barrier 1 with a reduction).
+__device__ __forceinline__ bool epi_all(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)ok)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ float apply_epi(float v, int epi, const float* residual, size_t idx) {
+  if (epi == PGQ_EPI_RELU2) {
+    v = fmaxf(v, 0.f);
+    return v * v;
+  }
+  if (epi == PGQ_EPI_ADD) return residual[idx] + v;
+  return v;
+}
+
+// Exact signed byte pair → binary16 pair: (0x64 << 8 | b + 128) is the half
+// 1024 + b + 128; subtracting 1152 leaves b.
+__device__ __forceinline__ __half2 s8pair_to_h2(uint32_t u_biased, uint32_t sel) {
+  const uint32_t h = __byte_perm(u_biased, 0x64646464u, sel);
+  return __hsub2(*reinterpret_cast<const __half2*>(&h), __half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
+}
+
+template <bool A_TMEM>
+__global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_constant__ TcParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int Bp = P.Bp;
+  const int x_bytes = 2 * Bp * 128;  // two 64-column halves of the X slice
+  const int stage_bytes = TC_CODES_BYTES + x_bytes + TC_PARAMS_BYTES;
+  uint8_t* stages = smem;
+  uint8_t* abuf = stages + TC_STAGES * stage_bytes;            // A in shared memory (A_TMEM == false)
+  uint8_t* tail = abuf + (A_TMEM ? 0 : 2 * TC_BM * TC_BK * 2);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tail);
+  // barrier slots
+  const int B_FULL = 0, B_EMPTY = TC_STAGES, B_AFULL = 2 * TC_STAGES, B_AEMPTY = B_AFULL + 2, B_ACCF = B_AEMPTY + 2,
+            B_ACCE = B_ACCF + 2, B_DRAIN = B_ACCE + 2, NBARS = B_DRAIN + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+
+  auto bar = [&](int i) { return tc::smem_addr(bars + i); };
+  auto stage_codes = [&](int s) { return stages + s * stage_bytes; };
+  auto stage_x = [&](int s) { return stages + s * stage_bytes + TC_CODES_BYTES; };
+  auto stage_params = [&](int s) { return stages + s * stage_bytes + TC_CODES_BYTES + x_bytes; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < TC_STAGES; ++s) {
+      tc::mbar_init(bar(B_FULL + s), 1);
+      tc::mbar_init(bar(B_EMPTY + s), 4 + 1);  // 4 dequant warps + the MMA commit
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(bar(B_AFULL + a), 4);
+      tc::mbar_init(bar(B_AEMPTY + a), 1);
+      tc::mbar_init(bar(B_ACCF + a), 1);
+      tc::mbar_init(bar(B_ACCE + a), 4);
+    }
+    tc::mbar_init(bar(B_DRAIN), 1);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 1) tc::tmem_alloc(tc::smem_addr(tmem_slot), TC_TMEM_COLS);
+  if (warp == 0 && lane == 0) {
+    tc::prefetch_tensormap(&P.xmap);
+    for (int j = 0; j < P.njobs; ++j) {
+      tc::prefetch_tensormap(&P.cmap[j]);
+      tc::prefetch_tensormap(&P.pmap[j]);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  const int G = gridDim.x;
+  const long long T = P.total_items;
+  const long long beg = item_begin(blockIdx.x, G, T), end = item_begin(blockIdx.x + 1, G, T);
+  const int ks = P.ks;
+  Waiter W{P, abort_flag};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t evict_first = tc::policy_evict_first();
+      const uint32_t tx = (uint32_t)stage_bytes;
+      int s = 0;
+      uint32_t ph = 0;
+      long long issued = 0;
+      for (long long it = beg; it < end; ++it) {
+        const int tile = (int)(it / ks), k = (int)(it % ks);
+        const int j = job_of_tile(P, tile);
+        const int row0 = (tile - P.tile_begin[j]) * TC_BM;
+        if (!W.wait(bar(B_EMPTY + s), ph ^ 1)) break;
+        tc::mbar_expect_tx(bar(B_FULL + s), tx);
+        tc::tma_load_2d_hint(tc::smem_addr(stage_codes(s)), &P.cmap[j], k * TC_BK, row0, bar(B_FULL + s),
+                             evict_first);
+        tc::tma_load_2d_hint(tc::smem_addr(stage_params(s)), &P.pmap[j], k * (TC_BK / 32), row0, bar(B_FULL + s),
+                             evict_first);
+        tc::tma_load_2d(tc::smem_addr(stage_x(s)), &P.xmap, k * TC_BK, 0, bar(B_FULL + s));
+        tc::tma_load_2d(tc::smem_addr(stage_x(s) + Bp * 128), &P.xmap, k * TC_BK + 64, 0, bar(B_FULL + s));
+        ++issued;
+        if (++s == TC_STAGES) { s = 0; ph ^= 1; }
+      }
+      if (*abort_flag) {
+        // let the copies already issued land before the block can exit
+        const int n = issued < TC_STAGES ? (int)issued : TC_STAGES;
+        int ss = s;
+        uint32_t pp = ph;
+        for (int i = 0; i < n; ++i) {
+          if (--ss < 0) { ss = TC_STAGES - 1; pp ^= 1; }
+          W.drain(bar(B_FULL + ss), pp);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = tc::idesc_f16_f32(TC_BM, Bp);
+      int s = 0, a = 0, t = 0;
+      uint32_t ph = 0, pha = 0, pht = 0;
+      bool any = false;
+      for (long long it = beg; it < end; ++it) {
+        const int k = (int)(it % ks);
+        const bool first = (k == 0) || (it == beg);
+        const bool last = (k == ks - 1) || (it == end - 1);
+        if (first && !W.wait(bar(B_ACCE + t), pht ^ 1)) break;
+        if (!W.wait(bar(B_AFULL + a), pha)) break;
+        if (!W.wait(bar(B_FULL + s), ph)) break;
+        tc::fence_after_sync();
+        const uint32_t d = tmem + t * TC_ACC_COLS;
+        const uint32_t xs = tc::smem_addr(stage_x(s));
+#pragma unroll
+        for (int kk = 0; kk < TC_BK / 16; ++kk) {
+          const uint64_t bdesc = tc::sdesc_sw128(xs + (kk >> 2) * Bp * 128 + (kk & 3) * 32);
+          const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+          if constexpr (A_TMEM) {
+            tc::mma_f16_ts(d, tmem + 2 * TC_ACC_COLS + a * TC_A_COLS + kk * 8, bdesc, idesc, acc);
+          } else {
+            const uint32_t as = tc::smem_addr(abuf + a * (TC_BM * TC_BK * 2));
+            tc::mma_f16_ss(d, tc::sdesc_sw128(as + (kk >> 2) * (TC_BM * 128) + (kk & 3) * 32), bdesc, idesc, acc);
+          }
+        }
+        any = true;
+        tc::mma_commit(bar(B_EMPTY + s));
+        tc::mma_commit(bar(B_AEMPTY + a));
+        if (last) {
+          tc::mma_commit(bar(B_ACCF + t));
+          if (++t == 2) { t = 0; pht ^= 1; }
+        }
+        if (++s == TC_STAGES) { s = 0; ph ^= 1; }
+        if (++a == 2) { a = 0; pha ^= 1; }
+      }
+      if (any) {
+        // every MMA issued by this thread has completed before TMEM is released
+        tc::mma_commit(bar(B_DRAIN));
+        W.drain(bar(B_DRAIN), 0);
+      }
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ dequantisation
+    const int q = warp & 3;            // TMEM lane quarter of this warp
+    const int r = q * 32 + lane;       // weight row within the tile
+    int s = 0, a = 0;
+    uint32_t ph = 0, pha = 0;
+    for (long long it = beg; it < end; ++it) {
+      if (!W.wait(bar(B_FULL + s), ph)) break;
+      if (!W.wait(bar(B_AEMPTY + a), pha ^ 1)) break;
+      const uint8_t* crow = stage_codes(s) + r * 128;
+      uint4 cw[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) cw[c] = *reinterpret_cast<const uint4*>(crow + ((c ^ (r & 7)) << 4));
+      const uint4 pr = *reinterpret_cast<const uint4*>(stage_params(s) + r * 16);
+      const uint32_t prw[4] = {pr.x, pr.y, pr.z, pr.w};
+      uint32_t out[64];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const __half2 so = *reinterpret_cast<const __half2*>(&prw[c >> 1]);
+        const __half2 s2 = __low2half2(so), o2 = __high2half2(so);
+        const uint32_t wv[4] = {cw[c].x, cw[c].y, cw[c].z, cw[c].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t u = wv[i] ^ 0x80808080u;
+          const __half2 lo = __hfma2(s8pair_to_h2(u, 0x4140), s2, o2);
+          const __half2 hi = __hfma2(s8pair_to_h2(u, 0x4342), s2, o2);
+          out[c * 8 + 2 * i] = *reinterpret_cast<const uint32_t*>(&lo);
+          out[c * 8 + 2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+        }
+      }
+      if constexpr (A_TMEM) {
+        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + 2 * TC_ACC_COLS + a * TC_A_COLS;
+        uint32_t (&o0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&out[0]);
+        uint32_t (&o1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&out[32]);
+        tc::tmem_st_32x32b_x32(ta, o0);
+        tc::tmem_st_32x32b_x32(ta + 32, o1);
+        tc::tmem_wait_st();
+        tc::fence_before_sync();
+      } else {
+        uint8_t* ab = abuf + a * (TC_BM * TC_BK * 2);
+#pragma unroll
+        for (int g = 0; g < 16; ++g) {
+          uint8_t* dst = ab + (g >> 3) * (TC_BM * 128) + (r >> 3) * 1024 + (r & 7) * 128 + (((g & 7) ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(dst) = make_uint4(out[4 * g], out[4 * g + 1], out[4 * g + 2], out[4 * g + 3]);
+        }
+        tc::fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive(bar(B_AFULL + a));
+        tc::mbar_arrive(bar(B_EMPTY + s));
+      }
+      if (++s == TC_STAGES) { s = 0; ph ^= 1; }
+      if (++a == 2) { a = 0; pha ^= 1; }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const int et = threadIdx.x - 6 * 32;  // 0..127
+    int t = 0;
+    uint32_t pht = 0;
+    long long it = beg;
+    while (it < end) {
+      const int tile = (int)(it / ks);
+      const long long tile_end = (long long)(tile + 1) * ks;
+      const long long seg_end = end < tile_end ? end : tile_end;
+      const bool whole = (it == (long long)tile * ks) && (seg_end == tile_end);
+      const int j = job_of_tile(P, tile);
+      const int rows = P.rows[j];
+      const int row = (tile - P.tile_begin[j]) * TC_BM + r;
+      const bool ok = W.wait(bar(B_ACCF + t), pht);
+      // leave together: a warp missing from the named barriers below would hang the rest
+      if (!epi_all(ok)) break;
+      tc::fence_after_sync();
+      float v[TC_ACC_COLS];
+      const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + t * TC_ACC_COLS;
+#pragma unroll
+      for (int c0 = 0; c0 < TC_ACC_COLS; c0 += 16) {
+        if (c0 < Bp) {
+          uint32_t u[16];
+          tc::tmem_ld_32x32b_x16(ta + c0, u);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[c0 + i] = __uint_as_float(u[i]);
+        }
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(bar(B_ACCE + t));
+      if (++t == 2) { t = 0; pht ^= 1; }
+
+      const int epi = P.epi[j];
+      float* y = P.y[j];
+      const float* res = P.residual[j];
+      if (whole) {
+        if (row < rows) {
+#pragma unroll
+          for (int b = 0; b < TC_ACC_COLS; ++b) {
+            if (b < P.B) {
+              const size_t idx = (size_t)b * rows + row;
+              y[idx] = apply_epi(v[b] * P.xinv[b], epi, res, idx);
+            }
+          }
+        }
+      } else {
+        // f32 partial of this block for the tile, then the last block to finish sums
+        const int first_tile = (int)(beg / ks);
+        float* part = P.partials + ((size_t)blockIdx.x * P.maxseg + (tile - first_tile)) * Bp * TC_BM;
+#pragma unroll
+        for (int b = 0; b < TC_ACC_COLS; ++b)
+          if (b < P.B) part[(size_t)b * TC_BM + r] = v[b] * P.xinv[b];
+        __threadfence();
+        epi_bar();
+        if (et == 0) {
+          const int c_first = cta_of_item((long long)tile * ks, G, T);
+          const int c_last = cta_of_item(tile_end - 1, G, T);
+          const unsigned n = (unsigned)(c_last - c_first + 1);
+          *last_flag = (atomicAdd(P.tile_cnt + tile, 1u) == n - 1) ? 1 : 0;
+        }
+        epi_bar();
+        if (*last_flag) {
+          __threadfence();
+          const int c_first = cta_of_item((long long)tile * ks, G, T);
+          const int c_last = cta_of_item(tile_end - 1, G, T);
+          if (row < rows) {
+            for (int b = 0; b < P.B; ++b) {
+              float acc = 0.f;
+              for (int c = c_first; c <= c_last; ++c) {
+                const int ft = (int)(item_begin(c, G, T) / ks);
+                const float* pc = P.partials + ((size_t)c * P.maxseg + (tile - ft)) * Bp * TC_BM;
+                acc += __ldcg(pc + (size_t)b * TC_BM + r);
+              }
+              const size_t idx = (size_t)b * rows + row;
+              y[idx] = apply_epi(acc, epi, res, idx);
+            }
+          }
+          if (et == 0) P.tile_cnt[tile] = 0u;
+        }
+        epi_bar();
+      }
+      it = seg_end;
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, TC_TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ X → binary16
+// One block per position b < Bp: amax, a power-of-two scale 2^(14 - e) with
+// amax < 2^e, x·scale rounded to binary16; xinv[b] = 2^(e - 14).  Rows b >= B are 0.
+__global__ void __launch_bounds__(256) xprep_kernel(const float* __restrict__ X, int B, int cols,
+                                                    __half* __restrict__ Xh, float* __restrict__ xinv) {
+  __shared__ float red[8];
+  const int b = blockIdx.x;
+  __half* out = Xh + (size_t)b * cols;
+  if (b >= B) {
+    for (int c = threadIdx.x; c < cols; c += 256) out[c] = __ushort_as_half(0);
+    if (threadIdx.x == 0) xinv[b] = 0.f;
+    return;
+  }
+  const float* x = X + (size_t)b * cols;
+  float m = 0.f;
+  for (int c = threadIdx.x; c < cols; c += 256) m = fmaxf(m, fabsf(x[c]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m = fmaxf(m, red[i]);
+  int e = 0;
+  if (m > 0.f && m <= 3.0e38f) frexpf(m, &e);   // m = f·2^e, f in [0.5, 1)
+  const int k = max(-120, min(120, 14 - e));
+  const float sc = ldexpf(1.f, k);
+  for (int c = threadIdx.x; c < cols; c += 256) out[c] = __float2half_rn(x[c] * sc);
+  if (threadIdx.x == 0) xinv[b] = ldexpf(1.f, -k);
+}
+
+// ------------------------------------------------------------------ host side
+namespace {
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encoder() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+    cudaGetLastError();
+  });
+  return fn;
+}
+
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  EncodeFn fn = encoder();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool A_TMEM>
+size_t tc_smem_bytes(int Bp) {
+  const size_t stage = TC_CODES_BYTES + 2 * (size_t)Bp * 128 + TC_PARAMS_BYTES;
+  return 1024 /*alignment slack*/ + TC_STAGES * stage + (A_TMEM ? 0 : 2 * TC_BM * TC_BK * 2) + 256;
+}
+
+struct Plan {
+  int Bp, ks, ntiles, G, maxseg;
+  long long T;
+  size_t off_xh, off_xinv, off_status, off_cnt, off_part, total;
+};
+
+Plan make_plan(const int* rows, int njobs, int cols, int B, int sms) {
+  Plan p{};
+  p.Bp = (B + 15) / 16 * 16;
+  p.ks = (cols + TC_BK - 1) / TC_BK;
+  p.ntiles = 0;
+  for (int j = 0; j < njobs; ++j) p.ntiles += (rows[j] + TC_BM - 1) / TC_BM;
+  p.T = (long long)p.ntiles * p.ks;
+  p.G = (int)std::max<long long>(1, std::min<long long>(sms, p.T));
+  long long per = (p.T + p.G - 1) / p.G;
+  p.maxseg = (int)std::min<long long>(p.ntiles, (per + p.ks - 1) / p.ks + 1);
+  auto up = [](size_t v, size_t a) { return (v + a - 1) / a * a; };
+  size_t o = 0;
+  p.off_status = o; o += 256;
+  p.off_xh = o; o = up(o + (size_t)p.Bp * cols * 2, 1024);
+  p.off_xinv = o; o = up(o + (size_t)p.Bp * 4, 256);
+  p.off_cnt = o; o = up(o + (size_t)p.ntiles * 4, 256);
+  p.off_part = o; o = up(o + (size_t)p.G * p.maxseg * p.Bp * TC_BM * 4, 256);
+  p.total = o;
+  return p;
+}
+
+}  // namespace
+
+size_t prefill_workspace_bytes(const int* rows, int njobs, int cols, int B, const DeviceInfo& dev) {
+  return make_plan(rows, njobs, cols, B, dev.sms).total;
+}
+
+int prefill_status_offset() { return 0; }
+
+int launch_prefill(const PrefillJob* jobs, int njobs, const float* X, int cols, int B, void* ws, size_t ws_bytes,
+                   bool a_tmem, unsigned long long wait_limit_ns, const DeviceInfo& dev, cudaStream_t st) {
+  int rows[TC_MAXJOBS];
+  for (int j = 0; j < njobs; ++j) rows[j] = jobs[j].rows;
+  const Plan pl = make_plan(rows, njobs, cols, B, dev.sms);
+  if (ws_bytes < pl.total) return set_error(PGQ_EWORKSPACE, "prefill: workspace needs %zu bytes", pl.total);
+  char* w = static_cast<char*>(ws);
+  __half* Xh = reinterpret_cast<__half*>(w + pl.off_xh);
+  float* xinv = reinterpret_cast<float*>(w + pl.off_xinv);
+  static TcParams P;  // large (tensor maps); filled under the lock below
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  memset(&P, 0, sizeof(P));
+  if (!encode_2d(&P.xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Xh, cols, pl.Bp, (uint64_t)cols * 2, 64, pl.Bp,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return set_error(PGQ_ECUDA, "prefill: tensor map of X could not be encoded");
+  int tb = 0;
+  for (int j = 0; j < njobs; ++j) {
+    const PrefillJob& J = jobs[j];
+    if (!encode_2d(&P.cmap[j], CU_TENSOR_MAP_DATA_TYPE_UINT8, J.codes, cols, J.rows, (uint64_t)cols, TC_BK, TC_BM,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&P.pmap[j], CU_TENSOR_MAP_DATA_TYPE_UINT32, J.params, cols / 32, J.rows, (uint64_t)(cols / 32) * 4,
+                   TC_BK / 32, TC_BM, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return set_error(PGQ_ECUDA, "prefill: tensor map of job %d could not be encoded", j);
+    P.y[j] = J.y;
+    P.residual[j] = J.residual;
+    P.rows[j] = J.rows;
+    P.epi[j] = J.epilogue;
+    P.tile_begin[j] = tb;
+    tb += (J.rows + TC_BM - 1) / TC_BM;
+  }
+  P.tile_begin[njobs] = tb;
+  P.njobs = njobs;
+  P.ks = pl.ks;
+  P.B = B;
+  P.Bp = pl.Bp;
+  P.ntiles = pl.ntiles;
+  P.maxseg = pl.maxseg;
+  P.total_items = pl.T;
+  P.xinv = xinv;
+  P.partials = reinterpret_cast<float*>(w + pl.off_part);
+  P.tile_cnt = reinterpret_cast<unsigned*>(w + pl.off_cnt);
+  P.status = reinterpret_cast<int*>(w + pl.off_status);
+  P.wait_limit_ns = wait_limit_ns ? wait_limit_ns : 2000000000ull;
+
+  cudaError_t e = cudaMemsetAsync(w + pl.off_status, 0, 256, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(P.tile_cnt, 0, (size_t)pl.ntiles * 4, st);
+  if (e != cudaSuccess) return cuda_status(e);
+  xprep_kernel<<<pl.Bp, 256, 0, st>>>(X, B, cols, Xh, xinv);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e);
+
+  const void* fn = a_tmem ? reinterpret_cast<const void*>(&prefill_tc_kernel<true>)
+                          : reinterpret_cast<const void*>(&prefill_tc_kernel<false>);
+  const size_t smem = a_tmem ? tc_smem_bytes<true>(pl.Bp) : tc_smem_bytes<false>(pl.Bp);
+  if (smem > dev.smem_optin) return set_error(PGQ_EUNSUPPORTED, "prefill: %zu bytes of shared memory", smem);
+  if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+    return cuda_status(e);
+  void* args[] = {&P};
+  return cuda_status(cudaLaunchKernel(fn, dim3(pl.G), dim3(TC_THREADS), args, smem, st));
+}
+
+}  // namespace pgq
