@@ -206,6 +206,26 @@ int pgq_prefill_q8(const pgq_q8_job* jobs, int njobs, const float* X, int cols, 
  * PGQ_ETIMEOUT when a bounded device-side wait expired).  Synchronises the stream. */
 int pgq_prefill_status(const void* workspace, void* stream);
 
+/* ---------------------------------------------------------------- prefill pass
+ * The batched prefill pass over B <= 64 positions and L q8 layers (every weight of
+ * every layer read once per pass).  Per layer l (attention itself is outside this
+ * library: its output is stood in for by q):
+ *   n1 = rms(h)·gamma1[l];  q, k, v = W_q·n1, W_k·n1, W_v·n1
+ *   h  = h + W_o·q;         n2 = rms(h)·gamma2[l]
+ *   u  = relu²(W_up·n2);    h  = h + W_down·u
+ * h: device f32 [B][hidden], updated in place; gamma1, gamma2: device f32
+ * [L][hidden]; layers: host array of L layer descriptors (device weights).
+ * workspace: pgq_q8_prefill_pass_workspace_bytes(hidden, kv, inter, B) bytes,
+ * 256-byte aligned.  After the call the workspace holds the last layer's n1, q, k,
+ * v, h1 (= h + W_o·q), n2 and u at the byte offsets pgq_q8_prefill_pass_layout()
+ * reports (7 entries).
+ * Six kernel launches per layer plus the binary16 input conversions. */
+size_t pgq_q8_prefill_pass_workspace_bytes(int hidden, int kv, int inter, int B);
+int pgq_q8_prefill_pass_layout(int hidden, int kv, int inter, int B, size_t offsets[7]);
+int pgq_q8_prefill_pass(const pgq_q8_layer* layers, int L, float* h, int B, const float* gamma1,
+                        const float* gamma2, float eps, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
 #ifdef __cplusplus
 }
 #endif

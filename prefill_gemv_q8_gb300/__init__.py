@@ -67,6 +67,10 @@ _SIGS = {
     "pgq_prefill_q8_workspace_bytes": (C.c_size_t, [C.POINTER(C.c_int), C.c_int, C.c_int, C.c_int]),
     "pgq_prefill_q8": (C.c_int, [C.POINTER(Q8Job), C.c_int, _vp, C.c_int, C.c_int, _vp, C.c_size_t, _vp]),
     "pgq_prefill_status": (C.c_int, [_vp, _vp]),
+    "pgq_q8_prefill_pass_workspace_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int, C.c_int]),
+    "pgq_q8_prefill_pass_layout": (C.c_int, [C.c_int, C.c_int, C.c_int, C.c_int, C.POINTER(C.c_size_t)]),
+    "pgq_q8_prefill_pass": (C.c_int, [C.POINTER(Q8Layer), C.c_int, _vp, C.c_int, _vp, _vp, C.c_float, _vp,
+                                      C.c_size_t, _vp]),
 }
 
 _lib = None
@@ -331,3 +335,45 @@ def q8_decode_layer(mats, x, x_o, gamma, eps=1e-6, out=None, stream=None):
                                      _ptr(out["k"]), _ptr(out["v"]), _ptr(out["o"]), _ptr(out["u"]),
                                      _ptr(out["down"]), _stream(stream)))
     return out
+
+
+def prefill_pass_workspace(hidden, kv, inter, B, device="cuda"):
+    n = int(lib().pgq_q8_prefill_pass_workspace_bytes(hidden, kv, inter, B))
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def prefill_pass_taps(workspace, hidden, kv, inter, B):
+    """Views of the last layer's n1, q, k, v, h1, n2, u inside a pass workspace."""
+    off = (C.c_size_t * 7)()
+    _check(lib().pgq_q8_prefill_pass_layout(hidden, kv, inter, B, off))
+    sizes = (hidden, hidden, kv, kv, hidden, hidden, inter)
+    names = ("n1", "q", "k", "v", "h1", "n2", "u")
+    f = workspace.view(torch.uint8)
+    return {nm: f[o:o + B * n * 4].view(torch.float32).view(B, n) for nm, o, n in zip(names, off, sizes)}
+
+
+class PassLayers:
+    """ctypes array of L layer descriptors (keeps the tensors alive)."""
+
+    def __init__(self, layers):
+        self.layers = layers
+        self.arr = (Q8Layer * len(layers))(*[q8_layer_struct(m) for m in layers])
+        self.hidden, self.kv, self.inter = self.arr[0].hidden, self.arr[0].kv, self.arr[0].inter
+
+
+def prefill_pass(layers, h, gamma1, gamma2, eps=1e-6, workspace=None, stream=None):
+    """The batched prefill pass: h [B][hidden] updated in place through every layer.
+    ``layers`` is a PassLayers (or a list of {slot: (codes, params)}); gamma1/gamma2
+    [L][hidden].  Returns the workspace (it holds the last layer's intermediates)."""
+    if not isinstance(layers, PassLayers):
+        layers = PassLayers(layers)
+    _need(h, torch.float32, "h")
+    B, H = h.shape
+    L = len(layers.layers)
+    _need(gamma1, torch.float32, "gamma1", (L, H))
+    _need(gamma2, torch.float32, "gamma2", (L, H))
+    if workspace is None:
+        workspace = prefill_pass_workspace(layers.hidden, layers.kv, layers.inter, B, h.device)
+    _check(lib().pgq_q8_prefill_pass(layers.arr, L, _ptr(h), B, _ptr(gamma1), _ptr(gamma2), eps,
+                                     _ptr(workspace), workspace.numel(), _stream(stream)))
+    return workspace

@@ -3,6 +3,7 @@
 #include <cstdarg>
 #include <cstdlib>
 #include <cstdio>
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -327,6 +328,98 @@ int pgq_prefill_q8(const pgq_q8_job* jobs, int njobs, const float* X, int cols, 
   const size_t need = prefill_workspace_bytes(rows, njobs, cols, B, dev);
   REQUIRE(workspace_bytes >= need, PGQ_EWORKSPACE, "prefill_q8: workspace needs %zu bytes", need);
   return launch_prefill(pj, njobs, X, cols, B, workspace, workspace_bytes, use_a_tmem(), 0, dev, as_stream(stream));
+}
+
+// ------------------------------------------------------------------ prefill pass
+namespace {
+struct PassLayout {
+  size_t off[7];   // n1, q, k, v, h1, n2, u
+  size_t gemm;     // prefill workspace
+  size_t total;
+};
+PassLayout pass_layout(int H, int KV, int I, int B, const DeviceInfo& dev) {
+  PassLayout L{};
+  auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+  size_t o = 0;
+  const size_t sz[7] = {(size_t)B * H, (size_t)B * H, (size_t)B * KV, (size_t)B * KV,
+                        (size_t)B * H, (size_t)B * H, (size_t)B * I};
+  for (int i = 0; i < 7; ++i) {
+    L.off[i] = o;
+    o = up(o + sz[i] * 4);
+  }
+  L.gemm = o;
+  const int qkv[3] = {H, KV, KV};
+  const int one_h[1] = {H};
+  const int one_i[1] = {I};
+  size_t g = prefill_workspace_bytes(qkv, 3, H, B, dev);
+  g = std::max(g, prefill_workspace_bytes(one_h, 1, H, B, dev));
+  g = std::max(g, prefill_workspace_bytes(one_i, 1, H, B, dev));
+  g = std::max(g, prefill_workspace_bytes(one_h, 1, I, B, dev));
+  L.total = o + up(g);
+  return L;
+}
+}  // namespace
+
+size_t pgq_q8_prefill_pass_workspace_bytes(int hidden, int kv, int inter, int B) {
+  if (hidden < 128 || kv < 1 || inter < 128 || B < 1 || B > PGQ_PASS_BMAX) return 0;
+  DeviceInfo dev;
+  if (!device_info(&dev)) dev.sms = 160;
+  return pass_layout(hidden, kv, inter, B, dev).total;
+}
+
+int pgq_q8_prefill_pass_layout(int hidden, int kv, int inter, int B, size_t offsets[7]) {
+  REQUIRE(offsets && hidden >= 128 && kv >= 1 && inter >= 128 && B >= 1 && B <= PGQ_PASS_BMAX, PGQ_EINVAL,
+          "prefill_pass_layout: bad arguments");
+  DeviceInfo dev;
+  if (!device_info(&dev)) dev.sms = 160;
+  const PassLayout L = pass_layout(hidden, kv, inter, B, dev);
+  for (int i = 0; i < 7; ++i) offsets[i] = L.off[i];
+  return PGQ_OK;
+}
+
+int pgq_q8_prefill_pass(const pgq_q8_layer* layers, int L, float* h, int B, const float* gamma1,
+                        const float* gamma2, float eps, void* workspace, size_t workspace_bytes, void* stream) {
+  REQUIRE(layers && h && gamma1 && gamma2 && workspace, PGQ_EINVAL, "prefill_pass: null pointer");
+  REQUIRE(L >= 1, PGQ_EINVAL, "prefill_pass: L=%d", L);
+  const int H = layers[0].hidden, KV = layers[0].kv, I = layers[0].inter;
+  for (int l = 0; l < L; ++l)
+    REQUIRE(layers[l].hidden == H && layers[l].kv == KV && layers[l].inter == I, PGQ_EINVAL,
+            "prefill_pass: layer %d has a different shape", l);
+  REQUIRE(H % 128 == 0 && I % 128 == 0, PGQ_EUNSUPPORTED, "prefill_pass: hidden and inter must be multiples of 128");
+  REQUIRE(((uintptr_t)workspace & 255) == 0, PGQ_EWORKSPACE, "prefill_pass: workspace must be 256-byte aligned");
+  GET_DEVICE(dev);
+  const PassLayout PL = pass_layout(H, KV, I, B, dev);
+  REQUIRE(workspace_bytes >= PL.total, PGQ_EWORKSPACE, "prefill_pass: workspace needs %zu bytes", PL.total);
+  REQUIRE(!overlaps(h, (size_t)B * H * 4, workspace, workspace_bytes), PGQ_EINVAL, "prefill_pass: h overlaps workspace");
+  char* w = static_cast<char*>(workspace);
+  float* n1 = reinterpret_cast<float*>(w + PL.off[0]);
+  float* q = reinterpret_cast<float*>(w + PL.off[1]);
+  float* k = reinterpret_cast<float*>(w + PL.off[2]);
+  float* v = reinterpret_cast<float*>(w + PL.off[3]);
+  float* h1 = reinterpret_cast<float*>(w + PL.off[4]);
+  float* n2 = reinterpret_cast<float*>(w + PL.off[5]);
+  float* u = reinterpret_cast<float*>(w + PL.off[6]);
+  void* gws = w + PL.gemm;
+  const size_t gws_bytes = workspace_bytes - PL.gemm;
+  cudaStream_t st = as_stream(stream);
+  const bool at = use_a_tmem();
+  int rc;
+  for (int l = 0; l < L; ++l) {
+    const pgq_q8_layer& Y = layers[l];
+    if ((rc = launch_add_rmsnorm(h, nullptr, gamma1 + (size_t)l * H, eps, B, H, n1, nullptr, st))) return rc;
+    PrefillJob qkv[3] = {{Y.q.codes, Y.q.params, H, q, nullptr, PGQ_EPI_NONE},
+                         {Y.k.codes, Y.k.params, KV, k, nullptr, PGQ_EPI_NONE},
+                         {Y.v.codes, Y.v.params, KV, v, nullptr, PGQ_EPI_NONE}};
+    if ((rc = launch_prefill(qkv, 3, n1, H, B, gws, gws_bytes, at, 0, dev, st))) return rc;
+    PrefillJob o = {Y.o.codes, Y.o.params, H, h1, h, PGQ_EPI_ADD};
+    if ((rc = launch_prefill(&o, 1, q, H, B, gws, gws_bytes, at, 0, dev, st))) return rc;
+    if ((rc = launch_add_rmsnorm(h1, nullptr, gamma2 + (size_t)l * H, eps, B, H, n2, nullptr, st))) return rc;
+    PrefillJob upj = {Y.up.codes, Y.up.params, I, u, nullptr, PGQ_EPI_RELU2};
+    if ((rc = launch_prefill(&upj, 1, n2, H, B, gws, gws_bytes, at, 0, dev, st))) return rc;
+    PrefillJob dn = {Y.down.codes, Y.down.params, H, h, h1, PGQ_EPI_ADD};
+    if ((rc = launch_prefill(&dn, 1, u, I, B, gws, gws_bytes, at, 0, dev, st))) return rc;
+  }
+  return PGQ_OK;
 }
 
 int pgq_prefill_status(const void* workspace, void* stream) {

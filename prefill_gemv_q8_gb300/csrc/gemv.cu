@@ -33,23 +33,26 @@ namespace pgq {
 
 constexpr int GV_WARPS = 8;
 constexpr int GV_THREADS = GV_WARPS * 32;
-constexpr int GV_CHUNK = 256;
-constexpr int GV_R = 4;
 
-template <bool Q8>
-struct Raw;
-template <>
-struct Raw<true> {
-  uint2 c[GV_R];
-  uint32_t p[GV_R];
-  int job, row0, chunk;
-  bool ok;
+// Compile-time shape of one kernel instance.
+//   EPL: weight elements a lane loads per row per chunk (one 16- or 8-byte load),
+//   CW:  columns per chunk (32 lanes x EPL),
+//   R:   rows per task (they share every staged-x read),
+//   U:   chunks per batch (loads a lane issues per row before using any of them).
+template <bool Q8, int NB>
+struct GvShape {
+  static constexpr int R = NB <= 2 ? 2 : 4;
+  static constexpr int U = NB <= 2 ? 4 : 2;
+  static constexpr int EPL = (Q8 && NB <= 2) ? 16 : 8;
+  static constexpr int CW = 32 * EPL;
 };
-template <>
-struct Raw<false> {
-  uint4 w[GV_R];
-  int job, row0, chunk;
-  bool ok;
+
+template <bool Q8, int NB>
+struct Slot {
+  static constexpr int R = GvShape<Q8, NB>::R, U = GvShape<Q8, NB>::U;
+  uint4 w[R][U];
+  uint32_t p[R][U];
+  int job, ch0, nch;   // job, first chunk of the batch, chunks of the batch this warp owns
 };
 
 __device__ __forceinline__ void group_sync(int group, int wpt) {
@@ -80,18 +83,25 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[N], int lane) {
   return t;
 }
 
-// Position of column c in the staged (permuted) input row.
+// Position of column c in the staged (permuted) input row: the EPL values a lane
+// reads in a chunk sit as EPL/4 float4 that consecutive lanes read side by side.
+template <int EPL>
 __device__ __forceinline__ int perm_col(int c) {
-  const int chunk = c >> 8, within = c & 255;
-  return (chunk << 8) + (((within >> 2) & 1) << 7) + ((within >> 3) << 2) + (within & 3);
+  constexpr int CW = 32 * EPL;
+  const int ch = c / CW, within = c - ch * CW;
+  const int ln = within / EPL, t = within - ln * EPL;
+  return ch * CW + (t >> 2) * 128 + ln * 4 + (t & 3);
 }
 
-template <bool Q8, int NB, int D, bool ARGMAX>
-__global__ void __launch_bounds__(GV_THREADS, 1)
+template <bool Q8, int NB, bool ARGMAX>
+__global__ void __launch_bounds__(GV_THREADS, NB <= 2 ? 2 : 1)
 gemv_kernel(const __grid_constant__ GvParams P) {
+  using S = GvShape<Q8, NB>;
+  constexpr int R = S::R, U = S::U, EPL = S::EPL, CW = S::CW;
+  constexpr int ESZ = Q8 ? 1 : 2;
   extern __shared__ __align__(16) float smem[];
   float* xs = smem;                                           // [ninputs][NB][cols_pad]
-  float* red = xs + (size_t)P.ninputs * NB * P.cols_pad;      // [groups][2][wpt][GV_R*NB]
+  float* red = xs + (size_t)P.ninputs * NB * P.cols_pad;      // [groups][2][wpt][R*NB]
   __shared__ float s_inv[MAX_INPUTS * NB];
   __shared__ float s_red[GV_WARPS];
   __shared__ float s_gbv[GV_WARPS * NB];
@@ -134,50 +144,71 @@ gemv_kernel(const __grid_constant__ GvParams P) {
           v = make_float4(g.x * (v.x * inv), g.y * (v.y * inv), g.z * (v.z * inv), g.w * (v.w * inv));
         }
       }
-      *reinterpret_cast<float4*>(xs + (size_t)(i * NB + b) * cols_pad + perm_col(c4 * 4)) = v;
+      *reinterpret_cast<float4*>(xs + (size_t)(i * NB + b) * cols_pad + perm_col<EPL>(c4 * 4)) = v;
     }
   }
   __syncthreads();
 
-  // ---- task loop of this warp's group
+  // ---- this warp's share: tasks gg, gg+TG, ...; within a task the chunks
+  //      [wg*cpw, (wg+1)*cpw) in batches of U
   const int wpt = P.wpt, groups = P.groups, cpw = P.cpw;
   const int group = warp / wpt, wg = warp - group * wpt;
+  const bool active_warp = group < groups;
   const int gg = blockIdx.x * groups + group;
   const int TG = gridDim.x * groups;
-  const int my_tasks = gg < P.ntasks ? (P.ntasks - 1 - gg) / TG + 1 : 0;
-  const int nsteps = my_tasks * cpw;
-  float* gred = red + (size_t)group * 2 * wpt * (GV_R * NB);
+  const int my_tasks = (active_warp && gg < P.ntasks) ? (P.ntasks - 1 - gg) / TG + 1 : 0;
+  const int nbt = (cpw + U - 1) / U;               // batches per task
+  const int nsteps = my_tasks * nbt;
+  const int ch_begin = wg * cpw;
+  const int ch_end = min(ch_begin + cpw, P.nchunks);
+  float* gred = red + (size_t)(active_warp ? group : 0) * 2 * wpt * (R * NB);
+  const size_t row_bytes = (size_t)cols * ESZ;
+  const int pcols = cols >> 5;
 
-  auto fetch = [&](Raw<Q8>& raw, int s) {
-    raw.ok = false;
+  // incremental step -> (task, batch) walkers for the fetch and compute sides
+  int f_i = 0, f_tb = 0, f_job = 0;
+  int c_i = 0, c_tb = 0, c_job = 0;
+
+  auto fetch = [&](Slot<Q8, NB>& sl, int s) {
+    sl.nch = 0;
     if (s >= nsteps) return;
-    const int i = s / cpw, cc = s - i * cpw;
-    const int task = gg + i * TG;
-    int j = 0;
+    const int task = gg + f_i * TG;
 #pragma unroll 1
-    while (j + 1 < P.njobs && task >= P.job[j + 1].task_begin) ++j;
-    raw.job = j;
-    raw.row0 = (task - P.job[j].task_begin) * GV_R;
-    raw.chunk = wg + cc * wpt;
-    const int col = raw.chunk * GV_CHUNK + lane * 8;
-    if (raw.chunk >= P.nchunks || col >= cols) return;
-    raw.ok = true;
-    const int rows = P.job[j].rows;
+    while (f_job + 1 < P.njobs && task >= P.job[f_job + 1].task_begin) ++f_job;
+    const GvJob& J = P.job[f_job];
+    sl.job = f_job;
+    sl.ch0 = ch_begin + f_tb * U;
+    sl.nch = max(0, min(U, ch_end - sl.ch0));
+    const int row0 = (task - J.task_begin) * R;
+    const int col0 = sl.ch0 * CW + lane * EPL;
 #pragma unroll
-    for (int r = 0; r < GV_R; ++r) {
-      const size_t row = (size_t)min(raw.row0 + r, rows - 1);
-      if constexpr (Q8) {
-        raw.c[r] = ld_stream_u2(P.job[j].w + row * cols + col);
-        raw.p[r] = ld_nc_u32(P.job[j].params + row * (cols >> 5) + (col >> 5));
-      } else {
-        raw.w[r] = ld_stream_u4(P.job[j].w + (row * cols + col) * 2);
+    for (int r = 0; r < R; ++r) {
+      const size_t row = (size_t)min(row0 + r, J.rows - 1);
+      const uint8_t* wp = J.w + row * row_bytes + (size_t)col0 * ESZ;
+      const uint32_t* pp = Q8 ? J.params + row * pcols + (col0 >> 5) : nullptr;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (u < sl.nch && col0 + u * CW < cols) {
+          if constexpr (Q8) {
+            if constexpr (EPL == 16) {
+              sl.w[r][u] = ld_stream_u4(wp + u * CW);
+            } else {
+              const uint2 v = ld_stream_u2(wp + u * CW);
+              sl.w[r][u] = make_uint4(v.x, v.y, 0u, 0u);
+            }
+            sl.p[r][u] = ld_nc_u32(pp + u * (CW >> 5));
+          } else {
+            sl.w[r][u] = ld_stream_u4(wp + u * CW * 2);
+          }
+        }
       }
     }
+    if (++f_tb == nbt) { f_tb = 0; ++f_i; }
   };
 
-  float2 acc[GV_R][NB];
+  float2 acc[R][NB];
 #pragma unroll
-  for (int r = 0; r < GV_R; ++r)
+  for (int r = 0; r < R; ++r)
 #pragma unroll
     for (int b = 0; b < NB; ++b) acc[r][b] = make_float2(0.f, 0.f);
 
@@ -186,56 +217,66 @@ gemv_kernel(const __grid_constant__ GvParams P) {
 #pragma unroll
   for (int b = 0; b < NB; ++b) { best_v[b] = ARGMAX_FLOOR; best_i[b] = 0; }
 
-  auto compute = [&](const Raw<Q8>& raw) {
-    if (!raw.ok) return;
-    const float* xb = xs + (size_t)P.job[raw.job].input * NB * cols_pad + raw.chunk * GV_CHUNK + lane * 4;
-    float2 xv[NB][4];
+  auto compute = [&](const Slot<Q8, NB>& sl) {
+    const float* xin = xs + (size_t)P.job[sl.job].input * NB * cols_pad + lane * 4;
 #pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      const float4 a = *reinterpret_cast<const float4*>(xb + (size_t)b * cols_pad);
-      const float4 c = *reinterpret_cast<const float4*>(xb + (size_t)b * cols_pad + 128);
-      xv[b][0] = make_float2(a.x, a.y); xv[b][1] = make_float2(a.z, a.w);
-      xv[b][2] = make_float2(c.x, c.y); xv[b][3] = make_float2(c.z, c.w);
-    }
+    for (int u = 0; u < U; ++u) {
+      const int ch = sl.ch0 + u;
+      if (u < sl.nch && ch * CW + lane * EPL < cols) {
+        float2 wv[R][EPL / 2];
 #pragma unroll
-    for (int r = 0; r < GV_R; ++r) {
-      float2 w[4];
-      if constexpr (Q8) {
-        float2 q[4];
-        s8x4_to_f32(raw.c[r].x, q[0], q[1]);
-        s8x4_to_f32(raw.c[r].y, q[2], q[3]);
-        const float2 so = h2_to_f2(raw.p[r]);
-        const float2 s2 = make_float2(so.x, so.x), o2 = make_float2(so.y, so.y);
+        for (int r = 0; r < R; ++r) {
+          if constexpr (Q8) {
+            const float2 so = h2_to_f2(sl.p[r][u]);
+            const float2 s2 = make_float2(so.x, so.x), o2 = make_float2(so.y, so.y);
+            const uint32_t words[4] = {sl.w[r][u].x, sl.w[r][u].y, sl.w[r][u].z, sl.w[r][u].w};
 #pragma unroll
-        for (int t = 0; t < 4; ++t) w[t] = ffma2(q[t], s2, o2);
-      } else {
-        w[0] = h2_to_f2(raw.w[r].x); w[1] = h2_to_f2(raw.w[r].y);
-        w[2] = h2_to_f2(raw.w[r].z); w[3] = h2_to_f2(raw.w[r].w);
+            for (int k = 0; k < EPL / 4; ++k) {
+              float2 lo, hi;
+              s8x4_to_f32(words[k], lo, hi);
+              wv[r][2 * k] = ffma2(lo, s2, o2);
+              wv[r][2 * k + 1] = ffma2(hi, s2, o2);
+            }
+          } else {
+            wv[r][0] = h2_to_f2(sl.w[r][u].x); wv[r][1] = h2_to_f2(sl.w[r][u].y);
+            wv[r][2] = h2_to_f2(sl.w[r][u].z); wv[r][3] = h2_to_f2(sl.w[r][u].w);
+          }
+        }
+        const float* xc = xin + ch * CW;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          float2 xv[EPL / 2];
+#pragma unroll
+          for (int k = 0; k < EPL / 4; ++k) {
+            const float4 a = *reinterpret_cast<const float4*>(xc + (size_t)b * cols_pad + k * 128);
+            xv[2 * k] = make_float2(a.x, a.y);
+            xv[2 * k + 1] = make_float2(a.z, a.w);
+          }
+#pragma unroll
+          for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int t = 0; t < EPL / 2; ++t) acc[r][b] = ffma2(wv[r][t], xv[t], acc[r][b]);
+        }
       }
-#pragma unroll
-      for (int b = 0; b < NB; ++b)
-#pragma unroll
-        for (int t = 0; t < 4; ++t) acc[r][b] = ffma2(w[t], xv[b][t], acc[r][b]);
     }
   };
 
   int rbuf = 0;
-  auto finish_task = [&](int s) {
-    const int i = s / cpw;
-    const int task = gg + i * TG;
-    int j = 0;
+  auto finish_task = [&]() {
+    const int task = gg + c_i * TG;
 #pragma unroll 1
-    while (j + 1 < P.njobs && task >= P.job[j + 1].task_begin) ++j;
-    const int row0 = (task - P.job[j].task_begin) * GV_R;
-    float v[GV_R * NB];
+    while (c_job + 1 < P.njobs && task >= P.job[c_job + 1].task_begin) ++c_job;
+    const GvJob& J = P.job[c_job];
+    const int row0 = (task - J.task_begin) * R;
+    constexpr int N = R * NB;
+    float v[N];
 #pragma unroll
-    for (int r = 0; r < GV_R; ++r)
+    for (int r = 0; r < R; ++r)
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
         v[r * NB + b] = acc[r][b].x + acc[r][b].y;
         acc[r][b] = make_float2(0.f, 0.f);
       }
-    constexpr int N = GV_R * NB;
     const float t = reduce_scatter<N>(v, lane);
     float* buf = gred + (size_t)rbuf * wpt * N;
     if ((lane & (32 / N - 1)) == 0) buf[wg * N + lane / (32 / N)] = t;
@@ -246,18 +287,17 @@ gemv_kernel(const __grid_constant__ GvParams P) {
       if (lane < N) {
         for (int w = 0; w < wpt; ++w) out += buf[w * N + lane];
       }
-      const int rows = P.job[j].rows;
+      const int rows = J.rows;
       const int row = row0 + r;
       const bool live = lane < N && row < rows && b < P.B;
       if (live) {
-        const int epi = P.job[j].epilogue;
-        if (epi == PGQ_EPI_RELU2) {
+        if (J.epilogue == PGQ_EPI_RELU2) {
           out = fmaxf(out, 0.f);
           out = out * out;
-        } else if (epi == PGQ_EPI_ADD) {
-          out += P.job[j].residual[(size_t)b * rows + row];
+        } else if (J.epilogue == PGQ_EPI_ADD) {
+          out += J.residual[(size_t)b * rows + row];
         }
-        if (P.job[j].y) P.job[j].y[(size_t)b * rows + row] = out;
+        if (J.y) J.y[(size_t)b * rows + row] = out;
       }
       if constexpr (ARGMAX) {
         float cv = live ? out : __int_as_float(0xff800000u);
@@ -277,24 +317,28 @@ gemv_kernel(const __grid_constant__ GvParams P) {
     rbuf ^= 1;
   };
 
-  Raw<Q8> ring[D];
+  Slot<Q8, NB> ring[2];
+  fetch(ring[0], 0);
+  fetch(ring[1], 1);
+  for (int s0 = 0; s0 < nsteps; s0 += 2) {
 #pragma unroll
-  for (int d = 0; d < D; ++d) fetch(ring[d], d);
-  for (int s0 = 0; s0 < nsteps; s0 += D) {
-#pragma unroll
-    for (int d = 0; d < D; ++d) {
+    for (int d = 0; d < 2; ++d) {
       const int s = s0 + d;
       if (s < nsteps) {
         compute(ring[d]);
-        fetch(ring[d], s + D);
-        if ((s % cpw) == cpw - 1) finish_task(s);
+        fetch(ring[d], s + 2);
+        if (++c_tb == nbt) {
+          c_tb = 0;
+          finish_task();
+          ++c_i;
+        }
       }
     }
   }
 
   if constexpr (ARGMAX) {
     __syncthreads();
-    if (wg == 0) {
+    if (wg == 0 && active_warp) {
 #pragma unroll
       for (int bb = 0; bb < NB; ++bb)
         if (lane == bb) {
@@ -337,8 +381,14 @@ using KernelFn = void (*)(GvParams);
 
 template <bool Q8, int NB, bool ARGMAX>
 constexpr KernelFn pick_kernel() {
-  constexpr int D = NB <= 2 ? 4 : (NB <= 4 ? 3 : 2);
-  return reinterpret_cast<KernelFn>(&gemv_kernel<Q8, NB, D, ARGMAX>);
+  return reinterpret_cast<KernelFn>(&gemv_kernel<Q8, NB, ARGMAX>);
+}
+
+// (R, U, CW) of the instance launch_gemv will pick
+void shape_of(bool q8, int nb, int* R, int* U, int* CW) {
+  *R = nb <= 2 ? 2 : 4;
+  *U = nb <= 2 ? 4 : 2;
+  *CW = 32 * ((q8 && nb <= 2) ? 16 : 8);
 }
 
 KernelFn kernel_for(bool q8, int nb, bool argmax) {
@@ -428,20 +478,23 @@ size_t gemv_argmax_workspace_bytes(int B, const DeviceInfo& dev) {
 
 int launch_gemv(GvParams& P, bool q8, bool argmax, const DeviceInfo& dev, cudaStream_t st) {
   const int nb = round_nb(P.B);
-  P.nchunks = (P.cols + GV_CHUNK - 1) / GV_CHUNK;
-  P.cols_pad = P.nchunks * GV_CHUNK;
+  int R, U, CW;
+  shape_of(q8, nb, &R, &U, &CW);
+  P.nchunks = (P.cols + CW - 1) / CW;
+  P.cols_pad = P.nchunks * CW;
+  // enough warps per task that each owns at most U chunks (one batch), up to 8
   int wpt = 1;
-  while (wpt < GV_WARPS && P.nchunks >= 4 * (wpt * 2)) wpt *= 2;
+  while (wpt < GV_WARPS && (P.nchunks + wpt - 1) / wpt > U) wpt *= 2;
   P.wpt = wpt;
   P.groups = GV_WARPS / wpt;
   P.cpw = (P.nchunks + wpt - 1) / wpt;
   int t = 0;
   for (int j = 0; j < P.njobs; ++j) {
     P.job[j].task_begin = t;
-    t += (P.job[j].rows + GV_R - 1) / GV_R;
+    t += (P.job[j].rows + R - 1) / R;
   }
   P.ntasks = t;
-  const size_t smem = ((size_t)P.ninputs * nb * P.cols_pad + (size_t)P.groups * 2 * wpt * GV_R * nb) * sizeof(float);
+  const size_t smem = ((size_t)P.ninputs * nb * P.cols_pad + (size_t)P.groups * 2 * wpt * R * nb) * sizeof(float);
   if (smem + 2048 > dev.smem_optin) return set_error(PGQ_EUNSUPPORTED, "staged input needs %zu bytes of shared memory", smem);
   KernelFn fn = kernel_for(q8, nb, argmax);
   if (cudaError_t e = allow_smem(fn, smem); e != cudaSuccess)
