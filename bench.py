@@ -341,6 +341,9 @@ def main():
     ap.add_argument("--impl", default="pgq", choices=["pgq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-prefill", action="store_true", help="only the headline decode layer")
+    ap.add_argument("--only", choices=["decode", "prefill"], default=None,
+                    help="profiling aid: run one workload and print its JSON object")
+    ap.add_argument("--prefill-layers", type=int, default=None, help="layers of the prefill pass (default 32)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -367,6 +370,10 @@ def main():
         raise SystemExit("libpgq: " + pgq.lib().pgq_last_error().decode())
 
     pk = peaks()
+    if args.only == "prefill":
+        P = PrefillPass(torch, pgq, synth, layers=args.prefill_layers)
+        print(json.dumps(time_prefill(torch, P, args.steps, args.warmup, pk)), flush=True)
+        return
     W = Q8DecodeLayer(torch, pgq, synth)
     torch.cuda.synchronize()
     if dist:
@@ -403,8 +410,8 @@ def main():
         "gpu_launches": W.launches_per_step * args.steps,
         "clocks": clocks,
     }
-    if not args.skip_prefill:
-        P = PrefillPass(torch, pgq, synth)
+    if not args.skip_prefill and args.only != "decode":
+        P = PrefillPass(torch, pgq, synth, layers=args.prefill_layers)
         with Clocks(local) as clk2:
             pre = time_prefill(torch, P, max(3, args.steps // 5), args.warmup, pk)
         pre["clocks"] = clk2.summary()
