@@ -14,7 +14,8 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libpgq.so")
+# PGQ_LIBRARY may name another build of the same library (e.g. an instrumented one)
+LIB_PATH = os.environ.get("PGQ_LIBRARY") or os.path.join(_HERE, "libpgq.so")
 
 # status codes and epilogues (mirrors include/pgq.h)
 OK, EINVAL, EALIGN, EUNSUPPORTED, ECUDA, ETIMEOUT, ENODEV, EWORKSPACE = range(8)

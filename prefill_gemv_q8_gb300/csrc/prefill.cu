@@ -69,6 +69,25 @@ struct TcParams {
   unsigned long long wait_limit_ns;
 };
 
+// Optional event trace (compiled in only with -DPGQ_TRACE): block 0 records
+// (event, step, %globaltimer) triples into a device buffer for latency analysis.
+#ifdef PGQ_TRACE
+__device__ unsigned long long g_trace[3 * 8192];
+__device__ unsigned g_trace_n;
+__device__ __forceinline__ void trace(int ev, long long k) {
+  if (blockIdx.x != 0) return;
+  const unsigned i = atomicAdd(&g_trace_n, 1u);
+  if (i < 8192) {
+    g_trace[3 * i] = (unsigned long long)ev;
+    g_trace[3 * i + 1] = (unsigned long long)k;
+    g_trace[3 * i + 2] = tc::globaltimer();
+  }
+}
+#define TRACE(ev, k) trace(ev, k)
+#else
+#define TRACE(ev, k) ((void)0)
+#endif
+
 // ------------------------------------------------------------------ schedule
 __device__ __forceinline__ long long item_begin(int c, int G, long long T) { return (long long)c * T / G; }
 
@@ -216,6 +235,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
         const int j = job_of_tile(P, tile);
         const int row0 = (tile - P.tile_begin[j]) * TC_BM;
         if (!W.wait(bar(B_EMPTY + s), ph ^ 1)) break;
+        TRACE(0, it);
         tc::mbar_expect_tx(bar(B_FULL + s), tx);
         tc::tma_load_2d_hint(tc::smem_addr(stage_codes(s)), &P.cmap[j], k * TC_BK, row0, bar(B_FULL + s),
                              evict_first);
@@ -250,7 +270,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
         const bool last = (k == ks - 1) || (it == end - 1);
         if (first && !W.wait(bar(B_ACCE + t), pht ^ 1)) break;
         if (!W.wait(bar(B_AFULL + a), pha)) break;
+        TRACE(10, it);
         if (!W.wait(bar(B_FULL + s), ph)) break;
+        TRACE(11, it);
         tc::fence_after_sync();
         const uint32_t d = tmem + t * TC_ACC_COLS;
         const uint32_t xs = tc::smem_addr(stage_x(s));
@@ -266,6 +288,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
           }
         }
         any = true;
+        TRACE(12, it);
         tc::mma_commit(bar(B_EMPTY + s));
         tc::mma_commit(bar(B_AEMPTY + a));
         if (last) {
@@ -289,7 +312,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
     uint32_t ph = 0, pha = 0;
     for (long long it = beg; it < end; ++it) {
       if (!W.wait(bar(B_FULL + s), ph)) break;
+      if (warp == 2 && lane == 0) TRACE(20, it);
       if (!W.wait(bar(B_AEMPTY + a), pha ^ 1)) break;
+      if (warp == 2 && lane == 0) TRACE(21, it);
       const uint8_t* crow = stage_codes(s) + r * 128;
       uint4 cw[8];
 #pragma unroll
@@ -330,6 +355,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
       }
       __syncwarp();
       if (lane == 0) {
+        if (warp == 2) TRACE(22, it);
         tc::mbar_arrive(bar(B_AFULL + a));
         tc::mbar_arrive(bar(B_EMPTY + s));
       }
@@ -353,6 +379,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
       const int rows = P.rows[j];
       const int row = (tile - P.tile_begin[j]) * TC_BM + r;
       const bool ok = W.wait(bar(B_ACCF + t), pht);
+      if (et == 0) TRACE(30, it);
       // leave together: a warp missing from the named barriers below would hang the rest
       if (!epi_all(ok)) break;
       tc::fence_after_sync();
@@ -422,6 +449,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
         }
         epi_bar();
       }
+      if (et == 0) TRACE(31, it);
       it = seg_end;
     }
   }
@@ -602,3 +630,19 @@ int launch_prefill(const PrefillJob* jobs, int njobs, const float* X, int cols, 
 }
 
 }  // namespace pgq
+
+#ifdef PGQ_TRACE
+// Instrumented builds only: copy out and reset the event trace of block 0.
+extern "C" int pgq_debug_trace(unsigned long long* out, unsigned max_events) {
+  unsigned n = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+  if (cudaMemcpyFromSymbol(&n, pgq::g_trace_n, sizeof(n)) != cudaSuccess) return -1;
+  if (n > 8192) n = 8192;
+  if (n > max_events) n = max_events;
+  if (n && cudaMemcpyFromSymbol(out, pgq::g_trace, (size_t)n * 3 * sizeof(unsigned long long)) != cudaSuccess)
+    return -1;
+  const unsigned zero = 0;
+  cudaMemcpyToSymbol(pgq::g_trace_n, &zero, sizeof(zero));
+  return (int)n;
+}
+#endif
