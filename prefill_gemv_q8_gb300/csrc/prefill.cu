@@ -43,13 +43,17 @@ namespace pgq {
 
 constexpr int TC_BM = 128;
 constexpr int TC_BK = 128;
-constexpr int TC_THREADS = 320;  // warp 0 TMA, warp 1 MMA+TMEM, warps 2-5 dequant, 6-9 epilogue
+constexpr int TC_THREADS = 448;  // warp 0 TMA, warp 1 MMA+TMEM, warps 2-9 dequant, 10-13 epilogue
+constexpr int TC_DQ_WARPS = 8;   // two per TMEM lane quarter, each half of the step's columns
+constexpr int TC_EPI_WARP0 = 2 + TC_DQ_WARPS;
+constexpr int TC_NA_TMEM = 4;    // A buffers when A lives in tensor memory
+constexpr int TC_NA_SMEM = 2;    // A buffers when A lives in shared memory
 constexpr int TC_STAGES = 5;
 constexpr int TC_CODES_BYTES = TC_BM * TC_BK;       // 16 KB
 constexpr int TC_PARAMS_BYTES = TC_BM * 16;         // 4 (scale, offset) pairs per row
 constexpr int TC_ACC_COLS = 64;                     // TMEM columns per accumulator (N <= 64)
 constexpr int TC_A_COLS = TC_BK / 2;                // TMEM columns per A buffer (2 halves per column)
-constexpr uint32_t TC_TMEM_COLS = 256;              // 2 accumulators + 2 A buffers
+constexpr uint32_t TC_TMEM_COLS = 512;              // 2 accumulators + 4 A buffers (384 used)
 
 struct TcParams {
   CUtensorMap xmap;                       // X binary16 [Bp][cols], box {64, Bp}, 128B swizzle
@@ -74,9 +78,11 @@ struct TcParams {
 #ifdef PGQ_TRACE
 __device__ unsigned long long g_trace[3 * 8192];
 __device__ unsigned g_trace_n;
+__device__ unsigned long long g_cta[4 * 1024];   // per block: start, after setup, end, smid
+__shared__ unsigned s_trace_n;
 __device__ __forceinline__ void trace(int ev, long long k) {
   if (blockIdx.x != 0) return;
-  const unsigned i = atomicAdd(&g_trace_n, 1u);
+  const unsigned i = atomicAdd(&s_trace_n, 1u);
   if (i < 8192) {
     g_trace[3 * i] = (unsigned long long)ev;
     g_trace[3 * i + 1] = (unsigned long long)k;
@@ -166,6 +172,7 @@ __device__ __forceinline__ __half2 s8pair_to_h2(uint32_t u_biased, uint32_t sel)
 
 template <bool A_TMEM>
 __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_constant__ TcParams P) {
+  constexpr int TC_NA = A_TMEM ? TC_NA_TMEM : TC_NA_SMEM;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int Bp = P.Bp;
@@ -173,11 +180,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
   const int stage_bytes = TC_CODES_BYTES + x_bytes + TC_PARAMS_BYTES;
   uint8_t* stages = smem;
   uint8_t* abuf = stages + TC_STAGES * stage_bytes;            // A in shared memory (A_TMEM == false)
-  uint8_t* tail = abuf + (A_TMEM ? 0 : 2 * TC_BM * TC_BK * 2);
+  uint8_t* tail = abuf + (A_TMEM ? 0 : TC_NA * TC_BM * TC_BK * 2);
   uint64_t* bars = reinterpret_cast<uint64_t*>(tail);
   // barrier slots
-  const int B_FULL = 0, B_EMPTY = TC_STAGES, B_AFULL = 2 * TC_STAGES, B_AEMPTY = B_AFULL + 2, B_ACCF = B_AEMPTY + 2,
-            B_ACCE = B_ACCF + 2, B_DRAIN = B_ACCE + 2, NBARS = B_DRAIN + 1;
+  const int B_FULL = 0, B_EMPTY = TC_STAGES, B_AFULL = 2 * TC_STAGES, B_AEMPTY = B_AFULL + TC_NA,
+            B_ACCF = B_AEMPTY + TC_NA, B_ACCE = B_ACCF + 2, B_DRAIN = B_ACCE + 2, NBARS = B_DRAIN + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
@@ -188,16 +195,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
   auto stage_params = [&](int s) { return stages + s * stage_bytes + TC_CODES_BYTES + x_bytes; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#ifdef PGQ_TRACE
+  if (threadIdx.x == 0) {
+    s_trace_n = 0;
+    g_cta[4 * blockIdx.x] = tc::globaltimer();
+    unsigned smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    g_cta[4 * blockIdx.x + 3] = smid;
+  }
+#endif
   if (threadIdx.x == 0) {
     for (int s = 0; s < TC_STAGES; ++s) {
       tc::mbar_init(bar(B_FULL + s), 1);
-      tc::mbar_init(bar(B_EMPTY + s), 4 + 1);  // 4 dequant warps + the MMA commit
+      tc::mbar_init(bar(B_EMPTY + s), TC_DQ_WARPS + 1);  // dequant warps + the MMA commit
     }
-    for (int a = 0; a < 2; ++a) {
-      tc::mbar_init(bar(B_AFULL + a), 4);
+    for (int a = 0; a < TC_NA; ++a) {
+      tc::mbar_init(bar(B_AFULL + a), TC_DQ_WARPS);
       tc::mbar_init(bar(B_AEMPTY + a), 1);
-      tc::mbar_init(bar(B_ACCF + a), 1);
-      tc::mbar_init(bar(B_ACCE + a), 4);
+    }
+    for (int t = 0; t < 2; ++t) {
+      tc::mbar_init(bar(B_ACCF + t), 1);
+      tc::mbar_init(bar(B_ACCE + t), 4);
     }
     tc::mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0;
@@ -215,6 +233,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+#ifdef PGQ_TRACE
+  if (threadIdx.x == 0) g_cta[4 * blockIdx.x + 1] = tc::globaltimer();
+#endif
 
   const int G = gridDim.x;
   const long long T = P.total_items;
@@ -296,7 +317,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
           if (++t == 2) { t = 0; pht ^= 1; }
         }
         if (++s == TC_STAGES) { s = 0; ph ^= 1; }
-        if (++a == 2) { a = 0; pha ^= 1; }
+        if (++a == TC_NA) { a = 0; pha ^= 1; }
       }
       if (any) {
         // every MMA issued by this thread has completed before TMEM is released
@@ -304,10 +325,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
         W.drain(bar(B_DRAIN), 0);
       }
     }
-  } else if (warp < 6) {
+  } else if (warp < TC_EPI_WARP0) {
     // ------------------------------------------------------------ dequantisation
-    const int q = warp & 3;            // TMEM lane quarter of this warp
-    const int r = q * 32 + lane;       // weight row within the tile
+    const int q = warp & 3;              // TMEM lane quarter of this warp
+    const int hk = (warp - 2) >> 2;      // which 64 columns of the step
+    const int r = q * 32 + lane;         // weight row within the tile
     int s = 0, a = 0;
     uint32_t ph = 0, pha = 0;
     for (long long it = beg; it < end; ++it) {
@@ -316,14 +338,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
       if (!W.wait(bar(B_AEMPTY + a), pha ^ 1)) break;
       if (warp == 2 && lane == 0) TRACE(21, it);
       const uint8_t* crow = stage_codes(s) + r * 128;
-      uint4 cw[8];
+      uint4 cw[4];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) cw[c] = *reinterpret_cast<const uint4*>(crow + ((c ^ (r & 7)) << 4));
-      const uint4 pr = *reinterpret_cast<const uint4*>(stage_params(s) + r * 16);
-      const uint32_t prw[4] = {pr.x, pr.y, pr.z, pr.w};
-      uint32_t out[64];
+      for (int c = 0; c < 4; ++c) {
+        const int cc = hk * 4 + c;
+        cw[c] = *reinterpret_cast<const uint4*>(crow + ((cc ^ (r & 7)) << 4));
+      }
+      const uint2 pr = *reinterpret_cast<const uint2*>(stage_params(s) + r * 16 + hk * 8);
+      const uint32_t prw[2] = {pr.x, pr.y};
+      uint32_t out[32];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < 4; ++c) {
         const __half2 so = *reinterpret_cast<const __half2*>(&prw[c >> 1]);
         const __half2 s2 = __low2half2(so), o2 = __high2half2(so);
         const uint32_t wv[4] = {cw[c].x, cw[c].y, cw[c].z, cw[c].w};
@@ -337,19 +362,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
         }
       }
       if constexpr (A_TMEM) {
-        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + 2 * TC_ACC_COLS + a * TC_A_COLS;
-        uint32_t (&o0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&out[0]);
-        uint32_t (&o1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&out[32]);
-        tc::tmem_st_32x32b_x32(ta, o0);
-        tc::tmem_st_32x32b_x32(ta + 32, o1);
+        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + 2 * TC_ACC_COLS + a * TC_A_COLS + hk * 32;
+        tc::tmem_st_32x32b_x32(ta, out);
         tc::tmem_wait_st();
         tc::fence_before_sync();
       } else {
         uint8_t* ab = abuf + a * (TC_BM * TC_BK * 2);
 #pragma unroll
-        for (int g = 0; g < 16; ++g) {
+        for (int g8 = 0; g8 < 8; ++g8) {
+          const int g = hk * 8 + g8;       // 16-byte chunk of the row (8 halves)
           uint8_t* dst = ab + (g >> 3) * (TC_BM * 128) + (r >> 3) * 1024 + (r & 7) * 128 + (((g & 7) ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4*>(dst) = make_uint4(out[4 * g], out[4 * g + 1], out[4 * g + 2], out[4 * g + 3]);
+          *reinterpret_cast<uint4*>(dst) =
+              make_uint4(out[4 * g8], out[4 * g8 + 1], out[4 * g8 + 2], out[4 * g8 + 3]);
         }
         tc::fence_proxy_async_smem();
       }
@@ -360,13 +384,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
         tc::mbar_arrive(bar(B_EMPTY + s));
       }
       if (++s == TC_STAGES) { s = 0; ph ^= 1; }
-      if (++a == 2) { a = 0; pha ^= 1; }
+      if (++a == TC_NA) { a = 0; pha ^= 1; }
     }
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     const int r = q * 32 + lane;
-    const int et = threadIdx.x - 6 * 32;  // 0..127
+    const int et = threadIdx.x - TC_EPI_WARP0 * 32;  // 0..127
     int t = 0;
     uint32_t pht = 0;
     long long it = beg;
@@ -434,15 +458,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
           const int c_first = cta_of_item((long long)tile * ks, G, T);
           const int c_last = cta_of_item(tile_end - 1, G, T);
           if (row < rows) {
-            for (int b = 0; b < P.B; ++b) {
-              float acc = 0.f;
-              for (int c = c_first; c <= c_last; ++c) {
-                const int ft = (int)(item_begin(c, G, T) / ks);
-                const float* pc = P.partials + ((size_t)c * P.maxseg + (tile - ft)) * Bp * TC_BM;
-                acc += __ldcg(pc + (size_t)b * TC_BM + r);
+#pragma unroll
+            for (int b = 0; b < TC_ACC_COLS; ++b) v[b] = 0.f;
+            for (int c = c_first; c <= c_last; ++c) {
+              const int ft = (int)(item_begin(c, G, T) / ks);
+              const float* pc = P.partials + ((size_t)c * P.maxseg + (tile - ft)) * Bp * TC_BM + r;
+#pragma unroll
+              for (int b = 0; b < TC_ACC_COLS; ++b)
+                if (b < P.B) v[b] += __ldcg(pc + (size_t)b * TC_BM);
+            }
+#pragma unroll
+            for (int b = 0; b < TC_ACC_COLS; ++b) {
+              if (b < P.B) {
+                const size_t idx = (size_t)b * rows + row;
+                y[idx] = apply_epi(v[b], epi, res, idx);
               }
-              const size_t idx = (size_t)b * rows + row;
-              y[idx] = apply_epi(acc, epi, res, idx);
             }
           }
           if (et == 0) P.tile_cnt[tile] = 0u;
@@ -460,6 +490,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, TC_TMEM_COLS);
   }
+#ifdef PGQ_TRACE
+  if (threadIdx.x == 0) {
+    g_cta[4 * blockIdx.x + 2] = tc::globaltimer();
+    if (blockIdx.x == 0) g_trace_n = s_trace_n;
+  }
+#endif
 }
 
 // ------------------------------------------------------------------ X → binary16
@@ -530,7 +566,7 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_
 template <bool A_TMEM>
 size_t tc_smem_bytes(int Bp) {
   const size_t stage = TC_CODES_BYTES + 2 * (size_t)Bp * 128 + TC_PARAMS_BYTES;
-  return 1024 /*alignment slack*/ + TC_STAGES * stage + (A_TMEM ? 0 : 2 * TC_BM * TC_BK * 2) + 256;
+  return 1024 /*alignment slack*/ + TC_STAGES * stage + (A_TMEM ? 0 : TC_NA_SMEM * TC_BM * TC_BK * 2) + 256;
 }
 
 struct Plan {
@@ -633,6 +669,13 @@ int launch_prefill(const PrefillJob* jobs, int njobs, const float* X, int cols, 
 
 #ifdef PGQ_TRACE
 // Instrumented builds only: copy out and reset the event trace of block 0.
+extern "C" int pgq_debug_cta(unsigned long long* out, unsigned nblocks) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+  if (nblocks > 1024) nblocks = 1024;
+  return cudaMemcpyFromSymbol(out, pgq::g_cta, (size_t)nblocks * 4 * sizeof(unsigned long long)) == cudaSuccess
+             ? 0 : -1;
+}
+
 extern "C" int pgq_debug_trace(unsigned long long* out, unsigned max_events) {
   unsigned n = 0;
   if (cudaDeviceSynchronize() != cudaSuccess) return -1;
