@@ -48,7 +48,8 @@ constexpr int TC_DQ_WARPS = 8;   // two per TMEM lane quarter, each half of the 
 constexpr int TC_EPI_WARP0 = 2 + TC_DQ_WARPS;
 constexpr int TC_NA_TMEM = 4;    // A buffers when A lives in tensor memory
 constexpr int TC_NA_SMEM = 2;    // A buffers when A lives in shared memory
-constexpr int TC_STAGES = 5;
+constexpr int TC_STAGES_TMEM = 5;  // stage ring depth with A in tensor memory
+constexpr int TC_STAGES_SMEM = 4;  // with A in shared memory (its buffers take the room)
 constexpr int TC_CODES_BYTES = TC_BM * TC_BK;       // 16 KB
 constexpr int TC_PARAMS_BYTES = TC_BM * 16;         // 4 (scale, offset) pairs per row
 constexpr int TC_ACC_COLS = 64;                     // TMEM columns per accumulator (N <= 64)
@@ -76,22 +77,18 @@ struct TcParams {
 // Optional event trace (compiled in only with -DPGQ_TRACE): block 0 records
 // (event, step, %globaltimer) triples into a device buffer for latency analysis.
 #ifdef PGQ_TRACE
-__device__ unsigned long long g_trace[3 * 8192];
-__device__ unsigned g_trace_n;
-__device__ unsigned long long g_cta[4 * 1024];   // per block: start, after setup, end, smid
-__shared__ unsigned s_trace_n;
-__device__ __forceinline__ void trace(int ev, long long k) {
-  if (blockIdx.x != 0) return;
-  const unsigned i = atomicAdd(&s_trace_n, 1u);
-  if (i < 8192) {
-    g_trace[3 * i] = (unsigned long long)ev;
-    g_trace[3 * i + 1] = (unsigned long long)k;
-    g_trace[3 * i + 2] = tc::globaltimer();
-  }
+// block 0: per role and item, clock64 stamps kept in shared memory, written out at exit
+constexpr int TR_ITEMS = 64, TR_EV = 4;
+__device__ long long g_tr[4 * TR_ITEMS * TR_EV];      // [role][item][event]
+__device__ unsigned long long g_cta[4 * 1024];         // per block: start, after setup, end, smid
+__shared__ long long s_tr[4 * TR_ITEMS * TR_EV];
+__device__ __forceinline__ void trace(int role, int ev, long long item, long long beg) {
+  const long long i = item - beg;
+  if (blockIdx.x == 0 && i >= 0 && i < TR_ITEMS) s_tr[(role * TR_ITEMS + i) * TR_EV + ev] = clock64();
 }
-#define TRACE(ev, k) trace(ev, k)
+#define TRACE(role, ev, k) trace(role, ev, k, beg)
 #else
-#define TRACE(ev, k) ((void)0)
+#define TRACE(role, ev, k) ((void)0)
 #endif
 
 // ------------------------------------------------------------------ schedule
@@ -173,6 +170,7 @@ __device__ __forceinline__ __half2 s8pair_to_h2(uint32_t u_biased, uint32_t sel)
 template <bool A_TMEM>
 __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_constant__ TcParams P) {
   constexpr int TC_NA = A_TMEM ? TC_NA_TMEM : TC_NA_SMEM;
+  constexpr int TC_STAGES = A_TMEM ? TC_STAGES_TMEM : TC_STAGES_SMEM;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int Bp = P.Bp;
@@ -196,8 +194,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #ifdef PGQ_TRACE
+  for (int i = threadIdx.x; i < 4 * TR_ITEMS * TR_EV; i += blockDim.x) s_tr[i] = 0;
   if (threadIdx.x == 0) {
-    s_trace_n = 0;
     g_cta[4 * blockIdx.x] = tc::globaltimer();
     unsigned smid;
     asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
@@ -256,7 +254,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
         const int j = job_of_tile(P, tile);
         const int row0 = (tile - P.tile_begin[j]) * TC_BM;
         if (!W.wait(bar(B_EMPTY + s), ph ^ 1)) break;
-        TRACE(0, it);
+        TRACE(0, 0, it);
         tc::mbar_expect_tx(bar(B_FULL + s), tx);
         tc::tma_load_2d_hint(tc::smem_addr(stage_codes(s)), &P.cmap[j], k * TC_BK, row0, bar(B_FULL + s),
                              evict_first);
@@ -291,9 +289,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
         const bool last = (k == ks - 1) || (it == end - 1);
         if (first && !W.wait(bar(B_ACCE + t), pht ^ 1)) break;
         if (!W.wait(bar(B_AFULL + a), pha)) break;
-        TRACE(10, it);
+        TRACE(1, 0, it);
         if (!W.wait(bar(B_FULL + s), ph)) break;
-        TRACE(11, it);
+        TRACE(1, 1, it);
         tc::fence_after_sync();
         const uint32_t d = tmem + t * TC_ACC_COLS;
         const uint32_t xs = tc::smem_addr(stage_x(s));
@@ -309,9 +307,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
           }
         }
         any = true;
-        TRACE(12, it);
+        TRACE(1, 2, it);
         tc::mma_commit(bar(B_EMPTY + s));
         tc::mma_commit(bar(B_AEMPTY + a));
+        TRACE(1, 3, it);
         if (last) {
           tc::mma_commit(bar(B_ACCF + t));
           if (++t == 2) { t = 0; pht ^= 1; }
@@ -334,9 +333,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
     uint32_t ph = 0, pha = 0;
     for (long long it = beg; it < end; ++it) {
       if (!W.wait(bar(B_FULL + s), ph)) break;
-      if (warp == 2 && lane == 0) TRACE(20, it);
+      if (warp == 2 && lane == 0) TRACE(2, 0, it);
       if (!W.wait(bar(B_AEMPTY + a), pha ^ 1)) break;
-      if (warp == 2 && lane == 0) TRACE(21, it);
+      if (warp == 2 && lane == 0) TRACE(2, 1, it);
       const uint8_t* crow = stage_codes(s) + r * 128;
       uint4 cw[4];
 #pragma unroll
@@ -379,7 +378,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
       }
       __syncwarp();
       if (lane == 0) {
-        if (warp == 2) TRACE(22, it);
+        if (warp == 2) TRACE(2, 2, it);
         tc::mbar_arrive(bar(B_AFULL + a));
         tc::mbar_arrive(bar(B_EMPTY + s));
       }
@@ -403,7 +402,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
       const int rows = P.rows[j];
       const int row = (tile - P.tile_begin[j]) * TC_BM + r;
       const bool ok = W.wait(bar(B_ACCF + t), pht);
-      if (et == 0) TRACE(30, it);
+      if (et == 0) TRACE(3, 0, it);
       // leave together: a warp missing from the named barriers below would hang the rest
       if (!epi_all(ok)) break;
       tc::fence_after_sync();
@@ -479,7 +478,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
         }
         epi_bar();
       }
-      if (et == 0) TRACE(31, it);
+      if (et == 0) TRACE(3, 1, it);
       it = seg_end;
     }
   }
@@ -493,8 +492,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
 #ifdef PGQ_TRACE
   if (threadIdx.x == 0) {
     g_cta[4 * blockIdx.x + 2] = tc::globaltimer();
-    if (blockIdx.x == 0) g_trace_n = s_trace_n;
   }
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < 4 * TR_ITEMS * TR_EV; i += blockDim.x) g_tr[i] = s_tr[i];
 #endif
 }
 
@@ -566,7 +566,8 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_
 template <bool A_TMEM>
 size_t tc_smem_bytes(int Bp) {
   const size_t stage = TC_CODES_BYTES + 2 * (size_t)Bp * 128 + TC_PARAMS_BYTES;
-  return 1024 /*alignment slack*/ + TC_STAGES * stage + (A_TMEM ? 0 : TC_NA_SMEM * TC_BM * TC_BK * 2) + 256;
+  return 1024 /*alignment slack*/ + (A_TMEM ? TC_STAGES_TMEM : TC_STAGES_SMEM) * stage +
+         (A_TMEM ? 0 : TC_NA_SMEM * TC_BM * TC_BK * 2) + 256;
 }
 
 struct Plan {
@@ -676,16 +677,10 @@ extern "C" int pgq_debug_cta(unsigned long long* out, unsigned nblocks) {
              ? 0 : -1;
 }
 
-extern "C" int pgq_debug_trace(unsigned long long* out, unsigned max_events) {
-  unsigned n = 0;
+extern "C" int pgq_debug_trace(long long* out, unsigned max_values) {
   if (cudaDeviceSynchronize() != cudaSuccess) return -1;
-  if (cudaMemcpyFromSymbol(&n, pgq::g_trace_n, sizeof(n)) != cudaSuccess) return -1;
-  if (n > 8192) n = 8192;
-  if (n > max_events) n = max_events;
-  if (n && cudaMemcpyFromSymbol(out, pgq::g_trace, (size_t)n * 3 * sizeof(unsigned long long)) != cudaSuccess)
-    return -1;
-  const unsigned zero = 0;
-  cudaMemcpyToSymbol(pgq::g_trace_n, &zero, sizeof(zero));
-  return (int)n;
+  unsigned n = 4 * pgq::TR_ITEMS * pgq::TR_EV;
+  if (n > max_values) n = max_values;
+  return cudaMemcpyFromSymbol(out, pgq::g_tr, (size_t)n * sizeof(long long)) == cudaSuccess ? (int)n : -1;
 }
 #endif
