@@ -116,7 +116,7 @@ struct Waiter {
     if (tc::mbar_try(bar, parity)) return true;
     const uint64_t t0 = tc::globaltimer();
     while (true) {
-      if (tc::mbar_try(bar, parity)) return true;
+      if (tc::mbar_try_sleep(bar, parity, 20000u)) return true;
       if (*abort_flag) return false;
       if (tc::globaltimer() - t0 > P.wait_limit_ns) {
         *abort_flag = 1;
@@ -128,7 +128,7 @@ struct Waiter {
   // bounded wait that ignores the abort flag (drain of in-flight copies / MMAs)
   __device__ bool drain(uint32_t bar, uint32_t parity) const {
     const uint64_t t0 = tc::globaltimer();
-    while (!tc::mbar_try(bar, parity)) {
+    while (!tc::mbar_try_sleep(bar, parity, 20000u)) {
       if (tc::globaltimer() - t0 > P.wait_limit_ns) {
         atomicCAS(P.status, 0, PGQ_ETIMEOUT);
         return false;
@@ -294,16 +294,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
         TRACE(1, 1, it);
         tc::fence_after_sync();
         const uint32_t d = tmem + t * TC_ACC_COLS;
-        const uint32_t xs = tc::smem_addr(stage_x(s));
+        // descriptors: one base per stage, the K slices differ by constant offsets
+        const uint64_t b0 = tc::sdesc_sw128(tc::smem_addr(stage_x(s)));
+        const uint64_t bstep = (uint64_t)((Bp * 128) >> 4);  // second 64-column half
 #pragma unroll
         for (int kk = 0; kk < TC_BK / 16; ++kk) {
-          const uint64_t bdesc = tc::sdesc_sw128(xs + (kk >> 2) * Bp * 128 + (kk & 3) * 32);
+          const uint64_t bdesc = b0 + (uint64_t)((kk & 3) * 2) + (kk >> 2) * bstep;
           const uint32_t acc = (first && kk == 0) ? 0u : 1u;
           if constexpr (A_TMEM) {
             tc::mma_f16_ts(d, tmem + 2 * TC_ACC_COLS + a * TC_A_COLS + kk * 8, bdesc, idesc, acc);
           } else {
-            const uint32_t as = tc::smem_addr(abuf + a * (TC_BM * TC_BK * 2));
-            tc::mma_f16_ss(d, tc::sdesc_sw128(as + (kk >> 2) * (TC_BM * 128) + (kk & 3) * 32), bdesc, idesc, acc);
+            const uint64_t a0 = tc::sdesc_sw128(tc::smem_addr(abuf + a * (TC_BM * TC_BK * 2)));
+            tc::mma_f16_ss(d, a0 + (uint64_t)((kk & 3) * 2) + (kk >> 2) * (uint64_t)((TC_BM * 128) >> 4), bdesc,
+                           idesc, acc);
           }
         }
         any = true;
