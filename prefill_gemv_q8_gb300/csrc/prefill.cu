@@ -82,8 +82,8 @@ constexpr int TR_ITEMS = 64, TR_EV = 4;
 __device__ long long g_tr[4 * TR_ITEMS * TR_EV];      // [role][item][event]
 __device__ unsigned long long g_cta[4 * 1024];         // per block: start, after setup, end, smid
 __shared__ long long s_tr[4 * TR_ITEMS * TR_EV];
-__device__ __forceinline__ void trace(int role, int ev, long long item, long long beg) {
-  const long long i = item - beg;
+__device__ __forceinline__ void trace(int role, int ev, int item, int beg) {
+  const int i = item - beg;
   if (blockIdx.x == 0 && i >= 0 && i < TR_ITEMS) s_tr[(role * TR_ITEMS + i) * TR_EV + ev] = clock64();
 }
 #define TRACE(role, ev, k) trace(role, ev, k, beg)
@@ -92,10 +92,10 @@ __device__ __forceinline__ void trace(int role, int ev, long long item, long lon
 #endif
 
 // ------------------------------------------------------------------ schedule
-__device__ __forceinline__ long long item_begin(int c, int G, long long T) { return (long long)c * T / G; }
+__device__ __forceinline__ int item_begin(int c, int G, int T) { return (int)((long long)c * T / G); }
 
-__device__ __forceinline__ int cta_of_item(long long i, int G, long long T) {
-  int c = (int)((i * G) / T);
+__device__ __forceinline__ int cta_of_item(int i, int G, int T) {
+  int c = (int)(((long long)i * G) / T);
   if (c >= G) c = G - 1;
   while (c + 1 < G && item_begin(c + 1, G, T) <= i) ++c;
   while (c > 0 && item_begin(c, G, T) > i) --c;
@@ -236,25 +236,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
 #endif
 
   const int G = gridDim.x;
-  const long long T = P.total_items;
-  const long long beg = item_begin(blockIdx.x, G, T), end = item_begin(blockIdx.x + 1, G, T);
+  const int T = (int)P.total_items;
+  const int beg = item_begin(blockIdx.x, G, T), end = item_begin(blockIdx.x + 1, G, T);
   const int ks = P.ks;
   Waiter W{P, abort_flag};
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      const uint64_t evict_first = tc::policy_evict_first();
-      const uint32_t tx = (uint32_t)stage_bytes;
-      int s = 0;
-      uint32_t ph = 0;
-      long long issued = 0;
-      for (long long it = beg; it < end; ++it) {
-        const int tile = (int)(it / ks), k = (int)(it % ks);
-        const int j = job_of_tile(P, tile);
+    // ------------------------------------------------------------ TMA producer (whole warp, one lane issues)
+    const uint64_t evict_first = tc::policy_evict_first();
+    const uint32_t tx = (uint32_t)stage_bytes;
+    int s = 0;
+    uint32_t ph = 0;
+    int issued = 0;
+    int tile = beg / ks, k = beg - (beg / ks) * ks;
+    int j = job_of_tile(P, tile);
+    for (int it = beg; it < end; ++it) {
+      if (!__all_sync(0xffffffffu, W.wait(bar(B_EMPTY + s), ph ^ 1))) break;
+      TRACE(0, 0, it);
+      if (tc::elect_one()) {
         const int row0 = (tile - P.tile_begin[j]) * TC_BM;
-        if (!W.wait(bar(B_EMPTY + s), ph ^ 1)) break;
-        TRACE(0, 0, it);
         tc::mbar_expect_tx(bar(B_FULL + s), tx);
         tc::tma_load_2d_hint(tc::smem_addr(stage_codes(s)), &P.cmap[j], k * TC_BK, row0, bar(B_FULL + s),
                              evict_first);
@@ -262,70 +262,76 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
                              evict_first);
         tc::tma_load_2d(tc::smem_addr(stage_x(s)), &P.xmap, k * TC_BK, 0, bar(B_FULL + s));
         tc::tma_load_2d(tc::smem_addr(stage_x(s) + Bp * 128), &P.xmap, k * TC_BK + 64, 0, bar(B_FULL + s));
-        ++issued;
-        if (++s == TC_STAGES) { s = 0; ph ^= 1; }
       }
-      if (*abort_flag) {
-        // let the copies already issued land before the block can exit
-        const int n = issued < TC_STAGES ? (int)issued : TC_STAGES;
-        int ss = s;
-        uint32_t pp = ph;
-        for (int i = 0; i < n; ++i) {
-          if (--ss < 0) { ss = TC_STAGES - 1; pp ^= 1; }
-          W.drain(bar(B_FULL + ss), pp);
-        }
+      __syncwarp();
+      ++issued;
+      if (++s == TC_STAGES) { s = 0; ph ^= 1; }
+      if (++k == ks) {
+        k = 0;
+        ++tile;
+        while (j + 1 < P.njobs && tile >= P.tile_begin[j + 1]) ++j;
+      }
+    }
+    if (*abort_flag && lane == 0) {
+      // let the copies already issued land before the block can exit
+      const int n = issued < TC_STAGES ? issued : TC_STAGES;
+      int ss = s;
+      uint32_t pp = ph;
+      for (int i = 0; i < n; ++i) {
+        if (--ss < 0) { ss = TC_STAGES - 1; pp ^= 1; }
+        W.drain(bar(B_FULL + ss), pp);
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = tc::idesc_f16_f32(TC_BM, Bp);
-      int s = 0, a = 0, t = 0;
-      uint32_t ph = 0, pha = 0, pht = 0;
-      bool any = false;
-      for (long long it = beg; it < end; ++it) {
-        const int k = (int)(it % ks);
-        const bool first = (k == 0) || (it == beg);
-        const bool last = (k == ks - 1) || (it == end - 1);
-        if (first && !W.wait(bar(B_ACCE + t), pht ^ 1)) break;
-        if (!W.wait(bar(B_AFULL + a), pha)) break;
-        TRACE(1, 0, it);
-        if (!W.wait(bar(B_FULL + s), ph)) break;
-        TRACE(1, 1, it);
-        tc::fence_after_sync();
-        const uint32_t d = tmem + t * TC_ACC_COLS;
-        // descriptors: one base per stage, the K slices differ by constant offsets
-        const uint64_t b0 = tc::sdesc_sw128(tc::smem_addr(stage_x(s)));
-        const uint64_t bstep = (uint64_t)((Bp * 128) >> 4);  // second 64-column half
+    // ------------------------------------------------------------ MMA issuer (whole warp, one lane issues)
+    const uint32_t idesc = tc::idesc_f16_f32(TC_BM, Bp);
+    const uint64_t bstep = (uint64_t)((Bp * 128) >> 4);  // second 64-column half of the X slice
+    int s = 0, a = 0, t = 0;
+    uint32_t ph = 0, pha = 0, pht = 0;
+    bool any = false;
+    int k = beg - (beg / ks) * ks;
+    for (int it = beg; it < end; ++it) {
+      const bool first = (k == 0) || (it == beg);
+      const bool last = (k == ks - 1) || (it == end - 1);
+      if (first && !__all_sync(0xffffffffu, W.wait(bar(B_ACCE + t), pht ^ 1))) break;
+      if (!__all_sync(0xffffffffu, W.wait(bar(B_AFULL + a), pha))) break;
+      TRACE(1, 0, it);
+      if (!__all_sync(0xffffffffu, W.wait(bar(B_FULL + s), ph))) break;
+      TRACE(1, 1, it);
+      tc::fence_after_sync();
+      const uint32_t d = tmem + t * TC_ACC_COLS;
+      const uint64_t b0 = tc::sdesc_sw128(tc::smem_addr(stage_x(s)));
+      const uint32_t a_t = tmem + 2 * TC_ACC_COLS + a * TC_A_COLS;
+      const uint64_t a_s = A_TMEM ? 0 : tc::sdesc_sw128(tc::smem_addr(abuf + a * (TC_BM * TC_BK * 2)));
+      if (tc::elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < TC_BK / 16; ++kk) {
           const uint64_t bdesc = b0 + (uint64_t)((kk & 3) * 2) + (kk >> 2) * bstep;
           const uint32_t acc = (first && kk == 0) ? 0u : 1u;
           if constexpr (A_TMEM) {
-            tc::mma_f16_ts(d, tmem + 2 * TC_ACC_COLS + a * TC_A_COLS + kk * 8, bdesc, idesc, acc);
+            tc::mma_f16_ts(d, a_t + kk * 8, bdesc, idesc, acc);
           } else {
-            const uint64_t a0 = tc::sdesc_sw128(tc::smem_addr(abuf + a * (TC_BM * TC_BK * 2)));
-            tc::mma_f16_ss(d, a0 + (uint64_t)((kk & 3) * 2) + (kk >> 2) * (uint64_t)((TC_BM * 128) >> 4), bdesc,
+            tc::mma_f16_ss(d, a_s + (uint64_t)((kk & 3) * 2) + (kk >> 2) * (uint64_t)((TC_BM * 128) >> 4), bdesc,
                            idesc, acc);
           }
         }
-        any = true;
-        TRACE(1, 2, it);
         tc::mma_commit(bar(B_EMPTY + s));
         tc::mma_commit(bar(B_AEMPTY + a));
-        TRACE(1, 3, it);
-        if (last) {
-          tc::mma_commit(bar(B_ACCF + t));
-          if (++t == 2) { t = 0; pht ^= 1; }
-        }
-        if (++s == TC_STAGES) { s = 0; ph ^= 1; }
-        if (++a == TC_NA) { a = 0; pha ^= 1; }
+        if (last) tc::mma_commit(bar(B_ACCF + t));
       }
-      if (any) {
-        // every MMA issued by this thread has completed before TMEM is released
-        tc::mma_commit(bar(B_DRAIN));
-        W.drain(bar(B_DRAIN), 0);
-      }
+      __syncwarp();
+      any = true;
+      TRACE(1, 2, it);
+      if (last && ++t == 2) { t = 0; pht ^= 1; }
+      if (++s == TC_STAGES) { s = 0; ph ^= 1; }
+      if (++a == TC_NA) { a = 0; pha ^= 1; }
+      if (++k == ks) k = 0;
+    }
+    if (any) {
+      // every MMA issued by this warp has completed before TMEM is released
+      if (tc::elect_one()) tc::mma_commit(bar(B_DRAIN));
+      __syncwarp();
+      W.drain(bar(B_DRAIN), 0);
     }
   } else if (warp < TC_EPI_WARP0) {
     // ------------------------------------------------------------ dequantisation
@@ -334,7 +340,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
     const int r = q * 32 + lane;         // weight row within the tile
     int s = 0, a = 0;
     uint32_t ph = 0, pha = 0;
-    for (long long it = beg; it < end; ++it) {
+    for (int it = beg; it < end; ++it) {
       if (!W.wait(bar(B_FULL + s), ph)) break;
       if (warp == 2 && lane == 0) TRACE(2, 0, it);
       if (!W.wait(bar(B_AEMPTY + a), pha ^ 1)) break;
@@ -395,12 +401,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
     const int et = threadIdx.x - TC_EPI_WARP0 * 32;  // 0..127
     int t = 0;
     uint32_t pht = 0;
-    long long it = beg;
+    int it = beg;
     while (it < end) {
-      const int tile = (int)(it / ks);
-      const long long tile_end = (long long)(tile + 1) * ks;
-      const long long seg_end = end < tile_end ? end : tile_end;
-      const bool whole = (it == (long long)tile * ks) && (seg_end == tile_end);
+      const int tile = it / ks;
+      const int tile_end = (tile + 1) * ks;
+      const int seg_end = end < tile_end ? end : tile_end;
+      const bool whole = (it == tile * ks) && (seg_end == tile_end);
       const int j = job_of_tile(P, tile);
       const int rows = P.rows[j];
       const int row = (tile - P.tile_begin[j]) * TC_BM + r;
@@ -449,7 +455,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
         __threadfence();
         epi_bar();
         if (et == 0) {
-          const int c_first = cta_of_item((long long)tile * ks, G, T);
+          const int c_first = cta_of_item(tile * ks, G, T);
           const int c_last = cta_of_item(tile_end - 1, G, T);
           const unsigned n = (unsigned)(c_last - c_first + 1);
           *last_flag = (atomicAdd(P.tile_cnt + tile, 1u) == n - 1) ? 1 : 0;
@@ -457,7 +463,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
         epi_bar();
         if (*last_flag) {
           __threadfence();
-          const int c_first = cta_of_item((long long)tile * ks, G, T);
+          const int c_first = cta_of_item(tile * ks, G, T);
           const int c_last = cta_of_item(tile_end - 1, G, T);
           if (row < rows) {
 #pragma unroll
