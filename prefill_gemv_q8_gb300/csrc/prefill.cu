@@ -454,6 +454,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
           if (b < P.B) part[(size_t)b * TC_BM + r] = v[b] * P.xinv[b];
         __threadfence();
         epi_bar();
+        if (et == 0) TRACE(3, 2, it);
         if (et == 0) {
           const int c_first = cta_of_item(tile * ks, G, T);
           const int c_last = cta_of_item(tile_end - 1, G, T);
@@ -461,6 +462,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
           *last_flag = (atomicAdd(P.tile_cnt + tile, 1u) == n - 1) ? 1 : 0;
         }
         epi_bar();
+        if (et == 0) TRACE(3, 3, it);
         if (*last_flag) {
           __threadfence();
           const int c_first = cta_of_item(tile * ks, G, T);
