@@ -452,19 +452,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
 #pragma unroll
         for (int b = 0; b < TC_ACC_COLS; ++b)
           if (b < P.B) part[(size_t)b * TC_BM + r] = v[b] * P.xinv[b];
-        __threadfence();
+        // all partial stores of the block happen before one gpu-scope release
+        // (barrier + cumulative fence), then the ticket
         epi_bar();
         if (et == 0) TRACE(3, 2, it);
         if (et == 0) {
           const int c_first = cta_of_item(tile * ks, G, T);
           const int c_last = cta_of_item(tile_end - 1, G, T);
           const unsigned n = (unsigned)(c_last - c_first + 1);
-          *last_flag = (atomicAdd(P.tile_cnt + tile, 1u) == n - 1) ? 1 : 0;
+          asm volatile("fence.acq_rel.gpu;" ::: "memory");
+          const unsigned old = atomicAdd(P.tile_cnt + tile, 1u);
+          asm volatile("fence.acq_rel.gpu;" ::: "memory");
+          *last_flag = (old == n - 1) ? 1 : 0;
         }
         epi_bar();
         if (et == 0) TRACE(3, 3, it);
         if (*last_flag) {
-          __threadfence();
           const int c_first = cta_of_item(tile * ks, G, T);
           const int c_last = cta_of_item(tile_end - 1, G, T);
           if (row < rows) {
