@@ -160,6 +160,37 @@ __device__ __forceinline__ float apply_epi(float v, int epi, const float* residu
   return v;
 }
 
+// Stores out[b] = epilogue(v[b]) for b < B at y[b*rows + row].  The residual of
+// PGQ_EPI_ADD (possibly y itself) is read 16 positions at a time before their
+// stores, so the reads are not serialised behind the stores.
+template <int NV>
+__device__ __forceinline__ void store_row(float (&v)[NV], int B, int epi, float* y, const float* residual, int rows,
+                                          int row) {
+#pragma unroll
+  for (int b0 = 0; b0 < NV; b0 += 16) {
+    if (b0 < B) {
+      float rv[16];
+      if (epi == PGQ_EPI_ADD) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) rv[i] = (b0 + i < B) ? residual[(size_t)(b0 + i) * rows + row] : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (b0 + i < B) {
+          float o = v[b0 + i];
+          if (epi == PGQ_EPI_RELU2) {
+            o = fmaxf(o, 0.f);
+            o = o * o;
+          } else if (epi == PGQ_EPI_ADD) {
+            o = rv[i] + o;
+          }
+          y[(size_t)(b0 + i) * rows + row] = o;
+        }
+      }
+    }
+  }
+}
+
 // Exact signed byte pair → binary16 pair: (0x64 << 8 | b + 128) is the half
 // 1024 + b + 128; subtracting 1152 leaves b.
 __device__ __forceinline__ __half2 s8pair_to_h2(uint32_t u_biased, uint32_t sel) {
@@ -184,6 +215,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
   const int B_FULL = 0, B_EMPTY = TC_STAGES, B_AFULL = 2 * TC_STAGES, B_AEMPTY = B_AFULL + TC_NA,
             B_ACCF = B_AEMPTY + TC_NA, B_ACCE = B_ACCF + 2, B_DRAIN = B_ACCE + 2, NBARS = B_DRAIN + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
+  __shared__ float s_xinv[TC_ACC_COLS];
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
@@ -220,6 +252,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
     tc::fence_barrier_init();
   }
   if (warp == 1) tc::tmem_alloc(tc::smem_addr(tmem_slot), TC_TMEM_COLS);
+  if (threadIdx.x < TC_ACC_COLS) s_xinv[threadIdx.x] = threadIdx.x < Bp ? P.xinv[threadIdx.x] : 0.f;
   if (warp == 0 && lane == 0) {
     tc::prefetch_tensormap(&P.xmap);
     for (int j = 0; j < P.njobs; ++j) {
@@ -438,12 +471,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
       if (whole) {
         if (row < rows) {
 #pragma unroll
-          for (int b = 0; b < TC_ACC_COLS; ++b) {
-            if (b < P.B) {
-              const size_t idx = (size_t)b * rows + row;
-              y[idx] = apply_epi(v[b] * P.xinv[b], epi, res, idx);
-            }
-          }
+          for (int b = 0; b < TC_ACC_COLS; ++b) v[b] *= s_xinv[b];
+          store_row(v, P.B, epi, y, res, rows, row);
         }
       } else {
         // f32 partial of this block for the tile, then the last block to finish sums
@@ -451,7 +480,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
         float* part = P.partials + ((size_t)blockIdx.x * P.maxseg + (tile - first_tile)) * Bp * TC_BM;
 #pragma unroll
         for (int b = 0; b < TC_ACC_COLS; ++b)
-          if (b < P.B) part[(size_t)b * TC_BM + r] = v[b] * P.xinv[b];
+          if (b < P.B) part[(size_t)b * TC_BM + r] = v[b] * s_xinv[b];
         // all partial stores of the block happen before one gpu-scope release
         // (barrier + cumulative fence), then the ticket
         epi_bar();
@@ -480,13 +509,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
               for (int b = 0; b < TC_ACC_COLS; ++b)
                 if (b < P.B) v[b] += __ldcg(pc + (size_t)b * TC_BM);
             }
-#pragma unroll
-            for (int b = 0; b < TC_ACC_COLS; ++b) {
-              if (b < P.B) {
-                const size_t idx = (size_t)b * rows + row;
-                y[idx] = apply_epi(v[b], epi, res, idx);
-              }
-            }
+            store_row(v, P.B, epi, y, res, rows, row);
           }
           if (et == 0) P.tile_cnt[tile] = 0u;
         }
