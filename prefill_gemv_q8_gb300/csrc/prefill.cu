@@ -49,10 +49,11 @@ constexpr int TC_EPI_WARP0 = 2 + TC_DQ_WARPS;
 constexpr int TC_NA_TMEM = 4;    // A buffers when A lives in tensor memory
 constexpr int TC_NA_SMEM = 2;    // A buffers when A lives in shared memory
 constexpr int TC_STAGES_TMEM = 5;  // stage ring depth with A in tensor memory
-constexpr int TC_STAGES_SMEM = 4;  // with A in shared memory (its buffers take the room)
+constexpr int TC_STAGES_SMEM = 3;  // with A in shared memory (its buffers take the room)
 constexpr int TC_CODES_BYTES = TC_BM * TC_BK;       // 16 KB
 constexpr int TC_PARAMS_BYTES = TC_BM * 16;         // 4 (scale, offset) pairs per row
 constexpr int TC_ACC_COLS = 64;                     // TMEM columns per accumulator (N <= 64)
+constexpr int TC_ACC_TILE_BYTES = TC_ACC_COLS * TC_BM * 4;  // epilogue transpose tile
 constexpr int TC_A_COLS = TC_BK / 2;                // TMEM columns per A buffer (2 halves per column)
 constexpr uint32_t TC_TMEM_COLS = 512;              // 2 accumulators + 4 A buffers (384 used)
 
@@ -151,41 +152,39 @@ __device__ __forceinline__ bool epi_all(bool ok) {
   return r != 0;
 }
 
-__device__ __forceinline__ float apply_epi(float v, int epi, const float* residual, size_t idx) {
-  if (epi == PGQ_EPI_RELU2) {
-    v = fmaxf(v, 0.f);
-    return v * v;
-  }
-  if (epi == PGQ_EPI_ADD) return residual[idx] + v;
-  return v;
-}
 
-// Stores out[b] = epilogue(v[b]) for b < B at y[b*rows + row].  The residual of
-// PGQ_EPI_ADD (possibly y itself) is read 16 positions at a time before their
-// stores, so the reads are not serialised behind the stores.
-template <int NV>
-__device__ __forceinline__ void store_row(float (&v)[NV], int B, int epi, float* y, const float* residual, int rows,
-                                          int row) {
-#pragma unroll
-  for (int b0 = 0; b0 < NV; b0 += 16) {
-    if (b0 < B) {
-      float rv[16];
-      if (epi == PGQ_EPI_ADD) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) rv[i] = (b0 + i < B) ? residual[(size_t)(b0 + i) * rows + row] : 0.f;
+// Writes a tile's outputs from the shared transposed tile acc4 ([b][128 rows] as
+// float4): y[b][row0 + c] = epilogue(acc[b][c]) for c < rows - row0.  Each warp
+// covers whole 512-byte rows; a thread takes every 128th float4.
+__device__ __forceinline__ void out_rows(const float4* acc4, int nvec, int et, int epi, float* y, const float* res,
+                                         int rows, int row0, bool vec_ok) {
+#pragma unroll 4
+  for (int i = et; i < nvec; i += 128) {
+    const int b = i >> 5, c = (i & 31) * 4;
+    const int rr = row0 + c;
+    if (rr >= rows) continue;
+    float4 a = acc4[i];
+    const size_t idx = (size_t)b * rows + rr;
+    if (vec_ok) {
+      if (epi == PGQ_EPI_RELU2) {
+        a.x = fmaxf(a.x, 0.f); a.y = fmaxf(a.y, 0.f); a.z = fmaxf(a.z, 0.f); a.w = fmaxf(a.w, 0.f);
+        a = make_float4(a.x * a.x, a.y * a.y, a.z * a.z, a.w * a.w);
+      } else if (epi == PGQ_EPI_ADD) {
+        const float4 q = *reinterpret_cast<const float4*>(res + idx);
+        a = make_float4(q.x + a.x, q.y + a.y, q.z + a.z, q.w + a.w);
       }
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        if (b0 + i < B) {
-          float o = v[b0 + i];
-          if (epi == PGQ_EPI_RELU2) {
-            o = fmaxf(o, 0.f);
-            o = o * o;
-          } else if (epi == PGQ_EPI_ADD) {
-            o = rv[i] + o;
-          }
-          y[(size_t)(b0 + i) * rows + row] = o;
+      *reinterpret_cast<float4*>(y + idx) = a;
+    } else {
+      const float av[4] = {a.x, a.y, a.z, a.w};
+      for (int e = 0; e < 4 && rr + e < rows; ++e) {
+        float o = av[e];
+        if (epi == PGQ_EPI_RELU2) {
+          o = fmaxf(o, 0.f);
+          o = o * o;
+        } else if (epi == PGQ_EPI_ADD) {
+          o = res[idx + e] + o;
         }
+        y[idx + e] = o;
       }
     }
   }
@@ -209,7 +208,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
   const int stage_bytes = TC_CODES_BYTES + x_bytes + TC_PARAMS_BYTES;
   uint8_t* stages = smem;
   uint8_t* abuf = stages + TC_STAGES * stage_bytes;            // A in shared memory (A_TMEM == false)
-  uint8_t* tail = abuf + (A_TMEM ? 0 : TC_NA * TC_BM * TC_BK * 2);
+  float* s_acc = reinterpret_cast<float*>(abuf + (A_TMEM ? 0 : TC_NA * TC_BM * TC_BK * 2));  // [64][128]
+  uint8_t* tail = reinterpret_cast<uint8_t*>(s_acc) + TC_ACC_TILE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(tail);
   // barrier slots
   const int B_FULL = 0, B_EMPTY = TC_STAGES, B_AFULL = 2 * TC_STAGES, B_AEMPTY = B_AFULL + TC_NA,
@@ -468,19 +468,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
       const int epi = P.epi[j];
       float* y = P.y[j];
       const float* res = P.residual[j];
-      if (whole) {
-        if (row < rows) {
+      const int row0 = row - r;
+      // scaled accumulator transposed into shared memory: s_acc[b][r]
 #pragma unroll
-          for (int b = 0; b < TC_ACC_COLS; ++b) v[b] *= s_xinv[b];
-          store_row(v, P.B, epi, y, res, rows, row);
-        }
+      for (int b = 0; b < TC_ACC_COLS; ++b)
+        if (b < Bp) s_acc[b * TC_BM + r] = v[b] * s_xinv[b];
+      epi_bar();
+      const float4* acc4 = reinterpret_cast<const float4*>(s_acc);
+      const int nvec = P.B * (TC_BM / 4);
+      const bool vec_ok = ((rows & 3) == 0) && ((reinterpret_cast<uintptr_t>(y) & 15) == 0) &&
+                          (epi != PGQ_EPI_ADD || (reinterpret_cast<uintptr_t>(res) & 15) == 0);
+      if (whole) {
+        out_rows(acc4, nvec, et, epi, y, res, rows, row0, vec_ok);
       } else {
         // f32 partial of this block for the tile, then the last block to finish sums
-        const int first_tile = (int)(beg / ks);
-        float* part = P.partials + ((size_t)blockIdx.x * P.maxseg + (tile - first_tile)) * Bp * TC_BM;
-#pragma unroll
-        for (int b = 0; b < TC_ACC_COLS; ++b)
-          if (b < P.B) part[(size_t)b * TC_BM + r] = v[b] * s_xinv[b];
+        const int first_tile = beg / ks;
+        float4* part = reinterpret_cast<float4*>(P.partials +
+                                                 ((size_t)blockIdx.x * P.maxseg + (tile - first_tile)) * Bp * TC_BM);
+#pragma unroll 4
+        for (int i = et; i < nvec; i += 128) part[i] = acc4[i];
         // all partial stores of the block happen before one gpu-scope release
         // (barrier + cumulative fence), then the ticket
         epi_bar();
@@ -499,22 +505,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
         if (*last_flag) {
           const int c_first = cta_of_item(tile * ks, G, T);
           const int c_last = cta_of_item(tile_end - 1, G, T);
-          if (row < rows) {
-#pragma unroll
-            for (int b = 0; b < TC_ACC_COLS; ++b) v[b] = 0.f;
+          // sum the contributors' partials in block order into the shared tile
+          float4* sum4 = reinterpret_cast<float4*>(s_acc);
+#pragma unroll 4
+          for (int i = et; i < nvec; i += 128) {
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int c = c_first; c <= c_last; ++c) {
-              const int ft = (int)(item_begin(c, G, T) / ks);
-              const float* pc = P.partials + ((size_t)c * P.maxseg + (tile - ft)) * Bp * TC_BM + r;
-#pragma unroll
-              for (int b = 0; b < TC_ACC_COLS; ++b)
-                if (b < P.B) v[b] += __ldcg(pc + (size_t)b * TC_BM);
+              const int ft = item_begin(c, G, T) / ks;
+              const float4* pc =
+                  reinterpret_cast<const float4*>(P.partials + ((size_t)c * P.maxseg + (tile - ft)) * Bp * TC_BM);
+              const float4 u = __ldcg(pc + i);
+              a.x += u.x; a.y += u.y; a.z += u.z; a.w += u.w;
             }
-            store_row(v, P.B, epi, y, res, rows, row);
+            sum4[i] = a;
           }
+          epi_bar();
+          out_rows(acc4, nvec, et, epi, y, res, rows, row0, vec_ok);
           if (et == 0) P.tile_cnt[tile] = 0u;
         }
-        epi_bar();
       }
+      epi_bar();  // the shared tile is free for the next segment
       if (et == 0) TRACE(3, 1, it);
       it = seg_end;
     }
@@ -604,7 +614,7 @@ template <bool A_TMEM>
 size_t tc_smem_bytes(int Bp) {
   const size_t stage = TC_CODES_BYTES + 2 * (size_t)Bp * 128 + TC_PARAMS_BYTES;
   return 1024 /*alignment slack*/ + (A_TMEM ? TC_STAGES_TMEM : TC_STAGES_SMEM) * stage +
-         (A_TMEM ? 0 : TC_NA_SMEM * TC_BM * TC_BK * 2) + 256;
+         (A_TMEM ? 0 : TC_NA_SMEM * TC_BM * TC_BK * 2) + TC_ACC_TILE_BYTES + 256;
 }
 
 struct Plan {
