@@ -155,26 +155,52 @@ __device__ __forceinline__ bool epi_all(bool ok) {
 
 // Writes a tile's outputs from the shared transposed tile acc4 ([b][128 rows] as
 // float4): y[b][row0 + c] = epilogue(acc[b][c]) for c < rows - row0.  Each warp
-// covers whole 512-byte rows; a thread takes every 128th float4.
+// covers whole 512-byte rows; thread et takes float4 et, et+128, ... (at most 16).
+// All reads (shared tile, residual) are issued before the first store, so a
+// residual that is y itself costs one memory round trip, not one per element.
+constexpr int TC_OUT_K = TC_ACC_COLS * (TC_BM / 4) / 128;  // float4 per epilogue thread (16)
+constexpr int TC_OUT_P = 4;                                  // handled in passes (registers)
+constexpr int TC_OUT_H = TC_OUT_K / TC_OUT_P;
+
 __device__ __forceinline__ void out_rows(const float4* acc4, int nvec, int et, int epi, float* y, const float* res,
                                          int rows, int row0, bool vec_ok) {
-#pragma unroll 4
-  for (int i = et; i < nvec; i += 128) {
-    const int b = i >> 5, c = (i & 31) * 4;
-    const int rr = row0 + c;
-    if (rr >= rows) continue;
-    float4 a = acc4[i];
-    const size_t idx = (size_t)b * rows + rr;
-    if (vec_ok) {
-      if (epi == PGQ_EPI_RELU2) {
-        a.x = fmaxf(a.x, 0.f); a.y = fmaxf(a.y, 0.f); a.z = fmaxf(a.z, 0.f); a.w = fmaxf(a.w, 0.f);
-        a = make_float4(a.x * a.x, a.y * a.y, a.z * a.z, a.w * a.w);
-      } else if (epi == PGQ_EPI_ADD) {
-        const float4 q = *reinterpret_cast<const float4*>(res + idx);
-        a = make_float4(q.x + a.x, q.y + a.y, q.z + a.z, q.w + a.w);
+  if (vec_ok) {
+#pragma unroll
+    for (int h = 0; h < TC_OUT_P; ++h) {
+      float4 a[TC_OUT_H], q[TC_OUT_H];
+#pragma unroll
+      for (int k = 0; k < TC_OUT_H; ++k) {
+        const int i = et + 128 * (h * TC_OUT_H + k);
+        const int rr = row0 + (i & 31) * 4;
+        if (i < nvec) {
+          a[k] = acc4[i];
+          if (epi == PGQ_EPI_ADD && rr < rows) q[k] = *reinterpret_cast<const float4*>(res + (size_t)(i >> 5) * rows + rr);
+        }
       }
-      *reinterpret_cast<float4*>(y + idx) = a;
-    } else {
+#pragma unroll
+      for (int k = 0; k < TC_OUT_H; ++k) {
+        const int i = et + 128 * (h * TC_OUT_H + k);
+        const int rr = row0 + (i & 31) * 4;
+        if (i < nvec && rr < rows) {
+          float4 o = a[k];
+          if (epi == PGQ_EPI_RELU2) {
+            o.x = fmaxf(o.x, 0.f); o.y = fmaxf(o.y, 0.f); o.z = fmaxf(o.z, 0.f); o.w = fmaxf(o.w, 0.f);
+            o = make_float4(o.x * o.x, o.y * o.y, o.z * o.z, o.w * o.w);
+          } else if (epi == PGQ_EPI_ADD) {
+            o = make_float4(q[k].x + o.x, q[k].y + o.y, q[k].z + o.z, q[k].w + o.w);
+          }
+          *reinterpret_cast<float4*>(y + (size_t)(i >> 5) * rows + rr) = o;
+        }
+      }
+    }
+  } else {
+    // rows not a multiple of 4 or unaligned outputs: element by element
+    for (int k = 0; k < TC_OUT_K; ++k) {
+      const int i = et + 128 * k;
+      if (i >= nvec) break;
+      const int rr = row0 + (i & 31) * 4;
+      const size_t idx = (size_t)(i >> 5) * rows + rr;
+      const float4 a = acc4[i];
       const float av[4] = {a.x, a.y, a.z, a.w};
       for (int e = 0; e < 4 && rr + e < rows; ++e) {
         float o = av[e];
@@ -198,7 +224,7 @@ __device__ __forceinline__ __half2 s8pair_to_h2(uint32_t u_biased, uint32_t sel)
 }
 
 template <bool A_TMEM>
-__global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_constant__ TcParams P) {
+__global__ void __maxnreg__(144) prefill_tc_kernel(const __grid_constant__ TcParams P) {
   constexpr int TC_NA = A_TMEM ? TC_NA_TMEM : TC_NA_SMEM;
   constexpr int TC_STAGES = A_TMEM ? TC_STAGES_TMEM : TC_STAGES_SMEM;
   extern __shared__ uint8_t smem_raw[];
@@ -448,8 +474,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
       // leave together: a warp missing from the named barriers below would hang the rest
       if (!epi_all(ok)) break;
       tc::fence_after_sync();
-      float v[TC_ACC_COLS];
       const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + t * TC_ACC_COLS;
+      // accumulator row -> scaled, transposed into the shared tile s_acc[b][r]
 #pragma unroll
       for (int c0 = 0; c0 < TC_ACC_COLS; c0 += 16) {
         if (c0 < Bp) {
@@ -457,7 +483,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
           tc::tmem_ld_32x32b_x16(ta + c0, u);
           tc::tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[c0 + i] = __uint_as_float(u[i]);
+          for (int i = 0; i < 16; ++i) s_acc[(c0 + i) * TC_BM + r] = __uint_as_float(u[i]) * s_xinv[c0 + i];
         }
       }
       tc::fence_before_sync();
@@ -469,10 +495,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
       float* y = P.y[j];
       const float* res = P.residual[j];
       const int row0 = row - r;
-      // scaled accumulator transposed into shared memory: s_acc[b][r]
-#pragma unroll
-      for (int b = 0; b < TC_ACC_COLS; ++b)
-        if (b < Bp) s_acc[b * TC_BM + r] = v[b] * s_xinv[b];
       epi_bar();
       const float4* acc4 = reinterpret_cast<const float4*>(s_acc);
       const int nvec = P.B * (TC_BM / 4);
@@ -485,8 +507,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
         const int first_tile = beg / ks;
         float4* part = reinterpret_cast<float4*>(P.partials +
                                                  ((size_t)blockIdx.x * P.maxseg + (tile - first_tile)) * Bp * TC_BM);
-#pragma unroll 4
-        for (int i = et; i < nvec; i += 128) part[i] = acc4[i];
+#pragma unroll
+        for (int k = 0; k < TC_OUT_K; ++k)
+          if (et + 128 * k < nvec) part[et + 128 * k] = acc4[et + 128 * k];
         // all partial stores of the block happen before one gpu-scope release
         // (barrier + cumulative fence), then the ticket
         epi_bar();
@@ -506,18 +529,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
           const int c_first = cta_of_item(tile * ks, G, T);
           const int c_last = cta_of_item(tile_end - 1, G, T);
           // sum the contributors' partials in block order into the shared tile
+          // (this thread's own float4 slots only); 8 loads in flight at a time
           float4* sum4 = reinterpret_cast<float4*>(s_acc);
-#pragma unroll 4
-          for (int i = et; i < nvec; i += 128) {
-            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int c = c_first; c <= c_last; ++c) {
-              const int ft = item_begin(c, G, T) / ks;
-              const float4* pc =
-                  reinterpret_cast<const float4*>(P.partials + ((size_t)c * P.maxseg + (tile - ft)) * Bp * TC_BM);
-              const float4 u = __ldcg(pc + i);
-              a.x += u.x; a.y += u.y; a.z += u.z; a.w += u.w;
+          for (int c = c_first; c <= c_last; ++c) {
+            const int ft = item_begin(c, G, T) / ks;
+            const float4* pc =
+                reinterpret_cast<const float4*>(P.partials + ((size_t)c * P.maxseg + (tile - ft)) * Bp * TC_BM);
+#pragma unroll
+            for (int h = 0; h < TC_OUT_P; ++h) {
+              float4 u[TC_OUT_H];
+#pragma unroll
+              for (int k = 0; k < TC_OUT_H; ++k) {
+                const int i = et + 128 * (h * TC_OUT_H + k);
+                if (i < nvec) u[k] = __ldcg(pc + i);
+              }
+#pragma unroll
+              for (int k = 0; k < TC_OUT_H; ++k) {
+                const int i = et + 128 * (h * TC_OUT_H + k);
+                if (i < nvec) {
+                  float4 t4 = c == c_first ? make_float4(0.f, 0.f, 0.f, 0.f) : sum4[i];
+                  t4.x += u[k].x; t4.y += u[k].y; t4.z += u[k].z; t4.w += u[k].w;
+                  sum4[i] = t4;
+                }
+              }
             }
-            sum4[i] = a;
           }
           epi_bar();
           out_rows(acc4, nvec, et, epi, y, res, rows, row0, vec_ok);
