@@ -224,7 +224,7 @@ __device__ __forceinline__ __half2 s8pair_to_h2(uint32_t u_biased, uint32_t sel)
 }
 
 template <bool A_TMEM>
-__global__ void __maxnreg__(144) prefill_tc_kernel(const __grid_constant__ TcParams P) {
+__global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_constant__ TcParams P) {
   constexpr int TC_NA = A_TMEM ? TC_NA_TMEM : TC_NA_SMEM;
   constexpr int TC_STAGES = A_TMEM ? TC_STAGES_TMEM : TC_STAGES_SMEM;
   extern __shared__ uint8_t smem_raw[];
