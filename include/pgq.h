@@ -120,6 +120,27 @@ int pgq_gemv_f16_argmax(const uint16_t* W, int rows, int cols, const float* x, i
                         const float* gamma, float eps, float* logits, int32_t* ids,
                         void* workspace, size_t workspace_bytes, void* stream);
 
+/* Allocation-free form of pgq_gemv_f16_argmax.  The paper has no counterpart to
+ * this entry point; it exists for callers that cannot allocate device memory: code
+ * running while a CUDA graph is being captured (where cudaMalloc is not allowed),
+ * latency-bound decode loops that cannot afford the device synchronisation an
+ * allocation may bring, and plugins living inside a host framework that owns every
+ * byte of device memory through its own pools.  Such callers still pass W, x,
+ * gamma, logits and ids; the scratch the argmax needs (per-block partial maxima and
+ * a completion ticket) lives in a fixed array of PGQ_STATIC_SCRATCH_BYTES inside the
+ * library, which every GPU that loads the library keeps for the life of the process.
+ * Calls on one device share that array and it keeps the last call's contents; the
+ * call clears what must start at zero itself.  Two calls that overlap on the GPU
+ * (different streams, no ordering between them) race on it: order them.  The first
+ * call on each device looks up the array's device address, so make it before any
+ * stream capture.  Shapes whose scratch would exceed the array are rejected with
+ * PGQ_EUNSUPPORTED (about (SM count x B) x 8 bytes are needed).  It allocates
+ * nothing and calls no allocating routine. */
+#define PGQ_STATIC_SCRATCH_BYTES 32768
+int pgq_gemv_f16_argmax_static(const uint16_t* W, int rows, int cols, const float* x, int B,
+                               const float* gamma, float eps, float* logits, int32_t* ids,
+                               void* stream);
+
 /* Standalone argmax of logits f32 [B][V] (same rules) into ids int32 [B].
  * 1 <= B <= 65535, V >= 1. */
 int pgq_argmax(const float* logits, int B, int V, int32_t* ids, void* stream);

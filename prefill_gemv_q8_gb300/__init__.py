@@ -59,6 +59,7 @@ _SIGS = {
     "pgq_gemv_f16_argmax": (C.c_int, [_vp, C.c_int, C.c_int, _vp, C.c_int, _vp, C.c_float, _vp, _vp, _vp,
                                       C.c_size_t, _vp]),
     "pgq_argmax": (C.c_int, [_vp, C.c_int, C.c_int, _vp, _vp]),
+    "pgq_gemv_f16_argmax_static": (C.c_int, [_vp, C.c_int, C.c_int, _vp, C.c_int, _vp, C.c_float, _vp, _vp, _vp]),
     "pgq_gemv_q8": (C.c_int, [_vp, _vp, C.c_int, C.c_int, _vp, C.c_int, _vp, C.c_float, _vp, C.c_int, _vp, _vp]),
     "pgq_gemv_q8_multi": (C.c_int, [C.POINTER(Q8Job), C.c_int, C.POINTER(Input), C.c_int, C.c_int, C.c_int,
                                     C.c_float, _vp]),

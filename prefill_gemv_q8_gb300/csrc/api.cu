@@ -206,6 +206,22 @@ int pgq_gemv_f16_argmax(const uint16_t* W, int rows, int cols, const float* x, i
   return launch_gemv(P, false, true, dev, as_stream(stream));
 }
 
+int pgq_gemv_f16_argmax_static(const uint16_t* W, int rows, int cols, const float* x, int B, const float* gamma,
+                               float eps, float* logits, int32_t* ids, void* stream) {
+  REQUIRE(B >= 1 && B <= PGQ_DECODE_BMAX, PGQ_EINVAL, "gemv_f16_argmax_static: B=%d outside 1..%d", B,
+          PGQ_DECODE_BMAX);
+  GET_DEVICE(dev);
+  const size_t need = gemv_argmax_workspace_bytes(B, dev);
+  REQUIRE(need <= PGQ_STATIC_SCRATCH_BYTES, PGQ_EUNSUPPORTED,
+          "gemv_f16_argmax_static: %d SMs x B=%d need %zu bytes of scratch, more than the fixed %d", dev.sms, B, need,
+          PGQ_STATIC_SCRATCH_BYTES);
+  void* scratch = nullptr;
+  size_t scratch_bytes = 0;
+  const int st = argmax_static_scratch(&scratch, &scratch_bytes);
+  if (st) return st;
+  return pgq_gemv_f16_argmax(W, rows, cols, x, B, gamma, eps, logits, ids, scratch, scratch_bytes, stream);
+}
+
 int pgq_gemv_q8(const int8_t* codes, const uint16_t* params, int rows, int cols, const float* x, int B,
                 const float* gamma, float eps, float* y, int epilogue, const float* residual, void* stream) {
   pgq_q8_job job{codes, params, rows, 0, y, epilogue, residual};

@@ -469,6 +469,32 @@ int gemv_grid(int B, bool q8, bool argmax, const DeviceInfo& dev) {
   return dev.sms;
 }
 
+// ------------------------------------------------------------------ fixed scratch
+// Scratch for the allocation-free vocab-head entry point: a file-scope device array
+// that every GPU loading the library holds until exit.  Host code sees only a
+// host-side stand-in for it, so its device address is looked up once per device
+// (with that device current) and cached.
+static __device__ __align__(256) unsigned char g_argmax_scratch[PGQ_STATIC_SCRATCH_BYTES];
+
+int argmax_static_scratch(void** ptr, size_t* bytes) {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (dev < 0 || dev >= 64) return set_error(PGQ_ENODEV, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lk(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_argmax_scratch);
+    if (e != cudaSuccess) return set_error(PGQ_ECUDA, "static scratch address: %s", cudaGetErrorString(e));
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  *bytes = sizeof(g_argmax_scratch);
+  return PGQ_OK;
+}
+
 size_t gemv_argmax_workspace_bytes(int B, const DeviceInfo& dev) {
   const size_t parts = (size_t)dev.sms * (size_t)B;
   const size_t a = (parts * sizeof(float) + 15) & ~size_t(15);

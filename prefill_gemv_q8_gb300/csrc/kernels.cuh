@@ -48,6 +48,9 @@ int launch_argmax(const float* logits, int B, int V, int32_t* ids, cudaStream_t 
 int launch_gemv(GvParams& P, bool q8, bool argmax, const DeviceInfo& dev, cudaStream_t st);
 // Workspace of the argmax variant: partials [grid][B] (value, index) + ticket.
 size_t gemv_argmax_workspace_bytes(int B, const DeviceInfo& dev);
+// Device address and size of the fixed scratch array of the allocation-free
+// vocab-head entry point (looked up once per device).
+int argmax_static_scratch(void** ptr, size_t* bytes);
 // Exact grid of a decode GEMV launch (used to size the argmax partials).
 int gemv_grid(int B, bool q8, bool argmax, const DeviceInfo& dev);
 
