@@ -247,6 +247,72 @@ int pgq_q8_prefill_pass(const pgq_q8_layer* layers, int L, float* h, int B, cons
                         const float* gamma2, float eps, void* workspace, size_t workspace_bytes,
                         void* stream);
 
+/* ---------------------------------------------------------------- a6: MoE
+ * Router projection over a pass (nemotron_prefill.rs `pb_f32_mm`):
+ *   logits[b][e] = sum_c R[e][c] * n[b][c]
+ * R: device f32 [E][cols]; n: device f32 [B][cols]; logits: device f32 [B][E].
+ * cols % 4 == 0, cols <= 3072; 1 <= B; 1 <= E. */
+int pgq_moe_router(const float* R, int E, int cols, const float* n, int B, float* logits, void* stream);
+
+/* Softmax top-k per position (choice rule of nemotron_prefill.rs `pb_route`; the
+ * score is the softmax probability): sel[b][s] = the s-th largest logit's expert,
+ * an exact tie going to the lower id (NaN logits are never preferred);
+ * w[b][s] = p[sel] with p = softmax(logits[b]), divided by sum_s p[sel] when renorm
+ * != 0.  logits f32 [B][E]; sel int32 [B][k]; w f32 [B][k].  E <= 256, k <= min(E, 32). */
+int pgq_moe_route_topk(const float* logits, int B, int E, int k, int renorm, int32_t* sel, float* w,
+                       void* stream);
+
+/* Per-expert grouping of the pass's entries j = b*k + s (nemotron_prefill.rs
+ * `pb_lists`): counts[e] = #{j : sel[j] == e}; offsets = exclusive prefix [E+1];
+ * entries[offsets[e] .. offsets[e+1]) = the j with sel[j] == e in ascending order.
+ * Ids outside [0, E) belong to no list; entries past offsets[E] are set to -1.
+ * When x_gathered != NULL it also receives x_gathered[i] = x[entries[i] / xdiv]
+ * (x f32 [*][n]).  B*k + 2E + 1 <= 12288.  Deterministic (bit-exact). */
+int pgq_moe_group_gather(const int32_t* sel, int B, int k, int E, int32_t* counts, int32_t* offsets,
+                         int32_t* entries, const float* x, int n, int xdiv, float* x_gathered,
+                         void* stream);
+
+/* Grouped expert projections (nemotron_prefill.rs `pb_q8_bank`, q8 block format):
+ * for every expert e and every entry j in its group,
+ *   y[j][r] = epilogue( sum_c W_e[r][c] * x[j / xdiv][c] ),
+ * each expert's weights streamed once for all of its entries.  The bank is
+ * contiguous: codes int8 [E][rows][cols], params binary16 [E][rows][cols/32][2].
+ * counts, offsets, entries come from pgq_moe_group_gather (nentries = B*k);
+ * y f32 [nentries][rows].  Epilogue PGQ_EPI_NONE or PGQ_EPI_RELU2.
+ * cols % 32 == 0, cols <= 6144, E <= 1024. */
+int pgq_moe_experts_q8(const int8_t* codes, const uint16_t* params, int E, int rows, int cols,
+                       const int32_t* counts, const int32_t* offsets, const int32_t* entries, int nentries,
+                       const float* x, int xdiv, float* y, int epilogue, void* stream);
+
+/* Weighted MoE combine fused into add + RMSNorm (nemotron_prefill.rs `pb_add_rms`,
+ * add == 2): h[b] += o[b] + sum_s w[b][s] * eo[b*k + s]  (slots in ascending order,
+ * o may be NULL); y[b] = gamma * h[b] / sqrt(mean(h[b]^2) + eps).
+ * h f32 [B][n] in place; eo f32 [B*k][n]; w f32 [B][k]; y f32 [B][n]; inv_rms [B] or NULL. */
+int pgq_moe_combine_rmsnorm(float* h, const float* o, const float* eo, const float* w, int k,
+                            const float* gamma, float eps, int B, int n, float* y, float* inv_rms,
+                            void* stream);
+
+/* One MoE layer over a pass of B <= 64 positions:
+ *   n = rms(h)·gamma1; logits = R·n; (sel, w) = softmax top-k; grouping;
+ *   u_j = relu²(W_up[sel_j] · n[j / k]); eo_j = W_down[sel_j] · u_j;
+ *   h += Σ_s w·eo; y = rms(h)·gamma2.
+ * Seven launches.  workspace: pgq_moe_layer_workspace_bytes(layer, B) bytes, 256-byte
+ * aligned; afterwards it holds n, logits, sel, w, counts, offsets, entries, u and eo
+ * at the byte offsets pgq_moe_layer_layout() reports (9 entries). */
+typedef struct {
+  const float* router;          /* f32 [E][hidden] */
+  const int8_t* up_codes;       /* int8 [E][inter][hidden] */
+  const uint16_t* up_params;    /* binary16 [E][inter][hidden/32][2] */
+  const int8_t* down_codes;     /* int8 [E][hidden][inter] */
+  const uint16_t* down_params;  /* binary16 [E][hidden][inter/32][2] */
+  int E, k, hidden, inter, renorm;
+} pgq_moe_layer;
+size_t pgq_moe_layer_workspace_bytes(const pgq_moe_layer* layer, int B);
+int pgq_moe_layer_layout(const pgq_moe_layer* layer, int B, size_t offsets[9]);
+int pgq_moe_prefill_layer(const pgq_moe_layer* layer, float* h, int B, const float* gamma1,
+                          const float* gamma2, float eps, float* y, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

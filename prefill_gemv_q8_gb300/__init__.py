@@ -41,6 +41,11 @@ class Q8Matrix(C.Structure):
     _fields_ = [("codes", _vp), ("params", _vp)]
 
 
+class MoeLayer(C.Structure):
+    _fields_ = [("router", _vp), ("up_codes", _vp), ("up_params", _vp), ("down_codes", _vp), ("down_params", _vp),
+                ("E", C.c_int), ("k", C.c_int), ("hidden", C.c_int), ("inter", C.c_int), ("renorm", C.c_int)]
+
+
 class Q8Layer(C.Structure):
     _fields_ = [("q", Q8Matrix), ("k", Q8Matrix), ("v", Q8Matrix), ("o", Q8Matrix),
                 ("up", Q8Matrix), ("down", Q8Matrix),
@@ -69,6 +74,18 @@ _SIGS = {
     "pgq_prefill_q8_workspace_bytes": (C.c_size_t, [C.POINTER(C.c_int), C.c_int, C.c_int, C.c_int]),
     "pgq_prefill_q8": (C.c_int, [C.POINTER(Q8Job), C.c_int, _vp, C.c_int, C.c_int, _vp, C.c_size_t, _vp]),
     "pgq_prefill_status": (C.c_int, [_vp, _vp]),
+    "pgq_moe_router": (C.c_int, [_vp, C.c_int, C.c_int, _vp, C.c_int, _vp, _vp]),
+    "pgq_moe_route_topk": (C.c_int, [_vp, C.c_int, C.c_int, C.c_int, C.c_int, _vp, _vp, _vp]),
+    "pgq_moe_group_gather": (C.c_int, [_vp, C.c_int, C.c_int, C.c_int, _vp, _vp, _vp, _vp, C.c_int, C.c_int, _vp,
+                                       _vp]),
+    "pgq_moe_experts_q8": (C.c_int, [_vp, _vp, C.c_int, C.c_int, C.c_int, _vp, _vp, _vp, C.c_int, _vp, C.c_int, _vp,
+                                     C.c_int, _vp]),
+    "pgq_moe_combine_rmsnorm": (C.c_int, [_vp, _vp, _vp, _vp, C.c_int, _vp, C.c_float, C.c_int, C.c_int, _vp, _vp,
+                                          _vp]),
+    "pgq_moe_layer_workspace_bytes": (C.c_size_t, [C.POINTER(MoeLayer), C.c_int]),
+    "pgq_moe_layer_layout": (C.c_int, [C.POINTER(MoeLayer), C.c_int, C.POINTER(C.c_size_t)]),
+    "pgq_moe_prefill_layer": (C.c_int, [C.POINTER(MoeLayer), _vp, C.c_int, _vp, _vp, C.c_float, _vp, _vp,
+                                        C.c_size_t, _vp]),
     "pgq_q8_prefill_pass_workspace_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int, C.c_int]),
     "pgq_q8_prefill_pass_layout": (C.c_int, [C.c_int, C.c_int, C.c_int, C.c_int, C.POINTER(C.c_size_t)]),
     "pgq_q8_prefill_pass": (C.c_int, [C.POINTER(Q8Layer), C.c_int, _vp, C.c_int, _vp, _vp, C.c_float, _vp,
@@ -379,3 +396,110 @@ def prefill_pass(layers, h, gamma1, gamma2, eps=1e-6, workspace=None, stream=Non
     _check(lib().pgq_q8_prefill_pass(layers.arr, L, _ptr(h), B, _ptr(gamma1), _ptr(gamma2), eps,
                                      _ptr(workspace), workspace.numel(), _stream(stream)))
     return workspace
+
+
+# ------------------------------------------------------------------ MoE
+def moe_router(R, n, logits=None, stream=None):
+    _need(R, torch.float32, "R")
+    E, cols = R.shape
+    _need(n, torch.float32, "n")
+    B = n.shape[0]
+    logits = torch.empty(B, E, dtype=torch.float32, device=R.device) if logits is None else logits
+    _need(logits, torch.float32, "logits", (B, E))
+    _check(lib().pgq_moe_router(_ptr(R), E, cols, _ptr(n), B, _ptr(logits), _stream(stream)))
+    return logits
+
+
+def moe_route_topk(logits, k, renorm=False, stream=None):
+    _need(logits, torch.float32, "logits")
+    B, E = logits.shape
+    sel = torch.empty(B, k, dtype=torch.int32, device=logits.device)
+    w = torch.empty(B, k, dtype=torch.float32, device=logits.device)
+    _check(lib().pgq_moe_route_topk(_ptr(logits), B, E, k, int(renorm), _ptr(sel), _ptr(w), _stream(stream)))
+    return sel, w
+
+
+def moe_group_gather(sel, E, x=None, xdiv=1, stream=None):
+    _need(sel, torch.int32, "sel")
+    B, k = sel.shape
+    dev = sel.device
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    entries = torch.empty(B * k, dtype=torch.int32, device=dev)
+    xg = None
+    n = 0
+    if x is not None:
+        _need(x, torch.float32, "x")
+        n = x.shape[1]
+        xg = torch.empty(B * k, n, dtype=torch.float32, device=dev)
+    _check(lib().pgq_moe_group_gather(_ptr(sel), B, k, E, _ptr(counts), _ptr(offsets), _ptr(entries), _ptr(x), n,
+                                      xdiv, _ptr(xg), _stream(stream)))
+    return counts, offsets, entries, xg
+
+
+def moe_experts_q8(codes, params, counts, offsets, entries, x, xdiv, y, epilogue="none", stream=None):
+    _need(codes, torch.int8, "codes")
+    E, rows, cols = codes.shape
+    _need(params, torch.float16, "params", (E, rows, cols // QBLOCK, 2))
+    _need(x, torch.float32, "x")
+    _need(y, torch.float32, "y")
+    _check(lib().pgq_moe_experts_q8(_ptr(codes), _ptr(params), E, rows, cols, _ptr(counts), _ptr(offsets),
+                                    _ptr(entries), entries.numel(), _ptr(x), xdiv, _ptr(y), _epi(epilogue),
+                                    _stream(stream)))
+    return y
+
+
+def moe_combine_rmsnorm(h, eo, w, gamma, eps=1e-6, o=None, y=None, inv=None, stream=None):
+    _need(h, torch.float32, "h")
+    B, n = h.shape
+    k = w.shape[1]
+    y = torch.empty_like(h) if y is None else y
+    _check(lib().pgq_moe_combine_rmsnorm(_ptr(h), _ptr(o), _ptr(eo), _ptr(w), k, _ptr(gamma), eps, B, n, _ptr(y),
+                                         _ptr(inv), _stream(stream)))
+    return y
+
+
+class MoeWeights:
+    """ctypes view of an MoE layer (keeps the tensors alive)."""
+
+    def __init__(self, router, up_codes, up_params, down_codes, down_params, k, renorm=False):
+        self.t = (router, up_codes, up_params, down_codes, down_params)
+        E, inter, hidden = up_codes.shape
+        _need(router, torch.float32, "router", (E, hidden))
+        _need(down_codes, torch.int8, "down_codes", (E, hidden, inter))
+        self.s = MoeLayer(router.data_ptr(), up_codes.data_ptr(), up_params.data_ptr(), down_codes.data_ptr(),
+                          down_params.data_ptr(), E, k, hidden, inter, int(renorm))
+
+
+def moe_layer_workspace(W, B, device="cuda"):
+    n = int(lib().pgq_moe_layer_workspace_bytes(C.byref(W.s), B))
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def moe_layer_taps(W, workspace, B):
+    off = (C.c_size_t * 9)()
+    _check(lib().pgq_moe_layer_layout(C.byref(W.s), B, off))
+    s = W.s
+    nb = B * s.k
+    spec = [("n", torch.float32, (B, s.hidden)), ("logits", torch.float32, (B, s.E)), ("sel", torch.int32, (B, s.k)),
+            ("w", torch.float32, (B, s.k)), ("counts", torch.int32, (s.E,)), ("offsets", torch.int32, (s.E + 1,)),
+            ("entries", torch.int32, (nb,)), ("u", torch.float32, (nb, s.inter)), ("eo", torch.float32, (nb, s.hidden))]
+    out = {}
+    for (name, dt, shape), o in zip(spec, off):
+        cnt = 1
+        for d in shape:
+            cnt *= d
+        out[name] = workspace[o:o + cnt * 4].view(dt).view(*shape)
+    return out
+
+
+def moe_prefill_layer(W, h, gamma1, gamma2, eps=1e-6, y=None, workspace=None, stream=None):
+    """One MoE layer over the pass h [B][hidden] (h updated in place); returns (y, workspace)."""
+    _need(h, torch.float32, "h")
+    B = h.shape[0]
+    y = torch.empty_like(h) if y is None else y
+    if workspace is None:
+        workspace = moe_layer_workspace(W, B, h.device)
+    _check(lib().pgq_moe_prefill_layer(C.byref(W.s), _ptr(h), B, _ptr(gamma1), _ptr(gamma2), eps, _ptr(y),
+                                       _ptr(workspace), workspace.numel(), _stream(stream)))
+    return y, workspace

@@ -438,6 +438,128 @@ int pgq_q8_prefill_pass(const pgq_q8_layer* layers, int L, float* h, int B, cons
   return PGQ_OK;
 }
 
+// ------------------------------------------------------------------ MoE
+int pgq_moe_router(const float* R, int E, int cols, const float* n, int B, float* logits, void* stream) {
+  REQUIRE(R && n && logits, PGQ_EINVAL, "moe_router: null pointer");
+  REQUIRE(E >= 1 && B >= 1 && cols >= 4 && cols % 4 == 0, PGQ_EINVAL, "moe_router: bad shape E=%d B=%d cols=%d", E, B,
+          cols);
+  REQUIRE(aligned16(n) && aligned4(R) && aligned4(logits), PGQ_EALIGN, "moe_router: n 16-byte, R/logits 4-byte");
+  REQUIRE(!overlaps(logits, (size_t)B * E * 4, n, (size_t)B * cols * 4), PGQ_EINVAL, "moe_router: logits overlap n");
+  GET_DEVICE(dev);
+  return launch_router(R, n, B, E, cols, logits, dev, as_stream(stream));
+}
+
+int pgq_moe_route_topk(const float* logits, int B, int E, int k, int renorm, int32_t* sel, float* w, void* stream) {
+  REQUIRE(logits && sel && w, PGQ_EINVAL, "moe_route_topk: null pointer");
+  REQUIRE(B >= 1 && E >= 1 && E <= 256 && k >= 1 && k <= E && k <= 32, PGQ_EINVAL,
+          "moe_route_topk: B=%d E=%d k=%d out of range", B, E, k);
+  REQUIRE(aligned4(logits) && aligned4(sel) && aligned4(w), PGQ_EALIGN, "moe_route_topk: 4-byte alignment");
+  GET_DEVICE(dev);
+  return launch_route_topk(logits, B, E, k, renorm, sel, w, as_stream(stream));
+}
+
+int pgq_moe_group_gather(const int32_t* sel, int B, int k, int E, int32_t* counts, int32_t* offsets, int32_t* entries,
+                         const float* x, int n, int xdiv, float* x_gathered, void* stream) {
+  REQUIRE(sel && counts && offsets && entries, PGQ_EINVAL, "moe_group_gather: null pointer");
+  REQUIRE(B >= 1 && k >= 1 && E >= 1, PGQ_EINVAL, "moe_group_gather: B=%d k=%d E=%d", B, k, E);
+  REQUIRE((size_t)B * k + 2 * (size_t)E + 1 <= 12288, PGQ_EUNSUPPORTED, "moe_group_gather: too many entries/experts");
+  REQUIRE(!x_gathered || (x && n >= 1 && xdiv >= 1), PGQ_EINVAL, "moe_group_gather: gather needs x, n, xdiv");
+  GET_DEVICE(dev);
+  return launch_group(sel, B * k, E, counts, offsets, entries, x, n, xdiv, x_gathered, as_stream(stream));
+}
+
+int pgq_moe_experts_q8(const int8_t* codes, const uint16_t* params, int E, int rows, int cols, const int32_t* counts,
+                       const int32_t* offsets, const int32_t* entries, int nentries, const float* x, int xdiv, float* y,
+                       int epilogue, void* stream) {
+  REQUIRE(codes && params && counts && offsets && entries && x && y, PGQ_EINVAL, "moe_experts_q8: null pointer");
+  REQUIRE(E >= 1 && rows >= 1 && cols >= 32 && cols % 32 == 0 && nentries >= 1 && xdiv >= 1, PGQ_EINVAL,
+          "moe_experts_q8: bad shape");
+  REQUIRE(cols <= 6144, PGQ_EUNSUPPORTED, "moe_experts_q8: cols=%d > 6144", cols);
+  REQUIRE(epilogue == PGQ_EPI_NONE || epilogue == PGQ_EPI_RELU2, PGQ_EINVAL, "moe_experts_q8: epilogue NONE or RELU2");
+  REQUIRE(aligned8(codes) && aligned4(params) && aligned16(x) && aligned4(y), PGQ_EALIGN,
+          "moe_experts_q8: codes 8-byte, params 4-byte, x 16-byte, y 4-byte aligned");
+  GET_DEVICE(dev);
+  MoeBankArgs a{codes, params, E, rows, cols, counts, offsets, entries, nentries, x, xdiv, y, epilogue};
+  return launch_moe_bank(a, dev, as_stream(stream));
+}
+
+int pgq_moe_combine_rmsnorm(float* h, const float* o, const float* eo, const float* w, int k, const float* gamma,
+                            float eps, int B, int n, float* y, float* inv_rms, void* stream) {
+  REQUIRE(h && eo && w && gamma && y, PGQ_EINVAL, "moe_combine_rmsnorm: null pointer");
+  REQUIRE(B >= 1 && k >= 1 && n >= 1, PGQ_EINVAL, "moe_combine_rmsnorm: bad shape");
+  REQUIRE(!overlaps(y, (size_t)B * n * 4, h, (size_t)B * n * 4), PGQ_EINVAL, "moe_combine_rmsnorm: y overlaps h");
+  GET_DEVICE(dev);
+  return launch_moe_combine(h, o, eo, w, k, gamma, eps, B, n, y, inv_rms, as_stream(stream));
+}
+
+namespace {
+struct MoeLayout {
+  size_t off[9];  // n, logits, sel, w, counts, offsets, entries, u, eo
+  size_t total;
+};
+MoeLayout moe_layout(const pgq_moe_layer& L, int B) {
+  MoeLayout M{};
+  const size_t nb = (size_t)B * L.k;
+  const size_t sz[9] = {(size_t)B * L.hidden * 4, (size_t)B * L.E * 4, nb * 4, nb * 4, (size_t)L.E * 4,
+                        ((size_t)L.E + 1) * 4, nb * 4, nb * L.inter * 4, nb * L.hidden * 4};
+  size_t o = 0;
+  for (int i = 0; i < 9; ++i) {
+    M.off[i] = o;
+    o = (o + sz[i] + 255) / 256 * 256;
+  }
+  M.total = o;
+  return M;
+}
+bool moe_layer_ok(const pgq_moe_layer* L, int B) {
+  return L && L->router && L->up_codes && L->up_params && L->down_codes && L->down_params && L->E >= 1 && L->k >= 1 &&
+         L->k <= L->E && L->hidden >= 32 && L->inter >= 32 && B >= 1 && B <= PGQ_PASS_BMAX;
+}
+}  // namespace
+
+size_t pgq_moe_layer_workspace_bytes(const pgq_moe_layer* layer, int B) {
+  if (!moe_layer_ok(layer, B)) return 0;
+  return moe_layout(*layer, B).total;
+}
+
+int pgq_moe_layer_layout(const pgq_moe_layer* layer, int B, size_t offsets[9]) {
+  REQUIRE(offsets && moe_layer_ok(layer, B), PGQ_EINVAL, "moe_layer_layout: bad arguments");
+  const MoeLayout M = moe_layout(*layer, B);
+  for (int i = 0; i < 9; ++i) offsets[i] = M.off[i];
+  return PGQ_OK;
+}
+
+int pgq_moe_prefill_layer(const pgq_moe_layer* L, float* h, int B, const float* gamma1, const float* gamma2, float eps,
+                          float* y, void* workspace, size_t workspace_bytes, void* stream) {
+  REQUIRE(moe_layer_ok(L, B) && h && gamma1 && gamma2 && y && workspace, PGQ_EINVAL, "moe_prefill_layer: bad arguments");
+  REQUIRE(((uintptr_t)workspace & 255) == 0, PGQ_EWORKSPACE, "moe_prefill_layer: workspace must be 256-byte aligned");
+  const MoeLayout M = moe_layout(*L, B);
+  REQUIRE(workspace_bytes >= M.total, PGQ_EWORKSPACE, "moe_prefill_layer: workspace needs %zu bytes", M.total);
+  REQUIRE(L->hidden % 32 == 0 && L->inter % 32 == 0, PGQ_EINVAL, "moe_prefill_layer: hidden/inter % 32");
+  char* w = static_cast<char*>(workspace);
+  float* n = reinterpret_cast<float*>(w + M.off[0]);
+  float* logits = reinterpret_cast<float*>(w + M.off[1]);
+  int32_t* sel = reinterpret_cast<int32_t*>(w + M.off[2]);
+  float* wts = reinterpret_cast<float*>(w + M.off[3]);
+  int32_t* counts = reinterpret_cast<int32_t*>(w + M.off[4]);
+  int32_t* offs = reinterpret_cast<int32_t*>(w + M.off[5]);
+  int32_t* ents = reinterpret_cast<int32_t*>(w + M.off[6]);
+  float* u = reinterpret_cast<float*>(w + M.off[7]);
+  float* eo = reinterpret_cast<float*>(w + M.off[8]);
+  int rc;
+  if ((rc = pgq_add_rmsnorm(h, nullptr, gamma1, eps, B, L->hidden, n, nullptr, stream))) return rc;
+  if ((rc = pgq_moe_router(L->router, L->E, L->hidden, n, B, logits, stream))) return rc;
+  if ((rc = pgq_moe_route_topk(logits, B, L->E, L->k, L->renorm, sel, wts, stream))) return rc;
+  if ((rc = pgq_moe_group_gather(sel, B, L->k, L->E, counts, offs, ents, nullptr, 0, 1, nullptr, stream))) return rc;
+  const int nent = B * L->k;
+  if ((rc = pgq_moe_experts_q8(L->up_codes, L->up_params, L->E, L->inter, L->hidden, counts, offs, ents, nent, n, L->k,
+                               u, PGQ_EPI_RELU2, stream)))
+    return rc;
+  if ((rc = pgq_moe_experts_q8(L->down_codes, L->down_params, L->E, L->hidden, L->inter, counts, offs, ents, nent, u, 1,
+                               eo, PGQ_EPI_NONE, stream)))
+    return rc;
+  return pgq_moe_combine_rmsnorm(h, nullptr, eo, wts, L->k, gamma2, eps, B, L->hidden, y, nullptr, stream);
+}
+
 int pgq_prefill_status(const void* workspace, void* stream) {
   REQUIRE(workspace, PGQ_EINVAL, "prefill_status: null workspace");
   GET_DEVICE(dev);

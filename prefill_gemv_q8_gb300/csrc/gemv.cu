@@ -63,26 +63,6 @@ __device__ __forceinline__ void group_sync(int group, int wpt) {
   }
 }
 
-// Butterfly reduce-scatter of N (power of two, <= 32) per-lane values: afterwards
-// lane l with l % (32/N) == 0 holds the warp total of value l / (32/N).
-template <int N>
-__device__ __forceinline__ float reduce_scatter(float (&v)[N], int lane) {
-#pragma unroll
-  for (int n = N, o = 16; n > 1; n >>= 1, o >>= 1) {
-    const bool up = (lane & o) != 0;
-#pragma unroll
-    for (int j = 0; j < n / 2; ++j) {
-      const float mine = up ? v[j + n / 2] : v[j];
-      const float other = up ? v[j] : v[j + n / 2];
-      v[j] = mine + __shfl_xor_sync(0xffffffffu, other, o);
-    }
-  }
-  float t = v[0];
-#pragma unroll
-  for (int o = 16 / N; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-  return t;
-}
-
 // Position of column c in the staged (permuted) input row: the EPL values a lane
 // reads in a chunk sit as EPL/4 float4 that consecutive lanes read side by side.
 template <int EPL>

@@ -71,4 +71,27 @@ int prefill_status_offset();
 int launch_prefill(const PrefillJob* jobs, int njobs, const float* X, int cols, int B, void* ws, size_t ws_bytes,
                    bool a_tmem, unsigned long long wait_limit_ns, const DeviceInfo& dev, cudaStream_t st);
 
+// ------------------------------------------------------------------ MoE
+struct MoeBankArgs {
+  const int8_t* codes;       // [E][rows][cols]
+  const uint16_t* params;    // [E][rows][cols/32][2]
+  int E, rows, cols;
+  const int32_t* counts;     // [E]
+  const int32_t* offsets;    // [E+1]
+  const int32_t* entries;    // grouped entries
+  int nentries;
+  const float* x;            // input rows
+  int xdiv;                  // input row of entry j = j / xdiv
+  float* y;                  // [entries][rows]
+  int epilogue;
+};
+int launch_router(const float* R, const float* n, int B, int E, int cols, float* logits, const DeviceInfo& dev,
+                  cudaStream_t st);
+int launch_route_topk(const float* logits, int B, int E, int k, int renorm, int32_t* sel, float* w, cudaStream_t st);
+int launch_group(const int32_t* sel, int n, int E, int32_t* counts, int32_t* offsets, int32_t* entries,
+                 const float* x, int xcols, int xdiv, float* xg, cudaStream_t st);
+int launch_moe_bank(const MoeBankArgs& a, const DeviceInfo& dev, cudaStream_t st);
+int launch_moe_combine(float* h, const float* o, const float* eo, const float* w, int k, const float* gamma, float eps,
+                       int B, int n, float* y, float* inv, cudaStream_t st);
+
 }  // namespace pgq

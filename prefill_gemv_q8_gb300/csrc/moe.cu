@@ -1,0 +1,450 @@
+// MoE layer pieces over a prefill pass of B positions: the f32 router projection,
+// softmax top-k with lower-id ties, per-expert grouping of the pass's (position,
+// slot) entries, the grouped q8 expert projections (each chosen expert's weights
+// streamed once for all of its entries) and the weighted combine fused into
+// add + RMSNorm.
+//
+// Prior art: nemotron_prefill.rs `pb_f32_mm` (router), `pb_route` (top-k, ties to
+// the lowest lane), `pb_lists` (per-expert ascending entry lists), `pb_q8_bank`
+// (workgroup per (row block, expert), x row of entry j is j / xdiv, output row is the
+// entry) and `pb_add_rms` with add = 2 (weighted sum of the slots, then the norm).
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace pgq {
+
+// ------------------------------------------------------------------ router
+// logits[b][e] = Σ_c R[e][c]·n[b][c].  Block = 8 warps = 8 experts; the block stages
+// up to 16 positions of n in shared memory, each warp keeps its expert row in
+// registers (cols/32 values per lane) and walks the staged positions.
+constexpr int RT_WARPS = 8;
+constexpr int RT_POS = 16;
+constexpr int RT_MAXV = 96;   // cols <= 32 * 96 = 3072
+
+__global__ void __launch_bounds__(RT_WARPS * 32)
+router_kernel(const float* __restrict__ R, const float* __restrict__ n, int B, int E, int cols,
+              float* __restrict__ logits) {
+  extern __shared__ __align__(16) float xs[];   // [RT_POS][cols]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * RT_WARPS + warp;
+  const int b0 = blockIdx.y * RT_POS;
+  const int nb = min(RT_POS, B - b0);
+  for (int i = threadIdx.x; i < nb * cols; i += blockDim.x) xs[i] = n[(size_t)b0 * cols + i];
+  __syncthreads();
+  if (e >= E) return;
+  float w[RT_MAXV];
+  const float* row = R + (size_t)e * cols;
+#pragma unroll
+  for (int i = 0; i < RT_MAXV; ++i) w[i] = (lane + 32 * i < cols) ? row[lane + 32 * i] : 0.f;
+  for (int b = 0; b < nb; ++b) {
+    const float* x = xs + (size_t)b * cols;
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < RT_MAXV; ++i)
+      if (lane + 32 * i < cols) acc = fmaf(w[i], x[lane + 32 * i], acc);
+    acc = warp_sum(acc);
+    if (lane == 0) logits[(size_t)(b0 + b) * E + e] = acc;
+  }
+}
+
+// ------------------------------------------------------------------ softmax top-k
+// One warp per position: E <= 32 * RK_MAXV logits; p = softmax(logits) with a
+// fixed-order sum; k rounds of (largest logit, lowest index) selection — the order
+// of the logits is the order of the probabilities — then w = p (or p / Σp).
+constexpr int RK_MAXV = 8;   // E <= 256
+
+__global__ void route_topk_kernel(const float* __restrict__ logits, int B, int E, int k, int renorm,
+                                  int32_t* __restrict__ sel, float* __restrict__ wout) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (warp >= B) return;
+  const float* l = logits + (size_t)warp * E;
+  float v[RK_MAXV];
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < RK_MAXV; ++i) {
+    const int e = lane + 32 * i;
+    const float x = e < E ? l[e] : -INFINITY;
+    v[i] = isnan(x) ? -INFINITY : x;   // a NaN logit is never preferred
+    m = fmaxf(m, v[i]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < RK_MAXV; ++i)
+    if (lane + 32 * i < E) sum += expf(v[i] - m);
+  sum = warp_sum(sum);
+  bool taken[RK_MAXV];
+#pragma unroll
+  for (int i = 0; i < RK_MAXV; ++i) taken[i] = false;
+  float psel = 0.f;   // lane s holds the probability of slot s
+  for (int s = 0; s < k; ++s) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < RK_MAXV; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !taken[i] && (v[i] > bv || (v[i] == bv && e < bi) || bi == 0x7fffffff)) {
+        bv = v[i];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    // bi is the same in every lane now
+#pragma unroll
+    for (int i = 0; i < RK_MAXV; ++i)
+      if (lane + 32 * i == bi) taken[i] = true;
+    if (lane == s) psel = expf(bv - m) / sum;
+    if (lane == 0) sel[(size_t)warp * k + s] = bi;
+  }
+  float den = 1.f;
+  if (renorm) {
+    float t = lane < k ? psel : 0.f;
+    // fixed order: slot 0 + slot 1 + ... (lane 0 gathers)
+    float acc = 0.f;
+    for (int s = 0; s < k; ++s) acc += __shfl_sync(0xffffffffu, t, s);
+    den = acc;
+  }
+  if (lane < k) wout[(size_t)warp * k + lane] = psel / den;
+}
+
+// ------------------------------------------------------------------ grouping
+// One block.  Entry j = b·k + s chose expert e = sel[j]; its place among expert e's
+// entries is the number of earlier entries j' < j with the same expert, so every
+// list is in ascending j (nemotron_prefill.rs `pb_lists`).  Ids outside [0, E) are
+// skipped (they belong to no list); entries past Σ counts are set to -1.
+constexpr int GR_THREADS = 1024;
+
+__global__ void __launch_bounds__(GR_THREADS)
+group_kernel(const int32_t* __restrict__ sel, int n, int E, int32_t* __restrict__ counts,
+             int32_t* __restrict__ offsets, int32_t* __restrict__ entries, const float* __restrict__ x, int xcols,
+             int xdiv, float* __restrict__ xg) {
+  extern __shared__ int sh[];
+  int* s_sel = sh;            // [n]
+  int* s_cnt = sh + n;        // [E]
+  int* s_off = s_cnt + E;     // [E + 1]
+  for (int i = threadIdx.x; i < n; i += blockDim.x) s_sel[i] = sel[i];
+  for (int i = threadIdx.x; i < E; i += blockDim.x) s_cnt[i] = 0;
+  __syncthreads();
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    const int e = s_sel[j];
+    if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int e = 0; e < E; ++e) {
+      s_off[e] = acc;
+      acc += s_cnt[e];
+    }
+    s_off[E] = acc;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) counts[e] = s_cnt[e];
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = s_off[e];
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    const int e = s_sel[j];
+    if (e < 0 || e >= E) continue;
+    int rank = 0;
+    for (int jj = 0; jj < j; ++jj) rank += (s_sel[jj] == e);
+    const int pos = s_off[e] + rank;
+    entries[pos] = j;
+  }
+  for (int i = s_off[E] + threadIdx.x; i < n; i += blockDim.x) entries[i] = -1;
+  if (xg) {
+    __syncthreads();
+    // gathered input rows in grouped order: xg[i] = x[entries[i] / xdiv]
+    const int total = s_off[E];
+    for (int q = threadIdx.x; q < total * xcols; q += blockDim.x) {
+      const int i = q / xcols, c = q - i * xcols;
+      xg[q] = x[(size_t)(entries[i] / xdiv) * xcols + c];
+    }
+  }
+}
+
+// ------------------------------------------------------------------ expert bank
+// A block task is (expert e, chunk of up to 8 of e's entries, block of 32 weight
+// rows).  The block stages the chunk's input rows (x[entry / xdiv]) in shared
+// memory when the (expert, chunk) changes; each of its 8 warps then streams 4 rows
+// of W_e over the whole row (8-byte code loads, 4 chunks of 256 columns per batch)
+// against every staged entry, reduces across lanes and writes y[entry][row].
+constexpr int MB_WARPS = 8;
+constexpr int MB_R = 4;                 // rows per warp
+constexpr int MB_ROWS = MB_WARPS * MB_R;
+constexpr int MB_ENT = 8;               // entries per chunk
+constexpr int MB_MAXE = 1024;
+
+struct MoeBank {
+  const uint8_t* codes;      // [E][rows][cols]
+  const uint32_t* params;    // [E][rows][cols/32]
+  int E, rows, cols, cols_pad, nchunks;
+  const int32_t* counts;
+  const int32_t* offsets;
+  const int32_t* entries;
+  int nentries;
+  const float* x;            // input rows, [*][cols]
+  int xdiv;
+  float* y;                  // [entries][rows]
+  int epilogue;
+};
+
+__device__ __forceinline__ int perm8(int c) {
+  const int ch = c >> 8, within = c & 255;
+  const int ln = within >> 3, t = within & 7;
+  return (ch << 8) + (t >> 2) * 128 + ln * 4 + (t & 3);
+}
+
+template <int NB, int MB_U>
+__device__ __forceinline__ void bank_task(const MoeBank& P, const float* xs, int e, int row0, const int* ent,
+                                          int nent, int lane) {
+  const size_t wbase = (size_t)e * P.rows;
+  const int cols = P.cols;
+  const int pcols = cols >> 5;
+  float2 acc[MB_R][NB];
+#pragma unroll
+  for (int r = 0; r < MB_R; ++r)
+#pragma unroll
+    for (int b = 0; b < NB; ++b) acc[r][b] = make_float2(0.f, 0.f);
+  const uint8_t* wr[MB_R];
+  const uint32_t* pr[MB_R];
+#pragma unroll
+  for (int r = 0; r < MB_R; ++r) {
+    const size_t row = wbase + (size_t)min(row0 + r, P.rows - 1);
+    wr[r] = P.codes + row * cols + lane * 8;
+    pr[r] = P.params + row * pcols + (lane >> 2);
+  }
+  for (int ch0 = 0; ch0 < P.nchunks; ch0 += MB_U) {
+    uint2 w[MB_R][MB_U];
+    uint32_t pp[MB_R][MB_U];
+#pragma unroll
+    for (int u = 0; u < MB_U; ++u) {
+      const int ch = ch0 + u;
+      if (ch < P.nchunks && ch * 256 + lane * 8 < cols) {
+#pragma unroll
+        for (int r = 0; r < MB_R; ++r) {
+          w[r][u] = ld_stream_u2(wr[r] + ch * 256);
+          pp[r][u] = ld_nc_u32(pr[r] + ch * 8);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < MB_U; ++u) {
+      const int ch = ch0 + u;
+      if (ch < P.nchunks && ch * 256 + lane * 8 < cols) {
+        float2 wv[MB_R][4];
+#pragma unroll
+        for (int r = 0; r < MB_R; ++r) {
+          float2 q[4];
+          s8x4_to_f32(w[r][u].x, q[0], q[1]);
+          s8x4_to_f32(w[r][u].y, q[2], q[3]);
+          const float2 so = h2_to_f2(pp[r][u]);
+          const float2 s2 = make_float2(so.x, so.x), o2 = make_float2(so.y, so.y);
+#pragma unroll
+          for (int t = 0; t < 4; ++t) wv[r][t] = ffma2(q[t], s2, o2);
+        }
+        const float* xc = xs + ch * 256 + lane * 4;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          const float4 a = *reinterpret_cast<const float4*>(xc + (size_t)b * P.cols_pad);
+          const float4 c = *reinterpret_cast<const float4*>(xc + (size_t)b * P.cols_pad + 128);
+          const float2 xv[4] = {make_float2(a.x, a.y), make_float2(a.z, a.w), make_float2(c.x, c.y),
+                                make_float2(c.z, c.w)};
+#pragma unroll
+          for (int r = 0; r < MB_R; ++r)
+#pragma unroll
+            for (int t = 0; t < 4; ++t) acc[r][b] = ffma2(wv[r][t], xv[t], acc[r][b]);
+        }
+      }
+    }
+  }
+  constexpr int N = MB_R * NB;
+  float v[N];
+#pragma unroll
+  for (int r = 0; r < MB_R; ++r)
+#pragma unroll
+    for (int b = 0; b < NB; ++b) v[r * NB + b] = acc[r][b].x + acc[r][b].y;
+  const float t = reduce_scatter<N>(v, lane);
+  if ((lane & (32 / N - 1)) == 0) {
+    const int idx = lane / (32 / N);
+    const int r = idx / NB, b = idx - (idx / NB) * NB;
+    const int row = row0 + r;
+    if (b < nent && row < P.rows) {
+      float o = t;
+      if (P.epilogue == PGQ_EPI_RELU2) {
+        o = fmaxf(o, 0.f);
+        o = o * o;
+      }
+      P.y[(size_t)ent[b] * P.rows + row] = o;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(MB_WARPS * 32, 1)
+moe_bank_kernel(const __grid_constant__ MoeBank P) {
+  extern __shared__ __align__(16) float xs[];   // [MB_ENT][cols_pad]
+  __shared__ int s_pre[MB_MAXE + 1];
+  __shared__ int s_ent[MB_ENT];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nblk = (P.rows + MB_ROWS - 1) / MB_ROWS;
+  // task prefix over experts (every block computes the same list): the counts are
+  // read in parallel, then a fixed-order scan in shared memory
+  for (int e = threadIdx.x; e < P.E; e += blockDim.x) s_pre[e + 1] = ((P.counts[e] + MB_ENT - 1) / MB_ENT) * nblk;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    s_pre[0] = 0;
+    for (int e = 0; e < P.E; ++e) s_pre[e + 1] += s_pre[e];
+  }
+  __syncthreads();
+  const int T = s_pre[P.E];
+  const int t0 = (int)((long long)blockIdx.x * T / gridDim.x);
+  const int t1 = (int)((long long)(blockIdx.x + 1) * T / gridDim.x);
+  int cur_e = -1, cur_c = -1, nent = 0;
+  int e = 0;
+  for (int t = t0; t < t1; ++t) {
+    while (e + 1 < P.E && s_pre[e + 1] <= t) ++e;
+    const int local = t - s_pre[e];
+    const int chunk = local / nblk, blk = local - chunk * nblk;
+    if (e != cur_e || chunk != cur_c) {
+      __syncthreads();
+      const int first = P.offsets[e] + chunk * MB_ENT;
+      nent = min(MB_ENT, P.counts[e] - chunk * MB_ENT);
+      if (threadIdx.x < MB_ENT) {
+        int j = 0;
+        if ((int)threadIdx.x < nent && first + (int)threadIdx.x < P.nentries) j = P.entries[first + threadIdx.x];
+        s_ent[threadIdx.x] = (j >= 0 && j < P.nentries) ? j : 0;
+      }
+      __syncthreads();
+      const int cols4 = P.cols >> 2;
+      for (int i = threadIdx.x; i < MB_ENT * cols4; i += blockDim.x) {
+        const int b = i / cols4, c4 = i - b * cols4;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (b < nent) v = reinterpret_cast<const float4*>(P.x + (size_t)(s_ent[b] / P.xdiv) * P.cols)[c4];
+        *reinterpret_cast<float4*>(xs + (size_t)b * P.cols_pad + perm8(c4 * 4)) = v;
+      }
+      __syncthreads();
+      cur_e = e;
+      cur_c = chunk;
+    }
+    const int row0 = blk * MB_ROWS + warp * MB_R;
+    // chunks per load batch shrink as the entries (accumulators) grow; more than 4
+    // entries run as two passes of 4 over the same rows (the second pass finds the
+    // rows in L2)
+    if (nent <= 1) bank_task<1, 4>(P, xs, e, row0, s_ent, nent, lane);
+    else if (nent <= 2) bank_task<2, 4>(P, xs, e, row0, s_ent, nent, lane);
+    else if (nent <= 4) bank_task<4, 2>(P, xs, e, row0, s_ent, nent, lane);
+    else {
+      bank_task<4, 2>(P, xs, e, row0, s_ent, 4, lane);
+      bank_task<4, 2>(P, xs + (size_t)4 * P.cols_pad, e, row0, s_ent + 4, nent - 4, lane);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ combine + norm
+// For each position b (nemotron_prefill.rs `pb_add_rms`, add = 2):
+//   h[b] += o[b] + Σ_s w[b][s]·eo[b·k+s]   (slots ascending; o may be null)
+//   y[b] = γ·h[b]/√(mean h² + eps)
+__global__ void __launch_bounds__(256)
+moe_combine_kernel(float* __restrict__ h, const float* __restrict__ o, const float* __restrict__ eo,
+                   const float* __restrict__ w, int k, const float* __restrict__ gamma, float eps, int n,
+                   float* __restrict__ y, float* __restrict__ inv_out) {
+  __shared__ float red[8];
+  const int b = blockIdx.x;
+  float* hb = h + (size_t)b * n;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < n; i += 256) {
+    float m = o ? o[(size_t)b * n + i] : 0.f;
+    for (int s = 0; s < k; ++s) m += w[(size_t)b * k + s] * eo[((size_t)b * k + s) * n + i];
+    const float v = hb[i] + m;
+    hb[i] = v;
+    ss += v * v;
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) t += red[i];
+  const float inv = rsqrtf(t / (float)n + eps);
+  if (inv_out && threadIdx.x == 0) inv_out[b] = inv;
+  for (int i = threadIdx.x; i < n; i += 256) y[(size_t)b * n + i] = gamma[i] * (hb[i] * inv);
+}
+
+// ------------------------------------------------------------------ launchers
+int launch_router(const float* R, const float* n, int B, int E, int cols, float* logits, const DeviceInfo& dev,
+                  cudaStream_t st) {
+  if (cols > 32 * RT_MAXV) return set_error(PGQ_EUNSUPPORTED, "router: cols=%d > %d", cols, 32 * RT_MAXV);
+  const size_t smem = (size_t)RT_POS * cols * sizeof(float);
+  if (smem > dev.smem_optin) return set_error(PGQ_EUNSUPPORTED, "router: %zu bytes of shared memory", smem);
+  cudaError_t e = cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return cuda_status(e);
+  dim3 grid((E + RT_WARPS - 1) / RT_WARPS, (B + RT_POS - 1) / RT_POS);
+  router_kernel<<<grid, RT_WARPS * 32, smem, st>>>(R, n, B, E, cols, logits);
+  return cuda_status(cudaGetLastError());
+}
+
+int launch_route_topk(const float* logits, int B, int E, int k, int renorm, int32_t* sel, float* w, cudaStream_t st) {
+  if (E > 32 * RK_MAXV || k > 32) return set_error(PGQ_EUNSUPPORTED, "route: E=%d or k=%d too large", E, k);
+  const int warps_per_block = 8;
+  route_topk_kernel<<<(B + warps_per_block - 1) / warps_per_block, warps_per_block * 32, 0, st>>>(logits, B, E, k,
+                                                                                                  renorm, sel, w);
+  return cuda_status(cudaGetLastError());
+}
+
+int launch_group(const int32_t* sel, int n, int E, int32_t* counts, int32_t* offsets, int32_t* entries,
+                 const float* x, int xcols, int xdiv, float* xg, cudaStream_t st) {
+  const size_t smem = (size_t)(n + 2 * E + 1) * sizeof(int);
+  if (smem > 48 * 1024) return set_error(PGQ_EUNSUPPORTED, "group: %d entries and %d experts too many", n, E);
+  group_kernel<<<1, GR_THREADS, smem, st>>>(sel, n, E, counts, offsets, entries, x, xcols, xdiv, xg);
+  return cuda_status(cudaGetLastError());
+}
+
+int launch_moe_bank(const MoeBankArgs& a, const DeviceInfo& dev, cudaStream_t st) {
+  if (a.E > MB_MAXE) return set_error(PGQ_EUNSUPPORTED, "expert bank: E=%d > %d", a.E, MB_MAXE);
+  MoeBank P;
+  P.codes = reinterpret_cast<const uint8_t*>(a.codes);
+  P.params = reinterpret_cast<const uint32_t*>(a.params);
+  P.E = a.E;
+  P.rows = a.rows;
+  P.cols = a.cols;
+  P.nchunks = (a.cols + 255) / 256;
+  P.cols_pad = P.nchunks * 256;
+  P.counts = a.counts;
+  P.offsets = a.offsets;
+  P.entries = a.entries;
+  P.nentries = a.nentries;
+  P.x = a.x;
+  P.xdiv = a.xdiv;
+  P.y = a.y;
+  P.epilogue = a.epilogue;
+  const size_t smem = (size_t)MB_ENT * P.cols_pad * sizeof(float);
+  if (smem + 8192 > dev.smem_optin) return set_error(PGQ_EUNSUPPORTED, "expert bank: cols=%d too large", a.cols);
+  cudaError_t e = cudaFuncSetAttribute(moe_bank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return cuda_status(e);
+  int occ = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, moe_bank_kernel, MB_WARPS * 32, smem) != cudaSuccess) {
+    cudaGetLastError();
+    occ = 1;
+  }
+  occ = std::max(1, std::min(occ, 2));
+  void* args[] = {&P};
+  return cuda_status(cudaLaunchKernel(reinterpret_cast<const void*>(moe_bank_kernel), dim3(dev.sms * occ),
+                                      dim3(MB_WARPS * 32), args, smem, st));
+}
+
+int launch_moe_combine(float* h, const float* o, const float* eo, const float* w, int k, const float* gamma, float eps,
+                       int B, int n, float* y, float* inv, cudaStream_t st) {
+  moe_combine_kernel<<<B, 256, 0, st>>>(h, o, eo, w, k, gamma, eps, n, y, inv);
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace pgq

@@ -149,3 +149,27 @@ def q8_layer(workload, layer, hidden, kv, inter, backend="numpy", device=None):
     """The six q8 projections of one decode layer: {slot: (codes, params)}."""
     return {s: q8_matrix(r, c, workload, q8_tensor_id(layer, s), backend, device)
             for s, (r, c) in q8_layer_shapes(hidden, kv, inter).items()}
+
+
+def q8_bank(E, rows, cols, workload, which, backend="numpy", device=None):
+    """Contiguous bank of E q8 matrices (codes [E][rows][cols], params
+    [E][rows][cols/32][2]); expert e drawn from seed (workload, expert_tensor_id(e, which))."""
+    if backend == "numpy":
+        cs, ps = zip(*[q8_matrix(rows, cols, workload, expert_tensor_id(e, which)) for e in range(E)])
+        return np.stack(cs), np.stack(ps)
+    import torch
+    codes = torch.empty((E, rows, cols), dtype=torch.int8, device=device)
+    params = torch.empty((E, rows, cols // QBLOCK, 2), dtype=torch.float16, device=device)
+    for e in range(E):
+        c, p = q8_matrix(rows, cols, workload, expert_tensor_id(e, which), "torch", device)
+        codes[e].copy_(c)
+        params[e].copy_(p)
+    return codes, params
+
+
+def moe_layer(workload, E, hidden, inter, backend="numpy", device=None):
+    """Router f32 [E][hidden] ~ N(0, 1/hidden) and the up / down expert banks."""
+    router = normal((E, hidden), 1.0 / np.sqrt(hidden), workload, T_ROUTER, backend, device)
+    up = q8_bank(E, inter, hidden, workload, "up", backend, device)
+    down = q8_bank(E, hidden, inter, workload, "down", backend, device)
+    return router, up, down
