@@ -257,16 +257,8 @@ class PrefillPass:
 
 def time_prefill(torch, P, steps, warmup, pk):
     st = torch.cuda.current_stream()
-    for _ in range(warmup):
-        P.step()
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(st)
-    for _ in range(steps):
-        P.step()
-    b.record(st)
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / steps
+    ms_api = time_loop(torch, P.step, steps, warmup)
+    ms = time_graph(torch, P.step, steps, warmup)
     # dominant kernel alone: the up projection (14336 x 4096, relu²), rotating layers
     up_bytes = P.I * P.H + P.I * (P.H // 32) * 4
     X = P.h0
@@ -288,14 +280,120 @@ def time_prefill(torch, P, steps, warmup, pk):
     tf = P.flops / (ms * 1e-3) / 1e12
     return {
         "workload": P.name, "metric": "positions/s", "value": round(P.B / (ms * 1e-3), 1),
-        "ms_per_pass": round(ms, 4), "weight_GBps": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm"], 4),
+        "ms_per_pass": round(ms, 4), "ms_per_pass_api": round(ms_api, 4),
+        "timed": "CUDA-graph replay of the pass call (ms_per_pass_api: direct calls, host launch cost included)",
+        "weight_GBps": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm"], 4),
         "tflops": round(tf, 1), "frac_of_bf16_tensor": round(tf / pk["bf16_sustained"], 4),
         "bound": "hbm", "weight_bytes_per_pass": P.step_bytes, "launches_per_pass": P.launches_per_step,
         "roofline": {"bound": "hbm", "kernel": "prefill_tc_kernel (up 14336x4096, relu², B=64) + X conversion",
                      "achieved": round(ach, 1), "peak": pk["hbm"], "unit": "GB/s", "frac": round(ach / pk["hbm"], 4),
                      "traffic": ncu_traffic("prefill_tc_up", PREFILL_FILES), "algorithmic_bytes_per_launch": up_bytes,
-                     "avg_launch_ms": round(k_ms, 5), "timed": "separate event loop over 32 up matrices"},
+                     "avg_launch_ms": round(k_ms, 5), "timed": "separate event loop over 32 up matrices, direct calls"},
     }
+
+
+def _events(torch, n):
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def time_loop(torch, fn, steps, warmup):
+    """Average ms per call of fn() over `steps` calls, CUDA events on the current stream."""
+    st = torch.cuda.current_stream()
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = _events(torch, 2)
+    a.record(st)
+    for _ in range(steps):
+        fn()
+    b.record(st)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def time_graph(torch, fn, steps, warmup):
+    """The same through one CUDA graph capturing fn() (launch overhead removed)."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return time_loop(torch, g.replay, steps, warmup)
+
+
+def bench_tiny_mlp(torch, pgq, synth, steps, warmup, pk):
+    c = synth.TINY_MLP
+    H, I, wl = c["hidden"], c["inter"], c["workload"]
+    h = synth.normal((H,), 1.0, wl, synth.T_X, "torch", "cuda")
+    g = synth.gamma(H, wl, backend="torch", device="cuda")
+    Wu = synth.f16_matrix(I, H, wl, synth.T_WUP, "torch", "cuda")
+    Wd = synth.f16_matrix(H, I, wl, synth.T_WDOWN, "torch", "cuda")
+    copies = [(Wu, Wd)] + [(Wu.clone(), Wd.clone()) for _ in range(63)]   # 64 x 4 MiB > 2 x L2
+    u = torch.empty(I, device="cuda")
+    y = torch.empty(H, device="cuda")
+    it = [0]
+
+    def step():
+        a, b = copies[it[0] % len(copies)]
+        it[0] += 1
+        pgq.mlp_f16_decode(h, a, b, g, 1e-6, u=u, y=y)
+
+    ms = time_loop(torch, step, steps * 4, warmup)
+    nbytes = 2 * H * I * 2
+    return {"workload": "tiny decode MLP block B=1 (hidden 512, inter 2048, f16)", "metric": "weight GB/s",
+            "value": round(nbytes / (ms * 1e-3) / 1e9, 1), "us_per_step": round(ms * 1e3, 2),
+            "weight_bytes": nbytes, "launches_per_step": 2, "frac_of_hbm": round(nbytes / (ms * 1e-3) / 1e9 / pk["hbm"], 4),
+            "note": "launch-latency bound (4 MiB is 0.6 us at HBM peak); weights rotate over 64 copies"}
+
+
+def bench_vocab(torch, pgq, synth, steps, warmup, pk):
+    c = synth.VOCAB
+    V, H, wl = c["vocab"], c["hidden"], c["workload"]
+    W = synth.f16_matrix(V, H, wl, synth.T_W, "torch", "cuda")
+    g = synth.gamma(H, wl, backend="torch", device="cuda")
+    out = {}
+    for B in (1, 8):
+        x = synth.normal((B, H), 1.0, wl, synth.T_X, "torch", "cuda")
+        ids = torch.empty(B, dtype=torch.int32, device="cuda")
+        ws = torch.empty(pgq.argmax_workspace_bytes(B), dtype=torch.uint8, device="cuda")
+        fn = lambda: pgq.gemv_f16_argmax(W, x, gamma=g, logits=False, workspace=ws, ids=ids)  # noqa: E731
+        ms = time_loop(torch, fn, max(5, steps // 2), warmup)
+        gbs = W.numel() * 2 / (ms * 1e-3) / 1e9
+        out[f"B{B}"] = {"workload": f"vocab head 262144 x 4096 f16, B={B}, fused RMSNorm + argmax",
+                        "metric": "weight GB/s", "value": round(gbs, 1), "us_per_step": round(ms * 1e3, 2),
+                        "frac_of_hbm": round(gbs / pk["hbm"], 4), "weight_bytes": W.numel() * 2,
+                        "launches_per_step": 1}
+    return out
+
+
+def bench_moe(torch, pgq, synth, steps, warmup, pk):
+    c = synth.MOE
+    E, H, I, B, k, wl = c["experts"], c["hidden"], c["inter"], c["B"], c["topk"], c["workload"]
+    router, up, down = synth.moe_layer(wl, E, H, I, "torch", "cuda")
+    h0 = synth.normal((B, H), 1.0, wl, synth.T_X, "torch", "cuda")
+    g1 = synth.gamma(H, wl, backend="torch", device="cuda")
+    g2 = synth.gamma(H, wl, synth.T_GAMMA2, "torch", "cuda")
+    Wm = pgq.MoeWeights(router, up[0], up[1], down[0], down[1], k)
+    h = h0.clone()
+    y = torch.empty_like(h0)
+    ws = pgq.moe_layer_workspace(Wm, B)
+
+    def step():
+        h.copy_(h0)
+        pgq.moe_prefill_layer(Wm, h, g1, g2, 1e-6, y=y, workspace=ws)
+
+    ms = time_loop(torch, step, steps, warmup)
+    ms_graph = time_graph(torch, step, steps, warmup)
+    taps = pgq.moe_layer_taps(Wm, ws, B)
+    touched = int((taps["counts"] > 0).sum().item())
+    per_expert = 2 * (I * H + I * (H // 32) * 4)
+    nbytes = touched * per_expert + E * H * 4
+    gbs = nbytes / (ms_graph * 1e-3) / 1e9
+    return {"workload": "MoE prefill layer B=64 (hidden 2688, 128 experts of 1856x2688 q8, top-6)",
+            "metric": "positions/s", "value": round(B / (ms_graph * 1e-3), 1), "ms_per_layer": round(ms_graph, 4),
+            "ms_per_layer_api": round(ms, 4), "touched_experts": touched, "weight_bytes": nbytes,
+            "weight_GBps": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm"], 4), "launches_per_step": 7,
+            "timed": "CUDA-graph replay of the layer call (ms_per_layer_api: direct calls)"}
 
 
 def time_e2e(torch, W, steps, warmup):
@@ -418,6 +516,11 @@ def main():
         line["workloads"] = {"prefill_pass": pre}
         del P
         torch.cuda.empty_cache()
+        line["workloads"]["moe_layer"] = bench_moe(torch, pgq, synth, max(5, args.steps // 5), args.warmup, pk)
+        torch.cuda.empty_cache()
+        line["workloads"]["vocab_head"] = bench_vocab(torch, pgq, synth, args.steps, args.warmup, pk)
+        torch.cuda.empty_cache()
+        line["workloads"]["tiny_mlp"] = bench_tiny_mlp(torch, pgq, synth, args.steps, args.warmup, pk)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_q8(Wcpu)
     if rank == 0:
