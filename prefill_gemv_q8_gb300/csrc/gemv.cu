@@ -35,24 +35,18 @@ constexpr int GV_WARPS = 8;
 constexpr int GV_THREADS = GV_WARPS * 32;
 
 // Compile-time shape of one kernel instance.
-//   EPL: weight elements a lane loads per row per chunk (one 16- or 8-byte load),
+//   EPL: weight elements a lane loads per row per chunk (one 16-byte load),
 //   CW:  columns per chunk (32 lanes x EPL),
 //   R:   rows per task (they share every staged-x read),
-//   U:   chunks per batch (loads a lane issues per row before using any of them).
+//   U:   chunks per step (one cp.async group per step).
 template <bool Q8, int NB>
 struct GvShape {
   static constexpr int R = NB <= 2 ? 2 : 4;
   static constexpr int U = NB <= 2 ? 4 : 2;
-  static constexpr int EPL = (Q8 && NB <= 2) ? 16 : 8;
+  static constexpr int EPL = Q8 ? 16 : 8;
   static constexpr int CW = 32 * EPL;
-};
-
-template <bool Q8, int NB>
-struct Slot {
-  static constexpr int R = GvShape<Q8, NB>::R, U = GvShape<Q8, NB>::U;
-  uint4 w[R][U];
-  uint32_t p[R][U];
-  int job, ch0, nch;   // job, first chunk of the batch, chunks of the batch this warp owns
+  // bytes of one step in a warp's ring: codes (16 per lane per row-chunk) + q8 params
+  static constexpr int STEP_BYTES = R * U * 32 * (16 + (Q8 ? 4 : 0));
 };
 
 __device__ __forceinline__ void group_sync(int group, int wpt) {
@@ -61,6 +55,19 @@ __device__ __forceinline__ void group_sync(int group, int wpt) {
   } else {
     asm volatile("bar.sync %0, %1;" ::"r"(group + 1), "r"(wpt * 32) : "memory");
   }
+}
+
+// Asynchronous global → shared copies (issued per lane, completed per group).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Position of column c in the staged (permuted) input row: the EPL values a lane
@@ -73,15 +80,17 @@ __device__ __forceinline__ int perm_col(int c) {
   return ch * CW + (t >> 2) * 128 + ln * 4 + (t & 3);
 }
 
-template <bool Q8, int NB, bool ARGMAX>
-__global__ void __launch_bounds__(GV_THREADS, NB <= 2 ? 2 : 1)
+template <bool Q8, int NB, int ST, bool ARGMAX>
+__global__ void __launch_bounds__(GV_THREADS, 1)
 gemv_kernel(const __grid_constant__ GvParams P) {
-  using S = GvShape<Q8, NB>;
-  constexpr int R = S::R, U = S::U, EPL = S::EPL, CW = S::CW;
+  using SH = GvShape<Q8, NB>;
+  constexpr int R = SH::R, U = SH::U, EPL = SH::EPL, CW = SH::CW;
   constexpr int ESZ = Q8 ? 1 : 2;
+  constexpr int CODE_BYTES = R * U * 32 * 16;   // codes part of a step
   extern __shared__ __align__(16) float smem[];
   float* xs = smem;                                           // [ninputs][NB][cols_pad]
   float* red = xs + (size_t)P.ninputs * NB * P.cols_pad;      // [groups][2][wpt][R*NB]
+  uint8_t* rings = reinterpret_cast<uint8_t*>(red + (size_t)P.groups * 2 * P.wpt * R * NB);   // [warps][ST][step]
   __shared__ float s_inv[MAX_INPUTS * NB];
   __shared__ float s_red[GV_WARPS];
   __shared__ float s_gbv[GV_WARPS * NB];
@@ -130,60 +139,56 @@ gemv_kernel(const __grid_constant__ GvParams P) {
   __syncthreads();
 
   // ---- this warp's share: tasks gg, gg+TG, ...; within a task the chunks
-  //      [wg*cpw, (wg+1)*cpw) in batches of U
+  //      [wg*cpw, (wg+1)*cpw) in steps of U
   const int wpt = P.wpt, groups = P.groups, cpw = P.cpw;
   const int group = warp / wpt, wg = warp - group * wpt;
   const bool active_warp = group < groups;
   const int gg = blockIdx.x * groups + group;
   const int TG = gridDim.x * groups;
   const int my_tasks = (active_warp && gg < P.ntasks) ? (P.ntasks - 1 - gg) / TG + 1 : 0;
-  const int nbt = (cpw + U - 1) / U;               // batches per task
+  const int nbt = (cpw + U - 1) / U;               // steps per task
   const int nsteps = my_tasks * nbt;
   const int ch_begin = wg * cpw;
   const int ch_end = min(ch_begin + cpw, P.nchunks);
   float* gred = red + (size_t)(active_warp ? group : 0) * 2 * wpt * (R * NB);
   const size_t row_bytes = (size_t)cols * ESZ;
   const int pcols = cols >> 5;
+  uint8_t* ring = rings + (size_t)warp * ST * SH::STEP_BYTES;
+  const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
 
-  // incremental step -> (task, batch) walkers for the fetch and compute sides
+  // walkers step -> (task, step-in-task) for the issue side and the compute side
   int f_i = 0, f_tb = 0, f_job = 0;
   int c_i = 0, c_tb = 0, c_job = 0;
 
-  auto fetch = [&](Slot<Q8, NB>& sl, int s) {
-    sl.nch = 0;
-    if (s >= nsteps) return;
-    const int task = gg + f_i * TG;
+  // Issue the cp.async copies of step s into ring slot s % ST (one group per step).
+  auto issue = [&](int s) {
+    if (s < nsteps) {
+      const int task = gg + f_i * TG;
 #pragma unroll 1
-    while (f_job + 1 < P.njobs && task >= P.job[f_job + 1].task_begin) ++f_job;
-    const GvJob& J = P.job[f_job];
-    sl.job = f_job;
-    sl.ch0 = ch_begin + f_tb * U;
-    sl.nch = max(0, min(U, ch_end - sl.ch0));
-    const int row0 = (task - J.task_begin) * R;
-    const int col0 = sl.ch0 * CW + lane * EPL;
+      while (f_job + 1 < P.njobs && task >= P.job[f_job + 1].task_begin) ++f_job;
+      const GvJob& J = P.job[f_job];
+      const int ch0 = ch_begin + f_tb * U;
+      const int nch = min(U, ch_end - ch0);
+      const int row0 = (task - J.task_begin) * R;
+      const int col0 = ch0 * CW + lane * EPL;
+      const uint32_t slot = ring_s + (uint32_t)((s % ST) * SH::STEP_BYTES);
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const size_t row = (size_t)min(row0 + r, J.rows - 1);
-      const uint8_t* wp = J.w + row * row_bytes + (size_t)col0 * ESZ;
-      const uint32_t* pp = Q8 ? J.params + row * pcols + (col0 >> 5) : nullptr;
+      for (int r = 0; r < R; ++r) {
+        const size_t row = (size_t)min(row0 + r, J.rows - 1);
+        const uint8_t* wp = J.w + row * row_bytes + (size_t)col0 * ESZ;
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (u < sl.nch && col0 + u * CW < cols) {
-          if constexpr (Q8) {
-            if constexpr (EPL == 16) {
-              sl.w[r][u] = ld_stream_u4(wp + u * CW);
-            } else {
-              const uint2 v = ld_stream_u2(wp + u * CW);
-              sl.w[r][u] = make_uint4(v.x, v.y, 0u, 0u);
-            }
-            sl.p[r][u] = ld_nc_u32(pp + u * (CW >> 5));
-          } else {
-            sl.w[r][u] = ld_stream_u4(wp + u * CW * 2);
+        for (int u = 0; u < U; ++u) {
+          if (u < nch && col0 + u * CW < cols) {
+            cp_async16(slot + (uint32_t)(((r * U + u) * 32 + lane) * 16), wp + (size_t)u * CW * ESZ);
+            if constexpr (Q8)
+              cp_async4(slot + CODE_BYTES + (uint32_t)(((r * U + u) * 32 + lane) * 4),
+                        J.params + row * pcols + ((col0 + u * CW) >> 5));
           }
         }
       }
+      if (++f_tb == nbt) { f_tb = 0; ++f_i; }
     }
-    if (++f_tb == nbt) { f_tb = 0; ++f_i; }
+    cp_async_commit();
   };
 
   float2 acc[R][NB];
@@ -197,45 +202,84 @@ gemv_kernel(const __grid_constant__ GvParams P) {
 #pragma unroll
   for (int b = 0; b < NB; ++b) { best_v[b] = ARGMAX_FLOOR; best_i[b] = 0; }
 
-  auto compute = [&](const Slot<Q8, NB>& sl) {
-    const float* xin = xs + (size_t)P.job[sl.job].input * NB * cols_pad + lane * 4;
+  // With one position and one step per task, this lane's input values never change
+  // between tasks of the same input: keep them in registers.
+  constexpr bool XREG_OK = (NB == 1);
+  const bool xreg = XREG_OK && nbt == 1;
+  float2 xr[XREG_OK ? U : 1][EPL / 2];
+  int xr_input = -1;
+
+  auto compute = [&](int s) {
+    const int task = gg + c_i * TG;
+#pragma unroll 1
+    while (c_job + 1 < P.njobs && task >= P.job[c_job + 1].task_begin) ++c_job;
+    const int input = P.job[c_job].input;
+    const int ch0 = ch_begin + c_tb * U;
+    const int nch = min(U, ch_end - ch0);
+    const float* xin = xs + (size_t)input * NB * cols_pad + lane * 4;
+    const uint8_t* slot = ring + (s % ST) * SH::STEP_BYTES;
+    if constexpr (XREG_OK) {
+      if (xreg && input != xr_input) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const float* xc = xin + (size_t)(ch0 + u) * CW;
+#pragma unroll
+          for (int k = 0; k < EPL / 4; ++k) {
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (u < nch) a = *reinterpret_cast<const float4*>(xc + k * 128);
+            xr[u][2 * k] = make_float2(a.x, a.y);
+            xr[u][2 * k + 1] = make_float2(a.z, a.w);
+          }
+        }
+        xr_input = input;
+      }
+    }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int ch = sl.ch0 + u;
-      if (u < sl.nch && ch * CW + lane * EPL < cols) {
+      const int ch = ch0 + u;
+      if (u < nch && ch * CW + lane * EPL < cols) {
         float2 wv[R][EPL / 2];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
+          const uint4 cw = *reinterpret_cast<const uint4*>(slot + ((r * U + u) * 32 + lane) * 16);
           if constexpr (Q8) {
-            const float2 so = h2_to_f2(sl.p[r][u]);
+            const uint32_t pw = *reinterpret_cast<const uint32_t*>(slot + CODE_BYTES + ((r * U + u) * 32 + lane) * 4);
+            const float2 so = h2_to_f2(pw);
             const float2 s2 = make_float2(so.x, so.x), o2 = make_float2(so.y, so.y);
-            const uint32_t words[4] = {sl.w[r][u].x, sl.w[r][u].y, sl.w[r][u].z, sl.w[r][u].w};
+            const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
-            for (int k = 0; k < EPL / 4; ++k) {
+            for (int k = 0; k < 4; ++k) {
               float2 lo, hi;
               s8x4_to_f32(words[k], lo, hi);
               wv[r][2 * k] = ffma2(lo, s2, o2);
               wv[r][2 * k + 1] = ffma2(hi, s2, o2);
             }
           } else {
-            wv[r][0] = h2_to_f2(sl.w[r][u].x); wv[r][1] = h2_to_f2(sl.w[r][u].y);
-            wv[r][2] = h2_to_f2(sl.w[r][u].z); wv[r][3] = h2_to_f2(sl.w[r][u].w);
+            wv[r][0] = h2_to_f2(cw.x); wv[r][1] = h2_to_f2(cw.y);
+            wv[r][2] = h2_to_f2(cw.z); wv[r][3] = h2_to_f2(cw.w);
           }
         }
-        const float* xc = xin + ch * CW;
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          float2 xv[EPL / 2];
-#pragma unroll
-          for (int k = 0; k < EPL / 4; ++k) {
-            const float4 a = *reinterpret_cast<const float4*>(xc + (size_t)b * cols_pad + k * 128);
-            xv[2 * k] = make_float2(a.x, a.y);
-            xv[2 * k + 1] = make_float2(a.z, a.w);
-          }
+        if (XREG_OK && xreg) {
 #pragma unroll
           for (int r = 0; r < R; ++r)
 #pragma unroll
-            for (int t = 0; t < EPL / 2; ++t) acc[r][b] = ffma2(wv[r][t], xv[t], acc[r][b]);
+            for (int t = 0; t < EPL / 2; ++t) acc[r][0] = ffma2(wv[r][t], xr[XREG_OK ? u : 0][t], acc[r][0]);
+        } else {
+          const float* xc = xin + (size_t)ch * CW;
+#pragma unroll
+          for (int b = 0; b < NB; ++b) {
+            float2 xv[EPL / 2];
+#pragma unroll
+            for (int k = 0; k < EPL / 4; ++k) {
+              const float4 a = *reinterpret_cast<const float4*>(xc + (size_t)b * cols_pad + k * 128);
+              xv[2 * k] = make_float2(a.x, a.y);
+              xv[2 * k + 1] = make_float2(a.z, a.w);
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+              for (int t = 0; t < EPL / 2; ++t) acc[r][b] = ffma2(wv[r][t], xv[t], acc[r][b]);
+          }
         }
       }
     }
@@ -297,24 +341,21 @@ gemv_kernel(const __grid_constant__ GvParams P) {
     rbuf ^= 1;
   };
 
-  Slot<Q8, NB> ring[2];
-  fetch(ring[0], 0);
-  fetch(ring[1], 1);
-  for (int s0 = 0; s0 < nsteps; s0 += 2) {
+  // ---- the pipeline: ST-1 steps in flight ahead of the one being computed
 #pragma unroll
-    for (int d = 0; d < 2; ++d) {
-      const int s = s0 + d;
-      if (s < nsteps) {
-        compute(ring[d]);
-        fetch(ring[d], s + 2);
-        if (++c_tb == nbt) {
-          c_tb = 0;
-          finish_task();
-          ++c_i;
-        }
-      }
+  for (int i = 0; i < ST - 1; ++i) issue(i);
+  for (int s = 0; s < nsteps; ++s) {
+    cp_async_wait<ST - 2>();
+    compute(s);
+    __syncwarp();
+    issue(s + ST - 1);
+    if (++c_tb == nbt) {
+      c_tb = 0;
+      finish_task();
+      ++c_i;
     }
   }
+  cp_async_wait<0>();
 
   if constexpr (ARGMAX) {
     __syncthreads();
@@ -360,40 +401,42 @@ namespace {
 using KernelFn = void (*)(GvParams);
 
 template <bool Q8, int NB, bool ARGMAX>
-constexpr KernelFn pick_kernel() {
-  return reinterpret_cast<KernelFn>(&gemv_kernel<Q8, NB, ARGMAX>);
+KernelFn pick(int st) {
+  return st >= 4 ? reinterpret_cast<KernelFn>(&gemv_kernel<Q8, NB, 4, ARGMAX>)
+                 : reinterpret_cast<KernelFn>(&gemv_kernel<Q8, NB, 2, ARGMAX>);
 }
 
-// (R, U, CW) of the instance launch_gemv will pick
-void shape_of(bool q8, int nb, int* R, int* U, int* CW) {
-  *R = nb <= 2 ? 2 : 4;
-  *U = nb <= 2 ? 4 : 2;
-  *CW = 32 * ((q8 && nb <= 2) ? 16 : 8);
-}
-
-KernelFn kernel_for(bool q8, int nb, bool argmax) {
+KernelFn kernel_for(bool q8, int nb, bool argmax, int st) {
   if (q8) {
     switch (nb) {
-      case 1: return pick_kernel<true, 1, false>();
-      case 2: return pick_kernel<true, 2, false>();
-      case 4: return pick_kernel<true, 4, false>();
-      default: return pick_kernel<true, 8, false>();
+      case 1: return pick<true, 1, false>(st);
+      case 2: return pick<true, 2, false>(st);
+      case 4: return pick<true, 4, false>(st);
+      default: return pick<true, 8, false>(st);
     }
   }
   if (argmax) {
     switch (nb) {
-      case 1: return pick_kernel<false, 1, true>();
-      case 2: return pick_kernel<false, 2, true>();
-      case 4: return pick_kernel<false, 4, true>();
-      default: return pick_kernel<false, 8, true>();
+      case 1: return pick<false, 1, true>(st);
+      case 2: return pick<false, 2, true>(st);
+      case 4: return pick<false, 4, true>(st);
+      default: return pick<false, 8, true>(st);
     }
   }
   switch (nb) {
-    case 1: return pick_kernel<false, 1, false>();
-    case 2: return pick_kernel<false, 2, false>();
-    case 4: return pick_kernel<false, 4, false>();
-    default: return pick_kernel<false, 8, false>();
+    case 1: return pick<false, 1, false>(st);
+    case 2: return pick<false, 2, false>(st);
+    case 4: return pick<false, 4, false>(st);
+    default: return pick<false, 8, false>(st);
   }
+}
+
+// (R, U, CW, bytes of a ring step) of the instance launch_gemv will pick
+void shape_of(bool q8, int nb, int* R, int* U, int* CW, int* step_bytes) {
+  *R = nb <= 2 ? 2 : 4;
+  *U = nb <= 2 ? 4 : 2;
+  *CW = 32 * (q8 ? 16 : 8);
+  *step_bytes = *R * *U * 32 * (16 + (q8 ? 4 : 0));
 }
 
 int round_nb(int B) { return B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : 8; }
@@ -484,11 +527,11 @@ size_t gemv_argmax_workspace_bytes(int B, const DeviceInfo& dev) {
 
 int launch_gemv(GvParams& P, bool q8, bool argmax, const DeviceInfo& dev, cudaStream_t st) {
   const int nb = round_nb(P.B);
-  int R, U, CW;
-  shape_of(q8, nb, &R, &U, &CW);
+  int R, U, CW, step_bytes;
+  shape_of(q8, nb, &R, &U, &CW, &step_bytes);
   P.nchunks = (P.cols + CW - 1) / CW;
   P.cols_pad = P.nchunks * CW;
-  // enough warps per task that each owns at most U chunks (one batch), up to 8
+  // enough warps per task that each owns at most U chunks (one step), up to 8
   int wpt = 1;
   while (wpt < GV_WARPS && (P.nchunks + wpt - 1) / wpt > U) wpt *= 2;
   P.wpt = wpt;
@@ -500,9 +543,17 @@ int launch_gemv(GvParams& P, bool q8, bool argmax, const DeviceInfo& dev, cudaSt
     t += (P.job[j].rows + R - 1) / R;
   }
   P.ntasks = t;
-  const size_t smem = ((size_t)P.ninputs * nb * P.cols_pad + (size_t)P.groups * 2 * wpt * R * nb) * sizeof(float);
-  if (smem + 2048 > dev.smem_optin) return set_error(PGQ_EUNSUPPORTED, "staged input needs %zu bytes of shared memory", smem);
-  KernelFn fn = kernel_for(q8, nb, argmax);
+  const size_t fixed = ((size_t)P.ninputs * nb * P.cols_pad + (size_t)P.groups * 2 * wpt * R * nb) * sizeof(float);
+  // the deepest ring (4 or 2 steps per warp) that fits next to the staged input
+  int stages = 4;
+  size_t smem = fixed + (size_t)GV_WARPS * stages * step_bytes;
+  if (smem + 2048 > dev.smem_optin) {
+    stages = 2;
+    smem = fixed + (size_t)GV_WARPS * stages * step_bytes;
+  }
+  if (smem + 2048 > dev.smem_optin)
+    return set_error(PGQ_EUNSUPPORTED, "staged input needs %zu bytes of shared memory", smem);
+  KernelFn fn = kernel_for(q8, nb, argmax, stages);
   if (cudaError_t e = allow_smem(fn, smem); e != cudaSuccess)
     return set_error(PGQ_ECUDA, "gemv: shared-memory limit %zu: %s", smem, cudaGetErrorString(e));
   int grid;
