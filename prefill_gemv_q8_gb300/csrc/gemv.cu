@@ -31,7 +31,7 @@
 
 namespace pgq {
 
-constexpr int GV_WARPS = 8;
+constexpr int GV_WARPS = 16;
 constexpr int GV_THREADS = GV_WARPS * 32;
 
 // Compile-time shape of one kernel instance.
@@ -41,8 +41,8 @@ constexpr int GV_THREADS = GV_WARPS * 32;
 //   U:   chunks per step (one cp.async group per step).
 template <bool Q8, int NB>
 struct GvShape {
-  static constexpr int R = NB <= 2 ? 2 : 4;
-  static constexpr int U = NB <= 2 ? 4 : 2;
+  static constexpr int R = 2;
+  static constexpr int U = 2;
   static constexpr int EPL = Q8 ? 16 : 8;
   static constexpr int CW = 32 * EPL;
   // bytes of one step in a warp's ring: codes (16 per lane per row-chunk) + q8 params
@@ -84,6 +84,7 @@ template <bool Q8, int NB, int ST, bool ARGMAX>
 __global__ void __launch_bounds__(GV_THREADS, 1)
 gemv_kernel(const __grid_constant__ GvParams P) {
   using SH = GvShape<Q8, NB>;
+  static_assert(GV_WARPS <= 16, "named barriers");
   constexpr int R = SH::R, U = SH::U, EPL = SH::EPL, CW = SH::CW;
   constexpr int ESZ = Q8 ? 1 : 2;
   constexpr int CODE_BYTES = R * U * 32 * 16;   // codes part of a step
@@ -191,11 +192,15 @@ gemv_kernel(const __grid_constant__ GvParams P) {
     cp_async_commit();
   };
 
-  float2 acc[R][NB];
+  // at one position, two accumulators per row halve the dependent FMA chains
+  constexpr int NA = NB == 1 ? 2 : 1;
+  float2 acc[R][NB][NA];
 #pragma unroll
   for (int r = 0; r < R; ++r)
 #pragma unroll
-    for (int b = 0; b < NB; ++b) acc[r][b] = make_float2(0.f, 0.f);
+    for (int b = 0; b < NB; ++b)
+#pragma unroll
+      for (int q = 0; q < NA; ++q) acc[r][b][q] = make_float2(0.f, 0.f);
 
   float best_v[NB];
   int best_i[NB];
@@ -263,7 +268,8 @@ gemv_kernel(const __grid_constant__ GvParams P) {
 #pragma unroll
           for (int r = 0; r < R; ++r)
 #pragma unroll
-            for (int t = 0; t < EPL / 2; ++t) acc[r][0] = ffma2(wv[r][t], xr[XREG_OK ? u : 0][t], acc[r][0]);
+            for (int t = 0; t < EPL / 2; ++t)
+              acc[r][0][t % NA] = ffma2(wv[r][t], xr[XREG_OK ? u : 0][t], acc[r][0][t % NA]);
         } else {
           const float* xc = xin + (size_t)ch * CW;
 #pragma unroll
@@ -278,7 +284,7 @@ gemv_kernel(const __grid_constant__ GvParams P) {
 #pragma unroll
             for (int r = 0; r < R; ++r)
 #pragma unroll
-              for (int t = 0; t < EPL / 2; ++t) acc[r][b] = ffma2(wv[r][t], xv[t], acc[r][b]);
+              for (int t = 0; t < EPL / 2; ++t) acc[r][b][t % NA] = ffma2(wv[r][t], xv[t], acc[r][b][t % NA]);
           }
         }
       }
@@ -298,8 +304,12 @@ gemv_kernel(const __grid_constant__ GvParams P) {
     for (int r = 0; r < R; ++r)
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
-        v[r * NB + b] = acc[r][b].x + acc[r][b].y;
-        acc[r][b] = make_float2(0.f, 0.f);
+        float2 a = acc[r][b][0];
+#pragma unroll
+        for (int q = 1; q < NA; ++q) a = fadd2(a, acc[r][b][q]);
+        v[r * NB + b] = a.x + a.y;
+#pragma unroll
+        for (int q = 0; q < NA; ++q) acc[r][b][q] = make_float2(0.f, 0.f);
       }
     const float t = reduce_scatter<N>(v, lane);
     float* buf = gred + (size_t)rbuf * wpt * N;
@@ -433,8 +443,9 @@ KernelFn kernel_for(bool q8, int nb, bool argmax, int st) {
 
 // (R, U, CW, bytes of a ring step) of the instance launch_gemv will pick
 void shape_of(bool q8, int nb, int* R, int* U, int* CW, int* step_bytes) {
-  *R = nb <= 2 ? 2 : 4;
-  *U = nb <= 2 ? 4 : 2;
+  (void)nb;
+  *R = 2;
+  *U = 2;
   *CW = 32 * (q8 ? 16 : 8);
   *step_bytes = *R * *U * 32 * (16 + (q8 ? 4 : 0));
 }
