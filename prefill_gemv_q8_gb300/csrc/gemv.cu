@@ -537,6 +537,10 @@ size_t gemv_argmax_workspace_bytes(int B, const DeviceInfo& dev) {
 }
 
 int launch_gemv(GvParams& P, bool q8, bool argmax, const DeviceInfo& dev, cudaStream_t st) {
+  {
+    const int rc = launch_gemv_tma(P, q8, argmax, dev, st);
+    if (rc != PGQ_EUNSUPPORTED) return rc;
+  }
   const int nb = round_nb(P.B);
   int R, U, CW, step_bytes;
   shape_of(q8, nb, &R, &U, &CW, &step_bytes);

@@ -1,0 +1,456 @@
+// Decode projections fed by TMA bulk copies: the weights of SR consecutive rows are
+// one contiguous span of codes (and one of (scale, offset) pairs), so a single
+// thread streams whole stages of rows into a ring in shared memory with
+// cp.async.bulk, and all 16 warps of the block only read shared memory and compute.
+//
+// Stage = SR rows x all columns (~32 KB).  Warp w takes a pair of rows (2·(w / QW))
+// and the QW-th share of the chunks (QW = 32 / SR column shares), 16-byte reads per
+// lane; at one position its input values live in registers for the whole kernel.
+// Per stage the partial dot products are reduced across lanes (butterfly) and
+// across the QW column shares (shared memory, fixed order), then the epilogue is
+// applied and rows are stored.  The block barrier that ends a stage also frees its
+// ring slot, and thread 0 immediately refills it with the stage NST tasks ahead.
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.cuh"
+#include "tc.cuh"
+
+namespace pgq {
+
+constexpr int GT_WARPS = 16;
+constexpr int GT_THREADS = GT_WARPS * 32;
+constexpr int GT_STAGE_MAX = 37 * 1024;   // bytes of one ring stage (codes + params)
+constexpr int GT_NST = 4;                  // ring stages
+
+// Device status word of the TMA decode kernels: PGQ_ETIMEOUT after an expired wait.
+__device__ int g_decode_status;
+
+struct GtParams {
+  const uint8_t* w[PGQ_MULTI_MAX];
+  const uint8_t* p[PGQ_MULTI_MAX];
+  float* y[PGQ_MULTI_MAX];
+  const float* residual[PGQ_MULTI_MAX];
+  int rows[PGQ_MULTI_MAX], input[PGQ_MULTI_MAX], epi[PGQ_MULTI_MAX], task_begin[PGQ_MULTI_MAX + 1];
+  GvInput in[MAX_INPUTS];
+  int njobs, ninputs, B, cols, cols_pad, nchunks;
+  int SR, QW, cpw;
+  int code_bytes, stage_bytes;   // per stage: SR rows of codes, then SR rows of params
+  int ntasks;
+  float eps;
+  float* part_val;
+  int* part_idx;
+  unsigned* ticket;
+  int32_t* ids;
+  unsigned long long wait_limit_ns;
+};
+
+template <int EPL>
+__device__ __forceinline__ int gt_perm(int c) {
+  constexpr int CW = 32 * EPL;
+  const int ch = c / CW, within = c - ch * CW;
+  const int ln = within / EPL, t = within - ln * EPL;
+  return ch * CW + (t >> 2) * 128 + ln * 4 + (t & 3);
+}
+
+__device__ __forceinline__ int gt_job(const GtParams& P, int t) {
+  int j = 0;
+#pragma unroll 1
+  while (j + 1 < P.njobs && t >= P.task_begin[j + 1]) ++j;
+  return j;
+}
+
+template <bool Q8, int NB, bool ARGMAX>
+__global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_constant__ GtParams P) {
+  constexpr int EPL = Q8 ? 16 : 8;
+  constexpr int CW = 32 * EPL;
+  constexpr int ESZ = Q8 ? 1 : 2;
+  constexpr int MAXC = 2;                // chunks per warp (cpw <= 2)
+  constexpr int NA = NB == 1 ? 2 : 1;    // accumulators per row (breaks FMA chains)
+  extern __shared__ __align__(128) uint8_t gsm[];
+  const int cols = P.cols, cols_pad = P.cols_pad, cols4 = cols >> 2;
+  float* xs = reinterpret_cast<float*>(gsm);                                  // [ninputs][NB][cols_pad]
+  float* red = xs + (size_t)P.ninputs * NB * cols_pad;                        // [2][SR][NB][QW]
+  uint8_t* ring = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(red + 2 * P.SR * NB * P.QW) + 127) & ~uintptr_t(127));
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)GT_NST * P.stage_bytes);
+  __shared__ float s_inv[MAX_INPUTS * NB];
+  __shared__ float s_red[GT_WARPS];
+  __shared__ int s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x, T = P.ntasks;
+  const int t0 = (int)((long long)blockIdx.x * T / G), t1 = (int)((long long)(blockIdx.x + 1) * T / G);
+  const uint64_t policy = tc::policy_evict_first();
+
+  auto issue = [&](int t, int s) {   // thread 0 only
+    const int j = gt_job(P, t);
+    const int row0 = (t - P.task_begin[j]) * P.SR;
+    const int nr = min(P.SR, P.rows[j] - row0);
+    const uint32_t bar = tc::smem_addr(full + s);
+    const uint32_t cb = (uint32_t)((size_t)nr * cols * ESZ);
+    const uint32_t pb = Q8 ? (uint32_t)((size_t)nr * (cols >> 5) * 4) : 0u;
+    tc::mbar_expect_tx(bar, cb + pb);
+    uint8_t* dst = ring + (size_t)s * P.stage_bytes;
+    tc::bulk_load(tc::smem_addr(dst), P.w[j] + (size_t)row0 * cols * ESZ, cb, bar, policy);
+    if constexpr (Q8)
+      tc::bulk_load(tc::smem_addr(dst + P.code_bytes), P.p[j] + (size_t)row0 * (cols >> 5) * 4, pb, bar, policy);
+  };
+
+  if (tid == 0) {
+    for (int s = 0; s < GT_NST; ++s) tc::mbar_init(tc::smem_addr(full + s), 1);
+    s_abort = 0;
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+  // the weights do not depend on the input: start streaming before staging it
+  if (tid == 0)
+    for (int i = 0; i < GT_NST && t0 + i < t1; ++i) issue(t0 + i, i);
+
+  // ---- stage the inputs (RMS-normalised where gamma is given)
+  for (int i = 0; i < P.ninputs; ++i) {
+    const float4* x4 = reinterpret_cast<const float4*>(P.in[i].x);
+    const float4* g4 = reinterpret_cast<const float4*>(P.in[i].gamma);
+    if (g4) {
+      for (int b = 0; b < P.B; ++b) {
+        float ss = 0.f;
+        for (int c = tid; c < cols4; c += GT_THREADS) {
+          const float4 v = x4[(size_t)b * cols4 + c];
+          ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        }
+        ss = warp_sum(ss);
+        __syncthreads();
+        if (lane == 0) s_red[warp] = ss;
+        __syncthreads();
+        if (tid == 0) {
+          float t = 0.f;
+          for (int w = 0; w < GT_WARPS; ++w) t += s_red[w];
+          s_inv[i * NB + b] = rsqrtf(t / (float)cols + P.eps);
+        }
+      }
+      __syncthreads();
+    }
+    for (int e = tid; e < NB * cols4; e += GT_THREADS) {
+      const int b = e / cols4, c4 = e - b * cols4;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (b < P.B) {
+        v = x4[(size_t)b * cols4 + c4];
+        if (g4) {
+          const float inv = s_inv[i * NB + b];
+          const float4 g = g4[c4];
+          v = make_float4(g.x * (v.x * inv), g.y * (v.y * inv), g.z * (v.z * inv), g.w * (v.w * inv));
+        }
+      }
+      *reinterpret_cast<float4*>(xs + (size_t)(i * NB + b) * cols_pad + gt_perm<EPL>(c4 * 4)) = v;
+    }
+  }
+  __syncthreads();
+
+  // ---- this warp's rows and column share
+  const int rp = warp / P.QW, q = warp - rp * P.QW;
+  const int ch_begin = q * P.cpw, ch_end = min(ch_begin + P.cpw, P.nchunks);
+  const int row_a = 2 * rp;
+  float2 xr[NB == 1 ? MAXC : 1][EPL / 2];
+  int xr_input = -1;
+
+  float best_v = ARGMAX_FLOOR;   // argmax: thread b*SR keeps position b's best
+  int best_i = 0;
+  int buf = 0;
+  const uint64_t t_start = tc::globaltimer();
+
+  for (int t = t0; t < t1; ++t) {
+    const int s = (t - t0) % GT_NST;
+    const uint32_t parity = (uint32_t)(((t - t0) / GT_NST) & 1);
+    const int j = gt_job(P, t);
+    const int row0 = (t - P.task_begin[j]) * P.SR;
+    const int nr = min(P.SR, P.rows[j] - row0);
+    const int input = P.input[j];
+    // bounded wait for the stage
+    bool ok = true;
+    {
+      const uint32_t bar = tc::smem_addr(full + s);
+      if (!tc::mbar_try(bar, parity)) {
+        const uint64_t w0 = tc::globaltimer();
+        while (!tc::mbar_try_sleep(bar, parity, 20000u)) {
+          if (*(volatile int*)&s_abort || tc::globaltimer() - w0 > P.wait_limit_ns) {
+            ok = false;
+            s_abort = 1;
+            atomicExch(&g_decode_status, PGQ_ETIMEOUT);
+            break;
+          }
+        }
+      }
+    }
+    float2 acc[2][NB][NA];
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+      for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int a = 0; a < NA; ++a) acc[r][b][a] = make_float2(0.f, 0.f);
+    if (ok) {
+      const float* xin = xs + (size_t)input * NB * cols_pad + lane * 4;
+      if constexpr (NB == 1) {
+        if (input != xr_input) {
+#pragma unroll
+          for (int u = 0; u < MAXC; ++u) {
+#pragma unroll
+            for (int k = 0; k < EPL / 4; ++k) {
+              float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (ch_begin + u < ch_end) a = *reinterpret_cast<const float4*>(xin + (size_t)(ch_begin + u) * CW + k * 128);
+              xr[u][2 * k] = make_float2(a.x, a.y);
+              xr[u][2 * k + 1] = make_float2(a.z, a.w);
+            }
+          }
+          xr_input = input;
+        }
+      }
+      const uint8_t* st = ring + (size_t)s * P.stage_bytes;
+#pragma unroll
+      for (int u = 0; u < MAXC; ++u) {
+        const int ch = ch_begin + u;
+        if (ch < ch_end && ch * CW + lane * EPL < cols) {
+          const int col = ch * CW + lane * EPL;
+          float2 wv[2][EPL / 2];
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const int row = row_a + r;
+            const uint4 cw = *reinterpret_cast<const uint4*>(st + ((size_t)row * cols + col) * ESZ);
+            if constexpr (Q8) {
+              const uint32_t pw =
+                  *reinterpret_cast<const uint32_t*>(st + P.code_bytes + ((size_t)row * (cols >> 5) + (col >> 5)) * 4);
+              const float2 so = h2_to_f2(pw);
+              const float2 s2 = make_float2(so.x, so.x), o2 = make_float2(so.y, so.y);
+              const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                float2 lo, hi;
+                s8x4_to_f32(words[k], lo, hi);
+                wv[r][2 * k] = ffma2(lo, s2, o2);
+                wv[r][2 * k + 1] = ffma2(hi, s2, o2);
+              }
+            } else {
+              wv[r][0] = h2_to_f2(cw.x); wv[r][1] = h2_to_f2(cw.y);
+              wv[r][2] = h2_to_f2(cw.z); wv[r][3] = h2_to_f2(cw.w);
+            }
+          }
+          if constexpr (NB == 1) {
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+#pragma unroll
+              for (int k = 0; k < EPL / 2; ++k) acc[r][0][k % NA] = ffma2(wv[r][k], xr[u][k], acc[r][0][k % NA]);
+          } else {
+            const float* xc = xin + (size_t)ch * CW;
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+              float2 xv[EPL / 2];
+#pragma unroll
+              for (int k = 0; k < EPL / 4; ++k) {
+                const float4 a = *reinterpret_cast<const float4*>(xc + (size_t)b * cols_pad + k * 128);
+                xv[2 * k] = make_float2(a.x, a.y);
+                xv[2 * k + 1] = make_float2(a.z, a.w);
+              }
+#pragma unroll
+              for (int r = 0; r < 2; ++r)
+#pragma unroll
+                for (int k = 0; k < EPL / 2; ++k) acc[r][b][0] = ffma2(wv[r][k], xv[k], acc[r][b][0]);
+            }
+          }
+        }
+      }
+      // lane reduction: 2 rows x NB positions
+      constexpr int N = 2 * NB;
+      float v[N];
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          float2 a = acc[r][b][0];
+#pragma unroll
+          for (int k = 1; k < NA; ++k) a = fadd2(a, acc[r][b][k]);
+          v[r * NB + b] = a.x + a.y;
+        }
+      const float tot = reduce_scatter<N>(v, lane);
+      if ((lane & (32 / N - 1)) == 0) {
+        const int idx = lane / (32 / N);
+        const int r = idx / NB, b = idx - r * NB;
+        red[(((size_t)buf * P.SR + row_a + r) * NB + b) * P.QW + q] = tot;
+      }
+    }
+    if (!__syncthreads_and(ok)) break;
+    // the stage's slot is free: refill it with the task GT_NST ahead
+    if (tid == 0 && t + GT_NST < t1) issue(t + GT_NST, s);
+    // column shares summed in fixed order, epilogue, store (threads b*SR + r of
+    // the first two warps; whole warps take part in the argmax shuffles)
+    if (tid < 64) {
+      const int ct = tid;
+      const int b = ct / P.SR, r = ct - b * P.SR;
+      const bool act = ct < P.SR * NB;
+      float out = 0.f;
+      const int rows = P.rows[j];
+      const int row = row0 + r;
+      const bool live = act && r < nr && b < P.B;
+      if (act) {
+        const float* rr = red + (((size_t)buf * P.SR + r) * NB + b) * P.QW;
+        for (int k = 0; k < P.QW; ++k) out += rr[k];
+        if (live) {
+          if (P.epi[j] == PGQ_EPI_RELU2) {
+            out = fmaxf(out, 0.f);
+            out = out * out;
+          } else if (P.epi[j] == PGQ_EPI_ADD) {
+            out += P.residual[j][(size_t)b * rows + row];
+          }
+          if (P.y[j]) P.y[j][(size_t)b * rows + row] = out;
+        }
+      }
+      if constexpr (ARGMAX) {
+        // rows of position b sit in SR consecutive lanes: tree over them
+        float cv = live ? out : __int_as_float(0xff800000u);
+        int ci = live ? row : 0x7fffffff;
+        for (int o = 1; o < P.SR; o <<= 1) {
+          const float ov = __shfl_down_sync(0xffffffffu, cv, o);
+          const int oi = __shfl_down_sync(0xffffffffu, ci, o);
+          if ((r & (2 * o - 1)) == 0) argmax_merge(cv, ci, ov, oi);
+        }
+        if (act && r == 0) argmax_merge(best_v, best_i, cv, ci);
+      }
+    }
+    buf ^= 1;
+  }
+  (void)t_start;
+  // leave no bulk copy in flight (an aborted block may have issued ahead)
+  if (tid == 0 && *(volatile int*)&s_abort) {
+    for (int t = t0; t < t1 && t < t0 + GT_NST; ++t) {
+      const uint64_t w0 = tc::globaltimer();
+      while (!tc::mbar_try_sleep(tc::smem_addr(full + ((t - t0) % GT_NST)), 0u, 20000u) &&
+             tc::globaltimer() - w0 < P.wait_limit_ns) {
+      }
+    }
+  }
+
+  if constexpr (ARGMAX) {
+    __shared__ float s_bv[64];
+    __shared__ int s_bi[64];
+    __syncthreads();
+    if (tid < P.SR * NB && (tid % P.SR) == 0) {
+      s_bv[tid / P.SR] = best_v;
+      s_bi[tid / P.SR] = best_i;
+    }
+    __syncthreads();
+    if (tid < P.B) {
+      P.part_val[(size_t)blockIdx.x * P.B + tid] = s_bv[tid];
+      P.part_idx[(size_t)blockIdx.x * P.B + tid] = s_bi[tid];
+    }
+    __threadfence();
+    __syncthreads();
+    __shared__ unsigned s_ticket;
+    if (tid == 0) s_ticket = atomicAdd(P.ticket, 1u);
+    __syncthreads();
+    if (s_ticket == gridDim.x - 1) {
+      __threadfence();
+      if (tid < P.B) {
+        float bv = ARGMAX_FLOOR;
+        int bi = 0;
+        for (int c = 0; c < (int)gridDim.x; ++c)
+          argmax_merge(bv, bi, __ldcg(P.part_val + (size_t)c * P.B + tid),
+                       __ldcg(P.part_idx + (size_t)c * P.B + tid));
+        P.ids[tid] = bi;
+      }
+      if (tid == 0) *P.ticket = 0u;
+    }
+  }
+}
+
+namespace {
+using GtFn = void (*)(GtParams);
+template <bool Q8, bool AM>
+GtFn gt_pick(int nb) {
+  switch (nb) {
+    case 1: return reinterpret_cast<GtFn>(&gemv_tma_kernel<Q8, 1, AM>);
+    case 2: return reinterpret_cast<GtFn>(&gemv_tma_kernel<Q8, 2, AM>);
+    case 4: return reinterpret_cast<GtFn>(&gemv_tma_kernel<Q8, 4, AM>);
+    default: return reinterpret_cast<GtFn>(&gemv_tma_kernel<Q8, 8, AM>);
+  }
+}
+}  // namespace
+
+int launch_gemv_tma(const GvParams& V, bool q8, bool argmax, const DeviceInfo& dev, cudaStream_t st) {
+  const int nb = V.B <= 1 ? 1 : V.B <= 2 ? 2 : V.B <= 4 ? 4 : 8;
+  const int esz = q8 ? 1 : 2;
+  const int EPL = q8 ? 16 : 8, CW = 32 * EPL;
+  if (V.cols % 128 != 0) return PGQ_EUNSUPPORTED;          // 16-byte rows of params
+  const size_t row_bytes = (size_t)V.cols * esz + (q8 ? (size_t)V.cols / 8 : 0);
+  int SR = 8;
+  while (SR > 2 && (size_t)SR * row_bytes > GT_STAGE_MAX) SR >>= 1;
+  if ((size_t)SR * row_bytes > GT_STAGE_MAX) return PGQ_EUNSUPPORTED;
+  if (SR * nb > 64) return PGQ_EUNSUPPORTED;
+  const int QW = 32 / SR;
+  const int nchunks = (V.cols + CW - 1) / CW;
+  const int cpw = (nchunks + QW - 1) / QW;
+  if (cpw > 2) return PGQ_EUNSUPPORTED;
+  GtParams P{};
+  int t = 0;
+  for (int j = 0; j < V.njobs; ++j) {
+    P.w[j] = V.job[j].w;
+    P.p[j] = reinterpret_cast<const uint8_t*>(V.job[j].params);
+    P.y[j] = V.job[j].y;
+    P.residual[j] = V.job[j].residual;
+    P.rows[j] = V.job[j].rows;
+    P.input[j] = V.job[j].input;
+    P.epi[j] = V.job[j].epilogue;
+    P.task_begin[j] = t;
+    t += (V.job[j].rows + SR - 1) / SR;
+    // bulk copies need 16-byte aligned sources
+    if (!aligned16(V.job[j].w) || (q8 && !aligned16(V.job[j].params))) return PGQ_EUNSUPPORTED;
+  }
+  P.task_begin[V.njobs] = t;
+  P.ntasks = t;
+  for (int i = 0; i < V.ninputs; ++i) P.in[i] = V.in[i];
+  P.njobs = V.njobs;
+  P.ninputs = V.ninputs;
+  P.B = V.B;
+  P.cols = V.cols;
+  P.nchunks = nchunks;
+  P.cols_pad = nchunks * CW;
+  P.SR = SR;
+  P.QW = QW;
+  P.cpw = cpw;
+  P.code_bytes = (SR * V.cols * esz + 127) / 128 * 128;
+  P.stage_bytes = (P.code_bytes + (q8 ? SR * (V.cols / 32) * 4 : 0) + 127) / 128 * 128;
+  P.eps = V.eps;
+  P.part_val = V.part_val;
+  P.part_idx = V.part_idx;
+  P.ticket = V.ticket;
+  P.ids = V.ids;
+  P.wait_limit_ns = 2000000000ull;
+  const size_t smem = (size_t)V.ninputs * nb * P.cols_pad * 4 + 2 * (size_t)SR * nb * QW * 4 + 128 +
+                      (size_t)GT_NST * P.stage_bytes + GT_NST * 8 + 64;
+  if (smem + 1024 > dev.smem_optin) return PGQ_EUNSUPPORTED;
+  GtFn fn = q8 ? (argmax ? gt_pick<true, true>(nb) : gt_pick<true, false>(nb))
+               : (argmax ? gt_pick<false, true>(nb) : gt_pick<false, false>(nb));
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  if (argmax) {
+    if (cudaError_t e = cudaMemsetAsync(P.ticket, 0, sizeof(unsigned), st); e != cudaSuccess) return cuda_status(e);
+  }
+  const int grid = std::max(1, std::min(dev.sms, P.ntasks));
+  void* args[] = {&P};
+  return cuda_status(cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(grid), dim3(GT_THREADS), args, smem, st));
+}
+
+int decode_status_read_and_clear(int* out) {
+  int v = 0, z = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_decode_status, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_decode_status, &z, sizeof(int));
+  if (e != cudaSuccess) return cuda_status(e);
+  *out = v;
+  return PGQ_OK;
+}
+
+}  // namespace pgq

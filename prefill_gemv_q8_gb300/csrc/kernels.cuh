@@ -46,6 +46,10 @@ int launch_argmax(const float* logits, int B, int V, int32_t* ids, cudaStream_t 
 // Decode GEMV (q8 or f16), multi-job; `argmax` only with f16 and one job.
 // Fills the derived fields of P and the jobs' task_begin.
 int launch_gemv(GvParams& P, bool q8, bool argmax, const DeviceInfo& dev, cudaStream_t st);
+// The TMA-fed decode kernel (weights streamed by bulk copies into a shared-memory
+// ring).  Returns PGQ_EUNSUPPORTED (nothing launched) for shapes it does not take.
+int launch_gemv_tma(const GvParams& P, bool q8, bool argmax, const DeviceInfo& dev, cudaStream_t st);
+int decode_status_read_and_clear(int* out);
 // Workspace of the argmax variant: partials [grid][B] (value, index) + ticket.
 size_t gemv_argmax_workspace_bytes(int B, const DeviceInfo& dev);
 // Device address and size of the fixed scratch array of the allocation-free
