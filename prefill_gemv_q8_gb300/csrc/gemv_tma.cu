@@ -11,6 +11,7 @@
 // applied and rows are stored.  The block barrier that ends a stage also frees its
 // ring slot, and thread 0 immediately refills it with the stage NST tasks ahead.
 #include <algorithm>
+#include <map>
 #include <mutex>
 
 #include "common.cuh"
@@ -18,6 +19,10 @@
 #include "tc.cuh"
 
 namespace pgq {
+
+#ifndef PGQ_DOT_MODE
+#define PGQ_DOT_MODE 1   // q8 at one position: 0 dequantise then dot, 1 dot then scale (byte-permute), 2 dot then scale (I2F)
+#endif
 
 constexpr int GT_WARPS = 16;
 constexpr int GT_THREADS = GT_WARPS * 32;
@@ -152,6 +157,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
   const int ch_begin = q * P.cpw, ch_end = min(ch_begin + P.cpw, P.nchunks);
   const int row_a = 2 * rp;
   float2 xr[NB == 1 ? MAXC : 1][EPL / 2];
+  float xsum[NB == 1 ? MAXC : 1];   // Σ of this lane's input values per chunk
   int xr_input = -1;
 
   float best_v = ARGMAX_FLOOR;   // argmax: thread b*SR keeps position b's best
@@ -202,6 +208,10 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
               xr[u][2 * k] = make_float2(a.x, a.y);
               xr[u][2 * k + 1] = make_float2(a.z, a.w);
             }
+            float2 t = xr[u][0];
+#pragma unroll
+            for (int k = 1; k < EPL / 2; ++k) t = fadd2(t, xr[u][k]);
+            xsum[u] = t.x + t.y;
           }
           xr_input = input;
         }
@@ -212,6 +222,46 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
         const int ch = ch_begin + u;
         if (ch < ch_end && ch * CW + lane * EPL < cols) {
           const int col = ch * CW + lane * EPL;
+#if PGQ_DOT_MODE != 0
+          if constexpr (Q8 && NB == 1) {
+            // dot then scale: Σ u·x with the biased byte u = q + 128 in [0, 255], then
+            // y += scale·dot + (offset − 128·scale)·Σx  (one pair of FMAs per 16 codes)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const int row = row_a + r;
+              const uint4 cw = *reinterpret_cast<const uint4*>(st + (size_t)row * cols + col);
+              const uint32_t pw =
+                  *reinterpret_cast<const uint32_t*>(st + P.code_bytes + ((size_t)row * (cols >> 5) + (col >> 5)) * 4);
+              const float2 so = h2_to_f2(pw);
+              const uint32_t words[4] = {cw.x ^ 0x80808080u, cw.y ^ 0x80808080u, cw.z ^ 0x80808080u,
+                                         cw.w ^ 0x80808080u};
+              float2 d0 = make_float2(0.f, 0.f), d1 = make_float2(0.f, 0.f);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                float2 lo, hi;
+#if PGQ_DOT_MODE == 2
+                lo = make_float2(__uint2float_rn(words[k] & 0xffu), __uint2float_rn((words[k] >> 8) & 0xffu));
+                hi = make_float2(__uint2float_rn((words[k] >> 16) & 0xffu), __uint2float_rn(words[k] >> 24));
+#else
+                const float2 m23 = make_float2(-8388608.0f, -8388608.0f);
+                lo = fadd2(make_float2(__uint_as_float(__byte_perm(words[k], 0x4B000000u, 0x7540)),
+                                       __uint_as_float(__byte_perm(words[k], 0x4B000000u, 0x7541))), m23);
+                hi = fadd2(make_float2(__uint_as_float(__byte_perm(words[k], 0x4B000000u, 0x7542)),
+                                       __uint_as_float(__byte_perm(words[k], 0x4B000000u, 0x7543))), m23);
+#endif
+                d0 = ffma2(lo, xr[u][2 * k], d0);
+                d1 = ffma2(hi, xr[u][2 * k + 1], d1);
+              }
+              const float2 d = fadd2(d0, d1);
+              const float c = fmaf(-128.f, so.x, so.y);
+              float2 a = acc[r][0][0];
+              a.x = fmaf(so.x, d.x + d.y, a.x);
+              a.y = fmaf(c, xsum[u], a.y);
+              acc[r][0][0] = a;
+            }
+            continue;
+          }
+#endif
           float2 wv[2][EPL / 2];
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
@@ -429,12 +479,18 @@ int launch_gemv_tma(const GvParams& V, bool q8, bool argmax, const DeviceInfo& d
   if (smem + 1024 > dev.smem_optin) return PGQ_EUNSUPPORTED;
   GtFn fn = q8 ? (argmax ? gt_pick<true, true>(nb) : gt_pick<true, false>(nb))
                : (argmax ? gt_pick<false, true>(nb) : gt_pick<false, false>(nb));
-  static std::mutex mu;
   {
+    // raise the kernel's shared-memory limit once per (kernel, device, size)
+    static std::mutex mu;
+    static std::map<std::pair<GtFn, int>, size_t> done;
     std::lock_guard<std::mutex> lk(mu);
-    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return cuda_status(e);
+    size_t& cur = done[{fn, dev.device}];
+    if (smem > cur) {
+      cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return cuda_status(e);
+      cur = smem;
+    }
   }
   if (argmax) {
     if (cudaError_t e = cudaMemsetAsync(P.ticket, 0, sizeof(unsigned), st); e != cudaSuccess) return cuda_status(e);

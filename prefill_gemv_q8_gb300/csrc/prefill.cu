@@ -33,7 +33,9 @@
 //   and MMAs are drained with bounded waits, and tensor memory is released.
 #include <algorithm>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "common.cuh"
 #include "kernels.cuh"
@@ -584,9 +586,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
 // One block per position b < Bp: amax, a power-of-two scale 2^(14 - e) with
 // amax < 2^e, x·scale rounded to binary16; xinv[b] = 2^(e - 14).  Rows b >= B are 0.
 __global__ void __launch_bounds__(256) xprep_kernel(const float* __restrict__ X, int B, int cols,
-                                                    __half* __restrict__ Xh, float* __restrict__ xinv) {
+                                                    __half* __restrict__ Xh, float* __restrict__ xinv,
+                                                    unsigned* __restrict__ tile_cnt, int ntiles, int* __restrict__ status) {
   __shared__ float red[8];
   const int b = blockIdx.x;
+  // the GEMM that follows on the stream starts from zero tickets and a clear status
+  if (b == 0) {
+    for (int i = threadIdx.x; i < ntiles; i += 256) tile_cnt[i] = 0u;
+    if (threadIdx.x == 0) *status = PGQ_OK;
+  }
   __half* out = Xh + (size_t)b * cols;
   if (b >= B) {
     for (int c = threadIdx.x; c < cols; c += 256) out[c] = __ushort_as_half(0);
@@ -633,16 +641,40 @@ EncodeFn encoder() {
   return fn;
 }
 
+struct MapKey {
+  const void* base;
+  uint64_t inner, outer, row_bytes;
+  uint32_t box_inner, box_outer;
+  int dt, sw;
+  bool operator<(const MapKey& o) const {
+    return std::tie(base, inner, outer, row_bytes, box_inner, box_outer, dt, sw) <
+           std::tie(o.base, o.inner, o.outer, o.row_bytes, o.box_inner, o.box_outer, o.dt, o.sw);
+  }
+};
+
+// Encodes a 2-D tensor map; encodings are cached (the host-side encode costs as much
+// as a launch), keyed by every field that goes into them.
 bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
                uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  static std::map<MapKey, CUtensorMap> cache;   // callers hold the launch mutex
+  const MapKey key{base, inner, outer, row_bytes, box_inner, box_outer, (int)dt, (int)sw};
+  auto it = cache.find(key);
+  if (it != cache.end()) {
+    *m = it->second;
+    return true;
+  }
   EncodeFn fn = encoder();
   if (!fn) return false;
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {row_bytes};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
-  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  if (cache.size() > 4096) cache.clear();
+  cache[key] = *m;
+  return true;
 }
 
 template <bool A_TMEM>
@@ -732,18 +764,23 @@ int launch_prefill(const PrefillJob* jobs, int njobs, const float* X, int cols, 
   P.status = reinterpret_cast<int*>(w + pl.off_status);
   P.wait_limit_ns = wait_limit_ns ? wait_limit_ns : 2000000000ull;
 
-  cudaError_t e = cudaMemsetAsync(w + pl.off_status, 0, 256, st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(P.tile_cnt, 0, (size_t)pl.ntiles * 4, st);
-  if (e != cudaSuccess) return cuda_status(e);
-  xprep_kernel<<<pl.Bp, 256, 0, st>>>(X, B, cols, Xh, xinv);
+  cudaError_t e;
+  xprep_kernel<<<pl.Bp, 256, 0, st>>>(X, B, cols, Xh, xinv, P.tile_cnt, pl.ntiles, P.status);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e);
 
   const void* fn = a_tmem ? reinterpret_cast<const void*>(&prefill_tc_kernel<true>)
                           : reinterpret_cast<const void*>(&prefill_tc_kernel<false>);
   const size_t smem = a_tmem ? tc_smem_bytes<true>(pl.Bp) : tc_smem_bytes<false>(pl.Bp);
   if (smem > dev.smem_optin) return set_error(PGQ_EUNSUPPORTED, "prefill: %zu bytes of shared memory", smem);
-  if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
-    return cuda_status(e);
+  {
+    static std::map<std::pair<const void*, int>, size_t> done;   // guarded by `mu` above
+    size_t& cur = done[{fn, dev.device}];
+    if (smem > cur) {
+      if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+        return cuda_status(e);
+      cur = smem;
+    }
+  }
   void* args[] = {&P};
   return cuda_status(cudaLaunchKernel(fn, dim3(pl.G), dim3(TC_THREADS), args, smem, st));
 }
