@@ -245,6 +245,76 @@ def time_q8_layer(torch, W, steps, warmup):
     return total, per_launch(g_k1), per_launch(g_k2)
 
 
+PREFILL_FILES = ["prefill.cu", "tc.cuh", "common.cuh", "kernels.cuh"]
+
+
+class PrefillPass:
+    """32-layer batched prefill pass, B = 64 positions, hidden 4096 (the q8 decode
+    layer's projections per layer, 5,737,807,872 weight bytes per pass)."""
+    name = "prefill pass B=64, 32 layers (hidden 4096, kv 1024, inter 14336)"
+
+    def __init__(self, torch, pgq, synth, layers=None):
+        c = synth.PREFILL
+        self.t, self.pgq = torch, pgq
+        self.B, self.H, self.KV, self.I = c["B"], c["hidden"], c["kv"], c["inter"]
+        self.L = layers or c["layers"]
+        wl = c["workload"]
+        self.layers = [synth.q8_layer(wl, l, self.H, self.KV, self.I, "torch", "cuda") for l in range(self.L)]
+        self.PL = pgq.PassLayers(self.layers)
+        self.h0 = synth.normal((self.B, self.H), 1.0, wl, synth.T_X, "torch", "cuda")
+        self.h = self.h0.clone()
+        self.g1 = synth.uniform((self.L, self.H), 0.5, 1.5, wl, synth.T_GAMMA, "torch", "cuda")
+        self.g2 = synth.uniform((self.L, self.H), 0.5, 1.5, wl, synth.T_GAMMA2, "torch", "cuda")
+        self.ws = pgq.prefill_pass_workspace(self.H, self.KV, self.I, self.B)
+        per_layer = sum(r * c_ + r * (c_ // 32) * 4 for r, c_ in synth.q8_layer_shapes(self.H, self.KV, self.I).values())
+        self.step_bytes = per_layer * self.L
+        self.flops = 2 * self.B * sum(r * c_ for r, c_ in synth.q8_layer_shapes(self.H, self.KV, self.I).values()) * self.L
+        # launches per pass: per layer 2 norms + 4 GEMMs, each GEMM = X conversion + GEMM
+        # (memsets are not kernels of ours)
+        self.launches_per_step = self.L * (2 + 4 * 2)
+
+    def step(self):
+        self.h.copy_(self.h0)
+        self.pgq.prefill_pass(self.PL, self.h, self.g1, self.g2, 1e-6, workspace=self.ws)
+
+
+def time_prefill(torch, P, steps, warmup, pk):
+    st = torch.cuda.current_stream()
+    ms_api = time_loop(torch, P.step, steps, warmup)
+    ms = time_graph(torch, P.step, steps, warmup)
+    # dominant kernel alone: the up projection (14336 x 4096, relu²), rotating layers
+    up_bytes = P.I * P.H + P.I * (P.H // 32) * 4
+    X = P.h0
+    U = torch.empty(P.B, P.I, device="cuda")
+    gws = P.pgq.prefill_workspace([P.I], P.H, P.B)
+    jobs = [[dict(codes=L["up"][0], params=L["up"][1], y=U, epilogue="relu2")] for L in P.layers]
+    for i in range(warmup):
+        P.pgq.prefill_q8(jobs[i % len(jobs)], X, workspace=gws)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        ev[i][0].record(st)
+        P.pgq.prefill_q8(jobs[i % len(jobs)], X, workspace=gws)
+        ev[i][1].record(st)
+    torch.cuda.synchronize()
+    k_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+    gbs = P.step_bytes / (ms * 1e-3) / 1e9
+    ach = up_bytes / (k_ms * 1e-3) / 1e9
+    tf = P.flops / (ms * 1e-3) / 1e12
+    return {
+        "workload": P.name, "metric": "positions/s", "value": round(P.B / (ms * 1e-3), 1),
+        "ms_per_pass": round(ms, 4), "ms_per_pass_api": round(ms_api, 4),
+        "timed": "CUDA-graph replay of the pass call (ms_per_pass_api: direct calls, host launch cost included)",
+        "weight_GBps": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm"], 4),
+        "tflops": round(tf, 1), "frac_of_bf16_tensor": round(tf / pk["bf16_sustained"], 4),
+        "bound": "hbm", "weight_bytes_per_pass": P.step_bytes, "launches_per_pass": P.launches_per_step,
+        "roofline": {"bound": "hbm", "kernel": "prefill_tc_kernel (up 14336x4096, relu², B=64) + X conversion",
+                     "achieved": round(ach, 1), "peak": pk["hbm"], "unit": "GB/s", "frac": round(ach / pk["hbm"], 4),
+                     "traffic": ncu_traffic("prefill_tc_up", PREFILL_FILES), "algorithmic_bytes_per_launch": up_bytes,
+                     "avg_launch_ms": round(k_ms, 5), "timed": "separate event loop over 32 up matrices, direct calls"},
+    }
+
+
 def _events(torch, n):
     return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
 
