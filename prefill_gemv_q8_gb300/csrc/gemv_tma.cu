@@ -24,8 +24,8 @@ namespace pgq {
 #define PGQ_DOT_MODE 1   // q8 at one position: 0 dequantise then dot, 1 dot then scale (byte-permute), 2 dot then scale (I2F)
 #endif
 
-constexpr int GT_WARPS = 16;
-constexpr int GT_THREADS = GT_WARPS * 32;
+constexpr int GT_WARPS = 16;                 // computing warps
+constexpr int GT_THREADS = (GT_WARPS + 1) * 32;  // + one producer warp
 constexpr int GT_STAGE_MAX = 37 * 1024;   // bytes of one ring stage (codes + params)
 constexpr int GT_NST = 4;                  // ring stages
 
@@ -80,8 +80,9 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(red + 2 * P.SR * NB * P.QW) + 127) & ~uintptr_t(127));
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)GT_NST * P.stage_bytes);
+  uint64_t* empty = full + GT_NST;
   __shared__ float s_inv[MAX_INPUTS * NB];
-  __shared__ float s_red[GT_WARPS];
+  __shared__ float s_red[GT_WARPS + 1];
   __shared__ int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -103,14 +104,18 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
       tc::bulk_load(tc::smem_addr(dst + P.code_bytes), P.p[j] + (size_t)row0 * (cols >> 5) * 4, pb, bar, policy);
   };
 
+  const bool producer = warp == GT_WARPS;
   if (tid == 0) {
-    for (int s = 0; s < GT_NST; ++s) tc::mbar_init(tc::smem_addr(full + s), 1);
+    for (int s = 0; s < GT_NST; ++s) {
+      tc::mbar_init(tc::smem_addr(full + s), 1);
+      tc::mbar_init(tc::smem_addr(empty + s), GT_WARPS);
+    }
     s_abort = 0;
     tc::fence_barrier_init();
   }
   __syncthreads();
   // the weights do not depend on the input: start streaming before staging it
-  if (tid == 0)
+  if (producer && lane == 0)
     for (int i = 0; i < GT_NST && t0 + i < t1; ++i) issue(t0 + i, i);
 
   // ---- stage the inputs (RMS-normalised where gamma is given)
@@ -130,7 +135,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
         __syncthreads();
         if (tid == 0) {
           float t = 0.f;
-          for (int w = 0; w < GT_WARPS; ++w) t += s_red[w];
+          for (int w = 0; w <= GT_WARPS; ++w) t += s_red[w];
           s_inv[i * NB + b] = rsqrtf(t / (float)cols + P.eps);
         }
       }
@@ -152,6 +157,35 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
   }
   __syncthreads();
 
+  // bounded wait on an mbarrier phase; false after an expired wait (or another
+  // role's), which then also marks the block aborted
+  auto wait_bar = [&](uint32_t bar, uint32_t parity) -> bool {
+    if (tc::mbar_try(bar, parity)) return true;
+    const uint64_t w0 = tc::globaltimer();
+    while (!tc::mbar_try_sleep(bar, parity, 20000u)) {
+      if (*(volatile int*)&s_abort) return false;
+      if (tc::globaltimer() - w0 > P.wait_limit_ns) {
+        *(volatile int*)&s_abort = 1;
+        atomicExch(&g_decode_status, PGQ_ETIMEOUT);
+        return false;
+      }
+    }
+    return true;
+  };
+
+  float best_v = ARGMAX_FLOOR;   // argmax: lane 2b of a row pair's first warp keeps position b's best
+  int best_i = 0;
+  if (producer) {
+    // ---- refill each ring slot once all computing warps have released it
+    if (lane == 0) {
+      for (int t = t0 + GT_NST; t < t1; ++t) {
+        const int s = (t - t0) % GT_NST;
+        const uint32_t parity = (uint32_t)((((t - t0) / GT_NST) - 1) & 1);
+        if (!wait_bar(tc::smem_addr(empty + s), parity)) break;
+        issue(t, s);
+      }
+    }
+  } else {
   // ---- this warp's rows and column share
   const int rp = warp / P.QW, q = warp - rp * P.QW;
   const int ch_begin = q * P.cpw, ch_end = min(ch_begin + P.cpw, P.nchunks);
@@ -160,8 +194,6 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
   float xsum[NB == 1 ? MAXC : 1];   // Σ of this lane's input values per chunk
   int xr_input = -1;
 
-  float best_v = ARGMAX_FLOOR;   // argmax: thread b*SR keeps position b's best
-  int best_i = 0;
   int buf = 0;
   const uint64_t t_start = tc::globaltimer();
 
@@ -172,22 +204,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
     const int row0 = (t - P.task_begin[j]) * P.SR;
     const int nr = min(P.SR, P.rows[j] - row0);
     const int input = P.input[j];
-    // bounded wait for the stage
-    bool ok = true;
-    {
-      const uint32_t bar = tc::smem_addr(full + s);
-      if (!tc::mbar_try(bar, parity)) {
-        const uint64_t w0 = tc::globaltimer();
-        while (!tc::mbar_try_sleep(bar, parity, 20000u)) {
-          if (*(volatile int*)&s_abort || tc::globaltimer() - w0 > P.wait_limit_ns) {
-            ok = false;
-            s_abort = 1;
-            atomicExch(&g_decode_status, PGQ_ETIMEOUT);
-            break;
-          }
-        }
-      }
-    }
+    const bool ok = wait_bar(tc::smem_addr(full + s), parity);
     float2 acc[2][NB][NA];
 #pragma unroll
     for (int r = 0; r < 2; ++r)
@@ -328,21 +345,31 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
         red[(((size_t)buf * P.SR + row_a + r) * NB + b) * P.QW + q] = tot;
       }
     }
-    if (!__syncthreads_and(ok)) break;
-    // the stage's slot is free: refill it with the task GT_NST ahead
-    if (tid == 0 && t + GT_NST < t1) issue(t + GT_NST, s);
-    // column shares summed in fixed order, epilogue, store (threads b*SR + r of
-    // the first two warps; whole warps take part in the argmax shuffles)
-    if (tid < 64) {
-      const int ct = tid;
-      const int b = ct / P.SR, r = ct - b * P.SR;
-      const bool act = ct < P.SR * NB;
+    // the warp's reads of the stage are done: release the slot to the producer
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(tc::smem_addr(empty + s));
+    // the QW warps of this row pair meet; all leave together if one wait expired
+    {
+      uint32_t all;
+      asm volatile(
+          "{\n\t.reg .pred p, r;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+          "bar.red.and.pred r, %2, %3, p;\n\tselp.u32 %0, 1, 0, r;\n\t}"
+          : "=r"(all)
+          : "r"((uint32_t)ok), "r"(1 + rp), "r"(P.QW * 32)
+          : "memory");
+      if (!all) break;
+    }
+    // the row pair's column shares summed in fixed order, epilogue, store
+    // (lanes b*2 + r of the pair's first warp)
+    if (q == 0) {
+      const int b = lane >> 1, r = lane & 1;
+      const bool act = lane < 2 * NB;
       float out = 0.f;
       const int rows = P.rows[j];
-      const int row = row0 + r;
-      const bool live = act && r < nr && b < P.B;
+      const int row = row0 + row_a + r;
+      const bool live = act && row_a + r < nr && b < P.B;
       if (act) {
-        const float* rr = red + (((size_t)buf * P.SR + r) * NB + b) * P.QW;
+        const float* rr = red + (((size_t)buf * P.SR + row_a + r) * NB + b) * P.QW;
         for (int k = 0; k < P.QW; ++k) out += rr[k];
         if (live) {
           if (P.epi[j] == PGQ_EPI_RELU2) {
@@ -355,22 +382,20 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
         }
       }
       if constexpr (ARGMAX) {
-        // rows of position b sit in SR consecutive lanes: tree over them
         float cv = live ? out : __int_as_float(0xff800000u);
         int ci = live ? row : 0x7fffffff;
-        for (int o = 1; o < P.SR; o <<= 1) {
-          const float ov = __shfl_down_sync(0xffffffffu, cv, o);
-          const int oi = __shfl_down_sync(0xffffffffu, ci, o);
-          if ((r & (2 * o - 1)) == 0) argmax_merge(cv, ci, ov, oi);
-        }
+        const float ov = __shfl_down_sync(0xffffffffu, cv, 1);
+        const int oi = __shfl_down_sync(0xffffffffu, ci, 1);
+        if (r == 0) argmax_merge(cv, ci, ov, oi);
         if (act && r == 0) argmax_merge(best_v, best_i, cv, ci);
       }
     }
     buf ^= 1;
   }
   (void)t_start;
+  }  // computing warps
   // leave no bulk copy in flight (an aborted block may have issued ahead)
-  if (tid == 0 && *(volatile int*)&s_abort) {
+  if (producer && lane == 0 && *(volatile int*)&s_abort) {
     for (int t = t0; t < t1 && t < t0 + GT_NST; ++t) {
       const uint64_t w0 = tc::globaltimer();
       while (!tc::mbar_try_sleep(tc::smem_addr(full + ((t - t0) % GT_NST)), 0u, 20000u) &&
@@ -380,17 +405,22 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
   }
 
   if constexpr (ARGMAX) {
-    __shared__ float s_bv[64];
-    __shared__ int s_bi[64];
+    // each row pair's first warp holds its best per position (lanes 2b)
+    __shared__ float s_bv[8 * 8];
+    __shared__ int s_bi[8 * 8];
     __syncthreads();
-    if (tid < P.SR * NB && (tid % P.SR) == 0) {
-      s_bv[tid / P.SR] = best_v;
-      s_bi[tid / P.SR] = best_i;
+    const int npairs = P.SR / 2;
+    if (!producer && (warp % P.QW) == 0 && lane < 2 * NB && (lane & 1) == 0) {
+      s_bv[(warp / P.QW) * 8 + (lane >> 1)] = best_v;
+      s_bi[(warp / P.QW) * 8 + (lane >> 1)] = best_i;
     }
     __syncthreads();
     if (tid < P.B) {
-      P.part_val[(size_t)blockIdx.x * P.B + tid] = s_bv[tid];
-      P.part_idx[(size_t)blockIdx.x * P.B + tid] = s_bi[tid];
+      float bv = ARGMAX_FLOOR;
+      int bi = 0;
+      for (int g = 0; g < npairs; ++g) argmax_merge(bv, bi, s_bv[g * 8 + tid], s_bi[g * 8 + tid]);
+      P.part_val[(size_t)blockIdx.x * P.B + tid] = bv;
+      P.part_idx[(size_t)blockIdx.x * P.B + tid] = bi;
     }
     __threadfence();
     __syncthreads();
@@ -475,7 +505,7 @@ int launch_gemv_tma(const GvParams& V, bool q8, bool argmax, const DeviceInfo& d
   P.ids = V.ids;
   P.wait_limit_ns = 2000000000ull;
   const size_t smem = (size_t)V.ninputs * nb * P.cols_pad * 4 + 2 * (size_t)SR * nb * QW * 4 + 128 +
-                      (size_t)GT_NST * P.stage_bytes + GT_NST * 8 + 64;
+                      (size_t)GT_NST * P.stage_bytes + 2 * GT_NST * 8 + 64;
   if (smem + 1024 > dev.smem_optin) return PGQ_EUNSUPPORTED;
   GtFn fn = q8 ? (argmax ? gt_pick<true, true>(nb) : gt_pick<true, false>(nb))
                : (argmax ? gt_pick<false, true>(nb) : gt_pick<false, false>(nb));
