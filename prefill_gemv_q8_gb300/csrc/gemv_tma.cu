@@ -259,6 +259,11 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
 #if PGQ_DOT_MODE == 2
                 lo = make_float2(__uint2float_rn(words[k] & 0xffu), __uint2float_rn((words[k] >> 8) & 0xffu));
                 hi = make_float2(__uint2float_rn((words[k] >> 16) & 0xffu), __uint2float_rn(words[k] >> 24));
+#elif PGQ_DOT_MODE == 3
+                // one byte-permute makes two binary16 values 1024 + u (exact), widened
+                // to f32; the 1024 joins the 128 of the bias below
+                lo = h2_to_f2(__byte_perm(words[k], 0x64646464u, 0x4140));
+                hi = h2_to_f2(__byte_perm(words[k], 0x64646464u, 0x4342));
 #else
                 const float2 m23 = make_float2(-8388608.0f, -8388608.0f);
                 lo = fadd2(make_float2(__uint_as_float(__byte_perm(words[k], 0x4B000000u, 0x7540)),
@@ -270,7 +275,11 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
                 d1 = ffma2(hi, xr[u][2 * k + 1], d1);
               }
               const float2 d = fadd2(d0, d1);
+#if PGQ_DOT_MODE == 3
+              const float c = fmaf(-1152.f, so.x, so.y);
+#else
               const float c = fmaf(-128.f, so.x, so.y);
+#endif
               float2 a = acc[r][0][0];
               a.x = fmaf(so.x, d.x + d.y, a.x);
               a.y = fmaf(c, xsum[u], a.y);
