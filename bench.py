@@ -118,7 +118,7 @@ class Clocks:
 
 
 # ------------------------------------------------------------------ workloads
-Q8_FILES = ["gemv.cu", "common.cuh", "kernels.cuh"]
+Q8_FILES = ["gemv_tma.cu", "gemv.cu", "tc.cuh", "common.cuh", "kernels.cuh"]
 
 
 class Q8DecodeLayer:
@@ -462,7 +462,7 @@ def main():
     ap.add_argument("--impl", default="pgq", choices=["pgq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-prefill", action="store_true", help="only the headline decode layer")
-    ap.add_argument("--only", choices=["decode", "prefill"], default=None,
+    ap.add_argument("--only", choices=["decode", "prefill", "moe", "vocab"], default=None,
                     help="profiling aid: run one workload and print its JSON object")
     ap.add_argument("--prefill-layers", type=int, default=None, help="layers of the prefill pass (default 32)")
     args = ap.parse_args()
@@ -495,6 +495,12 @@ def main():
         P = PrefillPass(torch, pgq, synth, layers=args.prefill_layers)
         print(json.dumps(time_prefill(torch, P, args.steps, args.warmup, pk)), flush=True)
         return
+    if args.only == "moe":
+        print(json.dumps(bench_moe(torch, pgq, synth, args.steps, args.warmup, pk)), flush=True)
+        return
+    if args.only == "vocab":
+        print(json.dumps(bench_vocab(torch, pgq, synth, args.steps, args.warmup, pk)), flush=True)
+        return
     W = Q8DecodeLayer(torch, pgq, synth)
     torch.cuda.synchronize()
     if dist:
@@ -521,7 +527,7 @@ def main():
                    "timing": "CUDA graph of the step (2 launches) per weight copy, replayed in rotation",
                    "parallelism": f"replicas x{world}"},
         "frac_of_hbm": round(value / world / pk["hbm"], 4),
-        "roofline": {"bound": "hbm", "kernel": "gemv_kernel<q8,B=1> (norm + q,k,v,o,up)",
+        "roofline": {"bound": "hbm", "kernel": "gemv_tma_kernel<q8,B=1> (norm + q,k,v,o,up)",
                      "achieved": round(achieved, 1), "peak": pk["hbm"], "unit": "GB/s",
                      "frac": round(achieved / pk["hbm"], 4), "peak_src": pk["src"],
                      "traffic": ncu_traffic("gemv_q8_layer_multi", Q8_FILES),

@@ -1,15 +1,16 @@
 // Decode projections fed by TMA bulk copies: the weights of SR consecutive rows are
-// one contiguous span of codes (and one of (scale, offset) pairs), so a single
-// thread streams whole stages of rows into a ring in shared memory with
-// cp.async.bulk, and all 16 warps of the block only read shared memory and compute.
+// one contiguous span of codes (and one of (scale, offset) pairs), so one producer
+// warp streams whole stages of rows into a ring in shared memory with cp.async.bulk
+// (full/empty mbarriers per slot), and 16 computing warps only read shared memory.
 //
-// Stage = SR rows x all columns (~32 KB).  Warp w takes a pair of rows (2·(w / QW))
-// and the QW-th share of the chunks (QW = 32 / SR column shares), 16-byte reads per
-// lane; at one position its input values live in registers for the whole kernel.
+// Stage = SR rows x all columns (<= 37 KB).  Warp w takes RPW = 2 rows (group
+// w / QW, QW = 32 / SR warps per group) and an even share of the 512-column chunks;
+// at one position its input values live in registers for the whole kernel.  q8 at
+// one position uses dot-then-scale: the biased byte u = q + 128 is widened by one
+// byte-permute into the f32 2^15 + u, so the dot needs no conversion arithmetic.
 // Per stage the partial dot products are reduced across lanes (butterfly) and
-// across the QW column shares (shared memory, fixed order), then the epilogue is
-// applied and rows are stored.  The block barrier that ends a stage also frees its
-// ring slot, and thread 0 immediately refills it with the stage NST tasks ahead.
+// across the QW column shares (shared memory, fixed order, after a named barrier of
+// the group), then the group's first warp applies the epilogue and stores.
 #include <algorithm>
 #include <map>
 #include <mutex>
@@ -21,13 +22,14 @@
 namespace pgq {
 
 #ifndef PGQ_DOT_MODE
-#define PGQ_DOT_MODE 1   // q8 at one position: 0 dequantise then dot, 1 dot then scale (byte-permute), 2 dot then scale (I2F)
+#define PGQ_DOT_MODE 4   // q8 at one position: 0 dequantise then dot; dot then scale with codes widened
+                         // 1 by byte-permute into f32 2^23 + u, 3 by byte-permute into binary16 pairs,
+                         // 4 by byte-permute into f32 2^15 + u
 #endif
 
-constexpr int GT_WARPS = 16;                 // computing warps
-constexpr int GT_THREADS = (GT_WARPS + 1) * 32;  // + one producer warp
 constexpr int GT_STAGE_MAX = 37 * 1024;   // bytes of one ring stage (codes + params)
 constexpr int GT_NST = 4;                  // ring stages
+constexpr int GT_RED = 2;                  // buffers of per-warp partial sums
 
 // Device status word of the TMA decode kernels: PGQ_ETIMEOUT after an expired wait.
 __device__ int g_decode_status;
@@ -59,30 +61,26 @@ __device__ __forceinline__ int gt_perm(int c) {
   return ch * CW + (t >> 2) * 128 + ln * 4 + (t & 3);
 }
 
-__device__ __forceinline__ int gt_job(const GtParams& P, int t) {
-  int j = 0;
-#pragma unroll 1
-  while (j + 1 < P.njobs && t >= P.task_begin[j + 1]) ++j;
-  return j;
-}
-
-template <bool Q8, int NB, bool ARGMAX>
-__global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_constant__ GtParams P) {
+// W computing warps + one producer warp.  A stage holds SR rows; warp w takes RPW of
+// them (group w / QW, QW = W·RPW / SR warps per group) and the (w mod QW)-th share of
+// the column chunks (at most MAXC chunks of 32 lanes x EPL values).
+template <bool Q8, int NB, bool ARGMAX, int W, int RPW, int MAXC>
+__global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_constant__ GtParams P) {
+  constexpr int THREADS = (W + 1) * 32;
   constexpr int EPL = Q8 ? 16 : 8;
   constexpr int CW = 32 * EPL;
   constexpr int ESZ = Q8 ? 1 : 2;
-  constexpr int MAXC = 2;                // chunks per warp (cpw <= 2)
   constexpr int NA = NB == 1 ? 2 : 1;    // accumulators per row (breaks FMA chains)
   extern __shared__ __align__(128) uint8_t gsm[];
   const int cols = P.cols, cols_pad = P.cols_pad, cols4 = cols >> 2;
   float* xs = reinterpret_cast<float*>(gsm);                                  // [ninputs][NB][cols_pad]
-  float* red = xs + (size_t)P.ninputs * NB * cols_pad;                        // [2][SR][NB][QW]
+  float* red = xs + (size_t)P.ninputs * NB * cols_pad;                        // [GT_RED][SR][NB][QW]
   uint8_t* ring = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(red + 2 * P.SR * NB * P.QW) + 127) & ~uintptr_t(127));
+      (reinterpret_cast<uintptr_t>(red + GT_RED * P.SR * NB * P.QW) + 127) & ~uintptr_t(127));
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)GT_NST * P.stage_bytes);
   uint64_t* empty = full + GT_NST;
   __shared__ float s_inv[MAX_INPUTS * NB];
-  __shared__ float s_red[GT_WARPS + 1];
+  __shared__ float s_red[W + 1];
   __shared__ int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -90,8 +88,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
   const int t0 = (int)((long long)blockIdx.x * T / G), t1 = (int)((long long)(blockIdx.x + 1) * T / G);
   const uint64_t policy = tc::policy_evict_first();
 
-  auto issue = [&](int t, int s) {   // thread 0 only
-    const int j = gt_job(P, t);
+  auto issue = [&](int t, int j, int s) {   // one thread
     const int row0 = (t - P.task_begin[j]) * P.SR;
     const int nr = min(P.SR, P.rows[j] - row0);
     const uint32_t bar = tc::smem_addr(full + s);
@@ -103,20 +100,30 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
     if constexpr (Q8)
       tc::bulk_load(tc::smem_addr(dst + P.code_bytes), P.p[j] + (size_t)row0 * (cols >> 5) * 4, pb, bar, policy);
   };
+  // job of task t, found by walking forward from job j (tasks are visited in order)
+  auto job_of = [&](int t, int j) {
+    while (j + 1 < P.njobs && t >= P.task_begin[j + 1]) ++j;
+    return j;
+  };
 
-  const bool producer = warp == GT_WARPS;
+  const bool producer = warp == W;
   if (tid == 0) {
     for (int s = 0; s < GT_NST; ++s) {
       tc::mbar_init(tc::smem_addr(full + s), 1);
-      tc::mbar_init(tc::smem_addr(empty + s), GT_WARPS);
+      tc::mbar_init(tc::smem_addr(empty + s), W);
     }
     s_abort = 0;
     tc::fence_barrier_init();
   }
   __syncthreads();
   // the weights do not depend on the input: start streaming before staging it
-  if (producer && lane == 0)
-    for (int i = 0; i < GT_NST && t0 + i < t1; ++i) issue(t0 + i, i);
+  if (producer && lane == 0) {
+    int j = job_of(t0, 0);
+    for (int i = 0; i < GT_NST && t0 + i < t1; ++i) {
+      j = job_of(t0 + i, j);
+      issue(t0 + i, j, i);
+    }
+  }
 
   // ---- stage the inputs (RMS-normalised where gamma is given)
   for (int i = 0; i < P.ninputs; ++i) {
@@ -125,7 +132,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
     if (g4) {
       for (int b = 0; b < P.B; ++b) {
         float ss = 0.f;
-        for (int c = tid; c < cols4; c += GT_THREADS) {
+        for (int c = tid; c < cols4; c += THREADS) {
           const float4 v = x4[(size_t)b * cols4 + c];
           ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
         }
@@ -135,13 +142,13 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
         __syncthreads();
         if (tid == 0) {
           float t = 0.f;
-          for (int w = 0; w <= GT_WARPS; ++w) t += s_red[w];
+          for (int w = 0; w <= W; ++w) t += s_red[w];
           s_inv[i * NB + b] = rsqrtf(t / (float)cols + P.eps);
         }
       }
       __syncthreads();
     }
-    for (int e = tid; e < NB * cols4; e += GT_THREADS) {
+    for (int e = tid; e < NB * cols4; e += THREADS) {
       const int b = e / cols4, c4 = e - b * cols4;
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
       if (b < P.B) {
@@ -173,49 +180,68 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
     return true;
   };
 
-  float best_v = ARGMAX_FLOOR;   // argmax: lane 2b of a row pair's first warp keeps position b's best
+  float best_v = ARGMAX_FLOOR;   // argmax: lane RPW·b of a group's first warp keeps position b's best
   int best_i = 0;
   if (producer) {
     // ---- refill each ring slot once all computing warps have released it
     if (lane == 0) {
+      int j = job_of(t0, 0);
+      int s = 0;
+      uint32_t parity = 0;
       for (int t = t0 + GT_NST; t < t1; ++t) {
-        const int s = (t - t0) % GT_NST;
-        const uint32_t parity = (uint32_t)((((t - t0) / GT_NST) - 1) & 1);
         if (!wait_bar(tc::smem_addr(empty + s), parity)) break;
-        issue(t, s);
+        j = job_of(t, j);
+        issue(t, j, s);
+        if (++s == GT_NST) { s = 0; parity ^= 1u; }
       }
     }
   } else {
   // ---- this warp's rows and column share
-  const int rp = warp / P.QW, q = warp - rp * P.QW;
-  const int ch_begin = q * P.cpw, ch_end = min(ch_begin + P.cpw, P.nchunks);
-  const int row_a = 2 * rp;
+  const int QW = P.QW;
+  const int rg = warp / QW, q = warp - rg * QW;
+  // chunks split as evenly as possible, the larger shares first (warps q, q + 4, ...
+  // share an SM sub-partition, so each sub-partition gets an even load)
+  const int ch_base = P.nchunks / QW, ch_extra = P.nchunks - ch_base * QW;
+  const int ch_begin = q * ch_base + min(q, ch_extra);
+  const int ch_end = ch_begin + ch_base + (q < ch_extra ? 1 : 0);
+  const int row_a = RPW * rg;
+  // fixed shared-memory offsets of this lane's codes and (scale, offset) words
+  int off_c[RPW][MAXC], off_p[RPW][MAXC];
+  bool lane_ok[MAXC];
+#pragma unroll
+  for (int u = 0; u < MAXC; ++u) {
+    const int ch = min(ch_begin + u, P.nchunks - 1);
+    const int col = min(ch * CW + lane * EPL, cols - EPL);
+    lane_ok[u] = (ch_begin + u < ch_end) && (ch_begin + u) * CW + lane * EPL < cols;
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) {
+      off_c[r][u] = ((row_a + r) * cols + col) * ESZ;
+      off_p[r][u] = P.code_bytes + ((row_a + r) * (cols >> 5) + (col >> 5)) * 4;
+    }
+  }
   float2 xr[NB == 1 ? MAXC : 1][EPL / 2];
   float xsum[NB == 1 ? MAXC : 1];   // Σ of this lane's input values per chunk
-  int xr_input = -1;
 
-  int buf = 0;
-  const uint64_t t_start = tc::globaltimer();
+  // per-job values, reloaded when the task walk enters the next job
+  int j = -1, job_end = 0, job_first = 0, rows_j = 0, input_j = -1, epi_j = 0;
+  float* y_j = nullptr;
+  const float* res_j = nullptr;
+  int buf = 0, s = 0;
+  uint32_t parity = 0;
 
   for (int t = t0; t < t1; ++t) {
-    const int s = (t - t0) % GT_NST;
-    const uint32_t parity = (uint32_t)(((t - t0) / GT_NST) & 1);
-    const int j = gt_job(P, t);
-    const int row0 = (t - P.task_begin[j]) * P.SR;
-    const int nr = min(P.SR, P.rows[j] - row0);
-    const int input = P.input[j];
-    const bool ok = wait_bar(tc::smem_addr(full + s), parity);
-    float2 acc[2][NB][NA];
-#pragma unroll
-    for (int r = 0; r < 2; ++r)
-#pragma unroll
-      for (int b = 0; b < NB; ++b)
-#pragma unroll
-        for (int a = 0; a < NA; ++a) acc[r][b][a] = make_float2(0.f, 0.f);
-    if (ok) {
-      const float* xin = xs + (size_t)input * NB * cols_pad + lane * 4;
+    if (t >= job_end) {
+      j = job_of(t, j < 0 ? 0 : j);
+      job_first = P.task_begin[j];
+      job_end = P.task_begin[j + 1];
+      rows_j = P.rows[j];
+      epi_j = P.epi[j];
+      y_j = P.y[j];
+      res_j = P.residual[j];
+      const int input = P.input[j];
       if constexpr (NB == 1) {
-        if (input != xr_input) {
+        if (input != input_j) {
+          const float* xin = xs + (size_t)input * cols_pad + lane * 4;
 #pragma unroll
           for (int u = 0; u < MAXC; ++u) {
 #pragma unroll
@@ -225,45 +251,67 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
               xr[u][2 * k] = make_float2(a.x, a.y);
               xr[u][2 * k + 1] = make_float2(a.z, a.w);
             }
-            float2 t = xr[u][0];
+            float2 sum2 = xr[u][0];
 #pragma unroll
-            for (int k = 1; k < EPL / 2; ++k) t = fadd2(t, xr[u][k]);
-            xsum[u] = t.x + t.y;
+            for (int k = 1; k < EPL / 2; ++k) sum2 = fadd2(sum2, xr[u][k]);
+            xsum[u] = sum2.x + sum2.y;
           }
-          xr_input = input;
         }
       }
+      input_j = input;
+    }
+    const int row0 = (t - job_first) * P.SR;
+    const int nr = min(P.SR, rows_j - row0);
+    // warp-uniform: every lane of the warp leaves the same way
+    const bool ok = __all_sync(0xffffffffu, wait_bar(tc::smem_addr(full + s), parity));
+    float2 acc[RPW][NB][NA];
+#pragma unroll
+    for (int r = 0; r < RPW; ++r)
+#pragma unroll
+      for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int a = 0; a < NA; ++a) acc[r][b][a] = make_float2(0.f, 0.f);
+    if (ok) {
+      const float* xin = xs + (size_t)input_j * NB * cols_pad + lane * 4;
       const uint8_t* st = ring + (size_t)s * P.stage_bytes;
-#pragma unroll
-      for (int u = 0; u < MAXC; ++u) {
-        const int ch = ch_begin + u;
-        if (ch < ch_end && ch * CW + lane * EPL < cols) {
-          const int col = ch * CW + lane * EPL;
 #if PGQ_DOT_MODE != 0
-          if constexpr (Q8 && NB == 1) {
-            // dot then scale: Σ u·x with the biased byte u = q + 128 in [0, 255], then
-            // y += scale·dot + (offset − 128·scale)·Σx  (one pair of FMAs per 16 codes)
+      if constexpr (Q8 && NB == 1) {
+        // dot then scale: Σ u·x with the biased byte u = q + 128 in [0, 255], then
+        // y += scale·dot + (offset − 128·scale)·Σx.  Every shared-memory read of the
+        // stage is issued first (fixed per-warp offsets), then the arithmetic.
+        uint4 cw[RPW][MAXC];
+        uint32_t pw[RPW][MAXC];
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              const int row = row_a + r;
-              const uint4 cw = *reinterpret_cast<const uint4*>(st + (size_t)row * cols + col);
-              const uint32_t pw =
-                  *reinterpret_cast<const uint32_t*>(st + P.code_bytes + ((size_t)row * (cols >> 5) + (col >> 5)) * 4);
-              const float2 so = h2_to_f2(pw);
-              const uint32_t words[4] = {cw.x ^ 0x80808080u, cw.y ^ 0x80808080u, cw.z ^ 0x80808080u,
-                                         cw.w ^ 0x80808080u};
+        for (int u = 0; u < MAXC; ++u)
+#pragma unroll
+          for (int r = 0; r < RPW; ++r) {
+            cw[r][u] = *reinterpret_cast<const uint4*>(st + off_c[r][u]);
+            pw[r][u] = *reinterpret_cast<const uint32_t*>(st + off_p[r][u]);
+          }
+#pragma unroll
+        for (int u = 0; u < MAXC; ++u) {
+          if (lane_ok[u]) {
+#pragma unroll
+            for (int r = 0; r < RPW; ++r) {
+              const float2 so = h2_to_f2(pw[r][u]);
+              const uint32_t words[4] = {cw[r][u].x ^ 0x80808080u, cw[r][u].y ^ 0x80808080u,
+                                         cw[r][u].z ^ 0x80808080u, cw[r][u].w ^ 0x80808080u};
               float2 d0 = make_float2(0.f, 0.f), d1 = make_float2(0.f, 0.f);
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
                 float2 lo, hi;
-#if PGQ_DOT_MODE == 2
-                lo = make_float2(__uint2float_rn(words[k] & 0xffu), __uint2float_rn((words[k] >> 8) & 0xffu));
-                hi = make_float2(__uint2float_rn((words[k] >> 16) & 0xffu), __uint2float_rn(words[k] >> 24));
-#elif PGQ_DOT_MODE == 3
+#if PGQ_DOT_MODE == 3
                 // one byte-permute makes two binary16 values 1024 + u (exact), widened
                 // to f32; the 1024 joins the 128 of the bias below
                 lo = h2_to_f2(__byte_perm(words[k], 0x64646464u, 0x4140));
                 hi = h2_to_f2(__byte_perm(words[k], 0x64646464u, 0x4342));
+#elif PGQ_DOT_MODE == 4
+                // one byte-permute makes the f32 2^15 + u exactly (u in mantissa bits
+                // 8..15, exponent 15); the 2^15·Σx it adds is taken out per chunk below
+                lo = make_float2(__uint_as_float(__byte_perm(words[k], 0x47000000u, 0x7504)),
+                                 __uint_as_float(__byte_perm(words[k], 0x47000000u, 0x7514)));
+                hi = make_float2(__uint_as_float(__byte_perm(words[k], 0x47000000u, 0x7524)),
+                                 __uint_as_float(__byte_perm(words[k], 0x47000000u, 0x7534)));
 #else
                 const float2 m23 = make_float2(-8388608.0f, -8388608.0f);
                 lo = fadd2(make_float2(__uint_as_float(__byte_perm(words[k], 0x4B000000u, 0x7540)),
@@ -281,65 +329,74 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
               const float c = fmaf(-128.f, so.x, so.y);
 #endif
               float2 a = acc[r][0][0];
+#if PGQ_DOT_MODE == 4
+              a.x = fmaf(so.x, fmaf(-32768.f, xsum[u], d.x + d.y), a.x);
+#else
               a.x = fmaf(so.x, d.x + d.y, a.x);
+#endif
               a.y = fmaf(c, xsum[u], a.y);
               acc[r][0][0] = a;
             }
-            continue;
           }
+        }
+      } else
 #endif
-          float2 wv[2][EPL / 2];
+      {
 #pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const int row = row_a + r;
-            const uint4 cw = *reinterpret_cast<const uint4*>(st + ((size_t)row * cols + col) * ESZ);
-            if constexpr (Q8) {
-              const uint32_t pw =
-                  *reinterpret_cast<const uint32_t*>(st + P.code_bytes + ((size_t)row * (cols >> 5) + (col >> 5)) * 4);
-              const float2 so = h2_to_f2(pw);
-              const float2 s2 = make_float2(so.x, so.x), o2 = make_float2(so.y, so.y);
-              const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+        for (int u = 0; u < MAXC; ++u) {
+          const int ch = ch_begin + u;
+          if (ch < ch_end && ch * CW + lane * EPL < cols) {
+            float2 wv[RPW][EPL / 2];
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                float2 lo, hi;
-                s8x4_to_f32(words[k], lo, hi);
-                wv[r][2 * k] = ffma2(lo, s2, o2);
-                wv[r][2 * k + 1] = ffma2(hi, s2, o2);
+            for (int r = 0; r < RPW; ++r) {
+              const uint4 cw = *reinterpret_cast<const uint4*>(st + off_c[r][u]);
+              if constexpr (Q8) {
+                const uint32_t pw = *reinterpret_cast<const uint32_t*>(st + off_p[r][u]);
+                const float2 so = h2_to_f2(pw);
+                const float2 s2 = make_float2(so.x, so.x), o2 = make_float2(so.y, so.y);
+                const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  float2 lo, hi;
+                  s8x4_to_f32(words[k], lo, hi);
+                  wv[r][2 * k] = ffma2(lo, s2, o2);
+                  wv[r][2 * k + 1] = ffma2(hi, s2, o2);
+                }
+              } else {
+                wv[r][0] = h2_to_f2(cw.x); wv[r][1] = h2_to_f2(cw.y);
+                wv[r][2] = h2_to_f2(cw.z); wv[r][3] = h2_to_f2(cw.w);
               }
-            } else {
-              wv[r][0] = h2_to_f2(cw.x); wv[r][1] = h2_to_f2(cw.y);
-              wv[r][2] = h2_to_f2(cw.z); wv[r][3] = h2_to_f2(cw.w);
             }
-          }
-          if constexpr (NB == 1) {
+            if constexpr (NB == 1) {
 #pragma unroll
-            for (int r = 0; r < 2; ++r)
+              for (int r = 0; r < RPW; ++r)
 #pragma unroll
-              for (int k = 0; k < EPL / 2; ++k) acc[r][0][k % NA] = ffma2(wv[r][k], xr[u][k], acc[r][0][k % NA]);
-          } else {
-            const float* xc = xin + (size_t)ch * CW;
+                for (int k = 0; k < EPL / 2; ++k) acc[r][0][k % NA] = ffma2(wv[r][k], xr[u][k], acc[r][0][k % NA]);
+            } else {
+              const float* xc = xin + (size_t)ch * CW;
 #pragma unroll
-            for (int b = 0; b < NB; ++b) {
-              float2 xv[EPL / 2];
+              for (int b = 0; b < NB; ++b) {
+                float2 xv[EPL / 2];
 #pragma unroll
-              for (int k = 0; k < EPL / 4; ++k) {
-                const float4 a = *reinterpret_cast<const float4*>(xc + (size_t)b * cols_pad + k * 128);
-                xv[2 * k] = make_float2(a.x, a.y);
-                xv[2 * k + 1] = make_float2(a.z, a.w);
+                for (int k = 0; k < EPL / 4; ++k) {
+                  const float4 a = *reinterpret_cast<const float4*>(xc + (size_t)b * cols_pad + k * 128);
+                  xv[2 * k] = make_float2(a.x, a.y);
+                  xv[2 * k + 1] = make_float2(a.z, a.w);
+                }
+#pragma unroll
+                for (int r = 0; r < RPW; ++r)
+#pragma unroll
+                  for (int k = 0; k < EPL / 2; ++k) acc[r][b][0] = ffma2(wv[r][k], xv[k], acc[r][b][0]);
               }
-#pragma unroll
-              for (int r = 0; r < 2; ++r)
-#pragma unroll
-                for (int k = 0; k < EPL / 2; ++k) acc[r][b][0] = ffma2(wv[r][k], xv[k], acc[r][b][0]);
             }
           }
         }
       }
-      // lane reduction: 2 rows x NB positions
-      constexpr int N = 2 * NB;
+      // lane reduction: RPW rows x NB positions
+      constexpr int N = RPW * NB;
       float v[N];
 #pragma unroll
-      for (int r = 0; r < 2; ++r)
+      for (int r = 0; r < RPW; ++r)
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
           float2 a = acc[r][b][0];
@@ -351,57 +408,59 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
       if ((lane & (32 / N - 1)) == 0) {
         const int idx = lane / (32 / N);
         const int r = idx / NB, b = idx - r * NB;
-        red[(((size_t)buf * P.SR + row_a + r) * NB + b) * P.QW + q] = tot;
+        red[(((size_t)buf * P.SR + row_a + r) * NB + b) * QW + q] = tot;
       }
     }
     // the warp's reads of the stage are done: release the slot to the producer
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(tc::smem_addr(empty + s));
-    // the QW warps of this row pair meet; all leave together if one wait expired
+    // the QW warps of the row group meet (named barrier; all leave together if one
+    // wait expired); then its first warp adds the partial sums in fixed order,
+    // applies the epilogue and stores
     {
       uint32_t all;
       asm volatile(
           "{\n\t.reg .pred p, r;\n\tsetp.ne.u32 p, %1, 0;\n\t"
           "bar.red.and.pred r, %2, %3, p;\n\tselp.u32 %0, 1, 0, r;\n\t}"
           : "=r"(all)
-          : "r"((uint32_t)ok), "r"(1 + rp), "r"(P.QW * 32)
+          : "r"((uint32_t)ok), "r"(1 + rg), "r"(QW * 32)
           : "memory");
       if (!all) break;
     }
-    // the row pair's column shares summed in fixed order, epilogue, store
-    // (lanes b*2 + r of the pair's first warp)
     if (q == 0) {
-      const int b = lane >> 1, r = lane & 1;
-      const bool act = lane < 2 * NB;
+      const int b = lane / RPW, r = lane - b * RPW;
+      const bool act = lane < RPW * NB;
       float out = 0.f;
-      const int rows = P.rows[j];
       const int row = row0 + row_a + r;
       const bool live = act && row_a + r < nr && b < P.B;
       if (act) {
-        const float* rr = red + (((size_t)buf * P.SR + row_a + r) * NB + b) * P.QW;
-        for (int k = 0; k < P.QW; ++k) out += rr[k];
+        const float* rr = red + (((size_t)buf * P.SR + row_a + r) * NB + b) * QW;
+        for (int k = 0; k < QW; ++k) out += rr[k];
         if (live) {
-          if (P.epi[j] == PGQ_EPI_RELU2) {
+          if (epi_j == PGQ_EPI_RELU2) {
             out = fmaxf(out, 0.f);
             out = out * out;
-          } else if (P.epi[j] == PGQ_EPI_ADD) {
-            out += P.residual[j][(size_t)b * rows + row];
+          } else if (epi_j == PGQ_EPI_ADD) {
+            out += res_j[(size_t)b * rows_j + row];
           }
-          if (P.y[j]) P.y[j][(size_t)b * rows + row] = out;
+          if (y_j) y_j[(size_t)b * rows_j + row] = out;
         }
       }
       if constexpr (ARGMAX) {
         float cv = live ? out : __int_as_float(0xff800000u);
         int ci = live ? row : 0x7fffffff;
-        const float ov = __shfl_down_sync(0xffffffffu, cv, 1);
-        const int oi = __shfl_down_sync(0xffffffffu, ci, 1);
-        if (r == 0) argmax_merge(cv, ci, ov, oi);
+#pragma unroll
+        for (int o = 1; o < RPW; o <<= 1) {
+          const float ov = __shfl_down_sync(0xffffffffu, cv, o);
+          const int oi = __shfl_down_sync(0xffffffffu, ci, o);
+          argmax_merge(cv, ci, ov, oi);
+        }
         if (act && r == 0) argmax_merge(best_v, best_i, cv, ci);
       }
     }
     buf ^= 1;
+    if (++s == GT_NST) { s = 0; parity ^= 1u; }
   }
-  (void)t_start;
   }  // computing warps
   // leave no bulk copy in flight (an aborted block may have issued ahead)
   if (producer && lane == 0 && *(volatile int*)&s_abort) {
@@ -414,20 +473,19 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
   }
 
   if constexpr (ARGMAX) {
-    // each row pair's first warp holds its best per position (lanes 2b)
-    __shared__ float s_bv[8 * 8];
-    __shared__ int s_bi[8 * 8];
+    // each group's first warp holds its best per position (lanes RPW·b); the others hold the floor
+    __shared__ float s_bv[W * 8];
+    __shared__ int s_bi[W * 8];
     __syncthreads();
-    const int npairs = P.SR / 2;
-    if (!producer && (warp % P.QW) == 0 && lane < 2 * NB && (lane & 1) == 0) {
-      s_bv[(warp / P.QW) * 8 + (lane >> 1)] = best_v;
-      s_bi[(warp / P.QW) * 8 + (lane >> 1)] = best_i;
+    if (!producer && lane < RPW * NB && (lane % RPW) == 0) {
+      s_bv[warp * 8 + lane / RPW] = best_v;
+      s_bi[warp * 8 + lane / RPW] = best_i;
     }
     __syncthreads();
     if (tid < P.B) {
       float bv = ARGMAX_FLOOR;
       int bi = 0;
-      for (int g = 0; g < npairs; ++g) argmax_merge(bv, bi, s_bv[g * 8 + tid], s_bi[g * 8 + tid]);
+      for (int w = 0; w < W; ++w) argmax_merge(bv, bi, s_bv[w * 8 + tid], s_bi[w * 8 + tid]);
       P.part_val[(size_t)blockIdx.x * P.B + tid] = bv;
       P.part_idx[(size_t)blockIdx.x * P.B + tid] = bi;
     }
@@ -456,10 +514,10 @@ using GtFn = void (*)(GtParams);
 template <bool Q8, bool AM>
 GtFn gt_pick(int nb) {
   switch (nb) {
-    case 1: return reinterpret_cast<GtFn>(&gemv_tma_kernel<Q8, 1, AM>);
-    case 2: return reinterpret_cast<GtFn>(&gemv_tma_kernel<Q8, 2, AM>);
-    case 4: return reinterpret_cast<GtFn>(&gemv_tma_kernel<Q8, 4, AM>);
-    default: return reinterpret_cast<GtFn>(&gemv_tma_kernel<Q8, 8, AM>);
+    case 1: return reinterpret_cast<GtFn>(&gemv_tma_kernel<Q8, 1, AM, 16, 2, 2>);
+    case 2: return reinterpret_cast<GtFn>(&gemv_tma_kernel<Q8, 2, AM, 16, 2, 2>);
+    case 4: return reinterpret_cast<GtFn>(&gemv_tma_kernel<Q8, 4, AM, 16, 2, 2>);
+    default: return reinterpret_cast<GtFn>(&gemv_tma_kernel<Q8, 8, AM, 16, 2, 2>);
   }
 }
 }  // namespace
@@ -474,10 +532,11 @@ int launch_gemv_tma(const GvParams& V, bool q8, bool argmax, const DeviceInfo& d
   while (SR > 2 && (size_t)SR * row_bytes > GT_STAGE_MAX) SR >>= 1;
   if ((size_t)SR * row_bytes > GT_STAGE_MAX) return PGQ_EUNSUPPORTED;
   if (SR * nb > 64) return PGQ_EUNSUPPORTED;
-  const int QW = 32 / SR;
   const int nchunks = (V.cols + CW - 1) / CW;
+  constexpr int W = 16, RPW = 2, MAXC = 2;   // the launch shape (see gemv_tma_kernel)
+  const int QW = W * RPW / SR;
   const int cpw = (nchunks + QW - 1) / QW;
-  if (cpw > 2) return PGQ_EUNSUPPORTED;
+  if (cpw > MAXC) return PGQ_EUNSUPPORTED;
   GtParams P{};
   int t = 0;
   for (int j = 0; j < V.njobs; ++j) {
@@ -513,7 +572,7 @@ int launch_gemv_tma(const GvParams& V, bool q8, bool argmax, const DeviceInfo& d
   P.ticket = V.ticket;
   P.ids = V.ids;
   P.wait_limit_ns = 2000000000ull;
-  const size_t smem = (size_t)V.ninputs * nb * P.cols_pad * 4 + 2 * (size_t)SR * nb * QW * 4 + 128 +
+  const size_t smem = (size_t)V.ninputs * nb * P.cols_pad * 4 + GT_RED * (size_t)SR * nb * QW * 4 + 128 +
                       (size_t)GT_NST * P.stage_bytes + 2 * GT_NST * 8 + 64;
   if (smem + 1024 > dev.smem_optin) return PGQ_EUNSUPPORTED;
   GtFn fn = q8 ? (argmax ? gt_pick<true, true>(nb) : gt_pick<true, false>(nb))
@@ -536,7 +595,7 @@ int launch_gemv_tma(const GvParams& V, bool q8, bool argmax, const DeviceInfo& d
   }
   const int grid = std::max(1, std::min(dev.sms, P.ntasks));
   void* args[] = {&P};
-  return cuda_status(cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(grid), dim3(GT_THREADS), args, smem, st));
+  return cuda_status(cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(grid), dim3((W + 1) * 32), args, smem, st));
 }
 
 int decode_status_read_and_clear(int* out) {
