@@ -389,7 +389,7 @@ def bench_vocab(torch, pgq, synth, steps, warmup, pk):
     return out
 
 
-def bench_moe(torch, pgq, synth, steps, warmup, pk):
+def bench_moe(torch, pgq, synth, steps, warmup, pk, graph=True):
     c = synth.MOE
     E, H, I, B, k, wl = c["experts"], c["hidden"], c["inter"], c["B"], c["topk"], c["workload"]
     router, up, down = synth.moe_layer(wl, E, H, I, "torch", "cuda")
@@ -406,7 +406,7 @@ def bench_moe(torch, pgq, synth, steps, warmup, pk):
         pgq.moe_prefill_layer(Wm, h, g1, g2, 1e-6, y=y, workspace=ws)
 
     ms = time_loop(torch, step, steps, warmup)
-    ms_graph = time_graph(torch, step, steps, warmup)
+    ms_graph = time_graph(torch, step, steps, warmup) if graph else ms
     taps = pgq.moe_layer_taps(Wm, ws, B)
     touched = int((taps["counts"] > 0).sum().item())
     per_expert = 2 * (I * H + I * (H // 32) * 4)
@@ -416,7 +416,8 @@ def bench_moe(torch, pgq, synth, steps, warmup, pk):
             "metric": "positions/s", "value": round(B / (ms_graph * 1e-3), 1), "ms_per_layer": round(ms_graph, 4),
             "ms_per_layer_api": round(ms, 4), "touched_experts": touched, "weight_bytes": nbytes,
             "weight_GBps": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm"], 4), "launches_per_step": 7,
-            "timed": "CUDA-graph replay of the layer call (ms_per_layer_api: direct calls)"}
+            "timed": ("CUDA-graph replay of the layer call (ms_per_layer_api: direct calls)" if graph
+                      else "direct calls (no graph)")}
 
 
 def time_e2e(torch, W, steps, warmup):
@@ -464,6 +465,7 @@ def main():
     ap.add_argument("--skip-prefill", action="store_true", help="only the headline decode layer")
     ap.add_argument("--only", choices=["decode", "prefill", "moe", "vocab"], default=None,
                     help="profiling aid: run one workload and print its JSON object")
+    ap.add_argument("--no-graph", action="store_true", help="profiling aid (--only moe): direct calls only")
     ap.add_argument("--prefill-layers", type=int, default=None, help="layers of the prefill pass (default 32)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -496,7 +498,8 @@ def main():
         print(json.dumps(time_prefill(torch, P, args.steps, args.warmup, pk)), flush=True)
         return
     if args.only == "moe":
-        print(json.dumps(bench_moe(torch, pgq, synth, args.steps, args.warmup, pk)), flush=True)
+        print(json.dumps(bench_moe(torch, pgq, synth, args.steps, args.warmup, pk, graph=not args.no_graph)),
+              flush=True)
         return
     if args.only == "vocab":
         print(json.dumps(bench_vocab(torch, pgq, synth, args.steps, args.warmup, pk)), flush=True)

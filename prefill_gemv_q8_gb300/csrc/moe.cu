@@ -10,6 +10,9 @@
 // entry) and `pb_add_rms` with add = 2 (weighted sum of the slots, then the norm).
 #include <algorithm>
 
+#include <map>
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -298,7 +301,9 @@ moe_bank_kernel(const __grid_constant__ MoeBank P) {
   const int nblk = (P.rows + MB_ROWS - 1) / MB_ROWS;
   // task prefix over experts (every block computes the same list): the counts are
   // read in parallel, then a fixed-order scan in shared memory
-  for (int e = threadIdx.x; e < P.E; e += blockDim.x) s_pre[e + 1] = ((P.counts[e] + MB_ENT - 1) / MB_ENT) * nblk;
+  // (counts clamped to [0, nentries]: a bad count cannot send a block out of range)
+  for (int e = threadIdx.x; e < P.E; e += blockDim.x)
+    s_pre[e + 1] = ((min(max(P.counts[e], 0), P.nentries) + MB_ENT - 1) / MB_ENT) * nblk;
   __syncthreads();
   if (threadIdx.x == 0) {
     s_pre[0] = 0;
@@ -317,10 +322,11 @@ moe_bank_kernel(const __grid_constant__ MoeBank P) {
     if (e != cur_e || chunk != cur_c) {
       __syncthreads();
       const int first = P.offsets[e] + chunk * MB_ENT;
-      nent = min(MB_ENT, P.counts[e] - chunk * MB_ENT);
+      nent = min(MB_ENT, min(max(P.counts[e], 0), P.nentries) - chunk * MB_ENT);
       if (threadIdx.x < MB_ENT) {
         int j = 0;
-        if ((int)threadIdx.x < nent && first + (int)threadIdx.x < P.nentries) j = P.entries[first + threadIdx.x];
+        const int at = first + (int)threadIdx.x;
+        if ((int)threadIdx.x < nent && at >= 0 && at < P.nentries) j = P.entries[at];
         s_ent[threadIdx.x] = (j >= 0 && j < P.nentries) ? j : 0;
       }
       __syncthreads();
@@ -380,13 +386,42 @@ moe_combine_kernel(float* __restrict__ h, const float* __restrict__ o, const flo
 }
 
 // ------------------------------------------------------------------ launchers
+namespace {
+// Function attributes and occupancy are set/queried once per (kernel, device, size),
+// so a launch made under stream capture issues nothing but the launch itself.
+std::mutex g_moe_mu;
+cudaError_t moe_allow_smem(const void* fn, int device, size_t smem) {
+  std::lock_guard<std::mutex> lk(g_moe_mu);
+  static std::map<std::pair<const void*, int>, size_t> done;
+  size_t& cur = done[{fn, device}];
+  if (smem <= cur) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess) cur = smem;
+  return e;
+}
+int bank_blocks_per_sm(int device, size_t smem) {
+  std::lock_guard<std::mutex> lk(g_moe_mu);
+  static std::map<std::pair<int, size_t>, int> known;
+  auto it = known.find({device, smem});
+  if (it != known.end()) return it->second;
+  int occ = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, moe_bank_kernel, MB_WARPS * 32, smem) != cudaSuccess) {
+    cudaGetLastError();
+    occ = 1;
+  }
+  occ = std::max(1, std::min(occ, 2));
+  known[{device, smem}] = occ;
+  return occ;
+}
+}  // namespace
+
 int launch_router(const float* R, const float* n, int B, int E, int cols, float* logits, const DeviceInfo& dev,
                   cudaStream_t st) {
   if (cols > 32 * RT_MAXV) return set_error(PGQ_EUNSUPPORTED, "router: cols=%d > %d", cols, 32 * RT_MAXV);
   const size_t smem = (size_t)RT_POS * cols * sizeof(float);
   if (smem > dev.smem_optin) return set_error(PGQ_EUNSUPPORTED, "router: %zu bytes of shared memory", smem);
-  cudaError_t e = cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return cuda_status(e);
+  if (cudaError_t e = moe_allow_smem(reinterpret_cast<const void*>(router_kernel), dev.device, smem); e != cudaSuccess)
+    return cuda_status(e);
   dim3 grid((E + RT_WARPS - 1) / RT_WARPS, (B + RT_POS - 1) / RT_POS);
   router_kernel<<<grid, RT_WARPS * 32, smem, st>>>(R, n, B, E, cols, logits);
   return cuda_status(cudaGetLastError());
@@ -428,14 +463,9 @@ int launch_moe_bank(const MoeBankArgs& a, const DeviceInfo& dev, cudaStream_t st
   P.epilogue = a.epilogue;
   const size_t smem = (size_t)MB_ENT * P.cols_pad * sizeof(float);
   if (smem + 8192 > dev.smem_optin) return set_error(PGQ_EUNSUPPORTED, "expert bank: cols=%d too large", a.cols);
-  cudaError_t e = cudaFuncSetAttribute(moe_bank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return cuda_status(e);
-  int occ = 1;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, moe_bank_kernel, MB_WARPS * 32, smem) != cudaSuccess) {
-    cudaGetLastError();
-    occ = 1;
-  }
-  occ = std::max(1, std::min(occ, 2));
+  if (cudaError_t e = moe_allow_smem(reinterpret_cast<const void*>(moe_bank_kernel), dev.device, smem); e != cudaSuccess)
+    return cuda_status(e);
+  const int occ = bank_blocks_per_sm(dev.device, smem);
   void* args[] = {&P};
   return cuda_status(cudaLaunchKernel(reinterpret_cast<const void*>(moe_bank_kernel), dim3(dev.sms * occ),
                                       dim3(MB_WARPS * 32), args, smem, st));
