@@ -245,7 +245,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   __shared__ float s_xinv[TC_ACC_COLS];
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
   auto bar = [&](int i) { return tc::smem_addr(bars + i); };
   auto stage_codes = [&](int s) { return stages + s * stage_bytes; };
@@ -505,60 +504,88 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
       if (whole) {
         out_rows(acc4, nvec, et, epi, y, res, rows, row0, vec_ok);
       } else {
-        // f32 partial of this block for the tile, then the last block to finish sums
-        const int first_tile = beg / ks;
-        float4* part = reinterpret_cast<float4*>(P.partials +
-                                                 ((size_t)blockIdx.x * P.maxseg + (tile - first_tile)) * Bp * TC_BM);
+        const int c_first = cta_of_item(tile * ks, G, T);
+        const int c_last = cta_of_item(tile_end - 1, G, T);
+        if ((int)blockIdx.x != c_first) {
+          // a contributor: publish this block's f32 partial of the tile, then count it
+          // on the tile's counter (one gpu-scope release after the block's stores)
+          const int first_tile = beg / ks;
+          float4* part = reinterpret_cast<float4*>(P.partials +
+                                                   ((size_t)blockIdx.x * P.maxseg + (tile - first_tile)) * Bp * TC_BM);
 #pragma unroll
-        for (int k = 0; k < TC_OUT_K; ++k)
-          if (et + 128 * k < nvec) part[et + 128 * k] = acc4[et + 128 * k];
-        // all partial stores of the block happen before one gpu-scope release
-        // (barrier + cumulative fence), then the ticket
-        epi_bar();
-        if (et == 0) TRACE(3, 2, it);
-        if (et == 0) {
-          const int c_first = cta_of_item(tile * ks, G, T);
-          const int c_last = cta_of_item(tile_end - 1, G, T);
-          const unsigned n = (unsigned)(c_last - c_first + 1);
-          asm volatile("fence.acq_rel.gpu;" ::: "memory");
-          const unsigned old = atomicAdd(P.tile_cnt + tile, 1u);
-          asm volatile("fence.acq_rel.gpu;" ::: "memory");
-          *last_flag = (old == n - 1) ? 1 : 0;
-        }
-        epi_bar();
-        if (et == 0) TRACE(3, 3, it);
-        if (*last_flag) {
-          const int c_first = cta_of_item(tile * ks, G, T);
-          const int c_last = cta_of_item(tile_end - 1, G, T);
-          // sum the contributors' partials in block order into the shared tile
-          // (this thread's own float4 slots only); 8 loads in flight at a time
-          float4* sum4 = reinterpret_cast<float4*>(s_acc);
-          for (int c = c_first; c <= c_last; ++c) {
-            const int ft = item_begin(c, G, T) / ks;
-            const float4* pc =
-                reinterpret_cast<const float4*>(P.partials + ((size_t)c * P.maxseg + (tile - ft)) * Bp * TC_BM);
-#pragma unroll
-            for (int h = 0; h < TC_OUT_P; ++h) {
-              float4 u[TC_OUT_H];
-#pragma unroll
-              for (int k = 0; k < TC_OUT_H; ++k) {
-                const int i = et + 128 * (h * TC_OUT_H + k);
-                if (i < nvec) u[k] = __ldcg(pc + i);
+          for (int k = 0; k < TC_OUT_K; ++k)
+            if (et + 128 * k < nvec) part[et + 128 * k] = acc4[et + 128 * k];
+          epi_bar();
+          if (et == 0) {
+            asm volatile("fence.acq_rel.gpu;" ::: "memory");
+            atomicAdd(P.tile_cnt + tile, 1u);
+          }
+          if (et == 0) TRACE(3, 2, it);
+        } else {
+          // the owner (the block holding the tile's first k-steps, which it reaches at
+          // the end of its range): wait for the other contributors' partials, add them
+          // in block order to its own accumulator and write the tile.  Blocks only ever
+          // wait for higher-numbered blocks, and the launch is cooperative (all blocks
+          // resident), so the waits always end.
+          bool ok = true;
+          if (et == 0) {
+            const unsigned need = (unsigned)(c_last - c_first);
+            const uint64_t w0 = tc::globaltimer();
+            while (true) {
+              unsigned v;
+              asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(P.tile_cnt + tile) : "memory");
+              if (v >= need) break;
+              if (*abort_flag || tc::globaltimer() - w0 > P.wait_limit_ns) {
+                *abort_flag = 1;
+                atomicCAS(P.status, 0, PGQ_ETIMEOUT);
+                ok = false;
+                break;
               }
+              __nanosleep(64);
+            }
+            P.tile_cnt[tile] = 0u;
+          }
+          if (!epi_all(ok)) break;
+          if (et == 0) TRACE(3, 2, it);
+          // the contributors' partials land in the (now idle) stage ring, a batch of
+          // whole partials at a time, each thread copying and adding its own float4 slots
+          const int part_f4 = Bp * TC_BM / 4;
+          const int per_batch = (TC_STAGES * stage_bytes) / (part_f4 * 16);
+          float4* ring4 = reinterpret_cast<float4*>(stages);
+          float4* sum4 = reinterpret_cast<float4*>(s_acc);
+          for (int c0 = c_first + 1; c0 <= c_last; c0 += per_batch) {
+            const int c1 = min(c_last, c0 + per_batch - 1);
+            for (int c = c0; c <= c1; ++c) {
+              const int ft = item_begin(c, G, T) / ks;
+              const float4* pc =
+                  reinterpret_cast<const float4*>(P.partials + ((size_t)c * P.maxseg + (tile - ft)) * Bp * TC_BM);
+              float4* dst = ring4 + (size_t)(c - c0) * part_f4;
 #pragma unroll
-              for (int k = 0; k < TC_OUT_H; ++k) {
-                const int i = et + 128 * (h * TC_OUT_H + k);
+              for (int k = 0; k < TC_OUT_K; ++k) {
+                const int i = et + 128 * k;
+                if (i < nvec)
+                  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_addr(dst + i)),
+                               "l"(pc + i)
+                               : "memory");
+              }
+            }
+            asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+            for (int c = c0; c <= c1; ++c) {
+              const float4* src = ring4 + (size_t)(c - c0) * part_f4;
+#pragma unroll
+              for (int k = 0; k < TC_OUT_K; ++k) {
+                const int i = et + 128 * k;
                 if (i < nvec) {
-                  float4 t4 = c == c_first ? make_float4(0.f, 0.f, 0.f, 0.f) : sum4[i];
-                  t4.x += u[k].x; t4.y += u[k].y; t4.z += u[k].z; t4.w += u[k].w;
+                  const float4 u = src[i];
+                  float4 t4 = sum4[i];
+                  t4.x += u.x; t4.y += u.y; t4.z += u.z; t4.w += u.w;
                   sum4[i] = t4;
                 }
               }
             }
           }
-          epi_bar();
           out_rows(acc4, nvec, et, epi, y, res, rows, row0, vec_ok);
-          if (et == 0) P.tile_cnt[tile] = 0u;
+          if (et == 0) TRACE(3, 3, it);
         }
       }
       epi_bar();  // the shared tile is free for the next segment
@@ -781,8 +808,20 @@ int launch_prefill(const PrefillJob* jobs, int njobs, const float* X, int cols, 
       cur = smem;
     }
   }
+  // cooperative: the owner of a tile split between blocks waits for the others'
+  // partials, so every block of the launch must be resident at once
   void* args[] = {&P};
-  return cuda_status(cudaLaunchKernel(fn, dim3(pl.G), dim3(TC_THREADS), args, smem, st));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pl.G);
+  cfg.blockDim = dim3(TC_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_status(cudaLaunchKernelExC(&cfg, fn, args));
 }
 
 }  // namespace pgq
