@@ -19,7 +19,7 @@
  *                     w[r][c] = scale[r][c/32] * codes[r][c] + offset[r][c/32]
  *
  * The projection is the one the cortiq-engine pages compute in gemma_batch.rs
- * (`encode_q82_mm` / `q8_2f_mm_r2`: "y[nb][rows] = x[nb][cols]·Wᵀ") and in the row
+ * (`encode_q82_mm` / `q8_2f_mm_r2`: y[nb][rows] = x[nb][cols]·Wᵀ) and in the row
  * kernels the header of embryo_wide.wgsl describes (matrices kept in their packed
  * form on the device and read in 16-byte loads).  The q8 block format (int8 codes
  * with a binary16 scale and offset per 32-element block along the row) is this
@@ -206,8 +206,8 @@ int pgq_q8_decode_layer(const pgq_q8_layer* layer, const float* x, const float* 
 
 /* ---------------------------------------------------------------- a4: prefill q8
  * Batched prefill projection of a pass of 1 <= B <= 64 positions through q8
- * matrices, every weight read from memory once per pass (nemotron_prefill.rs
- * module header: "every weight read once per pass"; gemma_batch.rs `q8_2f_mm_r2`):
+ * matrices, every weight read from memory once per pass (the read-once rule of the
+ * nemotron_prefill.rs module header; gemma_batch.rs `q8_2f_mm_r2`):
  *   Y[b][r] = epilogue( sum_c (scale[r][c/32]*codes[r][c] + offset[r][c/32]) * X[b][c] )
  * computed on the tensor cores with binary16 operands and f32 accumulation: w is
  * rounded once to binary16, X[b] is scaled by a power of two per position and

@@ -296,15 +296,7 @@ int pgq_q8_decode_layer(const pgq_q8_layer* L, const float* x, const float* x_o,
 }
 
 // ------------------------------------------------------------------ prefill
-static int prefill_a_tmem = -1;  // A operand in tensor memory (1) or shared memory (0)
 
-static bool use_a_tmem() {
-  if (prefill_a_tmem < 0) {
-    const char* e = getenv("PGQ_PREFILL_A_SMEM");
-    prefill_a_tmem = (e && e[0] == '1') ? 0 : 1;
-  }
-  return prefill_a_tmem == 1;
-}
 
 size_t pgq_prefill_q8_workspace_bytes(const int* rows, int njobs, int cols, int B) {
   if (!rows || njobs < 1 || njobs > TC_MAXJOBS || cols < 128 || B < 1 || B > PGQ_PASS_BMAX) return 0;
@@ -343,7 +335,7 @@ int pgq_prefill_q8(const pgq_q8_job* jobs, int njobs, const float* X, int cols, 
   GET_DEVICE(dev);
   const size_t need = prefill_workspace_bytes(rows, njobs, cols, B, dev);
   REQUIRE(workspace_bytes >= need, PGQ_EWORKSPACE, "prefill_q8: workspace needs %zu bytes", need);
-  return launch_prefill(pj, njobs, X, cols, B, workspace, workspace_bytes, use_a_tmem(), 0, dev, as_stream(stream));
+  return launch_prefill(pj, njobs, X, cols, B, workspace, workspace_bytes, 0, dev, as_stream(stream));
 }
 
 // ------------------------------------------------------------------ prefill pass
@@ -356,22 +348,16 @@ struct PassLayout {
 PassLayout pass_layout(int H, int KV, int I, int B, const DeviceInfo& dev) {
   PassLayout L{};
   auto up = [](size_t v) { return (v + 255) / 256 * 256; };
-  size_t o = 0;
+  // the GEMM part first: its status word is at offset 0 (pgq_prefill_status)
+  L.gemm = 0;
+  size_t o = up(prefill_pass_gemm_bytes(H, KV, I, B, dev));
   const size_t sz[7] = {(size_t)B * H, (size_t)B * H, (size_t)B * KV, (size_t)B * KV,
                         (size_t)B * H, (size_t)B * H, (size_t)B * I};
   for (int i = 0; i < 7; ++i) {
     L.off[i] = o;
     o = up(o + sz[i] * 4);
   }
-  L.gemm = o;
-  const int qkv[3] = {H, KV, KV};
-  const int one_h[1] = {H};
-  const int one_i[1] = {I};
-  size_t g = prefill_workspace_bytes(qkv, 3, H, B, dev);
-  g = std::max(g, prefill_workspace_bytes(one_h, 1, H, B, dev));
-  g = std::max(g, prefill_workspace_bytes(one_i, 1, H, B, dev));
-  g = std::max(g, prefill_workspace_bytes(one_h, 1, I, B, dev));
-  L.total = o + up(g);
+  L.total = o;
   return L;
 }
 }  // namespace
@@ -397,6 +383,9 @@ int pgq_q8_prefill_pass(const pgq_q8_layer* layers, int L, float* h, int B, cons
                         const float* gamma2, float eps, void* workspace, size_t workspace_bytes, void* stream) {
   REQUIRE(layers && h && gamma1 && gamma2 && workspace, PGQ_EINVAL, "prefill_pass: null pointer");
   REQUIRE(L >= 1, PGQ_EINVAL, "prefill_pass: L=%d", L);
+  REQUIRE(B >= 1 && B <= PGQ_PASS_BMAX, PGQ_EINVAL, "prefill_pass: B=%d outside 1..%d", B, PGQ_PASS_BMAX);
+  REQUIRE(aligned16(h) && aligned16(gamma1) && aligned16(gamma2), PGQ_EALIGN,
+          "prefill_pass: h, gamma1 and gamma2 must be 16-byte aligned");
   const int H = layers[0].hidden, KV = layers[0].kv, I = layers[0].inter;
   for (int l = 0; l < L; ++l)
     REQUIRE(layers[l].hidden == H && layers[l].kv == KV && layers[l].inter == I, PGQ_EINVAL,
@@ -415,27 +404,9 @@ int pgq_q8_prefill_pass(const pgq_q8_layer* layers, int L, float* h, int B, cons
   float* h1 = reinterpret_cast<float*>(w + PL.off[4]);
   float* n2 = reinterpret_cast<float*>(w + PL.off[5]);
   float* u = reinterpret_cast<float*>(w + PL.off[6]);
-  void* gws = w + PL.gemm;
-  const size_t gws_bytes = workspace_bytes - PL.gemm;
-  cudaStream_t st = as_stream(stream);
-  const bool at = use_a_tmem();
-  int rc;
-  for (int l = 0; l < L; ++l) {
-    const pgq_q8_layer& Y = layers[l];
-    if ((rc = launch_add_rmsnorm(h, nullptr, gamma1 + (size_t)l * H, eps, B, H, n1, nullptr, st))) return rc;
-    PrefillJob qkv[3] = {{Y.q.codes, Y.q.params, H, q, nullptr, PGQ_EPI_NONE},
-                         {Y.k.codes, Y.k.params, KV, k, nullptr, PGQ_EPI_NONE},
-                         {Y.v.codes, Y.v.params, KV, v, nullptr, PGQ_EPI_NONE}};
-    if ((rc = launch_prefill(qkv, 3, n1, H, B, gws, gws_bytes, at, 0, dev, st))) return rc;
-    PrefillJob o = {Y.o.codes, Y.o.params, H, h1, h, PGQ_EPI_ADD};
-    if ((rc = launch_prefill(&o, 1, q, H, B, gws, gws_bytes, at, 0, dev, st))) return rc;
-    if ((rc = launch_add_rmsnorm(h1, nullptr, gamma2 + (size_t)l * H, eps, B, H, n2, nullptr, st))) return rc;
-    PrefillJob upj = {Y.up.codes, Y.up.params, I, u, nullptr, PGQ_EPI_RELU2};
-    if ((rc = launch_prefill(&upj, 1, n2, H, B, gws, gws_bytes, at, 0, dev, st))) return rc;
-    PrefillJob dn = {Y.down.codes, Y.down.params, H, h, h1, PGQ_EPI_ADD};
-    if ((rc = launch_prefill(&dn, 1, u, I, B, gws, gws_bytes, at, 0, dev, st))) return rc;
-  }
-  return PGQ_OK;
+  const PassTaps taps{n1, q, k, v, h1, n2, u};
+  return launch_prefill_pass(layers, L, h, B, gamma1, gamma2, eps, taps, w + PL.gemm, PL.off[0] - PL.gemm, dev,
+                             as_stream(stream));
 }
 
 // ------------------------------------------------------------------ MoE

@@ -70,10 +70,20 @@ struct PrefillJob {
 };
 size_t prefill_workspace_bytes(const int* rows, int njobs, int cols, int B, const DeviceInfo& dev);
 int prefill_status_offset();
-// One launch of the binary16 conversion of X and one of the tensor-core GEMM.
-// `a_tmem` selects the A operand in tensor memory (else in shared memory).
+// One projection step: the input's binary16 conversion, then one persistent launch.
 int launch_prefill(const PrefillJob* jobs, int njobs, const float* X, int cols, int B, void* ws, size_t ws_bytes,
-                   bool a_tmem, unsigned long long wait_limit_ns, const DeviceInfo& dev, cudaStream_t st);
+                   unsigned long long wait_limit_ns, const DeviceInfo& dev, cudaStream_t st);
+// Where the pass leaves the last layer's intermediates (f32 [B][...]).
+struct PassTaps {
+  float *n1, *q, *k, *v, *h1, *n2, *u;
+};
+// Bytes of the GEMM part of the pass workspace (its status word at offset 0).
+size_t prefill_pass_gemm_bytes(int H, int KV, int I, int B, const DeviceInfo& dev);
+// The pass over L layers: per 8 layers one input kernel and one persistent launch of
+// 4 phases per layer (q,k,v; o; up; down), inputs made inside the launch.
+int launch_prefill_pass(const pgq_q8_layer* layers, int L, float* h, int B, const float* gamma1,
+                        const float* gamma2, float eps, const PassTaps& taps, void* ws, size_t ws_bytes,
+                        const DeviceInfo& dev, cudaStream_t st);
 
 // ------------------------------------------------------------------ MoE
 struct MoeBankArgs {

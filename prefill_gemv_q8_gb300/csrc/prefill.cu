@@ -1,36 +1,37 @@
-// Batched prefill projection Y[b][r] = Σ_c W[r][c]·X[b][c] for up to 64 positions,
+// Batched prefill projections Y[b][r] = Σ_c W[r][c]·X[b][c] for up to 64 positions,
 // q8 block-format weights read from HBM once per pass, on the 5th-generation tensor
 // cores (tcgen05.mma, binary16 operands, f32 accumulation in tensor memory).
 //
 // Prior art: nemotron_prefill.rs (a pass of at most PB_MAX = 64 positions, every
-// weight read once per pass) and gemma_batch.rs `q8_2f_mm_r2` (64×64 register tiles
-// on the shader cores, the scale factors folded in around the int8 products).
-// Here the contraction runs on the tensor cores:
+// weight read once per pass, RMSNorm and relu² between the projections) and
+// gemma_batch.rs `q8_2f_mm_r2` (64×64 register tiles on the shader cores, the scale
+// factors folded in around the int8 products).  Here:
 //
-// * X (f32) is first converted to binary16 with one power-of-two scale per position
-//   (exact; keeps any activation range inside binary16), and the scale is undone in
-//   the epilogue.
-// * A tile is 128 weight rows × all positions (N = B rounded up to 16).  The K
-//   dimension is walked in 128-column steps.  One warp issues TMA loads of the step's
-//   int8 codes (128×128 bytes, 128-byte swizzle), (scale, offset) pairs and the X
-//   slice (binary16, 128-byte swizzle, the MMA's B operand) into a ring of stages.
-// * Four dequantisation warps (one thread per weight row) turn codes into binary16
-//   w = scale·q + offset (exact byte→half conversion, one fused multiply-add,
-//   rounded once) and store the row into tensor memory, where it is the MMA's A
-//   operand: the dequantised weights never touch shared memory.
-// * One thread issues 8 tcgen05.mma (M=128, N, K=16) per step into one of two TMEM
-//   accumulators; tcgen05.commit releases the stage, the A buffer and, at the end of
-//   a tile, the accumulator.
-// * Four epilogue warps read the accumulator (one row per thread), undo the position
-//   scale, apply relu² / the residual add and store f32 rows, coalesced along rows.
-// * Work is split stream-K style: the (tile, k-step) items of the launch are cut into
-//   equal contiguous ranges, one per block (≤ one block per SM), so every SM streams
-//   the same number of weight bytes.  A tile cut between blocks leaves f32 partials
-//   in the workspace; the block that finishes a tile last (atomic ticket) sums the
-//   partials in block order (deterministic) and applies the epilogue.
+// * One persistent, cooperative launch runs a sequence of phases; a phase is one
+//   projection step (up to three matrices sharing one input, e.g. q, k, v).  Between
+//   two phases the input of the next one is made inside the launch: RMSNorm where the
+//   layer has one, then binary16 with one power-of-two scale per position (exact;
+//   keeps any activation range inside binary16), undone in the epilogue.
+// * A tile is 128 weight rows × all positions (N = B rounded up to 16); K is walked
+//   in 128-column steps.  Per phase the (tile, k-step) items are cut into equal
+//   contiguous ranges, one per block (stream-K), so every SM streams the same bytes.
+// * Roles (warps): 0 streams the weight steps (int8 codes with 128-byte swizzle,
+//   (scale, offset) pairs) into a ring with TMA; 14 streams the binary16 input slices
+//   into a second ring, once the phase's input exists; 2-9 turn codes into binary16
+//   w = scale·q + offset (exact byte→half conversion, one fused multiply-add) and
+//   store them into tensor memory, the MMA's A operand; 1 issues 8 tcgen05.mma
+//   (M=128, N, K=16) per step into one of two TMEM accumulators; 10-13 are the
+//   epilogue (scale, relu² / residual add, stores) and make the next phase's input.
+//   Weight streaming never waits for the phase boundary: the ring keeps filling.
+// * A tile cut between blocks: the other blocks publish f32 partials; the block
+//   holding the tile's first k-steps (it reaches them last) adds them in block order
+//   (deterministic) and writes the tile.  Every final tile also leaves per-position
+//   Σy² and max|γ·y| for the next phase's RMSNorm and scale, so the input of the next
+//   phase is made by all blocks at once, each a slice of columns.
 // * Every wait is bounded (%globaltimer); on expiry the block records PGQ_ETIMEOUT in
-//   the workspace status word, the other roles leave their loops, outstanding copies
-//   and MMAs are drained with bounded waits, and tensor memory is released.
+//   the workspace status word, every role leaves its loop (the others notice the
+//   status word), copies and MMAs in flight are drained with bounded waits and tensor
+//   memory is released.
 #include <algorithm>
 #include <cstring>
 #include <map>
@@ -45,54 +46,62 @@ namespace pgq {
 
 constexpr int TC_BM = 128;
 constexpr int TC_BK = 128;
-constexpr int TC_THREADS = 448;  // warp 0 TMA, warp 1 MMA+TMEM, warps 2-9 dequant, 10-13 epilogue
-constexpr int TC_DQ_WARPS = 8;   // two per TMEM lane quarter, each half of the step's columns
-constexpr int TC_EPI_WARP0 = 2 + TC_DQ_WARPS;
-constexpr int TC_NA_TMEM = 4;    // A buffers when A lives in tensor memory
-constexpr int TC_NA_SMEM = 2;    // A buffers when A lives in shared memory
-constexpr int TC_STAGES_TMEM = 5;  // stage ring depth with A in tensor memory
-constexpr int TC_STAGES_SMEM = 3;  // with A in shared memory (its buffers take the room)
-constexpr int TC_CODES_BYTES = TC_BM * TC_BK;       // 16 KB
-constexpr int TC_PARAMS_BYTES = TC_BM * 16;         // 4 (scale, offset) pairs per row
-constexpr int TC_ACC_COLS = 64;                     // TMEM columns per accumulator (N <= 64)
-constexpr int TC_ACC_TILE_BYTES = TC_ACC_COLS * TC_BM * 4;  // epilogue transpose tile
-constexpr int TC_A_COLS = TC_BK / 2;                // TMEM columns per A buffer (2 halves per column)
-constexpr uint32_t TC_TMEM_COLS = 512;              // 2 accumulators + 4 A buffers (384 used)
+constexpr int PS_THREADS = 480;    // 15 warps
+constexpr int PS_DQ_WARPS = 8;     // warps 2..9: two per TMEM lane quarter, each half of a step
+constexpr int PS_EPI_WARP0 = 10;   // warps 10..13
+constexpr int PS_XP_WARP = 14;     // input-slice producer
+constexpr int PS_NA = 4;           // A buffers in tensor memory
+constexpr int PS_WST_MAX = 10;     // weight ring stages (at most; set by the shared memory left)
+constexpr int PS_XST = 3;          // input ring stages
+constexpr int PS_CODES_BYTES = TC_BM * TC_BK;                 // 16 KB
+constexpr int PS_PARAMS_BYTES = TC_BM * 16;                   // 4 (scale, offset) pairs per row
+constexpr int PS_W_BYTES = PS_CODES_BYTES + PS_PARAMS_BYTES;  // 18 KB, a multiple of 1 KB
+constexpr int PS_ACC_COLS = 64;                               // TMEM columns per accumulator (N <= 64)
+constexpr int PS_A_COLS = TC_BK / 2;                          // TMEM columns per A buffer
+constexpr uint32_t PS_TMEM_COLS = 512;                        // 2 accumulators + 4 A buffers (384 used)
+constexpr int PS_MAXL = 8;                                    // layers per pass launch
+constexpr int PS_MAXPH = 4 * PS_MAXL;                         // phases per launch
+constexpr int PS_MAXJ = 6 * PS_MAXL;                          // matrices per launch
+constexpr int PS_NX = 4;                                      // input buffers (n1, q, n2, u)
+constexpr int PS_STATIC_SMEM = 2048;                          // bound on the kernel's static shared memory
+constexpr int PS_OUT_K = PS_ACC_COLS * (TC_BM / 4) / 128;     // float4 slots per epilogue thread (16)
+constexpr int PS_OUT_P = 4;                                   // handled in passes (registers)
+constexpr int PS_OUT_H = PS_OUT_K / PS_OUT_P;
 
-struct TcParams {
-  CUtensorMap xmap;                       // X binary16 [Bp][cols], box {64, Bp}, 128B swizzle
-  CUtensorMap cmap[TC_MAXJOBS];           // codes int8 [rows][cols], box {128, 128}, 128B swizzle
-  CUtensorMap pmap[TC_MAXJOBS];           // params u32 [rows][cols/32], box {4, 128}
-  float* y[TC_MAXJOBS];
-  const float* residual[TC_MAXJOBS];
-  int rows[TC_MAXJOBS];
-  int tile_begin[TC_MAXJOBS + 1];
-  int epi[TC_MAXJOBS];
-  int njobs, ks, B, Bp, ntiles, maxseg;
-  long long total_items;
-  const float* xinv;                      // [Bp]
-  float* partials;                        // [grid][maxseg][Bp][128]
-  unsigned* tile_cnt;                     // [ntiles]
+struct PsJob {
+  CUtensorMap cmap;          // codes int8 [rows][cols], box {128, 128}, 128-byte swizzle
+  CUtensorMap pmap;          // params u32 [rows][cols/32], box {4, 128}
+  float* y;                  // [B][rows]
+  const float* residual;     // [B][rows] for PGQ_EPI_ADD
+  int rows, epi, tile0, ntiles;   // tile0: first tile of the job within its phase
+};
+struct PsPhase {
+  int job0, njobs;           // jobs [job0, job0 + njobs)
+  int ks, K, ntiles, T;      // k-steps, input width, tiles, items (tiles × k-steps)
+  int xk;                    // input buffer
+  int stats_job;             // job whose final tiles report Σy², max|γ·y| (-1: none)
+  int src_job;               // phases after the first: the previous phase's job that is the input
+  const float* next_gamma;   // γ the next phase normalises with (max|γ·y|), or null
+  const float* gamma;        // this phase's input: RMSNorm weight, or null (scale only)
+  float* tap;                // f32 copy of the normalised input, or null
+};
+struct PsParams {
+  PsJob job[PS_MAXJ];
+  CUtensorMap xmap[PS_NX];   // binary16 [Bp][K], box {64, Bp}, 128-byte swizzle
+  PsPhase ph[PS_MAXPH];
+  __half* xh[PS_NX];
+  const float* xinv0;        // [Bp] inverse input scales of the first phase
+  float* partials;           // [2][G][maxseg][Bp][128]
+  unsigned* tile_cnt;        // [2][maxtiles]
+  unsigned* done;            // [nph] final tiles per phase
+  unsigned* prep_done;       // [nph] blocks that wrote their slice of the phase's input
+  float2* stats;             // [2][maxtiles][64]
   int* status;
   unsigned long long wait_limit_ns;
+  float eps;
+  int nph, B, Bp, G, maxseg, maxtiles, wst;
 };
-
-// Optional event trace (compiled in only with -DPGQ_TRACE): block 0 records
-// (event, step, %globaltimer) triples into a device buffer for latency analysis.
-#ifdef PGQ_TRACE
-// block 0: per role and item, clock64 stamps kept in shared memory, written out at exit
-constexpr int TR_ITEMS = 64, TR_EV = 4;
-__device__ long long g_tr[4 * TR_ITEMS * TR_EV];      // [role][item][event]
-__device__ unsigned long long g_cta[4 * 1024];         // per block: start, after setup, end, smid
-__shared__ long long s_tr[4 * TR_ITEMS * TR_EV];
-__device__ __forceinline__ void trace(int role, int ev, int item, int beg) {
-  const int i = item - beg;
-  if (blockIdx.x == 0 && i >= 0 && i < TR_ITEMS) s_tr[(role * TR_ITEMS + i) * TR_EV + ev] = clock64();
-}
-#define TRACE(role, ev, k) trace(role, ev, k, beg)
-#else
-#define TRACE(role, ev, k) ((void)0)
-#endif
+static_assert(sizeof(PsParams) <= 32000, "kernel parameters");
 
 // ------------------------------------------------------------------ schedule
 __device__ __forceinline__ int item_begin(int c, int G, int T) { return (int)((long long)c * T / G); }
@@ -105,30 +114,54 @@ __device__ __forceinline__ int cta_of_item(int i, int G, int T) {
   return c;
 }
 
-__device__ __forceinline__ int job_of_tile(const TcParams& P, int tile) {
-  int j = 0;
+__device__ __forceinline__ int job_of_tile(const PsParams& P, const PsPhase& F, int tile) {
+  int j = F.job0;
 #pragma unroll 1
-  while (j + 1 < P.njobs && tile >= P.tile_begin[j + 1]) ++j;
+  while (j + 1 < F.job0 + F.njobs && tile >= P.job[j + 1].tile0) ++j;
   return j;
 }
 
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Publishes this thread's (and, through a preceding block barrier, its group's)
+// earlier writes at gpu scope, then counts them.
+__device__ __forceinline__ void release_add(unsigned* p) {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+  atomicAdd(p, 1u);
+}
+
 struct Waiter {
-  const TcParams& P;
+  const PsParams& P;
   volatile int* abort_flag;
+  __device__ bool failed() const {
+    if (*abort_flag) return true;
+    if (*(volatile int*)P.status != 0) {   // another block gave up
+      *abort_flag = 1;
+      return true;
+    }
+    return false;
+  }
+  __device__ void give_up() const {
+    *abort_flag = 1;
+    atomicCAS(P.status, 0, PGQ_ETIMEOUT);
+  }
+  // bounded wait on an mbarrier phase
   __device__ bool wait(uint32_t bar, uint32_t parity) const {
     if (tc::mbar_try(bar, parity)) return true;
     const uint64_t t0 = tc::globaltimer();
     while (true) {
       if (tc::mbar_try_sleep(bar, parity, 20000u)) return true;
-      if (*abort_flag) return false;
+      if (failed()) return false;
       if (tc::globaltimer() - t0 > P.wait_limit_ns) {
-        *abort_flag = 1;
-        atomicCAS(P.status, 0, PGQ_ETIMEOUT);
+        give_up();
         return false;
       }
     }
   }
-  // bounded wait that ignores the abort flag (drain of in-flight copies / MMAs)
+  // bounded wait that ignores the abort flag (drain of copies / MMAs in flight)
   __device__ bool drain(uint32_t bar, uint32_t parity) const {
     const uint64_t t0 = tc::globaltimer();
     while (!tc::mbar_try_sleep(bar, parity, 20000u)) {
@@ -138,6 +171,20 @@ struct Waiter {
       }
     }
     return true;
+  }
+  // bounded wait until a global counter reaches `need` (acquire)
+  __device__ bool count(const unsigned* c, unsigned need) const {
+    if (ld_acquire(c) >= need) return true;
+    const uint64_t t0 = tc::globaltimer();
+    while (true) {
+      __nanosleep(128);
+      if (ld_acquire(c) >= need) return true;
+      if (failed()) return false;
+      if (tc::globaltimer() - t0 > P.wait_limit_ns) {
+        give_up();
+        return false;
+      }
+    }
   }
 };
 
@@ -154,34 +201,75 @@ __device__ __forceinline__ bool epi_all(bool ok) {
   return r != 0;
 }
 
+// Butterfly max over the lanes, scattered like reduce_scatter (index lane / (32/N)).
+template <int N>
+__device__ __forceinline__ float reduce_scatter_max(float (&v)[N], int lane) {
+#pragma unroll
+  for (int n = N, o = 16; n > 1; n >>= 1, o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int j = 0; j < n / 2; ++j) {
+      const float mine = up ? v[j + n / 2] : v[j];
+      const float other = up ? v[j] : v[j + n / 2];
+      v[j] = fmaxf(mine, __shfl_xor_sync(0xffffffffu, other, o));
+    }
+  }
+  float t = v[0];
+#pragma unroll
+  for (int o = 16 / N; o > 0; o >>= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
+  return t;
+}
 
-// Writes a tile's outputs from the shared transposed tile acc4 ([b][128 rows] as
-// float4): y[b][row0 + c] = epilogue(acc[b][c]) for c < rows - row0.  Each warp
-// covers whole 512-byte rows; thread et takes float4 et, et+128, ... (at most 16).
-// All reads (shared tile, residual) are issued before the first store, so a
-// residual that is y itself costs one memory round trip, not one per element.
-constexpr int TC_OUT_K = TC_ACC_COLS * (TC_BM / 4) / 128;  // float4 per epilogue thread (16)
-constexpr int TC_OUT_P = 4;                                  // handled in passes (registers)
-constexpr int TC_OUT_H = TC_OUT_K / TC_OUT_P;
+// Statistics of four consecutive values of one position: Σ y² (fixed fma order) and
+// max |γ·y|.  Used by the epilogue (final tiles) and by the first input's kernel, so
+// both make bit-identical inputs.
+__device__ __forceinline__ float sq4(float4 a) { return fmaf(a.w, a.w, fmaf(a.z, a.z, fmaf(a.y, a.y, a.x * a.x))); }
+__device__ __forceinline__ float gmax4(float4 a, float4 g) {
+  return fmaxf(fmaxf(fabsf(g.x * a.x), fabsf(g.y * a.y)), fmaxf(fabsf(g.z * a.z), fabsf(g.w * a.w)));
+}
+// The input scale of one position from its statistics: inv = 1/√(Σy²/K + eps) when
+// normalised (else 1), then the power of two that puts max|v| just below 2^14.
+__device__ __forceinline__ void input_scale(float ss, float mx, int K, float eps, bool norm, float& inv, float& sc,
+                                            float& xi) {
+  inv = norm ? rsqrtf(ss / (float)K + eps) : 1.f;
+  const float m = norm ? mx * inv : mx;
+  int e = 0;
+  if (m > 0.f && m <= 3.0e38f) frexpf(m, &e);   // m = f·2^e, f in [0.5, 1)
+  const int k = max(-120, min(120, 14 - e));
+  sc = ldexpf(1.f, k);
+  xi = ldexpf(1.f, -k);
+}
 
-__device__ __forceinline__ void out_rows(const float4* acc4, int nvec, int et, int epi, float* y, const float* res,
-                                         int rows, int row0, bool vec_ok) {
+// Exact signed byte pair → binary16 pair: (0x64 << 8 | b + 128) is the half
+// 1024 + b + 128; subtracting 1152 leaves b.
+__device__ __forceinline__ __half2 s8pair_to_h2(uint32_t u_biased, uint32_t sel) {
+  const uint32_t h = __byte_perm(u_biased, 0x64646464u, sel);
+  return __hsub2(*reinterpret_cast<const __half2*>(&h), __half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
+}
+
+// Writes a tile from the shared transposed tile acc4 ([b][128 rows] as float4):
+// y[b][row0 + c] = epilogue(acc[b][c]) for c < rows - row0, and (writeback) leaves
+// the final values in acc4.  Thread et takes float4 et, et+128, ... (at most 16); all
+// reads (shared tile, residual) of a pass are issued before its first store.
+__device__ __forceinline__ void out_rows(float4* acc4, int nvec, int et, int epi, float* y, const float* res, int rows,
+                                         int row0, bool vec_ok, bool writeback) {
   if (vec_ok) {
 #pragma unroll
-    for (int h = 0; h < TC_OUT_P; ++h) {
-      float4 a[TC_OUT_H], q[TC_OUT_H];
+    for (int h = 0; h < PS_OUT_P; ++h) {
+      float4 a[PS_OUT_H], q[PS_OUT_H];
 #pragma unroll
-      for (int k = 0; k < TC_OUT_H; ++k) {
-        const int i = et + 128 * (h * TC_OUT_H + k);
+      for (int k = 0; k < PS_OUT_H; ++k) {
+        const int i = et + 128 * (h * PS_OUT_H + k);
         const int rr = row0 + (i & 31) * 4;
         if (i < nvec) {
           a[k] = acc4[i];
-          if (epi == PGQ_EPI_ADD && rr < rows) q[k] = *reinterpret_cast<const float4*>(res + (size_t)(i >> 5) * rows + rr);
+          if (epi == PGQ_EPI_ADD && rr < rows)
+            q[k] = __ldcg(reinterpret_cast<const float4*>(res + (size_t)(i >> 5) * rows + rr));
         }
       }
 #pragma unroll
-      for (int k = 0; k < TC_OUT_H; ++k) {
-        const int i = et + 128 * (h * TC_OUT_H + k);
+      for (int k = 0; k < PS_OUT_H; ++k) {
+        const int i = et + 128 * (h * PS_OUT_H + k);
         const int rr = row0 + (i & 31) * 4;
         if (i < nvec && rr < rows) {
           float4 o = a[k];
@@ -192,12 +280,13 @@ __device__ __forceinline__ void out_rows(const float4* acc4, int nvec, int et, i
             o = make_float4(q[k].x + o.x, q[k].y + o.y, q[k].z + o.z, q[k].w + o.w);
           }
           *reinterpret_cast<float4*>(y + (size_t)(i >> 5) * rows + rr) = o;
+          if (writeback) acc4[i] = o;
         }
       }
     }
   } else {
     // rows not a multiple of 4 or unaligned outputs: element by element
-    for (int k = 0; k < TC_OUT_K; ++k) {
+    for (int k = 0; k < PS_OUT_K; ++k) {
       const int i = et + 128 * k;
       if (i >= nvec) break;
       const int rr = row0 + (i & 31) * 4;
@@ -210,7 +299,7 @@ __device__ __forceinline__ void out_rows(const float4* acc4, int nvec, int et, i
           o = fmaxf(o, 0.f);
           o = o * o;
         } else if (epi == PGQ_EPI_ADD) {
-          o = res[idx + e] + o;
+          o = __ldcg(res + idx + e) + o;
         }
         y[idx + e] = o;
       }
@@ -218,379 +307,476 @@ __device__ __forceinline__ void out_rows(const float4* acc4, int nvec, int et, i
   }
 }
 
-// Exact signed byte pair → binary16 pair: (0x64 << 8 | b + 128) is the half
-// 1024 + b + 128; subtracting 1152 leaves b.
-__device__ __forceinline__ __half2 s8pair_to_h2(uint32_t u_biased, uint32_t sel) {
-  const uint32_t h = __byte_perm(u_biased, 0x64646464u, sel);
-  return __hsub2(*reinterpret_cast<const __half2*>(&h), __half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
+// Per-position statistics of a final tile (values in acc4, rows a multiple of 4):
+// out[b] = (Σ over the tile's rows of y², max |γ·y|).  Lanes hold rows lane·4..+3 of
+// positions warp + 4k; the lane sums are combined by a butterfly (xor 16, 8, 4, 2, 1).
+__device__ __forceinline__ void tile_stats(const float4* acc4, int nvec, int et, int rows, int row0,
+                                           const float* gam, float2* out) {
+  const int lane = et & 31, we = et >> 5;
+  const int rr = row0 + lane * 4;
+  float4 g = make_float4(1.f, 1.f, 1.f, 1.f);
+  if (gam && rr < rows) g = *reinterpret_cast<const float4*>(gam + rr);
+  float ss[PS_OUT_K], mx[PS_OUT_K];
+#pragma unroll
+  for (int k = 0; k < PS_OUT_K; ++k) {
+    const int i = et + 128 * k;
+    ss[k] = 0.f;
+    mx[k] = 0.f;
+    if (i < nvec && rr < rows) {
+      const float4 a = acc4[i];
+      ss[k] = sq4(a);
+      mx[k] = gmax4(a, g);
+    }
+  }
+  const float tss = reduce_scatter<PS_OUT_K>(ss, lane);
+  const float tmx = reduce_scatter_max<PS_OUT_K>(mx, lane);
+  if ((lane & 1) == 0) out[we + 4 * (lane >> 1)] = make_float2(tss, tmx);
 }
 
-template <bool A_TMEM>
-__global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_constant__ TcParams P) {
-  constexpr int TC_NA = A_TMEM ? TC_NA_TMEM : TC_NA_SMEM;
-  constexpr int TC_STAGES = A_TMEM ? TC_STAGES_TMEM : TC_STAGES_SMEM;
+__global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __grid_constant__ PsParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int Bp = P.Bp;
-  const int x_bytes = 2 * Bp * 128;  // two 64-column halves of the X slice
-  const int stage_bytes = TC_CODES_BYTES + x_bytes + TC_PARAMS_BYTES;
-  uint8_t* stages = smem;
-  uint8_t* abuf = stages + TC_STAGES * stage_bytes;            // A in shared memory (A_TMEM == false)
-  float* s_acc = reinterpret_cast<float*>(abuf + (A_TMEM ? 0 : TC_NA * TC_BM * TC_BK * 2));  // [64][128]
-  uint8_t* tail = reinterpret_cast<uint8_t*>(s_acc) + TC_ACC_TILE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(tail);
-  // barrier slots
-  const int B_FULL = 0, B_EMPTY = TC_STAGES, B_AFULL = 2 * TC_STAGES, B_AEMPTY = B_AFULL + TC_NA,
-            B_ACCF = B_AEMPTY + TC_NA, B_ACCE = B_ACCF + 2, B_DRAIN = B_ACCE + 2, NBARS = B_DRAIN + 1;
+  const int Bp = P.Bp, WST = P.wst, G = P.G;
+  const int xst_bytes = 2 * Bp * 128;   // two 64-column halves of an input slice
+  uint8_t* wring = smem;
+  uint8_t* xring = wring + WST * PS_W_BYTES;
+  float* s_acc = reinterpret_cast<float*>(xring + PS_XST * xst_bytes);   // [Bp][128]
+  float* fixb = s_acc + Bp * TC_BM;                                      // [Bp][128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(fixb + Bp * TC_BM);
+  enum {
+    FULL_W = 0,
+    EMPTY_W = PS_WST_MAX,
+    FULL_X = 2 * PS_WST_MAX,
+    EMPTY_X = FULL_X + PS_XST,
+    AFULL = EMPTY_X + PS_XST,
+    AEMPTY = AFULL + PS_NA,
+    ACCF = AEMPTY + PS_NA,
+    ACCE = ACCF + 2,
+    DRAIN = ACCE + 2,
+    NBARS = DRAIN + 1
+  };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
-  __shared__ float s_xinv[TC_ACC_COLS];
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  __shared__ float s_xinv[64], s_inv[64], s_sc[64];
+  __shared__ float2 s_st[2][64];
 
   auto bar = [&](int i) { return tc::smem_addr(bars + i); };
-  auto stage_codes = [&](int s) { return stages + s * stage_bytes; };
-  auto stage_x = [&](int s) { return stages + s * stage_bytes + TC_CODES_BYTES; };
-  auto stage_params = [&](int s) { return stages + s * stage_bytes + TC_CODES_BYTES + x_bytes; };
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-#ifdef PGQ_TRACE
-  for (int i = threadIdx.x; i < 4 * TR_ITEMS * TR_EV; i += blockDim.x) s_tr[i] = 0;
+  const int cta = blockIdx.x;
+
   if (threadIdx.x == 0) {
-    g_cta[4 * blockIdx.x] = tc::globaltimer();
-    unsigned smid;
-    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-    g_cta[4 * blockIdx.x + 3] = smid;
-  }
-#endif
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < TC_STAGES; ++s) {
-      tc::mbar_init(bar(B_FULL + s), 1);
-      tc::mbar_init(bar(B_EMPTY + s), TC_DQ_WARPS + 1);  // dequant warps + the MMA commit
+    for (int s = 0; s < WST; ++s) {
+      tc::mbar_init(bar(FULL_W + s), 1);
+      tc::mbar_init(bar(EMPTY_W + s), PS_DQ_WARPS);
     }
-    for (int a = 0; a < TC_NA; ++a) {
-      tc::mbar_init(bar(B_AFULL + a), TC_DQ_WARPS);
-      tc::mbar_init(bar(B_AEMPTY + a), 1);
+    for (int s = 0; s < PS_XST; ++s) {
+      tc::mbar_init(bar(FULL_X + s), 1);
+      tc::mbar_init(bar(EMPTY_X + s), 1);
+    }
+    for (int a = 0; a < PS_NA; ++a) {
+      tc::mbar_init(bar(AFULL + a), PS_DQ_WARPS);
+      tc::mbar_init(bar(AEMPTY + a), 1);
     }
     for (int t = 0; t < 2; ++t) {
-      tc::mbar_init(bar(B_ACCF + t), 1);
-      tc::mbar_init(bar(B_ACCE + t), 4);
+      tc::mbar_init(bar(ACCF + t), 1);
+      tc::mbar_init(bar(ACCE + t), 4);
     }
-    tc::mbar_init(bar(B_DRAIN), 1);
+    tc::mbar_init(bar(DRAIN), 1);
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
-  if (warp == 1) tc::tmem_alloc(tc::smem_addr(tmem_slot), TC_TMEM_COLS);
-  if (threadIdx.x < TC_ACC_COLS) s_xinv[threadIdx.x] = threadIdx.x < Bp ? P.xinv[threadIdx.x] : 0.f;
-  if (warp == 0 && lane == 0) {
-    tc::prefetch_tensormap(&P.xmap);
-    for (int j = 0; j < P.njobs; ++j) {
-      tc::prefetch_tensormap(&P.cmap[j]);
-      tc::prefetch_tensormap(&P.pmap[j]);
-    }
-  }
+  if (warp == 1) tc::tmem_alloc(tc::smem_addr(tmem_slot), PS_TMEM_COLS);
+  if (threadIdx.x < 64) s_xinv[threadIdx.x] = (int)threadIdx.x < Bp ? P.xinv0[threadIdx.x] : 0.f;
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-#ifdef PGQ_TRACE
-  if (threadIdx.x == 0) g_cta[4 * blockIdx.x + 1] = tc::globaltimer();
-#endif
-
-  const int G = gridDim.x;
-  const int T = (int)P.total_items;
-  const int beg = item_begin(blockIdx.x, G, T), end = item_begin(blockIdx.x + 1, G, T);
-  const int ks = P.ks;
   Waiter W{P, abort_flag};
+  auto range = [&](int p, int& beg, int& end) {
+    beg = item_begin(cta, G, P.ph[p].T);
+    end = item_begin(cta + 1, G, P.ph[p].T);
+  };
+  constexpr unsigned FULL = 0xffffffffu;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer (whole warp, one lane issues)
+    // ------------------------------------------------------------ weight producer
     const uint64_t evict_first = tc::policy_evict_first();
-    const uint32_t tx = (uint32_t)stage_bytes;
-    int s = 0;
+    int s = 0, issued = 0;
     uint32_t ph = 0;
-    int issued = 0;
-    int tile = beg / ks, k = beg - (beg / ks) * ks;
-    int j = job_of_tile(P, tile);
-    for (int it = beg; it < end; ++it) {
-      if (!__all_sync(0xffffffffu, W.wait(bar(B_EMPTY + s), ph ^ 1))) break;
-      TRACE(0, 0, it);
-      if (tc::elect_one()) {
-        const int row0 = (tile - P.tile_begin[j]) * TC_BM;
-        tc::mbar_expect_tx(bar(B_FULL + s), tx);
-        tc::tma_load_2d_hint(tc::smem_addr(stage_codes(s)), &P.cmap[j], k * TC_BK, row0, bar(B_FULL + s),
-                             evict_first);
-        tc::tma_load_2d_hint(tc::smem_addr(stage_params(s)), &P.pmap[j], k * (TC_BK / 32), row0, bar(B_FULL + s),
-                             evict_first);
-        tc::tma_load_2d(tc::smem_addr(stage_x(s)), &P.xmap, k * TC_BK, 0, bar(B_FULL + s));
-        tc::tma_load_2d(tc::smem_addr(stage_x(s) + Bp * 128), &P.xmap, k * TC_BK + 64, 0, bar(B_FULL + s));
-      }
-      __syncwarp();
-      ++issued;
-      if (++s == TC_STAGES) { s = 0; ph ^= 1; }
-      if (++k == ks) {
-        k = 0;
-        ++tile;
-        while (j + 1 < P.njobs && tile >= P.tile_begin[j + 1]) ++j;
+    bool stop = false;
+    for (int p = 0; p < P.nph && !stop; ++p) {
+      const PsPhase& F = P.ph[p];
+      int beg, end;
+      range(p, beg, end);
+      int tile = beg / F.ks, k = beg - (beg / F.ks) * F.ks;
+      int j = job_of_tile(P, F, tile);
+      for (int it = beg; it < end; ++it) {
+        if (!__all_sync(FULL, W.wait(bar(EMPTY_W + s), ph ^ 1))) {
+          stop = true;
+          break;
+        }
+        if (tc::elect_one()) {
+          const int row0 = (tile - P.job[j].tile0) * TC_BM;
+          uint8_t* st = wring + s * PS_W_BYTES;
+          tc::mbar_expect_tx(bar(FULL_W + s), PS_W_BYTES);
+          tc::tma_load_2d_hint(tc::smem_addr(st), &P.job[j].cmap, k * TC_BK, row0, bar(FULL_W + s), evict_first);
+          tc::tma_load_2d_hint(tc::smem_addr(st + PS_CODES_BYTES), &P.job[j].pmap, k * (TC_BK / 32), row0,
+                               bar(FULL_W + s), evict_first);
+        }
+        __syncwarp();
+        ++issued;
+        if (++s == WST) { s = 0; ph ^= 1; }
+        if (++k == F.ks) {
+          k = 0;
+          ++tile;
+          while (j + 1 < F.job0 + F.njobs && tile >= P.job[j + 1].tile0) ++j;
+        }
       }
     }
     if (*abort_flag && lane == 0) {
       // let the copies already issued land before the block can exit
-      const int n = issued < TC_STAGES ? issued : TC_STAGES;
+      const int n = issued < WST ? issued : WST;
       int ss = s;
       uint32_t pp = ph;
       for (int i = 0; i < n; ++i) {
-        if (--ss < 0) { ss = TC_STAGES - 1; pp ^= 1; }
-        W.drain(bar(B_FULL + ss), pp);
+        if (--ss < 0) { ss = WST - 1; pp ^= 1; }
+        W.drain(bar(FULL_W + ss), pp);
+      }
+    }
+  } else if (warp == PS_XP_WARP) {
+    // ------------------------------------------------------------ input-slice producer
+    const uint32_t xbytes = (uint32_t)xst_bytes;
+    int s = 0, issued = 0;
+    uint32_t ph = 0;
+    bool stop = false;
+    for (int p = 0; p < P.nph && !stop; ++p) {
+      const PsPhase& F = P.ph[p];
+      if (p > 0) {
+        // the phase's input is complete once every block wrote its slice; the copies
+        // (async proxy) then read what the blocks wrote (generic proxy)
+        if (!__all_sync(FULL, W.count(P.prep_done + p, (unsigned)G))) break;
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
+      int beg, end;
+      range(p, beg, end);
+      int k = beg - (beg / F.ks) * F.ks;
+      const CUtensorMap* xm = &P.xmap[F.xk];
+      for (int it = beg; it < end; ++it) {
+        if (!__all_sync(FULL, W.wait(bar(EMPTY_X + s), ph ^ 1))) {
+          stop = true;
+          break;
+        }
+        if (tc::elect_one()) {
+          uint8_t* st = xring + s * xst_bytes;
+          tc::mbar_expect_tx(bar(FULL_X + s), xbytes);
+          tc::tma_load_2d(tc::smem_addr(st), xm, k * TC_BK, 0, bar(FULL_X + s));
+          tc::tma_load_2d(tc::smem_addr(st + Bp * 128), xm, k * TC_BK + 64, 0, bar(FULL_X + s));
+        }
+        __syncwarp();
+        ++issued;
+        if (++s == PS_XST) { s = 0; ph ^= 1; }
+        if (++k == F.ks) k = 0;
+      }
+    }
+    if (*abort_flag && lane == 0) {
+      const int n = issued < PS_XST ? issued : PS_XST;
+      int ss = s;
+      uint32_t pp = ph;
+      for (int i = 0; i < n; ++i) {
+        if (--ss < 0) { ss = PS_XST - 1; pp ^= 1; }
+        W.drain(bar(FULL_X + ss), pp);
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (whole warp, one lane issues)
+    // ------------------------------------------------------------ MMA issuer
     const uint32_t idesc = tc::idesc_f16_f32(TC_BM, Bp);
-    const uint64_t bstep = (uint64_t)((Bp * 128) >> 4);  // second 64-column half of the X slice
-    int s = 0, a = 0, t = 0;
-    uint32_t ph = 0, pha = 0, pht = 0;
-    bool any = false;
-    int k = beg - (beg / ks) * ks;
-    for (int it = beg; it < end; ++it) {
-      const bool first = (k == 0) || (it == beg);
-      const bool last = (k == ks - 1) || (it == end - 1);
-      if (first && !__all_sync(0xffffffffu, W.wait(bar(B_ACCE + t), pht ^ 1))) break;
-      if (!__all_sync(0xffffffffu, W.wait(bar(B_AFULL + a), pha))) break;
-      TRACE(1, 0, it);
-      if (!__all_sync(0xffffffffu, W.wait(bar(B_FULL + s), ph))) break;
-      TRACE(1, 1, it);
-      tc::fence_after_sync();
-      const uint32_t d = tmem + t * TC_ACC_COLS;
-      const uint64_t b0 = tc::sdesc_sw128(tc::smem_addr(stage_x(s)));
-      const uint32_t a_t = tmem + 2 * TC_ACC_COLS + a * TC_A_COLS;
-      const uint64_t a_s = A_TMEM ? 0 : tc::sdesc_sw128(tc::smem_addr(abuf + a * (TC_BM * TC_BK * 2)));
-      if (tc::elect_one()) {
+    const uint64_t bstep = (uint64_t)((Bp * 128) >> 4);   // second 64-column half of the slice
+    int sx = 0, a = 0, t = 0;
+    uint32_t phx = 0, pha = 0, pht = 0;
+    bool any = false, stop = false;
+    for (int p = 0; p < P.nph && !stop; ++p) {
+      const PsPhase& F = P.ph[p];
+      int beg, end;
+      range(p, beg, end);
+      int k = beg - (beg / F.ks) * F.ks;
+      for (int it = beg; it < end; ++it) {
+        const bool first = (k == 0) || (it == beg);
+        const bool last = (k == F.ks - 1) || (it == end - 1);
+        if (first && !__all_sync(FULL, W.wait(bar(ACCE + t), pht ^ 1))) { stop = true; break; }
+        if (!__all_sync(FULL, W.wait(bar(AFULL + a), pha))) { stop = true; break; }
+        if (!__all_sync(FULL, W.wait(bar(FULL_X + sx), phx))) { stop = true; break; }
+        tc::fence_after_sync();
+        const uint32_t d = tmem + t * PS_ACC_COLS;
+        const uint64_t b0 = tc::sdesc_sw128(tc::smem_addr(xring + sx * xst_bytes));
+        const uint32_t a_t = tmem + 2 * PS_ACC_COLS + a * PS_A_COLS;
+        if (tc::elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < TC_BK / 16; ++kk) {
-          const uint64_t bdesc = b0 + (uint64_t)((kk & 3) * 2) + (kk >> 2) * bstep;
-          const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-          if constexpr (A_TMEM) {
-            tc::mma_f16_ts(d, a_t + kk * 8, bdesc, idesc, acc);
-          } else {
-            tc::mma_f16_ss(d, a_s + (uint64_t)((kk & 3) * 2) + (kk >> 2) * (uint64_t)((TC_BM * 128) >> 4), bdesc,
-                           idesc, acc);
+          for (int kk = 0; kk < TC_BK / 16; ++kk) {
+            const uint64_t bdesc = b0 + (uint64_t)((kk & 3) * 2) + (kk >> 2) * bstep;
+            tc::mma_f16_ts(d, a_t + kk * 8, bdesc, idesc, (first && kk == 0) ? 0u : 1u);
           }
+          tc::mma_commit(bar(EMPTY_X + sx));
+          tc::mma_commit(bar(AEMPTY + a));
+          if (last) tc::mma_commit(bar(ACCF + t));
         }
-        tc::mma_commit(bar(B_EMPTY + s));
-        tc::mma_commit(bar(B_AEMPTY + a));
-        if (last) tc::mma_commit(bar(B_ACCF + t));
+        __syncwarp();
+        any = true;
+        if (last && ++t == 2) { t = 0; pht ^= 1; }
+        if (++sx == PS_XST) { sx = 0; phx ^= 1; }
+        if (++a == PS_NA) { a = 0; pha ^= 1; }
+        if (++k == F.ks) k = 0;
       }
-      __syncwarp();
-      any = true;
-      TRACE(1, 2, it);
-      if (last && ++t == 2) { t = 0; pht ^= 1; }
-      if (++s == TC_STAGES) { s = 0; ph ^= 1; }
-      if (++a == TC_NA) { a = 0; pha ^= 1; }
-      if (++k == ks) k = 0;
     }
     if (any) {
       // every MMA issued by this warp has completed before TMEM is released
-      if (tc::elect_one()) tc::mma_commit(bar(B_DRAIN));
+      if (tc::elect_one()) tc::mma_commit(bar(DRAIN));
       __syncwarp();
-      W.drain(bar(B_DRAIN), 0);
+      W.drain(bar(DRAIN), 0);
     }
-  } else if (warp < TC_EPI_WARP0) {
+  } else if (warp < PS_EPI_WARP0) {
     // ------------------------------------------------------------ dequantisation
     const int q = warp & 3;              // TMEM lane quarter of this warp
     const int hk = (warp - 2) >> 2;      // which 64 columns of the step
     const int r = q * 32 + lane;         // weight row within the tile
     int s = 0, a = 0;
     uint32_t ph = 0, pha = 0;
-    for (int it = beg; it < end; ++it) {
-      if (!W.wait(bar(B_FULL + s), ph)) break;
-      if (warp == 2 && lane == 0) TRACE(2, 0, it);
-      if (!W.wait(bar(B_AEMPTY + a), pha ^ 1)) break;
-      if (warp == 2 && lane == 0) TRACE(2, 1, it);
-      const uint8_t* crow = stage_codes(s) + r * 128;
-      uint4 cw[4];
+    bool stop = false;
+    for (int p = 0; p < P.nph && !stop; ++p) {
+      int beg, end;
+      range(p, beg, end);
+      for (int it = beg; it < end; ++it) {
+        if (!__all_sync(FULL, W.wait(bar(FULL_W + s), ph))) { stop = true; break; }
+        if (!__all_sync(FULL, W.wait(bar(AEMPTY + a), pha ^ 1))) { stop = true; break; }
+        const uint8_t* st = wring + s * PS_W_BYTES;
+        const uint8_t* crow = st + r * 128;
+        uint4 cw[4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int cc = hk * 4 + c;
-        cw[c] = *reinterpret_cast<const uint4*>(crow + ((cc ^ (r & 7)) << 4));
-      }
-      const uint2 pr = *reinterpret_cast<const uint2*>(stage_params(s) + r * 16 + hk * 8);
-      const uint32_t prw[2] = {pr.x, pr.y};
-      uint32_t out[32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const __half2 so = *reinterpret_cast<const __half2*>(&prw[c >> 1]);
-        const __half2 s2 = __low2half2(so), o2 = __high2half2(so);
-        const uint32_t wv[4] = {cw[c].x, cw[c].y, cw[c].z, cw[c].w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t u = wv[i] ^ 0x80808080u;
-          const __half2 lo = __hfma2(s8pair_to_h2(u, 0x4140), s2, o2);
-          const __half2 hi = __hfma2(s8pair_to_h2(u, 0x4342), s2, o2);
-          out[c * 8 + 2 * i] = *reinterpret_cast<const uint32_t*>(&lo);
-          out[c * 8 + 2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+        for (int c = 0; c < 4; ++c) {
+          const int cc = hk * 4 + c;
+          cw[c] = *reinterpret_cast<const uint4*>(crow + ((cc ^ (r & 7)) << 4));
         }
-      }
-      if constexpr (A_TMEM) {
-        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + 2 * TC_ACC_COLS + a * TC_A_COLS + hk * 32;
+        const uint2 pr = *reinterpret_cast<const uint2*>(st + PS_CODES_BYTES + r * 16 + hk * 8);
+        const uint32_t prw[2] = {pr.x, pr.y};
+        uint32_t out[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const __half2 so = *reinterpret_cast<const __half2*>(&prw[c >> 1]);
+          const __half2 s2 = __low2half2(so), o2 = __high2half2(so);
+          const uint32_t wv[4] = {cw[c].x, cw[c].y, cw[c].z, cw[c].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t u = wv[i] ^ 0x80808080u;
+            const __half2 lo = __hfma2(s8pair_to_h2(u, 0x4140), s2, o2);
+            const __half2 hi = __hfma2(s8pair_to_h2(u, 0x4342), s2, o2);
+            out[c * 8 + 2 * i] = *reinterpret_cast<const uint32_t*>(&lo);
+            out[c * 8 + 2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+          }
+        }
+        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + 2 * PS_ACC_COLS + a * PS_A_COLS + hk * 32;
         tc::tmem_st_32x32b_x32(ta, out);
         tc::tmem_wait_st();
         tc::fence_before_sync();
-      } else {
-        uint8_t* ab = abuf + a * (TC_BM * TC_BK * 2);
-#pragma unroll
-        for (int g8 = 0; g8 < 8; ++g8) {
-          const int g = hk * 8 + g8;       // 16-byte chunk of the row (8 halves)
-          uint8_t* dst = ab + (g >> 3) * (TC_BM * 128) + (r >> 3) * 1024 + (r & 7) * 128 + (((g & 7) ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4*>(dst) =
-              make_uint4(out[4 * g8], out[4 * g8 + 1], out[4 * g8 + 2], out[4 * g8 + 3]);
+        __syncwarp();
+        if (lane == 0) {
+          tc::mbar_arrive(bar(AFULL + a));
+          tc::mbar_arrive(bar(EMPTY_W + s));
         }
-        tc::fence_proxy_async_smem();
+        if (++s == WST) { s = 0; ph ^= 1; }
+        if (++a == PS_NA) { a = 0; pha ^= 1; }
       }
-      __syncwarp();
-      if (lane == 0) {
-        if (warp == 2) TRACE(2, 2, it);
-        tc::mbar_arrive(bar(B_AFULL + a));
-        tc::mbar_arrive(bar(B_EMPTY + s));
-      }
-      if (++s == TC_STAGES) { s = 0; ph ^= 1; }
-      if (++a == TC_NA) { a = 0; pha ^= 1; }
     }
-  } else {
-    // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;
-    const int r = q * 32 + lane;
-    const int et = threadIdx.x - TC_EPI_WARP0 * 32;  // 0..127
+  } else if (warp < PS_XP_WARP) {
+    // ------------------------------------------------------------ epilogue, and the inputs of later phases
+    const int q = warp & 3;                          // TMEM lane quarter
+    const int r = q * 32 + lane;                     // accumulator row of this thread
+    const int et = threadIdx.x - PS_EPI_WARP0 * 32;  // 0..127
+    float4* acc4 = reinterpret_cast<float4*>(s_acc);
+    float4* fix4 = reinterpret_cast<float4*>(fixb);
+    const int nvec = P.B * (TC_BM / 4);
+
+    // Input of phase p >= 1, made by all blocks once every tile of phase p-1 is final:
+    // per position (Σy², max|γ·y|) from the tiles' statistics (same values in every
+    // block), then this block's slices of 32 columns: v = γ·(y·inv) or y, tap = v,
+    // X = binary16(v·2^k).
+    auto make_input = [&](int p) -> bool {
+      const PsPhase& F = P.ph[p];
+      bool ok = true;
+      if (et == 0) ok = W.count(P.done + (p - 1), (unsigned)P.ph[p - 1].ntiles);
+      if (!epi_all(ok)) return false;
+      const PsJob& S = P.job[F.src_job];
+      const int nt = S.ntiles;
+      const int prev = (p - 1) & 1;
+      {
+        const int b = et & 63, half = et >> 6;
+        float ss = 0.f, mx = 0.f;
+        if (b < P.B) {
+          const int lo = half ? nt / 2 : 0, hi = half ? nt : nt / 2;
+          for (int tt = lo; tt < hi; ++tt) {
+            const float2 v = __ldcg(P.stats + ((size_t)prev * P.maxtiles + tt) * 64 + b);
+            ss += v.x;
+            mx = fmaxf(mx, v.y);
+          }
+        }
+        s_st[half][b] = make_float2(ss, mx);
+      }
+      epi_bar();
+      if (et < 64) {
+        float inv = 0.f, sc = 0.f, xi = 0.f;
+        if (et < P.B)
+          input_scale(s_st[0][et].x + s_st[1][et].x, fmaxf(s_st[0][et].y, s_st[1][et].y), F.K, P.eps,
+                      F.gamma != nullptr, inv, sc, xi);
+        s_inv[et] = inv;
+        s_sc[et] = sc;
+        s_xinv[et] = xi;
+      }
+      epi_bar();
+      const float* src = S.y;
+      __half* xh = P.xh[F.xk];
+      const int rb = et >> 1, cofs = (et & 1) * 16;
+      for (int sl = cta; sl * 32 < F.K; sl += G) {
+        const int col = sl * 32 + cofs;
+        if (rb < Bp) {
+          uint32_t hv[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+          if (rb < P.B) {
+            const float inv = s_inv[rb], sc = s_sc[rb];
+            const float4* y4 = reinterpret_cast<const float4*>(src + (size_t)rb * F.K + col);
+            float4 v[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = __ldcg(y4 + i);
+            if (F.gamma) {
+              const float4* g4 = reinterpret_cast<const float4*>(F.gamma + col);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float4 g = g4[i];
+                v[i] = make_float4(g.x * (v[i].x * inv), g.y * (v[i].y * inv), g.z * (v[i].z * inv),
+                                   g.w * (v[i].w * inv));
+              }
+              if (F.tap) {
+                float4* t4 = reinterpret_cast<float4*>(F.tap + (size_t)rb * F.K + col);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) t4[i] = v[i];
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const __half2 lo = __floats2half2_rn(v[i].x * sc, v[i].y * sc);
+              const __half2 hi = __floats2half2_rn(v[i].z * sc, v[i].w * sc);
+              hv[2 * i] = *reinterpret_cast<const uint32_t*>(&lo);
+              hv[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+            }
+          }
+          uint4* d = reinterpret_cast<uint4*>(xh + (size_t)rb * F.K + col);
+          d[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+          d[1] = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+        }
+      }
+      // the input is read by tensor copies (async proxy) in every block
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      epi_bar();
+      if (et == 0) release_add(P.prep_done + p);
+      return true;
+    };
+
     int t = 0;
     uint32_t pht = 0;
-    int it = beg;
-    while (it < end) {
-      const int tile = it / ks;
-      const int tile_end = (tile + 1) * ks;
-      const int seg_end = end < tile_end ? end : tile_end;
-      const bool whole = (it == tile * ks) && (seg_end == tile_end);
-      const int j = job_of_tile(P, tile);
-      const int rows = P.rows[j];
-      const int row = (tile - P.tile_begin[j]) * TC_BM + r;
-      const bool ok = W.wait(bar(B_ACCF + t), pht);
-      if (et == 0) TRACE(3, 0, it);
-      // leave together: a warp missing from the named barriers below would hang the rest
-      if (!epi_all(ok)) break;
-      tc::fence_after_sync();
-      const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + t * TC_ACC_COLS;
-      // accumulator row -> scaled, transposed into the shared tile s_acc[b][r]
+    bool stop = false;
+    for (int p = 0; p < P.nph && !stop; ++p) {
+      const PsPhase& F = P.ph[p];
+      const int par = p & 1;
+      if (p > 0 && !make_input(p)) break;
+      epi_bar();   // this phase's s_xinv
+      int beg, end;
+      range(p, beg, end);
+      const int first_tile = beg / F.ks;
+      int it = beg;
+      while (it < end) {
+        const int tile = it / F.ks;
+        const int tile_end = (tile + 1) * F.ks;
+        const int seg_end = end < tile_end ? end : tile_end;
+        const bool whole = (it == tile * F.ks) && (seg_end == tile_end);
+        const int j = job_of_tile(P, F, tile);
+        const PsJob& J = P.job[j];
+        const int rows = J.rows;
+        const int row0 = (tile - J.tile0) * TC_BM;
+        const bool ok = W.wait(bar(ACCF + t), pht);
+        if (!epi_all(ok)) { stop = true; break; }
+        tc::fence_after_sync();
+        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + t * PS_ACC_COLS;
+        const int c_first = whole ? cta : cta_of_item(tile * F.ks, G, F.T);
+        const int c_last = whole ? cta : cta_of_item(tile_end - 1, G, F.T);
+        const bool contributor = cta != c_first;
+        // accumulator row r, scaled, into this block's partial (a contributor) or the
+        // shared transposed tile; layout [position][128 rows] in both
+        float* dst = contributor
+                         ? P.partials + (((size_t)par * G + cta) * P.maxseg + (tile - first_tile)) * Bp * TC_BM
+                         : s_acc;
 #pragma unroll
-      for (int c0 = 0; c0 < TC_ACC_COLS; c0 += 16) {
-        if (c0 < Bp) {
-          uint32_t u[16];
-          tc::tmem_ld_32x32b_x16(ta + c0, u);
-          tc::tmem_wait_ld();
+        for (int c0 = 0; c0 < PS_ACC_COLS; c0 += 16) {
+          if (c0 < Bp) {
+            uint32_t u[16];
+            tc::tmem_ld_32x32b_x16(ta + c0, u);
+            tc::tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) s_acc[(c0 + i) * TC_BM + r] = __uint_as_float(u[i]) * s_xinv[c0 + i];
+            for (int i = 0; i < 16; ++i) dst[(c0 + i) * TC_BM + r] = __uint_as_float(u[i]) * s_xinv[c0 + i];
+          }
         }
-      }
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(bar(B_ACCE + t));
-      if (++t == 2) { t = 0; pht ^= 1; }
-
-      const int epi = P.epi[j];
-      float* y = P.y[j];
-      const float* res = P.residual[j];
-      const int row0 = row - r;
-      epi_bar();
-      const float4* acc4 = reinterpret_cast<const float4*>(s_acc);
-      const int nvec = P.B * (TC_BM / 4);
-      const bool vec_ok = ((rows & 3) == 0) && ((reinterpret_cast<uintptr_t>(y) & 15) == 0) &&
-                          (epi != PGQ_EPI_ADD || (reinterpret_cast<uintptr_t>(res) & 15) == 0);
-      if (whole) {
-        out_rows(acc4, nvec, et, epi, y, res, rows, row0, vec_ok);
-      } else {
-        const int c_first = cta_of_item(tile * ks, G, T);
-        const int c_last = cta_of_item(tile_end - 1, G, T);
-        if ((int)blockIdx.x != c_first) {
-          // a contributor: publish this block's f32 partial of the tile, then count it
-          // on the tile's counter (one gpu-scope release after the block's stores)
-          const int first_tile = beg / ks;
-          float4* part = reinterpret_cast<float4*>(P.partials +
-                                                   ((size_t)blockIdx.x * P.maxseg + (tile - first_tile)) * Bp * TC_BM);
-#pragma unroll
-          for (int k = 0; k < TC_OUT_K; ++k)
-            if (et + 128 * k < nvec) part[et + 128 * k] = acc4[et + 128 * k];
-          epi_bar();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(bar(ACCE + t));
+        if (++t == 2) { t = 0; pht ^= 1; }
+        epi_bar();
+        if (contributor) {
+          // the block's stores, then one gpu-scope release and the count on the tile
+          if (et == 0) release_add(P.tile_cnt + (size_t)par * P.maxtiles + tile);
+          it = seg_end;
+          continue;
+        }
+        if (!whole) {
+          // the owner: the other contributors' partials, one at a time through the
+          // shared buffer (each thread copies and adds its own float4 slots), in block
+          // order.  Blocks only wait for higher-numbered blocks, and the launch is
+          // cooperative (all blocks resident), so the wait ends.
+          bool okc = true;
           if (et == 0) {
-            asm volatile("fence.acq_rel.gpu;" ::: "memory");
-            atomicAdd(P.tile_cnt + tile, 1u);
+            okc = W.count(P.tile_cnt + (size_t)par * P.maxtiles + tile, (unsigned)(c_last - c_first));
+            if (okc) P.tile_cnt[(size_t)par * P.maxtiles + tile] = 0u;
           }
-          if (et == 0) TRACE(3, 2, it);
-        } else {
-          // the owner (the block holding the tile's first k-steps, which it reaches at
-          // the end of its range): wait for the other contributors' partials, add them
-          // in block order to its own accumulator and write the tile.  Blocks only ever
-          // wait for higher-numbered blocks, and the launch is cooperative (all blocks
-          // resident), so the waits always end.
-          bool ok = true;
-          if (et == 0) {
-            const unsigned need = (unsigned)(c_last - c_first);
-            const uint64_t w0 = tc::globaltimer();
-            while (true) {
-              unsigned v;
-              asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(P.tile_cnt + tile) : "memory");
-              if (v >= need) break;
-              if (*abort_flag || tc::globaltimer() - w0 > P.wait_limit_ns) {
-                *abort_flag = 1;
-                atomicCAS(P.status, 0, PGQ_ETIMEOUT);
-                ok = false;
-                break;
-              }
-              __nanosleep(64);
-            }
-            P.tile_cnt[tile] = 0u;
-          }
-          if (!epi_all(ok)) break;
-          if (et == 0) TRACE(3, 2, it);
-          // the contributors' partials land in the (now idle) stage ring, a batch of
-          // whole partials at a time, each thread copying and adding its own float4 slots
-          const int part_f4 = Bp * TC_BM / 4;
-          const int per_batch = (TC_STAGES * stage_bytes) / (part_f4 * 16);
-          float4* ring4 = reinterpret_cast<float4*>(stages);
-          float4* sum4 = reinterpret_cast<float4*>(s_acc);
-          for (int c0 = c_first + 1; c0 <= c_last; c0 += per_batch) {
-            const int c1 = min(c_last, c0 + per_batch - 1);
-            for (int c = c0; c <= c1; ++c) {
-              const int ft = item_begin(c, G, T) / ks;
-              const float4* pc =
-                  reinterpret_cast<const float4*>(P.partials + ((size_t)c * P.maxseg + (tile - ft)) * Bp * TC_BM);
-              float4* dst = ring4 + (size_t)(c - c0) * part_f4;
+          if (!epi_all(okc)) { stop = true; break; }
+          for (int cc = c_first + 1; cc <= c_last; ++cc) {
+            const int ft = item_begin(cc, G, F.T) / F.ks;
+            const float4* pc = reinterpret_cast<const float4*>(
+                P.partials + (((size_t)par * G + cc) * P.maxseg + (tile - ft)) * Bp * TC_BM);
 #pragma unroll
-              for (int k = 0; k < TC_OUT_K; ++k) {
-                const int i = et + 128 * k;
-                if (i < nvec)
-                  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_addr(dst + i)),
-                               "l"(pc + i)
-                               : "memory");
-              }
+            for (int k = 0; k < PS_OUT_K; ++k) {
+              const int i = et + 128 * k;
+              if (i < nvec)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_addr(fix4 + i)), "l"(pc + i)
+                             : "memory");
             }
             asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-            for (int c = c0; c <= c1; ++c) {
-              const float4* src = ring4 + (size_t)(c - c0) * part_f4;
 #pragma unroll
-              for (int k = 0; k < TC_OUT_K; ++k) {
-                const int i = et + 128 * k;
-                if (i < nvec) {
-                  const float4 u = src[i];
-                  float4 t4 = sum4[i];
-                  t4.x += u.x; t4.y += u.y; t4.z += u.z; t4.w += u.w;
-                  sum4[i] = t4;
-                }
+            for (int k = 0; k < PS_OUT_K; ++k) {
+              const int i = et + 128 * k;
+              if (i < nvec) {
+                const float4 u = fix4[i];
+                float4 s4 = acc4[i];
+                s4.x += u.x; s4.y += u.y; s4.z += u.z; s4.w += u.w;
+                acc4[i] = s4;
               }
             }
           }
-          out_rows(acc4, nvec, et, epi, y, res, rows, row0, vec_ok);
-          if (et == 0) TRACE(3, 3, it);
         }
+        const bool vec_ok = ((rows & 3) == 0) && ((reinterpret_cast<uintptr_t>(J.y) & 15) == 0) &&
+                            (J.epi != PGQ_EPI_ADD || (reinterpret_cast<uintptr_t>(J.residual) & 15) == 0);
+        const bool stats = vec_ok && j == F.stats_job;
+        out_rows(acc4, nvec, et, J.epi, J.y, J.residual, rows, row0, vec_ok, stats);
+        if (stats)
+          tile_stats(acc4, nvec, et, rows, row0, F.next_gamma,
+                     P.stats + ((size_t)par * P.maxtiles + (tile - J.tile0)) * 64);
+        epi_bar();   // the tile's stores are issued and the shared tile is free
+        if (et == 0) release_add(P.done + p);
+        it = seg_end;
       }
-      epi_bar();  // the shared tile is free for the next segment
-      if (et == 0) TRACE(3, 1, it);
-      it = seg_end;
     }
   }
 
@@ -598,52 +784,78 @@ __global__ void __launch_bounds__(TC_THREADS, 1) prefill_tc_kernel(const __grid_
   __syncthreads();
   if (warp == 1) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, TC_TMEM_COLS);
+    tc::tmem_dealloc(tmem, PS_TMEM_COLS);
   }
-#ifdef PGQ_TRACE
-  if (threadIdx.x == 0) {
-    g_cta[4 * blockIdx.x + 2] = tc::globaltimer();
-  }
-  if (blockIdx.x == 0)
-    for (int i = threadIdx.x; i < 4 * TR_ITEMS * TR_EV; i += blockDim.x) g_tr[i] = s_tr[i];
-#endif
 }
 
-// ------------------------------------------------------------------ X → binary16
-// One block per position b < Bp: amax, a power-of-two scale 2^(14 - e) with
-// amax < 2^e, x·scale rounded to binary16; xinv[b] = 2^(e - 14).  Rows b >= B are 0.
-__global__ void __launch_bounds__(256) xprep_kernel(const float* __restrict__ X, int B, int cols,
-                                                    __half* __restrict__ Xh, float* __restrict__ xinv,
-                                                    unsigned* __restrict__ tile_cnt, int ntiles, int* __restrict__ status) {
-  __shared__ float red[8];
-  const int b = blockIdx.x;
-  // the GEMM that follows on the stream starts from zero tickets and a clear status
+// The input of a launch's first phase, one block per position: optionally
+// RMS-normalised (tap = f32 copy), then binary16 with the power-of-two scale.  The
+// statistics are formed exactly as the epilogue forms them (per 128-column tile, lane
+// sums of 4 columns combined by a butterfly; tiles added in two halves), so a launch
+// that starts here and one that reaches the same input at a phase boundary make
+// identical inputs.  Block 0 also clears the launch's counters and status word.
+__global__ void __launch_bounds__(256) pass_input_kernel(const float* __restrict__ src, int B, int K,
+                                                         const float* __restrict__ gamma, float eps, float* tap,
+                                                         __half* __restrict__ xh, float* __restrict__ xinv,
+                                                         unsigned* counters, int ncounters, int* status) {
+  extern __shared__ float2 s_tiles[];   // [K / 128]
+  __shared__ float s_v[2];
+  const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (b == 0) {
-    for (int i = threadIdx.x; i < ntiles; i += 256) tile_cnt[i] = 0u;
+    for (int i = threadIdx.x; i < ncounters; i += 256) counters[i] = 0u;
     if (threadIdx.x == 0) *status = PGQ_OK;
   }
-  __half* out = Xh + (size_t)b * cols;
+  __half* out = xh + (size_t)b * K;
   if (b >= B) {
-    for (int c = threadIdx.x; c < cols; c += 256) out[c] = __ushort_as_half(0);
+    for (int c = threadIdx.x * 8; c < K; c += 256 * 8) *reinterpret_cast<uint4*>(out + c) = make_uint4(0u, 0u, 0u, 0u);
     if (threadIdx.x == 0) xinv[b] = 0.f;
     return;
   }
-  const float* x = X + (size_t)b * cols;
-  float m = 0.f;
-  for (int c = threadIdx.x; c < cols; c += 256) m = fmaxf(m, fabsf(x[c]));
+  const float* x = src + (size_t)b * K;
+  const int nt = K / TC_BM;
+  for (int tt = warp; tt < nt; tt += 8) {
+    const float4 a = *reinterpret_cast<const float4*>(x + tt * TC_BM + lane * 4);
+    float4 g = make_float4(1.f, 1.f, 1.f, 1.f);
+    if (gamma) g = *reinterpret_cast<const float4*>(gamma + tt * TC_BM + lane * 4);
+    float ss = sq4(a), mx = gmax4(a, g);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    for (int o = 16; o > 0; o >>= 1) {
+      ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    if (lane == 0) s_tiles[tt] = make_float2(ss, mx);
+  }
   __syncthreads();
-  m = 0.f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) m = fmaxf(m, red[i]);
-  int e = 0;
-  if (m > 0.f && m <= 3.0e38f) frexpf(m, &e);   // m = f·2^e, f in [0.5, 1)
-  const int k = max(-120, min(120, 14 - e));
-  const float sc = ldexpf(1.f, k);
-  for (int c = threadIdx.x; c < cols; c += 256) out[c] = __float2half_rn(x[c] * sc);
-  if (threadIdx.x == 0) xinv[b] = ldexpf(1.f, -k);
+  if (threadIdx.x == 0) {
+    float lo = 0.f, hi = 0.f, m0 = 0.f, m1 = 0.f;
+    for (int tt = 0; tt < nt / 2; ++tt) {
+      lo += s_tiles[tt].x;
+      m0 = fmaxf(m0, s_tiles[tt].y);
+    }
+    for (int tt = nt / 2; tt < nt; ++tt) {
+      hi += s_tiles[tt].x;
+      m1 = fmaxf(m1, s_tiles[tt].y);
+    }
+    float inv, sc, xi;
+    input_scale(lo + hi, fmaxf(m0, m1), K, eps, gamma != nullptr, inv, sc, xi);
+    s_v[0] = inv;
+    s_v[1] = sc;
+    xinv[b] = xi;
+  }
+  __syncthreads();
+  const float inv = s_v[0], sc = s_v[1];
+  for (int c = threadIdx.x * 4; c < K; c += 256 * 4) {
+    float4 v = *reinterpret_cast<const float4*>(x + c);
+    if (gamma) {
+      const float4 g = *reinterpret_cast<const float4*>(gamma + c);
+      v = make_float4(g.x * (v.x * inv), g.y * (v.y * inv), g.z * (v.z * inv), g.w * (v.w * inv));
+      if (tap) *reinterpret_cast<float4*>(tap + (size_t)b * K + c) = v;
+    }
+    const __half2 lo = __floats2half2_rn(v.x * sc, v.y * sc);
+    const __half2 hi = __floats2half2_rn(v.z * sc, v.w * sc);
+    *reinterpret_cast<uint2*>(out + c) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+  }
 }
 
 // ------------------------------------------------------------------ host side
@@ -704,117 +916,181 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_
   return true;
 }
 
-template <bool A_TMEM>
-size_t tc_smem_bytes(int Bp) {
-  const size_t stage = TC_CODES_BYTES + 2 * (size_t)Bp * 128 + TC_PARAMS_BYTES;
-  return 1024 /*alignment slack*/ + (A_TMEM ? TC_STAGES_TMEM : TC_STAGES_SMEM) * stage +
-         (A_TMEM ? 0 : TC_NA_SMEM * TC_BM * TC_BK * 2) + TC_ACC_TILE_BYTES + 256;
-}
+}  // namespace
 
-struct Plan {
-  int Bp, ks, ntiles, G, maxseg;
-  long long T;
-  size_t off_xh, off_xinv, off_status, off_cnt, off_part, total;
+namespace {
+
+// A phase as the host describes it: up to three matrices sharing one input.
+struct HostPhase {
+  PrefillJob job[TC_MAXJOBS];
+  int njobs;
+  int K;                     // input width
+  int xk;                    // input buffer
+  int stats_job;             // index within the phase, -1: none
+  const float* next_gamma;
+  const float* gamma;        // how this phase's input is made (see PsPhase)
+  float* tap;
 };
 
-Plan make_plan(const int* rows, int njobs, int cols, int B, int sms) {
+struct Plan {
+  int Bp, G, maxseg, maxtiles, wst, ncounters;
+  size_t smem;
+  size_t off_status, off_xh[PS_NX], off_xinv, off_cnt, off_stats, off_part, total;
+};
+
+// Shared memory of the kernel for Bp positions: the input ring, the shared tile and
+// the partial buffer are fixed; the weight ring takes the rest (at most 10 stages).
+bool kernel_smem(int Bp, const DeviceInfo& dev, int& wst, size_t& smem) {
+  const size_t fixed = 1024 /*alignment*/ + (size_t)PS_XST * 2 * Bp * 128 + 2 * (size_t)Bp * TC_BM * 4 + 512;
+  const size_t avail = (size_t)dev.smem_optin > PS_STATIC_SMEM ? (size_t)dev.smem_optin - PS_STATIC_SMEM : 0;
+  if (avail < fixed + 3 * (size_t)PS_W_BYTES) return false;
+  wst = (int)std::min<size_t>(PS_WST_MAX, (avail - fixed) / PS_W_BYTES);
+  smem = fixed + (size_t)wst * PS_W_BYTES;
+  return true;
+}
+
+Plan make_plan(const HostPhase* hp, int nph, int B, const DeviceInfo& dev) {
   Plan p{};
   p.Bp = (B + 15) / 16 * 16;
-  p.ks = (cols + TC_BK - 1) / TC_BK;
-  p.ntiles = 0;
-  for (int j = 0; j < njobs; ++j) p.ntiles += (rows[j] + TC_BM - 1) / TC_BM;
-  p.T = (long long)p.ntiles * p.ks;
-  p.G = (int)std::max<long long>(1, std::min<long long>(sms, p.T));
-  long long per = (p.T + p.G - 1) / p.G;
-  p.maxseg = (int)std::min<long long>(p.ntiles, (per + p.ks - 1) / p.ks + 1);
+  long long tmin = -1;
+  size_t xcols[PS_NX] = {0, 0, 0, 0};
+  for (int i = 0; i < nph; ++i) {
+    int tiles = 0;
+    for (int j = 0; j < hp[i].njobs; ++j) tiles += (hp[i].job[j].rows + TC_BM - 1) / TC_BM;
+    const int ks = (hp[i].K + TC_BK - 1) / TC_BK;
+    const long long T = (long long)tiles * ks;
+    tmin = tmin < 0 ? T : std::min(tmin, T);
+    p.maxtiles = std::max(p.maxtiles, tiles);
+    xcols[hp[i].xk] = std::max(xcols[hp[i].xk], (size_t)hp[i].K);
+  }
+  p.G = (int)std::max<long long>(1, std::min<long long>(dev.sms, tmin));
+  for (int i = 0; i < nph; ++i) {
+    int tiles = 0;
+    for (int j = 0; j < hp[i].njobs; ++j) tiles += (hp[i].job[j].rows + TC_BM - 1) / TC_BM;
+    const int ks = (hp[i].K + TC_BK - 1) / TC_BK;
+    const long long per = ((long long)tiles * ks + p.G - 1) / p.G;
+    p.maxseg = std::max(p.maxseg, (int)std::min<long long>(tiles, (per + ks - 1) / ks + 1));
+  }
+  if (!kernel_smem(p.Bp, dev, p.wst, p.smem)) p.wst = 0;
+  p.ncounters = 2 * PS_MAXPH + 2 * p.maxtiles;
   auto up = [](size_t v, size_t a) { return (v + a - 1) / a * a; };
   size_t o = 0;
   p.off_status = o; o += 256;
-  p.off_xh = o; o = up(o + (size_t)p.Bp * cols * 2, 1024);
-  p.off_xinv = o; o = up(o + (size_t)p.Bp * 4, 256);
-  p.off_cnt = o; o = up(o + (size_t)p.ntiles * 4, 256);
-  p.off_part = o; o = up(o + (size_t)p.G * p.maxseg * p.Bp * TC_BM * 4, 256);
+  for (int k = 0; k < PS_NX; ++k) {
+    p.off_xh[k] = o;
+    o = up(o + (size_t)p.Bp * xcols[k] * 2, 1024);
+  }
+  p.off_xinv = o; o = up(o + 64 * 4, 256);
+  p.off_cnt = o; o = up(o + (size_t)p.ncounters * 4, 256);
+  p.off_stats = o; o = up(o + 2 * (size_t)p.maxtiles * 64 * 8, 256);
+  p.off_part = o; o = up(o + 2 * (size_t)p.G * p.maxseg * p.Bp * TC_BM * 4, 256);
   p.total = o;
   return p;
 }
 
-}  // namespace
+std::mutex g_launch_mu;   // guards the parameter block and the tensor-map cache
 
-size_t prefill_workspace_bytes(const int* rows, int njobs, int cols, int B, const DeviceInfo& dev) {
-  return make_plan(rows, njobs, cols, B, dev.sms).total;
-}
-
-int prefill_status_offset() { return 0; }
-
-int launch_prefill(const PrefillJob* jobs, int njobs, const float* X, int cols, int B, void* ws, size_t ws_bytes,
-                   bool a_tmem, unsigned long long wait_limit_ns, const DeviceInfo& dev, cudaStream_t st) {
-  int rows[TC_MAXJOBS];
-  for (int j = 0; j < njobs; ++j) rows[j] = jobs[j].rows;
-  const Plan pl = make_plan(rows, njobs, cols, B, dev.sms);
+// One pass_input_kernel launch (the first phase's input) and one cooperative launch
+// of the phases.  x0 / gamma0 / tap0 make the first phase's input.
+int launch_phases(const HostPhase* hp, int nph, const float* x0, const float* gamma0, float* tap0, float eps, int B,
+                  void* ws, size_t ws_bytes, unsigned long long wait_limit_ns, const DeviceInfo& dev,
+                  cudaStream_t st) {
+  if (nph < 1 || nph > PS_MAXPH) return set_error(PGQ_EINVAL, "prefill: %d phases", nph);
+  const Plan pl = make_plan(hp, nph, B, dev);
+  if (pl.wst == 0) return set_error(PGQ_EUNSUPPORTED, "prefill: shared memory too small for B=%d", B);
   if (ws_bytes < pl.total) return set_error(PGQ_EWORKSPACE, "prefill: workspace needs %zu bytes", pl.total);
   char* w = static_cast<char*>(ws);
-  __half* Xh = reinterpret_cast<__half*>(w + pl.off_xh);
-  float* xinv = reinterpret_cast<float*>(w + pl.off_xinv);
-  static TcParams P;  // large (tensor maps); filled under the lock below
-  static std::mutex mu;
-  std::lock_guard<std::mutex> lk(mu);
+  static PsParams P;   // large (tensor maps); filled under the lock
+  std::lock_guard<std::mutex> lk(g_launch_mu);
   memset(&P, 0, sizeof(P));
-  if (!encode_2d(&P.xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Xh, cols, pl.Bp, (uint64_t)cols * 2, 64, pl.Bp,
-                 CU_TENSOR_MAP_SWIZZLE_128B))
-    return set_error(PGQ_ECUDA, "prefill: tensor map of X could not be encoded");
-  int tb = 0;
-  for (int j = 0; j < njobs; ++j) {
-    const PrefillJob& J = jobs[j];
-    if (!encode_2d(&P.cmap[j], CU_TENSOR_MAP_DATA_TYPE_UINT8, J.codes, cols, J.rows, (uint64_t)cols, TC_BK, TC_BM,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&P.pmap[j], CU_TENSOR_MAP_DATA_TYPE_UINT32, J.params, cols / 32, J.rows, (uint64_t)(cols / 32) * 4,
-                   TC_BK / 32, TC_BM, CU_TENSOR_MAP_SWIZZLE_NONE))
-      return set_error(PGQ_ECUDA, "prefill: tensor map of job %d could not be encoded", j);
-    P.y[j] = J.y;
-    P.residual[j] = J.residual;
-    P.rows[j] = J.rows;
-    P.epi[j] = J.epilogue;
-    P.tile_begin[j] = tb;
-    tb += (J.rows + TC_BM - 1) / TC_BM;
-  }
-  P.tile_begin[njobs] = tb;
-  P.njobs = njobs;
-  P.ks = pl.ks;
-  P.B = B;
-  P.Bp = pl.Bp;
-  P.ntiles = pl.ntiles;
-  P.maxseg = pl.maxseg;
-  P.total_items = pl.T;
-  P.xinv = xinv;
-  P.partials = reinterpret_cast<float*>(w + pl.off_part);
-  P.tile_cnt = reinterpret_cast<unsigned*>(w + pl.off_cnt);
-  P.status = reinterpret_cast<int*>(w + pl.off_status);
-  P.wait_limit_ns = wait_limit_ns ? wait_limit_ns : 2000000000ull;
-
-  cudaError_t e;
-  xprep_kernel<<<pl.Bp, 256, 0, st>>>(X, B, cols, Xh, xinv, P.tile_cnt, pl.ntiles, P.status);
-  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e);
-
-  const void* fn = a_tmem ? reinterpret_cast<const void*>(&prefill_tc_kernel<true>)
-                          : reinterpret_cast<const void*>(&prefill_tc_kernel<false>);
-  const size_t smem = a_tmem ? tc_smem_bytes<true>(pl.Bp) : tc_smem_bytes<false>(pl.Bp);
-  if (smem > dev.smem_optin) return set_error(PGQ_EUNSUPPORTED, "prefill: %zu bytes of shared memory", smem);
-  {
-    static std::map<std::pair<const void*, int>, size_t> done;   // guarded by `mu` above
-    size_t& cur = done[{fn, dev.device}];
-    if (smem > cur) {
-      if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
-        return cuda_status(e);
-      cur = smem;
+  for (int k = 0; k < PS_NX; ++k) P.xh[k] = reinterpret_cast<__half*>(w + pl.off_xh[k]);
+  bool mapped[PS_NX] = {false, false, false, false};
+  int nj = 0;
+  for (int i = 0; i < nph; ++i) {
+    const HostPhase& H = hp[i];
+    PsPhase& F = P.ph[i];
+    F.job0 = nj;
+    F.njobs = H.njobs;
+    F.K = H.K;
+    F.ks = (H.K + TC_BK - 1) / TC_BK;
+    F.xk = H.xk;
+    F.stats_job = H.stats_job >= 0 ? nj + H.stats_job : -1;
+    F.src_job = i > 0 ? P.ph[i - 1].stats_job : -1;
+    F.next_gamma = H.next_gamma;
+    F.gamma = H.gamma;
+    F.tap = H.tap;
+    if (i > 0 && (F.src_job < 0 || P.job[F.src_job].rows != H.K))
+      return set_error(PGQ_EINVAL, "prefill: phase %d has no input source of width %d", i, H.K);
+    if (H.njobs < 1 || H.njobs > TC_MAXJOBS) return set_error(PGQ_EINVAL, "prefill: phase %d has %d matrices", i, H.njobs);
+    int tb = 0;
+    for (int j = 0; j < H.njobs; ++j) {
+      if (nj >= PS_MAXJ) return set_error(PGQ_EINVAL, "prefill: more than %d matrices", PS_MAXJ);
+      const PrefillJob& J = H.job[j];
+      PsJob& D = P.job[nj++];
+      if (!encode_2d(&D.cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, J.codes, H.K, J.rows, (uint64_t)H.K, TC_BK, TC_BM,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !encode_2d(&D.pmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, J.params, H.K / 32, J.rows, (uint64_t)(H.K / 32) * 4,
+                     TC_BK / 32, TC_BM, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return set_error(PGQ_ECUDA, "prefill: tensor map of phase %d matrix %d could not be encoded", i, j);
+      D.y = J.y;
+      D.residual = J.residual;
+      D.rows = J.rows;
+      D.epi = J.epilogue;
+      D.tile0 = tb;
+      D.ntiles = (J.rows + TC_BM - 1) / TC_BM;
+      tb += D.ntiles;
+    }
+    F.ntiles = tb;
+    F.T = tb * F.ks;
+    if (!mapped[H.xk]) {
+      if (!encode_2d(&P.xmap[H.xk], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, P.xh[H.xk], H.K, pl.Bp, (uint64_t)H.K * 2, 64,
+                     pl.Bp, CU_TENSOR_MAP_SWIZZLE_128B))
+        return set_error(PGQ_ECUDA, "prefill: tensor map of input %d could not be encoded", H.xk);
+      mapped[H.xk] = true;
     }
   }
-  // cooperative: the owner of a tile split between blocks waits for the others'
-  // partials, so every block of the launch must be resident at once
+  float* xinv = reinterpret_cast<float*>(w + pl.off_xinv);
+  unsigned* cnt = reinterpret_cast<unsigned*>(w + pl.off_cnt);
+  P.xinv0 = xinv;
+  P.done = cnt;
+  P.prep_done = cnt + PS_MAXPH;
+  P.tile_cnt = cnt + 2 * PS_MAXPH;
+  P.stats = reinterpret_cast<float2*>(w + pl.off_stats);
+  P.partials = reinterpret_cast<float*>(w + pl.off_part);
+  P.status = reinterpret_cast<int*>(w + pl.off_status);
+  P.wait_limit_ns = wait_limit_ns ? wait_limit_ns : 2000000000ull;
+  P.eps = eps;
+  P.nph = nph;
+  P.B = B;
+  P.Bp = pl.Bp;
+  P.G = pl.G;
+  P.maxseg = pl.maxseg;
+  P.maxtiles = pl.maxtiles;
+  P.wst = pl.wst;
+
+  cudaError_t e;
+  const int K0 = hp[0].K;
+  pass_input_kernel<<<pl.Bp, 256, (size_t)(K0 / TC_BM) * sizeof(float2), st>>>(
+      x0, B, K0, gamma0, eps, tap0, P.xh[hp[0].xk], xinv, cnt, pl.ncounters, P.status);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e);
+
+  const void* fn = reinterpret_cast<const void*>(&prefill_pass_kernel);
+  {
+    static std::map<int, size_t> done;   // per device, guarded by the launch lock
+    size_t& cur = done[dev.device];
+    if (pl.smem > cur) {
+      if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem)) != cudaSuccess)
+        return cuda_status(e);
+      cur = pl.smem;
+    }
+  }
+  // cooperative: blocks wait for one another (split tiles, phase inputs), so every
+  // block of the launch must be resident at once
   void* args[] = {&P};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pl.G);
-  cfg.blockDim = dim3(TC_THREADS);
-  cfg.dynamicSmemBytes = smem;
+  cfg.blockDim = dim3(PS_THREADS);
+  cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -824,21 +1100,88 @@ int launch_prefill(const PrefillJob* jobs, int njobs, const float* X, int cols, 
   return cuda_status(cudaLaunchKernelExC(&cfg, fn, args));
 }
 
+HostPhase single_phase(const PrefillJob* jobs, int njobs, int cols) {
+  HostPhase h{};
+  for (int j = 0; j < njobs; ++j) h.job[j] = jobs[j];
+  h.njobs = njobs;
+  h.K = cols;
+  h.xk = 0;
+  h.stats_job = -1;
+  return h;
+}
+
+// The four phases of layer l: q,k,v; o (+h); up (relu²); down (+h1).  `next` says
+// whether the launch goes on with layer l + 1 (the down phase then reports the
+// statistics of the new h).
+void layer_phases(HostPhase* ph, const pgq_q8_layer& Y, int l, bool next, float* h, const float* gamma1,
+                  const float* gamma2, const PassTaps& tp) {
+  const int H = Y.hidden, KV = Y.kv, I = Y.inter;
+  HostPhase& a = ph[0];
+  a = HostPhase{};
+  a.job[0] = PrefillJob{Y.q.codes, Y.q.params, H, tp.q, nullptr, PGQ_EPI_NONE};
+  a.job[1] = PrefillJob{Y.k.codes, Y.k.params, KV, tp.k, nullptr, PGQ_EPI_NONE};
+  a.job[2] = PrefillJob{Y.v.codes, Y.v.params, KV, tp.v, nullptr, PGQ_EPI_NONE};
+  a.njobs = 3; a.K = H; a.xk = 0; a.stats_job = 0; a.next_gamma = nullptr;
+  a.gamma = gamma1 + (size_t)l * H; a.tap = tp.n1;
+  HostPhase& o = ph[1];
+  o = HostPhase{};
+  o.job[0] = PrefillJob{Y.o.codes, Y.o.params, H, tp.h1, h, PGQ_EPI_ADD};
+  o.njobs = 1; o.K = H; o.xk = 1; o.stats_job = 0; o.next_gamma = gamma2 + (size_t)l * H;
+  o.gamma = nullptr; o.tap = nullptr;
+  HostPhase& u = ph[2];
+  u = HostPhase{};
+  u.job[0] = PrefillJob{Y.up.codes, Y.up.params, I, tp.u, nullptr, PGQ_EPI_RELU2};
+  u.njobs = 1; u.K = H; u.xk = 2; u.stats_job = 0; u.next_gamma = nullptr;
+  u.gamma = gamma2 + (size_t)l * H; u.tap = tp.n2;
+  HostPhase& d = ph[3];
+  d = HostPhase{};
+  d.job[0] = PrefillJob{Y.down.codes, Y.down.params, H, h, tp.h1, PGQ_EPI_ADD};
+  d.njobs = 1; d.K = I; d.xk = 3; d.stats_job = next ? 0 : -1;
+  d.next_gamma = next ? gamma1 + (size_t)(l + 1) * H : nullptr;
+  d.gamma = nullptr; d.tap = nullptr;
+}
+
+}  // namespace
+
+size_t prefill_workspace_bytes(const int* rows, int njobs, int cols, int B, const DeviceInfo& dev) {
+  PrefillJob jobs[TC_MAXJOBS] = {};
+  for (int j = 0; j < njobs; ++j) jobs[j].rows = rows[j];
+  const HostPhase h = single_phase(jobs, njobs, cols);
+  return make_plan(&h, 1, B, dev).total;
+}
+
+size_t prefill_pass_gemm_bytes(int H, int KV, int I, int B, const DeviceInfo& dev) {
+  pgq_q8_layer Y{};
+  Y.hidden = H;
+  Y.kv = KV;
+  Y.inter = I;
+  HostPhase ph[PS_MAXPH];
+  PassTaps tp{};
+  for (int l = 0; l < PS_MAXL; ++l) layer_phases(ph + 4 * l, Y, l, l + 1 < PS_MAXL, nullptr, nullptr, nullptr, tp);
+  return make_plan(ph, PS_MAXPH, B, dev).total;
+}
+
+int prefill_status_offset() { return 0; }
+
+int launch_prefill(const PrefillJob* jobs, int njobs, const float* X, int cols, int B, void* ws, size_t ws_bytes,
+                   unsigned long long wait_limit_ns, const DeviceInfo& dev, cudaStream_t st) {
+  const HostPhase h = single_phase(jobs, njobs, cols);
+  return launch_phases(&h, 1, X, nullptr, nullptr, 0.f, B, ws, ws_bytes, wait_limit_ns, dev, st);
+}
+
+int launch_prefill_pass(const pgq_q8_layer* layers, int L, float* h, int B, const float* gamma1,
+                        const float* gamma2, float eps, const PassTaps& taps, void* ws, size_t ws_bytes,
+                        const DeviceInfo& dev, cudaStream_t st) {
+  HostPhase ph[PS_MAXPH];
+  for (int l0 = 0; l0 < L; l0 += PS_MAXL) {
+    const int n = std::min(PS_MAXL, L - l0);
+    for (int i = 0; i < n; ++i)
+      layer_phases(ph + 4 * i, layers[l0 + i], l0 + i, i + 1 < n, h, gamma1, gamma2, taps);
+    const int rc = launch_phases(ph, 4 * n, h, gamma1 + (size_t)l0 * layers[0].hidden, taps.n1, eps, B, ws,
+                                 ws_bytes, 0, dev, st);
+    if (rc) return rc;
+  }
+  return PGQ_OK;
+}
+
 }  // namespace pgq
-
-#ifdef PGQ_TRACE
-// Instrumented builds only: copy out and reset the event trace of block 0.
-extern "C" int pgq_debug_cta(unsigned long long* out, unsigned nblocks) {
-  if (cudaDeviceSynchronize() != cudaSuccess) return -1;
-  if (nblocks > 1024) nblocks = 1024;
-  return cudaMemcpyFromSymbol(out, pgq::g_cta, (size_t)nblocks * 4 * sizeof(unsigned long long)) == cudaSuccess
-             ? 0 : -1;
-}
-
-extern "C" int pgq_debug_trace(long long* out, unsigned max_values) {
-  if (cudaDeviceSynchronize() != cudaSuccess) return -1;
-  unsigned n = 4 * pgq::TR_ITEMS * pgq::TR_EV;
-  if (n > max_values) n = max_values;
-  return cudaMemcpyFromSymbol(out, pgq::g_tr, (size_t)n * sizeof(long long)) == cudaSuccess ? (int)n : -1;
-}
-#endif
