@@ -537,6 +537,10 @@ size_t gemv_argmax_workspace_bytes(int B, const DeviceInfo& dev) {
 }
 
 int launch_gemv(GvParams& P, bool q8, bool argmax, const DeviceInfo& dev, cudaStream_t st) {
+  if (argmax && !q8) {
+    const int rc = launch_head_tc(P, dev, st);   // binary16 head at 2..8 positions
+    if (rc != PGQ_EUNSUPPORTED) return rc;
+  }
   {
     const int rc = launch_gemv_tma(P, q8, argmax, dev, st);
     if (rc != PGQ_EUNSUPPORTED) return rc;

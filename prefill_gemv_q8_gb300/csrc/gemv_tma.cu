@@ -12,6 +12,7 @@
 // across the QW column shares (shared memory, fixed order, after a named barrier of
 // the group), then the group's first warp applies the epilogue and stores.
 #include <algorithm>
+#include <cstring>
 #include <map>
 #include <mutex>
 
@@ -605,6 +606,394 @@ int decode_status_read_and_clear(int* out) {
   if (e != cudaSuccess) return cuda_status(e);
   *out = v;
   return PGQ_OK;
+}
+
+
+// ------------------------------------------------------------------ vocab head, 2 <= B <= 8
+// With binary16 weights and several positions, the head is a small dense contraction:
+// the weight tiles (128 rows, walked in 64-column steps) go by TMA straight into the
+// operand layout and the tensor cores (tcgen05.mma, A and B from shared memory,
+// N = 16) take them as they are; no conversion work per weight.  The block's input, RMS-normalised and
+// converted to binary16 with one power-of-two scale per position (undone on the
+// logits), stays in shared memory for the whole launch.  Each block takes a contiguous
+// range of whole tiles; the epilogue keeps per thread the best (logit, row) of every
+// position (gemv_kernel's argmax rules), and the last block to finish merges the blocks'
+// partials in block order.
+constexpr int HD_THREADS = 192;        // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int HD_NP = 16;              // MMA N (positions, padded)
+constexpr int HD_BM = 128, HD_BK = 64;         // a k-step: 64 columns (one 128-byte swizzle atom row)
+constexpr int HD_STAGE = HD_BM * HD_BK * 2;   // 16 KB of weights per k-step
+constexpr int HD_COLS_MAX = 4096;
+
+struct HdParams {
+  CUtensorMap wmap;          // binary16 [rows][cols], box {64, 128}, 128-byte swizzle (one k-step)
+  const float* x;            // [B][cols]
+  const float* gamma;        // [cols] or null
+  float* logits;             // [B][rows] or null
+  int rows, cols, B, ks, ntiles, nst;
+  float eps;
+  float* part_val;
+  int* part_idx;
+  unsigned* ticket;
+  int32_t* ids;
+  unsigned long long wait_limit_ns;
+};
+
+__global__ void __launch_bounds__(HD_THREADS, 1) head_tc_kernel(const __grid_constant__ HdParams P) {
+  extern __shared__ uint8_t hsm_raw[];
+  uint8_t* hsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(hsm_raw) + 1023) & ~uintptr_t(1023));
+  const int ks = P.ks, NST = P.nst, B = P.B;
+  uint8_t* xsm = hsm;                                 // [ks][16 rows][128 B], swizzled
+  uint8_t* wring = xsm + (size_t)ks * HD_NP * 128;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(wring + (size_t)NST * HD_STAGE);
+  uint64_t* full = bars;                              // [NST]
+  uint64_t* empty = bars + 8;                         // [NST]
+  uint64_t* accf = bars + 16;                         // [2]
+  uint64_t* acce = bars + 18;                         // [2]
+  uint64_t* drain = bars + 20;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 21);
+  __shared__ float s_red[HD_THREADS / 32][8];
+  __shared__ float s_inv[8], s_xinv[8], s_sc[8];
+  __shared__ int s_abort;
+  __shared__ float s_bv[4][8];
+  __shared__ int s_bi[4][8];
+  __shared__ unsigned s_ticket;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x;
+  const int t0 = (int)((long long)blockIdx.x * P.ntiles / G), t1 = (int)((long long)(blockIdx.x + 1) * P.ntiles / G);
+  auto sa = [](const void* p) { return tc::smem_addr(p); };
+
+  if (tid == 0) {
+    for (int s = 0; s < NST; ++s) {
+      tc::mbar_init(sa(full + s), 1);
+      tc::mbar_init(sa(empty + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      tc::mbar_init(sa(accf + t), 1);
+      tc::mbar_init(sa(acce + t), 4);
+    }
+    tc::mbar_init(sa(drain), 1);
+    s_abort = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 1) tc::tmem_alloc(sa(tmem_slot), 32);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  auto wait_bar = [&](uint64_t* b, uint32_t parity) -> bool {
+    if (tc::mbar_try(sa(b), parity)) return true;
+    const uint64_t w0 = tc::globaltimer();
+    while (!tc::mbar_try_sleep(sa(b), parity, 20000u)) {
+      if (*(volatile int*)&s_abort) return false;
+      if (tc::globaltimer() - w0 > P.wait_limit_ns) {
+        *(volatile int*)&s_abort = 1;
+        atomicExch(&g_decode_status, PGQ_ETIMEOUT);
+        return false;
+      }
+    }
+    return true;
+  };
+  const uint64_t evict_first = tc::policy_evict_first();
+  constexpr unsigned FULLM = 0xffffffffu;
+  const int nitems = (t1 - t0) * ks;
+
+  // the weights do not depend on the input: the first stages are in flight while the
+  // input is staged
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < NST && i < nitems; ++i) {
+      const int tile = t0 + i / ks, k = i % ks;
+      tc::mbar_expect_tx(sa(full + i), HD_STAGE);
+      uint8_t* st = wring + (size_t)i * HD_STAGE;
+      tc::tma_load_2d_hint(sa(st), &P.wmap, k * HD_BK, tile * HD_BM, sa(full + i), evict_first);
+    }
+  }
+
+  // ---- the input: RMS statistics, the binary16 scale, then the swizzled operand
+  {
+    const int cols4 = P.cols >> 2;
+    float ss[8];
+#pragma unroll
+    for (int b = 0; b < 8; ++b) ss[b] = 0.f;
+    for (int c = tid; c < cols4; c += HD_THREADS) {
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        if (b < B) {
+          const float4 v = reinterpret_cast<const float4*>(P.x + (size_t)b * P.cols)[c];
+          ss[b] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        }
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < 8; ++b) ss[b] = warp_sum(ss[b]);
+    if (lane == 0)
+#pragma unroll
+      for (int b = 0; b < 8; ++b) s_red[warp][b] = ss[b];
+    __syncthreads();
+    if (tid < 8) {
+      float t = 0.f;
+      for (int w = 0; w < HD_THREADS / 32; ++w) t += s_red[w][tid];
+      s_inv[tid] = P.gamma ? rsqrtf(t / (float)P.cols + P.eps) : 1.f;
+    }
+    __syncthreads();
+    float mx[8];
+#pragma unroll
+    for (int b = 0; b < 8; ++b) mx[b] = 0.f;
+    for (int c = tid; c < cols4; c += HD_THREADS) {
+      const float4 g = P.gamma ? reinterpret_cast<const float4*>(P.gamma)[c] : make_float4(1.f, 1.f, 1.f, 1.f);
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        if (b < B) {
+          const float4 v = reinterpret_cast<const float4*>(P.x + (size_t)b * P.cols)[c];
+          const float inv = s_inv[b];
+          mx[b] = fmaxf(mx[b], fmaxf(fmaxf(fabsf(g.x * (v.x * inv)), fabsf(g.y * (v.y * inv))),
+                                     fmaxf(fabsf(g.z * (v.z * inv)), fabsf(g.w * (v.w * inv)))));
+        }
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < 8; ++b)
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx[b] = fmaxf(mx[b], __shfl_xor_sync(FULLM, mx[b], o));
+    __syncthreads();
+    if (lane == 0)
+#pragma unroll
+      for (int b = 0; b < 8; ++b) s_red[warp][b] = mx[b];
+    __syncthreads();
+    if (tid < 8) {
+      float m = 0.f;
+      for (int w = 0; w < HD_THREADS / 32; ++w) m = fmaxf(m, s_red[w][tid]);
+      int e = 0;
+      if (m > 0.f && m <= 3.0e38f) frexpf(m, &e);
+      const int k = max(-120, min(120, 14 - e));
+      s_sc[tid] = ldexpf(1.f, k);
+      s_xinv[tid] = ldexpf(1.f, -k);
+    }
+    __syncthreads();
+    // 16-byte chunks (8 columns) of the 16 operand rows; rows >= B are zero
+    const int nchunk = HD_NP * (P.cols >> 3);
+    for (int i = tid; i < nchunk; i += HD_THREADS) {
+      const int n = i / (P.cols >> 3), cg = i - n * (P.cols >> 3);   // row, 8-column group
+      const int c = cg * 8;
+      uint32_t h[4] = {0u, 0u, 0u, 0u};
+      if (n < B) {
+        const float inv = s_inv[n], sc = s_sc[n];
+        const float4 v0 = reinterpret_cast<const float4*>(P.x + (size_t)n * P.cols + c)[0];
+        const float4 v1 = reinterpret_cast<const float4*>(P.x + (size_t)n * P.cols + c)[1];
+        float4 g0 = make_float4(1.f, 1.f, 1.f, 1.f), g1 = g0;
+        if (P.gamma) {
+          g0 = reinterpret_cast<const float4*>(P.gamma + c)[0];
+          g1 = reinterpret_cast<const float4*>(P.gamma + c)[1];
+        }
+        const float f[8] = {g0.x * (v0.x * inv), g0.y * (v0.y * inv), g0.z * (v0.z * inv), g0.w * (v0.w * inv),
+                            g1.x * (v1.x * inv), g1.y * (v1.y * inv), g1.z * (v1.z * inv), g1.w * (v1.w * inv)};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __half2 hv = __floats2half2_rn(f[2 * e] * sc, f[2 * e + 1] * sc);
+          h[e] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
+      }
+      const int s = c / HD_BK, g = (c % HD_BK) / 8;
+      uint8_t* dst = xsm + (size_t)s * (HD_NP * 128) + (n >> 3) * 1024 + (n & 7) * 128 + ((g ^ (n & 7)) << 4);
+      *reinterpret_cast<uint4*>(dst) = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+    tc::fence_proxy_async_smem();   // the tensor cores read the operand through the async proxy
+    __syncthreads();
+  }
+
+  float best_v[8];
+  int best_i[8];
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    best_v[b] = ARGMAX_FLOOR;
+    best_i[b] = 0;
+  }
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ weight producer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      for (int i = 0; i < nitems; ++i) {
+        if (i >= NST) {
+          if (!wait_bar(empty + s, ph ^ 1)) break;
+          const int tile = t0 + i / ks, k = i % ks;
+          tc::mbar_expect_tx(sa(full + s), HD_STAGE);
+          uint8_t* st = wring + (size_t)s * HD_STAGE;
+          tc::tma_load_2d_hint(sa(st), &P.wmap, k * HD_BK, tile * HD_BM, sa(full + s), evict_first);
+        }
+        if (++s == NST) { s = 0; ph ^= 1; }
+      }
+      if (*(volatile int*)&s_abort) {
+        // let the copies already issued land before the block can exit
+        for (int i = 0; i < NST && i < nitems; ++i) {
+          const uint64_t w0 = tc::globaltimer();
+          while (!tc::mbar_try_sleep(sa(full + i), 0u, 20000u) && tc::globaltimer() - w0 < P.wait_limit_ns) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint32_t idesc = tc::idesc_f16_f32(HD_BM, HD_NP);
+    int s = 0, t = 0;
+    uint32_t ph = 0, pht = 0;
+    bool any = false;
+    for (int i = 0; i < nitems; ++i) {
+      const int k = i % ks;
+      if (k == 0 && !__all_sync(FULLM, wait_bar(acce + t, pht ^ 1))) break;
+      if (!__all_sync(FULLM, wait_bar(full + s, ph))) break;
+      tc::fence_after_sync();
+      const uint64_t a0 = tc::sdesc_sw128(sa(wring + (size_t)s * HD_STAGE));
+      const uint64_t b0 = tc::sdesc_sw128(sa(xsm + (size_t)k * HD_NP * 128));
+      if (tc::elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < HD_BK / 16; ++kk) {   // 32 bytes further along K per step
+          const uint64_t ad = a0 + (uint64_t)(kk * 2);
+          const uint64_t bd = b0 + (uint64_t)(kk * 2);
+          tc::mma_f16_ss(tmem + t * HD_NP, ad, bd, idesc, (k == 0 && kk == 0) ? 0u : 1u);
+        }
+        tc::mma_commit(sa(empty + s));
+        if (k == ks - 1) tc::mma_commit(sa(accf + t));
+      }
+      __syncwarp();
+      any = true;
+      if (k == ks - 1 && ++t == 2) { t = 0; pht ^= 1; }
+      if (++s == NST) { s = 0; ph ^= 1; }
+    }
+    if (any) {
+      if (tc::elect_one()) tc::mma_commit(sa(drain));
+      __syncwarp();
+      const uint64_t w0 = tc::globaltimer();
+      while (!tc::mbar_try_sleep(sa(drain), 0u, 20000u) && tc::globaltimer() - w0 < P.wait_limit_ns) {
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue: logits, argmax
+    const int q = warp & 3;             // TMEM lane quarter
+    const int r = q * 32 + lane;        // row within the tile
+    int t = 0;
+    uint32_t pht = 0;
+    for (int tile = t0; tile < t1; ++tile) {
+      if (!__all_sync(FULLM, wait_bar(accf + t, pht))) break;
+      tc::fence_after_sync();
+      uint32_t u[16];
+      tc::tmem_ld_32x32b_x16(tmem + ((uint32_t)(q * 32) << 16) + t * HD_NP, u);
+      tc::tmem_wait_ld();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(sa(acce + t));
+      if (++t == 2) { t = 0; pht ^= 1; }
+      const int row = tile * HD_BM + r;
+      if (row < P.rows) {
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          if (b < B) {
+            const float v = __uint_as_float(u[b]) * s_xinv[b];
+            if (P.logits) P.logits[(size_t)b * P.rows + row] = v;
+            argmax_merge(best_v[b], best_i[b], v, row);
+          }
+        }
+      }
+    }
+    // the warp's best per position, then the four warps' in shared memory
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(FULLM, best_v[b], o);
+        const int oi = __shfl_xor_sync(FULLM, best_i[b], o);
+        argmax_merge(best_v[b], best_i[b], ov, oi);
+      }
+    }
+    if (lane == 0)
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        s_bv[warp - 2][b] = best_v[b];
+        s_bi[warp - 2][b] = best_i[b];
+      }
+  }
+  __syncthreads();
+  if (tid < B) {
+    float bv = ARGMAX_FLOOR;
+    int bi = 0;
+    for (int w = 0; w < 4; ++w) argmax_merge(bv, bi, s_bv[w][tid], s_bi[w][tid]);
+    P.part_val[(size_t)blockIdx.x * B + tid] = bv;
+    P.part_idx[(size_t)blockIdx.x * B + tid] = bi;
+  }
+  __threadfence();
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, 32);
+  }
+  if (tid == 0) s_ticket = atomicAdd(P.ticket, 1u);
+  __syncthreads();
+  if (s_ticket == gridDim.x - 1) {
+    __threadfence();
+    if (tid < B) {
+      float bv = ARGMAX_FLOOR;
+      int bi = 0;
+      for (int c = 0; c < (int)gridDim.x; ++c)
+        argmax_merge(bv, bi, __ldcg(P.part_val + (size_t)c * B + tid), __ldcg(P.part_idx + (size_t)c * B + tid));
+      P.ids[tid] = bi;
+    }
+    if (tid == 0) *P.ticket = 0u;
+  }
+}
+
+int launch_head_tc(const GvParams& V, const DeviceInfo& dev, cudaStream_t st) {
+  const int B = V.B;
+  if (B < 2 || B > 8 || V.njobs != 1 || V.ninputs != 1) return PGQ_EUNSUPPORTED;
+  const int cols = V.cols, rows = V.job[0].rows;
+  if (cols % HD_BK != 0 || cols > HD_COLS_MAX || rows < HD_BM) return PGQ_EUNSUPPORTED;
+  if (!aligned16(V.job[0].w) || !aligned16(V.in[0].x) || (V.in[0].gamma && !aligned16(V.in[0].gamma)))
+    return PGQ_EUNSUPPORTED;
+  const int ks = cols / HD_BK;
+  const size_t xbytes = (size_t)ks * HD_NP * 128;
+  const size_t fixed = 1024 + xbytes + 256;
+  if ((size_t)dev.smem_optin < fixed + 4 * (size_t)HD_STAGE + 1024) return PGQ_EUNSUPPORTED;
+  const int nst = (int)std::min<size_t>(8, (dev.smem_optin - 1024 - fixed) / HD_STAGE);
+  const size_t smem = fixed + (size_t)nst * HD_STAGE;
+  static HdParams P;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  memset(&P, 0, sizeof(P));
+  if (!encode_2d(&P.wmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, V.job[0].w, cols, rows, (uint64_t)cols * 2, 64, HD_BM,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return PGQ_EUNSUPPORTED;
+  P.x = V.in[0].x;
+  P.gamma = V.in[0].gamma;
+  P.logits = V.job[0].y;
+  P.rows = rows;
+  P.cols = cols;
+  P.B = B;
+  P.ks = ks;
+  P.ntiles = (rows + HD_BM - 1) / HD_BM;
+  P.nst = nst;
+  P.eps = V.eps;
+  P.part_val = V.part_val;
+  P.part_idx = V.part_idx;
+  P.ticket = V.ticket;
+  P.ids = V.ids;
+  P.wait_limit_ns = 2000000000ull;
+  const void* fn = reinterpret_cast<const void*>(&head_tc_kernel);
+  {
+    static std::map<int, size_t> done;
+    size_t& cur = done[dev.device];
+    if (smem > cur) {
+      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return cuda_status(e);
+      cur = smem;
+    }
+  }
+  if (cudaError_t e = cudaMemsetAsync(P.ticket, 0, sizeof(unsigned), st); e != cudaSuccess) return cuda_status(e);
+  const int grid = std::max(1, std::min(dev.sms, P.ntiles));
+  void* args[] = {&P};
+  return cuda_status(cudaLaunchKernel(fn, dim3(grid), dim3(HD_THREADS), args, smem, st));
 }
 
 }  // namespace pgq

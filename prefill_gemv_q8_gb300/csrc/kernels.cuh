@@ -1,5 +1,7 @@
 // Internal launch interface between the C-ABI layer and the kernel files.
 #pragma once
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace pgq {
@@ -50,6 +52,12 @@ int launch_gemv(GvParams& P, bool q8, bool argmax, const DeviceInfo& dev, cudaSt
 // ring).  Returns PGQ_EUNSUPPORTED (nothing launched) for shapes it does not take.
 int launch_gemv_tma(const GvParams& P, bool q8, bool argmax, const DeviceInfo& dev, cudaStream_t st);
 int decode_status_read_and_clear(int* out);
+// Tensor-core vocab head (f16 weights, 2 <= B <= 8, fused RMSNorm and argmax); returns
+// PGQ_EUNSUPPORTED (nothing launched) for shapes it does not take.
+int launch_head_tc(const GvParams& P, const DeviceInfo& dev, cudaStream_t st);
+// 2-D tensor map of a row-major matrix (cached; thread-safe).
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
 // Workspace of the argmax variant: partials [grid][B] (value, index) + ticket.
 size_t gemv_argmax_workspace_bytes(int B, const DeviceInfo& dev);
 // Device address and size of the fixed scratch array of the allocation-free

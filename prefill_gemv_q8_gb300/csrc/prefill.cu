@@ -891,11 +891,15 @@ struct MapKey {
   }
 };
 
+}  // namespace
+
 // Encodes a 2-D tensor map; encodings are cached (the host-side encode costs as much
 // as a launch), keyed by every field that goes into them.
 bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
                uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
-  static std::map<MapKey, CUtensorMap> cache;   // callers hold the launch mutex
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  static std::map<MapKey, CUtensorMap> cache;
   const MapKey key{base, inner, outer, row_bytes, box_inner, box_outer, (int)dt, (int)sw};
   auto it = cache.find(key);
   if (it != cache.end()) {
@@ -915,8 +919,6 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_
   cache[key] = *m;
   return true;
 }
-
-}  // namespace
 
 namespace {
 
