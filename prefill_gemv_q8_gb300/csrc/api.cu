@@ -465,6 +465,7 @@ int pgq_moe_combine_rmsnorm(float* h, const float* o, const float* eo, const flo
 
 namespace {
 struct MoeLayout {
+  size_t gemm;
   size_t off[9];  // n, logits, sel, w, counts, offsets, entries, u, eo
   size_t total;
 };
@@ -478,7 +479,13 @@ MoeLayout moe_layout(const pgq_moe_layer& L, int B) {
     M.off[i] = o;
     o = (o + sz[i] + 255) / 256 * 256;
   }
-  M.total = o;
+  // the tensor-core expert bank's area (gathered binary16 inputs, split-tile partials)
+  DeviceInfo dev;
+  if (!device_info(&dev)) dev.sms = 160;
+  M.gemm = o;
+  const size_t g = std::max(moe_bank_tc_workspace_bytes(L.E, L.inter, L.hidden, (int)nb, dev),
+                            moe_bank_tc_workspace_bytes(L.E, L.hidden, L.inter, (int)nb, dev));
+  M.total = o + (g + 255) / 256 * 256;
   return M;
 }
 bool moe_layer_ok(const pgq_moe_layer* L, int B) {
@@ -522,12 +529,17 @@ int pgq_moe_prefill_layer(const pgq_moe_layer* L, float* h, int B, const float* 
   if ((rc = pgq_moe_route_topk(logits, B, L->E, L->k, L->renorm, sel, wts, stream))) return rc;
   if ((rc = pgq_moe_group_gather(sel, B, L->k, L->E, counts, offs, ents, nullptr, 0, 1, nullptr, stream))) return rc;
   const int nent = B * L->k;
-  if ((rc = pgq_moe_experts_q8(L->up_codes, L->up_params, L->E, L->inter, L->hidden, counts, offs, ents, nent, n, L->k,
-                               u, PGQ_EPI_RELU2, stream)))
-    return rc;
-  if ((rc = pgq_moe_experts_q8(L->down_codes, L->down_params, L->E, L->hidden, L->inter, counts, offs, ents, nent, u, 1,
-                               eo, PGQ_EPI_NONE, stream)))
-    return rc;
+  // each bank on the tensor cores where its shape allows, else the expert GEMV kernel
+  auto bank = [&](const int8_t* codes, const uint16_t* params, int rows, int cols, const float* x, int xdiv, float* yb,
+                  int epi) -> int {
+    GET_DEVICE(dev);
+    const MoeBankArgs a{codes, params, L->E, rows, cols, counts, offs, ents, nent, x, xdiv, yb, epi};
+    const int r = launch_moe_bank_tc(a, w + M.gemm, workspace_bytes - M.gemm, dev, as_stream(stream));
+    if (r != PGQ_EUNSUPPORTED) return r;
+    return pgq_moe_experts_q8(codes, params, L->E, rows, cols, counts, offs, ents, nent, x, xdiv, yb, epi, stream);
+  };
+  if ((rc = bank(L->up_codes, L->up_params, L->inter, L->hidden, n, L->k, u, PGQ_EPI_RELU2))) return rc;
+  if ((rc = bank(L->down_codes, L->down_params, L->hidden, L->inter, u, 1, eo, PGQ_EPI_NONE))) return rc;
   return pgq_moe_combine_rmsnorm(h, nullptr, eo, wts, L->k, gamma2, eps, B, L->hidden, y, nullptr, stream);
 }
 

@@ -63,7 +63,8 @@ constexpr int PS_MAXL = 8;                                    // layers per pass
 constexpr int PS_MAXPH = 4 * PS_MAXL;                         // phases per launch
 constexpr int PS_MAXJ = 6 * PS_MAXL;                          // matrices per launch
 constexpr int PS_NX = 4;                                      // input buffers (n1, q, n2, u)
-constexpr int PS_STATIC_SMEM = 2048;                          // bound on the kernel's static shared memory
+constexpr int PS_STATIC_SMEM = 4096;                          // bound on the kernel's static shared memory
+constexpr int PS_MOE_EMAX = 256;                              // experts of a grouped bank at most
 constexpr int PS_OUT_K = PS_ACC_COLS * (TC_BM / 4) / 128;     // float4 slots per epilogue thread (16)
 constexpr int PS_OUT_P = 4;                                   // handled in passes (registers)
 constexpr int PS_OUT_H = PS_OUT_K / PS_OUT_P;
@@ -100,6 +101,14 @@ struct PsParams {
   unsigned long long wait_limit_ns;
   float eps;
   int nph, B, Bp, G, maxseg, maxtiles, wst;
+  // A grouped expert bank (one phase, one matrix [E][rows][cols]): tile t is tile
+  // t mod tpe of expert t / tpe; the expert's entries are rows [off, off + cnt) of the
+  // gathered input (at most 64), and entry n's outputs go to row ent[off + n].
+  int moe, E, tpe, nent;
+  const int32_t* mcnt;
+  const int32_t* moff;
+  const int32_t* ments;
+  const float* mxinv;        // [nent] inverse input scales of the gathered rows
 };
 static_assert(sizeof(PsParams) <= 32000, "kernel parameters");
 
@@ -252,7 +261,7 @@ __device__ __forceinline__ __half2 s8pair_to_h2(uint32_t u_biased, uint32_t sel)
 // the final values in acc4.  Thread et takes float4 et, et+128, ... (at most 16); all
 // reads (shared tile, residual) of a pass are issued before its first store.
 __device__ __forceinline__ void out_rows(float4* acc4, int nvec, int et, int epi, float* y, const float* res, int rows,
-                                         int row0, bool vec_ok, bool writeback) {
+                                         int row0, bool vec_ok, bool writeback, const int* rowtab = nullptr) {
   if (vec_ok) {
 #pragma unroll
     for (int h = 0; h < PS_OUT_P; ++h) {
@@ -264,7 +273,7 @@ __device__ __forceinline__ void out_rows(float4* acc4, int nvec, int et, int epi
         if (i < nvec) {
           a[k] = acc4[i];
           if (epi == PGQ_EPI_ADD && rr < rows)
-            q[k] = __ldcg(reinterpret_cast<const float4*>(res + (size_t)(i >> 5) * rows + rr));
+            q[k] = __ldcg(reinterpret_cast<const float4*>(res + (size_t)(rowtab ? rowtab[i >> 5] : (i >> 5)) * rows + rr));
         }
       }
 #pragma unroll
@@ -279,7 +288,7 @@ __device__ __forceinline__ void out_rows(float4* acc4, int nvec, int et, int epi
           } else if (epi == PGQ_EPI_ADD) {
             o = make_float4(q[k].x + o.x, q[k].y + o.y, q[k].z + o.z, q[k].w + o.w);
           }
-          *reinterpret_cast<float4*>(y + (size_t)(i >> 5) * rows + rr) = o;
+          *reinterpret_cast<float4*>(y + (size_t)(rowtab ? rowtab[i >> 5] : (i >> 5)) * rows + rr) = o;
           if (writeback) acc4[i] = o;
         }
       }
@@ -290,7 +299,7 @@ __device__ __forceinline__ void out_rows(float4* acc4, int nvec, int et, int epi
       const int i = et + 128 * k;
       if (i >= nvec) break;
       const int rr = row0 + (i & 31) * 4;
-      const size_t idx = (size_t)(i >> 5) * rows + rr;
+      const size_t idx = (size_t)(rowtab ? rowtab[i >> 5] : (i >> 5)) * rows + rr;
       const float4 a = acc4[i];
       const float av[4] = {a.x, a.y, a.z, a.w};
       for (int e = 0; e < 4 && rr + e < rows; ++e) {
@@ -333,6 +342,7 @@ __device__ __forceinline__ void tile_stats(const float4* acc4, int nvec, int et,
   if ((lane & 1) == 0) out[we + 4 * (lane >> 1)] = make_float2(tss, tmx);
 }
 
+template <bool MOE>
 __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __grid_constant__ PsParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -358,6 +368,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   __shared__ float s_xinv[64], s_inv[64], s_sc[64];
+  __shared__ int s_mcnt[MOE ? PS_MOE_EMAX : 1], s_moff[MOE ? PS_MOE_EMAX : 1], s_ent[MOE ? 64 : 1];
   __shared__ float2 s_st[2][64];
 
   auto bar = [&](int i) { return tc::smem_addr(bars + i); };
@@ -387,11 +398,25 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
   }
   if (warp == 1) tc::tmem_alloc(tc::smem_addr(tmem_slot), PS_TMEM_COLS);
   if (threadIdx.x < 64) s_xinv[threadIdx.x] = (int)threadIdx.x < Bp ? P.xinv0[threadIdx.x] : 0.f;
+  if constexpr (MOE) {
+    // the experts' entry counts and offsets, clamped to the gathered rows
+    for (int e = threadIdx.x; e < P.E; e += blockDim.x) {
+      const int o = min(max(P.moff[e], 0), P.nent);
+      s_moff[e] = o;
+      s_mcnt[e] = min(min(max(P.mcnt[e], 0), 64), P.nent - o);
+    }
+  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   Waiter W{P, abort_flag};
+  // a grouped bank skips the tiles of experts without entries (every role alike)
+  const int tpe = MOE ? P.tpe : 1;
+  auto skipped = [&](int tile) -> bool {
+    if constexpr (MOE) return s_mcnt[tile / tpe] == 0;
+    return false;
+  };
   auto range = [&](int p, int& beg, int& end) {
     beg = item_begin(cta, G, P.ph[p].T);
     end = item_begin(cta + 1, G, P.ph[p].T);
@@ -411,21 +436,24 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
       int tile = beg / F.ks, k = beg - (beg / F.ks) * F.ks;
       int j = job_of_tile(P, F, tile);
       for (int it = beg; it < end; ++it) {
-        if (!__all_sync(FULL, W.wait(bar(EMPTY_W + s), ph ^ 1))) {
-          stop = true;
-          break;
+        if (!skipped(tile)) {
+          if (!__all_sync(FULL, W.wait(bar(EMPTY_W + s), ph ^ 1))) {
+            stop = true;
+            break;
+          }
+          if (tc::elect_one()) {
+            const int row0 = MOE ? (tile / tpe) * P.job[j].rows + (tile % tpe) * TC_BM
+                                 : (tile - P.job[j].tile0) * TC_BM;
+            uint8_t* st = wring + s * PS_W_BYTES;
+            tc::mbar_expect_tx(bar(FULL_W + s), PS_W_BYTES);
+            tc::tma_load_2d_hint(tc::smem_addr(st), &P.job[j].cmap, k * TC_BK, row0, bar(FULL_W + s), evict_first);
+            tc::tma_load_2d_hint(tc::smem_addr(st + PS_CODES_BYTES), &P.job[j].pmap, k * (TC_BK / 32), row0,
+                                 bar(FULL_W + s), evict_first);
+          }
+          __syncwarp();
+          ++issued;
+          if (++s == WST) { s = 0; ph ^= 1; }
         }
-        if (tc::elect_one()) {
-          const int row0 = (tile - P.job[j].tile0) * TC_BM;
-          uint8_t* st = wring + s * PS_W_BYTES;
-          tc::mbar_expect_tx(bar(FULL_W + s), PS_W_BYTES);
-          tc::tma_load_2d_hint(tc::smem_addr(st), &P.job[j].cmap, k * TC_BK, row0, bar(FULL_W + s), evict_first);
-          tc::tma_load_2d_hint(tc::smem_addr(st + PS_CODES_BYTES), &P.job[j].pmap, k * (TC_BK / 32), row0,
-                               bar(FULL_W + s), evict_first);
-        }
-        __syncwarp();
-        ++issued;
-        if (++s == WST) { s = 0; ph ^= 1; }
         if (++k == F.ks) {
           k = 0;
           ++tile;
@@ -459,23 +487,26 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
       }
       int beg, end;
       range(p, beg, end);
-      int k = beg - (beg / F.ks) * F.ks;
+      int tile = beg / F.ks, k = beg - (beg / F.ks) * F.ks;
       const CUtensorMap* xm = &P.xmap[F.xk];
       for (int it = beg; it < end; ++it) {
-        if (!__all_sync(FULL, W.wait(bar(EMPTY_X + s), ph ^ 1))) {
-          stop = true;
-          break;
+        if (!skipped(tile)) {
+          if (!__all_sync(FULL, W.wait(bar(EMPTY_X + s), ph ^ 1))) {
+            stop = true;
+            break;
+          }
+          if (tc::elect_one()) {
+            const int xrow = MOE ? s_moff[tile / tpe] : 0;   // first input row of the tile's entries
+            uint8_t* st = xring + s * xst_bytes;
+            tc::mbar_expect_tx(bar(FULL_X + s), xbytes);
+            tc::tma_load_2d(tc::smem_addr(st), xm, k * TC_BK, xrow, bar(FULL_X + s));
+            tc::tma_load_2d(tc::smem_addr(st + Bp * 128), xm, k * TC_BK + 64, xrow, bar(FULL_X + s));
+          }
+          __syncwarp();
+          ++issued;
+          if (++s == PS_XST) { s = 0; ph ^= 1; }
         }
-        if (tc::elect_one()) {
-          uint8_t* st = xring + s * xst_bytes;
-          tc::mbar_expect_tx(bar(FULL_X + s), xbytes);
-          tc::tma_load_2d(tc::smem_addr(st), xm, k * TC_BK, 0, bar(FULL_X + s));
-          tc::tma_load_2d(tc::smem_addr(st + Bp * 128), xm, k * TC_BK + 64, 0, bar(FULL_X + s));
-        }
-        __syncwarp();
-        ++issued;
-        if (++s == PS_XST) { s = 0; ph ^= 1; }
-        if (++k == F.ks) k = 0;
+        if (++k == F.ks) { k = 0; ++tile; }
       }
     }
     if (*abort_flag && lane == 0) {
@@ -498,8 +529,12 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
       const PsPhase& F = P.ph[p];
       int beg, end;
       range(p, beg, end);
-      int k = beg - (beg / F.ks) * F.ks;
+      int tile = beg / F.ks, k = beg - (beg / F.ks) * F.ks;
       for (int it = beg; it < end; ++it) {
+        if (skipped(tile)) {
+          if (++k == F.ks) { k = 0; ++tile; }
+          continue;
+        }
         const bool first = (k == 0) || (it == beg);
         const bool last = (k == F.ks - 1) || (it == end - 1);
         if (first && !__all_sync(FULL, W.wait(bar(ACCE + t), pht ^ 1))) { stop = true; break; }
@@ -524,7 +559,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
         if (last && ++t == 2) { t = 0; pht ^= 1; }
         if (++sx == PS_XST) { sx = 0; phx ^= 1; }
         if (++a == PS_NA) { a = 0; pha ^= 1; }
-        if (++k == F.ks) k = 0;
+        if (++k == F.ks) { k = 0; ++tile; }
       }
     }
     if (any) {
@@ -542,9 +577,16 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
     uint32_t ph = 0, pha = 0;
     bool stop = false;
     for (int p = 0; p < P.nph && !stop; ++p) {
+      const int ks = P.ph[p].ks;
       int beg, end;
       range(p, beg, end);
+      int tile = beg / ks, k = beg - (beg / ks) * ks;
       for (int it = beg; it < end; ++it) {
+        if constexpr (MOE) {
+          const bool skip = skipped(tile);
+          if (++k == ks) { k = 0; ++tile; }
+          if (skip) continue;
+        }
         if (!__all_sync(FULL, W.wait(bar(FULL_W + s), ph))) { stop = true; break; }
         if (!__all_sync(FULL, W.wait(bar(AEMPTY + a), pha ^ 1))) { stop = true; break; }
         const uint8_t* st = wring + s * PS_W_BYTES;
@@ -694,10 +736,27 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
         const int tile_end = (tile + 1) * F.ks;
         const int seg_end = end < tile_end ? end : tile_end;
         const bool whole = (it == tile * F.ks) && (seg_end == tile_end);
+        if (skipped(tile)) {
+          it = seg_end;
+          continue;
+        }
         const int j = job_of_tile(P, F, tile);
         const PsJob& J = P.job[j];
         const int rows = J.rows;
-        const int row0 = (tile - J.tile0) * TC_BM;
+        const int row0 = MOE ? (tile % tpe) * TC_BM : (tile - J.tile0) * TC_BM;
+        int nv = nvec;
+        if constexpr (MOE) {
+          // the tile's expert: its entries' input scales and output rows
+          const int e = tile / tpe;
+          epi_bar();   // every thread is done with the previous tile's tables
+          if (et < 64) {
+            const bool live = et < s_mcnt[e];
+            s_xinv[et] = live ? P.mxinv[s_moff[e] + et] : 0.f;
+            s_ent[et] = live ? P.ments[s_moff[e] + et] : 0;
+          }
+          epi_bar();
+          nv = s_mcnt[e] * (TC_BM / 4);
+        }
         const bool ok = W.wait(bar(ACCF + t), pht);
         if (!epi_all(ok)) { stop = true; break; }
         tc::fence_after_sync();
@@ -749,7 +808,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
 #pragma unroll
             for (int k = 0; k < PS_OUT_K; ++k) {
               const int i = et + 128 * k;
-              if (i < nvec)
+              if (i < nv)
                 asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_addr(fix4 + i)), "l"(pc + i)
                              : "memory");
             }
@@ -757,7 +816,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
 #pragma unroll
             for (int k = 0; k < PS_OUT_K; ++k) {
               const int i = et + 128 * k;
-              if (i < nvec) {
+              if (i < nv) {
                 const float4 u = fix4[i];
                 float4 s4 = acc4[i];
                 s4.x += u.x; s4.y += u.y; s4.z += u.z; s4.w += u.w;
@@ -769,9 +828,9 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
         const bool vec_ok = ((rows & 3) == 0) && ((reinterpret_cast<uintptr_t>(J.y) & 15) == 0) &&
                             (J.epi != PGQ_EPI_ADD || (reinterpret_cast<uintptr_t>(J.residual) & 15) == 0);
         const bool stats = vec_ok && j == F.stats_job;
-        out_rows(acc4, nvec, et, J.epi, J.y, J.residual, rows, row0, vec_ok, stats);
+        out_rows(acc4, nv, et, J.epi, J.y, J.residual, rows, row0, vec_ok, stats, MOE ? s_ent : nullptr);
         if (stats)
-          tile_stats(acc4, nvec, et, rows, row0, F.next_gamma,
+          tile_stats(acc4, nv, et, rows, row0, F.next_gamma,
                      P.stats + ((size_t)par * P.maxtiles + (tile - J.tile0)) * 64);
         epi_bar();   // the tile's stores are issued and the shared tile is free
         if (et == 0) release_add(P.done + p);
@@ -858,6 +917,48 @@ __global__ void __launch_bounds__(256) pass_input_kernel(const float* __restrict
   }
 }
 
+// The gathered input of a grouped expert bank: row i = x[ent[i] / xdiv] in binary16
+// with a power-of-two scale (xinv[i] its inverse), one block per row.  Block 0 also
+// clears the launch's counters and status word.
+__global__ void __launch_bounds__(256) moe_input_kernel(const float* __restrict__ x, int K,
+                                                        const int32_t* __restrict__ ent, int nent, int xrows,
+                                                        int xdiv, __half* __restrict__ xh, float* __restrict__ xinv,
+                                                        unsigned* counters, int ncounters, int* status) {
+  __shared__ float red[8];
+  const int i = blockIdx.x;
+  if (i == 0) {
+    for (int c = threadIdx.x; c < ncounters; c += 256) counters[c] = 0u;
+    if (threadIdx.x == 0) *status = PGQ_OK;
+  }
+  const int sr = min(max(ent[i], 0) / xdiv, xrows - 1);   // (entry ids are checked by the grouping)
+  const float* row = x + (size_t)sr * K;
+  float m = 0.f;
+  for (int c = threadIdx.x * 4; c < K; c += 1024) {
+    const float4 v = *reinterpret_cast<const float4*>(row + c);
+    m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  m = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) m = fmaxf(m, red[w]);
+  int e = 0;
+  if (m > 0.f && m <= 3.0e38f) frexpf(m, &e);
+  const int k = max(-120, min(120, 14 - e));
+  const float sc = ldexpf(1.f, k);
+  __half* out = xh + (size_t)i * K;
+  for (int c = threadIdx.x * 4; c < K; c += 1024) {
+    const float4 v = *reinterpret_cast<const float4*>(row + c);
+    const __half2 lo = __floats2half2_rn(v.x * sc, v.y * sc);
+    const __half2 hi = __floats2half2_rn(v.z * sc, v.w * sc);
+    *reinterpret_cast<uint2*>(out + c) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+  }
+  if (threadIdx.x == 0) xinv[i] = ldexpf(1.f, -k);
+}
+
 // ------------------------------------------------------------------ host side
 namespace {
 
@@ -932,6 +1033,18 @@ struct HostPhase {
   const float* next_gamma;
   const float* gamma;        // how this phase's input is made (see PsPhase)
   float* tap;
+  int moe_E;                 // > 0: job 0 is a grouped bank of moe_E experts
+  int xrows;                 // rows of the input buffer when more than the positions (grouped bank)
+};
+
+// A grouped expert bank's routing (see PsParams) and where its gathered input comes from.
+struct MoeSpec {
+  int E, nent;
+  const int32_t* cnt;
+  const int32_t* off;
+  const int32_t* ent;
+  const float* x;            // input row of gathered row i: x[ent[i] / xdiv], of xrows rows
+  int xrows, xdiv;
 };
 
 struct Plan {
@@ -956,9 +1069,16 @@ Plan make_plan(const HostPhase* hp, int nph, int B, const DeviceInfo& dev) {
   p.Bp = (B + 15) / 16 * 16;
   long long tmin = -1;
   size_t xcols[PS_NX] = {0, 0, 0, 0};
-  for (int i = 0; i < nph; ++i) {
+  auto phase_tiles = [](const HostPhase& h) {
+    if (h.moe_E > 0) return h.moe_E * ((h.job[0].rows + TC_BM - 1) / TC_BM);
     int tiles = 0;
-    for (int j = 0; j < hp[i].njobs; ++j) tiles += (hp[i].job[j].rows + TC_BM - 1) / TC_BM;
+    for (int j = 0; j < h.njobs; ++j) tiles += (h.job[j].rows + TC_BM - 1) / TC_BM;
+    return tiles;
+  };
+  size_t xrows = 64;
+  for (int i = 0; i < nph; ++i) {
+    const int tiles = phase_tiles(hp[i]);
+    xrows = std::max(xrows, (size_t)hp[i].xrows);
     const int ks = (hp[i].K + TC_BK - 1) / TC_BK;
     const long long T = (long long)tiles * ks;
     tmin = tmin < 0 ? T : std::min(tmin, T);
@@ -967,8 +1087,7 @@ Plan make_plan(const HostPhase* hp, int nph, int B, const DeviceInfo& dev) {
   }
   p.G = (int)std::max<long long>(1, std::min<long long>(dev.sms, tmin));
   for (int i = 0; i < nph; ++i) {
-    int tiles = 0;
-    for (int j = 0; j < hp[i].njobs; ++j) tiles += (hp[i].job[j].rows + TC_BM - 1) / TC_BM;
+    const int tiles = phase_tiles(hp[i]);
     const int ks = (hp[i].K + TC_BK - 1) / TC_BK;
     const long long per = ((long long)tiles * ks + p.G - 1) / p.G;
     p.maxseg = std::max(p.maxseg, (int)std::min<long long>(tiles, (per + ks - 1) / ks + 1));
@@ -980,9 +1099,9 @@ Plan make_plan(const HostPhase* hp, int nph, int B, const DeviceInfo& dev) {
   p.off_status = o; o += 256;
   for (int k = 0; k < PS_NX; ++k) {
     p.off_xh[k] = o;
-    o = up(o + (size_t)p.Bp * xcols[k] * 2, 1024);
+    o = up(o + std::max((size_t)p.Bp, xrows) * xcols[k] * 2, 1024);
   }
-  p.off_xinv = o; o = up(o + 64 * 4, 256);
+  p.off_xinv = o; o = up(o + xrows * 4, 256);
   p.off_cnt = o; o = up(o + (size_t)p.ncounters * 4, 256);
   p.off_stats = o; o = up(o + 2 * (size_t)p.maxtiles * 64 * 8, 256);
   p.off_part = o; o = up(o + 2 * (size_t)p.G * p.maxseg * p.Bp * TC_BM * 4, 256);
@@ -996,7 +1115,7 @@ std::mutex g_launch_mu;   // guards the parameter block and the tensor-map cache
 // of the phases.  x0 / gamma0 / tap0 make the first phase's input.
 int launch_phases(const HostPhase* hp, int nph, const float* x0, const float* gamma0, float* tap0, float eps, int B,
                   void* ws, size_t ws_bytes, unsigned long long wait_limit_ns, const DeviceInfo& dev,
-                  cudaStream_t st) {
+                  cudaStream_t st, const MoeSpec* moe = nullptr) {
   if (nph < 1 || nph > PS_MAXPH) return set_error(PGQ_EINVAL, "prefill: %d phases", nph);
   const Plan pl = make_plan(hp, nph, B, dev);
   if (pl.wst == 0) return set_error(PGQ_EUNSUPPORTED, "prefill: shared memory too small for B=%d", B);
@@ -1029,9 +1148,10 @@ int launch_phases(const HostPhase* hp, int nph, const float* x0, const float* ga
       if (nj >= PS_MAXJ) return set_error(PGQ_EINVAL, "prefill: more than %d matrices", PS_MAXJ);
       const PrefillJob& J = H.job[j];
       PsJob& D = P.job[nj++];
-      if (!encode_2d(&D.cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, J.codes, H.K, J.rows, (uint64_t)H.K, TC_BK, TC_BM,
+      const uint64_t mrows = (uint64_t)J.rows * (H.moe_E > 0 ? H.moe_E : 1);   // a bank: all experts' rows
+      if (!encode_2d(&D.cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, J.codes, H.K, mrows, (uint64_t)H.K, TC_BK, TC_BM,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
-          !encode_2d(&D.pmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, J.params, H.K / 32, J.rows, (uint64_t)(H.K / 32) * 4,
+          !encode_2d(&D.pmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, J.params, H.K / 32, mrows, (uint64_t)(H.K / 32) * 4,
                      TC_BK / 32, TC_BM, CU_TENSOR_MAP_SWIZZLE_NONE))
         return set_error(PGQ_ECUDA, "prefill: tensor map of phase %d matrix %d could not be encoded", i, j);
       D.y = J.y;
@@ -1039,13 +1159,14 @@ int launch_phases(const HostPhase* hp, int nph, const float* x0, const float* ga
       D.rows = J.rows;
       D.epi = J.epilogue;
       D.tile0 = tb;
-      D.ntiles = (J.rows + TC_BM - 1) / TC_BM;
+      D.ntiles = (J.rows + TC_BM - 1) / TC_BM * (H.moe_E > 0 ? H.moe_E : 1);
       tb += D.ntiles;
     }
     F.ntiles = tb;
     F.T = tb * F.ks;
     if (!mapped[H.xk]) {
-      if (!encode_2d(&P.xmap[H.xk], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, P.xh[H.xk], H.K, pl.Bp, (uint64_t)H.K * 2, 64,
+      const uint64_t xr = moe ? (uint64_t)moe->nent : (uint64_t)pl.Bp;   // a bank: the gathered rows
+      if (!encode_2d(&P.xmap[H.xk], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, P.xh[H.xk], H.K, xr, (uint64_t)H.K * 2, 64,
                      pl.Bp, CU_TENSOR_MAP_SWIZZLE_128B))
         return set_error(PGQ_ECUDA, "prefill: tensor map of input %d could not be encoded", H.xk);
       mapped[H.xk] = true;
@@ -1072,14 +1193,28 @@ int launch_phases(const HostPhase* hp, int nph, const float* x0, const float* ga
 
   cudaError_t e;
   const int K0 = hp[0].K;
-  pass_input_kernel<<<pl.Bp, 256, (size_t)(K0 / TC_BM) * sizeof(float2), st>>>(
-      x0, B, K0, gamma0, eps, tap0, P.xh[hp[0].xk], xinv, cnt, pl.ncounters, P.status);
+  if (moe) {
+    P.moe = 1;
+    P.E = moe->E;
+    P.tpe = (hp[0].job[0].rows + TC_BM - 1) / TC_BM;
+    P.nent = moe->nent;
+    P.mcnt = moe->cnt;
+    P.moff = moe->off;
+    P.ments = moe->ent;
+    P.mxinv = xinv;
+    moe_input_kernel<<<moe->nent, 256, 0, st>>>(moe->x, K0, moe->ent, moe->nent, moe->xrows, moe->xdiv,
+                                                P.xh[hp[0].xk], xinv, cnt, pl.ncounters, P.status);
+  } else {
+    pass_input_kernel<<<pl.Bp, 256, (size_t)(K0 / TC_BM) * sizeof(float2), st>>>(
+        x0, B, K0, gamma0, eps, tap0, P.xh[hp[0].xk], xinv, cnt, pl.ncounters, P.status);
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e);
 
-  const void* fn = reinterpret_cast<const void*>(&prefill_pass_kernel);
+  const void* fn = moe ? reinterpret_cast<const void*>(&prefill_pass_kernel<true>)
+                      : reinterpret_cast<const void*>(&prefill_pass_kernel<false>);
   {
-    static std::map<int, size_t> done;   // per device, guarded by the launch lock
-    size_t& cur = done[dev.device];
+    static std::map<std::pair<const void*, int>, size_t> done;   // guarded by the launch lock
+    size_t& cur = done[{fn, dev.device}];
     if (pl.smem > cur) {
       if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem)) != cudaSuccess)
         return cuda_status(e);
@@ -1169,6 +1304,35 @@ int launch_prefill(const PrefillJob* jobs, int njobs, const float* X, int cols, 
                    unsigned long long wait_limit_ns, const DeviceInfo& dev, cudaStream_t st) {
   const HostPhase h = single_phase(jobs, njobs, cols);
   return launch_phases(&h, 1, X, nullptr, nullptr, 0.f, B, ws, ws_bytes, wait_limit_ns, dev, st);
+}
+
+size_t moe_bank_tc_workspace_bytes(int E, int rows, int cols, int nent, const DeviceInfo& dev) {
+  HostPhase h{};
+  h.job[0].rows = rows;
+  h.njobs = 1;
+  h.K = cols;
+  h.stats_job = -1;
+  h.moe_E = E;
+  h.xrows = nent;
+  return make_plan(&h, 1, 64, dev).total;
+}
+
+int launch_moe_bank_tc(const MoeBankArgs& a, void* ws, size_t ws_bytes, const DeviceInfo& dev, cudaStream_t st) {
+  // the tensor copies need 16-byte row strides of codes and (scale, offset) pairs
+  if (a.cols % 128 != 0 || a.E > PS_MOE_EMAX || a.nentries < 1 || !aligned16(a.codes) || !aligned16(a.params) ||
+      !aligned16(a.x) || !aligned16(a.y) || a.rows % 4 != 0)
+    return PGQ_EUNSUPPORTED;
+  HostPhase h{};
+  h.job[0] = PrefillJob{a.codes, a.params, a.rows, a.y, nullptr, a.epilogue};
+  h.njobs = 1;
+  h.K = a.cols;
+  h.xk = 0;
+  h.stats_job = -1;
+  h.moe_E = a.E;
+  h.xrows = a.nentries;
+  const int xrows = a.xdiv > 1 ? (a.nentries + a.xdiv - 1) / a.xdiv : a.nentries;
+  const MoeSpec m{a.E, a.nentries, a.counts, a.offsets, a.entries, a.x, xrows, a.xdiv};
+  return launch_phases(&h, 1, nullptr, nullptr, nullptr, 0.f, 64, ws, ws_bytes, 0, dev, st, &m);
 }
 
 int launch_prefill_pass(const pgq_q8_layer* layers, int L, float* h, int B, const float* gamma1,
