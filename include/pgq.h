@@ -251,7 +251,8 @@ int pgq_q8_prefill_pass(const pgq_q8_layer* layers, int L, float* h, int B, cons
  * Router projection over a pass (nemotron_prefill.rs `pb_f32_mm`):
  *   logits[b][e] = sum_c R[e][c] * n[b][c]
  * R: device f32 [E][cols]; n: device f32 [B][cols]; logits: device f32 [B][E].
- * cols % 4 == 0, cols <= 3072; 1 <= B; 1 <= E. */
+ * cols % 4 == 0 and 8 * cols * 4 bytes of shared memory (cols <= 7168); R and n
+ * 16-byte aligned; 1 <= B; 1 <= E. */
 int pgq_moe_router(const float* R, int E, int cols, const float* n, int B, float* logits, void* stream);
 
 /* Softmax top-k per position (choice rule of nemotron_prefill.rs `pb_route`; the
@@ -287,7 +288,8 @@ int pgq_moe_experts_q8(const int8_t* codes, const uint16_t* params, int E, int r
 /* Weighted MoE combine fused into add + RMSNorm (nemotron_prefill.rs `pb_add_rms`,
  * add == 2): h[b] += o[b] + sum_s w[b][s] * eo[b*k + s]  (slots in ascending order,
  * o may be NULL); y[b] = gamma * h[b] / sqrt(mean(h[b]^2) + eps).
- * h f32 [B][n] in place; eo f32 [B*k][n]; w f32 [B][k]; y f32 [B][n]; inv_rms [B] or NULL. */
+ * h f32 [B][n] in place; eo f32 [B*k][n]; w f32 [B][k]; y f32 [B][n]; inv_rms [B] or NULL.
+ * n % 4 == 0, n <= 16384; h, o, eo, gamma and y 16-byte aligned. */
 int pgq_moe_combine_rmsnorm(float* h, const float* o, const float* eo, const float* w, int k,
                             const float* gamma, float eps, int B, int n, float* y, float* inv_rms,
                             void* stream);

@@ -414,7 +414,7 @@ int pgq_moe_router(const float* R, int E, int cols, const float* n, int B, float
   REQUIRE(R && n && logits, PGQ_EINVAL, "moe_router: null pointer");
   REQUIRE(E >= 1 && B >= 1 && cols >= 4 && cols % 4 == 0, PGQ_EINVAL, "moe_router: bad shape E=%d B=%d cols=%d", E, B,
           cols);
-  REQUIRE(aligned16(n) && aligned4(R) && aligned4(logits), PGQ_EALIGN, "moe_router: n 16-byte, R/logits 4-byte");
+  REQUIRE(aligned16(n) && aligned16(R) && aligned4(logits), PGQ_EALIGN, "moe_router: n and R 16-byte, logits 4-byte");
   REQUIRE(!overlaps(logits, (size_t)B * E * 4, n, (size_t)B * cols * 4), PGQ_EINVAL, "moe_router: logits overlap n");
   GET_DEVICE(dev);
   return launch_router(R, n, B, E, cols, logits, dev, as_stream(stream));
@@ -457,7 +457,9 @@ int pgq_moe_experts_q8(const int8_t* codes, const uint16_t* params, int E, int r
 int pgq_moe_combine_rmsnorm(float* h, const float* o, const float* eo, const float* w, int k, const float* gamma,
                             float eps, int B, int n, float* y, float* inv_rms, void* stream) {
   REQUIRE(h && eo && w && gamma && y, PGQ_EINVAL, "moe_combine_rmsnorm: null pointer");
-  REQUIRE(B >= 1 && k >= 1 && n >= 1, PGQ_EINVAL, "moe_combine_rmsnorm: bad shape");
+  REQUIRE(B >= 1 && k >= 1 && n >= 4 && n % 4 == 0 && n <= 16384, PGQ_EINVAL, "moe_combine_rmsnorm: bad shape");
+  REQUIRE(aligned16(h) && (!o || aligned16(o)) && aligned16(eo) && aligned16(gamma) && aligned16(y), PGQ_EALIGN,
+          "moe_combine_rmsnorm: h, o, eo, gamma and y must be 16-byte aligned");
   REQUIRE(!overlaps(y, (size_t)B * n * 4, h, (size_t)B * n * 4), PGQ_EINVAL, "moe_combine_rmsnorm: y overlaps h");
   GET_DEVICE(dev);
   return launch_moe_combine(h, o, eo, w, k, gamma, eps, B, n, y, inv_rms, as_stream(stream));

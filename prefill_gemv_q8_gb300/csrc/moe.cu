@@ -19,12 +19,11 @@
 namespace pgq {
 
 // ------------------------------------------------------------------ router
-// logits[b][e] = Σ_c R[e][c]·n[b][c].  Block = 8 warps = 8 experts; the block stages
-// up to 16 positions of n in shared memory, each warp keeps its expert row in
-// registers (cols/32 values per lane) and walks the staged positions.
+// logits[b][e] = Σ_c R[e][c]·n[b][c].  Block = 8 warps = 8 experts over 8 positions
+// staged in shared memory; each lane walks float4 column groups of its expert's row
+// against the staged positions, then a butterfly per position (fixed order).
 constexpr int RT_WARPS = 8;
-constexpr int RT_POS = 16;
-constexpr int RT_MAXV = 96;   // cols <= 32 * 96 = 3072
+constexpr int RT_POS = 8;
 
 __global__ void __launch_bounds__(RT_WARPS * 32)
 router_kernel(const float* __restrict__ R, const float* __restrict__ n, int B, int E, int cols,
@@ -34,21 +33,30 @@ router_kernel(const float* __restrict__ R, const float* __restrict__ n, int B, i
   const int e = blockIdx.x * RT_WARPS + warp;
   const int b0 = blockIdx.y * RT_POS;
   const int nb = min(RT_POS, B - b0);
-  for (int i = threadIdx.x; i < nb * cols; i += blockDim.x) xs[i] = n[(size_t)b0 * cols + i];
+  const int c4n = cols >> 2;
+  const float4* n4 = reinterpret_cast<const float4*>(n + (size_t)b0 * cols);
+  float4* xs4 = reinterpret_cast<float4*>(xs);
+  for (int i = threadIdx.x; i < nb * c4n; i += blockDim.x) xs4[i] = n4[i];
   __syncthreads();
   if (e >= E) return;
-  float w[RT_MAXV];
-  const float* row = R + (size_t)e * cols;
+  const float4* r4 = reinterpret_cast<const float4*>(R + (size_t)e * cols);
+  float acc[RT_POS];
 #pragma unroll
-  for (int i = 0; i < RT_MAXV; ++i) w[i] = (lane + 32 * i < cols) ? row[lane + 32 * i] : 0.f;
-  for (int b = 0; b < nb; ++b) {
-    const float* x = xs + (size_t)b * cols;
-    float acc = 0.f;
+  for (int b = 0; b < RT_POS; ++b) acc[b] = 0.f;
+  for (int c = lane; c < c4n; c += 32) {
+    const float4 w = r4[c];
 #pragma unroll
-    for (int i = 0; i < RT_MAXV; ++i)
-      if (lane + 32 * i < cols) acc = fmaf(w[i], x[lane + 32 * i], acc);
-    acc = warp_sum(acc);
-    if (lane == 0) logits[(size_t)(b0 + b) * E + e] = acc;
+    for (int b = 0; b < RT_POS; ++b) {
+      if (b < nb) {
+        const float4 x = xs4[b * c4n + c];
+        acc[b] = fmaf(w.x, x.x, fmaf(w.y, x.y, fmaf(w.z, x.z, fmaf(w.w, x.w, acc[b]))));
+      }
+    }
+  }
+#pragma unroll
+  for (int b = 0; b < RT_POS; ++b) {
+    const float t = warp_sum(acc[b]);
+    if (lane == 0 && b < nb) logits[(size_t)(b0 + b) * E + e] = t;
   }
 }
 
@@ -359,30 +367,53 @@ moe_bank_kernel(const __grid_constant__ MoeBank P) {
 // For each position b (nemotron_prefill.rs `pb_add_rms`, add = 2):
 //   h[b] += o[b] + Σ_s w[b][s]·eo[b·k+s]   (slots ascending; o may be null)
 //   y[b] = γ·h[b]/√(mean h² + eps)
-__global__ void __launch_bounds__(256)
+constexpr int MC_THREADS = 1024;
+__global__ void __launch_bounds__(MC_THREADS)
 moe_combine_kernel(float* __restrict__ h, const float* __restrict__ o, const float* __restrict__ eo,
                    const float* __restrict__ w, int k, const float* __restrict__ gamma, float eps, int n,
                    float* __restrict__ y, float* __restrict__ inv_out) {
-  __shared__ float red[8];
+  // one block per position; thread i holds float4 groups i, i + 1024, ... of the row
+  // (n <= 4·4·1024) in registers between the sum of squares and the scaling
+  constexpr int MC_V = 4;
+  __shared__ float red[MC_THREADS / 32];
   const int b = blockIdx.x;
-  float* hb = h + (size_t)b * n;
+  const int n4 = n >> 2;
+  float4* hb = reinterpret_cast<float4*>(h + (size_t)b * n);
+  float4 v[MC_V];
   float ss = 0.f;
-  for (int i = threadIdx.x; i < n; i += 256) {
-    float m = o ? o[(size_t)b * n + i] : 0.f;
-    for (int s = 0; s < k; ++s) m += w[(size_t)b * k + s] * eo[((size_t)b * k + s) * n + i];
-    const float v = hb[i] + m;
-    hb[i] = v;
-    ss += v * v;
+#pragma unroll
+  for (int q = 0; q < MC_V; ++q) {
+    const int i = threadIdx.x + q * MC_THREADS;
+    if (i < n4) {
+      float4 m = o ? reinterpret_cast<const float4*>(o + (size_t)b * n)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s = 0; s < k; ++s) {
+        const float ws = w[(size_t)b * k + s];
+        const float4 e4 = reinterpret_cast<const float4*>(eo + ((size_t)b * k + s) * n)[i];
+        m = make_float4(m.x + ws * e4.x, m.y + ws * e4.y, m.z + ws * e4.z, m.w + ws * e4.w);
+      }
+      const float4 hv = hb[i];
+      v[q] = make_float4(hv.x + m.x, hv.y + m.y, hv.z + m.z, hv.w + m.w);
+      hb[i] = v[q];
+      ss += v[q].x * v[q].x + v[q].y * v[q].y + v[q].z * v[q].z + v[q].w * v[q].w;
+    }
   }
   ss = warp_sum(ss);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
   __syncthreads();
   float t = 0.f;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) t += red[i];
+  for (int i = 0; i < MC_THREADS / 32; ++i) t += red[i];
   const float inv = rsqrtf(t / (float)n + eps);
   if (inv_out && threadIdx.x == 0) inv_out[b] = inv;
-  for (int i = threadIdx.x; i < n; i += 256) y[(size_t)b * n + i] = gamma[i] * (hb[i] * inv);
+#pragma unroll
+  for (int q = 0; q < MC_V; ++q) {
+    const int i = threadIdx.x + q * MC_THREADS;
+    if (i < n4) {
+      const float4 g = reinterpret_cast<const float4*>(gamma)[i];
+      reinterpret_cast<float4*>(y + (size_t)b * n)[i] =
+          make_float4(g.x * (v[q].x * inv), g.y * (v[q].y * inv), g.z * (v[q].z * inv), g.w * (v[q].w * inv));
+    }
+  }
 }
 
 // ------------------------------------------------------------------ launchers
@@ -417,7 +448,7 @@ int bank_blocks_per_sm(int device, size_t smem) {
 
 int launch_router(const float* R, const float* n, int B, int E, int cols, float* logits, const DeviceInfo& dev,
                   cudaStream_t st) {
-  if (cols > 32 * RT_MAXV) return set_error(PGQ_EUNSUPPORTED, "router: cols=%d > %d", cols, 32 * RT_MAXV);
+  if (cols % 4 != 0) return set_error(PGQ_EUNSUPPORTED, "router: cols=%d not a multiple of 4", cols);
   const size_t smem = (size_t)RT_POS * cols * sizeof(float);
   if (smem > dev.smem_optin) return set_error(PGQ_EUNSUPPORTED, "router: %zu bytes of shared memory", smem);
   if (cudaError_t e = moe_allow_smem(reinterpret_cast<const void*>(router_kernel), dev.device, smem); e != cudaSuccess)
@@ -473,7 +504,9 @@ int launch_moe_bank(const MoeBankArgs& a, const DeviceInfo& dev, cudaStream_t st
 
 int launch_moe_combine(float* h, const float* o, const float* eo, const float* w, int k, const float* gamma, float eps,
                        int B, int n, float* y, float* inv, cudaStream_t st) {
-  moe_combine_kernel<<<B, 256, 0, st>>>(h, o, eo, w, k, gamma, eps, n, y, inv);
+  if (n % 4 != 0 || n > 4 * 4 * MC_THREADS)
+    return set_error(PGQ_EUNSUPPORTED, "combine: n=%d must be a multiple of 4 and at most %d", n, 16 * MC_THREADS);
+  moe_combine_kernel<<<B, MC_THREADS, 0, st>>>(h, o, eo, w, k, gamma, eps, n, y, inv);
   return cuda_status(cudaGetLastError());
 }
 

@@ -112,6 +112,16 @@ struct PsParams {
 };
 static_assert(sizeof(PsParams) <= 32000, "kernel parameters");
 
+// Optional trace (compiled in only with -DPGQ_TRACE): per block and phase (or, for a
+// grouped bank, per tile of the block), %globaltimer at role milestones.
+#ifdef PGQ_TRACE
+constexpr int PT_EV = 12;
+__device__ unsigned long long g_pt[1024 * PS_MAXPH * PT_EV];
+#define PTRACE(p, ev) (g_pt[((size_t)blockIdx.x * PS_MAXPH + min((p), PS_MAXPH - 1)) * PT_EV + (ev)] = tc::globaltimer())
+#else
+#define PTRACE(p, ev) ((void)0)
+#endif
+
 // ------------------------------------------------------------------ schedule
 __device__ __forceinline__ int item_begin(int c, int G, int T) { return (int)((long long)c * T / G); }
 
@@ -426,7 +436,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
   if (warp == 0) {
     // ------------------------------------------------------------ weight producer
     const uint64_t evict_first = tc::policy_evict_first();
-    int s = 0, issued = 0;
+    int s = 0, issued = 0, wtile = 0;
     uint32_t ph = 0;
     bool stop = false;
     for (int p = 0; p < P.nph && !stop; ++p) {
@@ -442,6 +452,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
             break;
           }
           if (tc::elect_one()) {
+            if (MOE && (k == 0 || it == beg)) PTRACE(wtile, 0);
             const int row0 = MOE ? (tile / tpe) * P.job[j].rows + (tile % tpe) * TC_BM
                                  : (tile - P.job[j].tile0) * TC_BM;
             uint8_t* st = wring + s * PS_W_BYTES;
@@ -453,6 +464,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
           __syncwarp();
           ++issued;
           if (++s == WST) { s = 0; ph ^= 1; }
+          if (k == F.ks - 1 || it == end - 1) ++wtile;
         }
         if (++k == F.ks) {
           k = 0;
@@ -496,11 +508,21 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
             break;
           }
           if (tc::elect_one()) {
-            const int xrow = MOE ? s_moff[tile / tpe] : 0;   // first input row of the tile's entries
             uint8_t* st = xring + s * xst_bytes;
-            tc::mbar_expect_tx(bar(FULL_X + s), xbytes);
-            tc::tma_load_2d(tc::smem_addr(st), xm, k * TC_BK, xrow, bar(FULL_X + s));
-            tc::tma_load_2d(tc::smem_addr(st + Bp * 128), xm, k * TC_BK + 64, xrow, bar(FULL_X + s));
+            if constexpr (MOE) {
+              // the expert's entries only, in boxes of 16 rows (the MMA's N follows)
+              const int e = tile / tpe, xrow = s_moff[e], nbox = (s_mcnt[e] + 15) >> 4;
+              tc::mbar_expect_tx(bar(FULL_X + s), (uint32_t)(nbox * 2 * 16 * 128));
+              for (int i = 0; i < nbox; ++i) {
+                tc::tma_load_2d(tc::smem_addr(st + i * 16 * 128), xm, k * TC_BK, xrow + 16 * i, bar(FULL_X + s));
+                tc::tma_load_2d(tc::smem_addr(st + Bp * 128 + i * 16 * 128), xm, k * TC_BK + 64, xrow + 16 * i,
+                                bar(FULL_X + s));
+              }
+            } else {
+              tc::mbar_expect_tx(bar(FULL_X + s), xbytes);
+              tc::tma_load_2d(tc::smem_addr(st), xm, k * TC_BK, 0, bar(FULL_X + s));
+              tc::tma_load_2d(tc::smem_addr(st + Bp * 128), xm, k * TC_BK + 64, 0, bar(FULL_X + s));
+            }
           }
           __syncwarp();
           ++issued;
@@ -522,7 +544,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
     // ------------------------------------------------------------ MMA issuer
     const uint32_t idesc = tc::idesc_f16_f32(TC_BM, Bp);
     const uint64_t bstep = (uint64_t)((Bp * 128) >> 4);   // second 64-column half of the slice
-    int sx = 0, a = 0, t = 0;
+    int sx = 0, a = 0, t = 0, mtile = 0;
     uint32_t phx = 0, pha = 0, pht = 0;
     bool any = false, stop = false;
     for (int p = 0; p < P.nph && !stop; ++p) {
@@ -544,18 +566,23 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
         const uint32_t d = tmem + t * PS_ACC_COLS;
         const uint64_t b0 = tc::sdesc_sw128(tc::smem_addr(xring + sx * xst_bytes));
         const uint32_t a_t = tmem + 2 * PS_ACC_COLS + a * PS_A_COLS;
+        uint32_t id = idesc;
+        if constexpr (MOE) id = tc::idesc_f16_f32(TC_BM, 16 * ((s_mcnt[tile / tpe] + 15) >> 4));   // N: the entries
         if (tc::elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < TC_BK / 16; ++kk) {
             const uint64_t bdesc = b0 + (uint64_t)((kk & 3) * 2) + (kk >> 2) * bstep;
-            tc::mma_f16_ts(d, a_t + kk * 8, bdesc, idesc, (first && kk == 0) ? 0u : 1u);
+            tc::mma_f16_ts(d, a_t + kk * 8, bdesc, id, (first && kk == 0) ? 0u : 1u);
           }
           tc::mma_commit(bar(EMPTY_X + sx));
           tc::mma_commit(bar(AEMPTY + a));
           if (last) tc::mma_commit(bar(ACCF + t));
+          if (MOE && first) PTRACE(mtile, 4);
+          if (MOE && last) PTRACE(mtile, 5);
         }
         __syncwarp();
         any = true;
+        if (last) ++mtile;
         if (last && ++t == 2) { t = 0; pht ^= 1; }
         if (++sx == PS_XST) { sx = 0; phx ^= 1; }
         if (++a == PS_NA) { a = 0; pha ^= 1; }
@@ -719,7 +746,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
       return true;
     };
 
-    int t = 0;
+    int t = 0, etile = 0;
     uint32_t pht = 0;
     bool stop = false;
     for (int p = 0; p < P.nph && !stop; ++p) {
@@ -756,8 +783,10 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
           }
           epi_bar();
           nv = s_mcnt[e] * (TC_BM / 4);
+          if (et == 0) PTRACE(etile, 6);
         }
         const bool ok = W.wait(bar(ACCF + t), pht);
+        if (MOE && et == 0) PTRACE(etile, 10);
         if (!epi_all(ok)) { stop = true; break; }
         tc::fence_after_sync();
         const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + t * PS_ACC_COLS;
@@ -787,6 +816,8 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
         if (contributor) {
           // the block's stores, then one gpu-scope release and the count on the tile
           if (et == 0) release_add(P.tile_cnt + (size_t)par * P.maxtiles + tile);
+          if (MOE && et == 0) PTRACE(etile, 7);
+          ++etile;
           it = seg_end;
           continue;
         }
@@ -834,6 +865,8 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
                      P.stats + ((size_t)par * P.maxtiles + (tile - J.tile0)) * 64);
         epi_bar();   // the tile's stores are issued and the shared tile is free
         if (et == 0) release_add(P.done + p);
+        if (MOE && et == 0) PTRACE(etile, 7);
+        ++etile;
         it = seg_end;
       }
     }
@@ -914,6 +947,21 @@ __global__ void __launch_bounds__(256) pass_input_kernel(const float* __restrict
     const __half2 hi = __floats2half2_rn(v.z * sc, v.w * sc);
     *reinterpret_cast<uint2*>(out + c) =
         make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+  }
+}
+
+// (scale, offset) rows of a bank whose row of pairs is not a multiple of 16 bytes,
+// copied into rows of `pc` pairs (the tail zero) for the tensor copies; experts
+// without entries are left out.
+__global__ void __launch_bounds__(256) params_pad_kernel(const uint32_t* __restrict__ src, int rows, int c32, int pc,
+                                                         const int32_t* __restrict__ cnt, uint32_t* __restrict__ dst) {
+  // a warp per row, lanes along the row
+  const int e = blockIdx.y;
+  if (cnt[e] <= 0) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int r = blockIdx.x * 8 + warp; r < rows; r += gridDim.x * 8) {
+    const size_t row = (size_t)e * rows + r;
+    for (int c = lane; c < pc; c += 32) dst[row * pc + c] = c < c32 ? src[row * c32 + c] : 0u;
   }
 }
 
@@ -1034,6 +1082,7 @@ struct HostPhase {
   const float* gamma;        // how this phase's input is made (see PsPhase)
   float* tap;
   int moe_E;                 // > 0: job 0 is a grouped bank of moe_E experts
+  int pcols;                 // (scale, offset) pairs per row of the params (0: K / 32)
   int xrows;                 // rows of the input buffer when more than the positions (grouped bank)
 };
 
@@ -1149,10 +1198,11 @@ int launch_phases(const HostPhase* hp, int nph, const float* x0, const float* ga
       const PrefillJob& J = H.job[j];
       PsJob& D = P.job[nj++];
       const uint64_t mrows = (uint64_t)J.rows * (H.moe_E > 0 ? H.moe_E : 1);   // a bank: all experts' rows
+      const uint64_t pc = H.pcols > 0 ? (uint64_t)H.pcols : (uint64_t)(H.K / 32);
       if (!encode_2d(&D.cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, J.codes, H.K, mrows, (uint64_t)H.K, TC_BK, TC_BM,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
-          !encode_2d(&D.pmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, J.params, H.K / 32, mrows, (uint64_t)(H.K / 32) * 4,
-                     TC_BK / 32, TC_BM, CU_TENSOR_MAP_SWIZZLE_NONE))
+          !encode_2d(&D.pmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, J.params, pc, mrows, (uint64_t)pc * 4, TC_BK / 32, TC_BM,
+                     CU_TENSOR_MAP_SWIZZLE_NONE))
         return set_error(PGQ_ECUDA, "prefill: tensor map of phase %d matrix %d could not be encoded", i, j);
       D.y = J.y;
       D.residual = J.residual;
@@ -1167,7 +1217,7 @@ int launch_phases(const HostPhase* hp, int nph, const float* x0, const float* ga
     if (!mapped[H.xk]) {
       const uint64_t xr = moe ? (uint64_t)moe->nent : (uint64_t)pl.Bp;   // a bank: the gathered rows
       if (!encode_2d(&P.xmap[H.xk], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, P.xh[H.xk], H.K, xr, (uint64_t)H.K * 2, 64,
-                     pl.Bp, CU_TENSOR_MAP_SWIZZLE_128B))
+                     moe ? 16u : (uint32_t)pl.Bp, CU_TENSOR_MAP_SWIZZLE_128B))
         return set_error(PGQ_ECUDA, "prefill: tensor map of input %d could not be encoded", H.xk);
       mapped[H.xk] = true;
     }
@@ -1306,6 +1356,9 @@ int launch_prefill(const PrefillJob* jobs, int njobs, const float* X, int cols, 
   return launch_phases(&h, 1, X, nullptr, nullptr, 0.f, B, ws, ws_bytes, wait_limit_ns, dev, st);
 }
 
+// (scale, offset) pairs per row for the tensor copies: a multiple of 4 (16 bytes)
+static int padded_pairs(int cols) { return (cols / 32 + 3) / 4 * 4; }
+
 size_t moe_bank_tc_workspace_bytes(int E, int rows, int cols, int nent, const DeviceInfo& dev) {
   HostPhase h{};
   h.job[0].rows = rows;
@@ -1314,16 +1367,34 @@ size_t moe_bank_tc_workspace_bytes(int E, int rows, int cols, int nent, const De
   h.stats_job = -1;
   h.moe_E = E;
   h.xrows = nent;
-  return make_plan(&h, 1, 64, dev).total;
+  size_t pad = 0;
+  if (padded_pairs(cols) != cols / 32) pad = ((size_t)E * rows * padded_pairs(cols) * 4 + 255) / 256 * 256;
+  return make_plan(&h, 1, 64, dev).total + pad;
 }
 
 int launch_moe_bank_tc(const MoeBankArgs& a, void* ws, size_t ws_bytes, const DeviceInfo& dev, cudaStream_t st) {
-  // the tensor copies need 16-byte row strides of codes and (scale, offset) pairs
-  if (a.cols % 128 != 0 || a.E > PS_MOE_EMAX || a.nentries < 1 || !aligned16(a.codes) || !aligned16(a.params) ||
-      !aligned16(a.x) || !aligned16(a.y) || a.rows % 4 != 0)
+  // the tensor copies need 16-byte row strides of codes (and of the pairs, padded
+  // below when they are not)
+  if (a.cols % 32 != 0 || a.cols % 16 != 0 || a.E > PS_MOE_EMAX || a.nentries < 1 || !aligned16(a.codes) ||
+      !aligned16(a.params) || !aligned16(a.x) || !aligned16(a.y) || a.rows % 4 != 0)
     return PGQ_EUNSUPPORTED;
+  const int pc = padded_pairs(a.cols);
+  const uint16_t* params = a.params;
+  size_t gemm_bytes = ws_bytes;
+  if (pc != a.cols / 32) {
+    // padded pairs at the end of the workspace
+    const size_t pad = ((size_t)a.E * a.rows * pc * 4 + 255) / 256 * 256;
+    if (ws_bytes < pad) return set_error(PGQ_EWORKSPACE, "moe bank: workspace too small");
+    gemm_bytes = (ws_bytes - pad) / 256 * 256;
+    uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + gemm_bytes);
+    params_pad_kernel<<<dim3(64, a.E), 256, 0, st>>>(reinterpret_cast<const uint32_t*>(a.params), a.rows, a.cols / 32,
+                                                    pc, a.counts, dst);
+    if (cudaError_t e = cudaGetLastError(); e != cudaSuccess) return cuda_status(e);
+    params = reinterpret_cast<const uint16_t*>(dst);
+  }
   HostPhase h{};
-  h.job[0] = PrefillJob{a.codes, a.params, a.rows, a.y, nullptr, a.epilogue};
+  h.pcols = pc;
+  h.job[0] = PrefillJob{a.codes, params, a.rows, a.y, nullptr, a.epilogue};
   h.njobs = 1;
   h.K = a.cols;
   h.xk = 0;
@@ -1332,7 +1403,7 @@ int launch_moe_bank_tc(const MoeBankArgs& a, void* ws, size_t ws_bytes, const De
   h.xrows = a.nentries;
   const int xrows = a.xdiv > 1 ? (a.nentries + a.xdiv - 1) / a.xdiv : a.nentries;
   const MoeSpec m{a.E, a.nentries, a.counts, a.offsets, a.entries, a.x, xrows, a.xdiv};
-  return launch_phases(&h, 1, nullptr, nullptr, nullptr, 0.f, 64, ws, ws_bytes, 0, dev, st, &m);
+  return launch_phases(&h, 1, nullptr, nullptr, nullptr, 0.f, 64, ws, gemm_bytes, 0, dev, st, &m);
 }
 
 int launch_prefill_pass(const pgq_q8_layer* layers, int L, float* h, int B, const float* gamma1,
@@ -1351,3 +1422,13 @@ int launch_prefill_pass(const pgq_q8_layer* layers, int L, float* h, int B, cons
 }
 
 }  // namespace pgq
+
+#ifdef PGQ_TRACE
+// Instrumented builds only: copy out the trace.
+extern "C" int pgq_debug_ptrace(unsigned long long* out, size_t n) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+  const size_t all = sizeof(pgq::g_pt) / sizeof(unsigned long long);
+  if (n > all) n = all;
+  return cudaMemcpyFromSymbol(out, pgq::g_pt, n * sizeof(unsigned long long)) == cudaSuccess ? 0 : -1;
+}
+#endif
