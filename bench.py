@@ -139,6 +139,7 @@ class Q8DecodeLayer:
         self.g = synth.gamma(self.H, wl, backend="torch", device="cuda")
         f = lambda n: torch.empty(1, n, dtype=torch.float32, device="cuda")  # noqa: E731
         self.out = dict(q=f(self.H), k=f(self.KV), v=f(self.KV), o=f(self.H), u=f(self.I), down=f(self.H))
+        self.out1 = {k: v[0] for k, v in self.out.items()}
         sizes = {"q": (self.H, self.H), "k": (self.KV, self.H), "v": (self.KV, self.H), "o": (self.H, self.H),
                  "up": (self.I, self.H), "down": (self.H, self.I)}
         self.bytes = {s: r * c_ + r * (c_ // 32) * 4 for s, (r, c_) in sizes.items()}
@@ -159,6 +160,11 @@ class Q8DecodeLayer:
 
     def launch2(self, L):
         self.pgq.gemv_q8(L["down"][0], L["down"][1], self.out["u"], y=self.out["down"])
+
+    def step(self, L):
+        """The layer through its entry point (the down launch streams its weights while
+        the first launch finishes)."""
+        self.pgq.q8_decode_layer(L, self.x[0], self.xo[0], self.g, 1e-6, out=self.out1)
 
     def next_layer(self):
         L = self.layers[self.i % len(self.layers)]
@@ -211,38 +217,37 @@ def _capture(torch, fn):
 
 
 def time_q8_layer(torch, W, steps, warmup):
-    """The layer step (2 launches) as CUDA graphs, one per weight copy, replayed in
-    rotation: returns (total ms over `steps`, mean ms of the dominant launch, mean ms
-    of the down launch), the launch means from their own graphs' replays."""
+    """`steps` consecutive layer steps (2 launches each, through the layer entry point,
+    the weight copies in rotation) as one CUDA graph, replayed once for the timed
+    region after a graph of `warmup` such steps: returns (total ms over `steps`, mean
+    ms of the dominant launch, mean ms of the down launch), the launch means from
+    their own graphs' replays."""
     st = torch.cuda.current_stream()
     n = len(W.layers)
-    g_step = [_capture(torch, lambda L=L: (W.launch1(L), W.launch2(L))) for L in W.layers]
-    g_k1 = [_capture(torch, lambda L=L: W.launch1(L)) for L in W.layers]
-    g_k2 = [_capture(torch, lambda L=L: W.launch2(L)) for L in W.layers]
-    for i in range(warmup):
-        g_step[i % n].replay()
+    g_warm = _capture(torch, lambda: [W.step(W.layers[i % n]) for i in range(warmup)])
+    g_all = _capture(torch, lambda: [W.step(W.layers[i % n]) for i in range(steps)])
+    g_warm.replay()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(st)
-    for i in range(steps):
-        g_step[i % n].replay()
+    g_all.replay()
     b.record(st)
     torch.cuda.synchronize()
     total = a.elapsed_time(b)
 
-    def per_launch(gs):
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-        for i in range(warmup):
-            gs[i % n].replay()
+    def per_launch(fn):
+        """mean ms of one launch in a graph of `steps` of them back to back"""
+        g = _capture(torch, lambda: [fn(W.layers[i % n]) for i in range(steps)])
+        g.replay()
         torch.cuda.synchronize()
-        for i in range(steps):
-            ev[i][0].record(st)
-            gs[i % n].replay()
-            ev[i][1].record(st)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        g.replay()
+        e1.record(st)
         torch.cuda.synchronize()
-        return statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+        return e0.elapsed_time(e1) / steps
 
-    return total, per_launch(g_k1), per_launch(g_k2)
+    return total, per_launch(W.launch1), per_launch(W.launch2)
 
 
 PREFILL_FILES = ["prefill.cu", "tc.cuh", "common.cuh", "kernels.cuh"]
@@ -533,7 +538,7 @@ def main():
         "vs_baseline": None, "dtype": "q8 weights (int8 + f16 scale/offset), f32 arithmetic", "data": "synthetic",
         "config": {"workload": W.name, "weight_bytes_per_step": W.step_bytes, "B": 1,
                    "l2": "weights rotate over 3 copies (538 MB > 129 MB L2)", "launches_per_step": 2,
-                   "timing": "CUDA graph of the step (2 launches) per weight copy, replayed in rotation",
+                   "timing": "one CUDA graph of the K timed steps (2 launches each, weight copies in rotation)",
                    "parallelism": f"replicas x{world}"},
         "frac_of_hbm": round(value / world / pk["hbm"], 4),
         "roofline": {"bound": "hbm", "kernel": "gemv_tma_kernel<q8,B=1> (norm + q,k,v,o,up)",

@@ -153,8 +153,20 @@ static int check_decode_common(const char* name, int rows, int cols, const float
   return PGQ_OK;
 }
 
+namespace {
+int gemv_f16_impl(const uint16_t* W, int rows, int cols, const float* x, int B, const float* gamma, float eps, float* y,
+                  int epilogue, const float* residual, int early_weights, void* stream);
+}  // namespace
+
 int pgq_gemv_f16(const uint16_t* W, int rows, int cols, const float* x, int B, const float* gamma, float eps, float* y,
                  int epilogue, const float* residual, void* stream) {
+  return gemv_f16_impl(W, rows, cols, x, B, gamma, eps, y, epilogue, residual, 0, stream);
+}
+
+namespace {
+// pgq_gemv_f16 with the early-weights flag (GvParams::early_weights)
+int gemv_f16_impl(const uint16_t* W, int rows, int cols, const float* x, int B, const float* gamma, float eps, float* y,
+                  int epilogue, const float* residual, int early_weights, void* stream) {
   REQUIRE(W && y, PGQ_EINVAL, "gemv_f16: W and y must be non-null");
   REQUIRE(aligned16(W), PGQ_EALIGN, "gemv_f16: W must be 16-byte aligned");
   int st = check_decode_common("gemv_f16", rows, cols, x, B, gamma, eps, y, epilogue, residual);
@@ -168,8 +180,10 @@ int pgq_gemv_f16(const uint16_t* W, int rows, int cols, const float* x, int B, c
   P.B = B;
   P.cols = cols;
   P.eps = eps;
+  P.early_weights = early_weights;
   return launch_gemv(P, false, false, dev, as_stream(stream));
 }
+}  // namespace
 
 size_t pgq_argmax_workspace_bytes(int B) {
   DeviceInfo dev;
@@ -229,8 +243,20 @@ int pgq_gemv_q8(const int8_t* codes, const uint16_t* params, int rows, int cols,
   return pgq_gemv_q8_multi(&job, 1, &in, 1, cols, B, eps, stream);
 }
 
+namespace {
+// pgq_gemv_q8_multi with the early-weights flag (GvParams::early_weights)
+int gemv_q8_multi_impl(const pgq_q8_job* jobs, int njobs, const pgq_input* inputs, int ninputs, int cols, int B,
+                       float eps, int early_weights, void* stream);
+}  // namespace
+
 int pgq_gemv_q8_multi(const pgq_q8_job* jobs, int njobs, const pgq_input* inputs, int ninputs, int cols, int B,
                       float eps, void* stream) {
+  return gemv_q8_multi_impl(jobs, njobs, inputs, ninputs, cols, B, eps, 0, stream);
+}
+
+namespace {
+int gemv_q8_multi_impl(const pgq_q8_job* jobs, int njobs, const pgq_input* inputs, int ninputs, int cols, int B,
+                       float eps, int early_weights, void* stream) {
   REQUIRE(jobs && inputs, PGQ_EINVAL, "gemv_q8: jobs and inputs must be non-null");
   REQUIRE(njobs >= 1 && njobs <= PGQ_MULTI_MAX, PGQ_EINVAL, "gemv_q8: njobs=%d outside 1..%d", njobs, PGQ_MULTI_MAX);
   REQUIRE(ninputs >= 1 && ninputs <= MAX_INPUTS, PGQ_EINVAL, "gemv_q8: ninputs=%d outside 1..%d", ninputs,
@@ -264,8 +290,10 @@ int pgq_gemv_q8_multi(const pgq_q8_job* jobs, int njobs, const pgq_input* inputs
   P.B = B;
   P.cols = cols;
   P.eps = eps;
+  P.early_weights = early_weights;
   return launch_gemv(P, true, false, dev, as_stream(stream));
 }
+}  // namespace
 
 // ------------------------------------------------------------------ decode workloads
 int pgq_mlp_f16_decode(const float* h, const uint16_t* W_up, const uint16_t* W_down, int hidden, int inter,
@@ -275,7 +303,8 @@ int pgq_mlp_f16_decode(const float* h, const uint16_t* W_up, const uint16_t* W_d
           PGQ_EINVAL, "mlp_f16_decode: u must not overlap h or y");
   int st = pgq_gemv_f16(W_up, inter, hidden, h, 1, gamma, eps, u, PGQ_EPI_RELU2, nullptr, stream);
   if (st) return st;
-  return pgq_gemv_f16(W_down, hidden, inter, u, 1, nullptr, 0.f, y, PGQ_EPI_ADD, h, stream);
+  // the down launch follows the up launch, which writes no weights (early weight stream)
+  return gemv_f16_impl(W_down, hidden, inter, u, 1, nullptr, 0.f, y, PGQ_EPI_ADD, h, 1, stream);
 }
 
 int pgq_q8_decode_layer(const pgq_q8_layer* L, const float* x, const float* x_o, const float* gamma, float eps,
@@ -292,7 +321,11 @@ int pgq_q8_decode_layer(const pgq_q8_layer* L, const float* x, const float* x_o,
   pgq_input ins[2] = {{x, gamma}, {x_o, nullptr}};
   int st = pgq_gemv_q8_multi(jobs, 5, ins, 2, H, 1, eps, stream);
   if (st) return st;
-  return pgq_gemv_q8(L->down.codes, L->down.params, H, I, u, 1, nullptr, 0.f, down, PGQ_EPI_NONE, nullptr, stream);
+  // the down launch follows the launch above, which writes no weights: its weight
+  // stream may start while that launch finishes
+  pgq_q8_job dj{L->down.codes, L->down.params, H, 0, down, PGQ_EPI_NONE, nullptr};
+  pgq_input din{u, nullptr};
+  return gemv_q8_multi_impl(&dj, 1, &din, 1, I, 1, 0.f, 1, stream);
 }
 
 // ------------------------------------------------------------------ prefill

@@ -4,13 +4,20 @@
 // (full/empty mbarriers per slot), and 16 computing warps only read shared memory.
 //
 // Stage = SR rows x all columns (<= 37 KB).  Warp w takes RPW = 2 rows (group
-// w / QW, QW = 32 / SR warps per group) and an even share of the 512-column chunks;
-// at one position its input values live in registers for the whole kernel.  q8 at
-// one position uses dot-then-scale: the biased byte u = q + 128 is widened by one
-// byte-permute into the f32 2^15 + u, so the dot needs no conversion arithmetic.
-// Per stage the partial dot products are reduced across lanes (butterfly) and
-// across the QW column shares (shared memory, fixed order, after a named barrier of
-// the group), then the group's first warp applies the epilogue and stores.
+// w / QW, QW = 32 / SR warps per group) and an even share of the 512-column chunks.
+// At one position the input values of a warp's columns live in registers for the
+// whole kernel, q8 uses dot-then-scale (the biased byte u = q + 128 is widened by one
+// byte-permute into the f32 2^15 + u, so the dot needs no conversion arithmetic), and
+// the partial dot products of 4 consecutive stages are reduced together: across
+// lanes (one butterfly reduce-scatter) and across the QW column shares (shared
+// memory, fixed order, after a named barrier of the group), then the group's first
+// warp applies the epilogue and stores.  With several positions the inputs stay in
+// shared memory and the reduction runs per stage.
+//
+// The launch is a programmatic dependent of the previous kernel in the stream: it
+// waits for it (griddepcontrol.wait) before touching its inputs or outputs; the
+// weights, which no kernel of this library writes, may stream before that wait where
+// the launcher knows what ran before (the second launch of a decode layer).
 #include <algorithm>
 #include <cstring>
 #include <map>
@@ -22,18 +29,33 @@
 
 namespace pgq {
 
-#ifndef PGQ_DOT_MODE
-#define PGQ_DOT_MODE 4   // q8 at one position: 0 dequantise then dot; dot then scale with codes widened
-                         // 1 by byte-permute into f32 2^23 + u, 3 by byte-permute into binary16 pairs,
-                         // 4 by byte-permute into f32 2^15 + u
-#endif
 
 constexpr int GT_STAGE_MAX = 37 * 1024;   // bytes of one ring stage (codes + params)
 constexpr int GT_NST = 4;                  // ring stages
 constexpr int GT_RED = 2;                  // buffers of per-warp partial sums
+constexpr int GT_GROUP = 4;                // one position: stages per reduction group
+#ifndef PGQ_GT_RAMP
+#define PGQ_GT_RAMP 2
+#endif
+// Stages issued at launch; each further first-fill stage is issued when an earlier one
+// has landed.  All 152 SMs filling the whole ring at once share the bandwidth evenly,
+// so every block's first stage would land only when most of the fill has (several µs).
+constexpr int GT_RAMP = PGQ_GT_RAMP < GT_NST ? PGQ_GT_RAMP : GT_NST;
 
 // Device status word of the TMA decode kernels: PGQ_ETIMEOUT after an expired wait.
 __device__ int g_decode_status;
+
+// Optional trace (compiled in only with -DPGQ_TRACE): per block, the global timer at
+// entry, after the input is staged, at the first stage's arrival, at the last refill,
+// the latest end of a computing warp, and the block's task count.
+#ifdef PGQ_TRACE
+constexpr int GTR_EV = 16;
+__device__ unsigned long long g_gtr[1024 * GTR_EV];
+#define GTR_SLOT ((size_t)(blockIdx.x + (P.early ? 512 : 0)) * GTR_EV)
+#define GTRACE(ev) (g_gtr[GTR_SLOT + (ev)] = tc::globaltimer())
+#else
+#define GTRACE(ev) ((void)0)
+#endif
 
 struct GtParams {
   const uint8_t* w[PGQ_MULTI_MAX];
@@ -42,7 +64,8 @@ struct GtParams {
   const float* residual[PGQ_MULTI_MAX];
   int rows[PGQ_MULTI_MAX], input[PGQ_MULTI_MAX], epi[PGQ_MULTI_MAX], task_begin[PGQ_MULTI_MAX + 1];
   GvInput in[MAX_INPUTS];
-  int njobs, ninputs, B, cols, cols_pad, nchunks;
+  int gslot[MAX_INPUTS];   // one position: plane of the input's gamma in shared memory (-1: none)
+  int njobs, ninputs, ngamma, early, B, cols, cols_pad, nchunks;
   int SR, QW, cpw;
   int code_bytes, stage_bytes;   // per stage: SR rows of codes, then SR rows of params
   int ntasks;
@@ -75,11 +98,14 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
   extern __shared__ __align__(128) uint8_t gsm[];
   const int cols = P.cols, cols_pad = P.cols_pad, cols4 = cols >> 2;
   float* xs = reinterpret_cast<float*>(gsm);                                  // [ninputs][NB][cols_pad]
-  float* red = xs + (size_t)P.ninputs * NB * cols_pad;                        // [GT_RED][SR][NB][QW]
+  float* gs = xs + (size_t)P.ninputs * NB * cols_pad;                         // one position: [ngamma][cols_pad]
+  float* red = gs + (NB == 1 ? (size_t)P.ngamma * cols_pad : 0);  // [GT_RED][SR][NB][QW]; one position: [GT_RED][SR/RPW][GT_GROUP·RPW][QW]
   uint8_t* ring = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(red + GT_RED * P.SR * NB * P.QW) + 127) & ~uintptr_t(127));
+      (reinterpret_cast<uintptr_t>(red + GT_RED * P.SR * (NB > GT_GROUP ? NB : GT_GROUP) * P.QW) + 127) &
+      ~uintptr_t(127));
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)GT_NST * P.stage_bytes);
   uint64_t* empty = full + GT_NST;
+  uint64_t* inbar = empty + GT_NST;   // one position: the inputs' bulk copies
   __shared__ float s_inv[MAX_INPUTS * NB];
   __shared__ float s_red[W + 1];
   __shared__ int s_abort;
@@ -102,30 +128,159 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
       tc::bulk_load(tc::smem_addr(dst + P.code_bytes), P.p[j] + (size_t)row0 * (cols >> 5) * 4, pb, bar, policy);
   };
   // job of task t, found by walking forward from job j (tasks are visited in order)
-  auto job_of = [&](int t, int j) {
-    while (j + 1 < P.njobs && t >= P.task_begin[j + 1]) ++j;
+  // job of task t (j: a job at or before it, unused): the job boundaries are loaded
+  // together and counted, not walked one dependent load at a time
+  auto job_of = [&](int t, int) {
+    int j = 0;
+#pragma unroll
+    for (int i = 1; i < PGQ_MULTI_MAX; ++i) j += (i < P.njobs && t >= P.task_begin[i]) ? 1 : 0;
     return j;
   };
 
   const bool producer = warp == W;
   if (tid == 0) {
+    GTRACE(0);
+#ifdef PGQ_TRACE
+    g_gtr[GTR_SLOT + 7] = (unsigned long long)(t1 - t0);
+    g_gtr[GTR_SLOT + 5] = 0ull;
+#endif
     for (int s = 0; s < GT_NST; ++s) {
       tc::mbar_init(tc::smem_addr(full + s), 1);
       tc::mbar_init(tc::smem_addr(empty + s), W);
     }
+    tc::mbar_init(tc::smem_addr(inbar), 1);
     s_abort = 0;
     tc::fence_barrier_init();
   }
   __syncthreads();
-  // the weights do not depend on the input: start streaming before staging it
-  if (producer && lane == 0) {
-    int j = job_of(t0, 0);
-    for (int i = 0; i < GT_NST && t0 + i < t1; ++i) {
-      j = job_of(t0 + i, j);
-      issue(t0 + i, j, i);
+  // A launch that follows this one in the stream as a programmatic dependent may take
+  // the SMs this grid frees from here on; it reads nothing this grid writes before
+  // its own griddepcontrol.wait.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  // bounded wait on an mbarrier phase; false after an expired wait (or another
+  // role's), which then also marks the block aborted
+  auto wait_bar = [&](uint32_t bar, uint32_t parity) -> bool {
+    if (tc::mbar_try(bar, parity)) return true;
+    const uint64_t w0 = tc::globaltimer();
+    while (!tc::mbar_try_sleep(bar, parity, 20000u)) {
+      if (*(volatile int*)&s_abort) return false;
+      if (tc::globaltimer() - w0 > P.wait_limit_ns) {
+        *(volatile int*)&s_abort = 1;
+        atomicExch(&g_decode_status, PGQ_ETIMEOUT);
+        return false;
+      }
     }
+    return true;
+  };
+
+  // inputs read by this block's jobs (one bit per input)
+  unsigned used_in = 0u;
+  if (t0 < t1) {
+    const int j0 = job_of(t0, 0), j1 = job_of(t1 - 1, 0);
+#pragma unroll
+    for (int i = 0; i < PGQ_MULTI_MAX; ++i)
+      if (i >= j0 && i <= j1) used_in |= 1u << P.input[i];
   }
 
+  // The weights never depend on earlier kernels' results: where the launcher allows
+  // it they stream before the wait for the previous kernel, else right after it.  At
+  // one position the inputs (and gammas) come by bulk copies issued ahead of the
+  // weights, so that they do not queue behind the ring's first fill.
+  // (the inputs by warp 0, the weights by the producer warp: two threads issue at once)
+  if (producer && lane == 0) {
+    auto issue_ring = [&]() {
+      for (int i = 0; i < GT_RAMP && t0 + i < t1; ++i) issue(t0 + i, job_of(t0 + i, 0), i);
+    };
+    if (P.early) issue_ring();
+#ifdef PGQ_TRACE
+    GTRACE(11);
+#endif
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (!P.early) issue_ring();
+#ifdef PGQ_TRACE
+    GTRACE(3);
+#endif
+  }
+  if (tid == 0) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if constexpr (NB == 1) {
+      const uint32_t bar = tc::smem_addr(inbar);
+      const uint32_t xb = (uint32_t)cols * 4u;
+      uint32_t bytes = 0;
+      for (int i = 0; i < P.ninputs; ++i)
+        if (used_in >> i & 1) bytes += P.in[i].gamma ? 2u * xb : xb;
+      tc::mbar_expect_tx(bar, bytes);
+      const uint64_t keep = tc::policy_evict_last();
+      for (int i = 0; i < P.ninputs; ++i) {
+        if (!(used_in >> i & 1)) continue;
+        tc::bulk_load(tc::smem_addr(xs + (size_t)i * cols_pad), P.in[i].x, xb, bar, keep);
+        if (P.in[i].gamma)
+          tc::bulk_load(tc::smem_addr(gs + (size_t)P.gslot[i] * cols_pad), P.in[i].gamma, xb, bar, keep);
+      }
+    }
+  }
+#ifdef PGQ_TRACE
+  if (warp == 1 && lane == 0 && t0 < t1 && P.early) {   // when an early first weight stage lands
+    const uint64_t w0 = tc::globaltimer();
+    while (!tc::mbar_try_sleep(tc::smem_addr(full), 0u, 20000u) && tc::globaltimer() - w0 < P.wait_limit_ns) {
+    }
+    GTRACE(9);
+  }
+#endif
+  // ---- a computing warp's rows and column share (worked out while the inputs are
+  // on their way; the producer warp's values are not used)
+  const int QW = P.QW;
+  const int rg = warp / QW, q = warp - rg * QW;
+  // chunks split as evenly as possible, the larger shares first (warps q, q + 4, ...
+  // share an SM sub-partition, so each sub-partition gets an even load)
+  const int ch_base = P.nchunks / QW, ch_extra = P.nchunks - ch_base * QW;
+  const int ch_begin = q * ch_base + min(q, ch_extra);
+  const int ch_end = ch_begin + ch_base + (q < ch_extra ? 1 : 0);
+  const int row_a = RPW * rg;
+  // fixed shared-memory offsets of this lane's codes and (scale, offset) words
+  int off_c[RPW][MAXC], off_p[RPW][MAXC];
+  bool lane_ok[MAXC];
+#pragma unroll
+  for (int u = 0; u < MAXC; ++u) {
+    const int ch = min(ch_begin + u, P.nchunks - 1);
+    const int col = min(ch * CW + lane * EPL, cols - EPL);
+    lane_ok[u] = (ch_begin + u < ch_end) && (ch_begin + u) * CW + lane * EPL < cols;
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) {
+      off_c[r][u] = ((row_a + r) * cols + col) * ESZ;
+      off_p[r][u] = P.code_bytes + ((row_a + r) * (cols >> 5) + (col >> 5)) * 4;
+    }
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+#ifdef PGQ_TRACE
+  if (tid == 0) GTRACE(8);
+#endif
+
+  if constexpr (NB == 1) {
+    // ---- one position: the inputs arrive in natural order; only the RMS factors are
+    // computed here (each warp scales its own register copy when it loads it)
+    const bool in_ok = wait_bar(tc::smem_addr(inbar), 0u);
+    for (int i = 0; i < P.ninputs; ++i) {
+      if (!P.in[i].gamma || !(used_in >> i & 1)) continue;
+      const float4* x4 = reinterpret_cast<const float4*>(xs + (size_t)i * cols_pad);
+      float ss = 0.f;
+      if (in_ok)
+        for (int c = tid; c < cols4; c += THREADS) {
+          const float4 v = x4[c];
+          ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        }
+      ss = warp_sum(ss);
+      __syncthreads();
+      if (lane == 0) s_red[warp] = ss;
+      __syncthreads();
+      if (tid == 0) {
+        float t = 0.f;
+        for (int w = 0; w <= W; ++w) t += s_red[w];
+        s_inv[i] = rsqrtf(t / (float)cols + P.eps);
+      }
+    }
+  } else {
   // ---- stage the inputs (RMS-normalised where gamma is given)
   for (int i = 0; i < P.ninputs; ++i) {
     const float4* x4 = reinterpret_cast<const float4*>(P.in[i].x);
@@ -163,23 +318,9 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
       *reinterpret_cast<float4*>(xs + (size_t)(i * NB + b) * cols_pad + gt_perm<EPL>(c4 * 4)) = v;
     }
   }
+  }
   __syncthreads();
-
-  // bounded wait on an mbarrier phase; false after an expired wait (or another
-  // role's), which then also marks the block aborted
-  auto wait_bar = [&](uint32_t bar, uint32_t parity) -> bool {
-    if (tc::mbar_try(bar, parity)) return true;
-    const uint64_t w0 = tc::globaltimer();
-    while (!tc::mbar_try_sleep(bar, parity, 20000u)) {
-      if (*(volatile int*)&s_abort) return false;
-      if (tc::globaltimer() - w0 > P.wait_limit_ns) {
-        *(volatile int*)&s_abort = 1;
-        atomicExch(&g_decode_status, PGQ_ETIMEOUT);
-        return false;
-      }
-    }
-    return true;
-  };
+  if (tid == 0) GTRACE(1);
 
   float best_v = ARGMAX_FLOOR;   // argmax: lane RPW·b of a group's first warp keeps position b's best
   int best_i = 0;
@@ -187,6 +328,12 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
     // ---- refill each ring slot once all computing warps have released it
     if (lane == 0) {
       int j = job_of(t0, 0);
+      // the rest of the first fill, one stage per landed stage
+      for (int i = GT_RAMP; i < GT_NST && t0 + i < t1; ++i) {
+        if (!wait_bar(tc::smem_addr(full + (i - GT_RAMP)), 0u)) break;
+        j = job_of(t0 + i, j);
+        issue(t0 + i, j, i);
+      }
       int s = 0;
       uint32_t parity = 0;
       for (int t = t0 + GT_NST; t < t1; ++t) {
@@ -195,91 +342,75 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
         issue(t, j, s);
         if (++s == GT_NST) { s = 0; parity ^= 1u; }
       }
+      GTRACE(4);
     }
-  } else {
-  // ---- this warp's rows and column share
-  const int QW = P.QW;
-  const int rg = warp / QW, q = warp - rg * QW;
-  // chunks split as evenly as possible, the larger shares first (warps q, q + 4, ...
-  // share an SM sub-partition, so each sub-partition gets an even load)
-  const int ch_base = P.nchunks / QW, ch_extra = P.nchunks - ch_base * QW;
-  const int ch_begin = q * ch_base + min(q, ch_extra);
-  const int ch_end = ch_begin + ch_base + (q < ch_extra ? 1 : 0);
-  const int row_a = RPW * rg;
-  // fixed shared-memory offsets of this lane's codes and (scale, offset) words
-  int off_c[RPW][MAXC], off_p[RPW][MAXC];
-  bool lane_ok[MAXC];
+  } else if constexpr (NB == 1) {
+    // ---- one position.  Per group of GT_GROUP stages each lane keeps its partial
+    // sums of the group's RPW·GT_GROUP rows; the lane reduction (one reduce-scatter),
+    // the meeting of the row group's QW warps and the epilogue run once per group.
+    constexpr int GS = GT_GROUP, NV = GS * RPW;
+    static_assert(NV <= 32 && (NV & (NV - 1)) == 0, "partials per group: a power of two <= 32");
+    float2 xr[MAXC][EPL / 2];   // this lane's input values, per chunk
+    float xsum[MAXC];           // and their sum, per chunk
+    int job_end = 0, input_j = -1;
+    int buf = 0, s = 0;
+    uint32_t parity = 0;
+    const int ngrp = P.SR / RPW;
+    // this lane's EPL consecutive columns of each of its chunks (natural order),
+    // RMS-normalised where the input has a gamma; lanes 32/EPL apart would hit the
+    // same banks with the same 16-byte word, so each lane starts at word
+    // (lane / (32/EPL)) of its EPL/4 and the words are put back in order
+    auto load_x = [&](int input) {
+      const float* xin = xs + (size_t)input * cols_pad + lane * EPL;
+      const int gsl = P.gslot[input];
+      const float* gin = gsl >= 0 ? gs + (size_t)gsl * cols_pad + lane * EPL : nullptr;
+      const float inv = s_inv[input];
+      constexpr int NK = EPL / 4;
+      const int rot = (lane / (32 / EPL)) % NK;
 #pragma unroll
-  for (int u = 0; u < MAXC; ++u) {
-    const int ch = min(ch_begin + u, P.nchunks - 1);
-    const int col = min(ch * CW + lane * EPL, cols - EPL);
-    lane_ok[u] = (ch_begin + u < ch_end) && (ch_begin + u) * CW + lane * EPL < cols;
+      for (int u = 0; u < MAXC; ++u) {
+        float4 v[NK];
 #pragma unroll
-    for (int r = 0; r < RPW; ++r) {
-      off_c[r][u] = ((row_a + r) * cols + col) * ESZ;
-      off_p[r][u] = P.code_bytes + ((row_a + r) * (cols >> 5) + (col >> 5)) * 4;
-    }
-  }
-  float2 xr[NB == 1 ? MAXC : 1][EPL / 2];
-  float xsum[NB == 1 ? MAXC : 1];   // Σ of this lane's input values per chunk
-
-  // per-job values, reloaded when the task walk enters the next job
-  int j = -1, job_end = 0, job_first = 0, rows_j = 0, input_j = -1, epi_j = 0;
-  float* y_j = nullptr;
-  const float* res_j = nullptr;
-  int buf = 0, s = 0;
-  uint32_t parity = 0;
-
-  for (int t = t0; t < t1; ++t) {
-    if (t >= job_end) {
-      j = job_of(t, j < 0 ? 0 : j);
-      job_first = P.task_begin[j];
-      job_end = P.task_begin[j + 1];
-      rows_j = P.rows[j];
-      epi_j = P.epi[j];
-      y_j = P.y[j];
-      res_j = P.residual[j];
-      const int input = P.input[j];
-      if constexpr (NB == 1) {
-        if (input != input_j) {
-          const float* xin = xs + (size_t)input * cols_pad + lane * 4;
-#pragma unroll
-          for (int u = 0; u < MAXC; ++u) {
-#pragma unroll
-            for (int k = 0; k < EPL / 4; ++k) {
-              float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-              if (ch_begin + u < ch_end) a = *reinterpret_cast<const float4*>(xin + (size_t)(ch_begin + u) * CW + k * 128);
-              xr[u][2 * k] = make_float2(a.x, a.y);
-              xr[u][2 * k + 1] = make_float2(a.z, a.w);
+        for (int kk = 0; kk < NK; ++kk) {
+          const int k = (kk + rot) % NK;
+          float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (ch_begin + u < ch_end) {
+            const size_t o = (size_t)(ch_begin + u) * CW + k * 4;
+            a = *reinterpret_cast<const float4*>(xin + o);
+            if (gin) {
+              const float4 g = *reinterpret_cast<const float4*>(gin + o);
+              a = make_float4(g.x * (a.x * inv), g.y * (a.y * inv), g.z * (a.z * inv), g.w * (a.w * inv));
             }
-            float2 sum2 = xr[u][0];
-#pragma unroll
-            for (int k = 1; k < EPL / 2; ++k) sum2 = fadd2(sum2, xr[u][k]);
-            xsum[u] = sum2.x + sum2.y;
           }
+          v[kk] = a;
         }
+#pragma unroll
+        for (int k = 0; k < NK; ++k) {
+          float4 a = v[0];
+#pragma unroll
+          for (int kk = 1; kk < NK; ++kk)
+            if ((kk + rot) % NK == k) a = v[kk];
+          xr[u][2 * k] = make_float2(a.x, a.y);
+          xr[u][2 * k + 1] = make_float2(a.z, a.w);
+        }
+        float2 sum2 = xr[u][0];
+#pragma unroll
+        for (int k = 1; k < EPL / 2; ++k) sum2 = fadd2(sum2, xr[u][k]);
+        xsum[u] = sum2.x + sum2.y;
       }
-      input_j = input;
-    }
-    const int row0 = (t - job_first) * P.SR;
-    const int nr = min(P.SR, rows_j - row0);
-    // warp-uniform: every lane of the warp leaves the same way
-    const bool ok = __all_sync(0xffffffffu, wait_bar(tc::smem_addr(full + s), parity));
-    float2 acc[RPW][NB][NA];
+    };
+    // this lane's share of the RPW rows of one stage, added into out[0..RPW)
+    auto dot_stage = [&](const uint8_t* st, float* out) {
+      float2 acc[RPW][NA];
 #pragma unroll
-    for (int r = 0; r < RPW; ++r)
+      for (int r = 0; r < RPW; ++r)
 #pragma unroll
-      for (int b = 0; b < NB; ++b)
-#pragma unroll
-        for (int a = 0; a < NA; ++a) acc[r][b][a] = make_float2(0.f, 0.f);
-    if (ok) {
-      const float* xin = xs + (size_t)input_j * NB * cols_pad + lane * 4;
-      const uint8_t* st = ring + (size_t)s * P.stage_bytes;
-#if PGQ_DOT_MODE != 0
-      if constexpr (Q8 && NB == 1) {
-        // dot then scale: Σ u·x with the biased byte u = q + 128 in [0, 255], then
-        // y += scale·dot + (offset − 128·scale)·Σx.  Every shared-memory read of the
-        // stage is issued first (fixed per-warp offsets), then the arithmetic.
+        for (int a = 0; a < NA; ++a) acc[r][a] = make_float2(0.f, 0.f);
+      if constexpr (Q8) {
+        // dot then scale: Σ u·x with the biased byte u = q + 128 in [0, 255], widened by
+        // one byte-permute into the f32 2^15 + u (exponent 15, u in mantissa bits
+        // 8..15); then y += scale·(dot − 2^15·Σx) + (offset − 128·scale)·Σx.  Every
+        // shared-memory read of the stage is issued first, then the arithmetic.
         uint4 cw[RPW][MAXC];
         uint32_t pw[RPW][MAXC];
 #pragma unroll
@@ -300,96 +431,199 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
               float2 d0 = make_float2(0.f, 0.f), d1 = make_float2(0.f, 0.f);
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
-                float2 lo, hi;
-#if PGQ_DOT_MODE == 3
-                // one byte-permute makes two binary16 values 1024 + u (exact), widened
-                // to f32; the 1024 joins the 128 of the bias below
-                lo = h2_to_f2(__byte_perm(words[k], 0x64646464u, 0x4140));
-                hi = h2_to_f2(__byte_perm(words[k], 0x64646464u, 0x4342));
-#elif PGQ_DOT_MODE == 4
-                // one byte-permute makes the f32 2^15 + u exactly (u in mantissa bits
-                // 8..15, exponent 15); the 2^15·Σx it adds is taken out per chunk below
-                lo = make_float2(__uint_as_float(__byte_perm(words[k], 0x47000000u, 0x7504)),
-                                 __uint_as_float(__byte_perm(words[k], 0x47000000u, 0x7514)));
-                hi = make_float2(__uint_as_float(__byte_perm(words[k], 0x47000000u, 0x7524)),
-                                 __uint_as_float(__byte_perm(words[k], 0x47000000u, 0x7534)));
-#else
-                const float2 m23 = make_float2(-8388608.0f, -8388608.0f);
-                lo = fadd2(make_float2(__uint_as_float(__byte_perm(words[k], 0x4B000000u, 0x7540)),
-                                       __uint_as_float(__byte_perm(words[k], 0x4B000000u, 0x7541))), m23);
-                hi = fadd2(make_float2(__uint_as_float(__byte_perm(words[k], 0x4B000000u, 0x7542)),
-                                       __uint_as_float(__byte_perm(words[k], 0x4B000000u, 0x7543))), m23);
-#endif
+                const float2 lo = make_float2(__uint_as_float(__byte_perm(words[k], 0x47000000u, 0x7504)),
+                                              __uint_as_float(__byte_perm(words[k], 0x47000000u, 0x7514)));
+                const float2 hi = make_float2(__uint_as_float(__byte_perm(words[k], 0x47000000u, 0x7524)),
+                                              __uint_as_float(__byte_perm(words[k], 0x47000000u, 0x7534)));
                 d0 = ffma2(lo, xr[u][2 * k], d0);
                 d1 = ffma2(hi, xr[u][2 * k + 1], d1);
               }
               const float2 d = fadd2(d0, d1);
-#if PGQ_DOT_MODE == 3
-              const float c = fmaf(-1152.f, so.x, so.y);
-#else
               const float c = fmaf(-128.f, so.x, so.y);
-#endif
-              float2 a = acc[r][0][0];
-#if PGQ_DOT_MODE == 4
+              float2 a = acc[r][0];
               a.x = fmaf(so.x, fmaf(-32768.f, xsum[u], d.x + d.y), a.x);
-#else
-              a.x = fmaf(so.x, d.x + d.y, a.x);
-#endif
               a.y = fmaf(c, xsum[u], a.y);
-              acc[r][0][0] = a;
+              acc[r][0] = a;
             }
           }
         }
-      } else
-#endif
-      {
+      } else {
 #pragma unroll
         for (int u = 0; u < MAXC; ++u) {
-          const int ch = ch_begin + u;
-          if (ch < ch_end && ch * CW + lane * EPL < cols) {
-            float2 wv[RPW][EPL / 2];
+          if (lane_ok[u]) {
 #pragma unroll
             for (int r = 0; r < RPW; ++r) {
               const uint4 cw = *reinterpret_cast<const uint4*>(st + off_c[r][u]);
-              if constexpr (Q8) {
-                const uint32_t pw = *reinterpret_cast<const uint32_t*>(st + off_p[r][u]);
-                const float2 so = h2_to_f2(pw);
-                const float2 s2 = make_float2(so.x, so.x), o2 = make_float2(so.y, so.y);
-                const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+              const float2 wv[4] = {h2_to_f2(cw.x), h2_to_f2(cw.y), h2_to_f2(cw.z), h2_to_f2(cw.w)};
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  float2 lo, hi;
-                  s8x4_to_f32(words[k], lo, hi);
-                  wv[r][2 * k] = ffma2(lo, s2, o2);
-                  wv[r][2 * k + 1] = ffma2(hi, s2, o2);
-                }
-              } else {
-                wv[r][0] = h2_to_f2(cw.x); wv[r][1] = h2_to_f2(cw.y);
-                wv[r][2] = h2_to_f2(cw.z); wv[r][3] = h2_to_f2(cw.w);
-              }
+              for (int k = 0; k < EPL / 2; ++k) acc[r][k % NA] = ffma2(wv[k], xr[u][k], acc[r][k % NA]);
             }
-            if constexpr (NB == 1) {
+          }
+        }
+      }
 #pragma unroll
-              for (int r = 0; r < RPW; ++r)
+      for (int r = 0; r < RPW; ++r) {
+        float2 a = acc[r][0];
 #pragma unroll
-                for (int k = 0; k < EPL / 2; ++k) acc[r][0][k % NA] = ffma2(wv[r][k], xr[u][k], acc[r][0][k % NA]);
+        for (int k = 1; k < NA; ++k) a = fadd2(a, acc[r][k]);
+        out[r] = a.x + a.y;
+      }
+    };
+
+    for (int g0 = t0; g0 < t1; g0 += GS) {
+      float part[NV];
+#pragma unroll
+      for (int i = 0; i < NV; ++i) part[i] = 0.f;
+      bool ok = true;
+#pragma unroll
+      for (int gs = 0; gs < GS; ++gs) {
+        const int t = g0 + gs;
+        if (t < t1 && ok) {
+          if (t >= job_end) {
+            const int jn = job_of(t, 0);
+            job_end = P.task_begin[jn + 1];
+            const int input = P.input[jn];
+            if (input != input_j) load_x(input);
+            input_j = input;
+          }
+#ifdef PGQ_TRACE
+          if (warp == 0 && lane == 0 && t == t0) GTRACE(10);
+#endif
+          // warp-uniform: every lane of the warp leaves the same way
+          ok = __all_sync(0xffffffffu, wait_bar(tc::smem_addr(full + s), parity));
+#ifdef PGQ_TRACE
+          if (warp == 0 && lane == 0 && t == t0) GTRACE(2);
+#endif
+          if (ok) dot_stage(ring + (size_t)s * P.stage_bytes, part + gs * RPW);
+          // the warp's reads of the stage are done: release the slot to the producer
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(tc::smem_addr(empty + s));
+          if (++s == GT_NST) { s = 0; parity ^= 1u; }
+        }
+      }
+      // lane reduction of the group's NV partials; then the QW warps of the row group
+      // meet (named barrier; all leave together if one wait expired) and its first
+      // warp adds the partial sums in fixed order, applies the epilogue and stores
+      const float tot = reduce_scatter<NV>(part, lane);
+      if ((lane & (32 / NV - 1)) == 0) red[((size_t)(buf * ngrp + rg) * NV + lane / (32 / NV)) * QW + q] = tot;
+      {
+        uint32_t all;
+        asm volatile(
+            "{\n\t.reg .pred p, r;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+            "bar.red.and.pred r, %2, %3, p;\n\tselp.u32 %0, 1, 0, r;\n\t}"
+            : "=r"(all)
+            : "r"((uint32_t)ok), "r"(1 + rg), "r"(QW * 32)
+            : "memory");
+        if (!all) break;
+      }
+      if (q == 0 && lane < NV) {
+        const int gi = lane / RPW, r = lane - gi * RPW;
+        const int t = g0 + gi;
+        if (t < t1) {
+          const int jj = job_of(t, 0);
+          const int row = (t - P.task_begin[jj]) * P.SR + row_a + r;
+          const int rows = P.rows[jj];
+          if (row < rows) {
+            const float* rr = red + ((size_t)(buf * ngrp + rg) * NV + lane) * QW;
+            float out = 0.f;
+            for (int k = 0; k < QW; ++k) out += rr[k];
+            const int epi = P.epi[jj];
+            if (epi == PGQ_EPI_RELU2) {
+              out = fmaxf(out, 0.f);
+              out = out * out;
+            } else if (epi == PGQ_EPI_ADD) {
+              out += P.residual[jj][row];
+            }
+            if (float* y = P.y[jj]) y[row] = out;
+            if constexpr (ARGMAX) argmax_merge(best_v, best_i, out, row);
+          }
+        }
+      }
+      buf ^= 1;
+    }
+    if constexpr (ARGMAX) {
+      // lane 0 takes the warp's best (the merge keeps the lowest row among equals)
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, best_v, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, best_i, o);
+        argmax_merge(best_v, best_i, ov, oi);
+      }
+    }
+#ifdef PGQ_TRACE
+    if (lane == 0) atomicMax(&g_gtr[GTR_SLOT + 5], tc::globaltimer());
+#endif
+  } else {
+  // ---- several positions: the inputs stay in shared memory (permuted so that a
+  // lane's float4 reads are conflict-free), reduced once per stage
+  int j = -1, job_end = 0, job_first = 0, rows_j = 0, input_j = -1, epi_j = 0;
+  float* y_j = nullptr;
+  const float* res_j = nullptr;
+  int buf = 0, s = 0;
+  uint32_t parity = 0;
+
+  for (int t = t0; t < t1; ++t) {
+    if (t >= job_end) {
+      j = job_of(t, 0);
+      job_first = P.task_begin[j];
+      job_end = P.task_begin[j + 1];
+      rows_j = P.rows[j];
+      epi_j = P.epi[j];
+      y_j = P.y[j];
+      res_j = P.residual[j];
+      input_j = P.input[j];
+    }
+    const int row0 = (t - job_first) * P.SR;
+    const int nr = min(P.SR, rows_j - row0);
+    // warp-uniform: every lane of the warp leaves the same way
+    const bool ok = __all_sync(0xffffffffu, wait_bar(tc::smem_addr(full + s), parity));
+    float2 acc[RPW][NB];
+#pragma unroll
+    for (int r = 0; r < RPW; ++r)
+#pragma unroll
+      for (int b = 0; b < NB; ++b) acc[r][b] = make_float2(0.f, 0.f);
+    if (ok) {
+      const float* xin = xs + (size_t)input_j * NB * cols_pad + lane * 4;
+      const uint8_t* st = ring + (size_t)s * P.stage_bytes;
+#pragma unroll
+      for (int u = 0; u < MAXC; ++u) {
+        const int ch = ch_begin + u;
+        if (ch < ch_end && ch * CW + lane * EPL < cols) {
+          float2 wv[RPW][EPL / 2];
+#pragma unroll
+          for (int r = 0; r < RPW; ++r) {
+            const uint4 cw = *reinterpret_cast<const uint4*>(st + off_c[r][u]);
+            if constexpr (Q8) {
+              const uint32_t pw = *reinterpret_cast<const uint32_t*>(st + off_p[r][u]);
+              const float2 so = h2_to_f2(pw);
+              const float2 s2 = make_float2(so.x, so.x), o2 = make_float2(so.y, so.y);
+              const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                float2 lo, hi;
+                s8x4_to_f32(words[k], lo, hi);
+                wv[r][2 * k] = ffma2(lo, s2, o2);
+                wv[r][2 * k + 1] = ffma2(hi, s2, o2);
+              }
             } else {
-              const float* xc = xin + (size_t)ch * CW;
-#pragma unroll
-              for (int b = 0; b < NB; ++b) {
-                float2 xv[EPL / 2];
-#pragma unroll
-                for (int k = 0; k < EPL / 4; ++k) {
-                  const float4 a = *reinterpret_cast<const float4*>(xc + (size_t)b * cols_pad + k * 128);
-                  xv[2 * k] = make_float2(a.x, a.y);
-                  xv[2 * k + 1] = make_float2(a.z, a.w);
-                }
-#pragma unroll
-                for (int r = 0; r < RPW; ++r)
-#pragma unroll
-                  for (int k = 0; k < EPL / 2; ++k) acc[r][b][0] = ffma2(wv[r][k], xv[k], acc[r][b][0]);
-              }
+              wv[r][0] = h2_to_f2(cw.x); wv[r][1] = h2_to_f2(cw.y);
+              wv[r][2] = h2_to_f2(cw.z); wv[r][3] = h2_to_f2(cw.w);
             }
+          }
+          const float* xc = xin + (size_t)ch * CW;
+#pragma unroll
+          for (int b = 0; b < NB; ++b) {
+            float2 xv[EPL / 2];
+#pragma unroll
+            for (int k = 0; k < EPL / 4; ++k) {
+              const float4 a = *reinterpret_cast<const float4*>(xc + (size_t)b * cols_pad + k * 128);
+              xv[2 * k] = make_float2(a.x, a.y);
+              xv[2 * k + 1] = make_float2(a.z, a.w);
+            }
+#pragma unroll
+            for (int r = 0; r < RPW; ++r)
+#pragma unroll
+              for (int k = 0; k < EPL / 2; ++k) acc[r][b] = ffma2(wv[r][k], xv[k], acc[r][b]);
           }
         }
       }
@@ -399,12 +633,7 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
 #pragma unroll
       for (int r = 0; r < RPW; ++r)
 #pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          float2 a = acc[r][b][0];
-#pragma unroll
-          for (int k = 1; k < NA; ++k) a = fadd2(a, acc[r][b][k]);
-          v[r * NB + b] = a.x + a.y;
-        }
+        for (int b = 0; b < NB; ++b) v[r * NB + b] = acc[r][b].x + acc[r][b].y;
       const float tot = reduce_scatter<N>(v, lane);
       if ((lane & (32 / N - 1)) == 0) {
         const int idx = lane / (32 / N);
@@ -465,6 +694,11 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
   }  // computing warps
   // leave no bulk copy in flight (an aborted block may have issued ahead)
   if (producer && lane == 0 && *(volatile int*)&s_abort) {
+    if constexpr (NB == 1) {
+      const uint64_t w0 = tc::globaltimer();
+      while (!tc::mbar_try_sleep(tc::smem_addr(inbar), 0u, 20000u) && tc::globaltimer() - w0 < P.wait_limit_ns) {
+      }
+    }
     for (int t = t0; t < t1 && t < t0 + GT_NST; ++t) {
       const uint64_t w0 = tc::globaltimer();
       while (!tc::mbar_try_sleep(tc::smem_addr(full + ((t - t0) % GT_NST)), 0u, 20000u) &&
@@ -555,7 +789,17 @@ int launch_gemv_tma(const GvParams& V, bool q8, bool argmax, const DeviceInfo& d
   }
   P.task_begin[V.njobs] = t;
   P.ntasks = t;
-  for (int i = 0; i < V.ninputs; ++i) P.in[i] = V.in[i];
+  P.ngamma = 0;
+  for (int i = 0; i < V.ninputs; ++i) {
+    P.in[i] = V.in[i];
+    P.gslot[i] = -1;
+    if (nb == 1) {
+      // one position: inputs and gammas arrive by bulk copies (16-byte aligned sources)
+      if (!aligned16(V.in[i].x) || (V.in[i].gamma && !aligned16(V.in[i].gamma))) return PGQ_EUNSUPPORTED;
+      if (V.in[i].gamma) P.gslot[i] = P.ngamma++;
+    }
+  }
+  P.early = V.early_weights;
   P.njobs = V.njobs;
   P.ninputs = V.ninputs;
   P.B = V.B;
@@ -573,9 +817,10 @@ int launch_gemv_tma(const GvParams& V, bool q8, bool argmax, const DeviceInfo& d
   P.ticket = V.ticket;
   P.ids = V.ids;
   P.wait_limit_ns = 2000000000ull;
-  const size_t smem = (size_t)V.ninputs * nb * P.cols_pad * 4 + GT_RED * (size_t)SR * nb * QW * 4 + 128 +
-                      (size_t)GT_NST * P.stage_bytes + 2 * GT_NST * 8 + 64;
-  if (smem + 1024 > dev.smem_optin) return PGQ_EUNSUPPORTED;
+  const size_t smem = (size_t)(V.ninputs * nb + P.ngamma) * P.cols_pad * 4 +
+                      GT_RED * (size_t)SR * std::max(nb, GT_GROUP) * QW * 4 + 128 +
+                      (size_t)GT_NST * P.stage_bytes + (2 * GT_NST + 1) * 8 + 64;
+  if (smem + 2048 > dev.smem_optin) return PGQ_EUNSUPPORTED;   // + the static shared memory
   GtFn fn = q8 ? (argmax ? gt_pick<true, true>(nb) : gt_pick<true, false>(nb))
                : (argmax ? gt_pick<false, true>(nb) : gt_pick<false, false>(nb));
   {
@@ -594,9 +839,21 @@ int launch_gemv_tma(const GvParams& V, bool q8, bool argmax, const DeviceInfo& d
   if (argmax) {
     if (cudaError_t e = cudaMemsetAsync(P.ticket, 0, sizeof(unsigned), st); e != cudaSuccess) return cuda_status(e);
   }
-  const int grid = std::max(1, std::min(dev.sms, P.ntasks));
+  // launched as a programmatic dependent of the previous kernel in the stream: the
+  // kernel waits for it (griddepcontrol.wait) before it touches anything it may have
+  // written, and only the weight stream (with early_weights) may start before
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(std::max(1, std::min(dev.sms, P.ntasks)));
+  cfg.blockDim = dim3((W + 1) * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   void* args[] = {&P};
-  return cuda_status(cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(grid), dim3((W + 1) * 32), args, smem, st));
+  return cuda_status(cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(fn), args));
 }
 
 int decode_status_read_and_clear(int* out) {
@@ -997,3 +1254,12 @@ int launch_head_tc(const GvParams& V, const DeviceInfo& dev, cudaStream_t st) {
 }
 
 }  // namespace pgq
+
+#ifdef PGQ_TRACE
+// Trace builds only: copies the first n words of the decode kernels' trace.
+extern "C" int pgq_debug_gtrace(unsigned long long* out, size_t n) {
+  const size_t all = sizeof(pgq::g_gtr) / sizeof(unsigned long long);
+  if (n > all) n = all;
+  return cudaMemcpyFromSymbol(out, pgq::g_gtr, n * sizeof(unsigned long long)) == cudaSuccess ? 0 : -1;
+}
+#endif

@@ -38,6 +38,9 @@ struct GvParams {
   int* part_idx;             // [grid][B]
   unsigned* ticket;
   int32_t* ids;              // [B]
+  // The weights may be fetched before the previous kernel in the stream has finished
+  // (it writes none of them): set only where the launcher knows that kernel.
+  int early_weights;
 };
 
 int launch_add_rmsnorm(float* h, const float* add, const float* gamma, float eps, int B, int n,
