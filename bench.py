@@ -162,9 +162,9 @@ class Q8DecodeLayer:
         self.pgq.gemv_q8(L["down"][0], L["down"][1], self.out["u"], y=self.out["down"])
 
     def step(self, L):
-        """The layer through its entry point (the down launch streams its weights while
-        the first launch finishes)."""
-        self.pgq.q8_decode_layer(L, self.x[0], self.xo[0], self.g, 1e-6, out=self.out1)
+        """The layer through its entry point; the weights are loaded once, so each
+        launch may stream its weights while the kernel before it finishes."""
+        self.pgq.q8_decode_layer(L, self.x[0], self.xo[0], self.g, 1e-6, out=self.out1, weights_stable=True)
 
     def next_layer(self):
         L = self.layers[self.i % len(self.layers)]

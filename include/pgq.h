@@ -203,6 +203,16 @@ typedef struct {
 int pgq_q8_decode_layer(const pgq_q8_layer* layer, const float* x, const float* x_o,
                         const float* gamma, float eps, float* q, float* k, float* v, float* o,
                         float* u, float* down, void* stream);
+/* pgq_q8_decode_layer with flags.  PGQ_WEIGHTS_STABLE: the caller states that no work
+ * still in flight on `stream` writes this layer's codes or params (the usual case in
+ * a decode step, where weights are loaded once).  The first launch may then begin
+ * streaming its weights while the kernel before it on the stream finishes, as the
+ * second launch always does after the first; inputs and outputs stay ordered after
+ * the earlier work.  Other bits must be 0 (PGQ_EINVAL). */
+#define PGQ_WEIGHTS_STABLE 1
+int pgq_q8_decode_layer_ex(const pgq_q8_layer* layer, const float* x, const float* x_o,
+                           const float* gamma, float eps, float* q, float* k, float* v, float* o,
+                           float* u, float* down, int flags, void* stream);
 
 /* ---------------------------------------------------------------- a4: prefill q8
  * Batched prefill projection of a pass of 1 <= B <= 64 positions through q8

@@ -71,6 +71,8 @@ _SIGS = {
     "pgq_mlp_f16_decode": (C.c_int, [_vp, _vp, _vp, C.c_int, C.c_int, _vp, C.c_float, _vp, _vp, _vp]),
     "pgq_q8_decode_layer": (C.c_int, [C.POINTER(Q8Layer), _vp, _vp, _vp, C.c_float, _vp, _vp, _vp, _vp, _vp,
                                       _vp, _vp]),
+    "pgq_q8_decode_layer_ex": (C.c_int, [C.POINTER(Q8Layer), _vp, _vp, _vp, C.c_float, _vp, _vp, _vp, _vp, _vp,
+                                         _vp, C.c_int, _vp]),
     "pgq_prefill_q8_workspace_bytes": (C.c_size_t, [C.POINTER(C.c_int), C.c_int, C.c_int, C.c_int]),
     "pgq_prefill_q8": (C.c_int, [C.POINTER(Q8Job), C.c_int, _vp, C.c_int, C.c_int, _vp, C.c_size_t, _vp]),
     "pgq_prefill_status": (C.c_int, [_vp, _vp]),
@@ -343,16 +345,22 @@ def q8_layer_struct(mats):
     return L
 
 
-def q8_decode_layer(mats, x, x_o, gamma, eps=1e-6, out=None, stream=None):
-    """The q8 decode layer for one position; returns dict q, k, v, o, u, down."""
+WEIGHTS_STABLE = 1
+
+
+def q8_decode_layer(mats, x, x_o, gamma, eps=1e-6, out=None, stream=None, weights_stable=False):
+    """The q8 decode layer for one position; returns dict q, k, v, o, u, down.
+    weights_stable: no work still in flight on the stream writes these weights (both
+    launches may then start streaming them while the kernel before them finishes)."""
     L = q8_layer_struct(mats)
     dev = x.device
     if out is None:
         out = {s: torch.empty(n, dtype=torch.float32, device=dev) for s, n in
                (("q", L.hidden), ("k", L.kv), ("v", L.kv), ("o", L.hidden), ("u", L.inter), ("down", L.hidden))}
-    _check(lib().pgq_q8_decode_layer(C.byref(L), _ptr(x), _ptr(x_o), _ptr(gamma), eps, _ptr(out["q"]),
-                                     _ptr(out["k"]), _ptr(out["v"]), _ptr(out["o"]), _ptr(out["u"]),
-                                     _ptr(out["down"]), _stream(stream)))
+    _check(lib().pgq_q8_decode_layer_ex(C.byref(L), _ptr(x), _ptr(x_o), _ptr(gamma), eps, _ptr(out["q"]),
+                                        _ptr(out["k"]), _ptr(out["v"]), _ptr(out["o"]), _ptr(out["u"]),
+                                        _ptr(out["down"]), WEIGHTS_STABLE if weights_stable else 0,
+                                        _stream(stream)))
     return out
 
 

@@ -309,7 +309,13 @@ int pgq_mlp_f16_decode(const float* h, const uint16_t* W_up, const uint16_t* W_d
 
 int pgq_q8_decode_layer(const pgq_q8_layer* L, const float* x, const float* x_o, const float* gamma, float eps,
                         float* q, float* k, float* v, float* o, float* u, float* down, void* stream) {
+  return pgq_q8_decode_layer_ex(L, x, x_o, gamma, eps, q, k, v, o, u, down, 0, stream);
+}
+
+int pgq_q8_decode_layer_ex(const pgq_q8_layer* L, const float* x, const float* x_o, const float* gamma, float eps,
+                           float* q, float* k, float* v, float* o, float* u, float* down, int flags, void* stream) {
   REQUIRE(L && x && x_o && gamma && q && k && v && o && u && down, PGQ_EINVAL, "q8_decode_layer: null pointer");
+  REQUIRE((flags & ~PGQ_WEIGHTS_STABLE) == 0, PGQ_EINVAL, "q8_decode_layer: unknown flags 0x%x", flags);
   const int H = L->hidden, KV = L->kv, I = L->inter;
   pgq_q8_job jobs[5] = {
       {L->q.codes, L->q.params, H, 0, q, PGQ_EPI_NONE, nullptr},
@@ -319,7 +325,7 @@ int pgq_q8_decode_layer(const pgq_q8_layer* L, const float* x, const float* x_o,
       {L->up.codes, L->up.params, I, 0, u, PGQ_EPI_RELU2, nullptr},
   };
   pgq_input ins[2] = {{x, gamma}, {x_o, nullptr}};
-  int st = pgq_gemv_q8_multi(jobs, 5, ins, 2, H, 1, eps, stream);
+  int st = gemv_q8_multi_impl(jobs, 5, ins, 2, H, 1, eps, (flags & PGQ_WEIGHTS_STABLE) ? 1 : 0, stream);
   if (st) return st;
   // the down launch follows the launch above, which writes no weights: its weight
   // stream may start while that launch finishes

@@ -31,6 +31,7 @@ namespace pgq {
 
 
 constexpr int GT_STAGE_MAX = 37 * 1024;   // bytes of one ring stage (codes + params)
+constexpr int GT_SLOT = GT_STAGE_MAX + 256; // one position: fixed stride of the ring slots
 constexpr int GT_NST = 4;                  // ring stages
 constexpr int GT_RED = 2;                  // buffers of per-warp partial sums
 constexpr int GT_GROUP = 4;                // one position: stages per reduction group
@@ -68,6 +69,7 @@ struct GtParams {
   int njobs, ninputs, ngamma, early, B, cols, cols_pad, nchunks;
   int SR, QW, cpw;
   int code_bytes, stage_bytes;   // per stage: SR rows of codes, then SR rows of params
+  int slot_bytes;                // stride of the ring slots (GT_SLOT at one position)
   int ntasks;
   float eps;
   float* part_val;
@@ -103,7 +105,7 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(red + GT_RED * P.SR * (NB > GT_GROUP ? NB : GT_GROUP) * P.QW) + 127) &
       ~uintptr_t(127));
-  uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)GT_NST * P.stage_bytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)GT_NST * P.slot_bytes);
   uint64_t* empty = full + GT_NST;
   uint64_t* inbar = empty + GT_NST;   // one position: the inputs' bulk copies
   __shared__ float s_inv[MAX_INPUTS * NB];
@@ -122,7 +124,7 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
     const uint32_t cb = (uint32_t)((size_t)nr * cols * ESZ);
     const uint32_t pb = Q8 ? (uint32_t)((size_t)nr * (cols >> 5) * 4) : 0u;
     tc::mbar_expect_tx(bar, cb + pb);
-    uint8_t* dst = ring + (size_t)s * P.stage_bytes;
+    uint8_t* dst = ring + (size_t)s * P.slot_bytes;
     tc::bulk_load(tc::smem_addr(dst), P.w[j] + (size_t)row0 * cols * ESZ, cb, bar, policy);
     if constexpr (Q8)
       tc::bulk_load(tc::smem_addr(dst + P.code_bytes), P.p[j] + (size_t)row0 * (cols >> 5) * 4, pb, bar, policy);
@@ -352,9 +354,11 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
     static_assert(NV <= 32 && (NV & (NV - 1)) == 0, "partials per group: a power of two <= 32");
     float2 xr[MAXC][EPL / 2];   // this lane's input values, per chunk
     float xsum[MAXC];           // and their sum, per chunk
+    float xk[MAXC];             // −(2^15 + 128)·xsum: the start of a chunk's q8 dot
     int job_end = 0, input_j = -1;
-    int buf = 0, s = 0;
-    uint32_t parity = 0;
+    int buf = 0;
+    uint32_t parity = 0;   // of the ring's current pass (one group = one pass)
+    static_assert(GT_GROUP == GT_NST, "a group is one pass over the ring: stage gs sits in slot gs");
     const int ngrp = P.SR / RPW;
     // this lane's EPL consecutive columns of each of its chunks (natural order),
     // RMS-normalised where the input has a gamma; lanes 32/EPL apart would hit the
@@ -397,28 +401,42 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
 #pragma unroll
         for (int k = 1; k < EPL / 2; ++k) sum2 = fadd2(sum2, xr[u][k]);
         xsum[u] = sum2.x + sum2.y;
+        xk[u] = -32896.f * xsum[u];
       }
     };
-    // this lane's share of the RPW rows of one stage, added into out[0..RPW)
-    auto dot_stage = [&](const uint8_t* st, float* out) {
+    // shared-memory addresses of this lane's code and (scale, offset) words in slot 0
+    // (slot i is GT_SLOT·i further: with the group loop unrolled, an immediate offset)
+    uint32_t a_c[RPW][MAXC], a_p[RPW][MAXC];
+    {
+      const uint32_t r0 = tc::smem_addr(ring);
+#pragma unroll
+      for (int r = 0; r < RPW; ++r)
+#pragma unroll
+        for (int u = 0; u < MAXC; ++u) {
+          a_c[r][u] = r0 + (uint32_t)off_c[r][u];
+          a_p[r][u] = r0 + (uint32_t)off_p[r][u];
+        }
+    }
+    // this lane's share of the RPW rows of the stage in slot `slot`, into out[0..RPW)
+    auto dot_stage = [&](uint32_t slot_off, float* out) {
       float2 acc[RPW][NA];
 #pragma unroll
       for (int r = 0; r < RPW; ++r)
 #pragma unroll
         for (int a = 0; a < NA; ++a) acc[r][a] = make_float2(0.f, 0.f);
       if constexpr (Q8) {
-        // dot then scale: Σ u·x with the biased byte u = q + 128 in [0, 255], widened by
-        // one byte-permute into the f32 2^15 + u (exponent 15, u in mantissa bits
-        // 8..15); then y += scale·(dot − 2^15·Σx) + (offset − 128·scale)·Σx.  Every
-        // shared-memory read of the stage is issued first, then the arithmetic.
+        // dot then scale: the biased byte u = q + 128 in [0, 255] is widened by one
+        // byte-permute into the f32 2^15 + u (exponent 15, u in mantissa bits 8..15);
+        // Σ (2^15 + u)·x − (2^15 + 128)·Σx = Σ q·x, and y += scale·Σ q·x + offset·Σx.
+        // Every shared-memory read of the stage is issued first, then the arithmetic.
         uint4 cw[RPW][MAXC];
         uint32_t pw[RPW][MAXC];
 #pragma unroll
         for (int u = 0; u < MAXC; ++u)
 #pragma unroll
           for (int r = 0; r < RPW; ++r) {
-            cw[r][u] = *reinterpret_cast<const uint4*>(st + off_c[r][u]);
-            pw[r][u] = *reinterpret_cast<const uint32_t*>(st + off_p[r][u]);
+            cw[r][u] = tc::lds128(a_c[r][u] + slot_off);
+            pw[r][u] = tc::lds32(a_p[r][u] + slot_off);
           }
 #pragma unroll
         for (int u = 0; u < MAXC; ++u) {
@@ -428,7 +446,8 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
               const float2 so = h2_to_f2(pw[r][u]);
               const uint32_t words[4] = {cw[r][u].x ^ 0x80808080u, cw[r][u].y ^ 0x80808080u,
                                          cw[r][u].z ^ 0x80808080u, cw[r][u].w ^ 0x80808080u};
-              float2 d0 = make_float2(0.f, 0.f), d1 = make_float2(0.f, 0.f);
+              // the dot starts from −(2^15 + 128)·Σx, so that it ends as Σ (u − 128)·x = Σ q·x
+              float2 d0 = make_float2(xk[u], 0.f), d1 = make_float2(0.f, 0.f);
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
                 const float2 lo = make_float2(__uint_as_float(__byte_perm(words[k], 0x47000000u, 0x7504)),
@@ -439,10 +458,9 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
                 d1 = ffma2(hi, xr[u][2 * k + 1], d1);
               }
               const float2 d = fadd2(d0, d1);
-              const float c = fmaf(-128.f, so.x, so.y);
               float2 a = acc[r][0];
-              a.x = fmaf(so.x, fmaf(-32768.f, xsum[u], d.x + d.y), a.x);
-              a.y = fmaf(c, xsum[u], a.y);
+              a.x = fmaf(so.x, d.x + d.y, a.x);     // scale · Σ q·x
+              a.y = fmaf(so.y, xsum[u], a.y);       // offset · Σ x
               acc[r][0] = a;
             }
           }
@@ -453,7 +471,7 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
           if (lane_ok[u]) {
 #pragma unroll
             for (int r = 0; r < RPW; ++r) {
-              const uint4 cw = *reinterpret_cast<const uint4*>(st + off_c[r][u]);
+              const uint4 cw = tc::lds128(a_c[r][u] + slot_off);
               const float2 wv[4] = {h2_to_f2(cw.x), h2_to_f2(cw.y), h2_to_f2(cw.z), h2_to_f2(cw.w)};
 #pragma unroll
               for (int k = 0; k < EPL / 2; ++k) acc[r][k % NA] = ffma2(wv[k], xr[u][k], acc[r][k % NA]);
@@ -490,17 +508,17 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
           if (warp == 0 && lane == 0 && t == t0) GTRACE(10);
 #endif
           // warp-uniform: every lane of the warp leaves the same way
-          ok = __all_sync(0xffffffffu, wait_bar(tc::smem_addr(full + s), parity));
+          ok = __all_sync(0xffffffffu, wait_bar(tc::smem_addr(full + gs), parity));
 #ifdef PGQ_TRACE
           if (warp == 0 && lane == 0 && t == t0) GTRACE(2);
 #endif
-          if (ok) dot_stage(ring + (size_t)s * P.stage_bytes, part + gs * RPW);
+          if (ok) dot_stage((uint32_t)(gs * GT_SLOT), part + gs * RPW);
           // the warp's reads of the stage are done: release the slot to the producer
           __syncwarp();
-          if (lane == 0) tc::mbar_arrive(tc::smem_addr(empty + s));
-          if (++s == GT_NST) { s = 0; parity ^= 1u; }
+          if (lane == 0) tc::mbar_arrive(tc::smem_addr(empty + gs));
         }
       }
+      parity ^= 1u;
       // lane reduction of the group's NV partials; then the QW warps of the row group
       // meet (named barrier; all leave together if one wait expired) and its first
       // warp adds the partial sums in fixed order, applies the epilogue and stores
@@ -584,7 +602,7 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
       for (int b = 0; b < NB; ++b) acc[r][b] = make_float2(0.f, 0.f);
     if (ok) {
       const float* xin = xs + (size_t)input_j * NB * cols_pad + lane * 4;
-      const uint8_t* st = ring + (size_t)s * P.stage_bytes;
+      const uint8_t* st = ring + (size_t)s * P.slot_bytes;
 #pragma unroll
       for (int u = 0; u < MAXC; ++u) {
         const int ch = ch_begin + u;
@@ -811,6 +829,8 @@ int launch_gemv_tma(const GvParams& V, bool q8, bool argmax, const DeviceInfo& d
   P.cpw = cpw;
   P.code_bytes = (SR * V.cols * esz + 127) / 128 * 128;
   P.stage_bytes = (P.code_bytes + (q8 ? SR * (V.cols / 32) * 4 : 0) + 127) / 128 * 128;
+  if (P.stage_bytes > GT_SLOT) return PGQ_EUNSUPPORTED;
+  P.slot_bytes = nb == 1 ? GT_SLOT : P.stage_bytes;   // the one-position kernel assumes GT_SLOT
   P.eps = V.eps;
   P.part_val = V.part_val;
   P.part_idx = V.part_idx;
@@ -819,7 +839,7 @@ int launch_gemv_tma(const GvParams& V, bool q8, bool argmax, const DeviceInfo& d
   P.wait_limit_ns = 2000000000ull;
   const size_t smem = (size_t)(V.ninputs * nb + P.ngamma) * P.cols_pad * 4 +
                       GT_RED * (size_t)SR * std::max(nb, GT_GROUP) * QW * 4 + 128 +
-                      (size_t)GT_NST * P.stage_bytes + (2 * GT_NST + 1) * 8 + 64;
+                      (size_t)GT_NST * P.slot_bytes + (2 * GT_NST + 1) * 8 + 64;
   if (smem + 2048 > dev.smem_optin) return PGQ_EUNSUPPORTED;   // + the static shared memory
   GtFn fn = q8 ? (argmax ? gt_pick<true, true>(nb) : gt_pick<true, false>(nb))
                : (argmax ? gt_pick<false, true>(nb) : gt_pick<false, false>(nb));

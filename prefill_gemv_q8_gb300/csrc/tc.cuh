@@ -55,6 +55,19 @@ __device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity, ui
   return ok != 0;
 }
 
+// Shared-memory loads by 32-bit shared-window address (constant offsets fold into the
+// instruction); volatile so that they stay after the mbarrier wait that guards them.
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+
 // One lane of the (converged) warp gets true.
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred;

@@ -263,3 +263,41 @@ def test_q8_decode_layer_full_size():
     out = pgq.q8_decode_layer(dm, x, x_o, g, 1e-6)
     mats = {s: (host(cc), host(pp)) for s, (cc, pp) in dm.items()}
     _check_layer(out, mats, host(x), host(x_o), host(g))
+
+
+def _chain(dms, x0, x_o, g):
+    """Layer calls back to back with weights_stable, no host synchronisation between
+    them: call i+1 reads x = call i's down output (written by the launch just before)."""
+    outs, xs = [], [x0]
+    for dm in dms:
+        outs.append(pgq.q8_decode_layer(dm, xs[-1], x_o, g, 1e-6, weights_stable=True))
+        xs.append(outs[-1]["down"])
+    return outs, xs
+
+
+def test_q8_decode_layers_chained_weights_stable():
+    """Three layers with distinct weights chained through their down outputs: each
+    step checked against the oracle on the input the kernels actually read."""
+    hidden, kv, inter = 512, 128, 1792
+    mats = [_layer(hidden, kv, inter, wl=930 + i) for i in range(3)]
+    x = synth.normal((hidden,), 1.0, 930, synth.T_X)
+    x_o = synth.normal((hidden,), 1.0, 930, synth.T_XO)
+    g = synth.gamma(hidden, 930)
+    dms = [{s: (dev(c), dev(p)) for s, (c, p) in m.items()} for m in mats]
+    outs, xs = _chain(dms, dev(x), dev(x_o), dev(g))
+    for out, m, xi in zip(outs, mats, xs):
+        _check_layer(out, m, host(xi), x_o, g)
+
+
+def test_q8_decode_layers_chained_full_size():
+    """Two chained full-size layers (hidden 4096, kv 1024, inter 14336) with
+    weights_stable, as the benchmark runs them."""
+    c = synth.Q8_LAYER
+    dm = _layer(c["hidden"], c["kv"], c["inter"], wl=c["workload"], backend="torch")
+    x = synth.normal((c["hidden"],), 1.0, c["workload"], synth.T_X, "torch", "cuda")
+    x_o = synth.normal((c["hidden"],), 1.0, c["workload"], synth.T_XO, "torch", "cuda")
+    g = synth.gamma(c["hidden"], c["workload"], backend="torch", device="cuda")
+    outs, xs = _chain([dm, dm], x, x_o, g)
+    mats = {s: (host(cc), host(pp)) for s, (cc, pp) in dm.items()}
+    for out, xi in zip(outs, xs):
+        _check_layer(out, mats, host(xi), host(x_o), host(g))
