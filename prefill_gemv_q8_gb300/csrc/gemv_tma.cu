@@ -59,6 +59,11 @@ __device__ unsigned long long g_gtr[1024 * GTR_EV];
 #endif
 
 struct GtParams {
+  // one position: tensor maps of the staged planes (each input, then each gamma) as
+  // [cols/32][32] f32 rows, 128-byte swizzle, box {32, box_rows}
+  alignas(64) CUtensorMap xmap[2 * MAX_INPUTS];
+  int nplanes, box_rows, nbox;
+  int plane_dst[2 * MAX_INPUTS];   // float offset of the plane from the staging area
   const uint8_t* w[PGQ_MULTI_MAX];
   const uint8_t* p[PGQ_MULTI_MAX];
   float* y[PGQ_MULTI_MAX];
@@ -99,7 +104,8 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
   constexpr int NA = NB == 1 ? 2 : 1;    // accumulators per row (breaks FMA chains)
   extern __shared__ __align__(128) uint8_t gsm[];
   const int cols = P.cols, cols_pad = P.cols_pad, cols4 = cols >> 2;
-  float* xs = reinterpret_cast<float*>(gsm);                                  // [ninputs][NB][cols_pad]
+  // (1024-byte aligned: the one-position staging is written with a 128-byte swizzle)
+  float* xs = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(gsm) + 1023) & ~uintptr_t(1023));  // [ninputs][NB][cols_pad]
   float* gs = xs + (size_t)P.ninputs * NB * cols_pad;                         // one position: [ngamma][cols_pad]
   float* red = gs + (NB == 1 ? (size_t)P.ngamma * cols_pad : 0);  // [GT_RED][SR][NB][QW]; one position: [GT_RED][SR/RPW][GT_GROUP·RPW][QW]
   uint8_t* ring = reinterpret_cast<uint8_t*>(
@@ -114,7 +120,9 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, T = P.ntasks;
-  const int t0 = (int)((long long)blockIdx.x * T / G), t1 = (int)((long long)(blockIdx.x + 1) * T / G);
+  // (32-bit: tasks x blocks stays far below 2^32)
+  const int t0 = (int)((unsigned)blockIdx.x * (unsigned)T / (unsigned)G);
+  const int t1 = (int)((unsigned)(blockIdx.x + 1) * (unsigned)T / (unsigned)G);
   const uint64_t policy = tc::policy_evict_first();
 
   auto issue = [&](int t, int j, int s) {   // one thread
@@ -140,25 +148,6 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
   };
 
   const bool producer = warp == W;
-  if (tid == 0) {
-    GTRACE(0);
-#ifdef PGQ_TRACE
-    g_gtr[GTR_SLOT + 7] = (unsigned long long)(t1 - t0);
-    g_gtr[GTR_SLOT + 5] = 0ull;
-#endif
-    for (int s = 0; s < GT_NST; ++s) {
-      tc::mbar_init(tc::smem_addr(full + s), 1);
-      tc::mbar_init(tc::smem_addr(empty + s), W);
-    }
-    tc::mbar_init(tc::smem_addr(inbar), 1);
-    s_abort = 0;
-    tc::fence_barrier_init();
-  }
-  __syncthreads();
-  // A launch that follows this one in the stream as a programmatic dependent may take
-  // the SMs this grid frees from here on; it reads nothing this grid writes before
-  // its own griddepcontrol.wait.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // bounded wait on an mbarrier phase; false after an expired wait (or another
   // role's), which then also marks the block aborted
@@ -176,60 +165,61 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
     return true;
   };
 
-  // inputs read by this block's jobs (one bit per input)
-  unsigned used_in = 0u;
-  if (t0 < t1) {
-    const int j0 = job_of(t0, 0), j1 = job_of(t1 - 1, 0);
-#pragma unroll
-    for (int i = 0; i < PGQ_MULTI_MAX; ++i)
-      if (i >= j0 && i <= j1) used_in |= 1u << P.input[i];
-  }
+  // A launch that follows this one in the stream as a programmatic dependent may take
+  // the SMs this grid frees from here on; it reads nothing this grid writes before
+  // its own griddepcontrol.wait.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  // The weights never depend on earlier kernels' results: where the launcher allows
-  // it they stream before the wait for the previous kernel, else right after it.  At
-  // one position the inputs (and gammas) come by bulk copies issued ahead of the
-  // weights, so that they do not queue behind the ring's first fill.
-  // (the inputs by warp 0, the weights by the producer warp: two threads issue at once)
+  // The first copies go out before anything else, all from the producer lane, in the
+  // order they are needed: it sets up the barriers, then issues the ring's first
+  // stage, the inputs (at one position; all of them: every block then keeps them hot
+  // in L2) and the second stage.  The weights never depend on earlier kernels: where
+  // the launcher allows it they stream before the wait for the previous kernel (and
+  // so ahead of the inputs), else after it.  The block-wide barrier below publishes
+  // the barrier set-up to the other warps before any of them waits on one.
+  auto issue_inputs = [&]() {
+    if constexpr (NB == 1) {
+      // each plane lands 128-byte swizzled (16-byte word c of row R at c ^ (R mod 8))
+      const uint32_t bar = tc::smem_addr(inbar);
+      tc::mbar_expect_tx(bar, (uint32_t)(P.nplanes * P.nbox * P.box_rows * 128));
+      const uint32_t x0 = tc::smem_addr(xs);
+      const uint64_t keep = tc::policy_evict_last();
+      for (int pl = 0; pl < P.nplanes; ++pl)
+        for (int bx = 0; bx < P.nbox; ++bx)
+          tc::tma_load_2d_hint(x0 + (uint32_t)P.plane_dst[pl] * 4u + (uint32_t)(bx * P.box_rows * 128),
+                               &P.xmap[pl], 0, bx * P.box_rows, bar, keep);
+    }
+  };
   if (producer && lane == 0) {
-    auto issue_ring = [&]() {
-      for (int i = 0; i < GT_RAMP && t0 + i < t1; ++i) issue(t0 + i, job_of(t0 + i, 0), i);
+    for (int s = 0; s < GT_NST; ++s) {
+      tc::mbar_init(tc::smem_addr(full + s), 1);
+      tc::mbar_init(tc::smem_addr(empty + s), W);
+    }
+    tc::mbar_init(tc::smem_addr(inbar), 1);
+    tc::fence_barrier_init();
+    auto issue_ring = [&](int i0, int i1) {
+      for (int i = i0; i < i1 && i < GT_RAMP && t0 + i < t1; ++i) issue(t0 + i, job_of(t0 + i, 0), i);
     };
-    if (P.early) issue_ring();
+    if (P.early) issue_ring(0, GT_RAMP);
 #ifdef PGQ_TRACE
     GTRACE(11);
 #endif
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (!P.early) issue_ring();
+    if (!P.early) issue_ring(0, 1);
+    issue_inputs();
+    if (!P.early) issue_ring(1, GT_RAMP);
 #ifdef PGQ_TRACE
     GTRACE(3);
 #endif
   }
   if (tid == 0) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if constexpr (NB == 1) {
-      const uint32_t bar = tc::smem_addr(inbar);
-      const uint32_t xb = (uint32_t)cols * 4u;
-      uint32_t bytes = 0;
-      for (int i = 0; i < P.ninputs; ++i)
-        if (used_in >> i & 1) bytes += P.in[i].gamma ? 2u * xb : xb;
-      tc::mbar_expect_tx(bar, bytes);
-      const uint64_t keep = tc::policy_evict_last();
-      for (int i = 0; i < P.ninputs; ++i) {
-        if (!(used_in >> i & 1)) continue;
-        tc::bulk_load(tc::smem_addr(xs + (size_t)i * cols_pad), P.in[i].x, xb, bar, keep);
-        if (P.in[i].gamma)
-          tc::bulk_load(tc::smem_addr(gs + (size_t)P.gslot[i] * cols_pad), P.in[i].gamma, xb, bar, keep);
-      }
-    }
-  }
+    GTRACE(0);
 #ifdef PGQ_TRACE
-  if (warp == 1 && lane == 0 && t0 < t1 && P.early) {   // when an early first weight stage lands
-    const uint64_t w0 = tc::globaltimer();
-    while (!tc::mbar_try_sleep(tc::smem_addr(full), 0u, 20000u) && tc::globaltimer() - w0 < P.wait_limit_ns) {
-    }
-    GTRACE(9);
-  }
+    g_gtr[GTR_SLOT + 7] = (unsigned long long)(t1 - t0);
+    g_gtr[GTR_SLOT + 5] = 0ull;
 #endif
+    s_abort = 0;
+  }
   // ---- a computing warp's rows and column share (worked out while the inputs are
   // on their way; the producer warp's values are not used)
   const int QW = P.QW;
@@ -254,6 +244,15 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
       off_p[r][u] = P.code_bytes + ((row_a + r) * (cols >> 5) + (col >> 5)) * 4;
     }
   }
+  __syncthreads();   // the barriers are set up (and s_abort cleared) before any wait
+#ifdef PGQ_TRACE
+  if (warp == 1 && lane == 0 && t0 < t1 && P.early) {   // when an early first weight stage lands
+    const uint64_t w0 = tc::globaltimer();
+    while (!tc::mbar_try_sleep(tc::smem_addr(full), 0u, 20000u) && tc::globaltimer() - w0 < P.wait_limit_ns) {
+    }
+    GTRACE(9);
+  }
+#endif
   asm volatile("griddepcontrol.wait;" ::: "memory");
 #ifdef PGQ_TRACE
   if (tid == 0) GTRACE(8);
@@ -264,7 +263,7 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
     // computed here (each warp scales its own register copy when it loads it)
     const bool in_ok = wait_bar(tc::smem_addr(inbar), 0u);
     for (int i = 0; i < P.ninputs; ++i) {
-      if (!P.in[i].gamma || !(used_in >> i & 1)) continue;
+      if (!P.in[i].gamma) continue;
       const float4* x4 = reinterpret_cast<const float4*>(xs + (size_t)i * cols_pad);
       float ss = 0.f;
       if (in_ok)
@@ -359,41 +358,37 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
     int buf = 0;
     uint32_t parity = 0;   // of the ring's current pass (one group = one pass)
     static_assert(GT_GROUP == GT_NST, "a group is one pass over the ring: stage gs sits in slot gs");
+#ifdef PGQ_TRACE
+    if (warp == 0 && lane == 0) GTRACE(6);
+#endif
     const int ngrp = P.SR / RPW;
-    // this lane's EPL consecutive columns of each of its chunks (natural order),
-    // RMS-normalised where the input has a gamma; lanes 32/EPL apart would hit the
-    // same banks with the same 16-byte word, so each lane starts at word
-    // (lane / (32/EPL)) of its EPL/4 and the words are put back in order
+    // this lane's EPL consecutive columns of each of its chunks, RMS-normalised where
+    // the input has a gamma.  The planes are 128-byte swizzled (16-byte word c of
+    // 128-byte row R at word c ^ (R mod 8)), which spreads the lanes' reads over all
+    // banks.
     auto load_x = [&](int input) {
-      const float* xin = xs + (size_t)input * cols_pad + lane * EPL;
+      const uint32_t xin = tc::smem_addr(xs) + (uint32_t)(input * cols_pad * 4);
       const int gsl = P.gslot[input];
-      const float* gin = gsl >= 0 ? gs + (size_t)gsl * cols_pad + lane * EPL : nullptr;
+      const uint32_t gin = tc::smem_addr(gs) + (uint32_t)((gsl < 0 ? 0 : gsl) * cols_pad * 4);
       const float inv = s_inv[input];
-      constexpr int NK = EPL / 4;
-      const int rot = (lane / (32 / EPL)) % NK;
 #pragma unroll
       for (int u = 0; u < MAXC; ++u) {
-        float4 v[NK];
 #pragma unroll
-        for (int kk = 0; kk < NK; ++kk) {
-          const int k = (kk + rot) % NK;
+        for (int k = 0; k < EPL / 4; ++k) {
           float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
           if (ch_begin + u < ch_end) {
-            const size_t o = (size_t)(ch_begin + u) * CW + k * 4;
-            a = *reinterpret_cast<const float4*>(xin + o);
-            if (gin) {
-              const float4 g = *reinterpret_cast<const float4*>(gin + o);
+            const int f = (ch_begin + u) * CW + lane * EPL + 4 * k;   // natural column
+            const int row = f >> 5, word = (f >> 2) & 7;
+            const uint32_t o = (uint32_t)(row * 128 + ((word ^ (row & 7)) << 4));
+            const uint4 av = tc::lds128(xin + o);
+            a = make_float4(__uint_as_float(av.x), __uint_as_float(av.y), __uint_as_float(av.z), __uint_as_float(av.w));
+            if (gsl >= 0) {
+              const uint4 gv = tc::lds128(gin + o);
+              const float4 g = make_float4(__uint_as_float(gv.x), __uint_as_float(gv.y), __uint_as_float(gv.z),
+                                           __uint_as_float(gv.w));
               a = make_float4(g.x * (a.x * inv), g.y * (a.y * inv), g.z * (a.z * inv), g.w * (a.w * inv));
             }
           }
-          v[kk] = a;
-        }
-#pragma unroll
-        for (int k = 0; k < NK; ++k) {
-          float4 a = v[0];
-#pragma unroll
-          for (int kk = 1; kk < NK; ++kk)
-            if ((kk + rot) % NK == k) a = v[kk];
           xr[u][2 * k] = make_float2(a.x, a.y);
           xr[u][2 * k + 1] = make_float2(a.z, a.w);
         }
@@ -498,11 +493,20 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
         const int t = g0 + gs;
         if (t < t1 && ok) {
           if (t >= job_end) {
+#ifdef PGQ_TRACE
+            if (warp == 0 && lane == 0 && t == t0) GTRACE(12);
+#endif
             const int jn = job_of(t, 0);
             job_end = P.task_begin[jn + 1];
             const int input = P.input[jn];
+#ifdef PGQ_TRACE
+            if (warp == 0 && lane == 0 && t == t0) GTRACE(13);
+#endif
             if (input != input_j) load_x(input);
             input_j = input;
+#ifdef PGQ_TRACE
+            if (warp == 0 && lane == 0 && t == t0) GTRACE(14);
+#endif
           }
 #ifdef PGQ_TRACE
           if (warp == 0 && lane == 0 && t == t0) GTRACE(10);
@@ -812,7 +816,7 @@ int launch_gemv_tma(const GvParams& V, bool q8, bool argmax, const DeviceInfo& d
     P.in[i] = V.in[i];
     P.gslot[i] = -1;
     if (nb == 1) {
-      // one position: inputs and gammas arrive by bulk copies (16-byte aligned sources)
+      // one position: inputs and gammas arrive by TMA (16-byte aligned sources)
       if (!aligned16(V.in[i].x) || (V.in[i].gamma && !aligned16(V.in[i].gamma))) return PGQ_EUNSUPPORTED;
       if (V.in[i].gamma) P.gslot[i] = P.ngamma++;
     }
@@ -824,6 +828,28 @@ int launch_gemv_tma(const GvParams& V, bool q8, bool argmax, const DeviceInfo& d
   P.cols = V.cols;
   P.nchunks = nchunks;
   P.cols_pad = nchunks * CW;
+  if (nb == 1) {
+    // the staged planes: [cols/32][32] f32, boxes of the largest row count <= 256 that
+    // divides the rows (so that the boxes tile the plane exactly)
+    const int prow = V.cols / 32;
+    int br = std::min(prow, 256);
+    while (prow % br) --br;
+    P.box_rows = br;
+    P.nbox = prow / br;
+    if (P.nbox > 1 && br % 8) return PGQ_EUNSUPPORTED;   // every box starts on a 1024-byte swizzle atom
+    P.nplanes = 0;
+    auto plane = [&](const float* src, int dst) {
+      if (!encode_2d(&P.xmap[P.nplanes], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, src, 32, (uint64_t)prow, 128, 32,
+                     (uint32_t)br, CU_TENSOR_MAP_SWIZZLE_128B))
+        return false;
+      P.plane_dst[P.nplanes++] = dst;
+      return true;
+    };
+    for (int i = 0; i < V.ninputs; ++i)
+      if (!plane(V.in[i].x, i * P.cols_pad)) return PGQ_EUNSUPPORTED;
+    for (int i = 0; i < V.ninputs; ++i)
+      if (V.in[i].gamma && !plane(V.in[i].gamma, (V.ninputs + P.gslot[i]) * P.cols_pad)) return PGQ_EUNSUPPORTED;
+  }
   P.SR = SR;
   P.QW = QW;
   P.cpw = cpw;
@@ -837,7 +863,7 @@ int launch_gemv_tma(const GvParams& V, bool q8, bool argmax, const DeviceInfo& d
   P.ticket = V.ticket;
   P.ids = V.ids;
   P.wait_limit_ns = 2000000000ull;
-  const size_t smem = (size_t)(V.ninputs * nb + P.ngamma) * P.cols_pad * 4 +
+  const size_t smem = 1024 + (size_t)(V.ninputs * nb + P.ngamma) * P.cols_pad * 4 +
                       GT_RED * (size_t)SR * std::max(nb, GT_GROUP) * QW * 4 + 128 +
                       (size_t)GT_NST * P.slot_bytes + (2 * GT_NST + 1) * 8 + 64;
   if (smem + 2048 > dev.smem_optin) return PGQ_EUNSUPPORTED;   // + the static shared memory
