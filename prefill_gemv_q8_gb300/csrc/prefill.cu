@@ -63,7 +63,7 @@ constexpr int PS_MAXL = 8;                                    // layers per pass
 constexpr int PS_MAXPH = 4 * PS_MAXL;                         // phases per launch
 constexpr int PS_MAXJ = 6 * PS_MAXL;                          // matrices per launch
 constexpr int PS_NX = 4;                                      // input buffers (n1, q, n2, u)
-constexpr int PS_STATIC_SMEM = 4096;                          // bound on the kernel's static shared memory
+constexpr int PS_STATIC_SMEM = 6144;                          // bound on the kernel's static shared memory
 constexpr int PS_MOE_EMAX = 256;                              // experts of a grouped bank at most
 constexpr int PS_OUT_K = PS_ACC_COLS * (TC_BM / 4) / 128;     // float4 slots per epilogue thread (16)
 constexpr int PS_OUT_P = 4;                                   // handled in passes (registers)
@@ -71,7 +71,11 @@ constexpr int PS_OUT_H = PS_OUT_K / PS_OUT_P;
 
 struct PsJob {
   CUtensorMap cmap;          // codes int8 [rows][cols], box {128, 128}, 128-byte swizzle
-  CUtensorMap pmap;          // params u32 [rows][cols/32], box {4, 128}
+  CUtensorMap pmap;          // params u32 [rows][cols/32], box {4, 128} (unless praw)
+  // params whose rows are not a multiple of 16 bytes (no tensor copy): u32 [rows][pstride],
+  // copied 8 bytes at a time (cp.async) by the producer warp; null: pmap
+  const uint32_t* praw;
+  int pstride, prows;
   float* y;                  // [B][rows]
   const float* residual;     // [B][rows] for PGQ_EPI_ADD
   int rows, epi, tile0, ntiles;   // tile0: first tile of the job within its phase
@@ -379,6 +383,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   __shared__ float s_xinv[64], s_inv[64], s_sc[64];
   __shared__ int s_mcnt[MOE ? PS_MOE_EMAX : 1], s_moff[MOE ? PS_MOE_EMAX : 1], s_ent[MOE ? 64 : 1];
+  __shared__ int s_live[MOE ? PS_MOE_EMAX : 1], s_nlive;
   __shared__ float2 s_st[2][64];
 
   auto bar = [&](int i) { return tc::smem_addr(bars + i); };
@@ -421,15 +426,34 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   Waiter W{P, abort_flag};
-  // a grouped bank skips the tiles of experts without entries (every role alike)
+  // A grouped bank leaves out the experts without entries: its (tile, k-step) items
+  // run over the live experts' tiles only (every block lists them alike), so the
+  // blocks' equal ranges hold equal work.  Tile v of that list is the bank's tile
+  // live(v); the others (the partials, the tile counters) count in list tiles.
   const int tpe = MOE ? P.tpe : 1;
-  auto skipped = [&](int tile) -> bool {
-    if constexpr (MOE) return s_mcnt[tile / tpe] == 0;
-    return false;
+  if constexpr (MOE) {
+    if (warp == 0) {
+      int base = 0;
+      for (int e0 = 0; e0 < P.E; e0 += 32) {
+        const int e = e0 + lane;
+        const bool live = e < P.E && s_mcnt[e] > 0;
+        const unsigned m = __ballot_sync(0xffffffffu, live);
+        if (live) s_live[base + __popc(m & ((1u << lane) - 1u))] = e;
+        base += __popc(m);
+      }
+      if (lane == 0) s_nlive = base;
+    }
+    __syncthreads();
+  }
+  auto skipped = [&](int) -> bool { return false; };
+  auto expert_of = [&](int tile) -> int {   // grouped bank: the expert of list tile `tile`
+    if constexpr (MOE) return s_live[tile / tpe];
+    return 0;
   };
+  auto items_of = [&](int p) -> int { return MOE ? s_nlive * tpe * P.ph[p].ks : P.ph[p].T; };
   auto range = [&](int p, int& beg, int& end) {
-    beg = item_begin(cta, G, P.ph[p].T);
-    end = item_begin(cta + 1, G, P.ph[p].T);
+    beg = item_begin(cta, G, items_of(p));
+    end = item_begin(cta + 1, G, items_of(p));
   };
   constexpr unsigned FULL = 0xffffffffu;
 
@@ -451,15 +475,34 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
             stop = true;
             break;
           }
+          const int row0 = MOE ? expert_of(tile) * P.job[j].rows + (tile % tpe) * TC_BM
+                               : (tile - P.job[j].tile0) * TC_BM;
+          uint8_t* st = wring + s * PS_W_BYTES;
+          const PsJob& J = P.job[j];
+          if (J.praw) {
+            // the step's 16 bytes of pairs of each of the 128 rows, 8 bytes per copy;
+            // the barrier tracks the copies (each lane's arrive counts itself in and
+            // out), before the arrive that completes its count is made below
+#pragma unroll
+            for (int i = 0; i < TC_BM / 32; ++i) {
+              const int rr = lane + 32 * i;
+              if (row0 + rr < J.prows) {
+                const uint32_t* src = J.praw + (size_t)(row0 + rr) * J.pstride + k * (TC_BK / 32);
+                const uint32_t dst = tc::smem_addr(st + PS_CODES_BYTES + rr * 16);
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst + 8), "l"(src + 2) : "memory");
+              }
+            }
+            asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar(FULL_W + s)) : "memory");
+            __syncwarp();
+          }
           if (tc::elect_one()) {
             if (MOE && (k == 0 || it == beg)) PTRACE(wtile, 0);
-            const int row0 = MOE ? (tile / tpe) * P.job[j].rows + (tile % tpe) * TC_BM
-                                 : (tile - P.job[j].tile0) * TC_BM;
-            uint8_t* st = wring + s * PS_W_BYTES;
-            tc::mbar_expect_tx(bar(FULL_W + s), PS_W_BYTES);
-            tc::tma_load_2d_hint(tc::smem_addr(st), &P.job[j].cmap, k * TC_BK, row0, bar(FULL_W + s), evict_first);
-            tc::tma_load_2d_hint(tc::smem_addr(st + PS_CODES_BYTES), &P.job[j].pmap, k * (TC_BK / 32), row0,
-                                 bar(FULL_W + s), evict_first);
+            tc::mbar_expect_tx(bar(FULL_W + s), J.praw ? PS_CODES_BYTES : PS_W_BYTES);
+            tc::tma_load_2d_hint(tc::smem_addr(st), &J.cmap, k * TC_BK, row0, bar(FULL_W + s), evict_first);
+            if (!J.praw)
+              tc::tma_load_2d_hint(tc::smem_addr(st + PS_CODES_BYTES), &J.pmap, k * (TC_BK / 32), row0,
+                                   bar(FULL_W + s), evict_first);
           }
           __syncwarp();
           ++issued;
@@ -511,7 +554,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
             uint8_t* st = xring + s * xst_bytes;
             if constexpr (MOE) {
               // the expert's entries only, in boxes of 16 rows (the MMA's N follows)
-              const int e = tile / tpe, xrow = s_moff[e], nbox = (s_mcnt[e] + 15) >> 4;
+              const int e = expert_of(tile), xrow = s_moff[e], nbox = (s_mcnt[e] + 15) >> 4;
               tc::mbar_expect_tx(bar(FULL_X + s), (uint32_t)(nbox * 2 * 16 * 128));
               for (int i = 0; i < nbox; ++i) {
                 tc::tma_load_2d(tc::smem_addr(st + i * 16 * 128), xm, k * TC_BK, xrow + 16 * i, bar(FULL_X + s));
@@ -567,7 +610,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
         const uint64_t b0 = tc::sdesc_sw128(tc::smem_addr(xring + sx * xst_bytes));
         const uint32_t a_t = tmem + 2 * PS_ACC_COLS + a * PS_A_COLS;
         uint32_t id = idesc;
-        if constexpr (MOE) id = tc::idesc_f16_f32(TC_BM, 16 * ((s_mcnt[tile / tpe] + 15) >> 4));   // N: the entries
+        if constexpr (MOE) id = tc::idesc_f16_f32(TC_BM, 16 * ((s_mcnt[expert_of(tile)] + 15) >> 4));   // N: the entries
         if (tc::elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < TC_BK / 16; ++kk) {
@@ -774,7 +817,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
         int nv = nvec;
         if constexpr (MOE) {
           // the tile's expert: its entries' input scales and output rows
-          const int e = tile / tpe;
+          const int e = expert_of(tile);
           epi_bar();   // every thread is done with the previous tile's tables
           if (et < 64) {
             const bool live = et < s_mcnt[e];
@@ -790,8 +833,8 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
         if (!epi_all(ok)) { stop = true; break; }
         tc::fence_after_sync();
         const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + t * PS_ACC_COLS;
-        const int c_first = whole ? cta : cta_of_item(tile * F.ks, G, F.T);
-        const int c_last = whole ? cta : cta_of_item(tile_end - 1, G, F.T);
+        const int c_first = whole ? cta : cta_of_item(tile * F.ks, G, items_of(p));
+        const int c_last = whole ? cta : cta_of_item(tile_end - 1, G, items_of(p));
         const bool contributor = cta != c_first;
         // accumulator row r, scaled, into this block's partial (a contributor) or the
         // shared transposed tile; layout [position][128 rows] in both
@@ -833,7 +876,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
           }
           if (!epi_all(okc)) { stop = true; break; }
           for (int cc = c_first + 1; cc <= c_last; ++cc) {
-            const int ft = item_begin(cc, G, F.T) / F.ks;
+            const int ft = item_begin(cc, G, items_of(p)) / F.ks;
             const float4* pc = reinterpret_cast<const float4*>(
                 P.partials + (((size_t)par * G + cc) * P.maxseg + (tile - ft)) * Bp * TC_BM);
 #pragma unroll
@@ -950,20 +993,6 @@ __global__ void __launch_bounds__(256) pass_input_kernel(const float* __restrict
   }
 }
 
-// (scale, offset) rows of a bank whose row of pairs is not a multiple of 16 bytes,
-// copied into rows of `pc` pairs (the tail zero) for the tensor copies; experts
-// without entries are left out.
-__global__ void __launch_bounds__(256) params_pad_kernel(const uint32_t* __restrict__ src, int rows, int c32, int pc,
-                                                         const int32_t* __restrict__ cnt, uint32_t* __restrict__ dst) {
-  // a warp per row, lanes along the row
-  const int e = blockIdx.y;
-  if (cnt[e] <= 0) return;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int r = blockIdx.x * 8 + warp; r < rows; r += gridDim.x * 8) {
-    const size_t row = (size_t)e * rows + r;
-    for (int c = lane; c < pc; c += 32) dst[row * pc + c] = c < c32 ? src[row * c32 + c] : 0u;
-  }
-}
 
 // The gathered input of a grouped expert bank: row i = x[ent[i] / xdiv] in binary16
 // with a power-of-two scale (xinv[i] its inverse), one block per row.  Block 0 also
@@ -1083,6 +1112,7 @@ struct HostPhase {
   float* tap;
   int moe_E;                 // > 0: job 0 is a grouped bank of moe_E experts
   int pcols;                 // (scale, offset) pairs per row of the params (0: K / 32)
+  bool praw;                 // params rows not a multiple of 16 bytes: copied by cp.async
   int xrows;                 // rows of the input buffer when more than the positions (grouped bank)
 };
 
@@ -1201,9 +1231,12 @@ int launch_phases(const HostPhase* hp, int nph, const float* x0, const float* ga
       const uint64_t pc = H.pcols > 0 ? (uint64_t)H.pcols : (uint64_t)(H.K / 32);
       if (!encode_2d(&D.cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, J.codes, H.K, mrows, (uint64_t)H.K, TC_BK, TC_BM,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
-          !encode_2d(&D.pmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, J.params, pc, mrows, (uint64_t)pc * 4, TC_BK / 32, TC_BM,
-                     CU_TENSOR_MAP_SWIZZLE_NONE))
+          (!H.praw && !encode_2d(&D.pmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, J.params, pc, mrows, (uint64_t)pc * 4,
+                                 TC_BK / 32, TC_BM, CU_TENSOR_MAP_SWIZZLE_NONE)))
         return set_error(PGQ_ECUDA, "prefill: tensor map of phase %d matrix %d could not be encoded", i, j);
+      D.praw = H.praw ? reinterpret_cast<const uint32_t*>(J.params) : nullptr;
+      D.pstride = (int)pc;
+      D.prows = (int)mrows;
       D.y = J.y;
       D.residual = J.residual;
       D.rows = J.rows;
@@ -1357,7 +1390,6 @@ int launch_prefill(const PrefillJob* jobs, int njobs, const float* X, int cols, 
 }
 
 // (scale, offset) pairs per row for the tensor copies: a multiple of 4 (16 bytes)
-static int padded_pairs(int cols) { return (cols / 32 + 3) / 4 * 4; }
 
 size_t moe_bank_tc_workspace_bytes(int E, int rows, int cols, int nent, const DeviceInfo& dev) {
   HostPhase h{};
@@ -1367,34 +1399,19 @@ size_t moe_bank_tc_workspace_bytes(int E, int rows, int cols, int nent, const De
   h.stats_job = -1;
   h.moe_E = E;
   h.xrows = nent;
-  size_t pad = 0;
-  if (padded_pairs(cols) != cols / 32) pad = ((size_t)E * rows * padded_pairs(cols) * 4 + 255) / 256 * 256;
-  return make_plan(&h, 1, 64, dev).total + pad;
+  return make_plan(&h, 1, 64, dev).total;
 }
 
 int launch_moe_bank_tc(const MoeBankArgs& a, void* ws, size_t ws_bytes, const DeviceInfo& dev, cudaStream_t st) {
-  // the tensor copies need 16-byte row strides of codes (and of the pairs, padded
-  // below when they are not)
+  // the tensor copies need 16-byte row strides of codes (pairs whose rows are not
+  // go by 8-byte copies)
   if (a.cols % 32 != 0 || a.cols % 16 != 0 || a.E > PS_MOE_EMAX || a.nentries < 1 || !aligned16(a.codes) ||
       !aligned16(a.params) || !aligned16(a.x) || !aligned16(a.y) || a.rows % 4 != 0)
     return PGQ_EUNSUPPORTED;
-  const int pc = padded_pairs(a.cols);
-  const uint16_t* params = a.params;
-  size_t gemm_bytes = ws_bytes;
-  if (pc != a.cols / 32) {
-    // padded pairs at the end of the workspace
-    const size_t pad = ((size_t)a.E * a.rows * pc * 4 + 255) / 256 * 256;
-    if (ws_bytes < pad) return set_error(PGQ_EWORKSPACE, "moe bank: workspace too small");
-    gemm_bytes = (ws_bytes - pad) / 256 * 256;
-    uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + gemm_bytes);
-    params_pad_kernel<<<dim3(64, a.E), 256, 0, st>>>(reinterpret_cast<const uint32_t*>(a.params), a.rows, a.cols / 32,
-                                                    pc, a.counts, dst);
-    if (cudaError_t e = cudaGetLastError(); e != cudaSuccess) return cuda_status(e);
-    params = reinterpret_cast<const uint16_t*>(dst);
-  }
   HostPhase h{};
-  h.pcols = pc;
-  h.job[0] = PrefillJob{a.codes, params, a.rows, a.y, nullptr, a.epilogue};
+  // (scale, offset) rows that are not a multiple of 16 bytes go by 8-byte copies
+  h.praw = (a.cols / 32) % 4 != 0;
+  h.job[0] = PrefillJob{a.codes, a.params, a.rows, a.y, nullptr, a.epilogue};
   h.njobs = 1;
   h.K = a.cols;
   h.xk = 0;
@@ -1403,7 +1420,7 @@ int launch_moe_bank_tc(const MoeBankArgs& a, void* ws, size_t ws_bytes, const De
   h.xrows = a.nentries;
   const int xrows = a.xdiv > 1 ? (a.nentries + a.xdiv - 1) / a.xdiv : a.nentries;
   const MoeSpec m{a.E, a.nentries, a.counts, a.offsets, a.entries, a.x, xrows, a.xdiv};
-  return launch_phases(&h, 1, nullptr, nullptr, nullptr, 0.f, 64, ws, gemm_bytes, 0, dev, st, &m);
+  return launch_phases(&h, 1, nullptr, nullptr, nullptr, 0.f, 64, ws, ws_bytes, 0, dev, st, &m);
 }
 
 int launch_prefill_pass(const pgq_q8_layer* layers, int L, float* h, int B, const float* gamma1,
