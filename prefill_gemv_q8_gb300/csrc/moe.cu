@@ -24,6 +24,7 @@ namespace pgq {
 // against the staged positions, then a butterfly per position (fixed order).
 constexpr int RT_WARPS = 8;
 constexpr int RT_POS = 8;
+constexpr int RT_UNROLL = 7;   // router row float4 per lane loaded ahead (2688 columns: 21 = 3 rounds)
 
 __global__ void __launch_bounds__(RT_WARPS * 32)
 router_kernel(const float* __restrict__ R, const float* __restrict__ n, int B, int E, int cols,
@@ -36,20 +37,39 @@ router_kernel(const float* __restrict__ R, const float* __restrict__ n, int B, i
   const int c4n = cols >> 2;
   const float4* n4 = reinterpret_cast<const float4*>(n + (size_t)b0 * cols);
   float4* xs4 = reinterpret_cast<float4*>(xs);
-  for (int i = threadIdx.x; i < nb * c4n; i += blockDim.x) xs4[i] = n4[i];
-  __syncthreads();
-  if (e >= E) return;
-  const float4* r4 = reinterpret_cast<const float4*>(R + (size_t)e * cols);
+  // the positions, by asynchronous 16-byte copies all in flight at once (one trip to
+  // memory rather than one per loop iteration)
+  for (int i = threadIdx.x; i < nb * c4n; i += blockDim.x)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(xs4 + i)),
+                 "l"(n4 + i)
+                 : "memory");
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  // meanwhile this warp's router row, RT_UNROLL float4 per lane at a time in registers
+  const float4* r4 = reinterpret_cast<const float4*>(R + (size_t)min(e, E - 1) * cols);
   float acc[RT_POS];
 #pragma unroll
   for (int b = 0; b < RT_POS; ++b) acc[b] = 0.f;
-  for (int c = lane; c < c4n; c += 32) {
-    const float4 w = r4[c];
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+  if (e >= E) return;
+  for (int c0 = 0; c0 < c4n; c0 += 32 * RT_UNROLL) {
+    float4 w[RT_UNROLL];
 #pragma unroll
-    for (int b = 0; b < RT_POS; ++b) {
-      if (b < nb) {
-        const float4 x = xs4[b * c4n + c];
-        acc[b] = fmaf(w.x, x.x, fmaf(w.y, x.y, fmaf(w.z, x.z, fmaf(w.w, x.w, acc[b]))));
+    for (int u = 0; u < RT_UNROLL; ++u) {
+      const int c = c0 + u * 32 + lane;
+      w[u] = c < c4n ? __ldg(r4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < RT_UNROLL; ++u) {
+      const int c = c0 + u * 32 + lane;
+      if (c < c4n) {
+#pragma unroll
+        for (int b = 0; b < RT_POS; ++b) {
+          if (b < nb) {
+            const float4 x = xs4[b * c4n + c];
+            acc[b] = fmaf(w[u].x, x.x, fmaf(w[u].y, x.y, fmaf(w[u].z, x.z, fmaf(w[u].w, x.w, acc[b]))));
+          }
+        }
       }
     }
   }

@@ -52,7 +52,7 @@ constexpr int PS_EPI_WARP0 = 10;   // warps 10..13
 constexpr int PS_XP_WARP = 14;     // input-slice producer
 constexpr int PS_NA = 4;           // A buffers in tensor memory
 constexpr int PS_WST_MAX = 10;     // weight ring stages (at most; set by the shared memory left)
-constexpr int PS_XST = 3;          // input ring stages
+constexpr int PS_XST = 3;          // input ring stages (4-6 measured no faster)
 constexpr int PS_CODES_BYTES = TC_BM * TC_BK;                 // 16 KB
 constexpr int PS_PARAMS_BYTES = TC_BM * 16;                   // 4 (scale, offset) pairs per row
 constexpr int PS_W_BYTES = PS_CODES_BYTES + PS_PARAMS_BYTES;  // 18 KB, a multiple of 1 KB
