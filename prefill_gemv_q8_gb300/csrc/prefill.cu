@@ -498,6 +498,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
           }
           if (tc::elect_one()) {
             if (MOE && (k == 0 || it == beg)) PTRACE(wtile, 0);
+            if (!MOE && it == beg) PTRACE(p, 0);
             tc::mbar_expect_tx(bar(FULL_W + s), J.praw ? PS_CODES_BYTES : PS_W_BYTES);
             tc::tma_load_2d_hint(tc::smem_addr(st), &J.cmap, k * TC_BK, row0, bar(FULL_W + s), evict_first);
             if (!J.praw)
@@ -538,6 +539,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
         // the phase's input is complete once every block wrote its slice; the copies
         // (async proxy) then read what the blocks wrote (generic proxy)
         if (!__all_sync(FULL, W.count(P.prep_done + p, (unsigned)G))) break;
+        if (!MOE && lane == 0) PTRACE(p, 1);
         asm volatile("fence.proxy.async.global;" ::: "memory");
       }
       int beg, end;
@@ -622,6 +624,8 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
           if (last) tc::mma_commit(bar(ACCF + t));
           if (MOE && first) PTRACE(mtile, 4);
           if (MOE && last) PTRACE(mtile, 5);
+          if (!MOE && it == beg) PTRACE(p, 2);
+          if (!MOE && it == end - 1) PTRACE(p, 3);
         }
         __syncwarp();
         any = true;
@@ -713,7 +717,9 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
     auto make_input = [&](int p) -> bool {
       const PsPhase& F = P.ph[p];
       bool ok = true;
+      if (!MOE && et == 0) PTRACE(p, 4);
       if (et == 0) ok = W.count(P.done + (p - 1), (unsigned)P.ph[p - 1].ntiles);
+      if (!MOE && et == 0) PTRACE(p, 5);
       if (!epi_all(ok)) return false;
       const PsJob& S = P.job[F.src_job];
       const int nt = S.ntiles;
@@ -786,6 +792,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
       asm volatile("fence.proxy.async.global;" ::: "memory");
       epi_bar();
       if (et == 0) release_add(P.prep_done + p);
+      if (!MOE && et == 0) PTRACE(p, 6);
       return true;
     };
 
@@ -908,6 +915,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
                      P.stats + ((size_t)par * P.maxtiles + (tile - J.tile0)) * 64);
         epi_bar();   // the tile's stores are issued and the shared tile is free
         if (et == 0) release_add(P.done + p);
+        if (!MOE && et == 0) PTRACE(p, 7);
         if (MOE && et == 0) PTRACE(etile, 7);
         ++etile;
         it = seg_end;
