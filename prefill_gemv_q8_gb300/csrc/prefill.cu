@@ -729,7 +729,19 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
         float ss = 0.f, mx = 0.f;
         if (b < P.B) {
           const int lo = half ? nt / 2 : 0, hi = half ? nt : nt / 2;
-          for (int tt = lo; tt < hi; ++tt) {
+          // 4 loads in flight at a time, added in tile order as before
+          int tt = lo;
+          for (; tt + 4 <= hi; tt += 4) {
+            float2 v[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = __ldcg(P.stats + ((size_t)prev * P.maxtiles + tt + i) * 64 + b);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              ss += v[i].x;
+              mx = fmaxf(mx, v[i].y);
+            }
+          }
+          for (; tt < hi; ++tt) {
             const float2 v = __ldcg(P.stats + ((size_t)prev * P.maxtiles + tt) * 64 + b);
             ss += v.x;
             mx = fmaxf(mx, v.y);
@@ -751,34 +763,45 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
       const float* src = S.y;
       __half* xh = P.xh[F.xk];
       const int rb = et >> 1, cofs = (et & 1) * 16;
-      for (int sl = cta; sl * 32 < F.K; sl += G) {
-        const int col = sl * 32 + cofs;
-        if (rb < Bp) {
-          uint32_t hv[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-          if (rb < P.B) {
-            const float inv = s_inv[rb], sc = s_sc[rb];
-            const float4* y4 = reinterpret_cast<const float4*>(src + (size_t)rb * F.K + col);
-            float4 v[4];
+      // this block's slices, up to PS_SLB at a time with all their loads of y in flight
+      constexpr int PS_SLB = 2;
+      for (int sl0 = cta; sl0 * 32 < F.K; sl0 += PS_SLB * G) {
+        float4 v[PS_SLB][4];
+        const bool live = rb < P.B;
+        const float inv = live ? s_inv[rb] : 0.f, sc = live ? s_sc[rb] : 0.f;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) v[i] = __ldcg(y4 + i);
+        for (int q2 = 0; q2 < PS_SLB; ++q2) {
+          const int col = (sl0 + q2 * G) * 32 + cofs;
+          const bool in = live && col < F.K;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            v[q2][i] = in ? __ldcg(reinterpret_cast<const float4*>(src + (size_t)rb * F.K + col) + i)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int q2 = 0; q2 < PS_SLB; ++q2) {
+          const int col = (sl0 + q2 * G) * 32 + cofs;
+          if (rb >= Bp || col >= F.K) continue;
+          uint32_t hv[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+          if (live) {
             if (F.gamma) {
               const float4* g4 = reinterpret_cast<const float4*>(F.gamma + col);
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
                 const float4 g = g4[i];
-                v[i] = make_float4(g.x * (v[i].x * inv), g.y * (v[i].y * inv), g.z * (v[i].z * inv),
-                                   g.w * (v[i].w * inv));
+                v[q2][i] = make_float4(g.x * (v[q2][i].x * inv), g.y * (v[q2][i].y * inv), g.z * (v[q2][i].z * inv),
+                                       g.w * (v[q2][i].w * inv));
               }
               if (F.tap) {
                 float4* t4 = reinterpret_cast<float4*>(F.tap + (size_t)rb * F.K + col);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) t4[i] = v[i];
+                for (int i = 0; i < 4; ++i) t4[i] = v[q2][i];
               }
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const __half2 lo = __floats2half2_rn(v[i].x * sc, v[i].y * sc);
-              const __half2 hi = __floats2half2_rn(v[i].z * sc, v[i].w * sc);
+              const __half2 lo = __floats2half2_rn(v[q2][i].x * sc, v[q2][i].y * sc);
+              const __half2 hi = __floats2half2_rn(v[q2][i].z * sc, v[q2][i].w * sc);
               hv[2 * i] = *reinterpret_cast<const uint32_t*>(&lo);
               hv[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hi);
             }
