@@ -895,9 +895,12 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
           continue;
         }
         if (!whole) {
-          // the owner: the other contributors' partials, one at a time through the
-          // shared buffer (each thread copies and adds its own float4 slots), in block
-          // order.  Blocks only wait for higher-numbered blocks, and the launch is
+          // the owner: the other contributors' partials, through the shared buffer (each
+          // thread copies and adds its own float4 slots), added in block order.  At the
+          // block's last segment of the phase the input ring is idle (the phase's MMAs
+          // are done, and the next phase's copies wait for every block's share of its
+          // input, this block's included), so two partials are in flight at a time
+          // there.  Blocks only wait for higher-numbered blocks, and the launch is
           // cooperative (all blocks resident), so the wait ends.
           bool okc = true;
           if (et == 0) {
@@ -905,26 +908,34 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
             if (okc) P.tile_cnt[(size_t)par * P.maxtiles + tile] = 0u;
           }
           if (!epi_all(okc)) { stop = true; break; }
-          for (int cc = c_first + 1; cc <= c_last; ++cc) {
-            const int ft = item_begin(cc, G, items_of(p)) / F.ks;
-            const float4* pc = reinterpret_cast<const float4*>(
-                P.partials + (((size_t)par * G + cc) * P.maxseg + (tile - ft)) * Bp * TC_BM);
+          const int nbuf = (seg_end == end) ? 2 : 1;
+          float4* const ring4 = reinterpret_cast<float4*>(xring);
+          for (int c0 = c_first + 1; c0 <= c_last; c0 += nbuf) {
+            for (int q2 = 0; q2 < nbuf && c0 + q2 <= c_last; ++q2) {
+              const int cc = c0 + q2;
+              const int ft = item_begin(cc, G, items_of(p)) / F.ks;
+              const float4* pc = reinterpret_cast<const float4*>(
+                  P.partials + (((size_t)par * G + cc) * P.maxseg + (tile - ft)) * Bp * TC_BM);
 #pragma unroll
-            for (int k = 0; k < PS_OUT_K; ++k) {
-              const int i = et + 128 * k;
-              if (i < nv)
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_addr(fix4 + i)), "l"(pc + i)
-                             : "memory");
+              for (int k = 0; k < PS_OUT_K; ++k) {
+                const int i = et + 128 * k;
+                if (i < nv)
+                  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_addr((q2 ? ring4 : fix4) + i)),
+                               "l"(pc + i)
+                               : "memory");
+              }
             }
             asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+            for (int q2 = 0; q2 < nbuf && c0 + q2 <= c_last; ++q2) {
 #pragma unroll
-            for (int k = 0; k < PS_OUT_K; ++k) {
-              const int i = et + 128 * k;
-              if (i < nv) {
-                const float4 u = fix4[i];
-                float4 s4 = acc4[i];
-                s4.x += u.x; s4.y += u.y; s4.z += u.z; s4.w += u.w;
-                acc4[i] = s4;
+              for (int k = 0; k < PS_OUT_K; ++k) {
+                const int i = et + 128 * k;
+                if (i < nv) {
+                  const float4 u = (q2 ? ring4 : fix4)[i];
+                  float4 s4 = acc4[i];
+                  s4.x += u.x; s4.y += u.y; s4.z += u.z; s4.w += u.w;
+                  acc4[i] = s4;
+                }
               }
             }
           }
