@@ -273,12 +273,15 @@ __device__ __forceinline__ __half2 s8pair_to_h2(uint32_t u_biased, uint32_t sel)
 // Writes a tile from the shared transposed tile acc4 ([b][128 rows] as float4):
 // y[b][row0 + c] = epilogue(acc[b][c]) for c < rows - row0, and (writeback) leaves
 // the final values in acc4.  Thread et takes float4 et, et+128, ... (at most 16); all
-// reads (shared tile, residual) of a pass are issued before its first store.
+// reads (shared tile, residual) of a pass are issued before its first store.  ROLL
+// keeps the passes a loop (less code to fetch: this runs once per tile, cold in the
+// instruction cache; measured faster for the grouped expert banks, slower for the
+// dense pass).
+template <bool ROLL>
 __device__ __forceinline__ void out_rows(float4* acc4, int nvec, int et, int epi, float* y, const float* res, int rows,
                                          int row0, bool vec_ok, bool writeback, const int* rowtab = nullptr) {
   if (vec_ok) {
-#pragma unroll
-    for (int h = 0; h < PS_OUT_P; ++h) {
+    auto pass = [&](int h) {
       float4 a[PS_OUT_H], q[PS_OUT_H];
 #pragma unroll
       for (int k = 0; k < PS_OUT_H; ++k) {
@@ -306,6 +309,13 @@ __device__ __forceinline__ void out_rows(float4* acc4, int nvec, int et, int epi
           if (writeback) acc4[i] = o;
         }
       }
+    };
+    if constexpr (ROLL) {
+#pragma unroll 1
+      for (int h = 0; h < PS_OUT_P; ++h) pass(h);
+    } else {
+#pragma unroll
+      for (int h = 0; h < PS_OUT_P; ++h) pass(h);
     }
   } else {
     // rows not a multiple of 4 or unaligned outputs: element by element
@@ -871,8 +881,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
         float* dst = contributor
                          ? P.partials + (((size_t)par * G + cta) * P.maxseg + (tile - first_tile)) * Bp * TC_BM
                          : s_acc;
-#pragma unroll
-        for (int c0 = 0; c0 < PS_ACC_COLS; c0 += 16) {
+        auto drain16 = [&](int c0) {
           if (c0 < Bp) {
             uint32_t u[16];
             tc::tmem_ld_32x32b_x16(ta + c0, u);
@@ -880,6 +889,13 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
 #pragma unroll
             for (int i = 0; i < 16; ++i) dst[(c0 + i) * TC_BM + r] = __uint_as_float(u[i]) * s_xinv[c0 + i];
           }
+        };
+        if constexpr (MOE) {   // a grouped bank: the loop rolled (see out_rows)
+#pragma unroll 1
+          for (int c0 = 0; c0 < PS_ACC_COLS; c0 += 16) drain16(c0);
+        } else {
+#pragma unroll
+          for (int c0 = 0; c0 < PS_ACC_COLS; c0 += 16) drain16(c0);
         }
         tc::fence_before_sync();
         __syncwarp();
@@ -927,8 +943,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
             }
             asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
             for (int q2 = 0; q2 < nbuf && c0 + q2 <= c_last; ++q2) {
-#pragma unroll
-              for (int k = 0; k < PS_OUT_K; ++k) {
+              auto add1 = [&](int k) {
                 const int i = et + 128 * k;
                 if (i < nv) {
                   const float4 u = (q2 ? ring4 : fix4)[i];
@@ -936,6 +951,13 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
                   s4.x += u.x; s4.y += u.y; s4.z += u.z; s4.w += u.w;
                   acc4[i] = s4;
                 }
+              };
+              if constexpr (MOE) {   // a grouped bank: the loop rolled (see out_rows)
+#pragma unroll 1
+                for (int k = 0; k < PS_OUT_K; ++k) add1(k);
+              } else {
+#pragma unroll
+                for (int k = 0; k < PS_OUT_K; ++k) add1(k);
               }
             }
           }
@@ -943,7 +965,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
         const bool vec_ok = ((rows & 3) == 0) && ((reinterpret_cast<uintptr_t>(J.y) & 15) == 0) &&
                             (J.epi != PGQ_EPI_ADD || (reinterpret_cast<uintptr_t>(J.residual) & 15) == 0);
         const bool stats = vec_ok && j == F.stats_job;
-        out_rows(acc4, nv, et, J.epi, J.y, J.residual, rows, row0, vec_ok, stats, MOE ? s_ent : nullptr);
+        out_rows<MOE>(acc4, nv, et, J.epi, J.y, J.residual, rows, row0, vec_ok, stats, MOE ? s_ent : nullptr);
         if (stats)
           tile_stats(acc4, nv, et, rows, row0, F.next_gamma,
                      P.stats + ((size_t)par * P.maxtiles + (tile - J.tile0)) * 64);
