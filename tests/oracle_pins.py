@@ -361,6 +361,66 @@ def pin_prefill_layer_composition():
     close(out["h2"], h1 + R.relu2(n2), rel=1e-14)
 
 
+def _scaled_slots(n, scales):
+    """Slot matrices that are the identity times a power of two (code 1 on the
+    diagonal, offset 0): exact in binary16, and distinct per slot, so a slot fed
+    the wrong input or the wrong matrix changes the result."""
+    eye = np.eye(n, dtype=np.int8)
+    mats = {}
+    for s, sc in scales.items():
+        par = np.zeros((n, n // 32, 2), np.float16)
+        par[..., 0] = sc
+        mats[s] = (eye, par)
+    return mats
+
+
+def _rms_closed(h, g, eps):
+    """RMSNorm from its definition, row by row: h / sqrt(mean(h²) + eps) · γ."""
+    h = np.atleast_2d(np.asarray(h, np.float64))
+    return np.stack([row / math.sqrt(float(np.mean(row * row)) + eps) * np.asarray(g, np.float64) for row in h])
+
+
+def _relu2_closed(v):
+    v = np.asarray(v, np.float64)
+    return np.where(v > 0, v * v, 0.0)
+
+
+SLOT_SCALES = {"q": 2.0, "k": 4.0, "v": 0.5, "o": 8.0, "up": 0.25, "down": 16.0}
+
+
+def pin_q8_decode_layer_slots():
+    """Decode layer wiring: q, k, v and up read n = rms(x)·γ, o reads its own input
+    x_o, down reads relu²(up); each slot's scale shows which matrix it used."""
+    n = 64
+    mats = _scaled_slots(n, SLOT_SCALES)
+    r = _rng(27)
+    x, x_o, g = r.standard_normal(n), r.standard_normal(n), r.uniform(0.5, 1.5, n)
+    out = R.q8_decode_layer(x, x_o, g, 1e-6, mats)
+    nrm = _rms_closed(x, g, 1e-6)
+    for s in ("q", "k", "v", "up"):
+        close(out[s], SLOT_SCALES[s] * nrm, rel=1e-13)
+    close(out["o"], SLOT_SCALES["o"] * np.atleast_2d(x_o), rel=1e-13)
+    close(out["down"], SLOT_SCALES["down"] * _relu2_closed(SLOT_SCALES["up"] * nrm), rel=1e-13)
+
+
+def pin_prefill_layer_slots():
+    """Prefill layer wiring with distinct slot scales: h1 = h + s_o·(s_q·n1),
+    n2 = rms(h1)·γ2, h2 = h1 + s_down·relu²(s_up·n2), and k, v = s_k·n1, s_v·n1."""
+    n = 64
+    mats = _scaled_slots(n, SLOT_SCALES)
+    r = _rng(28)
+    h = r.standard_normal((3, n))
+    g1, g2 = r.uniform(0.5, 1.5, n), r.uniform(0.5, 1.5, n)
+    out = R.prefill_layer(h, mats, g1, g2, 1e-6)
+    n1 = _rms_closed(h, g1, 1e-6)
+    for s in ("q", "k", "v"):
+        close(out[s], SLOT_SCALES[s] * n1, rel=1e-13)
+    h1 = h + SLOT_SCALES["o"] * (SLOT_SCALES["q"] * n1)
+    close(out["h1"], h1, rel=1e-13)
+    n2 = _rms_closed(h1, g2, 1e-6)
+    close(out["h2"], h1 + SLOT_SCALES["down"] * _relu2_closed(SLOT_SCALES["up"] * n2), rel=1e-12)
+
+
 def pin_moe_layer_composition():
     """Experts whose up and down are the identity scaled by (e+1): the MoE output for
     a position is Σ_s w_s·(e_s+1)²·relu²(n) (with up scale e+1 and down scale 1:

@@ -122,6 +122,46 @@ def _argmax_numpy(l):
     return np.argmax(np.atleast_2d(R.as_f64(l)), axis=1).astype(np.int32)
 
 
+_layer = {k: getattr(R, k) for k in ("q8_decode_layer", "prefill_layer", "moe_layer")}
+
+
+def _decode_o_reads_n(x, x_o, gamma, eps, mats, u_in=None):
+    n, _ = _orig["rmsnorm"](x, gamma, eps)
+    return _layer["q8_decode_layer"](x, n, gamma, eps, mats, u_in)
+
+
+def _decode_down_reads_up(x, x_o, gamma, eps, mats, u_in=None):
+    first = _layer["q8_decode_layer"](x, x_o, gamma, eps, mats)
+    return _layer["q8_decode_layer"](x, x_o, gamma, eps, mats, u_in=first["up"])
+
+
+def _decode_k_v_swapped(x, x_o, gamma, eps, mats, u_in=None):
+    m = dict(mats)
+    m["k"], m["v"] = mats["v"], mats["k"]
+    return _layer["q8_decode_layer"](x, x_o, gamma, eps, m, u_in)
+
+
+def _prefill_o_reads_n1(h, mats, gamma1, gamma2, eps, stage_in=None):
+    n1, _ = _orig["rmsnorm"](np.atleast_2d(np.asarray(h, np.float64)), gamma1, eps)
+    return _layer["prefill_layer"](h, mats, gamma1, gamma2, eps, stage_in={"q": n1})
+
+
+def _prefill_second_norm_reads_h(h, mats, gamma1, gamma2, eps, stage_in=None):
+    return _layer["prefill_layer"](h, mats, gamma1, gamma2, eps, stage_in={"h1": h})
+
+
+def _prefill_h2_from_h(h, mats, gamma1, gamma2, eps, stage_in=None):
+    out = _layer["prefill_layer"](h, mats, gamma1, gamma2, eps, stage_in)
+    out["h2"] = np.atleast_2d(np.asarray(h, np.float64)) + out["down"]
+    return out
+
+
+def _moe_residual_from_n(h, gamma1, gamma2, eps, router, experts, k, renorm=False, stage_in=None):
+    out = _layer["moe_layer"](h, gamma1, gamma2, eps, router, experts, k, renorm, stage_in)
+    out["h"] = out["n"] + out["m"]
+    return out
+
+
 MUTATIONS = {
     "dequant drops the offset": ("dequant_q8", _dequant_no_offset),
     "offset read as a zero-point": ("dequant_q8", _dequant_zero_point),
@@ -141,6 +181,13 @@ MUTATIONS = {
     "combine with slots reversed": ("combine", _combine_slot_reversed),
     "argmax tie to the last index": ("argmax", _argmax_last),
     "argmax picks NaN / ignores the floor": ("argmax", _argmax_numpy),
+    "decode: o reads n instead of its own input": ("q8_decode_layer", _decode_o_reads_n),
+    "decode: down reads up instead of relu²(up)": ("q8_decode_layer", _decode_down_reads_up),
+    "decode: k and v matrices swapped": ("q8_decode_layer", _decode_k_v_swapped),
+    "prefill: o reads n1 instead of q": ("prefill_layer", _prefill_o_reads_n1),
+    "prefill: second norm reads h instead of h1": ("prefill_layer", _prefill_second_norm_reads_h),
+    "prefill: h2 adds the down output to h": ("prefill_layer", _prefill_h2_from_h),
+    "moe: residual added to the normalised input": ("moe_layer", _moe_residual_from_n),
 }
 
 
