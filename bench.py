@@ -467,6 +467,21 @@ def cpu_baseline_q8(W, target_s=15.0):
 
 
 # ------------------------------------------------------------------ main
+def max_over_ranks(torch, dist, vals, device):
+    """Every rank's timings, after a barrier, replaced by their maximum over the ranks
+    (the whole job is as fast as its slowest rank); one rank: the values as they are."""
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.barrier()
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_gbs(world, bytes_per_step, ms_per_step):
+    """Whole-job weight GB/s: every rank streams bytes_per_step per step."""
+    return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -525,13 +540,9 @@ def main():
     clocks = clk.summary()
     e2e_ms = time_e2e(torch, W, args.steps, args.warmup)
     Wcpu = W
-    t = torch.tensor([total_ms, e2e_ms], device="cuda")
-    if dist:
-        dist.barrier()
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms, e2e_ms = float(t[0]), float(t[1])
+    total_ms, e2e_ms = max_over_ranks(torch, dist, [total_ms, e2e_ms], "cuda")
     ms_step = total_ms / args.steps
-    value = world * W.step_bytes / (ms_step * 1e-3) / 1e9
+    value = job_gbs(world, W.step_bytes, ms_step)
     achieved = W.k1_bytes / (k1_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -549,7 +560,7 @@ def main():
                      "traffic": ncu_traffic("gemv_q8_layer_multi", Q8_FILES),
                      "algorithmic_bytes_per_launch": W.k1_bytes, "avg_launch_ms": round(k1_ms, 5),
                      "down_launch_ms": round(k2_ms, 5)},
-        "e2e": {"value": round(world * W.step_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+        "e2e": {"value": round(job_gbs(world, W.step_bytes, e2e_ms), 1), "unit": "GB/s",
                 "h2d_bytes_per_step": W.h2d, "d2h_bytes_per_step": W.d2h, "ms_per_step": round(e2e_ms, 5)},
         "gpu_launches": W.launches_per_step * args.steps,
         "clocks": clocks,
