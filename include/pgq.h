@@ -250,7 +250,11 @@ int pgq_prefill_status(const void* workspace, void* stream);
  * 256-byte aligned.  After the call the workspace holds the last layer's n1, q, k,
  * v, h1 (= h + W_o·q), n2 and u at the byte offsets pgq_q8_prefill_pass_layout()
  * reports (7 entries).
- * Six kernel launches per layer plus the binary16 input conversions. */
+ * Two launches per group of up to 8 layers: a small kernel that makes the first
+ * layer's binary16 input, then one persistent cooperative launch of all the group's
+ * projections (its blocks pass each projection's output to the next through device
+ * counters).  Returns PGQ_ETIMEOUT through pgq_prefill_status() if a bounded
+ * device-side wait expired. */
 size_t pgq_q8_prefill_pass_workspace_bytes(int hidden, int kv, int inter, int B);
 int pgq_q8_prefill_pass_layout(int hidden, int kv, int inter, int B, size_t offsets[7]);
 int pgq_q8_prefill_pass(const pgq_q8_layer* layers, int L, float* h, int B, const float* gamma1,
