@@ -112,3 +112,105 @@ def test_no_device_no_fallback(L):
     assert L.pgq_add_rmsnorm(p, None, q, 1e-6, 1, 64, C.c_void_p(FAKE * 3), None, None) == pgq.ENODEV
     assert L.pgq_gemv_f16(q, 8, 64, p, 1, None, 1e-6, C.c_void_p(FAKE * 3), 0, None, None) == pgq.ENODEV
     assert L.pgq_device_check() == pgq.ENODEV
+
+
+# The entry points of the decode layer, the prefill pass and the MoE stages reject bad
+# arguments before they look for a device.  Run where there is no GPU only, so that a
+# call that got past its checks could never reach one with these made-up addresses.
+no_gpu = pytest.mark.skipif(cuda_ok(), reason="made-up device addresses: only where no GPU exists")
+
+
+def _p(k):
+    return C.c_void_p(FAKE * k)
+
+
+@no_gpu
+def test_prefill_q8_arguments_rejected(L):
+    X, ws = _p(1), _p(2)
+    job = pgq.Q8Job(_p(3).value, _p(4).value, 256, 0, _p(5).value, pgq.EPI_NONE, None)
+    jobs = (pgq.Q8Job * 5)(*([job] * 5))
+    call = lambda **kw: L.pgq_prefill_q8(kw.get("jobs", jobs), kw.get("njobs", 1), kw.get("X", X), kw.get("cols", 512),
+                                         kw.get("B", 16), kw.get("ws", ws), 1 << 30, None)
+    assert call(jobs=None) == pgq.EINVAL
+    assert call(njobs=0) == pgq.EINVAL
+    assert call(njobs=5) == pgq.EINVAL            # at most 4 matrices reading one X
+    assert call(B=0) == pgq.EINVAL
+    assert call(B=65) == pgq.EINVAL
+    assert call(cols=480) == pgq.EUNSUPPORTED      # cols % 128
+    assert call(X=C.c_void_p(FAKE + 4)) == pgq.EALIGN
+    assert call(ws=C.c_void_p(FAKE * 2 + 128)) == pgq.EWORKSPACE
+    bad = (pgq.Q8Job * 1)(pgq.Q8Job(_p(3).value, _p(4).value, 0, 0, _p(5).value, pgq.EPI_NONE, None))
+    assert call(jobs=bad) == pgq.EINVAL            # rows 0
+    bad = (pgq.Q8Job * 1)(pgq.Q8Job(_p(3).value, _p(4).value, 256, 0, _p(5).value, pgq.EPI_ADD, None))
+    assert call(jobs=bad) == pgq.EINVAL            # add without a residual
+    bad = (pgq.Q8Job * 1)(pgq.Q8Job(_p(3).value, _p(4).value, 256, 0, X.value + 64, pgq.EPI_NONE, None))
+    assert call(jobs=bad) == pgq.EINVAL            # output overlaps X
+    assert L.pgq_prefill_q8_workspace_bytes((C.c_int * 1)(256), 1, 512, 65) == 0
+
+
+@no_gpu
+def test_prefill_pass_arguments_rejected(L):
+    def layer(h, kv, i):
+        m = pgq.Q8Matrix(_p(3).value, _p(4).value)
+        return pgq.Q8Layer(m, m, m, m, m, m, h, kv, i)
+    two = (pgq.Q8Layer * 2)(layer(512, 128, 1024), layer(512, 128, 1024))
+    h, g1, g2, ws = _p(1), _p(5), _p(6), _p(7)
+    call = lambda **kw: L.pgq_q8_prefill_pass(kw.get("layers", two), kw.get("L", 2), kw.get("h", h), kw.get("B", 8),
+                                              g1, g2, 1e-6, kw.get("ws", ws), 1 << 30, None)
+    assert call(L=0) == pgq.EINVAL
+    assert call(B=65) == pgq.EINVAL
+    assert call(h=C.c_void_p(FAKE + 8)) == pgq.EALIGN
+    assert call(layers=(pgq.Q8Layer * 2)(layer(512, 128, 1024), layer(512, 128, 2048))) == pgq.EINVAL
+    assert call(layers=(pgq.Q8Layer * 2)(layer(576, 128, 1024), layer(576, 128, 1024))) == pgq.EUNSUPPORTED
+    assert call(ws=C.c_void_p(FAKE * 7 + 64)) == pgq.EWORKSPACE
+    offs = (C.c_size_t * 7)()
+    assert L.pgq_q8_prefill_pass_layout(512, 128, 1024, 0, offs) == pgq.EINVAL
+    assert L.pgq_q8_prefill_pass_workspace_bytes(512, 128, 1024, 65) == 0
+    assert L.pgq_q8_prefill_pass_layout(512, 128, 1024, 8, offs) == pgq.OK
+    assert list(offs) == sorted(offs) and all(o % 256 == 0 for o in offs)
+
+
+@no_gpu
+def test_decode_layer_and_multi_arguments_rejected(L):
+    m = pgq.Q8Matrix(_p(3).value, _p(4).value)
+    lay = pgq.Q8Layer(m, m, m, m, m, m, 512, 128, 1024)
+    outs = [_p(10 + i) for i in range(6)]
+    assert L.pgq_q8_decode_layer_ex(C.byref(lay), _p(1), _p(2), _p(5), 1e-6, *outs, 2, None) == pgq.EINVAL  # flags
+    assert L.pgq_q8_decode_layer(None, _p(1), _p(2), _p(5), 1e-6, *outs, None) == pgq.EINVAL
+    job = pgq.Q8Job(_p(3).value, _p(4).value, 64, 0, _p(5).value, pgq.EPI_NONE, None)
+    jobs = (pgq.Q8Job * 9)(*([job] * 9))
+    ins = (pgq.Input * 5)(*([pgq.Input(_p(1).value, None)] * 5))
+    assert L.pgq_gemv_q8_multi(jobs, 9, ins, 1, 512, 1, 1e-6, None) == pgq.EINVAL          # > 8 jobs
+    assert L.pgq_gemv_q8_multi(jobs, 1, ins, 5, 512, 1, 1e-6, None) == pgq.EINVAL          # > 4 inputs
+    assert L.pgq_gemv_q8_multi(jobs, 1, ins, 4, 16384, 1, 1e-6, None) == pgq.EUNSUPPORTED  # staged values
+    bad = (pgq.Q8Job * 1)(pgq.Q8Job(_p(3).value, _p(4).value, 64, 3, _p(5).value, pgq.EPI_NONE, None))
+    assert L.pgq_gemv_q8_multi(bad, 1, ins, 1, 512, 1, 1e-6, None) == pgq.EINVAL          # input index
+
+
+@no_gpu
+def test_moe_arguments_rejected(L):
+    a, b, c = _p(1), _p(2), _p(3)
+    assert L.pgq_moe_router(a, 0, 64, b, 4, c, None) == pgq.EINVAL
+    assert L.pgq_moe_router(a, 8, 66, b, 4, c, None) == pgq.EINVAL                  # cols % 4
+    assert L.pgq_moe_router(a, 8, 64, C.c_void_p(FAKE * 2 + 4), 4, c, None) == pgq.EALIGN
+    assert L.pgq_moe_router(a, 8, 64, b, 4, C.c_void_p(FAKE * 2 + 64), None) == pgq.EINVAL  # logits overlap n
+    assert L.pgq_moe_route_topk(a, 4, 257, 6, 0, b, c, None) == pgq.EINVAL          # E > 256
+    assert L.pgq_moe_route_topk(a, 4, 8, 9, 0, b, c, None) == pgq.EINVAL            # k > E
+    assert L.pgq_moe_route_topk(a, 4, 64, 33, 0, b, c, None) == pgq.EINVAL          # k > 32
+    assert L.pgq_moe_group_gather(a, 64, 6, 6000, b, c, _p(4), None, 0, 1, None, None) == pgq.EUNSUPPORTED
+    assert L.pgq_moe_group_gather(a, 4, 2, 8, b, c, _p(4), None, 0, 1, _p(5), None) == pgq.EINVAL  # gather, no x
+    assert L.pgq_moe_experts_q8(a, b, 8, 64, 6176, c, _p(4), _p(5), 8, _p(6), 1, _p(7), 0, None) == pgq.EUNSUPPORTED
+    assert L.pgq_moe_experts_q8(a, b, 8, 64, 512, c, _p(4), _p(5), 8, _p(6), 1, _p(7), pgq.EPI_ADD,
+                                None) == pgq.EINVAL
+    assert L.pgq_moe_combine_rmsnorm(a, None, b, c, 2, _p(4), 1e-6, 2, 66, _p(5), None, None) == pgq.EINVAL  # n % 4
+    assert L.pgq_moe_combine_rmsnorm(a, None, b, c, 2, _p(4), 1e-6, 2, 64, C.c_void_p(FAKE + 256), None,
+                                     None) == pgq.EINVAL                                # y overlaps h
+    lay = pgq.MoeLayer(_p(1).value, _p(2).value, _p(3).value, _p(4).value, _p(5).value, 8, 9, 256, 128, 0)
+    assert L.pgq_moe_layer_workspace_bytes(C.byref(lay), 16) == 0                   # k > E
+    lay.k = 2
+    need = L.pgq_moe_layer_workspace_bytes(C.byref(lay), 16)
+    assert need > 0
+    assert L.pgq_moe_prefill_layer(C.byref(lay), _p(6), 16, _p(7), _p(8), 1e-6, _p(9), _p(10), need - 256,
+                                   None) == pgq.EWORKSPACE
+    assert L.pgq_moe_prefill_layer(C.byref(lay), _p(6), 65, _p(7), _p(8), 1e-6, _p(9), _p(10), need,
+                                   None) == pgq.EINVAL
