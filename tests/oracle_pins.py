@@ -423,8 +423,9 @@ def pin_prefill_layer_slots():
 
 def pin_moe_layer_composition():
     """Experts whose up and down are the identity scaled by (e+1): the MoE output for
-    a position is Σ_s w_s·(e_s+1)²·relu²(n) (with up scale e+1 and down scale 1:
-    eo = relu²((e+1)·n))."""
+    a position is Σ_s w_s·relu²((e_s+1)·n) (up scale e+1, down scale 1), and the
+    layer's output is the second norm of the updated residual, y = rms(h + m)·γ2,
+    with γ1 ≠ γ2 so that a norm taking the wrong weight (or none) is seen."""
     n, E, k, B = 32, 5, 2, 4
     eye = np.eye(n, dtype=np.int8)
     experts = []
@@ -436,18 +437,22 @@ def pin_moe_layer_composition():
         experts.append((eye, pu, eye, pd))
     r = _rng(25)
     h = r.standard_normal((B, n))
-    g1, g2 = np.ones(n), np.ones(n)
+    g1, g2 = r.uniform(0.5, 1.5, n), r.uniform(0.5, 1.5, n)
     router = r.standard_normal((E, n))
     out = R.moe_layer(h, g1, g2, 1e-6, router, experts, k)
-    nrm, _ = R.rmsnorm(h, g1, 1e-6)
+    nrm = _rms_closed(h, g1, 1e-6)
+    close(out["n"], nrm, rel=1e-13)
     logits = nrm @ router.T
     sel, w = R.route(logits, k)
     m = np.zeros_like(h)
     for b in range(B):
         for s in range(k):
-            m[b] += w[b, s] * R.relu2((sel[b, s] + 1) * nrm[b])
+            m[b] += w[b, s] * _relu2_closed((sel[b, s] + 1) * nrm[b])
     close(out["m"], m, rel=1e-12, abs_=1e-15)
     close(out["h"], h + m, rel=1e-13)
+    hn = h + m
+    close(out["y"], _rms_closed(hn, g2, 1e-6), rel=1e-12)
+    close(out["inv2"], 1.0 / np.sqrt(np.mean(hn * hn, axis=1) + 1e-6), rel=1e-13)
 
 
 def pin_vocab_head_ties():

@@ -162,6 +162,16 @@ def _moe_residual_from_n(h, gamma1, gamma2, eps, router, experts, k, renorm=Fals
     return out
 
 
+def _moe_second_norm_gamma1(h, gamma1, gamma2, eps, router, experts, k, renorm=False, stage_in=None):
+    return _layer["moe_layer"](h, gamma1, gamma1, eps, router, experts, k, renorm, stage_in)
+
+
+def _moe_second_norm_no_gamma(h, gamma1, gamma2, eps, router, experts, k, renorm=False, stage_in=None):
+    out = _layer["moe_layer"](h, gamma1, gamma2, eps, router, experts, k, renorm, stage_in)
+    out["y"] = out["y"] / np.asarray(gamma2, np.float64)[None, :]
+    return out
+
+
 MUTATIONS = {
     "dequant drops the offset": ("dequant_q8", _dequant_no_offset),
     "offset read as a zero-point": ("dequant_q8", _dequant_zero_point),
@@ -188,6 +198,8 @@ MUTATIONS = {
     "prefill: second norm reads h instead of h1": ("prefill_layer", _prefill_second_norm_reads_h),
     "prefill: h2 adds the down output to h": ("prefill_layer", _prefill_h2_from_h),
     "moe: residual added to the normalised input": ("moe_layer", _moe_residual_from_n),
+    "moe: second norm weighted by gamma1": ("moe_layer", _moe_second_norm_gamma1),
+    "moe: second norm without gamma": ("moe_layer", _moe_second_norm_no_gamma),
 }
 
 
