@@ -9,8 +9,8 @@ PASS_MAX = 64               # nemotron_prefill.rs `PB_MAX`: positions per prefil
 
 __all__ = [
     "QBLOCK", "ARGMAX_FLOOR", "PASS_MAX",
-    "as_f64", "dequant_q8", "project", "gemv_f16", "gemv_q8",
-    "rmsnorm", "add_rmsnorm", "relu2", "softmax", "topk", "route", "group",
+    "as_f64", "dequant_q8", "project", "gemv_f16", "gemv_q8", "dequant_q82f", "gemv_q82f",
+    "rmsnorm", "add_rmsnorm", "add_rmsnorm_ex", "sandwich", "relu2", "softmax", "topk", "route", "group",
     "combine", "argmax", "quantize_q8",
     "tiny_mlp", "q8_decode_layer", "prefill_layer", "moe_layer", "vocab_head",
 ]
@@ -60,6 +60,24 @@ def gemv_q8(codes, params, X):
     return project(dequant_q8(codes, params), X)
 
 
+def dequant_q82f(codes, row_scale, col_field) -> np.ndarray:
+    """q8_2f format → f64 weights (gemma_batch.rs `Q82_MM_WGSL`: an int8 body
+    [rows][cols], one binary16 scale per row and one binary16 factor per column, the
+    "column field"):  w[r][c] = row_scale[r] · q[r][c] · col_field[c].  The page's
+    kernel folds the column field into the staged activations and multiplies the
+    finished row sum by the row scale; this is the same product written per weight."""
+    q = as_f64(codes)
+    rows, cols = q.shape
+    rs = as_f64(row_scale).reshape(rows)
+    cf = as_f64(col_field).reshape(cols)
+    return rs[:, None] * q * cf[None, :]
+
+
+def gemv_q82f(codes, row_scale, col_field, X):
+    """Projection through a q8_2f matrix (gemma_batch.rs `q8_2f_mm_r2`)."""
+    return project(dequant_q82f(codes, row_scale, col_field), X)
+
+
 # ----------------------------------------------------------------- norms, activation
 def rmsnorm(h, gamma, eps):
     """nemotron_prefill.rs `pb_add_rms` / gemma_batch.rs `g4_add_norm_b`:
@@ -78,6 +96,35 @@ def add_rmsnorm(h, add, gamma, eps):
         h = h + np.atleast_2d(as_f64(add))
     y, inv = rmsnorm(h, gamma, eps)
     return h, y, inv
+
+
+def add_rmsnorm_ex(h, add, gamma, eps, scale=None, gemma=False):
+    """gemma_batch.rs `g4_add_norm_b`: h ← (h + d)·scale (no scale when ``scale`` is
+    None or 0: the page's "scale bits 0"), then y = h·inv·w with w = 1 + γ when
+    ``gemma`` (the page's `gemma` switch) else γ.  Returns (h_new, y, inv)."""
+    h = np.atleast_2d(as_f64(h))
+    if add is not None:
+        h = h + np.atleast_2d(as_f64(add))
+    if scale:
+        h = h * float(scale)
+    w = as_f64(gamma)
+    if gemma:
+        w = 1.0 + w
+    y, inv = rmsnorm(h, w, eps)
+    return h, y, inv
+
+
+def sandwich(x, w1, h, w2, eps, scale=None, gemma=False):
+    """gemma_batch.rs `g4_sandwich` (Gemma's sandwich residual in one dispatch), in
+    the page's order: mid = rms(x)·w1 (the mixer or FFN output norm), then
+    h ← (h + mid)·scale and n = rms(h)·w2 (`g4_add_norm_b`); with ``gemma`` both norm
+    weights are used as 1 + w.  Returns dict(mid, h, n, inv1, inv2)."""
+    w1 = as_f64(w1)
+    if gemma:
+        w1 = 1.0 + w1
+    mid, inv1 = rmsnorm(x, w1, eps)
+    h_new, n, inv2 = add_rmsnorm_ex(h, mid, w2, eps, scale, gemma)
+    return dict(mid=mid, h=h_new, n=n, inv1=inv1, inv2=inv2)
 
 
 def relu2(v):

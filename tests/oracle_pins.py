@@ -385,6 +385,148 @@ def _relu2_closed(v):
     return np.where(v > 0, v * v, 0.0)
 
 
+# ------------------------------------------------------------ q8_2f (row scale × column field)
+def _q82f(rows, cols, seed):
+    r = _rng(seed)
+    codes = np.clip(np.rint(r.standard_normal((rows, cols)) * 40), -127, 127).astype(np.int8)
+    rs = r.uniform(1e-3, 4e-3, rows).astype(np.float16)
+    cf = r.uniform(0.5, 2.0, cols).astype(np.float16)
+    return codes, rs, cf
+
+
+def brute_q82f(codes, rs, cf, x):
+    """y[r] = Σ_c rs[r]·q[r][c]·cf[c]·x[c], pure Python, binary16 decoded by hand."""
+    rows, cols = codes.shape
+    rsv, cfv = f16_list(rs), f16_list(cf)
+    xs = [float(v) for v in np.asarray(x, np.float32)]
+    return [sum(rsv[r] * int(codes[r, c]) * cfv[c] * xs[c] for c in range(cols)) for r in range(rows)]
+
+
+def pin_q82f_identity():
+    """Identity body, unit row scales and column field: y == x exactly."""
+    n = 64
+    x = _rng(40).standard_normal((3, n)).astype(np.float32)
+    y, _ = R.gemv_q82f(np.eye(n, dtype=np.int8), np.ones(n, np.float16), np.ones(n, np.float16), x)
+    assert np.array_equal(y, x.astype(np.float64))
+
+
+def pin_q82f_onehot_rectangular():
+    """One code per row at column π(r), on a 48×80 matrix: y[r] = rs[r]·q·cf[π(r)]·x[π(r)],
+    so a row scale read per column (or a column field read per row) cannot pass."""
+    rows, cols = 48, 80
+    r = _rng(41)
+    perm = r.permutation(cols)[:rows]
+    codes = np.zeros((rows, cols), np.int8)
+    qv = r.integers(-127, 128, rows)
+    codes[np.arange(rows), perm] = qv
+    rs = r.uniform(1e-3, 4e-3, rows).astype(np.float16)
+    cf = r.uniform(0.5, 2.0, cols).astype(np.float16)
+    x = r.standard_normal((2, cols)).astype(np.float32)
+    y, e = R.gemv_q82f(codes, rs, cf, x)
+    want = (rs.astype(np.float64)[None, :] * qv[None, :] * cf.astype(np.float64)[perm][None, :]
+            * x[:, perm].astype(np.float64))
+    close(y, want, rel=1e-15)
+    close(e, np.abs(want), rel=1e-15)
+
+
+def pin_q82f_ones_closed_form():
+    """x = 1: y[r] = rs[r]·Σ_c q[r][c]·cf[c]."""
+    codes, rs, cf = _q82f(24, 96, 42)
+    y, _ = R.gemv_q82f(codes, rs, cf, np.ones((1, 96), np.float32))
+    want = [float(rs[r]) * sum(int(codes[r, c]) * float(cf[c]) for c in range(96)) for r in range(24)]
+    close(y[0], want, rel=1e-12)
+
+
+def pin_q82f_brute_force():
+    for rows, cols, seed in ((5, 32, 43), (7, 64, 44), (3, 96, 45)):
+        codes, rs, cf = _q82f(rows, cols, seed)
+        x = _rng(seed + 100).standard_normal((2, cols)).astype(np.float32)
+        y, _ = R.gemv_q82f(codes, rs, cf, x)
+        for b in range(2):
+            close(y[b], brute_q82f(codes, rs, cf, x[b]), rel=1e-12, abs_=1e-300)
+
+
+def pin_q82f_folds_like_the_page():
+    """The page's arithmetic order: the column field folded into the activations,
+    the row scale applied to the finished integer-weighted sum."""
+    codes, rs, cf = _q82f(16, 64, 46)
+    x = _rng(47).standard_normal((3, 64))
+    y, _ = R.gemv_q82f(codes, rs, cf, x)
+    folded = x * cf.astype(np.float64)[None, :]
+    want = (folded @ codes.astype(np.float64).T) * rs.astype(np.float64)[None, :]
+    close(y, want, rel=1e-12)
+
+
+# ------------------------------------------------------------ sandwich residual
+def pin_add_rmsnorm_ex_closed_forms():
+    """h = 0, d = c (constant): h' = s·c, y = s·c/√((s·c)² + eps)·w, with w = 1 + γ
+    under the gemma switch; no scale when scale is 0 or None."""
+    n, c, s, eps = 16, 0.75, 2.5, 1e-6
+    g = _rng(48).uniform(0.5, 1.5, n)
+    h0 = np.zeros((1, n))
+    d = np.full((1, n), c)
+    hn, y, inv = R.add_rmsnorm_ex(h0, d, g, eps, scale=s, gemma=True)
+    close(hn, np.full((1, n), s * c), rel=1e-15)
+    close(inv, [1.0 / math.sqrt((s * c) ** 2 + eps)], rel=1e-15)
+    close(y, (s * c / math.sqrt((s * c) ** 2 + eps)) * (1.0 + g)[None, :], rel=1e-14)
+    for none in (None, 0.0):
+        hn, y, _ = R.add_rmsnorm_ex(h0, d, g, eps, scale=none)
+        close(hn, d, rel=0)
+        close(y, (c / math.sqrt(c * c + eps)) * g[None, :], rel=1e-14)
+
+
+def pin_sandwich_constant_inputs():
+    """x = a and h = b constant, w1 = 1, w2 = γ: mid = a/√(a² + eps),
+    h' = (b + mid)·s, n = h'/√(h'² + eps)·γ."""
+    n, a, b, s, eps = 32, -1.25, 0.5, 0.75, 1e-6
+    g = _rng(49).uniform(0.5, 1.5, n)
+    out = R.sandwich(np.full((2, n), a), np.ones(n), np.full((2, n), b), g, eps, scale=s)
+    mid = a / math.sqrt(a * a + eps)
+    hp = (b + mid) * s
+    close(out["mid"], np.full((2, n), mid), rel=1e-15)
+    close(out["h"], np.full((2, n), hp), rel=1e-15)
+    close(out["n"], np.tile(hp / math.sqrt(hp * hp + eps) * g, (2, 1)), rel=1e-14)
+
+
+def pin_sandwich_invariants_and_order():
+    """mean((n/w2)²) = ms/(ms + eps) with ms = mean(h'²); h' − h·s = mid·s (the add
+    comes before the scale); gemma with zero weights equals unit weights."""
+    n, eps, s = 40, 1e-6, 1.5
+    r = _rng(50)
+    x, h = r.standard_normal((3, n)) * 3, r.standard_normal((3, n))
+    w1, w2 = r.uniform(0.5, 1.5, n), r.uniform(0.5, 1.5, n)
+    out = R.sandwich(x, w1, h, w2, eps, scale=s)
+    ms = np.mean(out["h"] ** 2, axis=1)
+    close(np.mean((out["n"] / w2[None, :]) ** 2, axis=1), ms / (ms + eps), rel=1e-13)
+    ms1 = np.mean(x * x, axis=1)
+    close(np.mean((out["mid"] / w1[None, :]) ** 2, axis=1), ms1 / (ms1 + eps), rel=1e-13)
+    close(out["h"] - h * s, out["mid"] * s, rel=1e-12, abs_=1e-15)
+    a = R.sandwich(x, np.zeros(n), h, np.zeros(n), eps, gemma=True)
+    b = R.sandwich(x, np.ones(n), h, np.ones(n), eps)
+    for k in ("mid", "h", "n"):
+        close(a[k], b[k], rel=0)
+
+
+def pin_sandwich_brute_force():
+    """Pure-Python statement of the two norms on a tiny row."""
+    x = [0.5, -2.0, 1.0, 3.0]
+    h = [1.0, 0.25, -0.5, 2.0]
+    w1 = [1.5, 0.5, 1.0, 0.75]
+    w2 = [0.5, 1.25, 1.0, 2.0]
+    eps, s = 1e-6, 0.5
+    inv1 = 1.0 / math.sqrt(sum(v * v for v in x) / 4 + eps)
+    mid = [x[i] * inv1 * (1.0 + w1[i]) for i in range(4)]
+    hp = [(h[i] + mid[i]) * s for i in range(4)]
+    inv2 = 1.0 / math.sqrt(sum(v * v for v in hp) / 4 + eps)
+    nn = [hp[i] * inv2 * (1.0 + w2[i]) for i in range(4)]
+    out = R.sandwich(np.array([x]), np.array(w1), np.array([h]), np.array(w2), eps, scale=s, gemma=True)
+    close(out["mid"][0], mid, rel=1e-15)
+    close(out["h"][0], hp, rel=1e-15)
+    close(out["n"][0], nn, rel=1e-14)
+    close(out["inv1"], [inv1], rel=1e-15)
+    close(out["inv2"], [inv2], rel=1e-15)
+
+
 SLOT_SCALES = {"q": 2.0, "k": 4.0, "v": 0.5, "o": 8.0, "up": 0.25, "down": 16.0}
 
 

@@ -7,7 +7,8 @@ import oracle.ref as R
 from oracle_pins import PINS
 
 _orig = {k: getattr(R, k) for k in ("dequant_q8", "project", "rmsnorm", "relu2", "softmax",
-                                    "topk", "route", "group", "combine", "argmax")}
+                                    "topk", "route", "group", "combine", "argmax", "dequant_q82f",
+                                    "add_rmsnorm_ex", "sandwich")}
 
 
 def _dequant_no_offset(codes, params):
@@ -172,6 +173,50 @@ def _moe_second_norm_no_gamma(h, gamma1, gamma2, eps, router, experts, k, renorm
     return out
 
 
+def _q82f_scales_swapped(codes, row_scale, col_field):
+    # the row scale read per column and the column field per row (square blocks only)
+    q = R.as_f64(codes)
+    rows, cols = q.shape
+    rs = R.as_f64(row_scale).reshape(-1)
+    cf = R.as_f64(col_field).reshape(-1)
+    return cf[:rows, None] * q * rs[None, :cols] if rows <= cols else cf[:, None] * q * rs[None, :cols]
+
+
+def _q82f_no_col_field(codes, row_scale, col_field):
+    return _orig["dequant_q82f"](codes, row_scale, np.ones_like(R.as_f64(col_field)))
+
+
+def _q82f_col_field_shifted(codes, row_scale, col_field):
+    cf = np.roll(R.as_f64(col_field).reshape(-1), 1)
+    return _orig["dequant_q82f"](codes, row_scale, cf)
+
+
+def _add_norm_ex_scale_before_add(h, add, gamma, eps, scale=None, gemma=False):
+    h = np.atleast_2d(R.as_f64(h))
+    if scale:
+        h = h * float(scale)
+    if add is not None:
+        h = h + np.atleast_2d(R.as_f64(add))
+    w = R.as_f64(gamma) + (1.0 if gemma else 0.0)
+    y, inv = R.rmsnorm(h, w, eps)
+    return h, y, inv
+
+
+def _add_norm_ex_gemma_ignored(h, add, gamma, eps, scale=None, gemma=False):
+    return _orig["add_rmsnorm_ex"](h, add, gamma, eps, scale, False)
+
+
+def _sandwich_first_norm_w2(x, w1, h, w2, eps, scale=None, gemma=False):
+    return _orig["sandwich"](x, w2, h, w2, eps, scale, gemma)
+
+
+def _sandwich_adds_raw_x(x, w1, h, w2, eps, scale=None, gemma=False):
+    out = _orig["sandwich"](x, w1, h, w2, eps, scale, gemma)
+    hn, n, inv2 = _orig["add_rmsnorm_ex"](h, x, w2, eps, scale, gemma)
+    out.update(h=hn, n=n, inv2=inv2)
+    return out
+
+
 MUTATIONS = {
     "dequant drops the offset": ("dequant_q8", _dequant_no_offset),
     "offset read as a zero-point": ("dequant_q8", _dequant_zero_point),
@@ -200,6 +245,13 @@ MUTATIONS = {
     "moe: residual added to the normalised input": ("moe_layer", _moe_residual_from_n),
     "moe: second norm weighted by gamma1": ("moe_layer", _moe_second_norm_gamma1),
     "moe: second norm without gamma": ("moe_layer", _moe_second_norm_no_gamma),
+    "q8_2f: row scale and column field swapped": ("dequant_q82f", _q82f_scales_swapped),
+    "q8_2f: column field dropped": ("dequant_q82f", _q82f_no_col_field),
+    "q8_2f: column field off by one column": ("dequant_q82f", _q82f_col_field_shifted),
+    "add_rmsnorm_ex: scale applied before the add": ("add_rmsnorm_ex", _add_norm_ex_scale_before_add),
+    "add_rmsnorm_ex: gemma switch ignored": ("add_rmsnorm_ex", _add_norm_ex_gemma_ignored),
+    "sandwich: first norm weighted by w2": ("sandwich", _sandwich_first_norm_w2),
+    "sandwich: residual adds the raw x": ("sandwich", _sandwich_adds_raw_x),
 }
 
 
