@@ -172,38 +172,35 @@ class Q8DecodeLayer:
         return L
 
     def e2e_setup(self):
+        """Host buffers of the end-to-end step: x and x_o in one pinned buffer (one
+        copy in), the six outputs in one device buffer and one pinned buffer (one copy
+        out); the layer descriptors built once."""
         t = self.t
-        self.hx = t.empty((1, self.H), dtype=t.float32).pin_memory()
-        self.hxo = t.empty((1, self.H), dtype=t.float32).pin_memory()
-        self.hx.copy_(self.x.cpu())
-        self.hxo.copy_(self.xo.cpu())
-        self.hout = {k: t.empty(v.shape, dtype=t.float32).pin_memory() for k, v in self.out.items()}
-        self.h2d = (self.hx.numel() + self.hxo.numel()) * 4
-        self.d2h = sum(v.numel() for v in self.out.values()) * 4
+        H, KV, I = self.H, self.KV, self.I
+        self.xin = t.empty((2, H), dtype=t.float32, device="cuda")
+        self.hin = t.empty((2, H), dtype=t.float32).pin_memory()
+        self.hin[0].copy_(self.x[0].cpu())
+        self.hin[1].copy_(self.xo[0].cpu())
+        sizes = (("q", H), ("k", KV), ("v", KV), ("o", H), ("u", I), ("down", H))
+        n = sum(m for _, m in sizes)
+        self.obuf = t.empty(n, dtype=t.float32, device="cuda")
+        self.hobuf = t.empty(n, dtype=t.float32).pin_memory()
+        self.eout, o = {}, 0
+        for k, m in sizes:
+            self.eout[k] = self.obuf[o:o + m]
+            o += m
+        self.structs = [self.pgq.q8_layer_struct(L) for L in self.layers]
+        self.h2d = self.hin.numel() * 4
+        self.d2h = n * 4
 
     def e2e_step(self):
-        """Public API end to end: pinned host inputs in, the layer, outputs back out."""
-        self.x.copy_(self.hx, non_blocking=True)
-        self.xo.copy_(self.hxo, non_blocking=True)
-        L = self.next_layer()
-        self.pgq.q8_decode_layer(L, self.x[0], self.xo[0], self.g, 1e-6,
-                                 out={k: v[0] for k, v in self.out.items()})
-        for k, v in self.out.items():
-            self.hout[k].copy_(v, non_blocking=True)
-
-    def oracle_sample(self, frac):
-        """Oracle inputs for a row sample of every matrix (host copies of the inputs)."""
-        L = self.layers[0]
-        mats = {}
-        for s, (c, p) in L.items():
-            r = max(1, int(c.shape[0] * frac))
-            mats[s] = (c[:r].cpu().numpy(), p[:r].cpu().numpy())
-        x = self.x.cpu().numpy()[0]
-        xo = self.xo.cpu().numpy()[0]
-        g = self.g.cpu().numpy()
-        u = np.abs(np.random.default_rng(0).standard_normal(self.I)).astype(np.float32)
-        nbytes = sum(c.size + p.size * 2 for c, p in mats.values())
-        return mats, x, xo, g, u, nbytes
+        """Public API end to end: the inputs in from pinned host memory, the layer
+        call, the outputs back to pinned host memory."""
+        self.xin.copy_(self.hin, non_blocking=True)
+        L = self.structs[self.i % len(self.structs)]
+        self.i += 1
+        self.pgq.q8_decode_layer(L, self.xin[0], self.xin[1], self.g, 1e-6, out=self.eout, weights_stable=True)
+        self.hobuf.copy_(self.obuf, non_blocking=True)
 
 
 def _capture(torch, fn):
@@ -315,13 +312,13 @@ def time_prefill(torch, P, steps, warmup, pk):
         "bound": "hbm", "weight_bytes_per_pass": P.step_bytes, "launches_per_pass": P.launches_per_step,
         # the pass is one persistent launch per 8 layers (plus its input kernel): the
         # dominant kernel's roofline is the pass's weight bytes per launch
-        "roofline": {"bound": "hbm", "kernel": "prefill_pass_kernel (8 layers = 32 phases per launch, B=64)",
+        "roofline": {"bound": "hbm", "kernel": "pgq_prefill_pass_kernel (8 layers = 32 phases per launch, B=64)",
                      "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4),
                      "traffic": ncu_traffic("prefill_pass_8layers", PREFILL_FILES),
                      "algorithmic_bytes_per_launch": P.step_bytes // max(1, P.launches_per_step // 2),
                      "avg_launch_ms": round(ms / max(1, P.launches_per_step // 2), 5),
                      "timed": "CUDA-graph replay of the pass; per launch = pass / launches (input kernels included)"},
-        "up_alone": {"kernel": "prefill_pass_kernel, one phase (up 14336x4096, relu²) + input kernel",
+        "up_alone": {"kernel": "pgq_prefill_pass_kernel, one phase (up 14336x4096, relu²) + input kernel",
                      "GBps": round(ach, 1), "frac": round(ach / pk["hbm"], 4), "bytes": up_bytes,
                      "avg_launch_ms": round(k_ms, 5), "timed": "separate event loop over 32 up matrices, direct calls"},
     }
@@ -447,23 +444,81 @@ def time_e2e(torch, W, steps, warmup):
     return a.elapsed_time(b) / steps
 
 
-def cpu_baseline_q8(W, target_s=15.0):
-    """The oracle as it stands, timed on the host on a row sample of the layer."""
+def _host_layer_sample(frac):
+    """A row sample of the decode layer's six q8 matrices drawn on the host (same
+    recipe as the device copies), with its inputs; ``frac`` of each matrix's rows."""
+    import synth
+    c = synth.Q8_LAYER
+    H, KV, I, wl = c["hidden"], c["kv"], c["inter"], c["workload"]
+    mats, nb = {}, 0
+    for s, (r, cc) in synth.q8_layer_shapes(H, KV, I).items():
+        rr = max(4, int(r * frac))
+        codes, params = synth.q8_matrix(rr, cc, wl, synth.q8_tensor_id(0, s))
+        mats[s] = (codes, params)
+        nb += codes.size + params.size * 2
+    x = synth.normal((H,), 1.0, wl, synth.T_X)
+    xo = synth.normal((H,), 1.0, wl, synth.T_XO)
+    g = synth.gamma(H, wl)
+    u = np.abs(synth.normal((I,), 1.0, wl, 99))
+    return mats, x, xo, g, u, nb
+
+
+def _time_oracle_sample(frac, reps=1):
+    """Seconds of ``reps`` oracle passes over the row sample, and their weight bytes."""
     import oracle
+    mats, x, xo, g, u, nb = _host_layer_sample(frac)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.q8_decode_layer(x, xo, g, 1e-6, mats, u_in=u)
+    return time.perf_counter() - t0, nb * reps
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=20).stdout
+        for ln in out.splitlines():
+            if ln.strip().startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def cpu_baseline_q8(target_s=12.0):
+    """The oracle as it stands, timed on the host cores on a row sample of the decode
+    layer: with every core numpy uses (its matmuls are multi-threaded), and in a child
+    process limited to one thread."""
     frac = 0.02
-    mats, x, xo, g, u, nbytes = W.oracle_sample(frac)
-    t0 = time.perf_counter()
-    oracle.q8_decode_layer(x, xo, g, 1e-6, mats, u_in=u[: mats["down"][0].shape[1]])
-    dt = time.perf_counter() - t0
-    # grow the sample to about target_s of work
-    frac = min(1.0, frac * max(1.0, target_s / max(dt, 1e-3)))
-    mats, x, xo, g, u, nbytes = W.oracle_sample(frac)
-    t0 = time.perf_counter()
-    oracle.q8_decode_layer(x, xo, g, 1e-6, mats, u_in=u)
-    dt = time.perf_counter() - t0
-    return dict(value=nbytes / dt / 1e9, unit="GB/s", cores=os.cpu_count(), kind="oracle",
-                sample=f"{frac:.3f} of the rows of each of the six matrices ({nbytes} weight bytes), one pass, "
-                       f"{dt:.1f} s; numpy f64 (elementwise single-threaded, matmul multi-threaded)")
+    dt, _ = _time_oracle_sample(frac)
+    frac = min(1.0, frac * max(1.0, target_s / max(dt, 1e-3)))   # about target_s of work:
+    dt, _ = _time_oracle_sample(frac)                            # a larger sample, then
+    reps = max(1, min(30, int(round(target_s / max(dt, 1e-3)))))   # whole passes repeated
+    dt, nb = _time_oracle_sample(frac, reps)
+    one = None
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1", NUMEXPR_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker", repr(frac),
+                            "--cpu-reps", str(reps)], env=env,
+                           capture_output=True, text=True, timeout=600)
+        rec = json.loads(r.stdout.strip().splitlines()[-1])
+        one = dict(value=round(rec["bytes"] / rec["seconds"] / 1e9, 4), unit="GB/s", threads=1,
+                   seconds=round(rec["seconds"], 2))
+    except Exception as exc:   # reported, not fatal: the all-core figure stands
+        one = dict(error=f"one-thread run failed: {type(exc).__name__}")
+    return dict(value=round(nb / dt / 1e9, 4), unit="GB/s", cores=os.cpu_count(), threads=os.cpu_count(),
+                kind="oracle", cpu_model=cpu_model(), one_thread=one,
+                sample=f"{frac:.3f} of the rows of each of the decode layer's six q8 matrices, {reps} pass(es) "
+                       f"({nb} weight bytes), {dt:.1f} s with all cores; numpy f64 oracle (matmuls multi-threaded, the rest "
+                       f"single-threaded); one_thread: the same sample with every thread pool set to 1")
 
 
 # ------------------------------------------------------------------ main
@@ -494,7 +549,13 @@ def main():
                     help="profiling aid: run one workload and print its JSON object")
     ap.add_argument("--no-graph", action="store_true", help="profiling aid (--only moe): direct calls only")
     ap.add_argument("--prefill-layers", type=int, default=None, help="layers of the prefill pass (default 32)")
+    ap.add_argument("--cpu-worker", type=float, default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-reps", type=int, default=1, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.cpu_worker is not None:   # the one-thread oracle timing (a child of cpu_baseline_q8)
+        dt, nb = _time_oracle_sample(args.cpu_worker, args.cpu_reps)
+        print(json.dumps({"seconds": dt, "bytes": nb}), flush=True)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
@@ -539,7 +600,6 @@ def main():
         total_ms, k1_ms, k2_ms = time_q8_layer(torch, W, args.steps, args.warmup)
     clocks = clk.summary()
     e2e_ms = time_e2e(torch, W, args.steps, args.warmup)
-    Wcpu = W
     total_ms, e2e_ms = max_over_ranks(torch, dist, [total_ms, e2e_ms], "cuda")
     ms_step = total_ms / args.steps
     value = job_gbs(world, W.step_bytes, ms_step)
@@ -554,7 +614,7 @@ def main():
                              "uploaded by an untimed replay, after W warm-up steps",
                    "parallelism": f"replicas x{world}"},
         "frac_of_hbm": round(value / world / pk["hbm"], 4),
-        "roofline": {"bound": "hbm", "kernel": "gemv_tma_kernel<q8,B=1> (norm + q,k,v,o,up)",
+        "roofline": {"bound": "hbm", "kernel": "pgq_gemv_tma_kernel<q8,B=1> (norm + q,k,v,o,up)",
                      "achieved": round(achieved, 1), "peak": pk["hbm"], "unit": "GB/s",
                      "frac": round(achieved / pk["hbm"], 4), "peak_src": pk["src"],
                      "traffic": ncu_traffic("gemv_q8_layer_multi", Q8_FILES),
@@ -579,7 +639,7 @@ def main():
         torch.cuda.empty_cache()
         line["workloads"]["tiny_mlp"] = bench_tiny_mlp(torch, pgq, synth, args.steps, args.warmup, pk)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_q8(Wcpu)
+        line["cpu_baseline"] = cpu_baseline_q8()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
@@ -593,24 +653,9 @@ def run_reference(args, rank, world):
     import torch
     import synth
 
-    class HostLayer(Q8DecodeLayer):
+    class HostLayer:
         def __init__(self):
-            c = synth.Q8_LAYER
-            self.H, self.KV, self.I = c["hidden"], c["kv"], c["inter"]
-            self.frac = 1.0 / 8
-            wl = c["workload"]
-            self.mats = {}
-            nb = 0
-            for s, (r, cc) in synth.q8_layer_shapes(self.H, self.KV, self.I).items():
-                rr = max(4, int(r * self.frac))
-                codes, params = synth.q8_matrix(rr, cc, wl, synth.q8_tensor_id(0, s))
-                self.mats[s] = (codes, params)
-                nb += codes.size + params.size * 2
-            self.nbytes = nb
-            self.x = synth.normal((self.H,), 1.0, wl, synth.T_X)
-            self.xo = synth.normal((self.H,), 1.0, wl, synth.T_XO)
-            self.g = synth.gamma(self.H, wl)
-            self.u = np.abs(synth.normal((self.I,), 1.0, wl, 99))
+            self.mats, self.x, self.xo, self.g, self.u, self.nbytes = _host_layer_sample(1.0 / 8)
 
     import oracle
     Wh = HostLayer()
@@ -628,8 +673,8 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": Q8DecodeLayer.name, "B": 1},
-        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": os.cpu_count(), "threads": os.cpu_count(),
+                         "kind": "oracle", "cpu_model": cpu_model(), "sample": sample},
         "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
     del torch

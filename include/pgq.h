@@ -3,8 +3,9 @@
  *
  * C ABI.  Every pointer named "device" is a CUDA device address that the caller
  * allocated and owns; the library never allocates or frees device memory and keeps
- * no device state between calls (except the per-device launch configuration it
- * caches).  Calls are asynchronous and ordered on the given stream (`stream` is a
+ * no device state between calls except the per-device launch configuration it
+ * caches, the decode kernels' status word (pgq_last_device_status) and the fixed
+ * scratch array of pgq_gemv_f16_argmax_static.  Calls are asynchronous and ordered on the given stream (`stream` is a
  * cudaStream_t; NULL is the legacy default stream).  Argument errors are detected on
  * the host before anything is launched: the call then returns a non-zero status,
  * `pgq_last_error()` describes it, and no device memory is touched.  There is no CPU
@@ -75,6 +76,40 @@ int pgq_abi_version(void);
  * were built for; PGQ_ENODEV otherwise.  Synchronous, launches nothing. */
 int pgq_device_check(void);
 
+/* ---------------------------------------------------------------- device status
+ * Every wait inside a kernel (a copy landing, another block's result, the next
+ * phase's input) is bounded: when one runs longer than the wait limit the kernel
+ * records PGQ_ETIMEOUT, its blocks leave their loops, drain the copies they have in
+ * flight and return, and the outputs of that call are undefined.  A launch cannot
+ * report this through its return value (calls are asynchronous), so the caller asks
+ * afterwards, as the pages' callers learn from gemma_batch.rs `encode_q82_mm`
+ * returning false that the work was not (all) encoded.
+ *
+ * pgq_last_device_status: synchronises `stream`, then returns PGQ_ETIMEOUT if a
+ * decode kernel (pgq_gemv_*, pgq_mlp_f16_decode, pgq_q8_decode_layer*) on the
+ * current device recorded an expired wait since the previous call of this function
+ * (that record is per device, and reading it clears it), else, when workspace !=
+ * NULL, the status word of the last prefill / pass / MoE call that used that
+ * workspace (PGQ_OK or PGQ_ETIMEOUT; not cleared: the next call on the workspace
+ * resets it), else PGQ_OK.  PGQ_ECUDA if a CUDA call fails (e.g. an earlier launch
+ * faulted). */
+int pgq_last_device_status(const void* workspace, void* stream);
+
+/* Limit of every bounded device-side wait, in nanoseconds, for launches made after
+ * the call (process-wide).  0 restores the default of 2 s; otherwise 1000 ns ..
+ * 60e9 ns, else PGQ_EINVAL.  A limit shorter than a kernel's normal waits makes its
+ * calls report PGQ_ETIMEOUT. */
+int pgq_set_wait_limit_ns(unsigned long long ns);
+unsigned long long pgq_wait_limit_ns(void);
+
+/* Test hook of the timeout path (on = 1; 0 turns it off; process-wide): while it is
+ * on, a one-position decode launch never copies its inputs, so its blocks' wait for
+ * them runs out, and a prefill pass's wait for its first projection's last tile asks
+ * for one tile more than exists.  Either call then reports PGQ_ETIMEOUT through
+ * pgq_last_device_status after at most a few wait limits; nothing faults.  Not for
+ * production use. */
+int pgq_debug_stall(int on);
+
 /* ---------------------------------------------------------------- a1: add + RMSNorm
  * For each position b (nemotron_prefill.rs `pb_add_rms` with add = 0/1;
  * gemma_batch.rs `g4_add_norm_b`):
@@ -121,19 +156,21 @@ int pgq_gemv_f16_argmax(const uint16_t* W, int rows, int cols, const float* x, i
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /* Allocation-free form of pgq_gemv_f16_argmax.  The paper has no counterpart to
- * this entry point; it exists for callers that cannot allocate device memory: code
- * running while a CUDA graph is being captured (where cudaMalloc is not allowed),
- * latency-bound decode loops that cannot afford the device synchronisation an
- * allocation may bring, and plugins living inside a host framework that owns every
- * byte of device memory through its own pools.  Such callers still pass W, x,
- * gamma, logits and ids; the scratch the argmax needs (per-block partial maxima and
- * a completion ticket) lives in a fixed array of PGQ_STATIC_SCRATCH_BYTES inside the
- * library, which every GPU that loads the library keeps for the life of the process.
- * Calls on one device share that array and it keeps the last call's contents; the
- * call clears what must start at zero itself.  Two calls that overlap on the GPU
- * (different streams, no ordering between them) race on it: order them.  The first
- * call on each device looks up the array's device address, so make it before any
- * stream capture.  Shapes whose scratch would exceed the array are rejected with
+ * this entry point; it exists for callers that cannot allocate device memory when
+ * they need the vocab head: plugins living inside a host framework that owns every
+ * byte of device memory through its own pools, and latency-bound decode loops that
+ * cannot afford the device-wide synchronisation an allocation may bring.  Such
+ * callers still pass W, x, gamma, logits and ids; the scratch the argmax needs
+ * (per-block partial maxima and a completion ticket) lives in a fixed array of
+ * PGQ_STATIC_SCRATCH_BYTES inside the library, which every GPU that loads the library
+ * keeps for the life of the process.  Calls on one device share that array and it
+ * keeps the last call's contents; the call clears what must start at zero itself.
+ * Two calls that overlap on the GPU (different streams, no ordering between them)
+ * race on it: order them.  The first call on each device looks up the array's
+ * device address (cudaGetSymbolAddress, with that device current) and caches it, so
+ * make that first call before any stream capture, and do not use this entry point
+ * after a device reset (cudaDeviceReset) in the same process: the cached address
+ * would be stale.  Shapes whose scratch would exceed the array are rejected with
  * PGQ_EUNSUPPORTED (about (SM count x B) x 8 bytes are needed).  It allocates
  * nothing and calls no allocating routine. */
 #define PGQ_STATIC_SCRATCH_BYTES 32768
@@ -234,7 +271,8 @@ int pgq_prefill_q8(const pgq_q8_job* jobs, int njobs, const float* X, int cols, 
                    void* workspace, size_t workspace_bytes, void* stream);
 
 /* Status word of the last prefill call that used `workspace` (PGQ_OK or
- * PGQ_ETIMEOUT when a bounded device-side wait expired).  Synchronises the stream. */
+ * PGQ_ETIMEOUT when a bounded device-side wait expired).  Synchronises the stream.
+ * (pgq_last_device_status(workspace, stream) also reports the decode kernels.) */
 int pgq_prefill_status(const void* workspace, void* stream);
 
 /* ---------------------------------------------------------------- prefill pass

@@ -76,6 +76,10 @@ _SIGS = {
     "pgq_prefill_q8_workspace_bytes": (C.c_size_t, [C.POINTER(C.c_int), C.c_int, C.c_int, C.c_int]),
     "pgq_prefill_q8": (C.c_int, [C.POINTER(Q8Job), C.c_int, _vp, C.c_int, C.c_int, _vp, C.c_size_t, _vp]),
     "pgq_prefill_status": (C.c_int, [_vp, _vp]),
+    "pgq_last_device_status": (C.c_int, [_vp, _vp]),
+    "pgq_set_wait_limit_ns": (C.c_int, [C.c_ulonglong]),
+    "pgq_wait_limit_ns": (C.c_ulonglong, []),
+    "pgq_debug_stall": (C.c_int, [C.c_int]),
     "pgq_moe_router": (C.c_int, [_vp, C.c_int, C.c_int, _vp, C.c_int, _vp, _vp]),
     "pgq_moe_route_topk": (C.c_int, [_vp, C.c_int, C.c_int, C.c_int, C.c_int, _vp, _vp, _vp]),
     "pgq_moe_group_gather": (C.c_int, [_vp, C.c_int, C.c_int, C.c_int, _vp, _vp, _vp, _vp, C.c_int, C.c_int, _vp,
@@ -317,6 +321,28 @@ def prefill_status(workspace, stream=None):
     return int(lib().pgq_prefill_status(_ptr(workspace), _stream(stream)))
 
 
+def last_device_status(workspace=None, stream=None):
+    """Status of the device-side waits since the last check (synchronises the
+    stream): ``ETIMEOUT`` if a decode kernel's wait, or the last call on
+    ``workspace``, ran out; ``OK`` otherwise.  Clears the decode record."""
+    return int(lib().pgq_last_device_status(_ptr(workspace) if workspace is not None else None, _stream(stream)))
+
+
+def set_wait_limit_ns(ns):
+    """Limit of every bounded device-side wait for later launches (0: the default)."""
+    _check(lib().pgq_set_wait_limit_ns(int(ns)))
+
+
+def wait_limit_ns():
+    return int(lib().pgq_wait_limit_ns())
+
+
+def debug_stall(on):
+    """Test hook: while on, decode (one position) and prefill-pass launches wait for
+    an event that never comes, so their bounded waits run out."""
+    _check(lib().pgq_debug_stall(1 if on else 0))
+
+
 # ------------------------------------------------------------------ workloads
 def mlp_f16_decode(h, W_up, W_down, gamma, eps=1e-6, u=None, y=None, stream=None):
     """y = h + W_down · relu²(W_up · rms(h)·gamma) for one position; returns (y, u)."""
@@ -351,8 +377,10 @@ WEIGHTS_STABLE = 1
 def q8_decode_layer(mats, x, x_o, gamma, eps=1e-6, out=None, stream=None, weights_stable=False):
     """The q8 decode layer for one position; returns dict q, k, v, o, u, down.
     weights_stable: no work still in flight on the stream writes these weights (both
-    launches may then start streaming them while the kernel before them finishes)."""
-    L = q8_layer_struct(mats)
+    launches may then start streaming them while the kernel before them finishes).
+    ``mats`` may also be a prebuilt ``Q8Layer`` (q8_layer_struct), whose tensors the
+    caller keeps alive."""
+    L = mats if isinstance(mats, Q8Layer) else q8_layer_struct(mats)
     dev = x.device
     if out is None:
         out = {s: torch.empty(n, dtype=torch.float32, device=dev) for s, n in

@@ -4,6 +4,7 @@
 #include <cstdlib>
 #include <cstdio>
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -12,12 +13,18 @@
 namespace pgq {
 
 namespace {
+constexpr unsigned long long WAIT_LIMIT_DEFAULT_NS = 2000000000ull;   // 2 s
+std::atomic<unsigned long long> g_wait_limit_ns{WAIT_LIMIT_DEFAULT_NS};
+std::atomic<int> g_stall{0};
 thread_local char g_err[512] = "";
 std::mutex g_dev_mu;
 DeviceInfo g_dev[64];
 bool g_dev_ok[64];
 bool g_dev_done[64];
 }  // namespace
+
+unsigned long long wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+int stall_injected() { return g_stall.load(std::memory_order_relaxed); }
 
 int set_error(int status, const char* fmt, ...) {
   va_list ap;
@@ -95,6 +102,38 @@ int pgq_abi_version(void) { return 1; }
 int pgq_device_check(void) {
   GET_DEVICE(dev);
   return PGQ_OK;
+}
+
+int pgq_set_wait_limit_ns(unsigned long long ns) {
+  if (ns == 0) ns = WAIT_LIMIT_DEFAULT_NS;
+  REQUIRE(ns >= 1000ull && ns <= 60000000000ull, PGQ_EINVAL, "set_wait_limit_ns: %llu ns outside 1 us .. 60 s", ns);
+  g_wait_limit_ns.store(ns);
+  return PGQ_OK;
+}
+
+unsigned long long pgq_wait_limit_ns(void) { return wait_limit_ns(); }
+
+int pgq_debug_stall(int on) {
+  REQUIRE(on == 0 || on == 1, PGQ_EINVAL, "debug_stall: %d is neither 0 nor 1", on);
+  g_stall.store(on);
+  return PGQ_OK;
+}
+
+int pgq_last_device_status(const void* workspace, void* stream) {
+  GET_DEVICE(dev);
+  cudaError_t e = cudaStreamSynchronize(as_stream(stream));
+  if (e != cudaSuccess) return cuda_status(e);
+  int dec = PGQ_OK;
+  const int rc = decode_status_read_and_clear(&dec);
+  if (rc) return rc;
+  int ws = PGQ_OK;
+  if (workspace) {
+    e = cudaMemcpy(&ws, static_cast<const char*>(workspace) + prefill_status_offset(), sizeof(int),
+                   cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  if (dec != PGQ_OK) return dec;
+  return ws;
 }
 
 int pgq_add_rmsnorm(float* h, const float* add, const float* gamma, float eps, int B, int n, float* y,

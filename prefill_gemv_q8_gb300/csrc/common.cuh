@@ -26,6 +26,11 @@ inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3
 // Records a one-line description of the last error (per thread); returns status.
 int set_error(int status, const char* fmt, ...);
 
+// Limit of every bounded device-side wait, in nanoseconds (pgq_set_wait_limit_ns),
+// and whether the test hook pgq_debug_stall is on: read by the launchers.
+unsigned long long wait_limit_ns();
+int stall_injected();
+
 inline int cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return PGQ_OK;
   return set_error(PGQ_ECUDA, "CUDA: %s", cudaGetErrorString(e));

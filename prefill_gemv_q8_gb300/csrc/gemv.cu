@@ -82,7 +82,7 @@ __device__ __forceinline__ int perm_col(int c) {
 
 template <bool Q8, int NB, int ST, bool ARGMAX>
 __global__ void __launch_bounds__(GV_THREADS, 1)
-gemv_kernel(const __grid_constant__ GvParams P) {
+pgq_gemv_kernel(const __grid_constant__ GvParams P) {
   using SH = GvShape<Q8, NB>;
   static_assert(GV_WARPS <= 16, "named barriers");
   constexpr int R = SH::R, U = SH::U, EPL = SH::EPL, CW = SH::CW;
@@ -412,8 +412,8 @@ using KernelFn = void (*)(GvParams);
 
 template <bool Q8, int NB, bool ARGMAX>
 KernelFn pick(int st) {
-  return st >= 4 ? reinterpret_cast<KernelFn>(&gemv_kernel<Q8, NB, 4, ARGMAX>)
-                 : reinterpret_cast<KernelFn>(&gemv_kernel<Q8, NB, 2, ARGMAX>);
+  return st >= 4 ? reinterpret_cast<KernelFn>(&pgq_gemv_kernel<Q8, NB, 4, ARGMAX>)
+                 : reinterpret_cast<KernelFn>(&pgq_gemv_kernel<Q8, NB, 2, ARGMAX>);
 }
 
 KernelFn kernel_for(bool q8, int nb, bool argmax, int st) {

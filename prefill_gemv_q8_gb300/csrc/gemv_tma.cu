@@ -82,6 +82,9 @@ struct GtParams {
   unsigned* ticket;
   int32_t* ids;
   unsigned long long wait_limit_ns;
+  // test hook (pgq_debug_stall): at one position the inputs are never copied, so the
+  // wait for them runs out and the block takes its abort path
+  int stall;
 };
 
 template <int EPL>
@@ -96,7 +99,7 @@ __device__ __forceinline__ int gt_perm(int c) {
 // them (group w / QW, QW = W·RPW / SR warps per group) and the (w mod QW)-th share of
 // the column chunks (at most MAXC chunks of 32 lanes x EPL values).
 template <bool Q8, int NB, bool ARGMAX, int W, int RPW, int MAXC>
-__global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_constant__ GtParams P) {
+__global__ void __launch_bounds__((W + 1) * 32, 1) pgq_gemv_tma_kernel(const __grid_constant__ GtParams P) {
   constexpr int THREADS = (W + 1) * 32;
   constexpr int EPL = Q8 ? 16 : 8;
   constexpr int CW = 32 * EPL;
@@ -125,7 +128,9 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
   const int t1 = (int)((unsigned)(blockIdx.x + 1) * (unsigned)T / (unsigned)G);
   const uint64_t policy = tc::policy_evict_first();
 
+  int n_issued = 0;   // producer lane: ring stages issued (stage i = task t0 + i, slot i mod GT_NST)
   auto issue = [&](int t, int j, int s) {   // one thread
+    ++n_issued;
     const int row0 = (t - P.task_begin[j]) * P.SR;
     const int nr = min(P.SR, P.rows[j] - row0);
     const uint32_t bar = tc::smem_addr(full + s);
@@ -206,7 +211,7 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
 #endif
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (!P.early) issue_ring(0, 1);
-    issue_inputs();
+    if (!P.stall) issue_inputs();
     if (!P.early) issue_ring(1, GT_RAMP);
 #ifdef PGQ_TRACE
     GTRACE(3);
@@ -714,16 +719,20 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_tma_kernel(const __grid_
     if (++s == GT_NST) { s = 0; parity ^= 1u; }
   }
   }  // computing warps
-  // leave no bulk copy in flight (an aborted block may have issued ahead)
+  // leave no bulk copy in flight (an aborted block may have issued ahead): the
+  // inputs' copies, and the last stage issued into each ring slot (stage i is the
+  // (i / GT_NST)-th fill of slot i mod GT_NST, so it completes that phase's parity)
   if (producer && lane == 0 && *(volatile int*)&s_abort) {
     if constexpr (NB == 1) {
-      const uint64_t w0 = tc::globaltimer();
-      while (!tc::mbar_try_sleep(tc::smem_addr(inbar), 0u, 20000u) && tc::globaltimer() - w0 < P.wait_limit_ns) {
+      if (!P.stall) {
+        const uint64_t w0 = tc::globaltimer();
+        while (!tc::mbar_try_sleep(tc::smem_addr(inbar), 0u, 20000u) && tc::globaltimer() - w0 < P.wait_limit_ns) {
+        }
       }
     }
-    for (int t = t0; t < t1 && t < t0 + GT_NST; ++t) {
+    for (int i = max(0, n_issued - GT_NST); i < n_issued; ++i) {
       const uint64_t w0 = tc::globaltimer();
-      while (!tc::mbar_try_sleep(tc::smem_addr(full + ((t - t0) % GT_NST)), 0u, 20000u) &&
+      while (!tc::mbar_try_sleep(tc::smem_addr(full + (i % GT_NST)), (uint32_t)((i / GT_NST) & 1), 20000u) &&
              tc::globaltimer() - w0 < P.wait_limit_ns) {
       }
     }
@@ -771,10 +780,10 @@ using GtFn = void (*)(GtParams);
 template <bool Q8, bool AM>
 GtFn gt_pick(int nb) {
   switch (nb) {
-    case 1: return reinterpret_cast<GtFn>(&gemv_tma_kernel<Q8, 1, AM, 16, 2, 2>);
-    case 2: return reinterpret_cast<GtFn>(&gemv_tma_kernel<Q8, 2, AM, 16, 2, 2>);
-    case 4: return reinterpret_cast<GtFn>(&gemv_tma_kernel<Q8, 4, AM, 16, 2, 2>);
-    default: return reinterpret_cast<GtFn>(&gemv_tma_kernel<Q8, 8, AM, 16, 2, 2>);
+    case 1: return reinterpret_cast<GtFn>(&pgq_gemv_tma_kernel<Q8, 1, AM, 16, 2, 2>);
+    case 2: return reinterpret_cast<GtFn>(&pgq_gemv_tma_kernel<Q8, 2, AM, 16, 2, 2>);
+    case 4: return reinterpret_cast<GtFn>(&pgq_gemv_tma_kernel<Q8, 4, AM, 16, 2, 2>);
+    default: return reinterpret_cast<GtFn>(&pgq_gemv_tma_kernel<Q8, 8, AM, 16, 2, 2>);
   }
 }
 }  // namespace
@@ -790,7 +799,7 @@ int launch_gemv_tma(const GvParams& V, bool q8, bool argmax, const DeviceInfo& d
   if ((size_t)SR * row_bytes > GT_STAGE_MAX) return PGQ_EUNSUPPORTED;
   if (SR * nb > 64) return PGQ_EUNSUPPORTED;
   const int nchunks = (V.cols + CW - 1) / CW;
-  constexpr int W = 16, RPW = 2, MAXC = 2;   // the launch shape (see gemv_tma_kernel)
+  constexpr int W = 16, RPW = 2, MAXC = 2;   // the launch shape (see pgq_gemv_tma_kernel)
   const int QW = W * RPW / SR;
   const int cpw = (nchunks + QW - 1) / QW;
   if (cpw > MAXC) return PGQ_EUNSUPPORTED;
@@ -862,7 +871,8 @@ int launch_gemv_tma(const GvParams& V, bool q8, bool argmax, const DeviceInfo& d
   P.part_idx = V.part_idx;
   P.ticket = V.ticket;
   P.ids = V.ids;
-  P.wait_limit_ns = 2000000000ull;
+  P.wait_limit_ns = wait_limit_ns();
+  P.stall = (nb == 1 && stall_injected()) ? 1 : 0;
   const size_t smem = 1024 + (size_t)(V.ninputs * nb + P.ngamma) * P.cols_pad * 4 +
                       GT_RED * (size_t)SR * std::max(nb, GT_GROUP) * QW * 4 + 128 +
                       (size_t)GT_NST * P.slot_bytes + (2 * GT_NST + 1) * 8 + 64;
@@ -920,7 +930,7 @@ int decode_status_read_and_clear(int* out) {
 // converted to binary16 with one power-of-two scale per position (undone on the
 // logits), stays in shared memory for the whole launch.  Each block takes a contiguous
 // range of whole tiles; the epilogue keeps per thread the best (logit, row) of every
-// position (gemv_kernel's argmax rules), and the last block to finish merges the blocks'
+// position (pgq_gemv_kernel's argmax rules), and the last block to finish merges the blocks'
 // partials in block order.
 constexpr int HD_THREADS = 192;        // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int HD_NP = 16;              // MMA N (positions, padded)
@@ -942,7 +952,7 @@ struct HdParams {
   unsigned long long wait_limit_ns;
 };
 
-__global__ void __launch_bounds__(HD_THREADS, 1) head_tc_kernel(const __grid_constant__ HdParams P) {
+__global__ void __launch_bounds__(HD_THREADS, 1) pgq_head_tc_kernel(const __grid_constant__ HdParams P) {
   extern __shared__ uint8_t hsm_raw[];
   uint8_t* hsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(hsm_raw) + 1023) & ~uintptr_t(1023));
   const int ks = P.ks, NST = P.nst, B = P.B;
@@ -1282,8 +1292,8 @@ int launch_head_tc(const GvParams& V, const DeviceInfo& dev, cudaStream_t st) {
   P.part_idx = V.part_idx;
   P.ticket = V.ticket;
   P.ids = V.ids;
-  P.wait_limit_ns = 2000000000ull;
-  const void* fn = reinterpret_cast<const void*>(&head_tc_kernel);
+  P.wait_limit_ns = wait_limit_ns();
+  const void* fn = reinterpret_cast<const void*>(&pgq_head_tc_kernel);
   {
     static std::map<int, size_t> done;
     size_t& cur = done[dev.device];

@@ -27,7 +27,7 @@ constexpr int RT_POS = 8;
 constexpr int RT_UNROLL = 7;   // router row float4 per lane loaded ahead (2688 columns: 21 = 3 rounds)
 
 __global__ void __launch_bounds__(RT_WARPS * 32)
-router_kernel(const float* __restrict__ R, const float* __restrict__ n, int B, int E, int cols,
+pgq_router_kernel(const float* __restrict__ R, const float* __restrict__ n, int B, int E, int cols,
               float* __restrict__ logits) {
   extern __shared__ __align__(16) float xs[];   // [RT_POS][cols]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -86,7 +86,7 @@ router_kernel(const float* __restrict__ R, const float* __restrict__ n, int B, i
 // of the logits is the order of the probabilities — then w = p (or p / Σp).
 constexpr int RK_MAXV = 8;   // E <= 256
 
-__global__ void route_topk_kernel(const float* __restrict__ logits, int B, int E, int k, int renorm,
+__global__ void pgq_route_topk_kernel(const float* __restrict__ logits, int B, int E, int k, int renorm,
                                   int32_t* __restrict__ sel, float* __restrict__ wout) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (warp >= B) return;
@@ -157,7 +157,7 @@ __global__ void route_topk_kernel(const float* __restrict__ logits, int B, int E
 constexpr int GR_THREADS = 1024;
 
 __global__ void __launch_bounds__(GR_THREADS)
-group_kernel(const int32_t* __restrict__ sel, int n, int E, int32_t* __restrict__ counts,
+pgq_group_kernel(const int32_t* __restrict__ sel, int n, int E, int32_t* __restrict__ counts,
              int32_t* __restrict__ offsets, int32_t* __restrict__ entries, const float* __restrict__ x, int xcols,
              int xdiv, float* __restrict__ xg) {
   extern __shared__ int sh[];
@@ -321,7 +321,7 @@ __device__ __forceinline__ void bank_task(const MoeBank& P, const float* xs, int
 }
 
 __global__ void __launch_bounds__(MB_WARPS * 32, 1)
-moe_bank_kernel(const __grid_constant__ MoeBank P) {
+pgq_moe_bank_kernel(const __grid_constant__ MoeBank P) {
   extern __shared__ __align__(16) float xs[];   // [MB_ENT][cols_pad]
   __shared__ int s_pre[MB_MAXE + 1];
   __shared__ int s_ent[MB_ENT];
@@ -389,7 +389,7 @@ moe_bank_kernel(const __grid_constant__ MoeBank P) {
 //   y[b] = γ·h[b]/√(mean h² + eps)
 constexpr int MC_THREADS = 1024;
 __global__ void __launch_bounds__(MC_THREADS)
-moe_combine_kernel(float* __restrict__ h, const float* __restrict__ o, const float* __restrict__ eo,
+pgq_moe_combine_kernel(float* __restrict__ h, const float* __restrict__ o, const float* __restrict__ eo,
                    const float* __restrict__ w, int k, const float* __restrict__ gamma, float eps, int n,
                    float* __restrict__ y, float* __restrict__ inv_out) {
   // one block per position; thread i holds float4 groups i, i + 1024, ... of the row
@@ -456,7 +456,7 @@ int bank_blocks_per_sm(int device, size_t smem) {
   auto it = known.find({device, smem});
   if (it != known.end()) return it->second;
   int occ = 1;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, moe_bank_kernel, MB_WARPS * 32, smem) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, pgq_moe_bank_kernel, MB_WARPS * 32, smem) != cudaSuccess) {
     cudaGetLastError();
     occ = 1;
   }
@@ -471,17 +471,17 @@ int launch_router(const float* R, const float* n, int B, int E, int cols, float*
   if (cols % 4 != 0) return set_error(PGQ_EUNSUPPORTED, "router: cols=%d not a multiple of 4", cols);
   const size_t smem = (size_t)RT_POS * cols * sizeof(float);
   if (smem > dev.smem_optin) return set_error(PGQ_EUNSUPPORTED, "router: %zu bytes of shared memory", smem);
-  if (cudaError_t e = moe_allow_smem(reinterpret_cast<const void*>(router_kernel), dev.device, smem); e != cudaSuccess)
+  if (cudaError_t e = moe_allow_smem(reinterpret_cast<const void*>(pgq_router_kernel), dev.device, smem); e != cudaSuccess)
     return cuda_status(e);
   dim3 grid((E + RT_WARPS - 1) / RT_WARPS, (B + RT_POS - 1) / RT_POS);
-  router_kernel<<<grid, RT_WARPS * 32, smem, st>>>(R, n, B, E, cols, logits);
+  pgq_router_kernel<<<grid, RT_WARPS * 32, smem, st>>>(R, n, B, E, cols, logits);
   return cuda_status(cudaGetLastError());
 }
 
 int launch_route_topk(const float* logits, int B, int E, int k, int renorm, int32_t* sel, float* w, cudaStream_t st) {
   if (E > 32 * RK_MAXV || k > 32) return set_error(PGQ_EUNSUPPORTED, "route: E=%d or k=%d too large", E, k);
   const int warps_per_block = 8;
-  route_topk_kernel<<<(B + warps_per_block - 1) / warps_per_block, warps_per_block * 32, 0, st>>>(logits, B, E, k,
+  pgq_route_topk_kernel<<<(B + warps_per_block - 1) / warps_per_block, warps_per_block * 32, 0, st>>>(logits, B, E, k,
                                                                                                   renorm, sel, w);
   return cuda_status(cudaGetLastError());
 }
@@ -490,7 +490,7 @@ int launch_group(const int32_t* sel, int n, int E, int32_t* counts, int32_t* off
                  const float* x, int xcols, int xdiv, float* xg, cudaStream_t st) {
   const size_t smem = (size_t)(n + 2 * E + 1) * sizeof(int);
   if (smem > 48 * 1024) return set_error(PGQ_EUNSUPPORTED, "group: %d entries and %d experts too many", n, E);
-  group_kernel<<<1, GR_THREADS, smem, st>>>(sel, n, E, counts, offsets, entries, x, xcols, xdiv, xg);
+  pgq_group_kernel<<<1, GR_THREADS, smem, st>>>(sel, n, E, counts, offsets, entries, x, xcols, xdiv, xg);
   return cuda_status(cudaGetLastError());
 }
 
@@ -514,11 +514,11 @@ int launch_moe_bank(const MoeBankArgs& a, const DeviceInfo& dev, cudaStream_t st
   P.epilogue = a.epilogue;
   const size_t smem = (size_t)MB_ENT * P.cols_pad * sizeof(float);
   if (smem + 8192 > dev.smem_optin) return set_error(PGQ_EUNSUPPORTED, "expert bank: cols=%d too large", a.cols);
-  if (cudaError_t e = moe_allow_smem(reinterpret_cast<const void*>(moe_bank_kernel), dev.device, smem); e != cudaSuccess)
+  if (cudaError_t e = moe_allow_smem(reinterpret_cast<const void*>(pgq_moe_bank_kernel), dev.device, smem); e != cudaSuccess)
     return cuda_status(e);
   const int occ = bank_blocks_per_sm(dev.device, smem);
   void* args[] = {&P};
-  return cuda_status(cudaLaunchKernel(reinterpret_cast<const void*>(moe_bank_kernel), dim3(dev.sms * occ),
+  return cuda_status(cudaLaunchKernel(reinterpret_cast<const void*>(pgq_moe_bank_kernel), dim3(dev.sms * occ),
                                       dim3(MB_WARPS * 32), args, smem, st));
 }
 
@@ -526,7 +526,7 @@ int launch_moe_combine(float* h, const float* o, const float* eo, const float* w
                        int B, int n, float* y, float* inv, cudaStream_t st) {
   if (n % 4 != 0 || n > 4 * 4 * MC_THREADS)
     return set_error(PGQ_EUNSUPPORTED, "combine: n=%d must be a multiple of 4 and at most %d", n, 16 * MC_THREADS);
-  moe_combine_kernel<<<B, MC_THREADS, 0, st>>>(h, o, eo, w, k, gamma, eps, n, y, inv);
+  pgq_moe_combine_kernel<<<B, MC_THREADS, 0, st>>>(h, o, eo, w, k, gamma, eps, n, y, inv);
   return cuda_status(cudaGetLastError());
 }
 

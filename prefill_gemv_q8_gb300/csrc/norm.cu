@@ -24,7 +24,7 @@ __device__ __forceinline__ float block_sum_256(float v, float* red) {
 }
 
 __global__ void __launch_bounds__(NORM_THREADS)
-add_rmsnorm_kernel(float* __restrict__ h, const float* __restrict__ add,
+pgq_add_rmsnorm_kernel(float* __restrict__ h, const float* __restrict__ add,
                    const float* __restrict__ gamma, float eps, int n,
                    float* __restrict__ y, float* __restrict__ inv_out) {
   __shared__ float red[NORM_THREADS / 32];
@@ -54,7 +54,7 @@ add_rmsnorm_kernel(float* __restrict__ h, const float* __restrict__ add,
   }
 }
 
-__global__ void relu2_kernel(float4* __restrict__ v, size_t n4) {
+__global__ void pgq_relu2_kernel(float4* __restrict__ v, size_t n4) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4;
        i += (size_t)gridDim.x * blockDim.x) {
     float4 a = v[i];
@@ -62,7 +62,7 @@ __global__ void relu2_kernel(float4* __restrict__ v, size_t n4) {
     v[i] = make_float4(a.x * a.x, a.y * a.y, a.z * a.z, a.w * a.w);
   }
 }
-__global__ void relu2_tail_kernel(float* __restrict__ v, size_t from, size_t n) {
+__global__ void pgq_relu2_tail_kernel(float* __restrict__ v, size_t from, size_t n) {
   const size_t i = from + threadIdx.x;
   if (i < n) { const float a = fmaxf(v[i], 0.f); v[i] = a * a; }
 }
@@ -71,7 +71,7 @@ __global__ void relu2_tail_kernel(float* __restrict__ v, size_t from, size_t n) 
 // lowest index among its equal values), then a tree that keeps the larger value
 // or, on a tie, the lower index (nemotron_prefill.rs `pb_argmax`).
 __global__ void __launch_bounds__(NORM_THREADS)
-argmax_kernel(const float* __restrict__ logits, int V, int32_t* __restrict__ ids) {
+pgq_argmax_kernel(const float* __restrict__ logits, int V, int32_t* __restrict__ ids) {
   __shared__ float sv[NORM_THREADS];
   __shared__ int si[NORM_THREADS];
   const float* row = logits + (size_t)blockIdx.x * V;
@@ -100,7 +100,7 @@ argmax_kernel(const float* __restrict__ logits, int V, int32_t* __restrict__ ids
 // ------------------------------------------------------------------ launchers
 int launch_add_rmsnorm(float* h, const float* add, const float* gamma, float eps, int B, int n,
                        float* y, float* inv, cudaStream_t st) {
-  add_rmsnorm_kernel<<<B, NORM_THREADS, 0, st>>>(h, add, gamma, eps, n, y, inv);
+  pgq_add_rmsnorm_kernel<<<B, NORM_THREADS, 0, st>>>(h, add, gamma, eps, n, y, inv);
   return cuda_status(cudaGetLastError());
 }
 
@@ -109,14 +109,14 @@ int launch_relu2(float* v, size_t n, cudaStream_t st, int sms) {
   if (n4) {
     const size_t want = (n4 + 255) / 256;
     const int grid = (int)(want < (size_t)sms * 8 ? want : (size_t)sms * 8);
-    relu2_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<float4*>(v), n4);
+    pgq_relu2_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<float4*>(v), n4);
   }
-  if (n % 4) relu2_tail_kernel<<<1, 4, 0, st>>>(v, n4 * 4, n);
+  if (n % 4) pgq_relu2_tail_kernel<<<1, 4, 0, st>>>(v, n4 * 4, n);
   return cuda_status(cudaGetLastError());
 }
 
 int launch_argmax(const float* logits, int B, int V, int32_t* ids, cudaStream_t st) {
-  argmax_kernel<<<B, NORM_THREADS, 0, st>>>(logits, V, ids);
+  pgq_argmax_kernel<<<B, NORM_THREADS, 0, st>>>(logits, V, ids);
   return cuda_status(cudaGetLastError());
 }
 

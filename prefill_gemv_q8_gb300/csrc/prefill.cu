@@ -105,6 +105,9 @@ struct PsParams {
   unsigned long long wait_limit_ns;
   float eps;
   int nph, B, Bp, G, maxseg, maxtiles, wst;
+  // test hook (pgq_debug_stall): the wait for the first phase's tiles asks for one
+  // tile more than there are, so it runs out and every block takes its abort path
+  int stall;
   // A grouped expert bank (one phase, one matrix [E][rows][cols]): tile t is tile
   // t mod tpe of expert t / tpe; the expert's entries are rows [off, off + cnt) of the
   // gathered input (at most 64), and entry n's outputs go to row ent[off + n].
@@ -367,7 +370,7 @@ __device__ __forceinline__ void tile_stats(const float4* acc4, int nvec, int et,
 }
 
 template <bool MOE>
-__global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __grid_constant__ PsParams P) {
+__global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const __grid_constant__ PsParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int Bp = P.Bp, WST = P.wst, G = P.G;
@@ -728,7 +731,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
       const PsPhase& F = P.ph[p];
       bool ok = true;
       if (!MOE && et == 0) PTRACE(p, 4);
-      if (et == 0) ok = W.count(P.done + (p - 1), (unsigned)P.ph[p - 1].ntiles);
+      if (et == 0) ok = W.count(P.done + (p - 1), (unsigned)P.ph[p - 1].ntiles + (p == 1 ? (unsigned)P.stall : 0u));
       if (!MOE && et == 0) PTRACE(p, 5);
       if (!epi_all(ok)) return false;
       const PsJob& S = P.job[F.src_job];
@@ -993,7 +996,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) prefill_pass_kernel(const __gri
 // sums of 4 columns combined by a butterfly; tiles added in two halves), so a launch
 // that starts here and one that reaches the same input at a phase boundary make
 // identical inputs.  Block 0 also clears the launch's counters and status word.
-__global__ void __launch_bounds__(256) pass_input_kernel(const float* __restrict__ src, int B, int K,
+__global__ void __launch_bounds__(256) pgq_pass_input_kernel(const float* __restrict__ src, int B, int K,
                                                          const float* __restrict__ gamma, float eps, float* tap,
                                                          __half* __restrict__ xh, float* __restrict__ xinv,
                                                          unsigned* counters, int ncounters, int* status) {
@@ -1061,7 +1064,7 @@ __global__ void __launch_bounds__(256) pass_input_kernel(const float* __restrict
 // The gathered input of a grouped expert bank: row i = x[ent[i] / xdiv] in binary16
 // with a power-of-two scale (xinv[i] its inverse), one block per row.  Block 0 also
 // clears the launch's counters and status word.
-__global__ void __launch_bounds__(256) moe_input_kernel(const float* __restrict__ x, int K,
+__global__ void __launch_bounds__(256) pgq_moe_input_kernel(const float* __restrict__ x, int K,
                                                         const int32_t* __restrict__ ent, int nent, int xrows,
                                                         int xdiv, __half* __restrict__ xh, float* __restrict__ xinv,
                                                         unsigned* counters, int ncounters, int* status) {
@@ -1254,7 +1257,7 @@ Plan make_plan(const HostPhase* hp, int nph, int B, const DeviceInfo& dev) {
 
 std::mutex g_launch_mu;   // guards the parameter block and the tensor-map cache
 
-// One pass_input_kernel launch (the first phase's input) and one cooperative launch
+// One pgq_pass_input_kernel launch (the first phase's input) and one cooperative launch
 // of the phases.  x0 / gamma0 / tap0 make the first phase's input.
 int launch_phases(const HostPhase* hp, int nph, const float* x0, const float* gamma0, float* tap0, float eps, int B,
                   void* ws, size_t ws_bytes, unsigned long long wait_limit_ns, const DeviceInfo& dev,
@@ -1328,7 +1331,8 @@ int launch_phases(const HostPhase* hp, int nph, const float* x0, const float* ga
   P.stats = reinterpret_cast<float2*>(w + pl.off_stats);
   P.partials = reinterpret_cast<float*>(w + pl.off_part);
   P.status = reinterpret_cast<int*>(w + pl.off_status);
-  P.wait_limit_ns = wait_limit_ns ? wait_limit_ns : 2000000000ull;
+  P.wait_limit_ns = wait_limit_ns ? wait_limit_ns : pgq::wait_limit_ns();
+  P.stall = (nph > 1 && stall_injected()) ? 1 : 0;
   P.eps = eps;
   P.nph = nph;
   P.B = B;
@@ -1349,16 +1353,16 @@ int launch_phases(const HostPhase* hp, int nph, const float* x0, const float* ga
     P.moff = moe->off;
     P.ments = moe->ent;
     P.mxinv = xinv;
-    moe_input_kernel<<<moe->nent, 256, 0, st>>>(moe->x, K0, moe->ent, moe->nent, moe->xrows, moe->xdiv,
+    pgq_moe_input_kernel<<<moe->nent, 256, 0, st>>>(moe->x, K0, moe->ent, moe->nent, moe->xrows, moe->xdiv,
                                                 P.xh[hp[0].xk], xinv, cnt, pl.ncounters, P.status);
   } else {
-    pass_input_kernel<<<pl.Bp, 256, (size_t)(K0 / TC_BM) * sizeof(float2), st>>>(
+    pgq_pass_input_kernel<<<pl.Bp, 256, (size_t)(K0 / TC_BM) * sizeof(float2), st>>>(
         x0, B, K0, gamma0, eps, tap0, P.xh[hp[0].xk], xinv, cnt, pl.ncounters, P.status);
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e);
 
-  const void* fn = moe ? reinterpret_cast<const void*>(&prefill_pass_kernel<true>)
-                      : reinterpret_cast<const void*>(&prefill_pass_kernel<false>);
+  const void* fn = moe ? reinterpret_cast<const void*>(&pgq_prefill_pass_kernel<true>)
+                      : reinterpret_cast<const void*>(&pgq_prefill_pass_kernel<false>);
   {
     static std::map<std::pair<const void*, int>, size_t> done;   // guarded by the launch lock
     size_t& cur = done[{fn, dev.device}];

@@ -1,12 +1,14 @@
 """The allocation-free vocab-head entry point (pgq_gemv_f16_argmax_static).
 
-Some callers cannot allocate device memory at the moment they need a projection:
-code running while a CUDA graph is captured, decode loops that cannot afford the
-synchronisation an allocation may cause, or plugins inside a framework that owns
-all device memory.  For them the library keeps the argmax scratch in a fixed device
-array.  This test calls that entry point through the C ABI twice in a row and
-checks each result against the ordinary entry point, which takes caller-allocated
-scratch.  It lives in its own file, collected last.
+Some callers cannot allocate device memory at the moment they need the vocab head:
+a plugin living inside a host framework that owns every byte of device memory
+through its own pools, or a decode loop that cannot take the device-wide
+synchronisation an allocation may bring.  For them the library keeps the argmax
+scratch in a fixed device array.  This test calls that entry point through the C
+ABI several times in a row (one position, which takes the CUDA-core kernel, and 3
+and 8 positions, which take the tensor-core kernel) and checks each result against
+the ordinary entry point, which takes caller-allocated scratch, and against the
+oracle.  It lives in its own file, collected last.
 """
 import ctypes as C
 
@@ -31,7 +33,7 @@ def test_static_scratch_matches_caller_scratch_twice():
     import prefill_gemv_q8_gb300 as pgq
     L = pgq.lib()
     rows, cols = 6000, 4096
-    for call, B in enumerate((3, 8)):
+    for call, B in enumerate((1, 3, 8, 1)):
         W = synth.f16_matrix(rows, cols, 960, call)
         W[4321] = W[17]                                    # an exact tie: row 17 must win
         x = synth.normal((B, cols), 1.0, 961, call)
@@ -51,6 +53,7 @@ def test_static_scratch_matches_caller_scratch_twice():
         torch.cuda.synchronize()
         ref = oracle.vocab_head(x, g, 1e-6, W)
         check_proj(host(lg_s), host(lg_w), ref["e"], tol=TOL, what="static vs caller scratch logits")
+        check_proj(host(lg_s), ref["logits"], ref["e"], tol=TOL, what="static scratch logits vs oracle")
         assert host(ids_s).tolist() == host(ids_w).tolist()
         assert host(ids_s).tolist() == oracle.argmax(host(lg_s)).tolist()
         assert int(host(ids_s)[0]) == 17
