@@ -378,6 +378,47 @@ def bench_tiny_mlp(torch, pgq, synth, steps, warmup, pk):
             "note": "launch-latency bound (4 MiB is 0.6 us at HBM peak); weights rotate over 64 copies"}
 
 
+def bench_q82f_layer(torch, pgq, synth, steps, warmup, pk):
+    """The decode layer's shapes in the pages' q8_2f format (int8 body, row scale,
+    column field): one CUDA graph of `steps` layer calls (two launches each, weights
+    loaded once, three weight copies in rotation), like the headline."""
+    c = synth.Q8_LAYER
+    H, KV, I, wl = c["hidden"], c["kv"], c["inter"], c["workload"]
+    base = synth.q82f_layer(wl, 0, H, KV, I, "torch", "cuda")
+    copies = [base] + [{s: tuple(t.clone() for t in m) for s, m in base.items()} for _ in range(2)]
+    structs = [pgq.q82f_layer_struct(m) for m in copies]
+    x = synth.normal((H,), 1.0, wl, synth.T_X, "torch", "cuda")
+    xo = synth.normal((H,), 1.0, wl, synth.T_XO, "torch", "cuda")
+    g = synth.gamma(H, wl, backend="torch", device="cuda")
+    f = lambda n: torch.empty(n, dtype=torch.float32, device="cuda")  # noqa: E731
+    out = dict(q=f(H), k=f(KV), v=f(KV), o=f(H), u=f(I), down=f(H))
+    it = [0]
+
+    def step():
+        L = structs[it[0] % len(structs)]
+        it[0] += 1
+        pgq.q82f_decode_layer(L, x, xo, g, 1e-6, out=out, weights_stable=True)
+
+    g_warm = _capture(torch, lambda: [step() for _ in range(warmup)])
+    g_all = _capture(torch, lambda: [step() for _ in range(steps)])
+    g_all.replay()
+    g_warm.replay()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    a, b = _events(torch, 2)
+    a.record(st)
+    g_all.replay()
+    b.record(st)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    nbytes = sum(r * cc + 2 * r + 2 * cc for r, cc in synth.q8_layer_shapes(H, KV, I).values())
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": "q8_2f decode layer B=1 (hidden 4096, kv 1024, inter 14336; int8 body, f16 row scale, "
+                        "f16 column field)", "metric": "weight GB/s", "value": round(gbs, 1),
+            "us_per_step": round(ms * 1e3, 3), "frac_of_hbm": round(gbs / pk["hbm"], 4), "weight_bytes": nbytes,
+            "launches_per_step": 2, "timed": "one CUDA graph of the K steps, three weight copies in rotation"}
+
+
 def bench_vocab(torch, pgq, synth, steps, warmup, pk):
     c = synth.VOCAB
     V, H, wl = c["vocab"], c["hidden"], c["workload"]
@@ -545,7 +586,7 @@ def main():
     ap.add_argument("--impl", default="pgq", choices=["pgq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-prefill", action="store_true", help="only the headline decode layer")
-    ap.add_argument("--only", choices=["decode", "prefill", "moe", "vocab"], default=None,
+    ap.add_argument("--only", choices=["decode", "prefill", "moe", "vocab", "q82f"], default=None,
                     help="profiling aid: run one workload and print its JSON object")
     ap.add_argument("--no-graph", action="store_true", help="profiling aid (--only moe): direct calls only")
     ap.add_argument("--prefill-layers", type=int, default=None, help="layers of the prefill pass (default 32)")
@@ -588,6 +629,9 @@ def main():
     if args.only == "moe":
         print(json.dumps(bench_moe(torch, pgq, synth, args.steps, args.warmup, pk, graph=not args.no_graph)),
               flush=True)
+        return
+    if args.only == "q82f":
+        print(json.dumps(bench_q82f_layer(torch, pgq, synth, args.steps, args.warmup, pk)), flush=True)
         return
     if args.only == "vocab":
         print(json.dumps(bench_vocab(torch, pgq, synth, args.steps, args.warmup, pk)), flush=True)
@@ -638,6 +682,8 @@ def main():
         line["workloads"]["vocab_head"] = bench_vocab(torch, pgq, synth, args.steps, args.warmup, pk)
         torch.cuda.empty_cache()
         line["workloads"]["tiny_mlp"] = bench_tiny_mlp(torch, pgq, synth, args.steps, args.warmup, pk)
+        torch.cuda.empty_cache()
+        line["workloads"]["q8_2f_decode_layer"] = bench_q82f_layer(torch, pgq, synth, args.steps, args.warmup, pk)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_q8()
     if rank == 0:

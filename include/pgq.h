@@ -123,6 +123,38 @@ int pgq_debug_stall(int on);
 int pgq_add_rmsnorm(float* h, const float* add, const float* gamma, float eps, int B, int n,
                     float* y, float* inv_rms, void* stream);
 
+/* add + RMSNorm with the layer scale and the Gemma weight form of gemma_batch.rs
+ * `g4_add_norm_b` (the page's `scale` word, 0 meaning none, and its `gemma` switch):
+ *   h[b] <- (h[b] + add[b]) * scale      (add may be NULL; scale == 0: no scale)
+ *   y[b][i] = w[i] * (h[b][i] * inv[b]),  w = 1 + gamma with PGQ_NORM_GEMMA, else gamma
+ * Other arguments and limits as pgq_add_rmsnorm (which is this call with scale 0
+ * and no flags); scale must be finite.  h is written only when add or scale is
+ * given. */
+#define PGQ_NORM_GEMMA 1
+int pgq_add_rmsnorm_ex(float* h, const float* add, const float* gamma, float eps, float scale, int flags,
+                       int B, int n, float* y, float* inv_rms, void* stream);
+
+/* ---------------------------------------------------------------- sandwich residual
+ * Gemma's sandwich residual in one launch (gemma_batch.rs `g4_sandwich`): for each
+ * position b, the mixer's (or FFN's) output norm, the scaled residual add and the
+ * next norm,
+ *   mid = w1' * (x[b] * inv1),           inv1 = 1/sqrt(mean x[b]^2 + eps)
+ *   h[b] <- (h[b] + mid) * scale          (scale == 0: no scale)
+ *   out[b] = w2' * (h[b] * inv2),        inv2 = 1/sqrt(mean h[b]^2 + eps)
+ * with w' = 1 + w under PGQ_NORM_GEMMA.  Bit-identical to the chain
+ *   pgq_add_rmsnorm_ex(x, NULL, w1, eps, 0, flags, B, n, mid, inv1)
+ *   pgq_add_rmsnorm_ex(h, mid, w2, eps, scale, flags, B, n, out, inv2)
+ * (the same per-position code runs in both), one launch instead of two.
+ * x: device f32 [B][n] (read only); w1, w2: device f32 [n]; h: device f32 [B][n]
+ * in place; out: device f32 [B][n]; mid: device f32 [B][n] or NULL (then not
+ * written); inv1, inv2: device f32 [B] or NULL.  4 <= n <= PGQ_SANDWICH_NMAX,
+ * n % 4 == 0, 1 <= B <= 65535; x, w1, h, w2, out, mid 16-byte aligned; x, h, out and
+ * mid must not overlap. */
+#define PGQ_SANDWICH_NMAX 16384
+int pgq_sandwich_rmsnorm(const float* x, const float* w1, float* h, const float* w2, float eps, float scale,
+                         int flags, int B, int n, float* out, float* mid, float* inv1, float* inv2,
+                         void* stream);
+
 /* ---------------------------------------------------------------- a5: relu²
  * v[i] <- max(v[i], 0)^2 in place (nemotron_prefill.rs `pb_relu2`).  v: device f32 [n],
  * 16-byte aligned.  n == 0 is a no-op. */
@@ -213,6 +245,37 @@ typedef struct {
 } pgq_input;
 int pgq_gemv_q8_multi(const pgq_q8_job* jobs, int njobs, const pgq_input* inputs, int ninputs,
                       int cols, int B, float eps, void* stream);
+
+/* ---------------------------------------------------------------- q8_2f format
+ * The weight format of the pages' own q8 projections (gemma_batch.rs `Q82_MM_WGSL`
+ * and `q8_2f_mm_r2`; the q8_2f bank payload of nemotron_prefill.rs `pb_q8_bank`):
+ * an int8 body [rows][cols], one binary16 scale per row and one binary16 factor per
+ * column (the "column field"):
+ *   w[r][c] = row_scale[r] * codes[r][c] * col_field[c]
+ *   y[b][r] = epilogue( row_scale[r] * sum_c codes[r][c] * (col_field[c] * xin[b][c]) )
+ * As on the page, the column field folds into the input values (f32) and the row
+ * scale multiplies the finished sum.  The page's single payload buffer maps to
+ * codes = buf, row_scale = buf + rows*cols bytes, col_field = row_scale + rows.
+ * codes: device int8 [rows][cols], 16-byte aligned; row_scale: device binary16
+ * [rows], 2-byte aligned; col_field: device binary16 [cols], 16-byte aligned;
+ * x, gamma, y, residual, epilogue and limits as pgq_gemv_q8. */
+int pgq_gemv_q82f(const int8_t* codes, const uint16_t* row_scale, const uint16_t* col_field, int rows, int cols,
+                  const float* x, int B, const float* gamma, float eps, float* y, int epilogue,
+                  const float* residual, void* stream);
+
+/* The q8 decode layer (as pgq_q8_decode_layer_ex) with q8_2f matrices. */
+typedef struct {
+  const int8_t* codes;
+  const uint16_t* row_scale;
+  const uint16_t* col_field;
+} pgq_q82f_matrix;
+typedef struct {
+  pgq_q82f_matrix q, k, v, o, up, down;
+  int hidden, kv, inter;
+} pgq_q82f_layer;
+int pgq_q82f_decode_layer(const pgq_q82f_layer* layer, const float* x, const float* x_o, const float* gamma,
+                          float eps, float* q, float* k, float* v, float* o, float* u, float* down, int flags,
+                          void* stream);
 
 /* ---------------------------------------------------------------- decode workloads
  * Tiny f16 MLP block for one position (the embryo_wide.wgsl `w_norm` → `w_ffn_up`

@@ -46,6 +46,16 @@ class MoeLayer(C.Structure):
                 ("E", C.c_int), ("k", C.c_int), ("hidden", C.c_int), ("inter", C.c_int), ("renorm", C.c_int)]
 
 
+class Q82Matrix(C.Structure):
+    _fields_ = [("codes", _vp), ("row_scale", _vp), ("col_field", _vp)]
+
+
+class Q82Layer(C.Structure):
+    _fields_ = [("q", Q82Matrix), ("k", Q82Matrix), ("v", Q82Matrix), ("o", Q82Matrix),
+                ("up", Q82Matrix), ("down", Q82Matrix),
+                ("hidden", C.c_int), ("kv", C.c_int), ("inter", C.c_int)]
+
+
 class Q8Layer(C.Structure):
     _fields_ = [("q", Q8Matrix), ("k", Q8Matrix), ("v", Q8Matrix), ("o", Q8Matrix),
                 ("up", Q8Matrix), ("down", Q8Matrix),
@@ -58,6 +68,10 @@ _SIGS = {
     "pgq_abi_version": (C.c_int, []),
     "pgq_device_check": (C.c_int, []),
     "pgq_add_rmsnorm": (C.c_int, [_vp, _vp, _vp, C.c_float, C.c_int, C.c_int, _vp, _vp, _vp]),
+    "pgq_add_rmsnorm_ex": (C.c_int, [_vp, _vp, _vp, C.c_float, C.c_float, C.c_int, C.c_int, C.c_int, _vp, _vp,
+                                     _vp]),
+    "pgq_sandwich_rmsnorm": (C.c_int, [_vp, _vp, _vp, _vp, C.c_float, C.c_float, C.c_int, C.c_int, C.c_int, _vp,
+                                       _vp, _vp, _vp, _vp]),
     "pgq_relu2": (C.c_int, [_vp, C.c_size_t, _vp]),
     "pgq_gemv_f16": (C.c_int, [_vp, C.c_int, C.c_int, _vp, C.c_int, _vp, C.c_float, _vp, C.c_int, _vp, _vp]),
     "pgq_argmax_workspace_bytes": (C.c_size_t, [C.c_int]),
@@ -68,6 +82,10 @@ _SIGS = {
     "pgq_gemv_q8": (C.c_int, [_vp, _vp, C.c_int, C.c_int, _vp, C.c_int, _vp, C.c_float, _vp, C.c_int, _vp, _vp]),
     "pgq_gemv_q8_multi": (C.c_int, [C.POINTER(Q8Job), C.c_int, C.POINTER(Input), C.c_int, C.c_int, C.c_int,
                                     C.c_float, _vp]),
+    "pgq_gemv_q82f": (C.c_int, [_vp, _vp, _vp, C.c_int, C.c_int, _vp, C.c_int, _vp, C.c_float, _vp, C.c_int, _vp,
+                                _vp]),
+    "pgq_q82f_decode_layer": (C.c_int, [C.POINTER(Q82Layer), _vp, _vp, _vp, C.c_float, _vp, _vp, _vp, _vp, _vp,
+                                        _vp, C.c_int, _vp]),
     "pgq_mlp_f16_decode": (C.c_int, [_vp, _vp, _vp, C.c_int, C.c_int, _vp, C.c_float, _vp, _vp, _vp]),
     "pgq_q8_decode_layer": (C.c_int, [C.POINTER(Q8Layer), _vp, _vp, _vp, C.c_float, _vp, _vp, _vp, _vp, _vp,
                                       _vp, _vp]),
@@ -171,6 +189,41 @@ def add_rmsnorm(h, gamma, eps, add=None, y=None, inv=None, stream=None):
         _need(inv, torch.float32, "inv", (B,))
     _check(lib().pgq_add_rmsnorm(_ptr(h), _ptr(add), _ptr(gamma), eps, B, n, _ptr(y), _ptr(inv), _stream(stream)))
     return y
+
+
+NORM_GEMMA = 1
+
+
+def add_rmsnorm_ex(h, gamma, eps, add=None, scale=0.0, gemma=False, y=None, inv=None, stream=None):
+    """h <- (h + add)·scale in place (scale 0: none), y = w·(h·inv) with w = 1 + gamma
+    when ``gemma``; returns y."""
+    _need(h, torch.float32, "h")
+    B, n = h.shape
+    _need(gamma, torch.float32, "gamma", (n,))
+    if add is not None:
+        _need(add, torch.float32, "add", (B, n))
+    if y is None:
+        y = torch.empty_like(h)
+    _check(lib().pgq_add_rmsnorm_ex(_ptr(h), _ptr(add), _ptr(gamma), eps, float(scale), NORM_GEMMA if gemma else 0,
+                                    B, n, _ptr(y), _ptr(inv), _stream(stream)))
+    return y
+
+
+def sandwich_rmsnorm(x, w1, h, w2, eps, scale=0.0, gemma=False, out=None, mid=None, inv1=None, inv2=None,
+                     stream=None):
+    """Gemma's sandwich residual in one launch: mid = rms(x)·w1', h <- (h + mid)·scale,
+    out = rms(h)·w2' (w' = 1 + w when ``gemma``); returns out."""
+    _need(x, torch.float32, "x")
+    B, n = x.shape
+    _need(h, torch.float32, "h", (B, n))
+    _need(w1, torch.float32, "w1", (n,))
+    _need(w2, torch.float32, "w2", (n,))
+    if out is None:
+        out = torch.empty_like(h)
+    _check(lib().pgq_sandwich_rmsnorm(_ptr(x), _ptr(w1), _ptr(h), _ptr(w2), eps, float(scale),
+                                      NORM_GEMMA if gemma else 0, B, n, _ptr(out), _ptr(mid), _ptr(inv1), _ptr(inv2),
+                                      _stream(stream)))
+    return out
 
 
 def relu2(v, stream=None):
@@ -357,6 +410,52 @@ def mlp_f16_decode(h, W_up, W_down, gamma, eps=1e-6, u=None, y=None, stream=None
     _check(lib().pgq_mlp_f16_decode(_ptr(h), _ptr(W_up), _ptr(W_down), hidden, inter, _ptr(gamma), eps, _ptr(u),
                                     _ptr(y), _stream(stream)))
     return y, u
+
+
+def _q82f_check(codes, rs, cf, name="W"):
+    _need(codes, torch.int8, name + ".codes")
+    rows, cols = codes.shape
+    _need(rs, torch.float16, name + ".row_scale", (rows,))
+    _need(cf, torch.float16, name + ".col_field", (cols,))
+
+
+def gemv_q82f(codes, row_scale, col_field, x, gamma=None, eps=1e-6, epilogue="none", residual=None, y=None,
+              stream=None):
+    """y[b] = epilogue(row_scale ⊙ (codes · (col_field ⊙ xin[b]))) for a q8_2f matrix."""
+    _q82f_check(codes, row_scale, col_field)
+    rows, cols = codes.shape
+    _need(x, torch.float32, "x")
+    x2 = x.view(-1, cols)
+    B = x2.shape[0]
+    if y is None:
+        y = torch.empty(B, rows, dtype=torch.float32, device=x.device)
+    _check(lib().pgq_gemv_q82f(_ptr(codes), _ptr(row_scale), _ptr(col_field), rows, cols, _ptr(x2), B, _ptr(gamma),
+                               eps, _ptr(y), _epi(epilogue), _ptr(residual), _stream(stream)))
+    return y
+
+
+def q82f_layer_struct(mats):
+    """ctypes view of a q8_2f decode layer {slot: (codes, row_scale, col_field)}."""
+    L = Q82Layer()
+    for s in ("q", "k", "v", "o", "up", "down"):
+        c, r, f = mats[s]
+        _q82f_check(c, r, f, s)
+        setattr(L, s, Q82Matrix(c.data_ptr(), r.data_ptr(), f.data_ptr()))
+    L.hidden, L.kv, L.inter = mats["q"][0].shape[1], mats["k"][0].shape[0], mats["up"][0].shape[0]
+    return L
+
+
+def q82f_decode_layer(mats, x, x_o, gamma, eps=1e-6, out=None, stream=None, weights_stable=False):
+    """The decode layer with q8_2f matrices (see q8_decode_layer); ``mats`` maps slot →
+    (codes, row_scale, col_field), or is a prebuilt Q82Layer."""
+    L = mats if isinstance(mats, Q82Layer) else q82f_layer_struct(mats)
+    if out is None:
+        out = {s: torch.empty(n, dtype=torch.float32, device=x.device) for s, n in
+               (("q", L.hidden), ("k", L.kv), ("v", L.kv), ("o", L.hidden), ("u", L.inter), ("down", L.hidden))}
+    _check(lib().pgq_q82f_decode_layer(C.byref(L), _ptr(x), _ptr(x_o), _ptr(gamma), eps, _ptr(out["q"]),
+                                       _ptr(out["k"]), _ptr(out["v"]), _ptr(out["o"]), _ptr(out["u"]),
+                                       _ptr(out["down"]), WEIGHTS_STABLE if weights_stable else 0, _stream(stream)))
+    return out
 
 
 def q8_layer_struct(mats):

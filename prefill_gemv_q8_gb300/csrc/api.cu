@@ -3,6 +3,7 @@
 #include <cstdarg>
 #include <cstdlib>
 #include <cstdio>
+#include <cmath>
 #include <algorithm>
 #include <atomic>
 #include <mutex>
@@ -149,7 +150,50 @@ int pgq_add_rmsnorm(float* h, const float* add, const float* gamma, float eps, i
   REQUIRE(!overlaps(y, bytes, h, bytes) && (!add || !overlaps(y, bytes, add, bytes)), PGQ_EINVAL,
           "add_rmsnorm: y must not overlap h or add");
   GET_DEVICE(dev);
-  return launch_add_rmsnorm(h, add, gamma, eps, B, n, y, inv_rms, as_stream(stream));
+  return launch_add_rmsnorm(h, add, gamma, eps, 0.f, 0, B, n, y, inv_rms, as_stream(stream));
+}
+
+int pgq_add_rmsnorm_ex(float* h, const float* add, const float* gamma, float eps, float scale, int flags, int B, int n,
+                       float* y, float* inv_rms, void* stream) {
+  REQUIRE((flags & ~PGQ_NORM_GEMMA) == 0, PGQ_EINVAL, "add_rmsnorm_ex: unknown flags 0x%x", flags);
+  REQUIRE(scale == scale && scale != INFINITY && scale != -INFINITY, PGQ_EINVAL, "add_rmsnorm_ex: scale must be finite");
+  REQUIRE(h && gamma && y, PGQ_EINVAL, "add_rmsnorm_ex: h, gamma and y must be non-null");
+  REQUIRE(B >= 1 && B <= 65535, PGQ_EINVAL, "add_rmsnorm_ex: B=%d outside 1..65535", B);
+  REQUIRE(n >= 4 && n <= (1 << 20) && n % 4 == 0, PGQ_EINVAL, "add_rmsnorm_ex: n=%d must be a multiple of 4 in 4..2^20",
+          n);
+  REQUIRE(eps >= 0.f, PGQ_EINVAL, "add_rmsnorm_ex: eps must be >= 0");
+  REQUIRE(aligned16(h) && aligned16(gamma) && aligned16(y) && (!add || aligned16(add)), PGQ_EALIGN,
+          "add_rmsnorm_ex: h, add, gamma, y must be 16-byte aligned");
+  REQUIRE(!inv_rms || aligned4(inv_rms), PGQ_EALIGN, "add_rmsnorm_ex: inv_rms must be 4-byte aligned");
+  const size_t bytes = (size_t)B * n * sizeof(float);
+  REQUIRE(!overlaps(y, bytes, h, bytes) && (!add || !overlaps(y, bytes, add, bytes)), PGQ_EINVAL,
+          "add_rmsnorm_ex: y must not overlap h or add");
+  GET_DEVICE(dev);
+  return launch_add_rmsnorm(h, add, gamma, eps, scale, (flags & PGQ_NORM_GEMMA) ? 1 : 0, B, n, y, inv_rms,
+                            as_stream(stream));
+}
+
+int pgq_sandwich_rmsnorm(const float* x, const float* w1, float* h, const float* w2, float eps, float scale, int flags,
+                         int B, int n, float* out, float* mid, float* inv1, float* inv2, void* stream) {
+  REQUIRE((flags & ~PGQ_NORM_GEMMA) == 0, PGQ_EINVAL, "sandwich_rmsnorm: unknown flags 0x%x", flags);
+  REQUIRE(scale == scale && scale != INFINITY && scale != -INFINITY, PGQ_EINVAL,
+          "sandwich_rmsnorm: scale must be finite");
+  REQUIRE(x && w1 && h && w2 && out, PGQ_EINVAL, "sandwich_rmsnorm: x, w1, h, w2 and out must be non-null");
+  REQUIRE(B >= 1 && B <= 65535, PGQ_EINVAL, "sandwich_rmsnorm: B=%d outside 1..65535", B);
+  REQUIRE(n >= 4 && n <= PGQ_SANDWICH_NMAX && n % 4 == 0, PGQ_EINVAL,
+          "sandwich_rmsnorm: n=%d must be a multiple of 4 in 4..%d", n, PGQ_SANDWICH_NMAX);
+  REQUIRE(eps >= 0.f, PGQ_EINVAL, "sandwich_rmsnorm: eps must be >= 0");
+  REQUIRE(aligned16(x) && aligned16(w1) && aligned16(h) && aligned16(w2) && aligned16(out) && (!mid || aligned16(mid)),
+          PGQ_EALIGN, "sandwich_rmsnorm: x, w1, h, w2, out and mid must be 16-byte aligned");
+  REQUIRE((!inv1 || aligned4(inv1)) && (!inv2 || aligned4(inv2)), PGQ_EALIGN, "sandwich_rmsnorm: inv1/inv2 4-byte");
+  const size_t bytes = (size_t)B * n * sizeof(float);
+  REQUIRE(!overlaps(out, bytes, h, bytes) && !overlaps(out, bytes, x, bytes) && !overlaps(h, bytes, x, bytes),
+          PGQ_EINVAL, "sandwich_rmsnorm: x, h and out must not overlap");
+  REQUIRE(!mid || (!overlaps(mid, bytes, x, bytes) && !overlaps(mid, bytes, h, bytes) && !overlaps(mid, bytes, out, bytes)),
+          PGQ_EINVAL, "sandwich_rmsnorm: mid must not overlap x, h or out");
+  GET_DEVICE(dev);
+  return launch_sandwich(x, w1, h, w2, eps, scale, (flags & PGQ_NORM_GEMMA) ? 1 : 0, B, n, out, mid, inv1, inv2, dev,
+                         as_stream(stream));
 }
 
 int pgq_relu2(float* v, size_t n, void* stream) {
@@ -333,6 +377,95 @@ int gemv_q8_multi_impl(const pgq_q8_job* jobs, int njobs, const pgq_input* input
   return launch_gemv(P, true, false, dev, as_stream(stream));
 }
 }  // namespace
+
+// ------------------------------------------------------------------ q8_2f decode
+namespace {
+// One launch of q8_2f projections sharing cols and B (the TMA decode kernel only).
+struct Q82Job {
+  const int8_t* codes;
+  const uint16_t* rs;
+  const uint16_t* cf;
+  int rows, input;
+  float* y;
+  int epilogue;
+  const float* residual;
+};
+int gemv_q82f_multi_impl(const Q82Job* jobs, int njobs, const pgq_input* inputs, int ninputs, int cols, int B,
+                         float eps, int early_weights, void* stream) {
+  REQUIRE(njobs >= 1 && njobs <= PGQ_MULTI_MAX && ninputs >= 1 && ninputs <= MAX_INPUTS, PGQ_EINVAL,
+          "gemv_q82f: %d jobs, %d inputs", njobs, ninputs);
+  REQUIRE((size_t)ninputs * B * cols <= PGQ_STAGE_MAX, PGQ_EUNSUPPORTED,
+          "gemv_q82f: ninputs*B*cols=%d exceeds %d staged values", ninputs * B * cols, PGQ_STAGE_MAX);
+  for (int i = 0; i < ninputs; ++i) {
+    int st = check_decode_common("gemv_q82f", 1, cols, inputs[i].x, B, inputs[i].gamma, eps, nullptr, PGQ_EPI_NONE,
+                                 nullptr);
+    if (st) return st;
+  }
+  GvParams P{};
+  for (int j = 0; j < njobs; ++j) {
+    const Q82Job& J = jobs[j];
+    REQUIRE(J.codes && J.rs && J.cf && J.y, PGQ_EINVAL, "gemv_q82f: job %d has a null codes/row_scale/col_field/y", j);
+    REQUIRE(aligned16(J.codes) && aligned16(J.cf) && (reinterpret_cast<uintptr_t>(J.rs) & 1) == 0, PGQ_EALIGN,
+            "gemv_q82f: job %d codes and col_field 16-byte, row_scale 2-byte aligned", j);
+    REQUIRE(J.input >= 0 && J.input < ninputs, PGQ_EINVAL, "gemv_q82f: job %d input %d out of range", j, J.input);
+    int st = check_decode_common("gemv_q82f", J.rows, cols, inputs[J.input].x, B, inputs[J.input].gamma, eps, J.y,
+                                 J.epilogue, J.residual);
+    if (st) return st;
+    for (int i = 0; i < ninputs; ++i)
+      REQUIRE(!overlaps(J.y, (size_t)B * J.rows * 4, inputs[i].x, (size_t)B * cols * 4), PGQ_EINVAL,
+              "gemv_q82f: job %d output overlaps input %d", j, i);
+    GvJob g{};
+    g.w = reinterpret_cast<const uint8_t*>(J.codes);
+    g.y = J.y;
+    g.residual = J.residual;
+    g.rows = J.rows;
+    g.input = J.input;
+    g.epilogue = J.epilogue;
+    g.rs = J.rs;
+    g.cf = J.cf;
+    P.job[j] = g;
+  }
+  GET_DEVICE(dev);
+  for (int i = 0; i < ninputs; ++i) P.in[i] = GvInput{inputs[i].x, inputs[i].gamma};
+  P.njobs = njobs;
+  P.ninputs = ninputs;
+  P.B = B;
+  P.cols = cols;
+  P.eps = eps;
+  P.early_weights = early_weights;
+  P.q82f = 1;
+  return launch_gemv(P, true, false, dev, as_stream(stream));
+}
+}  // namespace
+
+int pgq_gemv_q82f(const int8_t* codes, const uint16_t* row_scale, const uint16_t* col_field, int rows, int cols,
+                  const float* x, int B, const float* gamma, float eps, float* y, int epilogue, const float* residual,
+                  void* stream) {
+  const Q82Job job{codes, row_scale, col_field, rows, 0, y, epilogue, residual};
+  const pgq_input in{x, gamma};
+  return gemv_q82f_multi_impl(&job, 1, &in, 1, cols, B, eps, 0, stream);
+}
+
+int pgq_q82f_decode_layer(const pgq_q82f_layer* L, const float* x, const float* x_o, const float* gamma, float eps,
+                          float* q, float* k, float* v, float* o, float* u, float* down, int flags, void* stream) {
+  REQUIRE(L && x && x_o && gamma && q && k && v && o && u && down, PGQ_EINVAL, "q82f_decode_layer: null pointer");
+  REQUIRE((flags & ~PGQ_WEIGHTS_STABLE) == 0, PGQ_EINVAL, "q82f_decode_layer: unknown flags 0x%x", flags);
+  const int H = L->hidden, KV = L->kv, I = L->inter;
+  const Q82Job jobs[5] = {
+      {L->q.codes, L->q.row_scale, L->q.col_field, H, 0, q, PGQ_EPI_NONE, nullptr},
+      {L->k.codes, L->k.row_scale, L->k.col_field, KV, 0, k, PGQ_EPI_NONE, nullptr},
+      {L->v.codes, L->v.row_scale, L->v.col_field, KV, 0, v, PGQ_EPI_NONE, nullptr},
+      {L->o.codes, L->o.row_scale, L->o.col_field, H, 1, o, PGQ_EPI_NONE, nullptr},
+      {L->up.codes, L->up.row_scale, L->up.col_field, I, 0, u, PGQ_EPI_RELU2, nullptr},
+  };
+  const pgq_input ins[2] = {{x, gamma}, {x_o, nullptr}};
+  int st = gemv_q82f_multi_impl(jobs, 5, ins, 2, H, 1, eps, (flags & PGQ_WEIGHTS_STABLE) ? 1 : 0, stream);
+  if (st) return st;
+  // the down launch follows the launch above, which writes no weights
+  const Q82Job dj{L->down.codes, L->down.row_scale, L->down.col_field, H, 0, down, PGQ_EPI_NONE, nullptr};
+  const pgq_input din{u, nullptr};
+  return gemv_q82f_multi_impl(&dj, 1, &din, 1, I, 1, 0.f, 1, stream);
+}
 
 // ------------------------------------------------------------------ decode workloads
 int pgq_mlp_f16_decode(const float* h, const uint16_t* W_up, const uint16_t* W_down, int hidden, int inter,

@@ -39,14 +39,15 @@ constexpr int GV_THREADS = GV_WARPS * 32;
 //   CW:  columns per chunk (32 lanes x EPL),
 //   R:   rows per task (they share every staged-x read),
 //   U:   chunks per step (one cp.async group per step).
-template <bool Q8, int NB>
+template <int FMT, int NB>
 struct GvShape {
   static constexpr int R = 2;
   static constexpr int U = 2;
-  static constexpr int EPL = Q8 ? 16 : 8;
+  static constexpr int EPL = FMT != 0 ? 16 : 8;   // int8 codes: 16 per 16-byte load
   static constexpr int CW = 32 * EPL;
-  // bytes of one step in a warp's ring: codes (16 per lane per row-chunk) + q8 params
-  static constexpr int STEP_BYTES = R * U * 32 * (16 + (Q8 ? 4 : 0));
+  // bytes of one step in a warp's ring: codes (16 per lane per row-chunk) + the
+  // (scale, offset) words of the q8 block format
+  static constexpr int STEP_BYTES = R * U * 32 * (16 + (FMT == 1 ? 4 : 0));
 };
 
 __device__ __forceinline__ void group_sync(int group, int wpt) {
@@ -80,10 +81,13 @@ __device__ __forceinline__ int perm_col(int c) {
   return ch * CW + (t >> 2) * 128 + ln * 4 + (t & 3);
 }
 
-template <bool Q8, int NB, int ST, bool ARGMAX>
+// FMT: 0 binary16, 1 q8 block format, 2 q8_2f (w = row_scale·q·col_field: the lane's
+// q·cf products are exact in f32 and the row scale multiplies the finished sum).
+template <int FMT, int NB, int ST, bool ARGMAX>
 __global__ void __launch_bounds__(GV_THREADS, 1)
 pgq_gemv_kernel(const __grid_constant__ GvParams P) {
-  using SH = GvShape<Q8, NB>;
+  constexpr bool Q8 = FMT != 0, BLK = FMT == 1, F2 = FMT == 2;
+  using SH = GvShape<FMT, NB>;
   static_assert(GV_WARPS <= 16, "named barriers");
   constexpr int R = SH::R, U = SH::U, EPL = SH::EPL, CW = SH::CW;
   constexpr int ESZ = Q8 ? 1 : 2;
@@ -181,7 +185,7 @@ pgq_gemv_kernel(const __grid_constant__ GvParams P) {
         for (int u = 0; u < U; ++u) {
           if (u < nch && col0 + u * CW < cols) {
             cp_async16(slot + (uint32_t)(((r * U + u) * 32 + lane) * 16), wp + (size_t)u * CW * ESZ);
-            if constexpr (Q8)
+            if constexpr (BLK)
               cp_async4(slot + CODE_BYTES + (uint32_t)(((r * U + u) * 32 + lane) * 4),
                         J.params + row * pcols + ((col0 + u * CW) >> 5));
           }
@@ -244,10 +248,29 @@ pgq_gemv_kernel(const __grid_constant__ GvParams P) {
       const int ch = ch0 + u;
       if (u < nch && ch * CW + lane * EPL < cols) {
         float2 wv[R][EPL / 2];
+        float2 cfv[EPL / 2];   // q8_2f: the lane's column-field values
+        if constexpr (F2) {
+          const uint16_t* cf = P.job[c_job].cf + ch * CW + lane * EPL;
+#pragma unroll
+          for (int k = 0; k < EPL / 8; ++k) {
+            const uint4 c4 = __ldg(reinterpret_cast<const uint4*>(cf) + k);
+            cfv[4 * k] = h2_to_f2(c4.x); cfv[4 * k + 1] = h2_to_f2(c4.y);
+            cfv[4 * k + 2] = h2_to_f2(c4.z); cfv[4 * k + 3] = h2_to_f2(c4.w);
+          }
+        }
 #pragma unroll
         for (int r = 0; r < R; ++r) {
           const uint4 cw = *reinterpret_cast<const uint4*>(slot + ((r * U + u) * 32 + lane) * 16);
-          if constexpr (Q8) {
+          if constexpr (F2) {
+            const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              float2 lo, hi;
+              s8x4_to_f32(words[k], lo, hi);
+              wv[r][2 * k] = make_float2(lo.x * cfv[2 * k].x, lo.y * cfv[2 * k].y);
+              wv[r][2 * k + 1] = make_float2(hi.x * cfv[2 * k + 1].x, hi.y * cfv[2 * k + 1].y);
+            }
+          } else if constexpr (Q8) {
             const uint32_t pw = *reinterpret_cast<const uint32_t*>(slot + CODE_BYTES + ((r * U + u) * 32 + lane) * 4);
             const float2 so = h2_to_f2(pw);
             const float2 s2 = make_float2(so.x, so.x), o2 = make_float2(so.y, so.y);
@@ -324,6 +347,9 @@ pgq_gemv_kernel(const __grid_constant__ GvParams P) {
       const int rows = J.rows;
       const int row = row0 + r;
       const bool live = lane < N && row < rows && b < P.B;
+      if constexpr (F2) {
+        if (live) out *= __half2float(__ushort_as_half(J.rs[row]));
+      }
       if (live) {
         if (J.epilogue == PGQ_EPI_RELU2) {
           out = fmaxf(out, 0.f);
@@ -410,44 +436,42 @@ namespace {
 
 using KernelFn = void (*)(GvParams);
 
-template <bool Q8, int NB, bool ARGMAX>
+template <int FMT, int NB, bool ARGMAX>
 KernelFn pick(int st) {
-  return st >= 4 ? reinterpret_cast<KernelFn>(&pgq_gemv_kernel<Q8, NB, 4, ARGMAX>)
-                 : reinterpret_cast<KernelFn>(&pgq_gemv_kernel<Q8, NB, 2, ARGMAX>);
+  return st >= 4 ? reinterpret_cast<KernelFn>(&pgq_gemv_kernel<FMT, NB, 4, ARGMAX>)
+                 : reinterpret_cast<KernelFn>(&pgq_gemv_kernel<FMT, NB, 2, ARGMAX>);
 }
 
-KernelFn kernel_for(bool q8, int nb, bool argmax, int st) {
-  if (q8) {
-    switch (nb) {
-      case 1: return pick<true, 1, false>(st);
-      case 2: return pick<true, 2, false>(st);
-      case 4: return pick<true, 4, false>(st);
-      default: return pick<true, 8, false>(st);
-    }
+template <int FMT>
+KernelFn pick_nb(int nb, int st) {
+  switch (nb) {
+    case 1: return pick<FMT, 1, false>(st);
+    case 2: return pick<FMT, 2, false>(st);
+    case 4: return pick<FMT, 4, false>(st);
+    default: return pick<FMT, 8, false>(st);
   }
+}
+
+KernelFn kernel_for(bool q8, bool q82f, int nb, bool argmax, int st) {
+  if (q8) return q82f ? pick_nb<2>(nb, st) : pick_nb<1>(nb, st);
   if (argmax) {
     switch (nb) {
-      case 1: return pick<false, 1, true>(st);
-      case 2: return pick<false, 2, true>(st);
-      case 4: return pick<false, 4, true>(st);
-      default: return pick<false, 8, true>(st);
+      case 1: return pick<0, 1, true>(st);
+      case 2: return pick<0, 2, true>(st);
+      case 4: return pick<0, 4, true>(st);
+      default: return pick<0, 8, true>(st);
     }
   }
-  switch (nb) {
-    case 1: return pick<false, 1, false>(st);
-    case 2: return pick<false, 2, false>(st);
-    case 4: return pick<false, 4, false>(st);
-    default: return pick<false, 8, false>(st);
-  }
+  return pick_nb<0>(nb, st);
 }
 
 // (R, U, CW, bytes of a ring step) of the instance launch_gemv will pick
-void shape_of(bool q8, int nb, int* R, int* U, int* CW, int* step_bytes) {
+void shape_of(bool q8, bool q82f, int nb, int* R, int* U, int* CW, int* step_bytes) {
   (void)nb;
   *R = 2;
   *U = 2;
   *CW = 32 * (q8 ? 16 : 8);
-  *step_bytes = *R * *U * 32 * (16 + (q8 ? 4 : 0));
+  *step_bytes = *R * *U * 32 * (16 + (q8 && !q82f ? 4 : 0));
 }
 
 int round_nb(int B) { return B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : 8; }
@@ -547,7 +571,7 @@ int launch_gemv(GvParams& P, bool q8, bool argmax, const DeviceInfo& dev, cudaSt
   }
   const int nb = round_nb(P.B);
   int R, U, CW, step_bytes;
-  shape_of(q8, nb, &R, &U, &CW, &step_bytes);
+  shape_of(q8, P.q82f != 0, nb, &R, &U, &CW, &step_bytes);
   P.nchunks = (P.cols + CW - 1) / CW;
   P.cols_pad = P.nchunks * CW;
   // enough warps per task that each owns at most U chunks (one step), up to 8
@@ -572,7 +596,7 @@ int launch_gemv(GvParams& P, bool q8, bool argmax, const DeviceInfo& dev, cudaSt
   }
   if (smem + 2048 > dev.smem_optin)
     return set_error(PGQ_EUNSUPPORTED, "staged input needs %zu bytes of shared memory", smem);
-  KernelFn fn = kernel_for(q8, nb, argmax, stages);
+  KernelFn fn = kernel_for(q8, P.q82f != 0, nb, argmax, stages);
   if (cudaError_t e = allow_smem(fn, smem); e != cudaSuccess)
     return set_error(PGQ_ECUDA, "gemv: shared-memory limit %zu: %s", smem, cudaGetErrorString(e));
   int grid;

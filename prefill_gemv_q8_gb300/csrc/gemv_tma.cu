@@ -6,9 +6,9 @@
 // Stage = SR rows x all columns (<= 37 KB).  Warp w takes RPW = 2 rows (group
 // w / QW, QW = 32 / SR warps per group) and an even share of the 512-column chunks.
 // At one position the input values of a warp's columns live in registers for the
-// whole kernel, q8 uses dot-then-scale (the biased byte u = q + 128 is widened by one
-// byte-permute into the f32 2^15 + u, so the dot needs no conversion arithmetic), and
-// the partial dot products of 4 consecutive stages are reduced together: across
+// whole kernel, q8 uses dot-then-scale (codes converted exactly to f32, the per-block
+// scale applied once per 16 codes; q8_2f: the column field folded into the input
+// registers, the row scale applied to the finished sum), and the partial dot products of 4 consecutive stages are reduced together: across
 // lanes (one butterfly reduce-scatter) and across the QW column shares (shared
 // memory, fixed order, after a named barrier of the group), then the group's first
 // warp applies the epilogue and stores.  With several positions the inputs stay in
@@ -66,6 +66,8 @@ struct GtParams {
   int plane_dst[2 * MAX_INPUTS];   // float offset of the plane from the staging area
   const uint8_t* w[PGQ_MULTI_MAX];
   const uint8_t* p[PGQ_MULTI_MAX];
+  const __half* rs[PGQ_MULTI_MAX];   // q8_2f: row scales [rows]
+  const __half* cf[PGQ_MULTI_MAX];   // q8_2f: column field [cols]
   float* y[PGQ_MULTI_MAX];
   const float* residual[PGQ_MULTI_MAX];
   int rows[PGQ_MULTI_MAX], input[PGQ_MULTI_MAX], epi[PGQ_MULTI_MAX], task_begin[PGQ_MULTI_MAX + 1];
@@ -98,8 +100,14 @@ __device__ __forceinline__ int gt_perm(int c) {
 // W computing warps + one producer warp.  A stage holds SR rows; warp w takes RPW of
 // them (group w / QW, QW = W·RPW / SR warps per group) and the (w mod QW)-th share of
 // the column chunks (at most MAXC chunks of 32 lanes x EPL values).
-template <bool Q8, int NB, bool ARGMAX, int W, int RPW, int MAXC>
+// FMT: 0 binary16 rows; 1 q8 block format (per-32 scale and offset); 2 q8_2f (row
+// scale x column field: the column field folds into the input values, the row
+// scale multiplies the finished sum, as gemma_batch.rs `q8_2f_mm_r2` does).
+template <int FMT, int NB, bool ARGMAX, int W, int RPW, int MAXC>
 __global__ void __launch_bounds__((W + 1) * 32, 1) pgq_gemv_tma_kernel(const __grid_constant__ GtParams P) {
+  constexpr bool Q8 = FMT != 0;    // int8 codes
+  constexpr bool BLK = FMT == 1;   // with a plane of (scale, offset) pairs
+  constexpr bool F2 = FMT == 2;
   constexpr int THREADS = (W + 1) * 32;
   constexpr int EPL = Q8 ? 16 : 8;
   constexpr int CW = 32 * EPL;
@@ -135,11 +143,11 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) pgq_gemv_tma_kernel(const __g
     const int nr = min(P.SR, P.rows[j] - row0);
     const uint32_t bar = tc::smem_addr(full + s);
     const uint32_t cb = (uint32_t)((size_t)nr * cols * ESZ);
-    const uint32_t pb = Q8 ? (uint32_t)((size_t)nr * (cols >> 5) * 4) : 0u;
+    const uint32_t pb = BLK ? (uint32_t)((size_t)nr * (cols >> 5) * 4) : 0u;
     tc::mbar_expect_tx(bar, cb + pb);
     uint8_t* dst = ring + (size_t)s * P.slot_bytes;
     tc::bulk_load(tc::smem_addr(dst), P.w[j] + (size_t)row0 * cols * ESZ, cb, bar, policy);
-    if constexpr (Q8)
+    if constexpr (BLK)
       tc::bulk_load(tc::smem_addr(dst + P.code_bytes), P.p[j] + (size_t)row0 * (cols >> 5) * 4, pb, bar, policy);
   };
   // job of task t, found by walking forward from job j (tasks are visited in order)
@@ -358,8 +366,7 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) pgq_gemv_tma_kernel(const __g
     static_assert(NV <= 32 && (NV & (NV - 1)) == 0, "partials per group: a power of two <= 32");
     float2 xr[MAXC][EPL / 2];   // this lane's input values, per chunk
     float xsum[MAXC];           // and their sum, per chunk
-    float xk[MAXC];             // −(2^15 + 128)·xsum: the start of a chunk's q8 dot
-    int job_end = 0, input_j = -1;
+    int job_end = 0, input_j = -1, job_j = -1;
     int buf = 0;
     uint32_t parity = 0;   // of the ring's current pass (one group = one pass)
     static_assert(GT_GROUP == GT_NST, "a group is one pass over the ring: stage gs sits in slot gs");
@@ -371,7 +378,8 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) pgq_gemv_tma_kernel(const __g
     // the input has a gamma.  The planes are 128-byte swizzled (16-byte word c of
     // 128-byte row R at word c ^ (R mod 8)), which spreads the lanes' reads over all
     // banks.
-    auto load_x = [&](int input) {
+    // q8_2f: the job's column field multiplies the values too (cfj != null)
+    auto load_x = [&](int input, const __half* cfj) {
       const uint32_t xin = tc::smem_addr(xs) + (uint32_t)(input * cols_pad * 4);
       const int gsl = P.gslot[input];
       const uint32_t gin = tc::smem_addr(gs) + (uint32_t)((gsl < 0 ? 0 : gsl) * cols_pad * 4);
@@ -393,6 +401,12 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) pgq_gemv_tma_kernel(const __g
                                            __uint_as_float(gv.w));
               a = make_float4(g.x * (a.x * inv), g.y * (a.y * inv), g.z * (a.z * inv), g.w * (a.w * inv));
             }
+            if constexpr (F2) {
+              // (lanes past the last column read nothing: their chunk share is unused)
+              const uint2 cw = f < cols ? *reinterpret_cast<const uint2*>(cfj + f) : make_uint2(0u, 0u);
+              const float2 c01 = h2_to_f2(cw.x), c23 = h2_to_f2(cw.y);
+              a = make_float4(a.x * c01.x, a.y * c01.y, a.z * c23.x, a.w * c23.y);
+            }
           }
           xr[u][2 * k] = make_float2(a.x, a.y);
           xr[u][2 * k + 1] = make_float2(a.z, a.w);
@@ -401,7 +415,6 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) pgq_gemv_tma_kernel(const __g
 #pragma unroll
         for (int k = 1; k < EPL / 2; ++k) sum2 = fadd2(sum2, xr[u][k]);
         xsum[u] = sum2.x + sum2.y;
-        xk[u] = -32896.f * xsum[u];
       }
     };
     // shared-memory addresses of this lane's code and (scale, offset) words in slot 0
@@ -425,9 +438,12 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) pgq_gemv_tma_kernel(const __g
 #pragma unroll
         for (int a = 0; a < NA; ++a) acc[r][a] = make_float2(0.f, 0.f);
       if constexpr (Q8) {
-        // dot then scale: the biased byte u = q + 128 in [0, 255] is widened by one
-        // byte-permute into the f32 2^15 + u (exponent 15, u in mantissa bits 8..15);
-        // Σ (2^15 + u)·x − (2^15 + 128)·Σx = Σ q·x, and y += scale·Σ q·x + offset·Σx.
+        // dot then scale: each code becomes the exact f32 q (its biased byte q + 128
+        // byte-permuted into the mantissa of 2^23, then one packed subtraction of
+        // 2^23 + 128), the lane's Σ q·x is taken with packed FMAs, and y += scale·Σ q·x
+        // + offset·Σx (the q8_2f form: y += Σ q·(cf·x), the row scale at the end).  The
+        // products are exact and the partial sums bounded by Σ|q||x|, so the error
+        // stays a small multiple of 2^-24·Σ|w||x| for any codes (identity rows too).
         // Every shared-memory read of the stage is issued first, then the arithmetic.
         uint4 cw[RPW][MAXC];
         uint32_t pw[RPW][MAXC];
@@ -436,7 +452,7 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) pgq_gemv_tma_kernel(const __g
 #pragma unroll
           for (int r = 0; r < RPW; ++r) {
             cw[r][u] = tc::lds128(a_c[r][u] + slot_off);
-            pw[r][u] = tc::lds32(a_p[r][u] + slot_off);
+            pw[r][u] = BLK ? tc::lds32(a_p[r][u] + slot_off) : 0u;
           }
 #pragma unroll
         for (int u = 0; u < MAXC; ++u) {
@@ -444,23 +460,23 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) pgq_gemv_tma_kernel(const __g
 #pragma unroll
             for (int r = 0; r < RPW; ++r) {
               const float2 so = h2_to_f2(pw[r][u]);
-              const uint32_t words[4] = {cw[r][u].x ^ 0x80808080u, cw[r][u].y ^ 0x80808080u,
-                                         cw[r][u].z ^ 0x80808080u, cw[r][u].w ^ 0x80808080u};
-              // the dot starts from −(2^15 + 128)·Σx, so that it ends as Σ (u − 128)·x = Σ q·x
-              float2 d0 = make_float2(xk[u], 0.f), d1 = make_float2(0.f, 0.f);
+              const uint32_t words[4] = {cw[r][u].x, cw[r][u].y, cw[r][u].z, cw[r][u].w};
+              float2 d0 = make_float2(0.f, 0.f), d1 = make_float2(0.f, 0.f);
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
-                const float2 lo = make_float2(__uint_as_float(__byte_perm(words[k], 0x47000000u, 0x7504)),
-                                              __uint_as_float(__byte_perm(words[k], 0x47000000u, 0x7514)));
-                const float2 hi = make_float2(__uint_as_float(__byte_perm(words[k], 0x47000000u, 0x7524)),
-                                              __uint_as_float(__byte_perm(words[k], 0x47000000u, 0x7534)));
+                float2 lo, hi;
+                s8x4_to_f32(words[k], lo, hi);
                 d0 = ffma2(lo, xr[u][2 * k], d0);
                 d1 = ffma2(hi, xr[u][2 * k + 1], d1);
               }
               const float2 d = fadd2(d0, d1);
               float2 a = acc[r][0];
-              a.x = fmaf(so.x, d.x + d.y, a.x);     // scale · Σ q·x
-              a.y = fmaf(so.y, xsum[u], a.y);       // offset · Σ x
+              if constexpr (BLK) {
+                a.x = fmaf(so.x, d.x + d.y, a.x);     // scale · Σ q·x
+                a.y = fmaf(so.y, xsum[u], a.y);       // offset · Σ x
+              } else {
+                a.x += d.x + d.y;                     // Σ q·(cf·x); the row scale comes last
+              }
               acc[r][0] = a;
             }
           }
@@ -504,10 +520,12 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) pgq_gemv_tma_kernel(const __g
             const int jn = job_of(t, 0);
             job_end = P.task_begin[jn + 1];
             const int input = P.input[jn];
+            if (F2 && jn != job_j) input_j = -1;   // every q8_2f job has its own column field
+            job_j = jn;
 #ifdef PGQ_TRACE
             if (warp == 0 && lane == 0 && t == t0) GTRACE(13);
 #endif
-            if (input != input_j) load_x(input);
+            if (input != input_j) load_x(input, F2 ? P.cf[jn] : nullptr);
             input_j = input;
 #ifdef PGQ_TRACE
             if (warp == 0 && lane == 0 && t == t0) GTRACE(14);
@@ -554,6 +572,7 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) pgq_gemv_tma_kernel(const __g
             const float* rr = red + ((size_t)(buf * ngrp + rg) * NV + lane) * QW;
             float out = 0.f;
             for (int k = 0; k < QW; ++k) out += rr[k];
+            if constexpr (F2) out *= __half2float(P.rs[jj][row]);
             const int epi = P.epi[jj];
             if (epi == PGQ_EPI_RELU2) {
               out = fmaxf(out, 0.f);
@@ -617,10 +636,29 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) pgq_gemv_tma_kernel(const __g
         const int ch = ch_begin + u;
         if (ch < ch_end && ch * CW + lane * EPL < cols) {
           float2 wv[RPW][EPL / 2];
+          float2 cfv[EPL / 2];   // q8_2f: this lane's column-field values (q·cf is exact in f32)
+          if constexpr (F2) {
+            const int c0 = ch * CW + lane * EPL;
+#pragma unroll
+            for (int k = 0; k < EPL / 8; ++k) {
+              const uint4 cw4 = *reinterpret_cast<const uint4*>(P.cf[j] + c0 + 8 * k);
+              cfv[4 * k] = h2_to_f2(cw4.x); cfv[4 * k + 1] = h2_to_f2(cw4.y);
+              cfv[4 * k + 2] = h2_to_f2(cw4.z); cfv[4 * k + 3] = h2_to_f2(cw4.w);
+            }
+          }
 #pragma unroll
           for (int r = 0; r < RPW; ++r) {
             const uint4 cw = *reinterpret_cast<const uint4*>(st + off_c[r][u]);
-            if constexpr (Q8) {
+            if constexpr (F2) {
+              const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                float2 lo, hi;
+                s8x4_to_f32(words[k], lo, hi);
+                wv[r][2 * k] = make_float2(lo.x * cfv[2 * k].x, lo.y * cfv[2 * k].y);
+                wv[r][2 * k + 1] = make_float2(hi.x * cfv[2 * k + 1].x, hi.y * cfv[2 * k + 1].y);
+              }
+            } else if constexpr (Q8) {
               const uint32_t pw = *reinterpret_cast<const uint32_t*>(st + off_p[r][u]);
               const float2 so = h2_to_f2(pw);
               const float2 s2 = make_float2(so.x, so.x), o2 = make_float2(so.y, so.y);
@@ -693,6 +731,9 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) pgq_gemv_tma_kernel(const __g
       if (act) {
         const float* rr = red + (((size_t)buf * P.SR + row_a + r) * NB + b) * QW;
         for (int k = 0; k < QW; ++k) out += rr[k];
+        if constexpr (F2) {
+          if (live) out *= __half2float(P.rs[j][row]);
+        }
         if (live) {
           if (epi_j == PGQ_EPI_RELU2) {
             out = fmaxf(out, 0.f);
@@ -777,13 +818,13 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) pgq_gemv_tma_kernel(const __g
 
 namespace {
 using GtFn = void (*)(GtParams);
-template <bool Q8, bool AM>
+template <int FMT, bool AM>
 GtFn gt_pick(int nb) {
   switch (nb) {
-    case 1: return reinterpret_cast<GtFn>(&pgq_gemv_tma_kernel<Q8, 1, AM, 16, 2, 2>);
-    case 2: return reinterpret_cast<GtFn>(&pgq_gemv_tma_kernel<Q8, 2, AM, 16, 2, 2>);
-    case 4: return reinterpret_cast<GtFn>(&pgq_gemv_tma_kernel<Q8, 4, AM, 16, 2, 2>);
-    default: return reinterpret_cast<GtFn>(&pgq_gemv_tma_kernel<Q8, 8, AM, 16, 2, 2>);
+    case 1: return reinterpret_cast<GtFn>(&pgq_gemv_tma_kernel<FMT, 1, AM, 16, 2, 2>);
+    case 2: return reinterpret_cast<GtFn>(&pgq_gemv_tma_kernel<FMT, 2, AM, 16, 2, 2>);
+    case 4: return reinterpret_cast<GtFn>(&pgq_gemv_tma_kernel<FMT, 4, AM, 16, 2, 2>);
+    default: return reinterpret_cast<GtFn>(&pgq_gemv_tma_kernel<FMT, 8, AM, 16, 2, 2>);
   }
 }
 }  // namespace
@@ -793,7 +834,9 @@ int launch_gemv_tma(const GvParams& V, bool q8, bool argmax, const DeviceInfo& d
   const int esz = q8 ? 1 : 2;
   const int EPL = q8 ? 16 : 8, CW = 32 * EPL;
   if (V.cols % 128 != 0) return PGQ_EUNSUPPORTED;          // 16-byte rows of params
-  const size_t row_bytes = (size_t)V.cols * esz + (q8 ? (size_t)V.cols / 8 : 0);
+  const bool f2 = q8 && V.q82f;   // q8_2f: no (scale, offset) plane in the stages
+  if (f2 && argmax) return PGQ_EUNSUPPORTED;
+  const size_t row_bytes = (size_t)V.cols * esz + (q8 && !f2 ? (size_t)V.cols / 8 : 0);
   int SR = 8;
   while (SR > 2 && (size_t)SR * row_bytes > GT_STAGE_MAX) SR >>= 1;
   if ((size_t)SR * row_bytes > GT_STAGE_MAX) return PGQ_EUNSUPPORTED;
@@ -815,8 +858,11 @@ int launch_gemv_tma(const GvParams& V, bool q8, bool argmax, const DeviceInfo& d
     P.epi[j] = V.job[j].epilogue;
     P.task_begin[j] = t;
     t += (V.job[j].rows + SR - 1) / SR;
+    P.rs[j] = reinterpret_cast<const __half*>(V.job[j].rs);
+    P.cf[j] = reinterpret_cast<const __half*>(V.job[j].cf);
     // bulk copies need 16-byte aligned sources
-    if (!aligned16(V.job[j].w) || (q8 && !aligned16(V.job[j].params))) return PGQ_EUNSUPPORTED;
+    if (!aligned16(V.job[j].w) || (q8 && !f2 && !aligned16(V.job[j].params))) return PGQ_EUNSUPPORTED;
+    if (f2 && (!V.job[j].rs || !V.job[j].cf || !aligned16(V.job[j].cf))) return PGQ_EUNSUPPORTED;
   }
   P.task_begin[V.njobs] = t;
   P.ntasks = t;
@@ -863,7 +909,7 @@ int launch_gemv_tma(const GvParams& V, bool q8, bool argmax, const DeviceInfo& d
   P.QW = QW;
   P.cpw = cpw;
   P.code_bytes = (SR * V.cols * esz + 127) / 128 * 128;
-  P.stage_bytes = (P.code_bytes + (q8 ? SR * (V.cols / 32) * 4 : 0) + 127) / 128 * 128;
+  P.stage_bytes = (P.code_bytes + (q8 && !f2 ? SR * (V.cols / 32) * 4 : 0) + 127) / 128 * 128;
   if (P.stage_bytes > GT_SLOT) return PGQ_EUNSUPPORTED;
   P.slot_bytes = nb == 1 ? GT_SLOT : P.stage_bytes;   // the one-position kernel assumes GT_SLOT
   P.eps = V.eps;
@@ -877,8 +923,9 @@ int launch_gemv_tma(const GvParams& V, bool q8, bool argmax, const DeviceInfo& d
                       GT_RED * (size_t)SR * std::max(nb, GT_GROUP) * QW * 4 + 128 +
                       (size_t)GT_NST * P.slot_bytes + (2 * GT_NST + 1) * 8 + 64;
   if (smem + 2048 > dev.smem_optin) return PGQ_EUNSUPPORTED;   // + the static shared memory
-  GtFn fn = q8 ? (argmax ? gt_pick<true, true>(nb) : gt_pick<true, false>(nb))
-               : (argmax ? gt_pick<false, true>(nb) : gt_pick<false, false>(nb));
+  GtFn fn = f2 ? gt_pick<2, false>(nb)
+               : q8 ? (argmax ? gt_pick<1, true>(nb) : gt_pick<1, false>(nb))
+                    : (argmax ? gt_pick<0, true>(nb) : gt_pick<0, false>(nb));
   {
     // raise the kernel's shared-memory limit once per (kernel, device, size)
     static std::mutex mu;

@@ -18,6 +18,9 @@ struct GvJob {
   int input;
   int epilogue;
   int task_begin;            // first task index of this job (filled by the launcher)
+  // q8_2f format (GvParams::q82f): binary16 row scales [rows] and column field [cols]
+  const uint16_t* rs;
+  const uint16_t* cf;
 };
 struct GvInput {
   const float* x;            // [B][cols]
@@ -41,10 +44,18 @@ struct GvParams {
   // The weights may be fetched before the previous kernel in the stream has finished
   // (it writes none of them): set only where the launcher knows that kernel.
   int early_weights;
+  // the q8 jobs are in the q8_2f format (int8 body, row scale, column field): only
+  // the TMA decode kernel takes it
+  int q82f;
 };
 
-int launch_add_rmsnorm(float* h, const float* add, const float* gamma, float eps, int B, int n,
-                       float* y, float* inv, cudaStream_t st);
+// scale == 0: no scale; gemma != 0: norm weights used as 1 + gamma
+int launch_add_rmsnorm(float* h, const float* add, const float* gamma, float eps, float scale, int gemma, int B,
+                       int n, float* y, float* inv, cudaStream_t st);
+// n * 4 bytes of dynamic shared memory (n <= 16384)
+int launch_sandwich(const float* x, const float* w1, float* h, const float* w2, float eps, float scale, int gemma,
+                    int B, int n, float* out, float* mid, float* inv1, float* inv2, const DeviceInfo& dev,
+                    cudaStream_t st);
 int launch_relu2(float* v, size_t n, cudaStream_t st, int sms);
 int launch_argmax(const float* logits, int B, int V, int32_t* ids, cudaStream_t st);
 

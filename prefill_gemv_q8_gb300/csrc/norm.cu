@@ -2,7 +2,10 @@
 //
 // add + RMSNorm follows nemotron_prefill.rs `pb_add_rms` (add = 0/1) and
 // gemma_batch.rs `g4_add_norm_b`: one block per position, the block's partial sums
-// of h² reduced in a fixed order, inv = 1/sqrt(mean + eps), y = γ·(h·inv).
+// of h² reduced in a fixed order, inv = 1/sqrt(mean + eps), y = γ·(h·inv); the
+// sandwich residual (gemma_batch.rs `g4_sandwich`) runs two of them in one block.
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -23,34 +26,77 @@ __device__ __forceinline__ float block_sum_256(float v, float* red) {
   return t;
 }
 
-__global__ void __launch_bounds__(NORM_THREADS)
-pgq_add_rmsnorm_kernel(float* __restrict__ h, const float* __restrict__ add,
-                   const float* __restrict__ gamma, float eps, int n,
-                   float* __restrict__ y, float* __restrict__ inv_out) {
-  __shared__ float red[NORM_THREADS / 32];
-  const size_t base = (size_t)blockIdx.x * n;
-  float4* h4 = reinterpret_cast<float4*>(h + base);
-  const float4* a4 = add ? reinterpret_cast<const float4*>(add + base) : nullptr;
+// The body of every add + RMSNorm here, for the position whose rows the pointers
+// address (gemma_batch.rs `g4_add_norm_b`): h <- (h + add)·scale (add and scale
+// optional; h is written only when one of them is given), inv = 1/sqrt(Σh²/n + eps),
+// y = w·(h·inv) with w = 1 + γ under the gemma switch.  The sum of squares is a
+// fixed fma chain per thread and a fixed-order block reduction, so the standalone
+// norm and the fused sandwich, which both run this code with the same 256 threads,
+// give the same bits.
+__device__ __forceinline__ float norm_row(float4* h4, const float4* a4, const float4* g4, int n, float eps,
+                                          float scale, bool gemma, float4* y4, float* red) {
   const int n4 = n >> 2;
+  const bool write_h = a4 != nullptr || scale != 0.f;
   float ss = 0.f;
   for (int i = threadIdx.x; i < n4; i += NORM_THREADS) {
     float4 v = h4[i];
     if (a4) {
       const float4 a = a4[i];
       v.x += a.x; v.y += a.y; v.z += a.z; v.w += a.w;
-      h4[i] = v;
     }
-    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    if (scale != 0.f) {
+      v.x *= scale; v.y *= scale; v.z *= scale; v.w *= scale;
+    }
+    if (write_h) h4[i] = v;
+    ss = fmaf(v.w, v.w, fmaf(v.z, v.z, fmaf(v.y, v.y, fmaf(v.x, v.x, ss))));
   }
   ss = block_sum_256(ss, red);
   const float inv = rsqrtf(ss / (float)n + eps);
-  if (inv_out && threadIdx.x == 0) inv_out[blockIdx.x] = inv;
-  const float4* g4 = reinterpret_cast<const float4*>(gamma);
-  float4* y4 = reinterpret_cast<float4*>(y + base);
   for (int i = threadIdx.x; i < n4; i += NORM_THREADS) {
     const float4 v = h4[i];
-    const float4 g = g4[i];
+    float4 g = g4[i];
+    if (gemma) g = make_float4(1.f + g.x, 1.f + g.y, 1.f + g.z, 1.f + g.w);
     y4[i] = make_float4(g.x * (v.x * inv), g.y * (v.y * inv), g.z * (v.z * inv), g.w * (v.w * inv));
+  }
+  return inv;
+}
+
+__global__ void __launch_bounds__(NORM_THREADS)
+pgq_add_rmsnorm_kernel(float* __restrict__ h, const float* __restrict__ add, const float* __restrict__ gamma,
+                       float eps, float scale, int gemma, int n, float* __restrict__ y, float* __restrict__ inv_out) {
+  __shared__ float red[NORM_THREADS / 32];
+  const size_t base = (size_t)blockIdx.x * n;
+  const float inv = norm_row(reinterpret_cast<float4*>(h + base),
+                             add ? reinterpret_cast<const float4*>(add + base) : nullptr,
+                             reinterpret_cast<const float4*>(gamma), n, eps, scale, gemma != 0,
+                             reinterpret_cast<float4*>(y + base), red);
+  if (inv_out && threadIdx.x == 0) inv_out[blockIdx.x] = inv;
+}
+
+// Gemma's sandwich residual for one position per block (gemma_batch.rs
+// `g4_sandwich`): mid = rms(x)·w1 into shared memory, then h <- (h + mid)·scale and
+// out = rms(h)·w2, each half the same code as pgq_add_rmsnorm_kernel (norm_row), so
+// the fused form and the chain of two norms are bit-identical.  x is only read.
+__global__ void __launch_bounds__(NORM_THREADS)
+pgq_sandwich_kernel(const float* __restrict__ x, const float* __restrict__ w1, float* __restrict__ h,
+                    const float* __restrict__ w2, float eps, float scale, int gemma, int n,
+                    float* __restrict__ out, float* __restrict__ mid_out, float* __restrict__ inv1,
+                    float* __restrict__ inv2) {
+  extern __shared__ float4 s_mid[];   // [n / 4]
+  __shared__ float red[NORM_THREADS / 32];
+  const size_t base = (size_t)blockIdx.x * n;
+  const float i1 = norm_row(const_cast<float4*>(reinterpret_cast<const float4*>(x + base)), nullptr,
+                            reinterpret_cast<const float4*>(w1), n, eps, 0.f, gemma != 0, s_mid, red);
+  if (mid_out) {
+    float4* m4 = reinterpret_cast<float4*>(mid_out + base);
+    for (int i = threadIdx.x; i < (n >> 2); i += NORM_THREADS) m4[i] = s_mid[i];
+  }
+  // each thread reads back the mid values it wrote (same index walk)
+  const float i2 = norm_row(reinterpret_cast<float4*>(h + base), s_mid, reinterpret_cast<const float4*>(w2), n, eps,
+                            scale, gemma != 0, reinterpret_cast<float4*>(out + base), red);
+  if (threadIdx.x == 0) {
+    if (inv1) inv1[blockIdx.x] = i1;
+    if (inv2) inv2[blockIdx.x] = i2;
   }
 }
 
@@ -98,9 +144,28 @@ pgq_argmax_kernel(const float* __restrict__ logits, int V, int32_t* __restrict__
 }
 
 // ------------------------------------------------------------------ launchers
-int launch_add_rmsnorm(float* h, const float* add, const float* gamma, float eps, int B, int n,
-                       float* y, float* inv, cudaStream_t st) {
-  pgq_add_rmsnorm_kernel<<<B, NORM_THREADS, 0, st>>>(h, add, gamma, eps, n, y, inv);
+int launch_add_rmsnorm(float* h, const float* add, const float* gamma, float eps, float scale, int gemma, int B,
+                       int n, float* y, float* inv, cudaStream_t st) {
+  pgq_add_rmsnorm_kernel<<<B, NORM_THREADS, 0, st>>>(h, add, gamma, eps, scale, gemma, n, y, inv);
+  return cuda_status(cudaGetLastError());
+}
+
+int launch_sandwich(const float* x, const float* w1, float* h, const float* w2, float eps, float scale, int gemma,
+                    int B, int n, float* out, float* mid, float* inv1, float* inv2, const DeviceInfo& dev,
+                    cudaStream_t st) {
+  const size_t smem = (size_t)n * sizeof(float);
+  {
+    static std::mutex mu;
+    static size_t done[64] = {};
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev.device >= 0 && dev.device < 64 && smem > done[dev.device]) {
+      const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&pgq_sandwich_kernel),
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return cuda_status(e);
+      done[dev.device] = smem;
+    }
+  }
+  pgq_sandwich_kernel<<<B, NORM_THREADS, smem, st>>>(x, w1, h, w2, eps, scale, gemma, n, out, mid, inv1, inv2);
   return cuda_status(cudaGetLastError());
 }
 

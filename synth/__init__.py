@@ -37,6 +37,7 @@ CODE_STD = 40.0
 CODE_CLIP = 127
 SCALE_LO, SCALE_HI = 1e-3, 4e-3
 OFFSET_STD = 1e-3
+CF_LO, CF_HI = 0.5, 1.5   # q8_2f column field (the pages give no distribution)
 EPS = 1e-6
 
 # tensor ids inside one workload seed space
@@ -110,6 +111,35 @@ def q8_matrix(rows, cols, workload, tensor, backend="numpy", device=None):
                       * (SCALE_HI - SCALE_LO) + SCALE_LO).to(torch.float16)
     params[..., 1] = (torch.randn((rows, nb), generator=g, device=device) * OFFSET_STD).to(torch.float16)
     return codes, params
+
+
+def q82f_matrix(rows, cols, workload, tensor, backend="numpy", device=None):
+    """q8_2f matrix: (codes int8 [rows][cols] as q8_matrix draws them, row_scale
+    binary16 [rows] ~ U(SCALE_LO, SCALE_HI), col_field binary16 [cols] ~ U(CF_LO, CF_HI))."""
+    if backend == "numpy":
+        r = _np_rng(workload, tensor)
+        codes = np.clip(np.rint(r.standard_normal((rows, cols)) * CODE_STD), -CODE_CLIP, CODE_CLIP)
+        codes = codes.astype(np.int8)
+        rs = r.uniform(SCALE_LO, SCALE_HI, rows).astype(np.float16)
+        cf = r.uniform(CF_LO, CF_HI, cols).astype(np.float16)
+        return codes, rs, cf
+    import torch
+    g = _torch_gen(workload, tensor, device)
+    codes = torch.empty((rows, cols), dtype=torch.int8, device=device)
+    step = max(1, (1 << 26) // cols)
+    for r0 in range(0, rows, step):
+        r1 = min(rows, r0 + step)
+        t = torch.randn((r1 - r0, cols), generator=g, device=device) * CODE_STD
+        codes[r0:r1] = torch.round(t).clamp_(-CODE_CLIP, CODE_CLIP).to(torch.int8)
+    rs = (torch.rand(rows, generator=g, device=device) * (SCALE_HI - SCALE_LO) + SCALE_LO).to(torch.float16)
+    cf = (torch.rand(cols, generator=g, device=device) * (CF_HI - CF_LO) + CF_LO).to(torch.float16)
+    return codes, rs, cf
+
+
+def q82f_layer(workload, layer, hidden, kv, inter, backend="numpy", device=None):
+    """The six projections of a decode layer in the q8_2f format: {slot: (codes, rs, cf)}."""
+    return {s: q82f_matrix(r, c, workload, q8_tensor_id(layer, s) + 500, backend, device)
+            for s, (r, c) in q8_layer_shapes(hidden, kv, inter).items()}
 
 
 def f16_matrix(rows, cols, workload, tensor, backend="numpy", device=None):

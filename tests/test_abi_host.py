@@ -214,3 +214,52 @@ def test_moe_arguments_rejected(L):
                                    None) == pgq.EWORKSPACE
     assert L.pgq_moe_prefill_layer(C.byref(lay), _p(6), 65, _p(7), _p(8), 1e-6, _p(9), _p(10), need,
                                    None) == pgq.EINVAL
+
+
+def test_norm_ex_and_sandwich_arguments_rejected(L):
+    f = C.c_void_p(FAKE)
+    g = C.c_void_p(FAKE + (1 << 20))
+    # unknown flags, non-finite scale, bad n, misalignment, overlap
+    assert L.pgq_add_rmsnorm_ex(f, None, g, 1e-6, 0.0, 2, 1, 64, C.c_void_p(FAKE + (2 << 20)), None, None) == pgq.EINVAL
+    assert L.pgq_add_rmsnorm_ex(f, None, g, 1e-6, float("inf"), 0, 1, 64, C.c_void_p(FAKE + (2 << 20)), None,
+                                None) == pgq.EINVAL
+    assert L.pgq_add_rmsnorm_ex(f, None, g, 1e-6, 1.0, 0, 1, 66, C.c_void_p(FAKE + (2 << 20)), None, None) == pgq.EINVAL
+    assert L.pgq_add_rmsnorm_ex(C.c_void_p(FAKE + 4), None, g, 1e-6, 1.0, 0, 1, 64, C.c_void_p(FAKE + (2 << 20)), None,
+                                None) == pgq.EALIGN
+    assert L.pgq_add_rmsnorm_ex(f, None, g, 1e-6, 1.0, 0, 1, 64, f, None, None) == pgq.EINVAL
+    x, h, o = C.c_void_p(FAKE), C.c_void_p(FAKE + (1 << 20)), C.c_void_p(FAKE + (2 << 20))
+    w = C.c_void_p(FAKE + (3 << 20))
+    assert L.pgq_sandwich_rmsnorm(x, w, h, w, 1e-6, 0.0, 4, 1, 64, o, None, None, None, None) == pgq.EINVAL
+    assert L.pgq_sandwich_rmsnorm(x, w, h, w, 1e-6, 0.0, 0, 1, 16388, o, None, None, None, None) == pgq.EINVAL
+    assert L.pgq_sandwich_rmsnorm(x, w, h, w, 1e-6, float("nan"), 0, 1, 64, o, None, None, None, None) == pgq.EINVAL
+    assert L.pgq_sandwich_rmsnorm(x, w, x, w, 1e-6, 0.0, 0, 1, 64, o, None, None, None, None) == pgq.EINVAL
+    assert L.pgq_sandwich_rmsnorm(x, w, h, w, 1e-6, 0.0, 0, 1, 64, o, h, None, None, None) == pgq.EINVAL
+    assert L.pgq_sandwich_rmsnorm(x, w, h, w, 1e-6, 0.0, 0, 1, 64, C.c_void_p(FAKE + (2 << 20) + 8), None, None, None,
+                                  None) == pgq.EALIGN
+    assert L.pgq_sandwich_rmsnorm(None, w, h, w, 1e-6, 0.0, 0, 1, 64, o, None, None, None, None) == pgq.EINVAL
+
+
+def test_wait_limit_and_stall_arguments(L):
+    assert L.pgq_set_wait_limit_ns(10) == pgq.EINVAL
+    assert L.pgq_set_wait_limit_ns(10 ** 12) == pgq.EINVAL
+    assert L.pgq_set_wait_limit_ns(5000) == pgq.OK
+    assert L.pgq_wait_limit_ns() == 5000
+    assert L.pgq_set_wait_limit_ns(0) == pgq.OK
+    assert L.pgq_wait_limit_ns() == 2_000_000_000
+    assert L.pgq_debug_stall(3) == pgq.EINVAL
+    assert L.pgq_debug_stall(0) == pgq.OK
+
+
+def test_q82f_arguments_rejected(L):
+    p = lambda k: C.c_void_p(FAKE + k * (1 << 24))  # noqa: E731
+    # cols not a multiple of 128, null pointers, misaligned column field, bad B
+    assert L.pgq_gemv_q82f(p(1), p(2), p(3), 64, 80, p(4), 1, None, 1e-6, p(5), 0, None, None) == pgq.EINVAL
+    assert L.pgq_gemv_q82f(p(1), None, p(3), 64, 128, p(4), 1, None, 1e-6, p(5), 0, None, None) == pgq.EINVAL
+    assert L.pgq_gemv_q82f(p(1), p(2), C.c_void_p(FAKE + 3 * (1 << 24) + 8), 64, 128, p(4), 1, None, 1e-6, p(5), 0,
+                           None, None) == pgq.EALIGN
+    assert L.pgq_gemv_q82f(p(1), p(2), p(3), 64, 128, p(4), 9, None, 1e-6, p(5), 0, None, None) == pgq.EINVAL
+    m = pgq.Q82Matrix(p(1).value, p(2).value, p(3).value)
+    lay = pgq.Q82Layer(m, m, m, m, m, m, 512, 128, 1024)
+    outs = [p(10 + i) for i in range(6)]
+    assert L.pgq_q82f_decode_layer(C.byref(lay), p(6), p(7), p(8), 1e-6, *outs, 4, None) == pgq.EINVAL
+    assert L.pgq_q82f_decode_layer(None, p(6), p(7), p(8), 1e-6, *outs, 0, None) == pgq.EINVAL

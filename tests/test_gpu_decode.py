@@ -126,6 +126,18 @@ def test_gemv_q8_identity_exact():
     assert np.array_equal(y, x)
 
 
+def test_gemv_q8_identity_one_position():
+    """Identity weights at one position (the register-resident kernel): within
+    1e-3·Σ|w||x| = 1e-3·|x_i| of x for every element, however small x_i is."""
+    n = 4096
+    codes = np.eye(n, dtype=np.int8)
+    params = np.zeros((n, n // 32, 2), np.float16)
+    params[..., 0] = 1.0
+    x = synth.normal((1, n), 1.0, 904, 2)
+    y = host(pgq.gemv_q8(dev(codes), dev(params), dev(x)))
+    check_proj(y, x.astype(np.float64), np.abs(x), what="q8 identity B=1")
+
+
 def test_gemv_q8_equal_rows_equal_bits_and_deterministic():
     codes, params = _q8(64, 4096, 12)
     codes[40] = codes[3]
