@@ -272,8 +272,9 @@ class PrefillPass:
         per_layer = sum(r * c_ + r * (c_ // 32) * 4 for r, c_ in synth.q8_layer_shapes(self.H, self.KV, self.I).values())
         self.step_bytes = per_layer * self.L
         self.flops = 2 * self.B * sum(r * c_ for r, c_ in synth.q8_layer_shapes(self.H, self.KV, self.I).values()) * self.L
-        # launches per pass: per 8 layers one input kernel and one persistent launch
-        self.launches_per_step = 2 * ((self.L + 7) // 8)
+        # launches per pass: per PASS_LMAX layers one input kernel and one persistent launch
+        self.persistent_launches = (self.L + pgq.PASS_LMAX - 1) // pgq.PASS_LMAX
+        self.launches_per_step = 2 * self.persistent_launches
 
     def step(self):
         self.h.copy_(self.h0)
@@ -310,14 +311,17 @@ def time_prefill(torch, P, steps, warmup, pk):
         "weight_GBps": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm"], 4),
         "tflops": round(tf, 1), "frac_of_bf16_tensor": round(tf / pk["bf16_sustained"], 4),
         "bound": "hbm", "weight_bytes_per_pass": P.step_bytes, "launches_per_pass": P.launches_per_step,
-        # the pass is one persistent launch per 8 layers (plus its input kernel): the
-        # dominant kernel's roofline is the pass's weight bytes per launch
-        "roofline": {"bound": "hbm", "kernel": "pgq_prefill_pass_kernel (8 layers = 32 phases per launch, B=64)",
+        # the pass is one persistent launch per PASS_LMAX layers (plus its input kernel):
+        # the dominant kernel's roofline is the pass's weight bytes per launch (average)
+        "roofline": {"bound": "hbm",
+                     "kernel": f"pgq_prefill_pass_kernel ({P.pgq.PASS_LMAX} layers = {4 * P.pgq.PASS_LMAX} phases per "
+                               f"launch, B=64; {P.persistent_launches} launches per pass)",
                      "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4),
-                     "traffic": ncu_traffic("prefill_pass_8layers", PREFILL_FILES),
-                     "algorithmic_bytes_per_launch": P.step_bytes // max(1, P.launches_per_step // 2),
-                     "avg_launch_ms": round(ms / max(1, P.launches_per_step // 2), 5),
-                     "timed": "CUDA-graph replay of the pass; per launch = pass / launches (input kernels included)"},
+                     "traffic": ncu_traffic("prefill_pass_launch", PREFILL_FILES),
+                     "algorithmic_bytes_per_launch": P.step_bytes // P.persistent_launches,
+                     "avg_launch_ms": round(ms / P.persistent_launches, 5),
+                     "timed": "CUDA-graph replay of the pass; per launch = pass / persistent launches (input kernels "
+                              "included)"},
         "up_alone": {"kernel": "pgq_prefill_pass_kernel, one phase (up 14336x4096, relu²) + input kernel",
                      "GBps": round(ach, 1), "frac": round(ach / pk["hbm"], 4), "bytes": up_bytes,
                      "avg_launch_ms": round(k_ms, 5), "timed": "separate event loop over 32 up matrices, direct calls"},

@@ -60,6 +60,7 @@ enum {
 #define PGQ_QBLOCK 32     /* columns per (scale, offset) block of the q8 format */
 #define PGQ_DECODE_BMAX 8 /* positions per decode call (gemv_*) */
 #define PGQ_PASS_BMAX 64  /* positions per prefill pass (nemotron_prefill.rs `PB_MAX`) */
+#define PGQ_PASS_LMAX 8   /* layers per persistent launch of pgq_q8_prefill_pass */
 #define PGQ_MULTI_MAX 8   /* matrices in one pgq_gemv_q8_multi launch */
 #define PGQ_STAGE_MAX 49152 /* f32 input values a decode launch stages on chip */
 
@@ -351,8 +352,8 @@ int pgq_prefill_status(const void* workspace, void* stream);
  * 256-byte aligned.  After the call the workspace holds the last layer's n1, q, k,
  * v, h1 (= h + W_o·q), n2 and u at the byte offsets pgq_q8_prefill_pass_layout()
  * reports (7 entries).
- * Two launches per group of up to 8 layers: a small kernel that makes the first
- * layer's binary16 input, then one persistent cooperative launch of all the group's
+ * Two launches per group of up to PGQ_PASS_LMAX layers: a small kernel that makes the
+ * first layer's binary16 input, then one persistent cooperative launch of all the group's
  * projections (its blocks pass each projection's output to the next through device
  * counters).  Returns PGQ_ETIMEOUT through pgq_prefill_status() if a bounded
  * device-side wait expired. */

@@ -24,6 +24,7 @@ EPILOGUES = {"none": EPI_NONE, "relu2": EPI_RELU2, "add": EPI_ADD}
 QBLOCK = 32
 DECODE_BMAX = 8
 PASS_BMAX = 64
+PASS_LMAX = 8      # layers per persistent launch of the prefill pass (PGQ_PASS_LMAX)
 
 _vp = C.c_void_p
 

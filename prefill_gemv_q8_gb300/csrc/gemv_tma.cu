@@ -1240,8 +1240,7 @@ __global__ void __launch_bounds__(HD_THREADS, 1) pgq_head_tc_kernel(const __grid
       if (!__all_sync(FULLM, wait_bar(accf + t, pht))) break;
       tc::fence_after_sync();
       uint32_t u[16];
-      tc::tmem_ld_32x32b_x16(tmem + ((uint32_t)(q * 32) << 16) + t * HD_NP, u);
-      tc::tmem_wait_ld();
+      tc::tmem_ld_32x32b_x16_sync(tmem + ((uint32_t)(q * 32) << 16) + t * HD_NP, u);
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(sa(acce + t));

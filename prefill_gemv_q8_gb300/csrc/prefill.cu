@@ -59,7 +59,7 @@ constexpr int PS_W_BYTES = PS_CODES_BYTES + PS_PARAMS_BYTES;  // 18 KB, a multip
 constexpr int PS_ACC_COLS = 64;                               // TMEM columns per accumulator (N <= 64)
 constexpr int PS_A_COLS = TC_BK / 2;                          // TMEM columns per A buffer
 constexpr uint32_t PS_TMEM_COLS = 512;                        // 2 accumulators + 4 A buffers (384 used)
-constexpr int PS_MAXL = 8;                                    // layers per pass launch
+constexpr int PS_MAXL = PGQ_PASS_LMAX;                        // layers per pass launch
 constexpr int PS_MAXPH = 4 * PS_MAXL;                         // phases per launch
 constexpr int PS_MAXJ = 6 * PS_MAXL;                          // matrices per launch
 constexpr int PS_NX = 4;                                      // input buffers (n1, q, n2, u)

@@ -4,12 +4,12 @@
   exactly at the 2^31-byte mark) for one position (CUDA-core kernel) and eight
   (tensor-core kernel): every logit against the oracle, the ids under both argmax
   checks, and an exact tie planted among the last rows, which the earlier row wins.
-* The prefill pass across its launch boundary: more than eight layers take several
-  persistent launches (eight layers each), each starting from the previous launch's
+* The prefill pass across its launch boundary: more than PASS_LMAX layers take several
+  persistent launches (PASS_LMAX layers each), each starting from the previous launch's
   h and the next layer's norm weights; results must be bit-identical to one layer
   per call, and the last layer must match the oracle stage by stage.
-* One full-size eight-layer launch (hidden 4096, kv 1024, inter 14336, 64 positions):
-  the last layer stage by stage on a row sample.
+* One full-size launch of PASS_LMAX layers (hidden 4096, kv 1024, inter 14336, 64
+  positions): the last layer stage by stage on a row sample.
 """
 import numpy as np
 import pytest
@@ -100,28 +100,28 @@ def test_pass_across_launches_equals_layer_by_layer(L, B):
     check_layer(mats, host(h_before_last), host(g1)[L - 1], host(g2)[L - 1], taps, host(ha))
 
 
-def test_pass_full_size_eight_layer_launch():
-    """Eight layers at the benchmark's shapes in one persistent launch (32 phases):
-    the last layer checked stage by stage on a row sample, the h it started from
-    taken from a seven-layer call."""
+def test_pass_full_size_one_launch():
+    """PASS_LMAX layers at the benchmark's shapes in one persistent launch: the last
+    layer checked stage by stage on a row sample, the h it started from taken from a
+    call over the layers before it."""
     c = synth.PREFILL
     H, KV, I, B, wl = c["hidden"], c["kv"], c["inter"], c["B"], c["workload"]
-    L = 8
+    L = pgq.PASS_LMAX
     layers = [synth.q8_layer(wl, l, H, KV, I, "torch", "cuda") for l in range(L)]
     h0 = synth.normal((B, H), 1.0, wl, synth.T_X, "torch", "cuda")
     g1 = synth.uniform((L, H), 0.5, 1.5, wl, synth.T_GAMMA, "torch", "cuda")
     g2 = synth.uniform((L, H), 0.5, 1.5, wl, synth.T_GAMMA2, "torch", "cuda")
-    h7 = h0.clone()
-    pgq.prefill_pass(layers[:7], h7, g1[:7].contiguous(), g2[:7].contiguous(), 1e-6)
+    hp = h0.clone()
+    pgq.prefill_pass(layers[:L - 1], hp, g1[:L - 1].contiguous(), g2[:L - 1].contiguous(), 1e-6)
     h = h0.clone()
     ws = pgq.prefill_pass(layers, h, g1, g2, 1e-6)
     assert pgq.last_device_status(ws) == pgq.OK
-    # one launch of eight layers and one launch of seven plus a one-layer call agree
-    h8 = h7.clone()
-    pgq.prefill_pass(layers[7:], h8, g1[7:].contiguous(), g2[7:].contiguous(), 1e-6)
-    assert torch.equal(h, h8)
+    # one launch of L layers equals a launch of L - 1 layers and a one-layer call
+    hl = hp.clone()
+    pgq.prefill_pass(layers[L - 1:], hl, g1[L - 1:].contiguous(), g2[L - 1:].contiguous(), 1e-6)
+    assert torch.equal(h, hl)
     taps = pgq.prefill_pass_taps(ws, H, KV, I, B)
     rng = np.random.default_rng(8)
     rows = np.sort(rng.choice(H, 192, replace=False))
     mats = {s: (host(cc), host(pp)) for s, (cc, pp) in layers[-1].items()}
-    check_layer(mats, host(h7), host(g1)[L - 1], host(g2)[L - 1], taps, host(h), rows_sample=rows)
+    check_layer(mats, host(hp), host(g1)[L - 1], host(g2)[L - 1], taps, host(h), rows_sample=rows)
