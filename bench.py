@@ -358,6 +358,10 @@ def time_graph(torch, fn, steps, warmup):
 
 
 def bench_tiny_mlp(torch, pgq, synth, steps, warmup, pk):
+    """The tiny f16 MLP block (4 MiB of weights): launch-latency bound.  Timed three
+    ways: direct calls of the two-launch form (host launch cost included), and CUDA
+    graphs of K steps of the two-launch and of the one-launch (fused) form; value =
+    the one-launch graph."""
     c = synth.TINY_MLP
     H, I, wl = c["hidden"], c["inter"], c["workload"]
     h = synth.normal((H,), 1.0, wl, synth.T_X, "torch", "cuda")
@@ -367,18 +371,41 @@ def bench_tiny_mlp(torch, pgq, synth, steps, warmup, pk):
     copies = [(Wu, Wd)] + [(Wu.clone(), Wd.clone()) for _ in range(63)]   # 64 x 4 MiB > 2 x L2
     u = torch.empty(I, device="cuda")
     y = torch.empty(H, device="cuda")
+    sync = pgq.layer_sync()
     it = [0]
 
-    def step():
+    def step(fused=False):
         a, b = copies[it[0] % len(copies)]
         it[0] += 1
-        pgq.mlp_f16_decode(h, a, b, g, 1e-6, u=u, y=y)
+        if fused:
+            pgq.mlp_f16_decode_fused(h, a, b, g, 1e-6, sync=sync, u=u, y=y)
+        else:
+            pgq.mlp_f16_decode(h, a, b, g, 1e-6, u=u, y=y)
 
-    ms = time_loop(torch, step, steps * 4, warmup)
+    ms_direct = time_loop(torch, step, steps * 4, warmup)
+
+    def graph_ms(fused):
+        g_all = _capture(torch, lambda: [step(fused) for _ in range(steps)])
+        g_all.replay()
+        torch.cuda.synchronize()
+        st = torch.cuda.current_stream()
+        a, b = _events(torch, 2)
+        a.record(st)
+        g_all.replay()
+        b.record(st)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
+    ms_two = graph_ms(False)
+    ms_one = graph_ms(True)
     nbytes = 2 * H * I * 2
+    gbs = nbytes / (ms_one * 1e-3) / 1e9
     return {"workload": "tiny decode MLP block B=1 (hidden 512, inter 2048, f16)", "metric": "weight GB/s",
-            "value": round(nbytes / (ms * 1e-3) / 1e9, 1), "us_per_step": round(ms * 1e3, 2),
-            "weight_bytes": nbytes, "launches_per_step": 2, "frac_of_hbm": round(nbytes / (ms * 1e-3) / 1e9 / pk["hbm"], 4),
+            "value": round(gbs, 1), "us_per_step": round(ms_one * 1e3, 2), "weight_bytes": nbytes,
+            "launches_per_step": 1, "frac_of_hbm": round(gbs / pk["hbm"], 4),
+            "timed": "CUDA graph of K steps of the one-launch form (pgq_mlp_f16_decode_fused)",
+            "two_launch_graph_us_per_step": round(ms_two * 1e3, 2),
+            "two_launch_direct_us_per_step": round(ms_direct * 1e3, 2),
             "note": "launch-latency bound (4 MiB is 0.6 us at HBM peak); weights rotate over 64 copies"}
 
 
@@ -472,6 +499,31 @@ def bench_moe(torch, pgq, synth, steps, warmup, pk, graph=True):
             "weight_GBps": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm"], 4), "launches_per_step": 7,
             "timed": ("CUDA-graph replay of the layer call (ms_per_layer_api: direct calls)" if graph
                       else "direct calls (no graph)")}
+
+
+def time_q8_layer_fused(torch, pgq, W, steps, warmup):
+    """ms per step of the one-launch form of the layer: one CUDA graph of `steps`
+    calls over the rotating weight copies (after a warm-up replay)."""
+    sync = pgq.layer_sync()
+    structs = [pgq.q8_layer_struct(L) for L in W.layers]
+    n = len(structs)
+
+    def steps_of(k):
+        for i in range(k):
+            pgq.q8_decode_layer_fused(structs[i % n], W.x[0], W.xo[0], W.g, 1e-6, sync=sync, out=W.out1,
+                                      weights_stable=True)
+
+    g_all = _capture(torch, lambda: steps_of(steps))
+    for _ in range(max(1, warmup // steps + 1)):
+        g_all.replay()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    a, b = _events(torch, 2)
+    a.record(st)
+    g_all.replay()
+    b.record(st)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
 
 
 def time_e2e(torch, W, steps, warmup):
@@ -647,6 +699,7 @@ def main():
     with Clocks(local) as clk:
         total_ms, k1_ms, k2_ms = time_q8_layer(torch, W, args.steps, args.warmup)
     clocks = clk.summary()
+    fused_ms = time_q8_layer_fused(torch, pgq, W, args.steps, args.warmup)
     e2e_ms = time_e2e(torch, W, args.steps, args.warmup)
     total_ms, e2e_ms = max_over_ranks(torch, dist, [total_ms, e2e_ms], "cuda")
     ms_step = total_ms / args.steps
@@ -670,6 +723,10 @@ def main():
                      "down_launch_ms": round(k2_ms, 5)},
         "e2e": {"value": round(job_gbs(world, W.step_bytes, e2e_ms), 1), "unit": "GB/s",
                 "h2d_bytes_per_step": W.h2d, "d2h_bytes_per_step": W.d2h, "ms_per_step": round(e2e_ms, 5)},
+        "one_launch_form": {"entry": "pgq_q8_decode_layer_fused", "us_per_step": round(fused_ms * 1e3, 3),
+                            "value": round(W.step_bytes / (fused_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                            "note": "the same layer in one persistent launch (device-side dependency); "
+                                    "slower than the two programmatic-dependent launches here"},
         "gpu_launches": W.launches_per_step * args.steps,
         "clocks": clocks,
     }

@@ -315,6 +315,30 @@ int pgq_q8_decode_layer_ex(const pgq_q8_layer* layer, const float* x, const floa
                            const float* gamma, float eps, float* q, float* k, float* v, float* o,
                            float* u, float* down, int flags, void* stream);
 
+/* ---------------------------------------------------------------- fused decode layers
+ * The same computations as pgq_q8_decode_layer_ex and pgq_mlp_f16_decode in ONE
+ * launch instead of two (the pages' first fusion rule: embryo_wide.wgsl's header
+ * puts a dispatch boundary at about 8 us on M4 and 5 us on RTX 2000 Ada, and fuses
+ * stages wherever one launch can hold the dependency).  The launch is persistent (one
+ * block per SM): its blocks run the first projections (norm + q, k, v, o, up; or the
+ * MLP's up), count themselves done in `sync`, stream their first weight stages of
+ * the second projection (down) and wait, bounded, until every block is done with the
+ * first before reading its output.  A wait that runs out is reported by
+ * pgq_last_device_status (PGQ_ETIMEOUT).
+ * sync: caller-owned device memory of PGQ_LAYER_SYNC_BYTES, 16-byte aligned, zero
+ * before the first call; every call leaves it zero again.  Calls that share a sync
+ * word must be ordered on one stream.  One position; other arguments and outputs as
+ * the two-launch forms.  PGQ_EUNSUPPORTED (nothing launched) for shapes the fused
+ * kernel does not take (those of pgq_q8_decode_layer with hidden and inter
+ * multiples of 128 fit). */
+#define PGQ_LAYER_SYNC_BYTES 16
+int pgq_q8_decode_layer_fused(const pgq_q8_layer* layer, const float* x, const float* x_o,
+                              const float* gamma, float eps, float* q, float* k, float* v, float* o,
+                              float* u, float* down, int flags, void* sync, void* stream);
+int pgq_mlp_f16_decode_fused(const float* h, const uint16_t* W_up, const uint16_t* W_down, int hidden,
+                             int inter, const float* gamma, float eps, float* u, float* y, void* sync,
+                             void* stream);
+
 /* ---------------------------------------------------------------- a4: prefill q8
  * Batched prefill projection of a pass of 1 <= B <= 64 positions through q8
  * matrices, every weight read from memory once per pass (the read-once rule of the

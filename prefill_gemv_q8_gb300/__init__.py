@@ -87,6 +87,9 @@ _SIGS = {
                                 _vp]),
     "pgq_q82f_decode_layer": (C.c_int, [C.POINTER(Q82Layer), _vp, _vp, _vp, C.c_float, _vp, _vp, _vp, _vp, _vp,
                                         _vp, C.c_int, _vp]),
+    "pgq_q8_decode_layer_fused": (C.c_int, [C.POINTER(Q8Layer), _vp, _vp, _vp, C.c_float, _vp, _vp, _vp, _vp, _vp,
+                                            _vp, C.c_int, _vp, _vp]),
+    "pgq_mlp_f16_decode_fused": (C.c_int, [_vp, _vp, _vp, C.c_int, C.c_int, _vp, C.c_float, _vp, _vp, _vp, _vp]),
     "pgq_mlp_f16_decode": (C.c_int, [_vp, _vp, _vp, C.c_int, C.c_int, _vp, C.c_float, _vp, _vp, _vp]),
     "pgq_q8_decode_layer": (C.c_int, [C.POINTER(Q8Layer), _vp, _vp, _vp, C.c_float, _vp, _vp, _vp, _vp, _vp,
                                       _vp, _vp]),
@@ -490,6 +493,49 @@ def q8_decode_layer(mats, x, x_o, gamma, eps=1e-6, out=None, stream=None, weight
                                         _ptr(out["down"]), WEIGHTS_STABLE if weights_stable else 0,
                                         _stream(stream)))
     return out
+
+
+LAYER_SYNC_BYTES = 16
+
+
+def layer_sync(device="cuda"):
+    """A zeroed sync word for the fused (one-launch) decode layers."""
+    return torch.zeros(LAYER_SYNC_BYTES // 4, dtype=torch.int32, device=device)
+
+
+def q8_decode_layer_fused(mats, x, x_o, gamma, eps=1e-6, sync=None, out=None, stream=None, weights_stable=False):
+    """The q8 decode layer in one launch (see q8_decode_layer); ``sync`` from
+    layer_sync(), ordered on one stream between calls."""
+    L = mats if isinstance(mats, Q8Layer) else q8_layer_struct(mats)
+    if sync is None:
+        sync = layer_sync(x.device)
+    if out is None:
+        out = {s: torch.empty(n, dtype=torch.float32, device=x.device) for s, n in
+               (("q", L.hidden), ("k", L.kv), ("v", L.kv), ("o", L.hidden), ("u", L.inter), ("down", L.hidden))}
+    _check(lib().pgq_q8_decode_layer_fused(C.byref(L), _ptr(x), _ptr(x_o), _ptr(gamma), eps, _ptr(out["q"]),
+                                           _ptr(out["k"]), _ptr(out["v"]), _ptr(out["o"]), _ptr(out["u"]),
+                                           _ptr(out["down"]), WEIGHTS_STABLE if weights_stable else 0, _ptr(sync),
+                                           _stream(stream)))
+    return out
+
+
+def mlp_f16_decode_fused(h, W_up, W_down, gamma, eps=1e-6, sync=None, u=None, y=None, stream=None):
+    """The tiny MLP block in one launch (see mlp_f16_decode); returns (y, u)."""
+    _need(h, torch.float32, "h")
+    hidden = h.numel()
+    inter = W_up.shape[0]
+    _need(W_up, torch.float16, "W_up", (inter, hidden))
+    _need(W_down, torch.float16, "W_down", (hidden, inter))
+    _need(gamma, torch.float32, "gamma", (hidden,))
+    if sync is None:
+        sync = layer_sync(h.device)
+    if u is None:
+        u = torch.empty(inter, dtype=torch.float32, device=h.device)
+    if y is None:
+        y = torch.empty(hidden, dtype=torch.float32, device=h.device)
+    _check(lib().pgq_mlp_f16_decode_fused(_ptr(h), _ptr(W_up), _ptr(W_down), hidden, inter, _ptr(gamma), eps, _ptr(u),
+                                          _ptr(y), _ptr(sync), _stream(stream)))
+    return y, u
 
 
 def prefill_pass_workspace(hidden, kv, inter, B, device="cuda"):

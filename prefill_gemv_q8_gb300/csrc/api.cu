@@ -237,8 +237,9 @@ static int check_decode_common(const char* name, int rows, int cols, const float
 }
 
 namespace {
+// (build_only != NULL: check the arguments and fill *build_only instead of launching)
 int gemv_f16_impl(const uint16_t* W, int rows, int cols, const float* x, int B, const float* gamma, float eps, float* y,
-                  int epilogue, const float* residual, int early_weights, void* stream);
+                  int epilogue, const float* residual, int early_weights, void* stream, GvParams* build_only = nullptr);
 }  // namespace
 
 int pgq_gemv_f16(const uint16_t* W, int rows, int cols, const float* x, int B, const float* gamma, float eps, float* y,
@@ -249,7 +250,7 @@ int pgq_gemv_f16(const uint16_t* W, int rows, int cols, const float* x, int B, c
 namespace {
 // pgq_gemv_f16 with the early-weights flag (GvParams::early_weights)
 int gemv_f16_impl(const uint16_t* W, int rows, int cols, const float* x, int B, const float* gamma, float eps, float* y,
-                  int epilogue, const float* residual, int early_weights, void* stream) {
+                  int epilogue, const float* residual, int early_weights, void* stream, GvParams* build_only) {
   REQUIRE(W && y, PGQ_EINVAL, "gemv_f16: W and y must be non-null");
   REQUIRE(aligned16(W), PGQ_EALIGN, "gemv_f16: W must be 16-byte aligned");
   int st = check_decode_common("gemv_f16", rows, cols, x, B, gamma, eps, y, epilogue, residual);
@@ -264,6 +265,10 @@ int gemv_f16_impl(const uint16_t* W, int rows, int cols, const float* x, int B, 
   P.cols = cols;
   P.eps = eps;
   P.early_weights = early_weights;
+  if (build_only) {
+    *build_only = P;
+    return PGQ_OK;
+  }
   return launch_gemv(P, false, false, dev, as_stream(stream));
 }
 }  // namespace
@@ -327,9 +332,10 @@ int pgq_gemv_q8(const int8_t* codes, const uint16_t* params, int rows, int cols,
 }
 
 namespace {
-// pgq_gemv_q8_multi with the early-weights flag (GvParams::early_weights)
+// pgq_gemv_q8_multi with the early-weights flag (GvParams::early_weights); with
+// build_only != NULL it checks the arguments and fills *build_only instead of launching
 int gemv_q8_multi_impl(const pgq_q8_job* jobs, int njobs, const pgq_input* inputs, int ninputs, int cols, int B,
-                       float eps, int early_weights, void* stream);
+                       float eps, int early_weights, void* stream, GvParams* build_only = nullptr);
 }  // namespace
 
 int pgq_gemv_q8_multi(const pgq_q8_job* jobs, int njobs, const pgq_input* inputs, int ninputs, int cols, int B,
@@ -339,7 +345,7 @@ int pgq_gemv_q8_multi(const pgq_q8_job* jobs, int njobs, const pgq_input* inputs
 
 namespace {
 int gemv_q8_multi_impl(const pgq_q8_job* jobs, int njobs, const pgq_input* inputs, int ninputs, int cols, int B,
-                       float eps, int early_weights, void* stream) {
+                       float eps, int early_weights, void* stream, GvParams* build_only) {
   REQUIRE(jobs && inputs, PGQ_EINVAL, "gemv_q8: jobs and inputs must be non-null");
   REQUIRE(njobs >= 1 && njobs <= PGQ_MULTI_MAX, PGQ_EINVAL, "gemv_q8: njobs=%d outside 1..%d", njobs, PGQ_MULTI_MAX);
   REQUIRE(ninputs >= 1 && ninputs <= MAX_INPUTS, PGQ_EINVAL, "gemv_q8: ninputs=%d outside 1..%d", ninputs,
@@ -374,6 +380,10 @@ int gemv_q8_multi_impl(const pgq_q8_job* jobs, int njobs, const pgq_input* input
   P.cols = cols;
   P.eps = eps;
   P.early_weights = early_weights;
+  if (build_only) {
+    *build_only = P;
+    return PGQ_OK;
+  }
   return launch_gemv(P, true, false, dev, as_stream(stream));
 }
 }  // namespace
@@ -504,6 +514,55 @@ int pgq_q8_decode_layer_ex(const pgq_q8_layer* L, const float* x, const float* x
   pgq_q8_job dj{L->down.codes, L->down.params, H, 0, down, PGQ_EPI_NONE, nullptr};
   pgq_input din{u, nullptr};
   return gemv_q8_multi_impl(&dj, 1, &din, 1, I, 1, 0.f, 1, stream);
+}
+
+// ------------------------------------------------------------------ fused decode layers
+static int check_sync(const void* sync) {
+  REQUIRE(sync && aligned16(sync), PGQ_EINVAL, "fused layer: the sync word must be non-null and 16-byte aligned");
+  return PGQ_OK;
+}
+
+int pgq_q8_decode_layer_fused(const pgq_q8_layer* L, const float* x, const float* x_o, const float* gamma, float eps,
+                              float* q, float* k, float* v, float* o, float* u, float* down, int flags, void* sync,
+                              void* stream) {
+  REQUIRE(L && x && x_o && gamma && q && k && v && o && u && down, PGQ_EINVAL, "q8_decode_layer_fused: null pointer");
+  REQUIRE((flags & ~PGQ_WEIGHTS_STABLE) == 0, PGQ_EINVAL, "q8_decode_layer_fused: unknown flags 0x%x", flags);
+  if (int st = check_sync(sync)) return st;
+  const int H = L->hidden, KV = L->kv, I = L->inter;
+  pgq_q8_job jobs[5] = {
+      {L->q.codes, L->q.params, H, 0, q, PGQ_EPI_NONE, nullptr},
+      {L->k.codes, L->k.params, KV, 0, k, PGQ_EPI_NONE, nullptr},
+      {L->v.codes, L->v.params, KV, 0, v, PGQ_EPI_NONE, nullptr},
+      {L->o.codes, L->o.params, H, 1, o, PGQ_EPI_NONE, nullptr},
+      {L->up.codes, L->up.params, I, 0, u, PGQ_EPI_RELU2, nullptr},
+  };
+  pgq_input ins[2] = {{x, gamma}, {x_o, nullptr}};
+  GvParams A{}, Bp{};
+  int st = gemv_q8_multi_impl(jobs, 5, ins, 2, H, 1, eps, (flags & PGQ_WEIGHTS_STABLE) ? 1 : 0, stream, &A);
+  if (st) return st;
+  pgq_q8_job dj{L->down.codes, L->down.params, H, 0, down, PGQ_EPI_NONE, nullptr};
+  pgq_input din{u, nullptr};
+  if ((st = gemv_q8_multi_impl(&dj, 1, &din, 1, I, 1, 0.f, 1, stream, &Bp))) return st;
+  GET_DEVICE(dev);
+  st = launch_gemv_layer(A, Bp, true, static_cast<unsigned*>(sync), dev, as_stream(stream));
+  if (st == PGQ_EUNSUPPORTED) return set_error(st, "q8_decode_layer_fused: shapes outside the fused kernel's limits");
+  return st;
+}
+
+int pgq_mlp_f16_decode_fused(const float* h, const uint16_t* W_up, const uint16_t* W_down, int hidden, int inter,
+                             const float* gamma, float eps, float* u, float* y, void* sync, void* stream) {
+  REQUIRE(h && W_up && W_down && gamma && u && y, PGQ_EINVAL, "mlp_f16_decode_fused: null pointer");
+  REQUIRE(!overlaps(u, (size_t)inter * 4, h, (size_t)hidden * 4) && !overlaps(u, (size_t)inter * 4, y, (size_t)hidden * 4),
+          PGQ_EINVAL, "mlp_f16_decode_fused: u must not overlap h or y");
+  if (int st = check_sync(sync)) return st;
+  GvParams A{}, Bp{};
+  int st = gemv_f16_impl(W_up, inter, hidden, h, 1, gamma, eps, u, PGQ_EPI_RELU2, nullptr, 0, stream, &A);
+  if (st) return st;
+  if ((st = gemv_f16_impl(W_down, hidden, inter, u, 1, nullptr, 0.f, y, PGQ_EPI_ADD, h, 1, stream, &Bp))) return st;
+  GET_DEVICE(dev);
+  st = launch_gemv_layer(A, Bp, false, static_cast<unsigned*>(sync), dev, as_stream(stream));
+  if (st == PGQ_EUNSUPPORTED) return set_error(st, "mlp_f16_decode_fused: shapes outside the fused kernel's limits");
+  return st;
 }
 
 // ------------------------------------------------------------------ prefill

@@ -103,8 +103,14 @@ __device__ __forceinline__ int gt_perm(int c) {
 // FMT: 0 binary16 rows; 1 q8 block format (per-32 scale and offset); 2 q8_2f (row
 // scale x column field: the column field folds into the input values, the row
 // scale multiplies the finished sum, as gemma_batch.rs `q8_2f_mm_r2` does).
+// The body of one decode launch.  mode 0: a launch of its own (it lets the next
+// kernel in the stream start early and waits for the previous one before reading its
+// inputs); modes 1 and 2: the first and second half of a fused layer launch
+// (pgq_gemv_layer_kernel), where the second half's input is the first half's output
+// and its wait is for every block of the grid to have finished the first half (the
+// count in sync[0]), not for a previous kernel.
 template <int FMT, int NB, bool ARGMAX, int W, int RPW, int MAXC>
-__global__ void __launch_bounds__((W + 1) * 32, 1) pgq_gemv_tma_kernel(const __grid_constant__ GtParams P) {
+__device__ __forceinline__ void gt_body(const GtParams& P, const int mode, const unsigned* sync) {
   constexpr bool Q8 = FMT != 0;    // int8 codes
   constexpr bool BLK = FMT == 1;   // with a plane of (scale, offset) pairs
   constexpr bool F2 = FMT == 2;
@@ -180,8 +186,8 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) pgq_gemv_tma_kernel(const __g
 
   // A launch that follows this one in the stream as a programmatic dependent may take
   // the SMs this grid frees from here on; it reads nothing this grid writes before
-  // its own griddepcontrol.wait.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // its own griddepcontrol.wait.  (A fused layer launch does this once, up front.)
+  if (mode == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // The first copies go out before anything else, all from the producer lane, in the
   // order they are needed: it sets up the barriers, then issues the ring's first
@@ -190,6 +196,7 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) pgq_gemv_tma_kernel(const __g
   // the launcher allows it they stream before the wait for the previous kernel (and
   // so ahead of the inputs), else after it.  The block-wide barrier below publishes
   // the barrier set-up to the other warps before any of them waits on one.
+  bool in_issued = false;   // producer lane: the inputs' copies are out
   auto issue_inputs = [&]() {
     if constexpr (NB == 1) {
       // each plane lands 128-byte swizzled (16-byte word c of row R at c ^ (R mod 8))
@@ -217,10 +224,15 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) pgq_gemv_tma_kernel(const __g
 #ifdef PGQ_TRACE
     GTRACE(11);
 #endif
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (!P.early) issue_ring(0, 1);
-    if (!P.stall) issue_inputs();
-    if (!P.early) issue_ring(1, GT_RAMP);
+    if (mode != 2) {   // (the second half of a fused launch waits for its input below)
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      if (!P.early) issue_ring(0, 1);
+      if (!P.stall) {
+        issue_inputs();
+        in_issued = true;
+      }
+      if (!P.early) issue_ring(1, GT_RAMP);
+    }
 #ifdef PGQ_TRACE
     GTRACE(3);
 #endif
@@ -266,7 +278,35 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) pgq_gemv_tma_kernel(const __g
     GTRACE(9);
   }
 #endif
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (mode != 2) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+  } else if (producer && lane == 0) {
+    // the second half's input (the first half's output) exists once every block of
+    // the grid has finished the first half; a bounded wait, then the input copies
+    // (async proxy) after the generic writes they read
+    const uint64_t w0 = tc::globaltimer();
+    bool ok = true;
+    while (true) {
+      unsigned v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(sync) : "memory");
+      if (v >= gridDim.x) break;
+      if (tc::globaltimer() - w0 > P.wait_limit_ns) {
+        ok = false;
+        break;
+      }
+      __nanosleep(64);
+    }
+    if (ok) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      if (!P.stall) {
+        issue_inputs();
+        in_issued = true;
+      }
+    } else {
+      *(volatile int*)&s_abort = 1;
+      atomicExch(&g_decode_status, PGQ_ETIMEOUT);
+    }
+  }
 #ifdef PGQ_TRACE
   if (tid == 0) GTRACE(8);
 #endif
@@ -765,7 +805,7 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) pgq_gemv_tma_kernel(const __g
   // (i / GT_NST)-th fill of slot i mod GT_NST, so it completes that phase's parity)
   if (producer && lane == 0 && *(volatile int*)&s_abort) {
     if constexpr (NB == 1) {
-      if (!P.stall) {
+      if (in_issued) {
         const uint64_t w0 = tc::globaltimer();
         while (!tc::mbar_try_sleep(tc::smem_addr(inbar), 0u, 20000u) && tc::globaltimer() - w0 < P.wait_limit_ns) {
         }
@@ -814,6 +854,53 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) pgq_gemv_tma_kernel(const __g
       if (tid == 0) *P.ticket = 0u;
     }
   }
+  if (mode == 1) {
+    // the second half lays out its own ring and barriers over this shared memory:
+    // this half's barriers are retired first (nothing waits on them any more)
+    __syncthreads();
+    if (producer && lane == 0) {
+      for (int s2 = 0; s2 < GT_NST; ++s2) {
+        asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(tc::smem_addr(full + s2)) : "memory");
+        asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(tc::smem_addr(empty + s2)) : "memory");
+      }
+      asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(tc::smem_addr(inbar)) : "memory");
+    }
+  }
+}
+
+template <int FMT, int NB, bool ARGMAX, int W, int RPW, int MAXC>
+__global__ void __launch_bounds__((W + 1) * 32, 1) pgq_gemv_tma_kernel(const __grid_constant__ GtParams P) {
+  gt_body<FMT, NB, ARGMAX, W, RPW, MAXC>(P, 0, nullptr);
+}
+
+// A decode layer's two dependent launches as one (one position): the first half
+// (e.g. norm + q, k, v, o, up) and the second (e.g. down, whose input is the first
+// half's relu² output).  Every block counts itself in sync[0] after the first half;
+// the second half streams its first weight stages, then waits (bounded) for the count
+// to reach the grid before its input copies.  The last block out of the second half
+// sets both counters back to zero, so the word is ready for the next call.  All
+// blocks are resident: one per SM, and the grid is at most the SM count.
+struct GtPair {
+  GtParams A, B;
+  unsigned* sync;   // [0]: blocks done with the first half, [1]: blocks done
+};
+template <int FMT, int W, int RPW, int MAXC>
+__global__ void __launch_bounds__((W + 1) * 32, 1) pgq_gemv_layer_kernel(const __grid_constant__ GtPair PP) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  gt_body<FMT, 1, false, W, RPW, MAXC>(PP.A, 1, PP.sync);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");   // the block's outputs, then its count
+    atomicAdd(PP.sync, 1u);
+  }
+  gt_body<FMT, 1, false, W, RPW, MAXC>(PP.B, 2, PP.sync);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (atomicAdd(PP.sync + 1, 1u) == gridDim.x - 1) {
+      atomicExch(PP.sync, 0u);
+      atomicExch(PP.sync + 1, 0u);
+    }
+  }
 }
 
 namespace {
@@ -829,7 +916,12 @@ GtFn gt_pick(int nb) {
 }
 }  // namespace
 
-int launch_gemv_tma(const GvParams& V, bool q8, bool argmax, const DeviceInfo& dev, cudaStream_t st) {
+namespace {
+// The launch parameters of one decode launch (the TMA kernel): P, the dynamic shared
+// memory and the position count it is compiled for.  PGQ_EUNSUPPORTED (nothing
+// launched) for shapes the kernel does not take.
+int prepare_gt(const GvParams& V, bool q8, bool argmax, const DeviceInfo& dev, GtParams& P, size_t& smem_out,
+               int& nb_out) {
   const int nb = V.B <= 1 ? 1 : V.B <= 2 ? 2 : V.B <= 4 ? 4 : 8;
   const int esz = q8 ? 1 : 2;
   const int EPL = q8 ? 16 : 8, CW = 32 * EPL;
@@ -846,7 +938,7 @@ int launch_gemv_tma(const GvParams& V, bool q8, bool argmax, const DeviceInfo& d
   const int QW = W * RPW / SR;
   const int cpw = (nchunks + QW - 1) / QW;
   if (cpw > MAXC) return PGQ_EUNSUPPORTED;
-  GtParams P{};
+  P = GtParams{};
   int t = 0;
   for (int j = 0; j < V.njobs; ++j) {
     P.w[j] = V.job[j].w;
@@ -923,22 +1015,37 @@ int launch_gemv_tma(const GvParams& V, bool q8, bool argmax, const DeviceInfo& d
                       GT_RED * (size_t)SR * std::max(nb, GT_GROUP) * QW * 4 + 128 +
                       (size_t)GT_NST * P.slot_bytes + (2 * GT_NST + 1) * 8 + 64;
   if (smem + 2048 > dev.smem_optin) return PGQ_EUNSUPPORTED;   // + the static shared memory
+  smem_out = smem;
+  nb_out = nb;
+  return PGQ_OK;
+}
+
+// Raises a kernel's dynamic shared-memory limit once per (kernel, device, size).
+int allow_dyn_smem(const void* fn, int device, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, size_t> done;
+  std::lock_guard<std::mutex> lk(mu);
+  size_t& cur = done[{fn, device}];
+  if (smem > cur) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_status(e);
+    cur = smem;
+  }
+  return PGQ_OK;
+}
+}  // namespace
+
+int launch_gemv_tma(const GvParams& V, bool q8, bool argmax, const DeviceInfo& dev, cudaStream_t st) {
+  GtParams P;
+  size_t smem = 0;
+  int nb = 1;
+  if (const int rc = prepare_gt(V, q8, argmax, dev, P, smem, nb)) return rc;
+  const bool f2 = q8 && V.q82f;
+  constexpr int W = 16;
   GtFn fn = f2 ? gt_pick<2, false>(nb)
                : q8 ? (argmax ? gt_pick<1, true>(nb) : gt_pick<1, false>(nb))
                     : (argmax ? gt_pick<0, true>(nb) : gt_pick<0, false>(nb));
-  {
-    // raise the kernel's shared-memory limit once per (kernel, device, size)
-    static std::mutex mu;
-    static std::map<std::pair<GtFn, int>, size_t> done;
-    std::lock_guard<std::mutex> lk(mu);
-    size_t& cur = done[{fn, dev.device}];
-    if (smem > cur) {
-      cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return cuda_status(e);
-      cur = smem;
-    }
-  }
+  if (const int rc = allow_dyn_smem(reinterpret_cast<const void*>(fn), dev.device, smem)) return rc;
   if (argmax) {
     if (cudaError_t e = cudaMemsetAsync(P.ticket, 0, sizeof(unsigned), st); e != cudaSuccess) return cuda_status(e);
   }
@@ -957,6 +1064,40 @@ int launch_gemv_tma(const GvParams& V, bool q8, bool argmax, const DeviceInfo& d
   cfg.numAttrs = 1;
   void* args[] = {&P};
   return cuda_status(cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(fn), args));
+}
+
+int launch_gemv_layer(const GvParams& VA, const GvParams& VB, bool q8, unsigned* sync, const DeviceInfo& dev,
+                      cudaStream_t st) {
+  if (VA.B != 1 || VB.B != 1 || (q8 && VA.q82f != VB.q82f)) return PGQ_EUNSUPPORTED;
+  GtPair PP;
+  size_t smem_a = 0, smem_b = 0;
+  int nb = 1;
+  if (const int rc = prepare_gt(VA, q8, false, dev, PP.A, smem_a, nb)) return rc;
+  if (const int rc = prepare_gt(VB, q8, false, dev, PP.B, smem_b, nb)) return rc;
+  PP.B.early = 1;   // the second half streams its first stages before its wait
+  PP.B.stall = 0;
+  PP.sync = sync;
+  const size_t smem = std::max(smem_a, smem_b);
+  constexpr int W = 16;
+  const bool f2 = q8 && VA.q82f;
+  const void* fn = f2   ? reinterpret_cast<const void*>(&pgq_gemv_layer_kernel<2, W, 2, 2>)
+                   : q8 ? reinterpret_cast<const void*>(&pgq_gemv_layer_kernel<1, W, 2, 2>)
+                        : reinterpret_cast<const void*>(&pgq_gemv_layer_kernel<0, W, 2, 2>);
+  if (const int rc = allow_dyn_smem(fn, dev.device, smem)) return rc;
+  // one block per SM at most (the shared memory allows no second), so every block of
+  // the grid is resident and the second half's wait ends
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(std::max(1, std::min(dev.sms, std::max(PP.A.ntasks, PP.B.ntasks))));
+  cfg.blockDim = dim3((W + 1) * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {&PP};
+  return cuda_status(cudaLaunchKernelExC(&cfg, fn, args));
 }
 
 int decode_status_read_and_clear(int* out) {

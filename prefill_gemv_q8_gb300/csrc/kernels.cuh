@@ -66,6 +66,10 @@ int launch_gemv(GvParams& P, bool q8, bool argmax, const DeviceInfo& dev, cudaSt
 // ring).  Returns PGQ_EUNSUPPORTED (nothing launched) for shapes it does not take.
 int launch_gemv_tma(const GvParams& P, bool q8, bool argmax, const DeviceInfo& dev, cudaStream_t st);
 int decode_status_read_and_clear(int* out);
+// Two dependent one-position decode launches (VA, then VB reading VA's output) as
+// one fused launch; sync: 2 device counters, zero before, left zero after.
+int launch_gemv_layer(const GvParams& VA, const GvParams& VB, bool q8, unsigned* sync, const DeviceInfo& dev,
+                      cudaStream_t st);
 // Tensor-core vocab head (f16 weights, 2 <= B <= 8, fused RMSNorm and argmax); returns
 // PGQ_EUNSUPPORTED (nothing launched) for shapes it does not take.
 int launch_head_tc(const GvParams& P, const DeviceInfo& dev, cudaStream_t st);
