@@ -127,14 +127,14 @@ int pgq_last_device_status(const void* workspace, void* stream) {
   int dec = PGQ_OK;
   const int rc = decode_status_read_and_clear(&dec);
   if (rc) return rc;
-  int ws = PGQ_OK;
+  int ws[2] = {PGQ_OK, PGQ_OK};
   if (workspace) {
-    e = cudaMemcpy(&ws, static_cast<const char*>(workspace) + prefill_status_offset(), sizeof(int),
+    e = cudaMemcpy(ws, static_cast<const char*>(workspace) + prefill_status_offset(), sizeof(ws),
                    cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_status(e);
   }
   if (dec != PGQ_OK) return dec;
-  return ws;
+  return ws[0] != PGQ_OK ? ws[0] : ws[1];
 }
 
 int pgq_add_rmsnorm(float* h, const float* add, const float* gamma, float eps, int B, int n, float* y,
@@ -737,27 +737,28 @@ int pgq_moe_combine_rmsnorm(float* h, const float* o, const float* eo, const flo
 
 namespace {
 struct MoeLayout {
-  size_t gemm;
+  size_t gemm;    // the tensor-core banks' area, first: its status word at offset 0
+  size_t gend;    // end of that area
   size_t off[9];  // n, logits, sel, w, counts, offsets, entries, u, eo
   size_t total;
 };
 MoeLayout moe_layout(const pgq_moe_layer& L, int B) {
   MoeLayout M{};
   const size_t nb = (size_t)B * L.k;
+  DeviceInfo dev;
+  if (!device_info(&dev)) dev.sms = 160;
+  const size_t g = std::max(moe_bank_tc_workspace_bytes(L.E, L.inter, L.hidden, (int)nb, dev),
+                            moe_bank_tc_workspace_bytes(L.E, L.hidden, L.inter, (int)nb, dev));
+  M.gemm = 0;
+  size_t o = (g + 255) / 256 * 256;
+  M.gend = o;
   const size_t sz[9] = {(size_t)B * L.hidden * 4, (size_t)B * L.E * 4, nb * 4, nb * 4, (size_t)L.E * 4,
                         ((size_t)L.E + 1) * 4, nb * 4, nb * L.inter * 4, nb * L.hidden * 4};
-  size_t o = 0;
   for (int i = 0; i < 9; ++i) {
     M.off[i] = o;
     o = (o + sz[i] + 255) / 256 * 256;
   }
-  // the tensor-core expert bank's area (gathered binary16 inputs, split-tile partials)
-  DeviceInfo dev;
-  if (!device_info(&dev)) dev.sms = 160;
-  M.gemm = o;
-  const size_t g = std::max(moe_bank_tc_workspace_bytes(L.E, L.inter, L.hidden, (int)nb, dev),
-                            moe_bank_tc_workspace_bytes(L.E, L.hidden, L.inter, (int)nb, dev));
-  M.total = o + (g + 255) / 256 * 256;
+  M.total = o;
   return M;
 }
 bool moe_layer_ok(const pgq_moe_layer* L, int B) {
@@ -800,30 +801,31 @@ int pgq_moe_prefill_layer(const pgq_moe_layer* L, float* h, int B, const float* 
   if ((rc = pgq_moe_router(L->router, L->E, L->hidden, n, B, logits, stream))) return rc;
   if ((rc = pgq_moe_route_topk(logits, B, L->E, L->k, L->renorm, sel, wts, stream))) return rc;
   if ((rc = pgq_moe_group_gather(sel, B, L->k, L->E, counts, offs, ents, nullptr, 0, 1, nullptr, stream))) return rc;
+  GET_DEVICE(dev);
   const int nent = B * L->k;
-  // each bank on the tensor cores where its shape allows, else the expert GEMV kernel
+  // each bank on the tensor cores where its shape allows, else the expert GEMV kernel;
+  // the first bank resets the banks' status word, the second keeps what it records
   auto bank = [&](const int8_t* codes, const uint16_t* params, int rows, int cols, const float* x, int xdiv, float* yb,
-                  int epi) -> int {
-    GET_DEVICE(dev);
+                  int epi, bool first) -> int {
     const MoeBankArgs a{codes, params, L->E, rows, cols, counts, offs, ents, nent, x, xdiv, yb, epi};
-    const int r = launch_moe_bank_tc(a, w + M.gemm, workspace_bytes - M.gemm, dev, as_stream(stream));
+    const int r = launch_moe_bank_tc(a, w + M.gemm, M.gend - M.gemm, dev, as_stream(stream), first);
     if (r != PGQ_EUNSUPPORTED) return r;
     return pgq_moe_experts_q8(codes, params, L->E, rows, cols, counts, offs, ents, nent, x, xdiv, yb, epi, stream);
   };
-  if ((rc = bank(L->up_codes, L->up_params, L->inter, L->hidden, n, L->k, u, PGQ_EPI_RELU2))) return rc;
-  if ((rc = bank(L->down_codes, L->down_params, L->hidden, L->inter, u, 1, eo, PGQ_EPI_NONE))) return rc;
+  if ((rc = bank(L->up_codes, L->up_params, L->inter, L->hidden, n, L->k, u, PGQ_EPI_RELU2, true))) return rc;
+  if ((rc = bank(L->down_codes, L->down_params, L->hidden, L->inter, u, 1, eo, PGQ_EPI_NONE, false))) return rc;
   return pgq_moe_combine_rmsnorm(h, nullptr, eo, wts, L->k, gamma2, eps, B, L->hidden, y, nullptr, stream);
 }
 
 int pgq_prefill_status(const void* workspace, void* stream) {
   REQUIRE(workspace, PGQ_EINVAL, "prefill_status: null workspace");
   GET_DEVICE(dev);
-  int v = 0;
-  cudaError_t e = cudaMemcpyAsync(&v, static_cast<const char*>(workspace) + prefill_status_offset(), sizeof(int),
+  int v[2] = {PGQ_OK, PGQ_OK};   // the status word, then a second one (reserved)
+  cudaError_t e = cudaMemcpyAsync(v, static_cast<const char*>(workspace) + prefill_status_offset(), sizeof(v),
                                   cudaMemcpyDeviceToHost, as_stream(stream));
   if (e == cudaSuccess) e = cudaStreamSynchronize(as_stream(stream));
   if (e != cudaSuccess) return cuda_status(e);
-  return v;
+  return v[0] != PGQ_OK ? v[0] : v[1];
 }
 
 }  // extern "C"

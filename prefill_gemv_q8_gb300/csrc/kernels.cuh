@@ -134,7 +134,10 @@ int launch_moe_bank(const MoeBankArgs& a, const DeviceInfo& dev, cudaStream_t st
 // The same on the tensor cores (the prefill kernel over a grouped bank, entries of an
 // expert as its N columns); PGQ_EUNSUPPORTED for shapes it does not take.
 size_t moe_bank_tc_workspace_bytes(int E, int rows, int cols, int nent, const DeviceInfo& dev);
-int launch_moe_bank_tc(const MoeBankArgs& a, void* ws, size_t ws_bytes, const DeviceInfo& dev, cudaStream_t st);
+// clear_status: the launch resets the workspace's status word first (the first bank of
+// a layer); else an earlier expired wait stays recorded
+int launch_moe_bank_tc(const MoeBankArgs& a, void* ws, size_t ws_bytes, const DeviceInfo& dev, cudaStream_t st,
+                       bool clear_status = true);
 int launch_moe_combine(float* h, const float* o, const float* eo, const float* w, int k, const float* gamma, float eps,
                        int B, int n, float* y, float* inv, cudaStream_t st);
 

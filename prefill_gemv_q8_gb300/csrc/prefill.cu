@@ -1005,7 +1005,10 @@ __global__ void __launch_bounds__(256) pgq_pass_input_kernel(const float* __rest
   const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (b == 0) {
     for (int i = threadIdx.x; i < ncounters; i += 256) counters[i] = 0u;
-    if (threadIdx.x == 0) *status = PGQ_OK;
+    if (threadIdx.x == 0) {
+      status[0] = PGQ_OK;
+      status[1] = PGQ_OK;   // (a second word, reserved: pgq_last_device_status reads both)
+    }
   }
   __half* out = xh + (size_t)b * K;
   if (b >= B) {
@@ -1067,12 +1070,16 @@ __global__ void __launch_bounds__(256) pgq_pass_input_kernel(const float* __rest
 __global__ void __launch_bounds__(256) pgq_moe_input_kernel(const float* __restrict__ x, int K,
                                                         const int32_t* __restrict__ ent, int nent, int xrows,
                                                         int xdiv, __half* __restrict__ xh, float* __restrict__ xinv,
-                                                        unsigned* counters, int ncounters, int* status) {
+                                                        unsigned* counters, int ncounters, int* status,
+                                                        int clear_status) {
   __shared__ float red[8];
   const int i = blockIdx.x;
   if (i == 0) {
     for (int c = threadIdx.x; c < ncounters; c += 256) counters[c] = 0u;
-    if (threadIdx.x == 0) *status = PGQ_OK;
+    if (threadIdx.x == 0 && clear_status) {
+      status[0] = PGQ_OK;
+      status[1] = PGQ_OK;
+    }
   }
   const int sr = min(max(ent[i], 0) / xdiv, xrows - 1);   // (entry ids are checked by the grouping)
   const float* row = x + (size_t)sr * K;
@@ -1191,6 +1198,7 @@ struct MoeSpec {
   const int32_t* ent;
   const float* x;            // input row of gathered row i: x[ent[i] / xdiv], of xrows rows
   int xrows, xdiv;
+  int clear_status;          // the gather kernel resets the status word first
 };
 
 struct Plan {
@@ -1354,7 +1362,8 @@ int launch_phases(const HostPhase* hp, int nph, const float* x0, const float* ga
     P.ments = moe->ent;
     P.mxinv = xinv;
     pgq_moe_input_kernel<<<moe->nent, 256, 0, st>>>(moe->x, K0, moe->ent, moe->nent, moe->xrows, moe->xdiv,
-                                                P.xh[hp[0].xk], xinv, cnt, pl.ncounters, P.status);
+                                                    P.xh[hp[0].xk], xinv, cnt, pl.ncounters, P.status,
+                                                    moe->clear_status);
   } else {
     pgq_pass_input_kernel<<<pl.Bp, 256, (size_t)(K0 / TC_BM) * sizeof(float2), st>>>(
         x0, B, K0, gamma0, eps, tap0, P.xh[hp[0].xk], xinv, cnt, pl.ncounters, P.status);
@@ -1470,7 +1479,8 @@ size_t moe_bank_tc_workspace_bytes(int E, int rows, int cols, int nent, const De
   return make_plan(&h, 1, 64, dev).total;
 }
 
-int launch_moe_bank_tc(const MoeBankArgs& a, void* ws, size_t ws_bytes, const DeviceInfo& dev, cudaStream_t st) {
+int launch_moe_bank_tc(const MoeBankArgs& a, void* ws, size_t ws_bytes, const DeviceInfo& dev, cudaStream_t st,
+                       bool clear_status) {
   // the tensor copies need 16-byte row strides of codes (pairs whose rows are not
   // go by 8-byte copies)
   if (a.cols % 32 != 0 || a.cols % 16 != 0 || a.E > PS_MOE_EMAX || a.nentries < 1 || !aligned16(a.codes) ||
@@ -1487,7 +1497,7 @@ int launch_moe_bank_tc(const MoeBankArgs& a, void* ws, size_t ws_bytes, const De
   h.moe_E = a.E;
   h.xrows = a.nentries;
   const int xrows = a.xdiv > 1 ? (a.nentries + a.xdiv - 1) / a.xdiv : a.nentries;
-  const MoeSpec m{a.E, a.nentries, a.counts, a.offsets, a.entries, a.x, xrows, a.xdiv};
+  const MoeSpec m{a.E, a.nentries, a.counts, a.offsets, a.entries, a.x, xrows, a.xdiv, clear_status ? 1 : 0};
   return launch_phases(&h, 1, nullptr, nullptr, nullptr, 0.f, 64, ws, ws_bytes, 0, dev, st, &m);
 }
 

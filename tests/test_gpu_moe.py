@@ -173,7 +173,11 @@ def test_moe_layer_small():
     g1, g2 = synth.gamma(H, 978), synth.gamma(H, 978, synth.T_GAMMA2)
     Wd = pgq.MoeWeights(dev(router), dev(up[0]), dev(up[1]), dev(down[0]), dev(down[1]), k)
     h = dev(h0)
-    y, ws = pgq.moe_prefill_layer(Wd, h, dev(g1), dev(g2), 1e-6)
+    ws = torch.full((pgq.moe_layer_workspace(Wd, B).numel(),), 0x55, dtype=torch.uint8, device="cuda")
+    y, ws = pgq.moe_prefill_layer(Wd, h, dev(g1), dev(g2), 1e-6, workspace=ws)
+    # the workspace's status words (the banks' area comes first) start from garbage
+    # and are set by the call itself
+    assert pgq.last_device_status(ws) == pgq.OK
     taps = pgq.moe_layer_taps(Wd, ws, B)
     _layer_check((up, down), router, h0, g1, g2, k, taps, h, y)
 
@@ -191,6 +195,7 @@ def test_moe_layer_full_size_sampled():
     W = pgq.MoeWeights(router, up[0], up[1], down[0], down[1], k)
     h = h0.clone()
     y, ws = pgq.moe_prefill_layer(W, h, g1, g2, 1e-6)
+    assert pgq.last_device_status(ws) == pgq.OK
     taps = pgq.moe_layer_taps(W, ws, B)
     sample = sorted(np.random.default_rng(0).choice(B * k, 36, replace=False).tolist())
     sel = host(taps["sel"]).reshape(-1)
