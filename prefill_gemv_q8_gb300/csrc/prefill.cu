@@ -52,7 +52,7 @@ constexpr int PS_EPI_WARP0 = 10;   // warps 10..13
 constexpr int PS_XP_WARP = 14;     // input-slice producer
 constexpr int PS_NA = 4;           // A buffers in tensor memory
 constexpr int PS_WST_MAX = 10;     // weight ring stages (at most; set by the shared memory left)
-constexpr int PS_XST = 3;          // input ring stages (4-6 measured no faster)
+constexpr int PS_XST = 3;          // input ring stages (4 measured no faster)
 constexpr int PS_CODES_BYTES = TC_BM * TC_BK;                 // 16 KB
 constexpr int PS_PARAMS_BYTES = TC_BM * 16;                   // 4 (scale, offset) pairs per row
 constexpr int PS_W_BYTES = PS_CODES_BYTES + PS_PARAMS_BYTES;  // 18 KB, a multiple of 1 KB
@@ -122,11 +122,15 @@ static_assert(sizeof(PsParams) <= 32000, "kernel parameters");
 // Optional trace (compiled in only with -DPGQ_TRACE): per block and phase (or, for a
 // grouped bank, per tile of the block), %globaltimer at role milestones.
 #ifdef PGQ_TRACE
-constexpr int PT_EV = 12;
+constexpr int PT_EV = 20;
 __device__ unsigned long long g_pt[1024 * PS_MAXPH * PT_EV];
 #define PTRACE(p, ev) (g_pt[((size_t)blockIdx.x * PS_MAXPH + min((p), PS_MAXPH - 1)) * PT_EV + (ev)] = tc::globaltimer())
+#define PTADD(p, ev, v) (g_pt[((size_t)blockIdx.x * PS_MAXPH + min((p), PS_MAXPH - 1)) * PT_EV + (ev)] += (v))
+#define PTSET(p, ev, v) (g_pt[((size_t)blockIdx.x * PS_MAXPH + min((p), PS_MAXPH - 1)) * PT_EV + (ev)] = (v))
 #else
 #define PTRACE(p, ev) ((void)0)
+#define PTADD(p, ev, v) ((void)0)
+#define PTSET(p, ev, v) ((void)0)
 #endif
 
 // ------------------------------------------------------------------ schedule
@@ -617,9 +621,22 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
         }
         const bool first = (k == 0) || (it == beg);
         const bool last = (k == F.ks - 1) || (it == end - 1);
+#ifdef PGQ_TRACE
+        if (!MOE && it == beg && lane == 0) { PTSET(p, 15, 0ull); PTSET(p, 16, 0ull); }
+        const uint64_t tw0 = tc::globaltimer();
+#endif
         if (first && !__all_sync(FULL, W.wait(bar(ACCE + t), pht ^ 1))) { stop = true; break; }
         if (!__all_sync(FULL, W.wait(bar(AFULL + a), pha))) { stop = true; break; }
+#ifdef PGQ_TRACE
+        const uint64_t tw1 = tc::globaltimer();
+#endif
         if (!__all_sync(FULL, W.wait(bar(FULL_X + sx), phx))) { stop = true; break; }
+#ifdef PGQ_TRACE
+        if (!MOE && lane == 0 && it > beg) {
+          PTADD(p, 15, tw1 - tw0);
+          PTADD(p, 16, tc::globaltimer() - tw1);
+        }
+#endif
         tc::fence_after_sync();
         const uint32_t d = tmem + t * PS_ACC_COLS;
         const uint64_t b0 = tc::sdesc_sw128(tc::smem_addr(xring + sx * xst_bytes));
@@ -674,8 +691,21 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
           if (++k == ks) { k = 0; ++tile; }
           if (skip) continue;
         }
+#ifdef PGQ_TRACE
+        if (!MOE && warp == 2 && lane == 0 && it == beg) { PTSET(p, 17, 0ull); PTSET(p, 18, 0ull); }
+        const uint64_t td0 = tc::globaltimer();
+#endif
         if (!__all_sync(FULL, W.wait(bar(FULL_W + s), ph))) { stop = true; break; }
+#ifdef PGQ_TRACE
+        const uint64_t td1 = tc::globaltimer();
+#endif
         if (!__all_sync(FULL, W.wait(bar(AEMPTY + a), pha ^ 1))) { stop = true; break; }
+#ifdef PGQ_TRACE
+        if (!MOE && warp == 2 && lane == 0 && it > beg) {
+          PTADD(p, 17, td1 - td0);
+          PTADD(p, 18, tc::globaltimer() - td1);
+        }
+#endif
         const uint8_t* st = wring + s * PS_W_BYTES;
         const uint8_t* crow = st + r * 128;
         uint4 cw[4];
@@ -742,20 +772,21 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
         float ss = 0.f, mx = 0.f;
         if (b < P.B) {
           const int lo = half ? nt / 2 : 0, hi = half ? nt : nt / 2;
-          // 4 loads in flight at a time, added in tile order as before
+          // 8 loads in flight at a time, added in tile order
+          const float2* const sp = P.stats + (size_t)prev * P.maxtiles * 64 + b;
           int tt = lo;
-          for (; tt + 4 <= hi; tt += 4) {
-            float2 v[4];
+          for (; tt + 8 <= hi; tt += 8) {
+            float2 v[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) v[i] = __ldcg(P.stats + ((size_t)prev * P.maxtiles + tt + i) * 64 + b);
+            for (int i = 0; i < 8; ++i) v[i] = __ldcg(sp + (size_t)(tt + i) * 64);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < 8; ++i) {
               ss += v[i].x;
               mx = fmaxf(mx, v[i].y);
             }
           }
           for (; tt < hi; ++tt) {
-            const float2 v = __ldcg(P.stats + ((size_t)prev * P.maxtiles + tt) * 64 + b);
+            const float2 v = __ldcg(sp + (size_t)tt * 64);
             ss += v.x;
             mx = fmaxf(mx, v.y);
           }
@@ -763,6 +794,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
         s_st[half][b] = make_float2(ss, mx);
       }
       epi_bar();
+      if (!MOE && et == 0) PTRACE(p, 14);
       if (et < 64) {
         float inv = 0.f, sc = 0.f, xi = 0.f;
         if (et < P.B)
@@ -871,40 +903,102 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
           nv = s_mcnt[e] * (TC_BM / 4);
           if (et == 0) PTRACE(etile, 6);
         }
-        const bool ok = W.wait(bar(ACCF + t), pht);
-        if (MOE && et == 0) PTRACE(etile, 10);
-        if (!epi_all(ok)) { stop = true; break; }
-        tc::fence_after_sync();
-        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + t * PS_ACC_COLS;
         const int c_first = whole ? cta : cta_of_item(tile * F.ks, G, items_of(p));
         const int c_last = whole ? cta : cta_of_item(tile_end - 1, G, items_of(p));
         const bool contributor = cta != c_first;
+        const bool vec_ok = ((rows & 3) == 0) && ((reinterpret_cast<uintptr_t>(J.y) & 15) == 0) &&
+                            (J.epi != PGQ_EPI_ADD || (reinterpret_cast<uintptr_t>(J.residual) & 15) == 0);
+        // Dense tiles: what is added to the block's own accumulator, in this order — the
+        // partials of blocks c_first+1 .. c_last, then the residual — is fetched by
+        // per-thread copies of the thread's own float4 slots (no other thread touches
+        // them), the first before the accumulator is ready (into the partial buffer, free
+        // between tiles) and, at the block's last segment of the phase (the input ring
+        // idle once the MMAs are done: the next phase's copies wait for every block's
+        // share of its input, this block's included), two at a time.  Blocks only wait
+        // for higher-numbered blocks, and the launch is cooperative (all blocks
+        // resident), so the waits end.
+        const bool res_fold = !MOE && J.epi == PGQ_EPI_ADD && vec_ok;
+        const int npart = contributor ? 0 : c_last - c_first;
+        const int nsrc = contributor ? 0 : npart + (res_fold ? 1 : 0);
+        float4* const ring4 = reinterpret_cast<float4*>(xring);
+        auto issue = [&](int sidx, float4* buf) {
+          if (sidx < npart) {
+            const int cc = c_first + 1 + sidx;
+            const int ft = item_begin(cc, G, items_of(p)) / F.ks;
+            const float4* pc = reinterpret_cast<const float4*>(
+                P.partials + (((size_t)par * G + cc) * P.maxseg + (tile - ft)) * Bp * TC_BM);
+#pragma unroll
+            for (int k = 0; k < PS_OUT_K; ++k) {
+              const int i = et + 128 * k;
+              if (i < nv)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_addr(buf + i)), "l"(pc + i)
+                             : "memory");
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < PS_OUT_K; ++k) {
+              const int i = et + 128 * k;
+              const int rr = row0 + (i & 31) * 4;
+              if (i < nv && rr < rows)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_addr(buf + i)),
+                             "l"(J.residual + (size_t)(i >> 5) * rows + rr)
+                             : "memory");
+            }
+          }
+          asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        if (!MOE && nsrc > 0) {
+          if (npart > 0) {
+            bool okc = true;
+            if (et == 0) {
+              okc = W.count(P.tile_cnt + (size_t)par * P.maxtiles + tile, (unsigned)npart);
+              if (okc) P.tile_cnt[(size_t)par * P.maxtiles + tile] = 0u;
+            }
+            if (!epi_all(okc)) { stop = true; break; }
+          }
+          if (et == 0) PTRACE(p, 10);
+          issue(0, fix4);
+        }
+        const bool ok = W.wait(bar(ACCF + t), pht);
+        if (MOE && et == 0) PTRACE(etile, 10);
+        if (!MOE && et == 0) PTRACE(p, 8);
+        if (!epi_all(ok)) { stop = true; break; }
+        tc::fence_after_sync();
+        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + t * PS_ACC_COLS;
         // accumulator row r, scaled, into this block's partial (a contributor) or the
         // shared transposed tile; layout [position][128 rows] in both
         float* dst = contributor
                          ? P.partials + (((size_t)par * G + cta) * P.maxseg + (tile - first_tile)) * Bp * TC_BM
                          : s_acc;
-        auto drain16 = [&](int c0) {
-          if (c0 < Bp) {
-            uint32_t u[16];
-            tc::tmem_ld_32x32b_x16(ta + c0, u);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) dst[(c0 + i) * TC_BM + r] = __uint_as_float(u[i]) * s_xinv[c0 + i];
-          }
-        };
         if constexpr (MOE) {   // a grouped bank: the loop rolled (see out_rows)
 #pragma unroll 1
-          for (int c0 = 0; c0 < PS_ACC_COLS; c0 += 16) drain16(c0);
-        } else {
+          for (int c0 = 0; c0 < PS_ACC_COLS; c0 += 16) {
+            if (c0 < Bp) {
+              uint32_t u[16];
+              tc::tmem_ld_32x32b_x16_sync(ta + c0, u);
 #pragma unroll
-          for (int c0 = 0; c0 < PS_ACC_COLS; c0 += 16) drain16(c0);
+              for (int i = 0; i < 16; ++i) dst[(c0 + i) * TC_BM + r] = __uint_as_float(u[i]) * s_xinv[c0 + i];
+            }
+          }
+        } else {
+          // the accumulator row in two loads of 32 columns
+#pragma unroll
+          for (int c0 = 0; c0 < PS_ACC_COLS; c0 += 32) {
+            if (c0 < Bp) {
+              uint32_t u[32];
+              tc::tmem_ld_32x32b_x32_sync(ta + c0, u);
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (c0 + i < Bp) dst[(c0 + i) * TC_BM + r] = __uint_as_float(u[i]) * s_xinv[c0 + i];
+            }
+          }
         }
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(bar(ACCE + t));
         if (++t == 2) { t = 0; pht ^= 1; }
         epi_bar();
+        if (!MOE && et == 0) PTRACE(p, 9);
         if (contributor) {
           // the block's stores, then one gpu-scope release and the count on the tile
           if (et == 0) release_add(P.tile_cnt + (size_t)par * P.maxtiles + tile);
@@ -913,14 +1007,32 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
           it = seg_end;
           continue;
         }
-        if (!whole) {
-          // the owner: the other contributors' partials, through the shared buffer (each
-          // thread copies and adds its own float4 slots), added in block order.  At the
-          // block's last segment of the phase the input ring is idle (the phase's MMAs
-          // are done, and the next phase's copies wait for every block's share of its
-          // input, this block's included), so two partials are in flight at a time
-          // there.  Blocks only wait for higher-numbered blocks, and the launch is
-          // cooperative (all blocks resident), so the wait ends.
+        if constexpr (!MOE) {
+          const bool two = seg_end == end;
+          if (two && nsrc > 1) issue(1, ring4);
+          for (int sidx = 0; sidx < nsrc; ++sidx) {
+            float4* const buf = (two && (sidx & 1)) ? ring4 : fix4;
+            if (two && sidx + 1 < nsrc)
+              asm volatile("cp.async.wait_group 1;" ::: "memory");
+            else
+              asm volatile("cp.async.wait_group 0;" ::: "memory");
+            const bool part = sidx < npart;
+#pragma unroll
+            for (int k = 0; k < PS_OUT_K; ++k) {
+              const int i = et + 128 * k;
+              if (i < nv && (part || row0 + (i & 31) * 4 < rows)) {
+                const float4 u = buf[i];
+                float4 s4 = acc4[i];
+                s4.x += u.x; s4.y += u.y; s4.z += u.z; s4.w += u.w;
+                acc4[i] = s4;
+              }
+            }
+            const int nx = sidx + (two ? 2 : 1);
+            if (nx < nsrc) issue(nx, buf);
+          }
+        } else if (!whole) {
+          // the owner of a grouped bank's tile: the partials two at a time at the
+          // block's last segment, else one at a time (as above, no residual)
           bool okc = true;
           if (et == 0) {
             okc = W.count(P.tile_cnt + (size_t)par * P.maxtiles + tile, (unsigned)(c_last - c_first));
@@ -928,7 +1040,6 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
           }
           if (!epi_all(okc)) { stop = true; break; }
           const int nbuf = (seg_end == end) ? 2 : 1;
-          float4* const ring4 = reinterpret_cast<float4*>(xring);
           for (int c0 = c_first + 1; c0 <= c_last; c0 += nbuf) {
             for (int q2 = 0; q2 < nbuf && c0 + q2 <= c_last; ++q2) {
               const int cc = c0 + q2;
@@ -946,7 +1057,8 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
             }
             asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
             for (int q2 = 0; q2 < nbuf && c0 + q2 <= c_last; ++q2) {
-              auto add1 = [&](int k) {
+#pragma unroll 1
+              for (int k = 0; k < PS_OUT_K; ++k) {
                 const int i = et + 128 * k;
                 if (i < nv) {
                   const float4 u = (q2 ? ring4 : fix4)[i];
@@ -954,25 +1066,20 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
                   s4.x += u.x; s4.y += u.y; s4.z += u.z; s4.w += u.w;
                   acc4[i] = s4;
                 }
-              };
-              if constexpr (MOE) {   // a grouped bank: the loop rolled (see out_rows)
-#pragma unroll 1
-                for (int k = 0; k < PS_OUT_K; ++k) add1(k);
-              } else {
-#pragma unroll
-                for (int k = 0; k < PS_OUT_K; ++k) add1(k);
               }
             }
           }
         }
-        const bool vec_ok = ((rows & 3) == 0) && ((reinterpret_cast<uintptr_t>(J.y) & 15) == 0) &&
-                            (J.epi != PGQ_EPI_ADD || (reinterpret_cast<uintptr_t>(J.residual) & 15) == 0);
+        if (!MOE && et == 0) PTRACE(p, 11);
         const bool stats = vec_ok && j == F.stats_job;
-        out_rows<MOE>(acc4, nv, et, J.epi, J.y, J.residual, rows, row0, vec_ok, stats, MOE ? s_ent : nullptr);
+        out_rows<MOE>(acc4, nv, et, res_fold ? PGQ_EPI_NONE : J.epi, J.y, J.residual, rows, row0, vec_ok, stats,
+                      MOE ? s_ent : nullptr);
+        if (!MOE && et == 0) PTRACE(p, 12);
         if (stats)
           tile_stats(acc4, nv, et, rows, row0, F.next_gamma,
                      P.stats + ((size_t)par * P.maxtiles + (tile - J.tile0)) * 64);
         epi_bar();   // the tile's stores are issued and the shared tile is free
+        if (!MOE && et == 0) PTRACE(p, 13);
         if (et == 0) release_add(P.done + p);
         if (!MOE && et == 0) PTRACE(p, 7);
         if (MOE && et == 0) PTRACE(etile, 7);
@@ -980,6 +1087,8 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
         it = seg_end;
       }
     }
+    // (after a give-up: no copy of this thread still lands in shared memory)
+    asm volatile("cp.async.wait_all;" ::: "memory");
   }
 
   tc::fence_before_sync();
