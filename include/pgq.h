@@ -188,7 +188,7 @@ int pgq_gemv_f16_argmax(const uint16_t* W, int rows, int cols, const float* x, i
                         const float* gamma, float eps, float* logits, int32_t* ids,
                         void* workspace, size_t workspace_bytes, void* stream);
 
-/* Allocation-free form of pgq_gemv_f16_argmax.  The paper has no counterpart to
+/* Allocation-free form of pgq_gemv_f16_argmax.  The pages have no counterpart to
  * this entry point; it exists for callers that cannot allocate device memory when
  * they need the vocab head: plugins living inside a host framework that owns every
  * byte of device memory through its own pools, and latency-bound decode loops that

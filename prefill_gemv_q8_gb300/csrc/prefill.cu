@@ -622,7 +622,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
         const bool first = (k == 0) || (it == beg);
         const bool last = (k == F.ks - 1) || (it == end - 1);
 #ifdef PGQ_TRACE
-        if (!MOE && it == beg && lane == 0) { PTSET(p, 15, 0ull); PTSET(p, 16, 0ull); }
+        if (it == beg && lane == 0) { PTSET(p, 15, 0ull); PTSET(p, 16, 0ull); }
         const uint64_t tw0 = tc::globaltimer();
 #endif
         if (first && !__all_sync(FULL, W.wait(bar(ACCE + t), pht ^ 1))) { stop = true; break; }
@@ -632,7 +632,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
 #endif
         if (!__all_sync(FULL, W.wait(bar(FULL_X + sx), phx))) { stop = true; break; }
 #ifdef PGQ_TRACE
-        if (!MOE && lane == 0 && it > beg) {
+        if (lane == 0 && it > beg) {
           PTADD(p, 15, tw1 - tw0);
           PTADD(p, 16, tc::globaltimer() - tw1);
         }
@@ -692,7 +692,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
           if (skip) continue;
         }
 #ifdef PGQ_TRACE
-        if (!MOE && warp == 2 && lane == 0 && it == beg) { PTSET(p, 17, 0ull); PTSET(p, 18, 0ull); }
+        if (warp == 2 && lane == 0 && it == beg) { PTSET(p, 17, 0ull); PTSET(p, 18, 0ull); }
         const uint64_t td0 = tc::globaltimer();
 #endif
         if (!__all_sync(FULL, W.wait(bar(FULL_W + s), ph))) { stop = true; break; }
@@ -701,7 +701,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
 #endif
         if (!__all_sync(FULL, W.wait(bar(AEMPTY + a), pha ^ 1))) { stop = true; break; }
 #ifdef PGQ_TRACE
-        if (!MOE && warp == 2 && lane == 0 && it > beg) {
+        if (warp == 2 && lane == 0 && it > beg) {
           PTADD(p, 17, td1 - td0);
           PTADD(p, 18, tc::globaltimer() - td1);
         }
