@@ -281,26 +281,58 @@ class PrefillPass:
         self.pgq.prefill_pass(self.PL, self.h, self.g1, self.g2, 1e-6, workspace=self.ws)
 
 
+class PrefillPassQ82F(PrefillPass):
+    """The same pass with the layers in the q8_2f format (int8 body, binary16 row
+    scale, binary16 column field)."""
+    name = "q8_2f prefill pass B=64, 32 layers (hidden 4096, kv 1024, inter 14336)"
+
+    def __init__(self, torch, pgq, synth, layers=None):
+        c = synth.PREFILL
+        self.t, self.pgq = torch, pgq
+        self.B, self.H, self.KV, self.I = c["B"], c["hidden"], c["kv"], c["inter"]
+        self.L = layers or c["layers"]
+        wl = c["workload"]
+        self.layers = [synth.q82f_layer(wl, l, self.H, self.KV, self.I, "torch", "cuda") for l in range(self.L)]
+        self.PL = pgq.Q82PassLayers(self.layers)
+        self.h0 = synth.normal((self.B, self.H), 1.0, wl, synth.T_X, "torch", "cuda")
+        self.h = self.h0.clone()
+        self.g1 = synth.uniform((self.L, self.H), 0.5, 1.5, wl, synth.T_GAMMA, "torch", "cuda")
+        self.g2 = synth.uniform((self.L, self.H), 0.5, 1.5, wl, synth.T_GAMMA2, "torch", "cuda")
+        self.ws = pgq.prefill_pass_workspace(self.H, self.KV, self.I, self.B)
+        shapes = synth.q8_layer_shapes(self.H, self.KV, self.I).values()
+        self.step_bytes = sum(r * c_ + 2 * r + 2 * c_ for r, c_ in shapes) * self.L
+        self.persistent_launches = (self.L + pgq.PASS_LMAX - 1) // pgq.PASS_LMAX
+
+    def step(self):
+        self.h.copy_(self.h0)
+        self.pgq.q82f_prefill_pass(self.PL, self.h, self.g1, self.g2, 1e-6, workspace=self.ws)
+
+
+def time_prefill_q82f(torch, P, steps, warmup, pk):
+    ms = time_graph(torch, P.step, steps, warmup)
+    gbs = P.step_bytes / (ms * 1e-3) / 1e9
+    return {"workload": P.name, "metric": "positions/s", "value": round(P.B / (ms * 1e-3), 1),
+            "ms_per_pass": round(ms, 4), "weight_GBps": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm"], 4),
+            "weight_bytes_per_pass": P.step_bytes, "launches_per_pass": 2 * P.persistent_launches,
+            "timed": "CUDA-graph replay of the pass call"}
+
+
 def time_prefill(torch, P, steps, warmup, pk):
     st = torch.cuda.current_stream()
     ms_api = time_loop(torch, P.step, steps, warmup)
     ms = time_graph(torch, P.step, steps, warmup)
-    # dominant kernel alone: the up projection (14336 x 4096, relu²), rotating layers
+    # dominant kernel alone: the up projection (14336 x 4096, relu²) of each of the
+    # layers in turn, one CUDA graph of back-to-back calls (host launch cost removed)
     up_bytes = P.I * P.H + P.I * (P.H // 32) * 4
     X = P.h0
     U = torch.empty(P.B, P.I, device="cuda")
     gws = P.pgq.prefill_workspace([P.I], P.H, P.B)
     jobs = [[dict(codes=L["up"][0], params=L["up"][1], y=U, epilogue="relu2")] for L in P.layers]
-    for i in range(warmup):
-        P.pgq.prefill_q8(jobs[i % len(jobs)], X, workspace=gws)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    torch.cuda.synchronize()
-    for i in range(steps):
-        ev[i][0].record(st)
-        P.pgq.prefill_q8(jobs[i % len(jobs)], X, workspace=gws)
-        ev[i][1].record(st)
-    torch.cuda.synchronize()
-    k_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+
+    def ups():
+        for j in jobs:
+            P.pgq.prefill_q8(j, X, workspace=gws)
+    k_ms = time_graph(torch, ups, max(2, steps // 4), max(1, warmup // 2)) / len(jobs)
     gbs = P.step_bytes / (ms * 1e-3) / 1e9
     ach = up_bytes / (k_ms * 1e-3) / 1e9
     tf = P.flops / (ms * 1e-3) / 1e12
@@ -324,7 +356,8 @@ def time_prefill(torch, P, steps, warmup, pk):
                               "included)"},
         "up_alone": {"kernel": "pgq_prefill_pass_kernel, one phase (up 14336x4096, relu²) + input kernel",
                      "GBps": round(ach, 1), "frac": round(ach / pk["hbm"], 4), "bytes": up_bytes,
-                     "avg_launch_ms": round(k_ms, 5), "timed": "separate event loop over 32 up matrices, direct calls"},
+                     "avg_launch_ms": round(k_ms, 5),
+                     "timed": "CUDA graph of one call per layer's up matrix, back to back; per call"},
     }
 
 
@@ -646,7 +679,7 @@ def main():
     ap.add_argument("--impl", default="pgq", choices=["pgq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-prefill", action="store_true", help="only the headline decode layer")
-    ap.add_argument("--only", choices=["decode", "prefill", "moe", "vocab", "q82f"], default=None,
+    ap.add_argument("--only", choices=["decode", "prefill", "moe", "vocab", "q82f", "q82f_prefill"], default=None,
                     help="profiling aid: run one workload and print its JSON object")
     ap.add_argument("--no-graph", action="store_true", help="profiling aid (--only moe): direct calls only")
     ap.add_argument("--prefill-layers", type=int, default=None, help="layers of the prefill pass (default 32)")
@@ -685,6 +718,10 @@ def main():
     if args.only == "prefill":
         P = PrefillPass(torch, pgq, synth, layers=args.prefill_layers)
         print(json.dumps(time_prefill(torch, P, args.steps, args.warmup, pk)), flush=True)
+        return
+    if args.only == "q82f_prefill":
+        P = PrefillPassQ82F(torch, pgq, synth, layers=args.prefill_layers)
+        print(json.dumps(time_prefill_q82f(torch, P, args.steps, args.warmup, pk)), flush=True)
         return
     if args.only == "moe":
         print(json.dumps(bench_moe(torch, pgq, synth, args.steps, args.warmup, pk, graph=not args.no_graph)),
@@ -749,6 +786,11 @@ def main():
         line["workloads"]["tiny_mlp"] = bench_tiny_mlp(torch, pgq, synth, args.steps, args.warmup, pk)
         torch.cuda.empty_cache()
         line["workloads"]["q8_2f_decode_layer"] = bench_q82f_layer(torch, pgq, synth, args.steps, args.warmup, pk)
+        torch.cuda.empty_cache()
+        P = PrefillPassQ82F(torch, pgq, synth, layers=args.prefill_layers)
+        line["workloads"]["q8_2f_prefill_pass"] = time_prefill_q82f(torch, P, max(3, args.steps // 5), args.warmup,
+                                                                    pk)
+        del P
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_q8()
     if rank == 0:

@@ -358,6 +358,25 @@ size_t pgq_prefill_q8_workspace_bytes(const int* rows, int njobs, int cols, int 
 int pgq_prefill_q8(const pgq_q8_job* jobs, int njobs, const float* X, int cols, int B,
                    void* workspace, size_t workspace_bytes, void* stream);
 
+/* pgq_prefill_q8 with q8_2f matrices (w[r][c] = row_scale[r]·codes[r][c]·col_field[c],
+ * the format of pgq_gemv_q82f; gemma_batch.rs `q8_2f_mm_r2`).  On the tensor cores the
+ * column field goes into the dequantised operand (codes·col_field rounded once to
+ * binary16, so |col_field| < 511 keeps it finite) and the row scale multiplies each
+ * finished f32 sum before the epilogue; the error bound of pgq_prefill_q8 holds.
+ * codes, row_scale, col_field: 16-byte aligned.  Workspace: pgq_prefill_q8_workspace_bytes
+ * with the same rows, cols and B; other arguments and limits as pgq_prefill_q8. */
+typedef struct {
+  const int8_t* codes;         /* device int8 [rows][cols] */
+  const uint16_t* row_scale;   /* device binary16 [rows] */
+  const uint16_t* col_field;   /* device binary16 [cols] */
+  int rows;
+  float* y;                    /* device f32 [B][rows] */
+  int epilogue;                /* PGQ_EPI_* */
+  const float* residual;       /* device f32 [B][rows] for PGQ_EPI_ADD */
+} pgq_q82f_job;
+int pgq_prefill_q82f(const pgq_q82f_job* jobs, int njobs, const float* X, int cols, int B,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
 /* Status word of the last prefill call that used `workspace` (PGQ_OK or
  * PGQ_ETIMEOUT when a bounded device-side wait expired).  Synchronises the stream.
  * (pgq_last_device_status(workspace, stream) also reports the decode kernels.) */
@@ -386,6 +405,13 @@ int pgq_q8_prefill_pass_layout(int hidden, int kv, int inter, int B, size_t offs
 int pgq_q8_prefill_pass(const pgq_q8_layer* layers, int L, float* h, int B, const float* gamma1,
                         const float* gamma2, float eps, void* workspace, size_t workspace_bytes,
                         void* stream);
+/* The same pass with q8_2f layers (the arithmetic of pgq_prefill_q82f for every
+ * projection); the workspace size and layout are the q8 pass's
+ * (pgq_q8_prefill_pass_workspace_bytes, pgq_q8_prefill_pass_layout).  Every matrix's
+ * codes, row_scale and col_field 16-byte aligned. */
+int pgq_q82f_prefill_pass(const pgq_q82f_layer* layers, int L, float* h, int B, const float* gamma1,
+                          const float* gamma2, float eps, void* workspace, size_t workspace_bytes,
+                          void* stream);
 
 /* ---------------------------------------------------------------- a6: MoE
  * Router projection over a pass (nemotron_prefill.rs `pb_f32_mm`):

@@ -51,6 +51,11 @@ class Q82Matrix(C.Structure):
     _fields_ = [("codes", _vp), ("row_scale", _vp), ("col_field", _vp)]
 
 
+class Q82Job(C.Structure):
+    _fields_ = [("codes", _vp), ("row_scale", _vp), ("col_field", _vp), ("rows", C.c_int), ("y", _vp),
+                ("epilogue", C.c_int), ("residual", _vp)]
+
+
 class Q82Layer(C.Structure):
     _fields_ = [("q", Q82Matrix), ("k", Q82Matrix), ("v", Q82Matrix), ("o", Q82Matrix),
                 ("up", Q82Matrix), ("down", Q82Matrix),
@@ -97,6 +102,7 @@ _SIGS = {
                                          _vp, C.c_int, _vp]),
     "pgq_prefill_q8_workspace_bytes": (C.c_size_t, [C.POINTER(C.c_int), C.c_int, C.c_int, C.c_int]),
     "pgq_prefill_q8": (C.c_int, [C.POINTER(Q8Job), C.c_int, _vp, C.c_int, C.c_int, _vp, C.c_size_t, _vp]),
+    "pgq_prefill_q82f": (C.c_int, [C.POINTER(Q82Job), C.c_int, _vp, C.c_int, C.c_int, _vp, C.c_size_t, _vp]),
     "pgq_prefill_status": (C.c_int, [_vp, _vp]),
     "pgq_last_device_status": (C.c_int, [_vp, _vp]),
     "pgq_set_wait_limit_ns": (C.c_int, [C.c_ulonglong]),
@@ -118,6 +124,8 @@ _SIGS = {
     "pgq_q8_prefill_pass_layout": (C.c_int, [C.c_int, C.c_int, C.c_int, C.c_int, C.POINTER(C.c_size_t)]),
     "pgq_q8_prefill_pass": (C.c_int, [C.POINTER(Q8Layer), C.c_int, _vp, C.c_int, _vp, _vp, C.c_float, _vp,
                                       C.c_size_t, _vp]),
+    "pgq_q82f_prefill_pass": (C.c_int, [C.POINTER(Q82Layer), C.c_int, _vp, C.c_int, _vp, _vp, C.c_float, _vp,
+                                        C.c_size_t, _vp]),
 }
 
 _lib = None
@@ -374,6 +382,29 @@ def prefill_q8(jobs, X, workspace=None, stream=None):
     return workspace
 
 
+def prefill_q82f(jobs, X, workspace=None, stream=None):
+    """prefill_q8 with q8_2f matrices: each job {codes, row_scale, col_field, y,
+    epilogue, residual}."""
+    _need(X, torch.float32, "X")
+    B, cols = X.shape
+    J = (Q82Job * len(jobs))()
+    for i, j in enumerate(jobs):
+        rows, c = _q82f_check(j["codes"], j["row_scale"], j["col_field"], "job")
+        if c != cols:
+            raise ValueError("all jobs of one launch must share cols")
+        _need(j["y"], torch.float32, "y", (B, rows))
+        res = j.get("residual")
+        if res is not None:
+            _need(res, torch.float32, "residual", (B, rows))
+        J[i] = Q82Job(j["codes"].data_ptr(), j["row_scale"].data_ptr(), j["col_field"].data_ptr(), rows,
+                      j["y"].data_ptr(), _epi(j.get("epilogue", "none")), res.data_ptr() if res is not None else None)
+    if workspace is None:
+        workspace = prefill_workspace([j["codes"].shape[0] for j in jobs], cols, B, X.device)
+    _check(lib().pgq_prefill_q82f(J, len(jobs), _ptr(X), cols, B, _ptr(workspace), workspace.numel(),
+                                  _stream(stream)))
+    return workspace
+
+
 def prefill_status(workspace, stream=None):
     return int(lib().pgq_prefill_status(_ptr(workspace), _stream(stream)))
 
@@ -421,6 +452,7 @@ def _q82f_check(codes, rs, cf, name="W"):
     rows, cols = codes.shape
     _need(rs, torch.float16, name + ".row_scale", (rows,))
     _need(cf, torch.float16, name + ".col_field", (cols,))
+    return rows, cols
 
 
 def gemv_q82f(codes, row_scale, col_field, x, gamma=None, eps=1e-6, epilogue="none", residual=None, y=None,
@@ -560,6 +592,32 @@ class PassLayers:
         self.layers = layers
         self.arr = (Q8Layer * len(layers))(*[q8_layer_struct(m) for m in layers])
         self.hidden, self.kv, self.inter = self.arr[0].hidden, self.arr[0].kv, self.arr[0].inter
+
+
+class Q82PassLayers:
+    """ctypes array of L q8_2f layer descriptors (keeps the tensors alive)."""
+
+    def __init__(self, layers):
+        self.layers = layers
+        self.arr = (Q82Layer * len(layers))(*[q82f_layer_struct(m) for m in layers])
+        self.hidden, self.kv, self.inter = self.arr[0].hidden, self.arr[0].kv, self.arr[0].inter
+
+
+def q82f_prefill_pass(layers, h, gamma1, gamma2, eps=1e-6, workspace=None, stream=None):
+    """prefill_pass with q8_2f layers ({slot: (codes, row_scale, col_field)}, or a
+    Q82PassLayers); the workspace is the q8 pass's."""
+    if not isinstance(layers, Q82PassLayers):
+        layers = Q82PassLayers(layers)
+    _need(h, torch.float32, "h")
+    B, H = h.shape
+    L = len(layers.layers)
+    _need(gamma1, torch.float32, "gamma1", (L, H))
+    _need(gamma2, torch.float32, "gamma2", (L, H))
+    if workspace is None:
+        workspace = prefill_pass_workspace(layers.hidden, layers.kv, layers.inter, B, h.device)
+    _check(lib().pgq_q82f_prefill_pass(layers.arr, L, _ptr(h), B, _ptr(gamma1), _ptr(gamma2), eps,
+                                       _ptr(workspace), workspace.numel(), _stream(stream)))
+    return workspace
 
 
 def prefill_pass(layers, h, gamma1, gamma2, eps=1e-6, workspace=None, stream=None):

@@ -608,6 +608,49 @@ int pgq_prefill_q8(const pgq_q8_job* jobs, int njobs, const float* X, int cols, 
   return launch_prefill(pj, njobs, X, cols, B, workspace, workspace_bytes, 0, dev, as_stream(stream));
 }
 
+int pgq_prefill_q82f(const pgq_q82f_job* jobs, int njobs, const float* X, int cols, int B, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  REQUIRE(jobs && X, PGQ_EINVAL, "prefill_q82f: jobs and X must be non-null");
+  REQUIRE(njobs >= 1 && njobs <= TC_MAXJOBS, PGQ_EINVAL, "prefill_q82f: njobs=%d outside 1..%d", njobs, TC_MAXJOBS);
+  REQUIRE(B >= 1 && B <= PGQ_PASS_BMAX, PGQ_EINVAL, "prefill_q82f: B=%d outside 1..%d", B, PGQ_PASS_BMAX);
+  REQUIRE(cols >= 128 && cols % 128 == 0, PGQ_EUNSUPPORTED, "prefill_q82f: cols=%d must be a multiple of 128", cols);
+  REQUIRE(aligned16(X), PGQ_EALIGN, "prefill_q82f: X must be 16-byte aligned");
+  REQUIRE(workspace && ((uintptr_t)workspace & 255) == 0, PGQ_EWORKSPACE,
+          "prefill_q82f: workspace must be non-null and 256-byte aligned");
+  PrefillJob pj[TC_MAXJOBS];
+  int rows[TC_MAXJOBS];
+  for (int j = 0; j < njobs; ++j) {
+    const pgq_q82f_job& J = jobs[j];
+    REQUIRE(J.codes && J.row_scale && J.col_field && J.y, PGQ_EINVAL,
+            "prefill_q82f: job %d has a null codes/row_scale/col_field/y", j);
+    REQUIRE(J.rows >= 1, PGQ_EINVAL, "prefill_q82f: job %d rows=%d", j, J.rows);
+    REQUIRE(aligned16(J.codes) && aligned16(J.row_scale) && aligned16(J.col_field), PGQ_EALIGN,
+            "prefill_q82f: job %d codes/row_scale/col_field 16-byte", j);
+    REQUIRE(aligned4(J.y) && (!J.residual || aligned4(J.residual)), PGQ_EALIGN, "prefill_q82f: job %d y/residual", j);
+    REQUIRE(J.epilogue >= PGQ_EPI_NONE && J.epilogue <= PGQ_EPI_ADD, PGQ_EINVAL, "prefill_q82f: bad epilogue");
+    REQUIRE(J.epilogue != PGQ_EPI_ADD || J.residual, PGQ_EINVAL, "prefill_q82f: PGQ_EPI_ADD needs a residual");
+    const size_t yb = (size_t)B * J.rows * 4;
+    REQUIRE(!overlaps(J.y, yb, X, (size_t)B * cols * 4), PGQ_EINVAL, "prefill_q82f: job %d output overlaps X", j);
+    REQUIRE(!J.residual || J.residual == J.y || !overlaps(J.y, yb, J.residual, yb), PGQ_EINVAL,
+            "prefill_q82f: residual must be y itself or not overlap it");
+    REQUIRE(!overlaps(J.y, yb, workspace, workspace_bytes), PGQ_EINVAL, "prefill_q82f: output overlaps workspace");
+    PrefillJob w{};
+    w.codes = J.codes;
+    w.rs = J.row_scale;
+    w.cf = J.col_field;
+    w.rows = J.rows;
+    w.y = J.y;
+    w.residual = J.residual;
+    w.epilogue = J.epilogue;
+    pj[j] = w;
+    rows[j] = J.rows;
+  }
+  GET_DEVICE(dev);
+  const size_t need = prefill_workspace_bytes(rows, njobs, cols, B, dev);
+  REQUIRE(workspace_bytes >= need, PGQ_EWORKSPACE, "prefill_q82f: workspace needs %zu bytes", need);
+  return launch_prefill(pj, njobs, X, cols, B, workspace, workspace_bytes, 0, dev, as_stream(stream));
+}
+
 // ------------------------------------------------------------------ prefill pass
 namespace {
 struct PassLayout {
@@ -649,23 +692,26 @@ int pgq_q8_prefill_pass_layout(int hidden, int kv, int inter, int B, size_t offs
   return PGQ_OK;
 }
 
-int pgq_q8_prefill_pass(const pgq_q8_layer* layers, int L, float* h, int B, const float* gamma1,
-                        const float* gamma2, float eps, void* workspace, size_t workspace_bytes, void* stream) {
-  REQUIRE(layers && h && gamma1 && gamma2 && workspace, PGQ_EINVAL, "prefill_pass: null pointer");
-  REQUIRE(L >= 1, PGQ_EINVAL, "prefill_pass: L=%d", L);
-  REQUIRE(B >= 1 && B <= PGQ_PASS_BMAX, PGQ_EINVAL, "prefill_pass: B=%d outside 1..%d", B, PGQ_PASS_BMAX);
+extern "C++" {
+namespace {
+template <class Layer>
+int prefill_pass_impl(const char* name, const Layer* layers, int L, float* h, int B, const float* gamma1,
+                      const float* gamma2, float eps, void* workspace, size_t workspace_bytes, void* stream) {
+  REQUIRE(layers && h && gamma1 && gamma2 && workspace, PGQ_EINVAL, "%s: null pointer", name);
+  REQUIRE(L >= 1, PGQ_EINVAL, "%s: L=%d", name, L);
+  REQUIRE(B >= 1 && B <= PGQ_PASS_BMAX, PGQ_EINVAL, "%s: B=%d outside 1..%d", name, B, PGQ_PASS_BMAX);
   REQUIRE(aligned16(h) && aligned16(gamma1) && aligned16(gamma2), PGQ_EALIGN,
-          "prefill_pass: h, gamma1 and gamma2 must be 16-byte aligned");
+          "%s: h, gamma1 and gamma2 must be 16-byte aligned", name);
   const int H = layers[0].hidden, KV = layers[0].kv, I = layers[0].inter;
   for (int l = 0; l < L; ++l)
     REQUIRE(layers[l].hidden == H && layers[l].kv == KV && layers[l].inter == I, PGQ_EINVAL,
-            "prefill_pass: layer %d has a different shape", l);
-  REQUIRE(H % 128 == 0 && I % 128 == 0, PGQ_EUNSUPPORTED, "prefill_pass: hidden and inter must be multiples of 128");
-  REQUIRE(((uintptr_t)workspace & 255) == 0, PGQ_EWORKSPACE, "prefill_pass: workspace must be 256-byte aligned");
+            "%s: layer %d has a different shape", name, l);
+  REQUIRE(H % 128 == 0 && I % 128 == 0, PGQ_EUNSUPPORTED, "%s: hidden and inter must be multiples of 128", name);
+  REQUIRE(((uintptr_t)workspace & 255) == 0, PGQ_EWORKSPACE, "%s: workspace must be 256-byte aligned", name);
   GET_DEVICE(dev);
   const PassLayout PL = pass_layout(H, KV, I, B, dev);
-  REQUIRE(workspace_bytes >= PL.total, PGQ_EWORKSPACE, "prefill_pass: workspace needs %zu bytes", PL.total);
-  REQUIRE(!overlaps(h, (size_t)B * H * 4, workspace, workspace_bytes), PGQ_EINVAL, "prefill_pass: h overlaps workspace");
+  REQUIRE(workspace_bytes >= PL.total, PGQ_EWORKSPACE, "%s: workspace needs %zu bytes", name, PL.total);
+  REQUIRE(!overlaps(h, (size_t)B * H * 4, workspace, workspace_bytes), PGQ_EINVAL, "%s: h overlaps workspace", name);
   char* w = static_cast<char*>(workspace);
   float* n1 = reinterpret_cast<float*>(w + PL.off[0]);
   float* q = reinterpret_cast<float*>(w + PL.off[1]);
@@ -677,6 +723,31 @@ int pgq_q8_prefill_pass(const pgq_q8_layer* layers, int L, float* h, int B, cons
   const PassTaps taps{n1, q, k, v, h1, n2, u};
   return launch_prefill_pass(layers, L, h, B, gamma1, gamma2, eps, taps, w + PL.gemm, PL.off[0] - PL.gemm, dev,
                              as_stream(stream));
+}
+}  // namespace
+}  // extern "C++"
+
+int pgq_q8_prefill_pass(const pgq_q8_layer* layers, int L, float* h, int B, const float* gamma1,
+                        const float* gamma2, float eps, void* workspace, size_t workspace_bytes, void* stream) {
+  return prefill_pass_impl("prefill_pass", layers, L, h, B, gamma1, gamma2, eps, workspace, workspace_bytes, stream);
+}
+
+int pgq_q82f_prefill_pass(const pgq_q82f_layer* layers, int L, float* h, int B, const float* gamma1,
+                          const float* gamma2, float eps, void* workspace, size_t workspace_bytes, void* stream) {
+  if (layers) {
+    for (int l = 0; l < L; ++l) {
+      const pgq_q82f_matrix* m[6] = {&layers[l].q, &layers[l].k, &layers[l].v, &layers[l].o, &layers[l].up,
+                                     &layers[l].down};
+      for (int i = 0; i < 6; ++i) {
+        REQUIRE(m[i]->codes && m[i]->row_scale && m[i]->col_field, PGQ_EINVAL,
+                "q82f_prefill_pass: layer %d matrix %d has a null pointer", l, i);
+        REQUIRE(aligned16(m[i]->codes) && aligned16(m[i]->row_scale) && aligned16(m[i]->col_field), PGQ_EALIGN,
+                "q82f_prefill_pass: layer %d matrix %d: codes, row_scale and col_field 16-byte aligned", l, i);
+      }
+    }
+  }
+  return prefill_pass_impl("q82f_prefill_pass", layers, L, h, B, gamma1, gamma2, eps, workspace, workspace_bytes,
+                           stream);
 }
 
 // ------------------------------------------------------------------ MoE

@@ -88,11 +88,13 @@ int gemv_grid(int B, bool q8, bool argmax, const DeviceInfo& dev);
 constexpr int TC_MAXJOBS = 4;
 struct PrefillJob {
   const int8_t* codes;
-  const uint16_t* params;
+  const uint16_t* params;   // block format: (scale, offset) pairs; null for q8_2f
   int rows;
   float* y;
   const float* residual;
   int epilogue;
+  const uint16_t* rs = nullptr;   // q8_2f: binary16 row scales [rows] (null: block format)
+  const uint16_t* cf = nullptr;   // q8_2f: binary16 column field [cols]
 };
 size_t prefill_workspace_bytes(const int* rows, int njobs, int cols, int B, const DeviceInfo& dev);
 int prefill_status_offset();
@@ -108,6 +110,9 @@ size_t prefill_pass_gemm_bytes(int H, int KV, int I, int B, const DeviceInfo& de
 // The pass over L layers: per 8 layers one input kernel and one persistent launch of
 // 4 phases per layer (q,k,v; o; up; down), inputs made inside the launch.
 int launch_prefill_pass(const pgq_q8_layer* layers, int L, float* h, int B, const float* gamma1,
+                        const float* gamma2, float eps, const PassTaps& taps, void* ws, size_t ws_bytes,
+                        const DeviceInfo& dev, cudaStream_t st);
+int launch_prefill_pass(const pgq_q82f_layer* layers, int L, float* h, int B, const float* gamma1,
                         const float* gamma2, float eps, const PassTaps& taps, void* ws, size_t ws_bytes,
                         const DeviceInfo& dev, cudaStream_t st);
 

@@ -56,6 +56,7 @@ constexpr int PS_XST = 3;          // input ring stages (4 measured no faster)
 constexpr int PS_CODES_BYTES = TC_BM * TC_BK;                 // 16 KB
 constexpr int PS_PARAMS_BYTES = TC_BM * 16;                   // 4 (scale, offset) pairs per row
 constexpr int PS_W_BYTES = PS_CODES_BYTES + PS_PARAMS_BYTES;  // 18 KB, a multiple of 1 KB
+constexpr int PS_CF_BYTES = TC_BK * 2;                        // q8_2f: the step's column field
 constexpr int PS_ACC_COLS = 64;                               // TMEM columns per accumulator (N <= 64)
 constexpr int PS_A_COLS = TC_BK / 2;                          // TMEM columns per A buffer
 constexpr uint32_t PS_TMEM_COLS = 512;                        // 2 accumulators + 4 A buffers (384 used)
@@ -78,6 +79,9 @@ struct PsJob {
   int pstride, prows;
   float* y;                  // [B][rows]
   const float* residual;     // [B][rows] for PGQ_EPI_ADD
+  // q8_2f (w = rs[r]·q[r][c]·cf[c]): binary16 row scales [rows]; pmap then maps the
+  // column field [cols] (box {128, 1}); null: the block format
+  const __half* rs;
   int rows, epi, tile0, ntiles;   // tile0: first tile of the job within its phase
 };
 struct PsPhase {
@@ -105,6 +109,7 @@ struct PsParams {
   unsigned long long wait_limit_ns;
   float eps;
   int nph, B, Bp, G, maxseg, maxtiles, wst;
+  int f2;                    // every matrix of the launch is q8_2f
   // test hook (pgq_debug_stall): the wait for the first phase's tiles asks for one
   // tile more than there are, so it runs out and every block takes its abort path
   int stall;
@@ -278,7 +283,8 @@ __device__ __forceinline__ __half2 s8pair_to_h2(uint32_t u_biased, uint32_t sel)
 }
 
 // Writes a tile from the shared transposed tile acc4 ([b][128 rows] as float4):
-// y[b][row0 + c] = epilogue(acc[b][c]) for c < rows - row0, and (writeback) leaves
+// y[b][row0 + c] = epilogue(rs[row0 + c]·acc[b][c]) (rs: q8_2f row scales, else 1)
+// for c < rows - row0, and (writeback) leaves
 // the final values in acc4.  Thread et takes float4 et, et+128, ... (at most 16); all
 // reads (shared tile, residual) of a pass are issued before its first store.  ROLL
 // keeps the passes a loop (less code to fetch: this runs once per tile, cold in the
@@ -286,8 +292,17 @@ __device__ __forceinline__ __half2 s8pair_to_h2(uint32_t u_biased, uint32_t sel)
 // dense pass).
 template <bool ROLL>
 __device__ __forceinline__ void out_rows(float4* acc4, int nvec, int et, int epi, float* y, const float* res, int rows,
-                                         int row0, bool vec_ok, bool writeback, const int* rowtab = nullptr) {
+                                         int row0, bool vec_ok, bool writeback, const int* rowtab = nullptr,
+                                         const __half* rs = nullptr) {
   if (vec_ok) {
+    // q8_2f: the row scales of this thread's 4 rows (every slot it takes has them)
+    float4 rsv = make_float4(1.f, 1.f, 1.f, 1.f);
+    if (rs && row0 + (et & 31) * 4 < rows) {
+      const uint2 w = *reinterpret_cast<const uint2*>(rs + row0 + (et & 31) * 4);
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
+      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+      rsv = make_float4(a.x, a.y, b.x, b.y);
+    }
     auto pass = [&](int h) {
       float4 a[PS_OUT_H], q[PS_OUT_H];
 #pragma unroll
@@ -306,6 +321,7 @@ __device__ __forceinline__ void out_rows(float4* acc4, int nvec, int et, int epi
         const int rr = row0 + (i & 31) * 4;
         if (i < nvec && rr < rows) {
           float4 o = a[k];
+          if (rs) o = make_float4(o.x * rsv.x, o.y * rsv.y, o.z * rsv.z, o.w * rsv.w);
           if (epi == PGQ_EPI_RELU2) {
             o.x = fmaxf(o.x, 0.f); o.y = fmaxf(o.y, 0.f); o.z = fmaxf(o.z, 0.f); o.w = fmaxf(o.w, 0.f);
             o = make_float4(o.x * o.x, o.y * o.y, o.z * o.z, o.w * o.w);
@@ -335,6 +351,7 @@ __device__ __forceinline__ void out_rows(float4* acc4, int nvec, int et, int epi
       const float av[4] = {a.x, a.y, a.z, a.w};
       for (int e = 0; e < 4 && rr + e < rows; ++e) {
         float o = av[e];
+        if (rs) o *= __half2float(rs[rr + e]);
         if (epi == PGQ_EPI_RELU2) {
           o = fmaxf(o, 0.f);
           o = o * o;
@@ -516,9 +533,12 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
           if (tc::elect_one()) {
             if (MOE && (k == 0 || it == beg)) PTRACE(wtile, 0);
             if (!MOE && it == beg) PTRACE(p, 0);
-            tc::mbar_expect_tx(bar(FULL_W + s), J.praw ? PS_CODES_BYTES : PS_W_BYTES);
+            tc::mbar_expect_tx(bar(FULL_W + s),
+                               J.praw ? PS_CODES_BYTES : PS_CODES_BYTES + (J.rs ? PS_CF_BYTES : PS_PARAMS_BYTES));
             tc::tma_load_2d_hint(tc::smem_addr(st), &J.cmap, k * TC_BK, row0, bar(FULL_W + s), evict_first);
-            if (!J.praw)
+            if (J.rs)   // q8_2f: the step's 128 column-field values (kept in L2: every tile reads them)
+              tc::tma_load_2d(tc::smem_addr(st + PS_CODES_BYTES), &J.pmap, k * TC_BK, 0, bar(FULL_W + s));
+            else if (!J.praw)
               tc::tma_load_2d_hint(tc::smem_addr(st + PS_CODES_BYTES), &J.pmap, k * (TC_BK / 32), row0,
                                    bar(FULL_W + s), evict_first);
           }
@@ -714,21 +734,41 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
           const int cc = hk * 4 + c;
           cw[c] = *reinterpret_cast<const uint4*>(crow + ((cc ^ (r & 7)) << 4));
         }
-        const uint2 pr = *reinterpret_cast<const uint2*>(st + PS_CODES_BYTES + r * 16 + hk * 8);
-        const uint32_t prw[2] = {pr.x, pr.y};
         uint32_t out[32];
+        if (!MOE && P.f2) {
+          // q8_2f: w = q·cf (the exact byte, times the column's field, rounded once);
+          // the step's 128 column-field values follow the codes (this warp's 64)
+          const uint4* cfv = reinterpret_cast<const uint4*>(st + PS_CODES_BYTES + hk * 128);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const __half2 so = *reinterpret_cast<const __half2*>(&prw[c >> 1]);
-          const __half2 s2 = __low2half2(so), o2 = __high2half2(so);
-          const uint32_t wv[4] = {cw[c].x, cw[c].y, cw[c].z, cw[c].w};
+          for (int c = 0; c < 4; ++c) {
+            const uint4 f0 = cfv[2 * c], f1 = cfv[2 * c + 1];   // columns 16c .. 16c+15
+            const uint32_t fw[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+            const uint32_t wv[4] = {cw[c].x, cw[c].y, cw[c].z, cw[c].w};
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t u = wv[i] ^ 0x80808080u;
-            const __half2 lo = __hfma2(s8pair_to_h2(u, 0x4140), s2, o2);
-            const __half2 hi = __hfma2(s8pair_to_h2(u, 0x4342), s2, o2);
-            out[c * 8 + 2 * i] = *reinterpret_cast<const uint32_t*>(&lo);
-            out[c * 8 + 2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t u = wv[i] ^ 0x80808080u;
+              const __half2 lo = __hmul2(s8pair_to_h2(u, 0x4140), *reinterpret_cast<const __half2*>(&fw[2 * i]));
+              const __half2 hi = __hmul2(s8pair_to_h2(u, 0x4342), *reinterpret_cast<const __half2*>(&fw[2 * i + 1]));
+              out[c * 8 + 2 * i] = *reinterpret_cast<const uint32_t*>(&lo);
+              out[c * 8 + 2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+            }
+          }
+        } else {
+          const uint2 pr = *reinterpret_cast<const uint2*>(st + PS_CODES_BYTES + r * 16 + hk * 8);
+          const uint32_t prw[2] = {pr.x, pr.y};
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const __half2 so = *reinterpret_cast<const __half2*>(&prw[c >> 1]);
+            const __half2 s2 = __low2half2(so), o2 = __high2half2(so);
+            const uint32_t wv[4] = {cw[c].x, cw[c].y, cw[c].z, cw[c].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t u = wv[i] ^ 0x80808080u;
+              const __half2 lo = __hfma2(s8pair_to_h2(u, 0x4140), s2, o2);
+              const __half2 hi = __hfma2(s8pair_to_h2(u, 0x4342), s2, o2);
+              out[c * 8 + 2 * i] = *reinterpret_cast<const uint32_t*>(&lo);
+              out[c * 8 + 2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+            }
           }
         }
         const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + 2 * PS_ACC_COLS + a * PS_A_COLS + hk * 32;
@@ -917,7 +957,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
         // share of its input, this block's included), two at a time.  Blocks only wait
         // for higher-numbered blocks, and the launch is cooperative (all blocks
         // resident), so the waits end.
-        const bool res_fold = !MOE && J.epi == PGQ_EPI_ADD && vec_ok;
+        const bool res_fold = !MOE && J.epi == PGQ_EPI_ADD && vec_ok && !J.rs;   // (q8_2f: the row scale first)
         const int npart = contributor ? 0 : c_last - c_first;
         const int nsrc = contributor ? 0 : npart + (res_fold ? 1 : 0);
         float4* const ring4 = reinterpret_cast<float4*>(xring);
@@ -1073,7 +1113,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
         if (!MOE && et == 0) PTRACE(p, 11);
         const bool stats = vec_ok && j == F.stats_job;
         out_rows<MOE>(acc4, nv, et, res_fold ? PGQ_EPI_NONE : J.epi, J.y, J.residual, rows, row0, vec_ok, stats,
-                      MOE ? s_ent : nullptr);
+                      MOE ? s_ent : nullptr, MOE ? nullptr : J.rs);
         if (!MOE && et == 0) PTRACE(p, 12);
         if (stats)
           tile_stats(acc4, nv, et, rows, row0, F.next_gamma,
@@ -1413,11 +1453,19 @@ int launch_phases(const HostPhase* hp, int nph, const float* x0, const float* ga
       PsJob& D = P.job[nj++];
       const uint64_t mrows = (uint64_t)J.rows * (H.moe_E > 0 ? H.moe_E : 1);   // a bank: all experts' rows
       const uint64_t pc = H.pcols > 0 ? (uint64_t)H.pcols : (uint64_t)(H.K / 32);
+      const bool f2 = J.rs != nullptr;
+      if (nj == 1) P.f2 = f2 ? 1 : 0;
+      if ((P.f2 != 0) != f2 || (f2 && (H.moe_E > 0 || H.praw)))
+        return set_error(PGQ_EINVAL, "prefill: q8_2f and block-format matrices in one launch");
       if (!encode_2d(&D.cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, J.codes, H.K, mrows, (uint64_t)H.K, TC_BK, TC_BM,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
-          (!H.praw && !encode_2d(&D.pmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, J.params, pc, mrows, (uint64_t)pc * 4,
-                                 TC_BK / 32, TC_BM, CU_TENSOR_MAP_SWIZZLE_NONE)))
+          (f2 && !encode_2d(&D.pmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, J.cf, H.K, 1, (uint64_t)H.K * 2, TC_BK, 1,
+                            CU_TENSOR_MAP_SWIZZLE_NONE)) ||
+          (!f2 && !H.praw &&
+           !encode_2d(&D.pmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, J.params, pc, mrows, (uint64_t)pc * 4, TC_BK / 32,
+                      TC_BM, CU_TENSOR_MAP_SWIZZLE_NONE)))
         return set_error(PGQ_ECUDA, "prefill: tensor map of phase %d matrix %d could not be encoded", i, j);
+      D.rs = reinterpret_cast<const __half*>(J.rs);
       D.praw = H.praw ? reinterpret_cast<const uint32_t*>(J.params) : nullptr;
       D.pstride = (int)pc;
       D.prows = (int)mrows;
@@ -1516,35 +1564,82 @@ HostPhase single_phase(const PrefillJob* jobs, int njobs, int cols) {
   return h;
 }
 
+// One layer's six matrices in either weight format (rows, outputs and epilogues are
+// set per phase below).
+struct LayerMats {
+  PrefillJob q, k, v, o, up, down;
+  int hidden, kv, inter;
+};
+LayerMats mats_of(const pgq_q8_layer& Y) {
+  LayerMats M{};
+  auto m = [](const pgq_q8_matrix& x) { PrefillJob j{}; j.codes = x.codes; j.params = x.params; return j; };
+  M.q = m(Y.q); M.k = m(Y.k); M.v = m(Y.v); M.o = m(Y.o); M.up = m(Y.up); M.down = m(Y.down);
+  M.hidden = Y.hidden; M.kv = Y.kv; M.inter = Y.inter;
+  return M;
+}
+LayerMats mats_of(const pgq_q82f_layer& Y) {
+  LayerMats M{};
+  auto m = [](const pgq_q82f_matrix& x) {
+    PrefillJob j{};
+    j.codes = x.codes; j.rs = x.row_scale; j.cf = x.col_field;
+    return j;
+  };
+  M.q = m(Y.q); M.k = m(Y.k); M.v = m(Y.v); M.o = m(Y.o); M.up = m(Y.up); M.down = m(Y.down);
+  M.hidden = Y.hidden; M.kv = Y.kv; M.inter = Y.inter;
+  return M;
+}
+PrefillJob job_of(PrefillJob w, int rows, float* y, const float* residual, int epi) {
+  w.rows = rows; w.y = y; w.residual = residual; w.epilogue = epi;
+  return w;
+}
+
 // The four phases of layer l: q,k,v; o (+h); up (relu²); down (+h1).  `next` says
 // whether the launch goes on with layer l + 1 (the down phase then reports the
 // statistics of the new h).
-void layer_phases(HostPhase* ph, const pgq_q8_layer& Y, int l, bool next, float* h, const float* gamma1,
+void layer_phases(HostPhase* ph, const LayerMats& Y, int l, bool next, float* h, const float* gamma1,
                   const float* gamma2, const PassTaps& tp) {
   const int H = Y.hidden, KV = Y.kv, I = Y.inter;
   HostPhase& a = ph[0];
   a = HostPhase{};
-  a.job[0] = PrefillJob{Y.q.codes, Y.q.params, H, tp.q, nullptr, PGQ_EPI_NONE};
-  a.job[1] = PrefillJob{Y.k.codes, Y.k.params, KV, tp.k, nullptr, PGQ_EPI_NONE};
-  a.job[2] = PrefillJob{Y.v.codes, Y.v.params, KV, tp.v, nullptr, PGQ_EPI_NONE};
+  a.job[0] = job_of(Y.q, H, tp.q, nullptr, PGQ_EPI_NONE);
+  a.job[1] = job_of(Y.k, KV, tp.k, nullptr, PGQ_EPI_NONE);
+  a.job[2] = job_of(Y.v, KV, tp.v, nullptr, PGQ_EPI_NONE);
   a.njobs = 3; a.K = H; a.xk = 0; a.stats_job = 0; a.next_gamma = nullptr;
   a.gamma = gamma1 + (size_t)l * H; a.tap = tp.n1;
   HostPhase& o = ph[1];
   o = HostPhase{};
-  o.job[0] = PrefillJob{Y.o.codes, Y.o.params, H, tp.h1, h, PGQ_EPI_ADD};
+  o.job[0] = job_of(Y.o, H, tp.h1, h, PGQ_EPI_ADD);
   o.njobs = 1; o.K = H; o.xk = 1; o.stats_job = 0; o.next_gamma = gamma2 + (size_t)l * H;
   o.gamma = nullptr; o.tap = nullptr;
   HostPhase& u = ph[2];
   u = HostPhase{};
-  u.job[0] = PrefillJob{Y.up.codes, Y.up.params, I, tp.u, nullptr, PGQ_EPI_RELU2};
+  u.job[0] = job_of(Y.up, I, tp.u, nullptr, PGQ_EPI_RELU2);
   u.njobs = 1; u.K = H; u.xk = 2; u.stats_job = 0; u.next_gamma = nullptr;
   u.gamma = gamma2 + (size_t)l * H; u.tap = tp.n2;
   HostPhase& d = ph[3];
   d = HostPhase{};
-  d.job[0] = PrefillJob{Y.down.codes, Y.down.params, H, h, tp.h1, PGQ_EPI_ADD};
+  d.job[0] = job_of(Y.down, H, h, tp.h1, PGQ_EPI_ADD);
   d.njobs = 1; d.K = I; d.xk = 3; d.stats_job = next ? 0 : -1;
   d.next_gamma = next ? gamma1 + (size_t)(l + 1) * H : nullptr;
   d.gamma = nullptr; d.tap = nullptr;
+}
+
+// L layers in groups of PS_MAXL, one launch pair per group (a layer type with a
+// mats_of above).
+template <class Layer>
+int launch_pass_groups(const Layer* layers, int L, float* h, int B, const float* gamma1, const float* gamma2,
+                       float eps, const PassTaps& taps, void* ws, size_t ws_bytes, const DeviceInfo& dev,
+                       cudaStream_t st) {
+  HostPhase ph[PS_MAXPH];
+  for (int l0 = 0; l0 < L; l0 += PS_MAXL) {
+    const int n = std::min(PS_MAXL, L - l0);
+    for (int i = 0; i < n; ++i)
+      layer_phases(ph + 4 * i, mats_of(layers[l0 + i]), l0 + i, i + 1 < n, h, gamma1, gamma2, taps);
+    const int rc = launch_phases(ph, 4 * n, h, gamma1 + (size_t)l0 * layers[0].hidden, taps.n1, eps, B, ws,
+                                 ws_bytes, 0, dev, st);
+    if (rc) return rc;
+  }
+  return PGQ_OK;
 }
 
 }  // namespace
@@ -1563,7 +1658,8 @@ size_t prefill_pass_gemm_bytes(int H, int KV, int I, int B, const DeviceInfo& de
   Y.inter = I;
   HostPhase ph[PS_MAXPH];
   PassTaps tp{};
-  for (int l = 0; l < PS_MAXL; ++l) layer_phases(ph + 4 * l, Y, l, l + 1 < PS_MAXL, nullptr, nullptr, nullptr, tp);
+  for (int l = 0; l < PS_MAXL; ++l)
+    layer_phases(ph + 4 * l, mats_of(Y), l, l + 1 < PS_MAXL, nullptr, nullptr, nullptr, tp);
   return make_plan(ph, PS_MAXPH, B, dev).total;
 }
 
@@ -1613,16 +1709,13 @@ int launch_moe_bank_tc(const MoeBankArgs& a, void* ws, size_t ws_bytes, const De
 int launch_prefill_pass(const pgq_q8_layer* layers, int L, float* h, int B, const float* gamma1,
                         const float* gamma2, float eps, const PassTaps& taps, void* ws, size_t ws_bytes,
                         const DeviceInfo& dev, cudaStream_t st) {
-  HostPhase ph[PS_MAXPH];
-  for (int l0 = 0; l0 < L; l0 += PS_MAXL) {
-    const int n = std::min(PS_MAXL, L - l0);
-    for (int i = 0; i < n; ++i)
-      layer_phases(ph + 4 * i, layers[l0 + i], l0 + i, i + 1 < n, h, gamma1, gamma2, taps);
-    const int rc = launch_phases(ph, 4 * n, h, gamma1 + (size_t)l0 * layers[0].hidden, taps.n1, eps, B, ws,
-                                 ws_bytes, 0, dev, st);
-    if (rc) return rc;
-  }
-  return PGQ_OK;
+  return launch_pass_groups(layers, L, h, B, gamma1, gamma2, eps, taps, ws, ws_bytes, dev, st);
+}
+
+int launch_prefill_pass(const pgq_q82f_layer* layers, int L, float* h, int B, const float* gamma1,
+                        const float* gamma2, float eps, const PassTaps& taps, void* ws, size_t ws_bytes,
+                        const DeviceInfo& dev, cudaStream_t st) {
+  return launch_pass_groups(layers, L, h, B, gamma1, gamma2, eps, taps, ws, ws_bytes, dev, st);
 }
 
 }  // namespace pgq

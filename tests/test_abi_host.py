@@ -263,3 +263,35 @@ def test_q82f_arguments_rejected(L):
     outs = [p(10 + i) for i in range(6)]
     assert L.pgq_q82f_decode_layer(C.byref(lay), p(6), p(7), p(8), 1e-6, *outs, 4, None) == pgq.EINVAL
     assert L.pgq_q82f_decode_layer(None, p(6), p(7), p(8), 1e-6, *outs, 0, None) == pgq.EINVAL
+
+
+@no_gpu
+def test_q82f_prefill_arguments_rejected(L):
+    X, ws = _p(1), _p(2)
+    job = pgq.Q82Job(_p(3).value, _p(4).value, _p(6).value, 256, _p(5).value, pgq.EPI_NONE, None)
+    jobs = (pgq.Q82Job * 1)(job)
+    call = lambda **kw: L.pgq_prefill_q82f(kw.get("jobs", jobs), kw.get("njobs", 1), kw.get("X", X),  # noqa: E731
+                                           kw.get("cols", 512), kw.get("B", 16), ws, 1 << 30, None)
+    assert call(jobs=None) == pgq.EINVAL
+    assert call(B=65) == pgq.EINVAL
+    assert call(cols=480) == pgq.EUNSUPPORTED
+    assert call(X=C.c_void_p(FAKE + 4)) == pgq.EALIGN
+    bad = (pgq.Q82Job * 1)(pgq.Q82Job(_p(3).value, None, _p(6).value, 256, _p(5).value, pgq.EPI_NONE, None))
+    assert call(jobs=bad) == pgq.EINVAL            # no row scales
+    bad = (pgq.Q82Job * 1)(pgq.Q82Job(_p(3).value, _p(4).value + 8, _p(6).value, 256, _p(5).value, pgq.EPI_NONE,
+                                      None))
+    assert call(jobs=bad) == pgq.EALIGN            # row scales 16-byte aligned
+    bad = (pgq.Q82Job * 1)(pgq.Q82Job(_p(3).value, _p(4).value, _p(6).value, 256, _p(5).value, pgq.EPI_ADD, None))
+    assert call(jobs=bad) == pgq.EINVAL            # add without a residual
+    m = pgq.Q82Matrix(_p(3).value, _p(4).value, _p(6).value)
+    lay = (pgq.Q82Layer * 2)(pgq.Q82Layer(m, m, m, m, m, m, 512, 128, 1024),
+                             pgq.Q82Layer(m, m, m, m, m, m, 512, 128, 1024))
+    h, g1, g2 = _p(7), _p(8), _p(9)
+    pcall = lambda **kw: L.pgq_q82f_prefill_pass(kw.get("layers", lay), kw.get("L", 2), h, 8, g1, g2,  # noqa: E731
+                                                 1e-6, kw.get("ws", ws), 1 << 30, None)
+    assert pcall(L=0) == pgq.EINVAL
+    assert pcall(layers=None) == pgq.EINVAL
+    nocf = pgq.Q82Matrix(_p(3).value, _p(4).value, None)
+    assert pcall(layers=(pgq.Q82Layer * 1)(pgq.Q82Layer(m, m, m, m, m, nocf, 512, 128, 1024)), L=1) == pgq.EINVAL
+    odd = pgq.Q82Matrix(_p(3).value, _p(4).value + 2, _p(6).value)
+    assert pcall(layers=(pgq.Q82Layer * 1)(pgq.Q82Layer(m, odd, m, m, m, m, 512, 128, 1024)), L=1) == pgq.EALIGN

@@ -47,8 +47,8 @@ def test_gemv_q82f_epilogues_and_identity():
     y = dev(res)
     pgq.gemv_q82f(dev(codes), dev(rs), dev(cf), dev(x), epilogue="add", residual=y, y=y)
     check_proj(host(y), res.astype(np.float64) + ref, e, extra=np.abs(res) * 2.0 ** -23, what="q8_2f add")
-    # identity body, unit scales: x back bit for bit at several positions (the
-    # one-position kernel's biased-byte dot is exact only up to f32 rounding)
+    # identity body, unit scales: x back bit for bit at several positions, and within
+    # the tolerance at one position
     n = 4096
     eye = dev(np.eye(n, dtype=np.int8))
     ones = dev(np.ones(n, np.float16))
