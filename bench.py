@@ -507,14 +507,15 @@ def bench_vocab(torch, pgq, synth, steps, warmup, pk):
     return out
 
 
-def bench_moe(torch, pgq, synth, steps, warmup, pk, graph=True):
+def bench_moe(torch, pgq, synth, steps, warmup, pk, graph=True, q82f=False):
+    """The MoE prefill layer (q82f: with q8_2f experts, the q8_2f bank payload)."""
     c = synth.MOE
     E, H, I, B, k, wl = c["experts"], c["hidden"], c["inter"], c["B"], c["topk"], c["workload"]
-    router, up, down = synth.moe_layer(wl, E, H, I, "torch", "cuda")
+    router, up, down = (synth.moe_q82f_layer if q82f else synth.moe_layer)(wl, E, H, I, "torch", "cuda")
     h0 = synth.normal((B, H), 1.0, wl, synth.T_X, "torch", "cuda")
     g1 = synth.gamma(H, wl, backend="torch", device="cuda")
     g2 = synth.gamma(H, wl, synth.T_GAMMA2, "torch", "cuda")
-    Wm = pgq.MoeWeights(router, up[0], up[1], down[0], down[1], k)
+    Wm = pgq.MoeQ82Weights(router, up, down, k) if q82f else pgq.MoeWeights(router, up[0], up[1], down[0], down[1], k)
     h = h0.clone()
     y = torch.empty_like(h0)
     ws = pgq.moe_layer_workspace(Wm, B)
@@ -527,10 +528,11 @@ def bench_moe(torch, pgq, synth, steps, warmup, pk, graph=True):
     ms_graph = time_graph(torch, step, steps, warmup) if graph else ms
     taps = pgq.moe_layer_taps(Wm, ws, B)
     touched = int((taps["counts"] > 0).sum().item())
-    per_expert = 2 * (I * H + I * (H // 32) * 4)
+    per_expert = 2 * (I * H + 2 * (I + H)) if q82f else 2 * (I * H + I * (H // 32) * 4)
     nbytes = touched * per_expert + E * H * 4
     gbs = nbytes / (ms_graph * 1e-3) / 1e9
-    return {"workload": "MoE prefill layer B=64 (hidden 2688, 128 experts of 1856x2688 q8, top-6)",
+    fmt = "q8_2f" if q82f else "q8"
+    return {"workload": f"MoE prefill layer B=64 (hidden 2688, 128 experts of 1856x2688 {fmt}, top-6)",
             "metric": "positions/s", "value": round(B / (ms_graph * 1e-3), 1), "ms_per_layer": round(ms_graph, 4),
             "ms_per_layer_api": round(ms, 4), "touched_experts": touched, "weight_bytes": nbytes,
             "weight_GBps": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm"], 4), "launches_per_step": 7,
@@ -679,7 +681,8 @@ def main():
     ap.add_argument("--impl", default="pgq", choices=["pgq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-prefill", action="store_true", help="only the headline decode layer")
-    ap.add_argument("--only", choices=["decode", "prefill", "moe", "vocab", "q82f", "q82f_prefill"], default=None,
+    ap.add_argument("--only", choices=["decode", "prefill", "moe", "vocab", "q82f", "q82f_prefill", "q82f_moe"],
+                    default=None,
                     help="profiling aid: run one workload and print its JSON object")
     ap.add_argument("--no-graph", action="store_true", help="profiling aid (--only moe): direct calls only")
     ap.add_argument("--prefill-layers", type=int, default=None, help="layers of the prefill pass (default 32)")
@@ -722,6 +725,10 @@ def main():
     if args.only == "q82f_prefill":
         P = PrefillPassQ82F(torch, pgq, synth, layers=args.prefill_layers)
         print(json.dumps(time_prefill_q82f(torch, P, args.steps, args.warmup, pk)), flush=True)
+        return
+    if args.only == "q82f_moe":
+        print(json.dumps(bench_moe(torch, pgq, synth, args.steps, args.warmup, pk, graph=not args.no_graph, q82f=True)),
+              flush=True)
         return
     if args.only == "moe":
         print(json.dumps(bench_moe(torch, pgq, synth, args.steps, args.warmup, pk, graph=not args.no_graph)),
@@ -791,6 +798,9 @@ def main():
         line["workloads"]["q8_2f_prefill_pass"] = time_prefill_q82f(torch, P, max(3, args.steps // 5), args.warmup,
                                                                     pk)
         del P
+        torch.cuda.empty_cache()
+        line["workloads"]["q8_2f_moe_layer"] = bench_moe(torch, pgq, synth, max(5, args.steps // 5), args.warmup, pk,
+                                                         q82f=True)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_q8()
     if rank == 0:

@@ -481,6 +481,32 @@ int pgq_moe_prefill_layer(const pgq_moe_layer* layer, float* h, int B, const flo
                           const float* gamma2, float eps, float* y, void* workspace,
                           size_t workspace_bytes, void* stream);
 
+/* The MoE layer (as pgq_moe_prefill_layer) with q8_2f experts: the q8_2f bank payload
+ * of nemotron_prefill.rs `pb_q8_bank`.  Expert e's matrix is
+ *   w_e[r][c] = row_scale[e][r] * codes[e][r][c] * col_field[e][c],
+ * each bank contiguous: codes int8 [E][rows][cols], row_scale binary16 [E][rows],
+ * col_field binary16 [E][cols], all 16-byte aligned.  The banks run on the tensor
+ * cores with the arithmetic of pgq_prefill_q82f (|col_field| < 511); shapes they do
+ * not take (E > PGQ_MOE_Q82F_EMAX, hidden or inter not a multiple of 32) give
+ * PGQ_EUNSUPPORTED before anything is launched.  Workspace size and layout as the q8
+ * layer's, through the two calls below. */
+#define PGQ_MOE_Q82F_EMAX 256
+typedef struct {
+  const float* router;              /* f32 [E][hidden] */
+  const int8_t* up_codes;           /* int8 [E][inter][hidden] */
+  const uint16_t* up_row_scale;     /* binary16 [E][inter] */
+  const uint16_t* up_col_field;     /* binary16 [E][hidden] */
+  const int8_t* down_codes;         /* int8 [E][hidden][inter] */
+  const uint16_t* down_row_scale;   /* binary16 [E][hidden] */
+  const uint16_t* down_col_field;   /* binary16 [E][inter] */
+  int E, k, hidden, inter, renorm;
+} pgq_moe_q82f_layer;
+size_t pgq_moe_q82f_layer_workspace_bytes(const pgq_moe_q82f_layer* layer, int B);
+int pgq_moe_q82f_layer_layout(const pgq_moe_q82f_layer* layer, int B, size_t offsets[9]);
+int pgq_moe_q82f_prefill_layer(const pgq_moe_q82f_layer* layer, float* h, int B, const float* gamma1,
+                               const float* gamma2, float eps, float* y, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -292,7 +292,9 @@ def moe_layer(h, gamma1, gamma2, eps, router, experts, k, renorm=False, stage_in
     n = rms(h)·γ1; logits = R·n; (sel, w) = softmax top-k; grouping per expert;
     for each entry j: u_j = relu²(up_e(n[j // k])), eo_j = down_e(u_j);
     m[b] = Σ_s w[b][s]·eo[b·k+s]; h' = h + m; y = rms(h')·γ2.
-    ``experts[e]`` = (up_codes, up_params, down_codes, down_params).
+    ``experts[e]`` = (up_codes, up_params, down_codes, down_params) in the block format,
+    or (up_codes, up_row_scale, up_col_field, down_codes, down_row_scale, down_col_field)
+    in the q8_2f format (nemotron_prefill.rs's q8_2f bank payload of `pb_q8_bank`).
     ``stage_in`` may give 'sel', 'w', 'u', 'eo' to check stages on their own."""
     si = stage_in or {}
     h = np.atleast_2d(as_f64(h))
@@ -315,11 +317,18 @@ def moe_layer(h, gamma1, gamma2, eps, router, experts, k, renorm=False, stage_in
         js = entries[offsets[e]:offsets[e + 1]]
         if len(js) == 0:
             continue
-        uc, up_p, dc, dp = experts[e]
-        y, ey = gemv_q8(uc, up_p, n[js // k])
+        if len(experts[e]) == 6:
+            uc, urs, ucf, dc, drs, dcf = experts[e]
+            up_proj = lambda x: gemv_q82f(uc, urs, ucf, x)    # noqa: E731
+            down_proj = lambda x: gemv_q82f(dc, drs, dcf, x)  # noqa: E731
+        else:
+            uc, up_p, dc, dp = experts[e]
+            up_proj = lambda x: gemv_q8(uc, up_p, x)          # noqa: E731
+            down_proj = lambda x: gemv_q8(dc, dp, x)          # noqa: E731
+        y, ey = up_proj(n[js // k])
         up[js], e_up[js] = y, ey
         u_e = relu2(y) if u_given is None else as_f64(u_given)[js]
-        y2, ey2 = gemv_q8(dc, dp, u_e)
+        y2, ey2 = down_proj(u_e)
         eo[js], e_eo[js] = y2, ey2
     u = relu2(up)
     eo_in = as_f64(si.get("eo", eo))

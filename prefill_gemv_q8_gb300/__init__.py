@@ -47,6 +47,12 @@ class MoeLayer(C.Structure):
                 ("E", C.c_int), ("k", C.c_int), ("hidden", C.c_int), ("inter", C.c_int), ("renorm", C.c_int)]
 
 
+class MoeQ82Layer(C.Structure):
+    _fields_ = [("router", _vp), ("up_codes", _vp), ("up_row_scale", _vp), ("up_col_field", _vp),
+                ("down_codes", _vp), ("down_row_scale", _vp), ("down_col_field", _vp),
+                ("E", C.c_int), ("k", C.c_int), ("hidden", C.c_int), ("inter", C.c_int), ("renorm", C.c_int)]
+
+
 class Q82Matrix(C.Structure):
     _fields_ = [("codes", _vp), ("row_scale", _vp), ("col_field", _vp)]
 
@@ -120,6 +126,10 @@ _SIGS = {
     "pgq_moe_layer_layout": (C.c_int, [C.POINTER(MoeLayer), C.c_int, C.POINTER(C.c_size_t)]),
     "pgq_moe_prefill_layer": (C.c_int, [C.POINTER(MoeLayer), _vp, C.c_int, _vp, _vp, C.c_float, _vp, _vp,
                                         C.c_size_t, _vp]),
+    "pgq_moe_q82f_layer_workspace_bytes": (C.c_size_t, [C.POINTER(MoeQ82Layer), C.c_int]),
+    "pgq_moe_q82f_layer_layout": (C.c_int, [C.POINTER(MoeQ82Layer), C.c_int, C.POINTER(C.c_size_t)]),
+    "pgq_moe_q82f_prefill_layer": (C.c_int, [C.POINTER(MoeQ82Layer), _vp, C.c_int, _vp, _vp, C.c_float, _vp, _vp,
+                                             C.c_size_t, _vp]),
     "pgq_q8_prefill_pass_workspace_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int, C.c_int]),
     "pgq_q8_prefill_pass_layout": (C.c_int, [C.c_int, C.c_int, C.c_int, C.c_int, C.POINTER(C.c_size_t)]),
     "pgq_q8_prefill_pass": (C.c_int, [C.POINTER(Q8Layer), C.c_int, _vp, C.c_int, _vp, _vp, C.c_float, _vp,
@@ -711,14 +721,37 @@ class MoeWeights:
                           down_params.data_ptr(), E, k, hidden, inter, int(renorm))
 
 
+class MoeQ82Weights:
+    """ctypes view of an MoE layer with q8_2f experts (keeps the tensors alive)."""
+
+    def __init__(self, router, up, down, k, renorm=False):
+        (uc, urs, ucf), (dc, drs, dcf) = up, down
+        self.t = (router, uc, urs, ucf, dc, drs, dcf)
+        E, inter, hidden = uc.shape
+        _need(router, torch.float32, "router", (E, hidden))
+        _need(urs, torch.float16, "up_row_scale", (E, inter))
+        _need(ucf, torch.float16, "up_col_field", (E, hidden))
+        _need(dc, torch.int8, "down_codes", (E, hidden, inter))
+        _need(drs, torch.float16, "down_row_scale", (E, hidden))
+        _need(dcf, torch.float16, "down_col_field", (E, inter))
+        self.s = MoeQ82Layer(router.data_ptr(), uc.data_ptr(), urs.data_ptr(), ucf.data_ptr(), dc.data_ptr(),
+                             drs.data_ptr(), dcf.data_ptr(), E, k, hidden, inter, int(renorm))
+
+
+def _moe_q82(W):
+    return isinstance(W, MoeQ82Weights)
+
+
 def moe_layer_workspace(W, B, device="cuda"):
-    n = int(lib().pgq_moe_layer_workspace_bytes(C.byref(W.s), B))
+    f = lib().pgq_moe_q82f_layer_workspace_bytes if _moe_q82(W) else lib().pgq_moe_layer_workspace_bytes
+    n = int(f(C.byref(W.s), B))
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
 def moe_layer_taps(W, workspace, B):
     off = (C.c_size_t * 9)()
-    _check(lib().pgq_moe_layer_layout(C.byref(W.s), B, off))
+    f = lib().pgq_moe_q82f_layer_layout if _moe_q82(W) else lib().pgq_moe_layer_layout
+    _check(f(C.byref(W.s), B, off))
     s = W.s
     nb = B * s.k
     spec = [("n", torch.float32, (B, s.hidden)), ("logits", torch.float32, (B, s.E)), ("sel", torch.int32, (B, s.k)),
@@ -734,12 +767,14 @@ def moe_layer_taps(W, workspace, B):
 
 
 def moe_prefill_layer(W, h, gamma1, gamma2, eps=1e-6, y=None, workspace=None, stream=None):
-    """One MoE layer over the pass h [B][hidden] (h updated in place); returns (y, workspace)."""
+    """One MoE layer over the pass h [B][hidden] (h updated in place); returns (y, workspace).
+    W: MoeWeights (block-format experts) or MoeQ82Weights (q8_2f experts)."""
     _need(h, torch.float32, "h")
     B = h.shape[0]
     y = torch.empty_like(h) if y is None else y
     if workspace is None:
         workspace = moe_layer_workspace(W, B, h.device)
-    _check(lib().pgq_moe_prefill_layer(C.byref(W.s), _ptr(h), B, _ptr(gamma1), _ptr(gamma2), eps, _ptr(y),
-                                       _ptr(workspace), workspace.numel(), _stream(stream)))
+    f = lib().pgq_moe_q82f_prefill_layer if _moe_q82(W) else lib().pgq_moe_prefill_layer
+    _check(f(C.byref(W.s), _ptr(h), B, _ptr(gamma1), _ptr(gamma2), eps, _ptr(y), _ptr(workspace), workspace.numel(),
+             _stream(stream)))
     return y, workspace

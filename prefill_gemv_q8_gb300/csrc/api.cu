@@ -888,6 +888,83 @@ int pgq_moe_prefill_layer(const pgq_moe_layer* L, float* h, int B, const float* 
   return pgq_moe_combine_rmsnorm(h, nullptr, eo, wts, L->k, gamma2, eps, B, L->hidden, y, nullptr, stream);
 }
 
+namespace {
+pgq_moe_layer dims_of(const pgq_moe_q82f_layer& Q) {
+  pgq_moe_layer L{};
+  L.router = Q.router;
+  L.E = Q.E;
+  L.k = Q.k;
+  L.hidden = Q.hidden;
+  L.inter = Q.inter;
+  L.renorm = Q.renorm;
+  return L;
+}
+bool moe_q82f_ok(const pgq_moe_q82f_layer* Q, int B) {
+  return Q && Q->router && Q->up_codes && Q->up_row_scale && Q->up_col_field && Q->down_codes &&
+         Q->down_row_scale && Q->down_col_field && Q->E >= 1 && Q->k >= 1 && Q->k <= Q->E && Q->hidden >= 32 &&
+         Q->inter >= 32 && B >= 1 && B <= PGQ_PASS_BMAX;
+}
+}  // namespace
+
+size_t pgq_moe_q82f_layer_workspace_bytes(const pgq_moe_q82f_layer* layer, int B) {
+  if (!moe_q82f_ok(layer, B)) return 0;
+  return moe_layout(dims_of(*layer), B).total;
+}
+int pgq_moe_q82f_layer_layout(const pgq_moe_q82f_layer* layer, int B, size_t offsets[9]) {
+  REQUIRE(offsets && moe_q82f_ok(layer, B), PGQ_EINVAL, "moe_q82f_layer_layout: bad arguments");
+  const MoeLayout M = moe_layout(dims_of(*layer), B);
+  for (int i = 0; i < 9; ++i) offsets[i] = M.off[i];
+  return PGQ_OK;
+}
+
+int pgq_moe_q82f_prefill_layer(const pgq_moe_q82f_layer* Q, float* h, int B, const float* gamma1, const float* gamma2,
+                               float eps, float* y, void* workspace, size_t workspace_bytes, void* stream) {
+  REQUIRE(moe_q82f_ok(Q, B) && h && gamma1 && gamma2 && y && workspace, PGQ_EINVAL,
+          "moe_q82f_prefill_layer: bad arguments");
+  REQUIRE(((uintptr_t)workspace & 255) == 0, PGQ_EWORKSPACE, "moe_q82f_prefill_layer: workspace must be 256-byte aligned");
+  // the banks run on the tensor cores only: what they take is checked before any launch
+  REQUIRE(Q->E <= PGQ_MOE_Q82F_EMAX && Q->hidden % 32 == 0 && Q->inter % 32 == 0, PGQ_EUNSUPPORTED,
+          "moe_q82f_prefill_layer: E=%d (at most %d), hidden %d and inter %d (multiples of 32)", Q->E,
+          PGQ_MOE_Q82F_EMAX, Q->hidden, Q->inter);
+  REQUIRE(aligned16(Q->up_codes) && aligned16(Q->up_row_scale) && aligned16(Q->up_col_field) &&
+              aligned16(Q->down_codes) && aligned16(Q->down_row_scale) && aligned16(Q->down_col_field),
+          PGQ_EALIGN, "moe_q82f_prefill_layer: codes, row scales and column fields 16-byte aligned");
+  const pgq_moe_layer D = dims_of(*Q);
+  const MoeLayout M = moe_layout(D, B);
+  REQUIRE(workspace_bytes >= M.total, PGQ_EWORKSPACE, "moe_q82f_prefill_layer: workspace needs %zu bytes", M.total);
+  char* w = static_cast<char*>(workspace);
+  float* n = reinterpret_cast<float*>(w + M.off[0]);
+  float* logits = reinterpret_cast<float*>(w + M.off[1]);
+  int32_t* sel = reinterpret_cast<int32_t*>(w + M.off[2]);
+  float* wts = reinterpret_cast<float*>(w + M.off[3]);
+  int32_t* counts = reinterpret_cast<int32_t*>(w + M.off[4]);
+  int32_t* offs = reinterpret_cast<int32_t*>(w + M.off[5]);
+  int32_t* ents = reinterpret_cast<int32_t*>(w + M.off[6]);
+  float* u = reinterpret_cast<float*>(w + M.off[7]);
+  float* eo = reinterpret_cast<float*>(w + M.off[8]);
+  int rc;
+  if ((rc = pgq_add_rmsnorm(h, nullptr, gamma1, eps, B, Q->hidden, n, nullptr, stream))) return rc;
+  if ((rc = pgq_moe_router(Q->router, Q->E, Q->hidden, n, B, logits, stream))) return rc;
+  if ((rc = pgq_moe_route_topk(logits, B, Q->E, Q->k, Q->renorm, sel, wts, stream))) return rc;
+  if ((rc = pgq_moe_group_gather(sel, B, Q->k, Q->E, counts, offs, ents, nullptr, 0, 1, nullptr, stream))) return rc;
+  GET_DEVICE(dev);
+  const int nent = B * Q->k;
+  auto bank = [&](const int8_t* codes, const uint16_t* rs, const uint16_t* cf, int rows, int cols, const float* x,
+                  int xdiv, float* yb, int epi, bool first) -> int {
+    MoeBankArgs a{codes, nullptr, Q->E, rows, cols, counts, offs, ents, nent, x, xdiv, yb, epi};
+    a.rs = rs;
+    a.cf = cf;
+    return launch_moe_bank_tc(a, w + M.gemm, M.gend - M.gemm, dev, as_stream(stream), first);
+  };
+  if ((rc = bank(Q->up_codes, Q->up_row_scale, Q->up_col_field, Q->inter, Q->hidden, n, Q->k, u, PGQ_EPI_RELU2,
+                 true)))
+    return rc;
+  if ((rc = bank(Q->down_codes, Q->down_row_scale, Q->down_col_field, Q->hidden, Q->inter, u, 1, eo, PGQ_EPI_NONE,
+                 false)))
+    return rc;
+  return pgq_moe_combine_rmsnorm(h, nullptr, eo, wts, Q->k, gamma2, eps, B, Q->hidden, y, nullptr, stream);
+}
+
 int pgq_prefill_status(const void* workspace, void* stream) {
   REQUIRE(workspace, PGQ_EINVAL, "prefill_status: null workspace");
   GET_DEVICE(dev);

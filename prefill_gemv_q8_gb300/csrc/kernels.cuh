@@ -129,6 +129,8 @@ struct MoeBankArgs {
   int xdiv;                  // input row of entry j = j / xdiv
   float* y;                  // [entries][rows]
   int epilogue;
+  const uint16_t* rs = nullptr;   // q8_2f bank (params unused): binary16 row scales [E][rows]
+  const uint16_t* cf = nullptr;   // and column fields [E][cols]
 };
 int launch_router(const float* R, const float* n, int B, int E, int cols, float* logits, const DeviceInfo& dev,
                   cudaStream_t st);

@@ -66,6 +66,7 @@ constexpr int PS_MAXJ = 6 * PS_MAXL;                          // matrices per la
 constexpr int PS_NX = 4;                                      // input buffers (n1, q, n2, u)
 constexpr int PS_STATIC_SMEM = 6144;                          // bound on the kernel's static shared memory
 constexpr int PS_MOE_EMAX = 256;                              // experts of a grouped bank at most
+static_assert(PGQ_MOE_Q82F_EMAX <= PS_MOE_EMAX, "the q8_2f MoE layer runs its banks here");
 constexpr int PS_OUT_K = PS_ACC_COLS * (TC_BM / 4) / 128;     // float4 slots per epilogue thread (16)
 constexpr int PS_OUT_P = 4;                                   // handled in passes (registers)
 constexpr int PS_OUT_H = PS_OUT_K / PS_OUT_P;
@@ -537,7 +538,8 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
                                J.praw ? PS_CODES_BYTES : PS_CODES_BYTES + (J.rs ? PS_CF_BYTES : PS_PARAMS_BYTES));
             tc::tma_load_2d_hint(tc::smem_addr(st), &J.cmap, k * TC_BK, row0, bar(FULL_W + s), evict_first);
             if (J.rs)   // q8_2f: the step's 128 column-field values (kept in L2: every tile reads them)
-              tc::tma_load_2d(tc::smem_addr(st + PS_CODES_BYTES), &J.pmap, k * TC_BK, 0, bar(FULL_W + s));
+              tc::tma_load_2d(tc::smem_addr(st + PS_CODES_BYTES), &J.pmap, k * TC_BK, MOE ? expert_of(tile) : 0,
+                              bar(FULL_W + s));
             else if (!J.praw)
               tc::tma_load_2d_hint(tc::smem_addr(st + PS_CODES_BYTES), &J.pmap, k * (TC_BK / 32), row0,
                                    bar(FULL_W + s), evict_first);
@@ -735,7 +737,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
           cw[c] = *reinterpret_cast<const uint4*>(crow + ((cc ^ (r & 7)) << 4));
         }
         uint32_t out[32];
-        if (!MOE && P.f2) {
+        if (P.f2) {
           // q8_2f: w = q·cf (the exact byte, times the column's field, rounded once);
           // the step's 128 column-field values follow the codes (this warp's 64)
           const uint4* cfv = reinterpret_cast<const uint4*>(st + PS_CODES_BYTES + hk * 128);
@@ -1112,8 +1114,9 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
         }
         if (!MOE && et == 0) PTRACE(p, 11);
         const bool stats = vec_ok && j == F.stats_job;
+        const __half* rs_t = (MOE && J.rs) ? J.rs + (size_t)expert_of(tile) * rows : J.rs;   // the tile's row scales
         out_rows<MOE>(acc4, nv, et, res_fold ? PGQ_EPI_NONE : J.epi, J.y, J.residual, rows, row0, vec_ok, stats,
-                      MOE ? s_ent : nullptr, MOE ? nullptr : J.rs);
+                      MOE ? s_ent : nullptr, rs_t);
         if (!MOE && et == 0) PTRACE(p, 12);
         if (stats)
           tile_stats(acc4, nv, et, rows, row0, F.next_gamma,
@@ -1455,12 +1458,12 @@ int launch_phases(const HostPhase* hp, int nph, const float* x0, const float* ga
       const uint64_t pc = H.pcols > 0 ? (uint64_t)H.pcols : (uint64_t)(H.K / 32);
       const bool f2 = J.rs != nullptr;
       if (nj == 1) P.f2 = f2 ? 1 : 0;
-      if ((P.f2 != 0) != f2 || (f2 && (H.moe_E > 0 || H.praw)))
+      if ((P.f2 != 0) != f2 || (f2 && H.praw))
         return set_error(PGQ_EINVAL, "prefill: q8_2f and block-format matrices in one launch");
       if (!encode_2d(&D.cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, J.codes, H.K, mrows, (uint64_t)H.K, TC_BK, TC_BM,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
-          (f2 && !encode_2d(&D.pmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, J.cf, H.K, 1, (uint64_t)H.K * 2, TC_BK, 1,
-                            CU_TENSOR_MAP_SWIZZLE_NONE)) ||
+          (f2 && !encode_2d(&D.pmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, J.cf, H.K, H.moe_E > 0 ? H.moe_E : 1,
+                            (uint64_t)H.K * 2, TC_BK, 1, CU_TENSOR_MAP_SWIZZLE_NONE)) ||
           (!f2 && !H.praw &&
            !encode_2d(&D.pmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, J.params, pc, mrows, (uint64_t)pc * 4, TC_BK / 32,
                       TC_BM, CU_TENSOR_MAP_SWIZZLE_NONE)))
@@ -1688,13 +1691,15 @@ int launch_moe_bank_tc(const MoeBankArgs& a, void* ws, size_t ws_bytes, const De
                        bool clear_status) {
   // the tensor copies need 16-byte row strides of codes (pairs whose rows are not
   // go by 8-byte copies)
+  const bool f2 = a.rs != nullptr;   // q8_2f bank: row scales [E][rows], column field [E][cols]
   if (a.cols % 32 != 0 || a.cols % 16 != 0 || a.E > PS_MOE_EMAX || a.nentries < 1 || !aligned16(a.codes) ||
-      !aligned16(a.params) || !aligned16(a.x) || !aligned16(a.y) || a.rows % 4 != 0)
+      (f2 ? !aligned16(a.rs) || !aligned16(a.cf) : !aligned16(a.params)) || !aligned16(a.x) || !aligned16(a.y) ||
+      a.rows % 4 != 0)
     return PGQ_EUNSUPPORTED;
   HostPhase h{};
   // (scale, offset) rows that are not a multiple of 16 bytes go by 8-byte copies
-  h.praw = (a.cols / 32) % 4 != 0;
-  h.job[0] = PrefillJob{a.codes, a.params, a.rows, a.y, nullptr, a.epilogue};
+  h.praw = !f2 && (a.cols / 32) % 4 != 0;
+  h.job[0] = PrefillJob{a.codes, a.params, a.rows, a.y, nullptr, a.epilogue, a.rs, a.cf};
   h.njobs = 1;
   h.K = a.cols;
   h.xk = 0;

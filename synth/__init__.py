@@ -197,6 +197,33 @@ def q8_bank(E, rows, cols, workload, which, backend="numpy", device=None):
     return codes, params
 
 
+def q82f_bank(E, rows, cols, workload, which, backend="numpy", device=None):
+    """Contiguous bank of E q8_2f matrices (codes [E][rows][cols], row scales [E][rows],
+    column fields [E][cols]); expert e drawn as q82f_matrix from seed (workload,
+    expert_tensor_id(e, which) + 500)."""
+    if backend == "numpy":
+        cs, rs, cf = zip(*[q82f_matrix(rows, cols, workload, expert_tensor_id(e, which) + 500) for e in range(E)])
+        return np.stack(cs), np.stack(rs), np.stack(cf)
+    import torch
+    codes = torch.empty((E, rows, cols), dtype=torch.int8, device=device)
+    rs = torch.empty((E, rows), dtype=torch.float16, device=device)
+    cf = torch.empty((E, cols), dtype=torch.float16, device=device)
+    for e in range(E):
+        c, r, f = q82f_matrix(rows, cols, workload, expert_tensor_id(e, which) + 500, "torch", device)
+        codes[e].copy_(c)
+        rs[e].copy_(r)
+        cf[e].copy_(f)
+    return codes, rs, cf
+
+
+def moe_q82f_layer(workload, E, hidden, inter, backend="numpy", device=None):
+    """Router (as moe_layer) and the up / down expert banks in the q8_2f format."""
+    router = normal((E, hidden), 1.0 / np.sqrt(hidden), workload, T_ROUTER, backend, device)
+    up = q82f_bank(E, inter, hidden, workload, "up", backend, device)
+    down = q82f_bank(E, hidden, inter, workload, "down", backend, device)
+    return router, up, down
+
+
 def moe_layer(workload, E, hidden, inter, backend="numpy", device=None):
     """Router f32 [E][hidden] ~ N(0, 1/hidden) and the up / down expert banks."""
     router = normal((E, hidden), 1.0 / np.sqrt(hidden), workload, T_ROUTER, backend, device)

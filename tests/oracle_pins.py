@@ -597,6 +597,39 @@ def pin_moe_layer_composition():
     close(out["inv2"], 1.0 / np.sqrt(np.mean(hn * hn, axis=1) + 1e-6), rel=1e-13)
 
 
+def pin_moe_layer_q82f_closed_form():
+    """q8_2f experts (nemotron_prefill.rs's q8_2f bank payload): expert e's up matrix is
+    a permutation P (row r reads column π(r) = (3r + 1) mod n) with row scales
+    (e+1)·a_r and a column field b_c, its down matrix the identity with unit scales, so
+    up_e(x)_r = (e+1)·a_r·b_π(r)·x_π(r) and m[b] = Σ_s w_s·relu²(up_e(n[b])).  Row scales
+    and column fields differ in pattern and the permutation is not symmetric, so a
+    transposed or swapped factor, or the down bank's scales used for up, is seen."""
+    n, E, k, B = 32, 4, 2, 5
+    pi = (3 * np.arange(n) + 1) % n
+    perm = np.zeros((n, n), np.int8)
+    perm[np.arange(n), pi] = 1
+    a = 2.0 ** (np.arange(n) % 3 - 1)
+    bfield = 1.0 + (np.arange(n) % 4) / 4.0
+    eye = np.eye(n, dtype=np.int8)
+    ones = np.ones(n, np.float16)
+    experts = [(perm, ((e + 1) * a).astype(np.float16), bfield.astype(np.float16), eye, ones, ones) for e in range(E)]
+    r = _rng(27)
+    h = r.standard_normal((B, n))
+    g1, g2 = r.uniform(0.5, 1.5, n), r.uniform(0.5, 1.5, n)
+    router = r.standard_normal((E, n))
+    out = R.moe_layer(h, g1, g2, 1e-6, router, experts, k)
+    nrm = _rms_closed(h, g1, 1e-6)
+    sel, w = R.route(nrm @ router.T, k)
+    m = np.zeros_like(h)
+    for b in range(B):
+        for s in range(k):
+            up = (sel[b, s] + 1) * a * bfield[pi] * nrm[b][pi]
+            close(out["up"][b * k + s], up, rel=1e-13, abs_=1e-15)
+            m[b] += w[b, s] * _relu2_closed(up)
+    close(out["m"], m, rel=1e-12, abs_=1e-15)
+    close(out["y"], _rms_closed(h + m, g2, 1e-6), rel=1e-12)
+
+
 def pin_vocab_head_ties():
     """Duplicated rows give exact ties, which go to the lowest row."""
     r = _rng(26)

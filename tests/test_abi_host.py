@@ -295,3 +295,23 @@ def test_q82f_prefill_arguments_rejected(L):
     assert pcall(layers=(pgq.Q82Layer * 1)(pgq.Q82Layer(m, m, m, m, m, nocf, 512, 128, 1024)), L=1) == pgq.EINVAL
     odd = pgq.Q82Matrix(_p(3).value, _p(4).value + 2, _p(6).value)
     assert pcall(layers=(pgq.Q82Layer * 1)(pgq.Q82Layer(m, odd, m, m, m, m, 512, 128, 1024)), L=1) == pgq.EALIGN
+
+
+@no_gpu
+def test_moe_q82f_arguments_rejected(L):
+    q = lambda k: _p(k).value  # noqa: E731
+    lay = pgq.MoeQ82Layer(q(1), q(2), q(3), q(4), q(5), q(6), q(7), 128, 6, 2688, 1856, 0)
+    h, g1, g2, y, ws = _p(8), _p(9), _p(10), _p(11), _p(12)
+    call = lambda s_, B=64: L.pgq_moe_q82f_prefill_layer(C.byref(s_), h, B, g1, g2, 1e-6, y, ws,  # noqa: E731
+                                                         1 << 34, None)
+    big = pgq.MoeQ82Layer(q(1), q(2), q(3), q(4), q(5), q(6), q(7), 300, 6, 2688, 1856, 0)
+    assert call(big) == pgq.EUNSUPPORTED           # more experts than the tensor-core bank takes
+    odd = pgq.MoeQ82Layer(q(1), q(2), q(3), q(4), q(5), q(6), q(7), 128, 6, 2688 + 16, 1856, 0)
+    assert call(odd) == pgq.EUNSUPPORTED           # hidden not a multiple of 32
+    nocf = pgq.MoeQ82Layer(q(1), q(2), q(3), None, q(5), q(6), q(7), 128, 6, 2688, 1856, 0)
+    assert call(nocf) == pgq.EINVAL
+    assert call(lay, B=65) == pgq.EINVAL
+    mis = pgq.MoeQ82Layer(q(1), q(2), q(3) + 8, q(4), q(5), q(6), q(7), 128, 6, 2688, 1856, 0)
+    assert call(mis) == pgq.EALIGN
+    assert L.pgq_moe_q82f_layer_workspace_bytes(C.byref(nocf), 64) == 0
+    assert L.pgq_moe_q82f_layer_workspace_bytes(C.byref(lay), 64) > 0

@@ -150,14 +150,18 @@ def _layer_check(W_np, router, h0, g1, g2, k, taps, h_after, y, entries_sample=N
     check_rel(t["w"], w_ref, 1e-5, "w")
     c, o, en = oracle.group(t["sel"], E)
     assert np.array_equal(t["counts"], c) and np.array_equal(t["offsets"], o) and np.array_equal(t["entries"], en)
-    (uc, up_p), (dc, dn_p) = W_np
+    up, down = W_np   # (codes, params) banks, or (codes, row_scale, col_field) for q8_2f
+
+    def proj(bank, e, x):
+        return oracle.gemv_q82f(bank[0][e], bank[1][e], bank[2][e], x) if len(bank) == 3 else \
+            oracle.gemv_q8(bank[0][e], bank[1][e], x)
     B = h0.shape[0]
     js = range(B * k) if entries_sample is None else entries_sample
     for j in js:
         e = t["sel"].reshape(-1)[j]
-        yu, eu = oracle.gemv_q8(uc[e], up_p[e], t["n"][j // k])
+        yu, eu = proj(up, e, t["n"][j // k])
         check_relu2(t["u"][j], yu[0], eu[0], what=f"u[{j}]")
-        yd, ed = oracle.gemv_q8(dc[e], dn_p[e], t["u"][j])
+        yd, ed = proj(down, e, t["u"][j])
         check_proj(t["eo"][j], yd[0], ed[0], what=f"eo[{j}]")
     m = oracle.combine(t["eo"], t["w"], k)
     scale = np.abs(h0) + np.abs(t["w"][:, :, None] * t["eo"].reshape(B, k, -1)).sum(axis=1)
@@ -206,4 +210,49 @@ def test_moe_layer_full_size_sampled():
     for e in need:
         up_np[0][e], up_np[1][e] = host(up[0][e]), host(up[1][e])
         dn_np[0][e], dn_np[1][e] = host(down[0][e]), host(down[1][e])
+    _layer_check((up_np, dn_np), host(router), host(h0), host(g1), host(g2), k, taps, h, y, entries_sample=sample)
+
+
+@pytest.mark.parametrize("E,H,I,B,k", [(16, 256, 128, 24, 4), (8, 384, 96, 64, 2)])
+def test_moe_q82f_layer_small(E, H, I, B, k):
+    """The MoE layer with q8_2f experts (nemotron_prefill.rs's q8_2f bank payload);
+    inter = 96 makes the down bank's last k-step ragged."""
+    router, up, down = synth.moe_q82f_layer(1230 + E, E, H, I)
+    h0 = synth.normal((B, H), 1.0, 1230 + E, synth.T_X)
+    g1, g2 = synth.gamma(H, 1230 + E), synth.gamma(H, 1230 + E, synth.T_GAMMA2)
+    W = pgq.MoeQ82Weights(dev(router), tuple(dev(a) for a in up), tuple(dev(a) for a in down), k)
+    h = dev(h0)
+    ws = torch.full((pgq.moe_layer_workspace(W, B).numel(),), 0x55, dtype=torch.uint8, device="cuda")
+    y, ws = pgq.moe_prefill_layer(W, h, dev(g1), dev(g2), 1e-6, workspace=ws)
+    assert pgq.last_device_status(ws) == pgq.OK
+    taps = pgq.moe_layer_taps(W, ws, B)
+    _layer_check((up, down), router, h0, g1, g2, k, taps, h, y)
+    # the oracle's whole layer agrees with the kernel's final output
+    ref = oracle.moe_layer(h0, g1, g2, 1e-6, router,
+                           [(up[0][e], up[1][e], up[2][e], down[0][e], down[1][e], down[2][e]) for e in range(E)], k)
+    assert np.array_equal(host(taps["sel"]), ref["sel"])
+
+
+def test_moe_q82f_layer_full_size_sampled():
+    """The q8_2f MoE layer at the full size (B = 64, hidden 2688, 128 experts of
+    1856 x 2688, top-6); float outputs checked on 36 sampled entries."""
+    c = synth.MOE
+    E, H, I, B, k, wl = c["experts"], c["hidden"], c["inter"], c["B"], c["topk"], c["workload"]
+    router, up, down = synth.moe_q82f_layer(wl, E, H, I, "torch", "cuda")
+    h0 = synth.normal((B, H), 1.0, wl, synth.T_X, "torch", "cuda")
+    g1 = synth.gamma(H, wl, backend="torch", device="cuda")
+    g2 = synth.gamma(H, wl, synth.T_GAMMA2, "torch", "cuda")
+    W = pgq.MoeQ82Weights(router, up, down, k)
+    h = h0.clone()
+    y, ws = pgq.moe_prefill_layer(W, h, g1, g2, 1e-6)
+    assert pgq.last_device_status(ws) == pgq.OK
+    taps = pgq.moe_layer_taps(W, ws, B)
+    sample = sorted(np.random.default_rng(2).choice(B * k, 36, replace=False).tolist())
+    sel = host(taps["sel"]).reshape(-1)
+    need = sorted(set(int(sel[j]) for j in sample))
+    up_np = (np.zeros((E, I, H), np.int8), np.zeros((E, I), np.float16), np.zeros((E, H), np.float16))
+    dn_np = (np.zeros((E, H, I), np.int8), np.zeros((E, H), np.float16), np.zeros((E, I), np.float16))
+    for e in need:
+        for i in range(3):
+            up_np[i][e], dn_np[i][e] = host(up[i][e]), host(down[i][e])
     _layer_check((up_np, dn_np), host(router), host(h0), host(g1), host(g2), k, taps, h, y, entries_sample=sample)
