@@ -91,9 +91,9 @@ int pgq_device_check(void);
  * current device recorded an expired wait since the previous call of this function
  * (that record is per device, and reading it clears it), else, when workspace !=
  * NULL, the status word of the last prefill / pass / MoE call that used that
- * workspace (PGQ_OK or PGQ_ETIMEOUT; not cleared: the next call on the workspace
- * resets it), else PGQ_OK.  PGQ_ECUDA if a CUDA call fails (e.g. an earlier launch
- * faulted). */
+ * workspace (PGQ_OK or PGQ_ETIMEOUT; a set word is cleared by this read, and the
+ * next call on the workspace resets it in any case), else PGQ_OK.  PGQ_ECUDA if a
+ * CUDA call fails (e.g. an earlier launch faulted). */
 int pgq_last_device_status(const void* workspace, void* stream);
 
 /* Limit of every bounded device-side wait, in nanoseconds, for launches made after

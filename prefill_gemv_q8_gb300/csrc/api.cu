@@ -129,13 +129,16 @@ int pgq_last_device_status(const void* workspace, void* stream) {
   if (rc) return rc;
   int ws[2] = {PGQ_OK, PGQ_OK};
   if (workspace) {
-    e = cudaMemcpy(ws, static_cast<const char*>(workspace) + prefill_status_offset(), sizeof(ws),
-                   cudaMemcpyDeviceToHost);
+    char* st = const_cast<char*>(static_cast<const char*>(workspace)) + prefill_status_offset();
+    e = cudaMemcpy(ws, st, sizeof(ws), cudaMemcpyDeviceToHost);
+    // read and clear: a later call on the workspace starts from a clean record
+    if (e == cudaSuccess && (ws[0] != PGQ_OK || ws[1] != PGQ_OK)) e = cudaMemset(st, 0, sizeof(ws));
     if (e != cudaSuccess) return cuda_status(e);
   }
   if (dec != PGQ_OK) return dec;
   return ws[0] != PGQ_OK ? ws[0] : ws[1];
 }
+
 
 int pgq_add_rmsnorm(float* h, const float* add, const float* gamma, float eps, int B, int n, float* y,
                     float* inv_rms, void* stream) {
