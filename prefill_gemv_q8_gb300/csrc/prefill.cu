@@ -56,6 +56,8 @@ constexpr int PS_XST = 3;          // input ring stages (4 measured no faster)
 constexpr int PS_CODES_BYTES = TC_BM * TC_BK;                 // 16 KB
 constexpr int PS_PARAMS_BYTES = TC_BM * 16;                   // 4 (scale, offset) pairs per row
 constexpr int PS_W_BYTES = PS_CODES_BYTES + PS_PARAMS_BYTES;  // 18 KB, a multiple of 1 KB
+constexpr int PS_PG_BYTES = 4 * 1024;                          // grouped banks: params of 4-row groups
+constexpr int PS_WM_BYTES = PS_CODES_BYTES + PS_PG_BYTES;      // a grouped bank's stage (20 KB)
 constexpr int PS_CF_BYTES = TC_BK * 2;                        // q8_2f: the step's column field
 constexpr int PS_ACC_COLS = 64;                               // TMEM columns per accumulator (N <= 64)
 constexpr int PS_A_COLS = TC_BK / 2;                          // TMEM columns per A buffer
@@ -73,11 +75,12 @@ constexpr int PS_OUT_H = PS_OUT_K / PS_OUT_P;
 
 struct PsJob {
   CUtensorMap cmap;          // codes int8 [rows][cols], box {128, 128}, 128-byte swizzle
-  CUtensorMap pmap;          // params u32 [rows][cols/32], box {4, 128} (unless praw)
-  // params whose rows are not a multiple of 16 bytes (no tensor copy): u32 [rows][pstride],
-  // copied 8 bytes at a time (cp.async) by the producer warp; null: pmap
-  const uint32_t* praw;
-  int pstride, prows;
+  CUtensorMap pmap;          // params u32 [rows][cols/32], box {4, 128} (psr = 0)
+  // A grouped bank whose params rows are not a multiple of 16 bytes: pmap views each 4
+  // rows as one row of 4·psr u32 (16·psr bytes), box {8, 32}, and a step is 4 copies,
+  // one per row j of the groups, from u32 4k + (j·psr rounded down to a multiple of 4):
+  // the step's 4 pairs of row j sit at u32 (j·psr) mod 4 of its 8.  psr = pairs per row
+  int psr;
   float* y;                  // [B][rows]
   const float* residual;     // [B][rows] for PGQ_EPI_ADD
   // q8_2f (w = rs[r]·q[r][c]·cf[c]): binary16 row scales [rows]; pmap then maps the
@@ -396,9 +399,10 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int Bp = P.Bp, WST = P.wst, G = P.G;
+  constexpr int WB = MOE ? PS_WM_BYTES : PS_W_BYTES;   // weight-ring stage bytes
   const int xst_bytes = 2 * Bp * 128;   // two 64-column halves of an input slice
   uint8_t* wring = smem;
-  uint8_t* xring = wring + WST * PS_W_BYTES;
+  uint8_t* xring = wring + WST * WB;
   float* s_acc = reinterpret_cast<float*>(xring + PS_XST * xst_bytes);   // [Bp][128]
   float* fixb = s_acc + Bp * TC_BM;                                      // [Bp][128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(fixb + Bp * TC_BM);
@@ -512,35 +516,23 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
           }
           const int row0 = MOE ? expert_of(tile) * P.job[j].rows + (tile % tpe) * TC_BM
                                : (tile - P.job[j].tile0) * TC_BM;
-          uint8_t* st = wring + s * PS_W_BYTES;
+          uint8_t* st = wring + s * WB;
           const PsJob& J = P.job[j];
-          if (J.praw) {
-            // the step's 16 bytes of pairs of each of the 128 rows, 8 bytes per copy;
-            // the barrier tracks the copies (each lane's arrive counts itself in and
-            // out), before the arrive that completes its count is made below
-#pragma unroll
-            for (int i = 0; i < TC_BM / 32; ++i) {
-              const int rr = lane + 32 * i;
-              if (row0 + rr < J.prows) {
-                const uint32_t* src = J.praw + (size_t)(row0 + rr) * J.pstride + k * (TC_BK / 32);
-                const uint32_t dst = tc::smem_addr(st + PS_CODES_BYTES + rr * 16);
-                asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
-                asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst + 8), "l"(src + 2) : "memory");
-              }
-            }
-            asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar(FULL_W + s)) : "memory");
-            __syncwarp();
-          }
           if (tc::elect_one()) {
             if (MOE && (k == 0 || it == beg)) PTRACE(wtile, 0);
             if (!MOE && it == beg) PTRACE(p, 0);
             tc::mbar_expect_tx(bar(FULL_W + s),
-                               J.praw ? PS_CODES_BYTES : PS_CODES_BYTES + (J.rs ? PS_CF_BYTES : PS_PARAMS_BYTES));
+                               PS_CODES_BYTES + (J.rs ? PS_CF_BYTES : (MOE && J.psr) ? PS_PG_BYTES : PS_PARAMS_BYTES));
             tc::tma_load_2d_hint(tc::smem_addr(st), &J.cmap, k * TC_BK, row0, bar(FULL_W + s), evict_first);
             if (J.rs)   // q8_2f: the step's 128 column-field values (kept in L2: every tile reads them)
               tc::tma_load_2d(tc::smem_addr(st + PS_CODES_BYTES), &J.pmap, k * TC_BK, MOE ? expert_of(tile) : 0,
                               bar(FULL_W + s));
-            else if (!J.praw)
+            else if (MOE && J.psr) {
+#pragma unroll
+              for (int g = 0; g < 4; ++g)
+                tc::tma_load_2d_hint(tc::smem_addr(st + PS_CODES_BYTES + g * 1024), &J.pmap,
+                                     k * (TC_BK / 32) + ((g * J.psr) & ~3), row0 >> 2, bar(FULL_W + s), evict_first);
+            } else
               tc::tma_load_2d_hint(tc::smem_addr(st + PS_CODES_BYTES), &J.pmap, k * (TC_BK / 32), row0,
                                    bar(FULL_W + s), evict_first);
           }
@@ -699,6 +691,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
     const int q = warp & 3;              // TMEM lane quarter of this warp
     const int hk = (warp - 2) >> 2;      // which 64 columns of the step
     const int r = q * 32 + lane;         // weight row within the tile
+    const int psr = MOE ? P.job[0].psr : 0;   // (a grouped bank has one matrix)
     int s = 0, a = 0;
     uint32_t ph = 0, pha = 0;
     bool stop = false;
@@ -728,7 +721,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
           PTADD(p, 18, tc::globaltimer() - td1);
         }
 #endif
-        const uint8_t* st = wring + s * PS_W_BYTES;
+        const uint8_t* st = wring + s * WB;
         const uint8_t* crow = st + r * 128;
         uint4 cw[4];
 #pragma unroll
@@ -756,8 +749,16 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
             }
           }
         } else {
-          const uint2 pr = *reinterpret_cast<const uint2*>(st + PS_CODES_BYTES + r * 16 + hk * 8);
-          const uint32_t prw[2] = {pr.x, pr.y};
+          uint32_t prw[2];
+          if (MOE && psr) {   // 4-row groups: row r is row r mod 4 of group r / 4
+            const uint8_t* pb = st + PS_CODES_BYTES + (r & 3) * 1024 + (r >> 2) * 32 + ((((r & 3) * psr) & 3) << 2) + hk * 8;
+            prw[0] = *reinterpret_cast<const uint32_t*>(pb);
+            prw[1] = *reinterpret_cast<const uint32_t*>(pb + 4);
+          } else {
+            const uint2 pr = *reinterpret_cast<const uint2*>(st + PS_CODES_BYTES + r * 16 + hk * 8);
+            prw[0] = pr.x;
+            prw[1] = pr.y;
+          }
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const __half2 so = *reinterpret_cast<const __half2*>(&prw[c >> 1]);
@@ -1338,7 +1339,7 @@ struct HostPhase {
   float* tap;
   int moe_E;                 // > 0: job 0 is a grouped bank of moe_E experts
   int pcols;                 // (scale, offset) pairs per row of the params (0: K / 32)
-  bool praw;                 // params rows not a multiple of 16 bytes: copied by cp.async
+  bool praw;                 // params rows not a multiple of 16 bytes: read in 4-row groups (a bank only)
   int xrows;                 // rows of the input buffer when more than the positions (grouped bank)
 };
 
@@ -1361,12 +1362,12 @@ struct Plan {
 
 // Shared memory of the kernel for Bp positions: the input ring, the shared tile and
 // the partial buffer are fixed; the weight ring takes the rest (at most 10 stages).
-bool kernel_smem(int Bp, const DeviceInfo& dev, int& wst, size_t& smem) {
+bool kernel_smem(int Bp, size_t wbytes, const DeviceInfo& dev, int& wst, size_t& smem) {
   const size_t fixed = 1024 /*alignment*/ + (size_t)PS_XST * 2 * Bp * 128 + 2 * (size_t)Bp * TC_BM * 4 + 512;
   const size_t avail = (size_t)dev.smem_optin > PS_STATIC_SMEM ? (size_t)dev.smem_optin - PS_STATIC_SMEM : 0;
-  if (avail < fixed + 3 * (size_t)PS_W_BYTES) return false;
-  wst = (int)std::min<size_t>(PS_WST_MAX, (avail - fixed) / PS_W_BYTES);
-  smem = fixed + (size_t)wst * PS_W_BYTES;
+  if (avail < fixed + 3 * wbytes) return false;
+  wst = (int)std::min<size_t>(PS_WST_MAX, (avail - fixed) / wbytes);
+  smem = fixed + (size_t)wst * wbytes;
   return true;
 }
 
@@ -1398,7 +1399,7 @@ Plan make_plan(const HostPhase* hp, int nph, int B, const DeviceInfo& dev) {
     const long long per = ((long long)tiles * ks + p.G - 1) / p.G;
     p.maxseg = std::max(p.maxseg, (int)std::min<long long>(tiles, (per + ks - 1) / ks + 1));
   }
-  if (!kernel_smem(p.Bp, dev, p.wst, p.smem)) p.wst = 0;
+  if (!kernel_smem(p.Bp, hp[0].moe_E > 0 ? PS_WM_BYTES : PS_W_BYTES, dev, p.wst, p.smem)) p.wst = 0;
   p.ncounters = 2 * PS_MAXPH + 2 * p.maxtiles;
   auto up = [](size_t v, size_t a) { return (v + a - 1) / a * a; };
   size_t o = 0;
@@ -1460,18 +1461,21 @@ int launch_phases(const HostPhase* hp, int nph, const float* x0, const float* ga
       if (nj == 1) P.f2 = f2 ? 1 : 0;
       if ((P.f2 != 0) != f2 || (f2 && H.praw))
         return set_error(PGQ_EINVAL, "prefill: q8_2f and block-format matrices in one launch");
+      if (H.praw && (H.moe_E <= 0 || mrows % 4 != 0))
+        return set_error(PGQ_EINVAL, "prefill: params rows of %d pairs need a grouped bank of rows %% 4 == 0", (int)pc);
       if (!encode_2d(&D.cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, J.codes, H.K, mrows, (uint64_t)H.K, TC_BK, TC_BM,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
           (f2 && !encode_2d(&D.pmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, J.cf, H.K, H.moe_E > 0 ? H.moe_E : 1,
                             (uint64_t)H.K * 2, TC_BK, 1, CU_TENSOR_MAP_SWIZZLE_NONE)) ||
           (!f2 && !H.praw &&
            !encode_2d(&D.pmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, J.params, pc, mrows, (uint64_t)pc * 4, TC_BK / 32,
-                      TC_BM, CU_TENSOR_MAP_SWIZZLE_NONE)))
+                      TC_BM, CU_TENSOR_MAP_SWIZZLE_NONE)) ||
+          (!f2 && H.praw &&   // 4 rows as one row of 16·pc bytes
+           !encode_2d(&D.pmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, J.params, 4 * pc, mrows / 4, 16 * pc, 8, TC_BM / 4,
+                      CU_TENSOR_MAP_SWIZZLE_NONE)))
         return set_error(PGQ_ECUDA, "prefill: tensor map of phase %d matrix %d could not be encoded", i, j);
       D.rs = reinterpret_cast<const __half*>(J.rs);
-      D.praw = H.praw ? reinterpret_cast<const uint32_t*>(J.params) : nullptr;
-      D.pstride = (int)pc;
-      D.prows = (int)mrows;
+      D.psr = H.praw ? (int)pc : 0;
       D.y = J.y;
       D.residual = J.residual;
       D.rows = J.rows;
@@ -1689,15 +1693,15 @@ size_t moe_bank_tc_workspace_bytes(int E, int rows, int cols, int nent, const De
 
 int launch_moe_bank_tc(const MoeBankArgs& a, void* ws, size_t ws_bytes, const DeviceInfo& dev, cudaStream_t st,
                        bool clear_status) {
-  // the tensor copies need 16-byte row strides of codes (pairs whose rows are not
-  // go by 8-byte copies)
+  // the tensor copies need 16-byte row strides of codes (params rows that are not
+  // are read in 4-row groups, which are)
   const bool f2 = a.rs != nullptr;   // q8_2f bank: row scales [E][rows], column field [E][cols]
   if (a.cols % 32 != 0 || a.cols % 16 != 0 || a.E > PS_MOE_EMAX || a.nentries < 1 || !aligned16(a.codes) ||
       (f2 ? !aligned16(a.rs) || !aligned16(a.cf) : !aligned16(a.params)) || !aligned16(a.x) || !aligned16(a.y) ||
       a.rows % 4 != 0)
     return PGQ_EUNSUPPORTED;
   HostPhase h{};
-  // (scale, offset) rows that are not a multiple of 16 bytes go by 8-byte copies
+  // (scale, offset) rows that are not a multiple of 16 bytes are read in 4-row groups
   h.praw = !f2 && (a.cols / 32) % 4 != 0;
   h.job[0] = PrefillJob{a.codes, a.params, a.rows, a.y, nullptr, a.epilogue, a.rs, a.cf};
   h.njobs = 1;

@@ -170,8 +170,11 @@ def _layer_check(W_np, router, h0, g1, g2, k, taps, h_after, y, entries_sample=N
     check_rel(host(y), y_ref, NORM_TOL + 1e-6, "y", abs_=1e-30)
 
 
-def test_moe_layer_small():
-    E, H, I, B, k = 16, 256, 128, 24, 4
+@pytest.mark.parametrize("E,H,I,B,k", [(16, 256, 128, 24, 4), (8, 288, 96, 24, 3), (6, 160, 224, 40, 2)])
+def test_moe_layer_small(E, H, I, B, k):
+    """(The second and third shapes have an odd number of (scale, offset) pairs per row
+    in both banks (9 and 3; 5 and 7): rows that start on 4-byte boundaries and a ragged
+    last k-step whose missing pairs are zero-filled.)"""
     router, up, down = synth.moe_layer(978, E, H, I)
     h0 = synth.normal((B, H), 1.0, 978, synth.T_X)
     g1, g2 = synth.gamma(H, 978), synth.gamma(H, 978, synth.T_GAMMA2)
