@@ -814,6 +814,7 @@ struct MoeLayout {
   size_t gemm;    // the tensor-core banks' area, first: its status word at offset 0
   size_t gend;    // end of that area
   size_t off[9];  // n, logits, sel, w, counts, offsets, entries, u, eo
+  size_t tick;    // the routing tickets (RouteOut::ticks words)
   size_t total;
 };
 MoeLayout moe_layout(const pgq_moe_layer& L, int B) {
@@ -832,8 +833,34 @@ MoeLayout moe_layout(const pgq_moe_layer& L, int B) {
     M.off[i] = o;
     o = (o + sz[i] + 255) / 256 * 256;
   }
+  M.tick = o;
+  o += 256;
   M.total = o;
   return M;
+}
+
+// The layer's first two launches: add + RMSNorm of h into n (which also clears the
+// routing tickets), then the router, whose tail makes the selection and the
+// per-expert lists (RouteOut).
+int moe_norm_route(float* h, int B, const float* gamma1, float eps, int hidden, const float* router, int E, int k,
+                   int renorm, char* w, const MoeLayout& M, const DeviceInfo& dev, cudaStream_t st) {
+  REQUIRE(aligned16(h) && aligned16(gamma1) && aligned16(router), PGQ_EALIGN,
+          "moe layer: h, gamma1 and the router must be 16-byte aligned");
+  REQUIRE(eps >= 0.f, PGQ_EINVAL, "moe layer: eps must be >= 0");
+  REQUIRE(!overlaps(h, (size_t)B * hidden * 4, w, M.total), PGQ_EINVAL, "moe layer: h overlaps the workspace");
+  float* n = reinterpret_cast<float*>(w + M.off[0]);
+  unsigned* tick = reinterpret_cast<unsigned*>(w + M.tick);
+  if (int rc = launch_add_rmsnorm(h, nullptr, gamma1, eps, 0.f, 0, B, hidden, n, nullptr, st, tick, RouteOut::ticks))
+    return rc;
+  const RouteOut ro{k,
+                    renorm,
+                    reinterpret_cast<int32_t*>(w + M.off[2]),
+                    reinterpret_cast<float*>(w + M.off[3]),
+                    reinterpret_cast<int32_t*>(w + M.off[4]),
+                    reinterpret_cast<int32_t*>(w + M.off[5]),
+                    reinterpret_cast<int32_t*>(w + M.off[6]),
+                    tick};
+  return launch_router(router, n, B, E, hidden, reinterpret_cast<float*>(w + M.off[1]), dev, st, &ro);
 }
 bool moe_layer_ok(const pgq_moe_layer* L, int B) {
   return L && L->router && L->up_codes && L->up_params && L->down_codes && L->down_params && L->E >= 1 && L->k >= 1 &&
@@ -862,8 +889,6 @@ int pgq_moe_prefill_layer(const pgq_moe_layer* L, float* h, int B, const float* 
   REQUIRE(L->hidden % 32 == 0 && L->inter % 32 == 0, PGQ_EINVAL, "moe_prefill_layer: hidden/inter % 32");
   char* w = static_cast<char*>(workspace);
   float* n = reinterpret_cast<float*>(w + M.off[0]);
-  float* logits = reinterpret_cast<float*>(w + M.off[1]);
-  int32_t* sel = reinterpret_cast<int32_t*>(w + M.off[2]);
   float* wts = reinterpret_cast<float*>(w + M.off[3]);
   int32_t* counts = reinterpret_cast<int32_t*>(w + M.off[4]);
   int32_t* offs = reinterpret_cast<int32_t*>(w + M.off[5]);
@@ -871,11 +896,10 @@ int pgq_moe_prefill_layer(const pgq_moe_layer* L, float* h, int B, const float* 
   float* u = reinterpret_cast<float*>(w + M.off[7]);
   float* eo = reinterpret_cast<float*>(w + M.off[8]);
   int rc;
-  if ((rc = pgq_add_rmsnorm(h, nullptr, gamma1, eps, B, L->hidden, n, nullptr, stream))) return rc;
-  if ((rc = pgq_moe_router(L->router, L->E, L->hidden, n, B, logits, stream))) return rc;
-  if ((rc = pgq_moe_route_topk(logits, B, L->E, L->k, L->renorm, sel, wts, stream))) return rc;
-  if ((rc = pgq_moe_group_gather(sel, B, L->k, L->E, counts, offs, ents, nullptr, 0, 1, nullptr, stream))) return rc;
   GET_DEVICE(dev);
+  if ((rc = moe_norm_route(h, B, gamma1, eps, L->hidden, L->router, L->E, L->k, L->renorm, w, M, dev,
+                           as_stream(stream))))
+    return rc;
   const int nent = B * L->k;
   // each bank on the tensor cores where its shape allows, else the expert GEMV kernel;
   // the first bank resets the banks' status word, the second keeps what it records
@@ -937,8 +961,6 @@ int pgq_moe_q82f_prefill_layer(const pgq_moe_q82f_layer* Q, float* h, int B, con
   REQUIRE(workspace_bytes >= M.total, PGQ_EWORKSPACE, "moe_q82f_prefill_layer: workspace needs %zu bytes", M.total);
   char* w = static_cast<char*>(workspace);
   float* n = reinterpret_cast<float*>(w + M.off[0]);
-  float* logits = reinterpret_cast<float*>(w + M.off[1]);
-  int32_t* sel = reinterpret_cast<int32_t*>(w + M.off[2]);
   float* wts = reinterpret_cast<float*>(w + M.off[3]);
   int32_t* counts = reinterpret_cast<int32_t*>(w + M.off[4]);
   int32_t* offs = reinterpret_cast<int32_t*>(w + M.off[5]);
@@ -946,11 +968,10 @@ int pgq_moe_q82f_prefill_layer(const pgq_moe_q82f_layer* Q, float* h, int B, con
   float* u = reinterpret_cast<float*>(w + M.off[7]);
   float* eo = reinterpret_cast<float*>(w + M.off[8]);
   int rc;
-  if ((rc = pgq_add_rmsnorm(h, nullptr, gamma1, eps, B, Q->hidden, n, nullptr, stream))) return rc;
-  if ((rc = pgq_moe_router(Q->router, Q->E, Q->hidden, n, B, logits, stream))) return rc;
-  if ((rc = pgq_moe_route_topk(logits, B, Q->E, Q->k, Q->renorm, sel, wts, stream))) return rc;
-  if ((rc = pgq_moe_group_gather(sel, B, Q->k, Q->E, counts, offs, ents, nullptr, 0, 1, nullptr, stream))) return rc;
   GET_DEVICE(dev);
+  if ((rc = moe_norm_route(h, B, gamma1, eps, Q->hidden, Q->router, Q->E, Q->k, Q->renorm, w, M, dev,
+                           as_stream(stream))))
+    return rc;
   const int nent = B * Q->k;
   auto bank = [&](const int8_t* codes, const uint16_t* rs, const uint16_t* cf, int rows, int cols, const float* x,
                   int xdiv, float* yb, int epi, bool first) -> int {

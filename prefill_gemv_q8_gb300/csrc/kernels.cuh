@@ -50,8 +50,9 @@ struct GvParams {
 };
 
 // scale == 0: no scale; gemma != 0: norm weights used as 1 + gamma
+// (zero: nzero <= 256 words cleared by the launch, e.g. a later launch's tickets)
 int launch_add_rmsnorm(float* h, const float* add, const float* gamma, float eps, float scale, int gemma, int B,
-                       int n, float* y, float* inv, cudaStream_t st);
+                       int n, float* y, float* inv, cudaStream_t st, unsigned* zero = nullptr, int nzero = 0);
 // n * 4 bytes of dynamic shared memory (n <= 16384)
 int launch_sandwich(const float* x, const float* w1, float* h, const float* w2, float eps, float scale, int gemma,
                     int B, int n, float* out, float* mid, float* inv1, float* inv2, const DeviceInfo& dev,
@@ -132,8 +133,21 @@ struct MoeBankArgs {
   const uint16_t* rs = nullptr;   // q8_2f bank (params unused): binary16 row scales [E][rows]
   const uint16_t* cf = nullptr;   // and column fields [E][cols]
 };
+// The MoE layer's routing, in the router launch itself (see pgq_router_kernel): the
+// selection (launch_route_topk's outputs) and the lists (launch_group's, no gather).
+// tick: RouteOut::ticks words, zero at launch (the launch leaves them zero).
+struct RouteOut {
+  static constexpr int ticks = 64 / 8 + 1;   // position groups of PGQ_PASS_BMAX, then one
+  int k, renorm;
+  int32_t* sel;
+  float* w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* entries;
+  unsigned* tick;
+};
 int launch_router(const float* R, const float* n, int B, int E, int cols, float* logits, const DeviceInfo& dev,
-                  cudaStream_t st);
+                  cudaStream_t st, const RouteOut* route = nullptr);
 int launch_route_topk(const float* logits, int B, int E, int k, int renorm, int32_t* sel, float* w, cudaStream_t st);
 int launch_group(const int32_t* sel, int n, int E, int32_t* counts, int32_t* offsets, int32_t* entries,
                  const float* x, int xcols, int xdiv, float* xg, cudaStream_t st);

@@ -26,9 +26,25 @@ constexpr int RT_WARPS = 8;
 constexpr int RT_POS = 8;
 constexpr int RT_UNROLL = 7;   // router row float4 per lane loaded ahead (2688 columns: 21 = 3 rounds)
 
+struct RouteArgs {   // the routing tail of the MoE layer's router launch
+  int k, renorm;
+  int32_t* sel;
+  float* w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* entries;
+  unsigned* tick;   // [gridDim.y + 1], zero at launch: per position group, then all groups
+};
+__device__ void group_block(const int32_t* __restrict__ sel, int n, int E, int32_t* __restrict__ counts,
+                            int32_t* __restrict__ offsets, int32_t* __restrict__ entries, int* sh);
+__device__ __forceinline__ void route_topk_warp(const float* __restrict__ l, int E, int k, int renorm,
+                                                int32_t* __restrict__ sel_row, float* __restrict__ w_row, int* s_row,
+                                                int lane);
+
+template <bool ROUTE>
 __global__ void __launch_bounds__(RT_WARPS * 32)
 pgq_router_kernel(const float* __restrict__ R, const float* __restrict__ n, int B, int E, int cols,
-              float* __restrict__ logits) {
+              float* __restrict__ logits, RouteArgs ra) {
   extern __shared__ __align__(16) float xs[];   // [RT_POS][cols]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * RT_WARPS + warp;
@@ -51,8 +67,7 @@ pgq_router_kernel(const float* __restrict__ R, const float* __restrict__ n, int 
   for (int b = 0; b < RT_POS; ++b) acc[b] = 0.f;
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
-  if (e >= E) return;
-  for (int c0 = 0; c0 < c4n; c0 += 32 * RT_UNROLL) {
+  for (int c0 = 0; e < E && c0 < c4n; c0 += 32 * RT_UNROLL) {
     float4 w[RT_UNROLL];
 #pragma unroll
     for (int u = 0; u < RT_UNROLL; ++u) {
@@ -76,7 +91,36 @@ pgq_router_kernel(const float* __restrict__ R, const float* __restrict__ n, int 
 #pragma unroll
   for (int b = 0; b < RT_POS; ++b) {
     const float t = warp_sum(acc[b]);
-    if (lane == 0 && b < nb) logits[(size_t)(b0 + b) * E + e] = t;
+    if (lane == 0 && b < nb && e < E) logits[(size_t)(b0 + b) * E + e] = t;
+  }
+  if constexpr (ROUTE) {
+    // The last block of this position group to finish (a ticket, no waiting) selects
+    // for the group's positions, one warp each; the last group to finish forms the
+    // per-expert lists.  Stores, then a fence, then the ticket; the reader fences after
+    // it and reads from L2.
+    __shared__ int s_last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      s_last = atomicAdd(ra.tick + blockIdx.y, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (warp < nb)
+      route_topk_warp(logits + (size_t)(b0 + warp) * E, E, ra.k, ra.renorm, ra.sel + (size_t)(b0 + warp) * ra.k,
+                      ra.w + (size_t)(b0 + warp) * ra.k, nullptr, lane);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      ra.tick[blockIdx.y] = 0u;   // every block of the group has counted
+      s_last = atomicAdd(ra.tick + gridDim.y, 1u) == gridDim.y - 1;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    group_block(ra.sel, B * ra.k, E, ra.counts, ra.offsets, ra.entries, reinterpret_cast<int*>(xs));
+    if (threadIdx.x == 0) ra.tick[gridDim.y] = 0u;
   }
 }
 
@@ -86,17 +130,17 @@ pgq_router_kernel(const float* __restrict__ R, const float* __restrict__ n, int 
 // of the logits is the order of the probabilities — then w = p (or p / Σp).
 constexpr int RK_MAXV = 8;   // E <= 256
 
-__global__ void pgq_route_topk_kernel(const float* __restrict__ logits, int B, int E, int k, int renorm,
-                                  int32_t* __restrict__ sel, float* __restrict__ wout) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  if (warp >= B) return;
-  const float* l = logits + (size_t)warp * E;
+// One warp: the selection of one position (logits row l) into sel_row[0..k) and
+// w_row[0..k) (and s_row, when given: a shared-memory copy of the selection).
+__device__ __forceinline__ void route_topk_warp(const float* __restrict__ l, int E, int k, int renorm,
+                                                int32_t* __restrict__ sel_row, float* __restrict__ w_row, int* s_row,
+                                                int lane) {
   float v[RK_MAXV];
   float m = -INFINITY;
 #pragma unroll
   for (int i = 0; i < RK_MAXV; ++i) {
     const int e = lane + 32 * i;
-    const float x = e < E ? l[e] : -INFINITY;
+    const float x = e < E ? __ldcg(l + e) : -INFINITY;
     v[i] = isnan(x) ? -INFINITY : x;   // a NaN logit is never preferred
     m = fmaxf(m, v[i]);
   }
@@ -136,7 +180,10 @@ __global__ void pgq_route_topk_kernel(const float* __restrict__ logits, int B, i
     for (int i = 0; i < RK_MAXV; ++i)
       if (lane + 32 * i == bi) taken[i] = true;
     if (lane == s) psel = expf(bv - m) / sum;
-    if (lane == 0) sel[(size_t)warp * k + s] = bi;
+    if (lane == 0) {
+      sel_row[s] = bi;
+      if (s_row) s_row[s] = bi;
+    }
   }
   float den = 1.f;
   if (renorm) {
@@ -146,7 +193,15 @@ __global__ void pgq_route_topk_kernel(const float* __restrict__ logits, int B, i
     for (int s = 0; s < k; ++s) acc += __shfl_sync(0xffffffffu, t, s);
     den = acc;
   }
-  if (lane < k) wout[(size_t)warp * k + lane] = psel / den;
+  if (lane < k) w_row[lane] = psel / den;
+}
+
+__global__ void pgq_route_topk_kernel(const float* __restrict__ logits, int B, int E, int k, int renorm,
+                                  int32_t* __restrict__ sel, float* __restrict__ wout) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (warp >= B) return;
+  route_topk_warp(logits + (size_t)warp * E, E, k, renorm, sel + (size_t)warp * k, wout + (size_t)warp * k, nullptr,
+                  lane);
 }
 
 // ------------------------------------------------------------------ grouping
@@ -201,6 +256,84 @@ pgq_group_kernel(const int32_t* __restrict__ sel, int n, int E, int32_t* __restr
       xg[q] = x[(size_t)(entries[i] / xdiv) * xcols + c];
     }
   }
+}
+
+// The lists of pgq_group_kernel (no gather) by one block of RT_WARPS warps, without a
+// serial scan: entry j's rank among expert e's entries is the count of e in the
+// 32-entry chunks before j's (a per-chunk count table, made exclusive per expert)
+// plus the lanes of j's chunk below j with the same e (__match_any_sync).  n <= 2048,
+// E <= RT_WARPS·32; sh holds route_group_smem(n, E) bytes.
+size_t route_group_smem(int n, int E) {
+  const int nch = (n + 31) / 32;
+  return (size_t)n * 4 + (size_t)(E + 1) * 4 + RT_WARPS * 4 + (size_t)((n + 1) & ~1) * 2 + (size_t)nch * E * 2;
+}
+
+__device__ void group_block(const int32_t* __restrict__ sel, int n, int E, int32_t* __restrict__ counts,
+                            int32_t* __restrict__ offsets, int32_t* __restrict__ entries, int* sh) {
+  constexpr int NT = RT_WARPS * 32;
+  const int nch = (n + 31) / 32;
+  int* s_sel = sh;                                           // [n]
+  int* s_off = s_sel + n;                                    // [E + 1]
+  int* s_wt = s_off + E + 1;                                 // [RT_WARPS]
+  uint16_t* s_rk = reinterpret_cast<uint16_t*>(s_wt + RT_WARPS);   // [n] rank within the chunk
+  uint16_t* s_tab = s_rk + ((n + 1) & ~1);                   // [nch][E] counts, then bases
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < n; i += NT) s_sel[i] = __ldcg(sel + i);
+  for (int i = tid; i < nch * E; i += NT) s_tab[i] = 0;
+  __syncthreads();
+  for (int c = warp; c < nch; c += RT_WARPS) {
+    const int j = c * 32 + lane;
+    const int e = j < n ? s_sel[j] : -1;
+    const unsigned same = __match_any_sync(0xffffffffu, e);
+    const unsigned below = same & ((1u << lane) - 1u);
+    if (j < n) s_rk[j] = (uint16_t)__popc(below);
+    if (e >= 0 && e < E && below == 0u) s_tab[c * E + e] = (uint16_t)__popc(same);
+  }
+  __syncthreads();
+  int tot = 0;   // (thread e: expert e's entries)
+  if (tid < E) {
+    for (int c = 0; c < nch; ++c) {
+      const int t = s_tab[c * E + tid];
+      s_tab[c * E + tid] = (uint16_t)tot;
+      tot += t;
+    }
+  }
+  // offsets: exclusive scan of the totals over the experts (warp scans, then the warps')
+  int inc = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += v;
+  }
+  if (lane == 31) s_wt[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int v = lane < RT_WARPS ? s_wt[lane] : 0;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += u;
+    }
+    if (lane < RT_WARPS) s_wt[lane] = x - v;   // the warps before
+  }
+  __syncthreads();
+  if (tid < E) {
+    const int off = s_wt[warp] + inc - tot;
+    s_off[tid] = off;
+    counts[tid] = tot;
+    offsets[tid] = off;
+    if (tid == E - 1) {
+      s_off[E] = off + tot;
+      offsets[E] = off + tot;
+    }
+  }
+  __syncthreads();
+  for (int j = tid; j < n; j += NT) {
+    const int e = s_sel[j];
+    if (e >= 0 && e < E) entries[s_off[e] + s_tab[(j >> 5) * E + e] + s_rk[j]] = j;
+  }
+  for (int i = s_off[E] + tid; i < n; i += NT) entries[i] = -1;
 }
 
 // ------------------------------------------------------------------ expert bank
@@ -467,14 +600,26 @@ int bank_blocks_per_sm(int device, size_t smem) {
 }  // namespace
 
 int launch_router(const float* R, const float* n, int B, int E, int cols, float* logits, const DeviceInfo& dev,
-                  cudaStream_t st) {
+                  cudaStream_t st, const RouteOut* route) {
   if (cols % 4 != 0) return set_error(PGQ_EUNSUPPORTED, "router: cols=%d not a multiple of 4", cols);
-  const size_t smem = (size_t)RT_POS * cols * sizeof(float);
+  size_t smem = (size_t)RT_POS * cols * sizeof(float);
+  RouteArgs ra{};
+  if (route) {
+    if (E > 32 * RK_MAXV || route->k > 32 || B * route->k > 64 * 32)
+      return set_error(PGQ_EUNSUPPORTED, "route: E=%d, k=%d or B=%d too large", E, route->k, B);
+    smem = std::max(smem, route_group_smem(B * route->k, E));
+    ra = RouteArgs{route->k, route->renorm, route->sel, route->w, route->counts, route->offsets, route->entries,
+                   route->tick};
+  }
   if (smem > dev.smem_optin) return set_error(PGQ_EUNSUPPORTED, "router: %zu bytes of shared memory", smem);
-  if (cudaError_t e = moe_allow_smem(reinterpret_cast<const void*>(pgq_router_kernel), dev.device, smem); e != cudaSuccess)
-    return cuda_status(e);
+  const void* fn = route ? reinterpret_cast<const void*>(pgq_router_kernel<true>)
+                         : reinterpret_cast<const void*>(pgq_router_kernel<false>);
+  if (cudaError_t e = moe_allow_smem(fn, dev.device, smem); e != cudaSuccess) return cuda_status(e);
   dim3 grid((E + RT_WARPS - 1) / RT_WARPS, (B + RT_POS - 1) / RT_POS);
-  pgq_router_kernel<<<grid, RT_WARPS * 32, smem, st>>>(R, n, B, E, cols, logits);
+  if (route)
+    pgq_router_kernel<true><<<grid, RT_WARPS * 32, smem, st>>>(R, n, B, E, cols, logits, ra);
+  else
+    pgq_router_kernel<false><<<grid, RT_WARPS * 32, smem, st>>>(R, n, B, E, cols, logits, ra);
   return cuda_status(cudaGetLastError());
 }
 

@@ -63,8 +63,11 @@ __device__ __forceinline__ float norm_row(float4* h4, const float4* a4, const fl
 
 __global__ void __launch_bounds__(NORM_THREADS)
 pgq_add_rmsnorm_kernel(float* __restrict__ h, const float* __restrict__ add, const float* __restrict__ gamma,
-                       float eps, float scale, int gemma, int n, float* __restrict__ y, float* __restrict__ inv_out) {
+                       float eps, float scale, int gemma, int n, float* __restrict__ y, float* __restrict__ inv_out,
+                       unsigned* __restrict__ zero, int nzero) {
   __shared__ float red[NORM_THREADS / 32];
+  // (words a later launch of the caller's needs cleared: the MoE layer's routing tickets)
+  if (blockIdx.x == 0 && (int)threadIdx.x < nzero) zero[threadIdx.x] = 0u;
   const size_t base = (size_t)blockIdx.x * n;
   const float inv = norm_row(reinterpret_cast<float4*>(h + base),
                              add ? reinterpret_cast<const float4*>(add + base) : nullptr,
@@ -145,8 +148,9 @@ pgq_argmax_kernel(const float* __restrict__ logits, int V, int32_t* __restrict__
 
 // ------------------------------------------------------------------ launchers
 int launch_add_rmsnorm(float* h, const float* add, const float* gamma, float eps, float scale, int gemma, int B,
-                       int n, float* y, float* inv, cudaStream_t st) {
-  pgq_add_rmsnorm_kernel<<<B, NORM_THREADS, 0, st>>>(h, add, gamma, eps, scale, gemma, n, y, inv);
+                       int n, float* y, float* inv, cudaStream_t st, unsigned* zero, int nzero) {
+  if (nzero > NORM_THREADS) return set_error(PGQ_EINVAL, "add_rmsnorm: %d words to clear", nzero);
+  pgq_add_rmsnorm_kernel<<<B, NORM_THREADS, 0, st>>>(h, add, gamma, eps, scale, gemma, n, y, inv, zero, nzero);
   return cuda_status(cudaGetLastError());
 }
 
