@@ -53,6 +53,10 @@ constexpr int PS_XP_WARP = 14;     // input-slice producer
 constexpr int PS_NA = 4;           // A buffers in tensor memory
 constexpr int PS_WST_MAX = 10;     // weight ring stages (at most; set by the shared memory left)
 constexpr int PS_XST = 3;          // input ring stages (4 measured no faster)
+// A grouped bank cuts the same input-ring bytes into stages of the largest expert's
+// 16-row boxes (4 KB per box: two 64-column halves), up to PS_XST_MAX of them: 12
+// stages when no expert has more than 16 entries, 3 when one has 64.
+constexpr int PS_XST_MAX = 12;
 constexpr int PS_CODES_BYTES = TC_BM * TC_BK;                 // 16 KB
 constexpr int PS_PARAMS_BYTES = TC_BM * 16;                   // 4 (scale, offset) pairs per row
 constexpr int PS_W_BYTES = PS_CODES_BYTES + PS_PARAMS_BYTES;  // 18 KB, a multiple of 1 KB
@@ -400,18 +404,17 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int Bp = P.Bp, WST = P.wst, G = P.G;
   constexpr int WB = MOE ? PS_WM_BYTES : PS_W_BYTES;   // weight-ring stage bytes
-  const int xst_bytes = 2 * Bp * 128;   // two 64-column halves of an input slice
   uint8_t* wring = smem;
   uint8_t* xring = wring + WST * WB;
-  float* s_acc = reinterpret_cast<float*>(xring + PS_XST * xst_bytes);   // [Bp][128]
+  float* s_acc = reinterpret_cast<float*>(xring + PS_XST * 2 * Bp * 128);   // [Bp][128]
   float* fixb = s_acc + Bp * TC_BM;                                      // [Bp][128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(fixb + Bp * TC_BM);
   enum {
     FULL_W = 0,
     EMPTY_W = PS_WST_MAX,
     FULL_X = 2 * PS_WST_MAX,
-    EMPTY_X = FULL_X + PS_XST,
-    AFULL = EMPTY_X + PS_XST,
+    EMPTY_X = FULL_X + PS_XST_MAX,
+    AFULL = EMPTY_X + PS_XST_MAX,
     AEMPTY = AFULL + PS_NA,
     ACCF = AEMPTY + PS_NA,
     ACCE = ACCF + 2,
@@ -422,7 +425,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   __shared__ float s_xinv[64], s_inv[64], s_sc[64];
   __shared__ int s_mcnt[MOE ? PS_MOE_EMAX : 1], s_moff[MOE ? PS_MOE_EMAX : 1], s_ent[MOE ? 64 : 1];
-  __shared__ int s_live[MOE ? PS_MOE_EMAX : 1], s_nlive;
+  __shared__ int s_live[MOE ? PS_MOE_EMAX : 1], s_nlive, s_xbox;
   __shared__ float2 s_st[2][64];
 
   auto bar = [&](int i) { return tc::smem_addr(bars + i); };
@@ -434,7 +437,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
       tc::mbar_init(bar(FULL_W + s), 1);
       tc::mbar_init(bar(EMPTY_W + s), PS_DQ_WARPS);
     }
-    for (int s = 0; s < PS_XST; ++s) {
+    for (int s = 0; s < PS_XST_MAX; ++s) {
       tc::mbar_init(bar(FULL_X + s), 1);
       tc::mbar_init(bar(EMPTY_X + s), 1);
     }
@@ -472,18 +475,29 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
   const int tpe = MOE ? P.tpe : 1;
   if constexpr (MOE) {
     if (warp == 0) {
-      int base = 0;
+      int base = 0, mx = 0;
       for (int e0 = 0; e0 < P.E; e0 += 32) {
         const int e = e0 + lane;
         const bool live = e < P.E && s_mcnt[e] > 0;
         const unsigned m = __ballot_sync(0xffffffffu, live);
         if (live) s_live[base + __popc(m & ((1u << lane) - 1u))] = e;
         base += __popc(m);
+        if (live) mx = max(mx, s_mcnt[e]);
       }
-      if (lane == 0) s_nlive = base;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      if (lane == 0) {
+        s_nlive = base;
+        s_xbox = max(1, (mx + 15) >> 4);   // 16-row boxes of the largest expert (<= 4)
+      }
     }
     __syncthreads();
   }
+  // The input ring: XST stages of two 64-column halves of xhalf bytes each, in the
+  // PS_XST·2·Bp·128 bytes before s_acc
+  const int xhalf = MOE ? s_xbox * 16 * 128 : Bp * 128;
+  const int xst_bytes = 2 * xhalf;
+  const int XST = MOE ? min(PS_XST_MAX, (PS_XST * 2 * Bp * 128) / xst_bytes) : PS_XST;
   auto skipped = [&](int) -> bool { return false; };
   auto expert_of = [&](int tile) -> int {   // grouped bank: the expert of list tile `tile`
     if constexpr (MOE) return s_live[tile / tpe];
@@ -591,7 +605,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
               tc::mbar_expect_tx(bar(FULL_X + s), (uint32_t)(nbox * 2 * 16 * 128));
               for (int i = 0; i < nbox; ++i) {
                 tc::tma_load_2d(tc::smem_addr(st + i * 16 * 128), xm, k * TC_BK, xrow + 16 * i, bar(FULL_X + s));
-                tc::tma_load_2d(tc::smem_addr(st + Bp * 128 + i * 16 * 128), xm, k * TC_BK + 64, xrow + 16 * i,
+                tc::tma_load_2d(tc::smem_addr(st + xhalf + i * 16 * 128), xm, k * TC_BK + 64, xrow + 16 * i,
                                 bar(FULL_X + s));
               }
             } else {
@@ -602,24 +616,24 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
           }
           __syncwarp();
           ++issued;
-          if (++s == PS_XST) { s = 0; ph ^= 1; }
+          if (++s == XST) { s = 0; ph ^= 1; }
         }
         if (++k == F.ks) { k = 0; ++tile; }
       }
     }
     if (*abort_flag && lane == 0) {
-      const int n = issued < PS_XST ? issued : PS_XST;
+      const int n = issued < XST ? issued : XST;
       int ss = s;
       uint32_t pp = ph;
       for (int i = 0; i < n; ++i) {
-        if (--ss < 0) { ss = PS_XST - 1; pp ^= 1; }
+        if (--ss < 0) { ss = XST - 1; pp ^= 1; }
         W.drain(bar(FULL_X + ss), pp);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t idesc = tc::idesc_f16_f32(TC_BM, Bp);
-    const uint64_t bstep = (uint64_t)((Bp * 128) >> 4);   // second 64-column half of the slice
+    const uint64_t bstep = (uint64_t)(xhalf >> 4);   // second 64-column half of the slice
     int sx = 0, a = 0, t = 0, mtile = 0;
     uint32_t phx = 0, pha = 0, pht = 0;
     bool any = false, stop = false;
@@ -675,7 +689,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
         any = true;
         if (last) ++mtile;
         if (last && ++t == 2) { t = 0; pht ^= 1; }
-        if (++sx == PS_XST) { sx = 0; phx ^= 1; }
+        if (++sx == XST) { sx = 0; phx ^= 1; }
         if (++a == PS_NA) { a = 0; pha ^= 1; }
         if (++k == F.ks) { k = 0; ++tile; }
       }
