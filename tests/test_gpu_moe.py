@@ -136,7 +136,7 @@ def test_combine_rmsnorm():
     check_rel(host(y), y_ref, NORM_TOL + 1e-6, "y", abs_=1e-30)
 
 
-def _layer_check(W_np, router, h0, g1, g2, k, taps, h_after, y, entries_sample=None):
+def _layer_check(W_np, router, h0, g1, g2, k, taps, h_after, y, entries_sample=None, renorm=False):
     """Stage-wise check of a MoE layer from its workspace taps."""
     t = {kk: host(v) for kk, v in taps.items()}
     E = router.shape[0]
@@ -145,7 +145,7 @@ def _layer_check(W_np, router, h0, g1, g2, k, taps, h_after, y, entries_sample=N
     lg, e_lg = oracle.project(router, t["n"])
     check_proj(t["logits"], lg, e_lg, what="logits")
     # selection from the kernel's own f32 logits: bit-exact (R12-i)
-    sel_ref, w_ref = oracle.route(t["logits"], k)
+    sel_ref, w_ref = oracle.route(t["logits"], k, renorm)
     assert np.array_equal(t["sel"], sel_ref)
     check_rel(t["w"], w_ref, 1e-5, "w")
     c, o, en = oracle.group(t["sel"], E)
@@ -187,6 +187,27 @@ def test_moe_layer_small(E, H, I, B, k):
     assert pgq.last_device_status(ws) == pgq.OK
     taps = pgq.moe_layer_taps(Wd, ws, B)
     _layer_check((up, down), router, h0, g1, g2, k, taps, h, y)
+
+
+@pytest.mark.parametrize("E,B,k,renorm", [(256, 64, 8, True), (40, 7, 32, False), (1, 3, 1, True)])
+def test_moe_layer_routing_extremes(E, B, k, renorm):
+    """The routing in the router launch at its limits: 256 experts and 8 full position
+    groups; a partial position group with k = 32 (2048-entry ceiling: 224 entries);
+    a single expert.  Selection and lists bit-exact, weights renormalised or not."""
+    H, I = 128, 64
+    router, up, down = synth.moe_layer(979, E, H, I)
+    h0 = synth.normal((B, H), 1.0, 979, synth.T_X)
+    g1, g2 = synth.gamma(H, 979), synth.gamma(H, 979, synth.T_GAMMA2)
+    Wd = pgq.MoeWeights(dev(router), dev(up[0]), dev(up[1]), dev(down[0]), dev(down[1]), k, renorm)
+    h = dev(h0)
+    ws = torch.full((pgq.moe_layer_workspace(Wd, B).numel(),), 0x55, dtype=torch.uint8, device="cuda")
+    for _ in range(2):   # the second call starts from the tickets the first one left
+        h = dev(h0)
+        y, ws = pgq.moe_prefill_layer(Wd, h, dev(g1), dev(g2), 1e-6, workspace=ws)
+        assert pgq.last_device_status(ws) == pgq.OK
+        taps = pgq.moe_layer_taps(Wd, ws, B)
+        js = range(0, B * k, max(1, B * k // 48))
+        _layer_check((up, down), router, h0, g1, g2, k, taps, h, y, entries_sample=js, renorm=renorm)
 
 
 def test_moe_layer_full_size_sampled():
