@@ -189,11 +189,14 @@ def test_moe_layer_small(E, H, I, B, k):
     _layer_check((up, down), router, h0, g1, g2, k, taps, h, y)
 
 
-@pytest.mark.parametrize("E,B,k,renorm", [(256, 64, 8, True), (40, 7, 32, False), (1, 3, 1, True)])
+@pytest.mark.parametrize("E,B,k,renorm", [(256, 64, 8, True), (40, 7, 32, False), (1, 3, 1, True),
+                                         (1, 64, 1, False), (2, 64, 1, False), (4, 64, 2, True)])
 def test_moe_layer_routing_extremes(E, B, k, renorm):
     """The routing in the router launch at its limits: 256 experts and 8 full position
     groups; a partial position group with k = 32 (2048-entry ceiling: 224 entries);
-    a single expert.  Selection and lists bit-exact, weights renormalised or not."""
+    a single expert.  Then crowded experts (64 entries for one expert; about 32; about
+    32 of 128 entries), which cut the grouped banks' input ring into 3, 4 or 6 stages
+    of 4, 3 or 2 boxes.  Selection and lists bit-exact, weights renormalised or not."""
     H, I = 128, 64
     router, up, down = synth.moe_layer(979, E, H, I)
     h0 = synth.normal((B, H), 1.0, 979, synth.T_X)
