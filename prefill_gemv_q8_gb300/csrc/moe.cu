@@ -2,7 +2,8 @@
 // softmax top-k with lower-id ties, per-expert grouping of the pass's (position,
 // slot) entries, the grouped q8 expert projections (each chosen expert's weights
 // streamed once for all of its entries) and the weighted combine fused into
-// add + RMSNorm.
+// add + RMSNorm.  In the MoE layer the top-k and the grouping run in the router
+// launch's tail (the last block of each position group, then the last group).
 //
 // Prior art: nemotron_prefill.rs `pb_f32_mm` (router), `pb_route` (top-k, ties to
 // the lowest lane), `pb_lists` (per-expert ascending entry lists), `pb_q8_bank`

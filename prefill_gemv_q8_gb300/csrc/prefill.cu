@@ -28,6 +28,11 @@
 //   (deterministic) and writes the tile.  Every final tile also leaves per-position
 //   Σy² and max|γ·y| for the next phase's RMSNorm and scale, so the input of the next
 //   phase is made by all blocks at once, each a slice of columns.
+// * The same kernel runs a grouped expert bank (one phase over [E][rows][cols]): the
+//   items run over the tiles of the experts that have entries, an expert's entries are
+//   the MMA's N columns, (scale, offset) rows that are not 16-byte strided come by
+//   tensor copies of 4-row groups, and the input ring's stages follow the largest
+//   expert's entry count.
 // * Every wait is bounded (%globaltimer); on expiry the block records PGQ_ETIMEOUT in
 //   the workspace status word, every role leaves its loop (the others notice the
 //   status word), copies and MMAs in flight are drained with bounded waits and tensor
