@@ -834,23 +834,40 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
         float ss = 0.f, mx = 0.f;
         if (b < P.B) {
           const int lo = half ? nt / 2 : 0, hi = half ? nt : nt / 2;
-          // 8 loads in flight at a time, added in tile order
           const float2* const sp = P.stats + (size_t)prev * P.maxtiles * 64 + b;
-          int tt = lo;
-          for (; tt + 8 <= hi; tt += 8) {
-            float2 v[8];
+          if constexpr (!MOE) {
+            // 16 loads in flight at a time, added in tile order (a short last group is
+            // padded with zeros: + 0 and max with 0 leave Σy² and max|γ·y| as they are)
+            for (int tt = lo; tt < hi; tt += 16) {
+              float2 v[16];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = __ldcg(sp + (size_t)(tt + i) * 64);
+              for (int i = 0; i < 16; ++i)
+                v[i] = tt + i < hi ? __ldcg(sp + (size_t)(tt + i) * 64) : make_float2(0.f, 0.f);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              ss += v[i].x;
-              mx = fmaxf(mx, v[i].y);
+              for (int i = 0; i < 16; ++i) {
+                ss += v[i].x;
+                mx = fmaxf(mx, v[i].y);
+              }
             }
-          }
-          for (; tt < hi; ++tt) {
-            const float2 v = __ldcg(sp + (size_t)tt * 64);
-            ss += v.x;
-            mx = fmaxf(mx, v.y);
+          } else {
+            // (a grouped bank never makes an input: this form, 8 loads at a time, is the
+            // one its build measured fastest with)
+            int tt = lo;
+            for (; tt + 8 <= hi; tt += 8) {
+              float2 v[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) v[i] = __ldcg(sp + (size_t)(tt + i) * 64);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                ss += v[i].x;
+                mx = fmaxf(mx, v[i].y);
+              }
+            }
+            for (; tt < hi; ++tt) {
+              const float2 v = __ldcg(sp + (size_t)tt * 64);
+              ss += v.x;
+              mx = fmaxf(mx, v.y);
+            }
           }
         }
         s_st[half][b] = make_float2(ss, mx);
