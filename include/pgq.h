@@ -464,9 +464,12 @@ int pgq_moe_combine_rmsnorm(float* h, const float* o, const float* eo, const flo
  *   n = rms(h)·gamma1; logits = R·n; (sel, w) = softmax top-k; grouping;
  *   u_j = relu²(W_up[sel_j] · n[j / k]); eo_j = W_down[sel_j] · u_j;
  *   h += Σ_s w·eo; y = rms(h)·gamma2.
- * Seven launches.  workspace: pgq_moe_layer_workspace_bytes(layer, B) bytes, 256-byte
- * aligned; afterwards it holds n, logits, sel, w, counts, offsets, entries, u and eo
- * at the byte offsets pgq_moe_layer_layout() reports (9 entries). */
+ * Seven launches: add + RMSNorm; the router, whose tail makes the selection and the
+ * per-expert lists (E <= 256, k <= 32); per bank the gathered binary16 input and the
+ * grouped projection; the combine + RMSNorm.  workspace:
+ * pgq_moe_layer_workspace_bytes(layer, B) bytes, 256-byte aligned; afterwards it holds
+ * n, logits, sel, w, counts, offsets, entries, u and eo at the byte offsets
+ * pgq_moe_layer_layout() reports (9 entries). */
 typedef struct {
   const float* router;          /* f32 [E][hidden] */
   const int8_t* up_codes;       /* int8 [E][inter][hidden] */
