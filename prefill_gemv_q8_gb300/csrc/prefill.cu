@@ -25,7 +25,10 @@
 //   Weight streaming never waits for the phase boundary: the ring keeps filling.
 // * A tile cut between blocks: the other blocks publish f32 partials; the block
 //   holding the tile's first k-steps (it reaches them last) adds them in block order
-//   (deterministic) and writes the tile.  Every final tile also leaves per-position
+//   (deterministic) and writes the tile; where three or more blocks share a tile, the
+//   second takes the upper half of the positions (it publishes its lower half and the
+//   first block its upper half, and each adds the others in the same order).  Every
+//   final tile also leaves per-position
 //   Σy² and max|γ·y| for the next phase's RMSNorm and scale, so the input of the next
 //   phase is made by all blocks at once, each a slice of columns.
 // * The same kernel runs a grouped expert bank (one phase over [E][rows][cols]): the
@@ -103,6 +106,7 @@ struct PsPhase {
   int xk;                    // input buffer
   int stats_job;             // job whose final tiles report Σy², max|γ·y| (-1: none)
   int src_job;               // phases after the first: the previous phase's job that is the input
+  int nsplit;                // tiles whose fix-up two blocks share (each counts once in done)
   const float* next_gamma;   // γ the next phase normalises with (max|γ·y|), or null
   const float* gamma;        // this phase's input: RMSNorm weight, or null (scale only)
   float* tap;                // f32 copy of the normalised input, or null
@@ -123,6 +127,9 @@ struct PsParams {
   float eps;
   int nph, B, Bp, G, maxseg, maxtiles, wst;
   int f2;                    // every matrix of the launch is q8_2f
+  // positions [0, bsplit) of a tile shared by three or more blocks are fixed up by its
+  // first block, [bsplit, B) by its second (32, or 0: no tile is split)
+  int bsplit;
   // test hook (pgq_debug_stall): the wait for the first phase's tiles asks for one
   // tile more than there are, so it runs out and every block takes its abort path
   int stall;
@@ -152,9 +159,9 @@ __device__ unsigned long long g_pt[1024 * PS_MAXPH * PT_EV];
 #endif
 
 // ------------------------------------------------------------------ schedule
-__device__ __forceinline__ int item_begin(int c, int G, int T) { return (int)((long long)c * T / G); }
+__host__ __device__ __forceinline__ int item_begin(int c, int G, int T) { return (int)((long long)c * T / G); }
 
-__device__ __forceinline__ int cta_of_item(int i, int G, int T) {
+__host__ __device__ __forceinline__ int cta_of_item(int i, int G, int T) {
   int c = (int)(((long long)i * G) / T);
   if (c >= G) c = G - 1;
   while (c + 1 < G && item_begin(c + 1, G, T) <= i) ++c;
@@ -379,9 +386,11 @@ __device__ __forceinline__ void out_rows(float4* acc4, int nvec, int et, int epi
 
 // Per-position statistics of a final tile (values in acc4, rows a multiple of 4):
 // out[b] = (Σ over the tile's rows of y², max |γ·y|).  Lanes hold rows lane·4..+3 of
-// positions warp + 4k; the lane sums are combined by a butterfly (xor 16, 8, 4, 2, 1).
+// positions warp + 4k; the lane sums are combined by a butterfly (xor 16, 8, 4, 2, 1),
+// the same tree for every position.  LIMIT: only positions below npos are written.
+template <bool LIMIT>
 __device__ __forceinline__ void tile_stats(const float4* acc4, int nvec, int et, int rows, int row0,
-                                           const float* gam, float2* out) {
+                                           const float* gam, float2* out, int npos) {
   const int lane = et & 31, we = et >> 5;
   const int rr = row0 + lane * 4;
   float4 g = make_float4(1.f, 1.f, 1.f, 1.f);
@@ -400,7 +409,7 @@ __device__ __forceinline__ void tile_stats(const float4* acc4, int nvec, int et,
   }
   const float tss = reduce_scatter<PS_OUT_K>(ss, lane);
   const float tmx = reduce_scatter_max<PS_OUT_K>(mx, lane);
-  if ((lane & 1) == 0) out[we + 4 * (lane >> 1)] = make_float2(tss, tmx);
+  if ((lane & 1) == 0 && (!LIMIT || we + 4 * (lane >> 1) < npos)) out[we + 4 * (lane >> 1)] = make_float2(tss, tmx);
 }
 
 template <bool MOE>
@@ -823,7 +832,11 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
       const PsPhase& F = P.ph[p];
       bool ok = true;
       if (!MOE && et == 0) PTRACE(p, 4);
-      if (et == 0) ok = W.count(P.done + (p - 1), (unsigned)P.ph[p - 1].ntiles + (p == 1 ? (unsigned)P.stall : 0u));
+      if (et == 0) {
+        unsigned need = (unsigned)P.ph[p - 1].ntiles;
+        if constexpr (!MOE) need += (unsigned)P.ph[p - 1].nsplit;
+        ok = W.count(P.done + (p - 1), need + (p == 1 ? (unsigned)P.stall : 0u));
+      }
       if (!MOE && et == 0) PTRACE(p, 5);
       if (!epi_all(ok)) return false;
       const PsJob& S = P.job[F.src_job];
@@ -984,7 +997,16 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
         }
         const int c_first = whole ? cta : cta_of_item(tile * F.ks, G, items_of(p));
         const int c_last = whole ? cta : cta_of_item(tile_end - 1, G, items_of(p));
-        const bool contributor = cta != c_first;
+        // A dense tile of three or more blocks is fixed up by two: its second block (the
+        // helper, whose whole range lies in the tile) takes positions [bsplit, B), its
+        // first [0, bsplit).  Each publishes the other's half of its accumulator, and
+        // each adds its sources in the unsplit order (the helper starts from its own
+        // accumulator plus the first block's: one addition, which commutes exactly).
+        const bool split = !MOE && P.bsplit > 0 && c_last - c_first >= 2;
+        const bool helper = split && cta == c_first + 1;
+        const bool contributor = cta != c_first && !helper;
+        const int off = helper ? P.bsplit * 32 : 0;                               // first float4 slot fixed up here
+        const int nvl = !split ? nv : (helper ? nv - off : min(nv, P.bsplit * 32));   // and the slots' count
         const bool vec_ok = ((rows & 3) == 0) && ((reinterpret_cast<uintptr_t>(J.y) & 15) == 0) &&
                             (J.epi != PGQ_EPI_ADD || (reinterpret_cast<uintptr_t>(J.residual) & 15) == 0);
         // Dense tiles: what is added to the block's own accumulator, in this order — the
@@ -1002,14 +1024,16 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
         float4* const ring4 = reinterpret_cast<float4*>(xring);
         auto issue = [&](int sidx, float4* buf) {
           if (sidx < npart) {
-            const int cc = c_first + 1 + sidx;
+            // (the helper's first source is the first block's upper half)
+            const int cc = c_first + 1 + sidx - (helper && sidx == 0 ? 1 : 0);
             const int ft = item_begin(cc, G, items_of(p)) / F.ks;
             const float4* pc = reinterpret_cast<const float4*>(
-                P.partials + (((size_t)par * G + cc) * P.maxseg + (tile - ft)) * Bp * TC_BM);
+                                   P.partials + (((size_t)par * G + cc) * P.maxseg + (tile - ft)) * Bp * TC_BM) +
+                               off;
 #pragma unroll
             for (int k = 0; k < PS_OUT_K; ++k) {
               const int i = et + 128 * k;
-              if (i < nv)
+              if (i < nvl)
                 asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_addr(buf + i)), "l"(pc + i)
                              : "memory");
             }
@@ -1018,15 +1042,15 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
             for (int k = 0; k < PS_OUT_K; ++k) {
               const int i = et + 128 * k;
               const int rr = row0 + (i & 31) * 4;
-              if (i < nv && rr < rows)
+              if (i < nvl && rr < rows)
                 asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_addr(buf + i)),
-                             "l"(J.residual + (size_t)(i >> 5) * rows + rr)
+                             "l"(J.residual + (size_t)((i + off) >> 5) * rows + rr)
                              : "memory");
             }
           }
           asm volatile("cp.async.commit_group;" ::: "memory");
         };
-        if (!MOE && nsrc > 0) {
+        if (!MOE && nsrc > 0 && !split) {
           if (npart > 0) {
             bool okc = true;
             if (et == 0) {
@@ -1045,7 +1069,8 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
         tc::fence_after_sync();
         const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + t * PS_ACC_COLS;
         // accumulator row r, scaled, into this block's partial (a contributor) or the
-        // shared transposed tile; layout [position][128 rows] in both
+        // shared transposed tile; layout [position][128 rows] in both.  A split tile's
+        // two fixers put the other's half of the positions into their partial.
         float* dst = contributor
                          ? P.partials + (((size_t)par * G + cta) * P.maxseg + (tile - first_tile)) * Bp * TC_BM
                          : s_acc;
@@ -1061,14 +1086,18 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
           }
         } else {
           // the accumulator row in two loads of 32 columns
+          // (a split tile: columns [0, 32) to the helper's partial or the first block's
+          // shared tile, columns [32, 64) the other way round)
+          float* const gpart = P.partials + (((size_t)par * G + cta) * P.maxseg + (tile - first_tile)) * Bp * TC_BM;
 #pragma unroll
           for (int c0 = 0; c0 < PS_ACC_COLS; c0 += 32) {
             if (c0 < Bp) {
+              float* const d = split && (helper == (c0 == 0)) ? gpart : dst;
               uint32_t u[32];
               tc::tmem_ld_32x32b_x32_sync(ta + c0, u);
 #pragma unroll
               for (int i = 0; i < 32; ++i)
-                if (c0 + i < Bp) dst[(c0 + i) * TC_BM + r] = __uint_as_float(u[i]) * s_xinv[c0 + i];
+                if (c0 + i < Bp) d[(c0 + i) * TC_BM + r] = __uint_as_float(u[i]) * s_xinv[c0 + i];
             }
           }
         }
@@ -1087,6 +1116,23 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
           continue;
         }
         if constexpr (!MOE) {
+          if (split) {
+            // publish this block's half, then wait for every block of the tile (the
+            // helper then acknowledges, so that the first block may clear the count)
+            unsigned* const tcnt = P.tile_cnt + (size_t)par * P.maxtiles + tile;
+            bool okc = true;
+            if (et == 0) {
+              release_add(tcnt);
+              okc = W.count(tcnt, (unsigned)npart + 1u);
+              if (okc && helper) atomicAdd(tcnt, 1u);
+            }
+            if (!epi_all(okc)) { stop = true; break; }
+            if (et == 0) {
+              PTRACE(p, 10);
+              PTSET(p, 19, helper ? 2 : 1);
+            }
+            issue(0, fix4);
+          }
           const bool two = seg_end == end;
           if (two && nsrc > 1) issue(1, ring4);
           for (int sidx = 0; sidx < nsrc; ++sidx) {
@@ -1099,11 +1145,11 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
 #pragma unroll
             for (int k = 0; k < PS_OUT_K; ++k) {
               const int i = et + 128 * k;
-              if (i < nv && (part || row0 + (i & 31) * 4 < rows)) {
+              if (i < nvl && (part || row0 + (i & 31) * 4 < rows)) {
                 const float4 u = buf[i];
-                float4 s4 = acc4[i];
+                float4 s4 = acc4[off + i];
                 s4.x += u.x; s4.y += u.y; s4.z += u.z; s4.w += u.w;
-                acc4[i] = s4;
+                acc4[off + i] = s4;
               }
             }
             const int nx = sidx + (two ? 2 : 1);
@@ -1152,14 +1198,27 @@ __global__ void __launch_bounds__(PS_THREADS, 1) pgq_prefill_pass_kernel(const _
         if (!MOE && et == 0) PTRACE(p, 11);
         const bool stats = vec_ok && j == F.stats_job;
         const __half* rs_t = (MOE && J.rs) ? J.rs + (size_t)expert_of(tile) * rows : J.rs;   // the tile's row scales
-        out_rows<MOE>(acc4, nv, et, res_fold ? PGQ_EPI_NONE : J.epi, J.y, J.residual, rows, row0, vec_ok, stats,
-                      MOE ? s_ent : nullptr, rs_t);
-        if (!MOE && et == 0) PTRACE(p, 12);
-        if (stats)
-          tile_stats(acc4, nv, et, rows, row0, F.next_gamma,
-                     P.stats + ((size_t)par * P.maxtiles + (tile - J.tile0)) * 64);
+        if constexpr (MOE) {
+          out_rows<MOE>(acc4, nv, et, J.epi, J.y, J.residual, rows, row0, vec_ok, stats, s_ent, rs_t);
+          if (stats)
+            tile_stats<false>(acc4, nv, et, rows, row0, F.next_gamma,
+                              P.stats + ((size_t)par * P.maxtiles + (tile - J.tile0)) * 64, 64);
+        } else {
+          const int boff = off >> 5;   // the first position fixed up here
+          out_rows<MOE>(acc4 + off, nvl, et, res_fold ? PGQ_EPI_NONE : J.epi, J.y + (size_t)boff * rows,
+                        J.residual ? J.residual + (size_t)boff * rows : nullptr, rows, row0, vec_ok, stats, nullptr,
+                        rs_t);
+          if (et == 0) PTRACE(p, 12);
+          if (stats)
+            tile_stats<true>(acc4 + off, nvl, et, rows, row0, F.next_gamma,
+                             P.stats + ((size_t)par * P.maxtiles + (tile - J.tile0)) * 64 + boff, nvl >> 5);
+        }
         epi_bar();   // the tile's stores are issued and the shared tile is free
         if (!MOE && et == 0) PTRACE(p, 13);
+        // a split tile's first block clears its count once the helper has seen it (the
+        // count is next used two phases later, after this phase's done count)
+        if (split && !helper && et == 0 && W.count(P.tile_cnt + (size_t)par * P.maxtiles + tile, (unsigned)npart + 2u))
+          P.tile_cnt[(size_t)par * P.maxtiles + tile] = 0u;
         if (et == 0) release_add(P.done + p);
         if (!MOE && et == 0) PTRACE(p, 7);
         if (MOE && et == 0) PTRACE(etile, 7);
@@ -1468,6 +1527,9 @@ int launch_phases(const HostPhase* hp, int nph, const float* x0, const float* ga
   std::lock_guard<std::mutex> lk(g_launch_mu);
   memset(&P, 0, sizeof(P));
   for (int k = 0; k < PS_NX; ++k) P.xh[k] = reinterpret_cast<__half*>(w + pl.off_xh[k]);
+  // a split tile's first block keeps positions [0, 32) (one of the accumulator's two
+  // 32-column loads), its helper the rest; at most 32 positions nothing is split
+  P.bsplit = (!moe && B > 32) ? 32 : 0;
   bool mapped[PS_NX] = {false, false, false, false};
   int nj = 0;
   for (int i = 0; i < nph; ++i) {
@@ -1522,6 +1584,12 @@ int launch_phases(const HostPhase* hp, int nph, const float* x0, const float* ga
     }
     F.ntiles = tb;
     F.T = tb * F.ks;
+    // the tiles that three or more blocks share (the kernel's schedule, item ranges
+    // of the G blocks over T items): two blocks fix each up, and each counts in done
+    F.nsplit = 0;
+    if (P.bsplit > 0)
+      for (int t = 0; t < F.ntiles; ++t)
+        if (cta_of_item((t + 1) * F.ks - 1, pl.G, F.T) - cta_of_item(t * F.ks, pl.G, F.T) >= 2) ++F.nsplit;
     if (!mapped[H.xk]) {
       const uint64_t xr = moe ? (uint64_t)moe->nent : (uint64_t)pl.Bp;   // a bank: the gathered rows
       if (!encode_2d(&P.xmap[H.xk], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, P.xh[H.xk], H.K, xr, (uint64_t)H.K * 2, 64,

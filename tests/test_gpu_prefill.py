@@ -110,3 +110,28 @@ def test_prefill_matches_decode_rows():
     yd = host(pgq.gemv_q8(dev(c), dev(p), dev(X)))
     ref, e = oracle.gemv_q8(c, p, X)
     check_proj(y, yd, 2 * e)
+
+
+@pytest.mark.parametrize("rows,epi", [(1024, "add"), (1024, "relu2"), (513, "none")])
+def test_prefill_split_fixup_halves_agree(rows, epi):
+    """Tiles that three or more blocks share are finished by two blocks, one per half of
+    the positions, each adding the tile's partial sums in the same block order: with the
+    two halves of the input swapped, the outputs come back swapped, bit for bit (a
+    helper that added its sources in another order would round differently)."""
+    cols, B = 4096, 64
+    c, p = synth.q8_matrix(rows, cols, 937, rows)
+    X = synth.normal((B, cols), 1.0, 937, 2)
+    swap = lambda a: np.concatenate([a[32:], a[:32]])
+    res = synth.normal((B, rows), 3.0, 937, 3) if epi == "add" else None
+    r1 = [dev(res)] if res is not None else None
+    r2 = [dev(swap(res))] if res is not None else None
+    (y1,), _ = run([(c, p)], X, epis=[epi], residuals=r1)
+    (y2,), _ = run([(c, p)], swap(X), epis=[epi], residuals=r2)
+    assert np.array_equal(y1, swap(y2))
+    ref, e = oracle.gemv_q8(c, p, X)
+    if epi == "add":
+        check_proj(y1, res + ref, e, extra=np.abs(res) * 2.0 ** -23)
+    elif epi == "relu2":
+        check_relu2(y1, ref, e)
+    else:
+        check_proj(y1, ref, e)
