@@ -349,7 +349,9 @@ def time_prefill(torch, P, steps, warmup, pk):
                      "kernel": f"pgq_prefill_pass_kernel ({P.pgq.PASS_LMAX} layers = {4 * P.pgq.PASS_LMAX} phases per "
                                f"launch, B=64; {P.persistent_launches} launches per pass)",
                      "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4),
-                     "traffic": ncu_traffic("prefill_pass_launch", PREFILL_FILES),
+                     # (the capture's figure is for a launch of PASS_LMAX layers)
+                     "traffic": ncu_traffic("prefill_pass_launch", PREFILL_FILES)
+                     if P.L % P.pgq.PASS_LMAX == 0 else None,
                      "algorithmic_bytes_per_launch": P.step_bytes // P.persistent_launches,
                      "avg_launch_ms": round(ms / P.persistent_launches, 5),
                      "timed": "CUDA-graph replay of the pass; per launch = pass / persistent launches (input kernels "
