@@ -25,12 +25,12 @@
 //   Weight streaming never waits for the phase boundary: the ring keeps filling.
 // * A tile cut between blocks: the other blocks publish f32 partials; the block
 //   holding the tile's first k-steps (it reaches them last) adds them in block order
-//   (deterministic) and writes the tile; where three or more blocks share a tile, the
-//   second takes the upper half of the positions (it publishes its lower half and the
-//   first block its upper half, and each adds the others in the same order).  Every
-//   final tile also leaves per-position
-//   Σy² and max|γ·y| for the next phase's RMSNorm and scale, so the input of the next
-//   phase is made by all blocks at once, each a slice of columns.
+//   (deterministic) and writes the tile.  Where three or more blocks share a tile
+//   and B > 32, its second block finishes positions 32..B-1 and the first block
+//   0..31: each publishes the other's half of its accumulator and adds its sources in
+//   the same order.  Every final tile also leaves per-position Σy² and max|γ·y| for
+//   the next phase's RMSNorm and scale, so the input of the next phase is made by all
+//   blocks at once, each a slice of columns.
 // * The same kernel runs a grouped expert bank (one phase over [E][rows][cols]): the
 //   items run over the tiles of the experts that have entries, an expert's entries are
 //   the MMA's N columns, (scale, offset) rows that are not 16-byte strided come by
